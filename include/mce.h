@@ -1,0 +1,178 @@
+/*
+ * mce.h -- C ABI of the GB300 maximal clique enumeration library (libmce_gb300.so).
+ *
+ * The problem is the one stated in "Parallelizing Maximal Clique Enumeration on GPUs"
+ * (arXiv 2212.01473v2), Section 2.1: given a simple undirected graph G = (V, E), find every
+ * maximal clique -- every complete subgraph that no further vertex can extend -- exactly, with
+ * no sampling or approximation.
+ *
+ * The search is the Bron-Kerbosch algorithm with pivoting (Section 2.3, Algorithm 2; pivot
+ * chosen over P u X, Tomita's rule), split into independent first-level subtrees
+ * (Section 2.4, Algorithm 3) taken in degeneracy order (Section 2.4, "Degeneracy Ordering"),
+ * each solved on a binary-encoded induced subgraph over P u X (Sections 2.4 and 3.4, "full"
+ * induced subgraph) with the compact X representation of Section 3.5 and the worker list of
+ * Section 3.3.  Everything runs on one GPU.
+ *
+ * Conventions shared by every entry point
+ *   - Streams are passed as `void *` holding a cudaStream_t (NULL = the legacy default
+ *     stream).  Calls that take a stream only enqueue work on it, in stream order, and return
+ *     without waiting, unless their comment says they synchronise.
+ *   - "device pointer" means memory the current CUDA device can address (cudaMalloc, a
+ *     PyTorch CUDA tensor, managed memory).  "host pointer" means ordinary host memory.
+ *   - A handle is bound to the CUDA device that was current when mce_create ran; every later
+ *     call must be made with that device current.  Handles are not thread-safe.
+ *   - Return codes report argument errors and CUDA launch/allocation failures at call time.
+ *     Errors that the GPU detects while running (a wait limit exceeded, an output buffer
+ *     overflow) are recorded in a status word on the device and returned by mce_last_error.
+ *   - Vertex ids are int32 in [0, n).  Results always name vertices by these original ids.
+ */
+#ifndef MCE_H
+#define MCE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct mce_graph mce_graph;   /* opaque; owned by the library */
+
+typedef enum mce_status {
+    MCE_OK = 0,
+    MCE_ERR_INVALID_ARG = 1,       /* a NULL pointer, a negative size, offsets not monotone   */
+    MCE_ERR_NOT_SIMPLE = 2,        /* a self-loop or a repeated neighbour                      */
+    MCE_ERR_NOT_SYMMETRIC = 3,     /* u in N(v) but v not in N(u)                              */
+    MCE_ERR_ID_RANGE = 4,          /* a neighbour id or a root id outside [0, n)               */
+    MCE_ERR_OUT_OF_MEMORY = 5,     /* a device or host allocation failed                       */
+    MCE_ERR_BUFFER_TOO_SMALL = 6,  /* an output buffer cannot hold the result                  */
+    MCE_ERR_DEVICE_TIMEOUT = 7,    /* a device-side wait exceeded mce_config.spin_limit_ns     */
+    MCE_ERR_LIMIT = 8,             /* the graph exceeds a documented size limit of this build  */
+    MCE_ERR_CUDA = 9               /* any other CUDA runtime error                             */
+} mce_status;
+
+/*
+ * Tuning knobs.  Fill with mce_config_default() and change fields; pass NULL for defaults.
+ *   worker_list      1: warps that run out of first-level subtrees receive branches donated by
+ *                    busy warps (Section 3.3); 0: static first-level distribution only.
+ *   donate_min_p     a branch is donated only if |P| >= this at its root (Section 3.3 uses 10).
+ *   warps_per_block  warps per CTA of the search kernel (0 = library default).
+ *   blocks_per_sm    CTAs per SM of the search kernel (0 = as many as can be resident).
+ *   spin_limit_ns    upper bound on any single device-side wait (grid barrier, idle warp
+ *                    waiting for a donation); on expiry the kernel records
+ *                    MCE_ERR_DEVICE_TIMEOUT and returns instead of hanging.
+ */
+typedef struct mce_config {
+    int32_t worker_list;
+    int32_t donate_min_p;
+    int32_t warps_per_block;
+    int32_t blocks_per_sm;
+    int64_t spin_limit_ns;
+} mce_config;
+
+/* Sizes and diagnostics of a handle (filled by mce_info). */
+typedef struct mce_info {
+    int32_t n;                 /* vertices                                                   */
+    int32_t degeneracy;        /* d: largest core number (Section 2.4)                        */
+    int64_t m;                 /* undirected edges                                            */
+    int32_t max_degree;        /* Delta                                                       */
+    int32_t hist_len;          /* d + 2: length of the size histogram in mce_count's output   */
+    int32_t peel_rounds;       /* rounds of the parallel peel                                 */
+    int32_t n_workers;         /* warps of the search kernel (each one a DFS worker)          */
+    int64_t workspace_bytes;   /* device workspace held by the handle                         */
+    uint64_t tree_nodes;       /* search-tree nodes visited by the last count/enumerate       */
+    uint64_t donations;        /* branches donated through the worker list, last call         */
+} mce_info;
+
+/* Writes the default configuration into *cfg.  Returns MCE_ERR_INVALID_ARG if cfg is NULL. */
+mce_status mce_config_default(mce_config *cfg);
+
+/*
+ * Copies a graph into the library and prepares it (input side of Section 2.1's problem).
+ *   offsets  int32[n+1], offsets[0] = 0, non-decreasing; adj int32[offsets[n]]: the neighbours
+ *            of v are adj[offsets[v] .. offsets[v+1]), in any order.  Both are host pointers
+ *            if is_device_ptr == 0, else device pointers.  The graph must be simple and
+ *            undirected: every edge listed in both directions, no self-loops, no repeats.
+ *            The library copies both arrays; the caller may free them on return.
+ *   n        number of vertices, 0 <= n.  offsets[n] must be < 2^31.
+ *   cfg      NULL for defaults.
+ *   stream   the copy, the input checks and the first degeneracy ordering run on it.
+ *   out      receives the handle; *out is NULL on failure.
+ * Synchronises `stream` (the input checks and the workspace size are read back to the host).
+ * Errors: MCE_ERR_INVALID_ARG, MCE_ERR_ID_RANGE, MCE_ERR_NOT_SIMPLE, MCE_ERR_NOT_SYMMETRIC,
+ * MCE_ERR_OUT_OF_MEMORY, MCE_ERR_LIMIT (a first-level P larger than 1024 vertices, or a degree
+ * of 2^21 or more), MCE_ERR_CUDA.
+ */
+mce_status mce_create(const int32_t *offsets, const int32_t *adj, int32_t n, int is_device_ptr,
+                      const mce_config *cfg, void *stream, mce_graph **out);
+
+/*
+ * Recomputes the degeneracy order (Section 2.4, "Degeneracy Ordering"): a parallel k-core peel
+ * on the GPU, then the split of every adjacency into earlier (X) and later (P) neighbours and
+ * the heavy-first schedule of first-level subtrees.  mce_count, mce_count_roots and
+ * mce_enumerate use the order computed last; mce_create computes it once.  This entry point
+ * exists so that a timing loop can include the preprocessing, as Section 4.1 ("Reporting of
+ * Measurements") does.  Asynchronous on `stream`.
+ */
+mce_status mce_order(mce_graph *g, void *stream);
+
+/*
+ * Counts all maximal cliques (Section 2.1) with one launch of the persistent search kernel.
+ *   d_out  device pointer to uint64[2 + hist_len] (hist_len from mce_info):
+ *          d_out[0] = number of maximal cliques,
+ *          d_out[1] = hash = sum over cliques C of mix64(sum_{c in C} key(c)) mod 2^64 with
+ *                     key(c) = mix64((c + 1) * 0x9E3779B97F4A7C15) and mix64 the SplitMix64
+ *                     output function -- independent of clique order and of vertex order,
+ *          d_out[2 + k] = number of maximal cliques with k vertices.
+ *          The pages define no summary; this one is the library's own.
+ * Asynchronous on `stream`; the caller owns d_out.
+ */
+mce_status mce_count(mce_graph *g, void *stream, uint64_t *d_out);
+
+/*
+ * Same as mce_count, restricted to the first-level subtrees (Algorithm 3) of the given roots:
+ * the maximal cliques whose earliest vertex in the current degeneracy order is one of them.
+ * Summing the outputs over a partition of V gives mce_count's output, which makes runs
+ * resumable and lets large graphs be processed in pieces.
+ *   d_roots  device pointer to int32[n_roots], original vertex ids (duplicates count twice).
+ * Root ids are checked on the device: an id outside [0, n) records MCE_ERR_ID_RANGE.
+ */
+mce_status mce_count_roots(mce_graph *g, void *stream, const int32_t *d_roots, int32_t n_roots,
+                           uint64_t *d_out);
+
+/*
+ * Writes every maximal clique as its vertex ids sorted ascending:
+ *   clique i = d_ids[d_offsets[i] .. d_offsets[i+1]), i < count.  Cliques are grouped by size
+ *   (ascending); the order inside a size group is unspecified.
+ *   d_ids      device int32[cap_ids]; d_offsets device int64[cap_cliques + 1].
+ *   h_sizes    host int64[2]: receives {number of cliques, number of ids}.
+ * Runs a counting pass first when the handle has no count of the full graph for its current
+ * order (the sizes come from it, as in count-scan-write compaction), then the writing pass.
+ * Synchronises `stream` once to read the sizes.  If a capacity is too small, nothing is written
+ * and MCE_ERR_BUFFER_TOO_SMALL is returned with the required sizes in h_sizes.
+ */
+mce_status mce_enumerate(mce_graph *g, void *stream, int32_t *d_ids, int64_t cap_ids,
+                         int64_t *d_offsets, int64_t cap_cliques, int64_t *h_sizes);
+
+/*
+ * Copies the current degeneracy order to device buffers (diagnostics and tests):
+ *   d_rank[v] = position of v in the order, d_core[v] = core number of v; either may be NULL.
+ */
+mce_status mce_get_order(mce_graph *g, void *stream, int32_t *d_rank, int32_t *d_core);
+
+/* Synchronises `stream`, then returns (and clears) the device-side status of the handle. */
+mce_status mce_last_error(mce_graph *g, void *stream);
+
+/* Fills *info; the diagnostics refer to the last completed call (synchronises the device). */
+mce_status mce_get_info(mce_graph *g, mce_info *info);
+
+/* Frees the handle and its device memory (synchronises the device first).  NULL is a no-op. */
+void mce_destroy(mce_graph *g);
+
+/* Static English description of a status code. */
+const char *mce_status_str(mce_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MCE_H */

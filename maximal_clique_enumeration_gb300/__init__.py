@@ -1,0 +1,266 @@
+"""GB300 maximal clique enumeration: Python binding of libmce_gb300.so (ctypes).
+
+The binding only marshals arguments: every step of the computation runs in the CUDA library
+declared in ``include/mce.h``.  PyTorch supplies device memory and streams.  There is no CPU
+fallback: if the library is missing, every call raises.
+
+    import maximal_clique_enumeration_gb300 as mce
+    g = mce.Graph(offsets, adj)          # CSR as torch tensors (CUDA or CPU) or numpy arrays
+    count, hash_, hist = g.count_result()
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from .build import LIB_PATH
+
+__all__ = ["Graph", "MceError", "Config", "Info", "library", "STATUS", "graphs"]
+
+STATUS = {
+    0: "MCE_OK", 1: "MCE_ERR_INVALID_ARG", 2: "MCE_ERR_NOT_SIMPLE", 3: "MCE_ERR_NOT_SYMMETRIC",
+    4: "MCE_ERR_ID_RANGE", 5: "MCE_ERR_OUT_OF_MEMORY", 6: "MCE_ERR_BUFFER_TOO_SMALL",
+    7: "MCE_ERR_DEVICE_TIMEOUT", 8: "MCE_ERR_LIMIT", 9: "MCE_ERR_CUDA",
+}
+EXPORTS = ["mce_config_default", "mce_create", "mce_order", "mce_count", "mce_count_roots",
+           "mce_enumerate", "mce_get_order", "mce_last_error", "mce_get_info", "mce_destroy",
+           "mce_status_str"]
+
+
+class MceError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = int(code)
+        self.name = STATUS.get(self.code, str(code))
+        super().__init__(f"{what}: {self.name}" if what else self.name)
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("worker_list", ctypes.c_int32), ("donate_min_p", ctypes.c_int32),
+                ("warps_per_block", ctypes.c_int32), ("blocks_per_sm", ctypes.c_int32),
+                ("spin_limit_ns", ctypes.c_int64)]
+
+
+class Info(ctypes.Structure):
+    _fields_ = [("n", ctypes.c_int32), ("degeneracy", ctypes.c_int32), ("m", ctypes.c_int64),
+                ("max_degree", ctypes.c_int32), ("hist_len", ctypes.c_int32),
+                ("peel_rounds", ctypes.c_int32), ("n_workers", ctypes.c_int32),
+                ("workspace_bytes", ctypes.c_int64), ("tree_nodes", ctypes.c_uint64),
+                ("donations", ctypes.c_uint64)]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_}
+
+
+_lib = None
+
+
+def library(path: str = LIB_PATH):
+    """Loads libmce_gb300.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with __graft_entry__.build() "
+                           "(nvcc, sm_103a); there is no CPU fallback")
+    lib = ctypes.CDLL(path)
+    P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    st = ctypes.c_int
+    lib.mce_config_default.restype = st
+    lib.mce_config_default.argtypes = [ctypes.POINTER(Config)]
+    lib.mce_create.restype = st
+    lib.mce_create.argtypes = [P, P, i32, ctypes.c_int, ctypes.POINTER(Config), P,
+                               ctypes.POINTER(P)]
+    lib.mce_order.restype = st
+    lib.mce_order.argtypes = [P, P]
+    lib.mce_count.restype = st
+    lib.mce_count.argtypes = [P, P, P]
+    lib.mce_count_roots.restype = st
+    lib.mce_count_roots.argtypes = [P, P, P, i32, P]
+    lib.mce_enumerate.restype = st
+    lib.mce_enumerate.argtypes = [P, P, P, i64, P, i64, P]
+    lib.mce_get_order.restype = st
+    lib.mce_get_order.argtypes = [P, P, P, P]
+    lib.mce_last_error.restype = st
+    lib.mce_last_error.argtypes = [P, P]
+    lib.mce_get_info.restype = st
+    lib.mce_get_info.argtypes = [P, ctypes.POINTER(Info)]
+    lib.mce_destroy.restype = None
+    lib.mce_destroy.argtypes = [P]
+    lib.mce_status_str.restype = ctypes.c_char_p
+    lib.mce_status_str.argtypes = [st]
+    _lib = lib
+    return lib
+
+
+def _check(code: int, what: str):
+    if code != 0:
+        raise MceError(code, what)
+
+
+def _stream_ptr(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def default_config(**overrides) -> Config:
+    cfg = Config()
+    _check(library().mce_config_default(ctypes.byref(cfg)), "mce_config_default")
+    for k, v in overrides.items():
+        setattr(cfg, k, v)
+    return cfg
+
+
+def _u64_view(t):
+    """uint64 numpy view of an int64 tensor's host copy."""
+    return t.detach().cpu().numpy().view(np.uint64)
+
+
+class Graph:
+    """One graph held by the library (mce_create ... mce_destroy)."""
+
+    def __init__(self, offsets, adj, n: int | None = None, config: Config | None = None,
+                 stream=None, **config_overrides):
+        import torch
+        lib = library()
+        if isinstance(offsets, np.ndarray):
+            offsets = torch.from_numpy(np.ascontiguousarray(offsets, dtype=np.int32))
+        if isinstance(adj, np.ndarray):
+            adj = torch.from_numpy(np.ascontiguousarray(adj, dtype=np.int32))
+        if offsets.dtype != torch.int32 or adj.dtype != torch.int32:
+            raise TypeError("offsets and adj must be int32")
+        offsets, adj = offsets.contiguous(), adj.contiguous()
+        if offsets.is_cuda != adj.is_cuda:
+            raise ValueError("offsets and adj must both be on the host or both on the device")
+        if n is None:
+            n = offsets.numel() - 1
+        if config is None:
+            config = default_config(**config_overrides)
+        self._keep = (offsets, adj)
+        self._h = ctypes.c_void_p(0)
+        adj_ptr = adj.data_ptr() if adj.numel() else 0
+        code = lib.mce_create(ctypes.c_void_p(offsets.data_ptr()), ctypes.c_void_p(adj_ptr),
+                              int(n), 1 if offsets.is_cuda else 0, ctypes.byref(config),
+                              _stream_ptr(stream), ctypes.byref(self._h))
+        self._keep = None
+        _check(code, "mce_create")
+        self.info = self.get_info()
+        self.n = self.info["n"]
+        self.hist_len = self.info["hist_len"]
+
+    # -- lifecycle
+    def close(self):
+        if getattr(self, "_h", None) and self._h.value:
+            library().mce_destroy(self._h)
+            self._h = ctypes.c_void_p(0)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    # -- calls
+    def get_info(self) -> dict:
+        info = Info()
+        _check(library().mce_get_info(self._h, ctypes.byref(info)), "mce_get_info")
+        return info.as_dict()
+
+    def order(self, stream=None):
+        _check(library().mce_order(self._h, _stream_ptr(stream)), "mce_order")
+
+    def new_output(self):
+        import torch
+        return torch.zeros(2 + self.hist_len, dtype=torch.int64, device="cuda")
+
+    def count(self, out=None, stream=None):
+        """Enqueues mce_count; returns the int64 device tensor holding the uint64 output."""
+        out = self.new_output() if out is None else out
+        _check(library().mce_count(self._h, _stream_ptr(stream), ctypes.c_void_p(out.data_ptr())),
+               "mce_count")
+        return out
+
+    def count_roots(self, roots, out=None, stream=None):
+        import torch
+        out = self.new_output() if out is None else out
+        if not isinstance(roots, torch.Tensor):
+            roots = torch.as_tensor(np.asarray(roots, dtype=np.int32))
+        roots = roots.to(device="cuda", dtype=torch.int32).contiguous()
+        self._roots_keep = roots
+        _check(library().mce_count_roots(self._h, _stream_ptr(stream),
+                                         ctypes.c_void_p(roots.data_ptr()), int(roots.numel()),
+                                         ctypes.c_void_p(out.data_ptr())), "mce_count_roots")
+        return out
+
+    def last_error(self, stream=None) -> int:
+        return int(library().mce_last_error(self._h, _stream_ptr(stream)))
+
+    def check(self, stream=None):
+        code = self.last_error(stream)
+        if code:
+            raise MceError(code, "device-side status")
+
+    @staticmethod
+    def unpack(out):
+        """(count, hash, hist tuple trimmed of trailing zeros) from an output tensor."""
+        u = _u64_view(out)
+        hist = np.trim_zeros(u[2:], "b")
+        return int(u[0]), int(u[1]), tuple(int(x) for x in hist)
+
+    def count_result(self, stream=None):
+        out = self.count(stream=stream)
+        self.check(stream)
+        return self.unpack(out)
+
+    def count_roots_result(self, roots, stream=None):
+        out = self.count_roots(roots, stream=stream)
+        self.check(stream)
+        return self.unpack(out)
+
+    def enumerate(self, stream=None):
+        """All maximal cliques: (ids int32 tensor, offsets int64 tensor) on the device."""
+        import torch
+        lib = library()
+        sizes = np.zeros(2, np.int64)
+        dummy = torch.zeros(1, dtype=torch.int64, device="cuda")
+        code = lib.mce_enumerate(self._h, _stream_ptr(stream), ctypes.c_void_p(0), 0,
+                                 ctypes.c_void_p(dummy.data_ptr()), 0,
+                                 sizes.ctypes.data_as(ctypes.c_void_p))
+        if code not in (0, 6):
+            raise MceError(code, "mce_enumerate (sizing)")
+        ids = torch.empty(max(int(sizes[1]), 1), dtype=torch.int32, device="cuda")
+        offs = torch.empty(int(sizes[0]) + 1, dtype=torch.int64, device="cuda")
+        _check(lib.mce_enumerate(self._h, _stream_ptr(stream), ctypes.c_void_p(ids.data_ptr()),
+                                 ids.numel(), ctypes.c_void_p(offs.data_ptr()), int(sizes[0]),
+                                 sizes.ctypes.data_as(ctypes.c_void_p)), "mce_enumerate")
+        self.check(stream)
+        return ids[: int(sizes[1])], offs
+
+    def order_arrays(self, stream=None):
+        """(rank, core) int32 device tensors of the current degeneracy order."""
+        import torch
+        rank = torch.empty(max(self.n, 1), dtype=torch.int32, device="cuda")
+        core = torch.empty(max(self.n, 1), dtype=torch.int32, device="cuda")
+        _check(library().mce_get_order(self._h, _stream_ptr(stream),
+                                       ctypes.c_void_p(rank.data_ptr()),
+                                       ctypes.c_void_p(core.data_ptr())), "mce_get_order")
+        return rank[: self.n], core[: self.n]
+
+
+def cliques_from(ids, offsets):
+    """List of tuples from an enumeration's (ids, offsets)."""
+    ids = ids.cpu().numpy()
+    offs = offsets.cpu().numpy()
+    return [tuple(int(x) for x in ids[offs[i]: offs[i + 1]]) for i in range(len(offs) - 1)]
+
+
+from . import graphs  # noqa: E402  (input generators; no CUDA needed)

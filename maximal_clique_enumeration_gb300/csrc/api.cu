@@ -1,0 +1,436 @@
+// Host side of the C ABI declared in include/mce.h.
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "mce_internal.cuh"
+
+using namespace mce;
+
+struct mce_graph {
+    int device = 0;
+    int n = 0;
+    long long nnz = 0;
+    mce_config cfg{};
+    int sm_count = 0;
+    int peel_blocks = 0;
+    int search_blocks = 0, search_threads = 0, n_workers = 0;
+    size_t search_smem = 0;
+    int degeneracy = 0, max_degree = 0, hist_len = 2, rounds = 0;
+    unsigned long long ws_words = 0;
+    std::vector<void *> allocs;
+    DevGraph g{};
+    unsigned long long *hist_acc = nullptr;     // [hist_len]
+    unsigned int *ws = nullptr;
+    int *ring = nullptr, *flag = nullptr;
+    long long *region_ids = nullptr, *region_cl = nullptr, *totals = nullptr;
+    unsigned long long *cursor = nullptr;
+    unsigned long long *count_cache = nullptr;  // [2 + hist_len], full-graph count
+    bool count_cache_valid = false;
+};
+
+namespace {
+
+mce_status from_cuda(cudaError_t e)
+{
+    if (e == cudaSuccess) return MCE_OK;
+    if (e == cudaErrorMemoryAllocation) return MCE_ERR_OUT_OF_MEMORY;
+    return MCE_ERR_CUDA;
+}
+
+#define MCE_TRY(expr)                                        \
+    do {                                                     \
+        mce_status _st = from_cuda(expr);                    \
+        if (_st != MCE_OK) return _st;                       \
+    } while (0)
+
+template <typename T>
+mce_status dev_alloc(mce_graph *h, T **p, size_t count)
+{
+    void *q = nullptr;
+    const size_t bytes = count * sizeof(T) > 0 ? count * sizeof(T) : 16;
+    cudaError_t e = cudaMalloc(&q, bytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        *p = nullptr;
+        return MCE_ERR_OUT_OF_MEMORY;
+    }
+    h->allocs.push_back(q);
+    *p = static_cast<T *>(q);
+    return MCE_OK;
+}
+
+#define MCE_ALLOC(h, p, count)                               \
+    do {                                                     \
+        mce_status _st = dev_alloc((h), &(p), (count));      \
+        if (_st != MCE_OK) return _st;                       \
+    } while (0)
+
+mce_status read_status(mce_graph *h, cudaStream_t s)
+{
+    int st = 0;
+    MCE_TRY(cudaMemcpyAsync(&st, &h->g.ctrl->status, sizeof(int), cudaMemcpyDeviceToHost, s));
+    MCE_TRY(cudaStreamSynchronize(s));
+    return (mce_status)st;
+}
+
+void free_all(mce_graph *h)
+{
+    for (void *p : h->allocs) cudaFree(p);
+    h->allocs.clear();
+}
+
+// Resets the per-search fields of the control block.
+mce_status reset_search(mce_graph *h, cudaStream_t s)
+{
+    DevCtrl *c = h->g.ctrl;
+    MCE_TRY(cudaMemsetAsync(&c->next_root, 0, sizeof(unsigned long long), s));
+    MCE_TRY(cudaMemsetAsync(&c->busy, 0, 3 * sizeof(int), s));
+    MCE_TRY(cudaMemsetAsync(&c->tree_nodes, 0, 4 * sizeof(unsigned long long), s));
+    MCE_TRY(cudaMemsetAsync(h->hist_acc, 0, sizeof(unsigned long long) * h->hist_len, s));
+    MCE_TRY(cudaMemsetAsync(h->flag, 0, sizeof(int) * (h->n_workers > 0 ? h->n_workers : 1), s));
+    return MCE_OK;
+}
+
+SearchArgs search_args(mce_graph *h, const int *roots, long long n_roots)
+{
+    SearchArgs a{};
+    a.g = h->g;
+    a.out.hist = h->hist_acc;
+    a.out.hist_len = h->hist_len;
+    a.roots = roots;
+    a.n_roots = n_roots;
+    a.ws = h->ws;
+    a.ws_words = h->ws_words;
+    a.ring = h->ring;
+    a.flag = h->flag;
+    a.n_workers = h->n_workers;
+    a.worker_list = h->cfg.worker_list;
+    a.donate_min_p = h->cfg.donate_min_p;
+    a.spin_limit_ns = h->cfg.spin_limit_ns;
+    return a;
+}
+
+mce_status run_search(mce_graph *h, cudaStream_t s, const int *roots, long long n_roots,
+                      const DevOut *enum_out)
+{
+    mce_status st = reset_search(h, s);
+    if (st != MCE_OK) return st;
+    SearchArgs a = search_args(h, roots, n_roots);
+    if (enum_out) {
+        a.out = *enum_out;
+        a.out.hist = h->hist_acc;
+        a.out.hist_len = h->hist_len;
+    }
+    MCE_TRY(launch_search(a, h->search_blocks, h->search_threads, h->search_smem, s));
+    return MCE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mce_status mce_config_default(mce_config *cfg)
+{
+    if (!cfg) return MCE_ERR_INVALID_ARG;
+    cfg->worker_list = 1;
+    cfg->donate_min_p = 10;
+    cfg->warps_per_block = kDefaultWarpsPerBlock;
+    cfg->blocks_per_sm = 0;
+    cfg->spin_limit_ns = 20LL * 1000 * 1000 * 1000;
+    return MCE_OK;
+}
+
+const char *mce_status_str(mce_status s)
+{
+    switch (s) {
+    case MCE_OK: return "ok";
+    case MCE_ERR_INVALID_ARG: return "invalid argument";
+    case MCE_ERR_NOT_SIMPLE: return "graph is not simple (self-loop or repeated neighbour)";
+    case MCE_ERR_NOT_SYMMETRIC: return "graph is not symmetric";
+    case MCE_ERR_ID_RANGE: return "vertex id out of range";
+    case MCE_ERR_OUT_OF_MEMORY: return "out of memory";
+    case MCE_ERR_BUFFER_TOO_SMALL: return "output buffer too small";
+    case MCE_ERR_DEVICE_TIMEOUT: return "device-side wait exceeded the spin limit";
+    case MCE_ERR_LIMIT: return "graph exceeds a size limit of this build";
+    case MCE_ERR_CUDA: return "CUDA error";
+    }
+    return "unknown status";
+}
+
+static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_t *adj, int32_t n,
+                              int is_device_ptr, cudaStream_t s)
+{
+    MCE_TRY(cudaGetDevice(&h->device));
+    MCE_TRY(cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, h->device));
+    h->n = n;
+    // offsets[0] and offsets[n] (= number of adjacency entries)
+    int first = 0, last = 0;
+    const cudaMemcpyKind k = is_device_ptr ? cudaMemcpyDeviceToHost : cudaMemcpyHostToHost;
+    MCE_TRY(cudaMemcpy(&first, offsets, sizeof(int), k));
+    MCE_TRY(cudaMemcpy(&last, offsets + n, sizeof(int), k));
+    if (first != 0 || last < 0 || (last > 0 && !adj)) return MCE_ERR_INVALID_ARG;
+    h->nnz = last;
+
+    DevGraph &g = h->g;
+    int *offs = nullptr, *adjm = nullptr;
+    MCE_ALLOC(h, offs, (size_t)n + 1);
+    MCE_ALLOC(h, adjm, (size_t)h->nnz);
+    MCE_ALLOC(h, g.ctrl, 1);
+    MCE_TRY(cudaMemsetAsync(g.ctrl, 0, sizeof(DevCtrl), s));
+    const cudaMemcpyKind kin = is_device_ptr ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice;
+    MCE_TRY(cudaMemcpyAsync(offs, offsets, sizeof(int) * ((size_t)n + 1), kin, s));
+    if (h->nnz) MCE_TRY(cudaMemcpyAsync(adjm, adj, sizeof(int) * (size_t)h->nnz, kin, s));
+    g.n = n;
+    g.nnz = h->nnz;
+    g.offs = offs;
+    g.adj = adjm;
+
+    // input checks: offsets, id range, sortedness
+    int *d_list = nullptr, *d_nlist = nullptr;
+    MCE_ALLOC(h, d_list, (size_t)n + 1);
+    MCE_ALLOC(h, d_nlist, 1);
+    MCE_TRY(cudaMemsetAsync(d_nlist, 0, sizeof(int), s));
+    MCE_TRY(launch_ingest_check(g, d_list, d_nlist, s));
+    mce_status st = read_status(h, s);
+    if (st != MCE_OK) return st;
+    int n_unsorted = 0;
+    MCE_TRY(cudaMemcpy(&n_unsorted, d_nlist, sizeof(int), cudaMemcpyDeviceToHost));
+    if (n_unsorted > 0) {
+        MCE_TRY(launch_ingest_sort(g, adjm, d_list, n_unsorted, nullptr, 0, s));
+        std::vector<int> list(n_unsorted), hoffs((size_t)n + 1);
+        MCE_TRY(cudaMemcpy(list.data(), d_list, sizeof(int) * n_unsorted, cudaMemcpyDeviceToHost));
+        MCE_TRY(cudaMemcpy(hoffs.data(), offs, sizeof(int) * ((size_t)n + 1),
+                           cudaMemcpyDeviceToHost));
+        int *scratch = nullptr;
+        long long scratch_len = 0;
+        for (int v : list) {
+            const long long len = hoffs[v + 1] - hoffs[v];
+            if (len <= 4096) continue;
+            long long p2 = 1;
+            while (p2 < len) p2 <<= 1;
+            if (p2 > scratch_len) {
+                MCE_ALLOC(h, scratch, (size_t)p2);
+                scratch_len = p2;
+            }
+            MCE_TRY(launch_ingest_sort_large(g, adjm, v, scratch, s));
+        }
+    }
+    MCE_TRY(launch_ingest_validate(g, s));
+    st = read_status(h, s);
+    if (st != MCE_OK) return st;
+
+    // degeneracy order buffers
+    MCE_ALLOC(h, g.rank, (size_t)n);
+    MCE_ALLOC(h, g.core, (size_t)n);
+    MCE_ALLOC(h, g.round_of, (size_t)n);
+    MCE_ALLOC(h, g.order, (size_t)n);
+    MCE_ALLOC(h, g.pcount, (size_t)n);
+    MCE_ALLOC(h, g.sched, (size_t)n);
+    MCE_ALLOC(h, g.deg, (size_t)n);
+    MCE_ALLOC(h, g.alive_a, (size_t)n);
+    MCE_ALLOC(h, g.alive_b, (size_t)n);
+    MCE_ALLOC(h, g.bucket, (size_t)kMaxP + 2);
+    int coop = 0;
+    MCE_TRY(cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, h->device));
+    if (!coop) return MCE_ERR_CUDA;
+    h->peel_blocks = h->sm_count;
+    MCE_ALLOC(h, g.blk_cnt, (size_t)2 * h->peel_blocks);
+    MCE_ALLOC(h, g.blk_min, (size_t)2 * h->peel_blocks);
+    MCE_TRY(launch_order(g, h->peel_blocks, h->cfg.spin_limit_ns, s));
+    st = read_status(h, s);
+    if (st != MCE_OK) return st;
+    DevCtrl c{};
+    MCE_TRY(cudaMemcpy(&c, g.ctrl, sizeof(DevCtrl), cudaMemcpyDeviceToHost));
+    h->degeneracy = c.degeneracy;
+    h->rounds = c.rounds;
+    h->max_degree = c.max_degree;
+    h->hist_len = c.degeneracy + 2;
+    if (c.max_pcount > kMaxP || c.max_degree > kMaxCode) return MCE_ERR_LIMIT;
+    h->ws_words = (c.ws_words + 3) & ~3ULL;
+    if (h->ws_words == 0) h->ws_words = 4;
+
+    // search kernel geometry: as many CTAs as can be resident (Section 3.3)
+    int wpb = h->cfg.warps_per_block > 0 ? h->cfg.warps_per_block : kDefaultWarpsPerBlock;
+    if (wpb > 4) wpb = 4;
+    h->search_threads = 32 * wpb;
+    h->search_smem = sizeof(unsigned long long) * (size_t)(h->hist_len + 1);
+    int per_sm = 0;
+    MCE_TRY(search_occupancy(h->search_threads, h->search_smem, &per_sm));
+    if (per_sm < 1) return MCE_ERR_CUDA;
+    if (h->cfg.blocks_per_sm > 0 && h->cfg.blocks_per_sm < per_sm) per_sm = h->cfg.blocks_per_sm;
+    h->search_blocks = per_sm * h->sm_count;
+    h->n_workers = h->search_blocks * wpb;
+    MCE_ALLOC(h, h->ws, (size_t)h->n_workers * h->ws_words);
+    MCE_ALLOC(h, h->ring, (size_t)h->n_workers);
+    MCE_ALLOC(h, h->flag, (size_t)h->n_workers);
+    MCE_ALLOC(h, h->hist_acc, (size_t)h->hist_len + 1);
+    MCE_ALLOC(h, h->region_ids, (size_t)h->hist_len + 2);
+    MCE_ALLOC(h, h->region_cl, (size_t)h->hist_len + 2);
+    MCE_ALLOC(h, h->cursor, (size_t)h->hist_len + 1);
+    MCE_ALLOC(h, h->totals, 2);
+    MCE_ALLOC(h, h->count_cache, (size_t)h->hist_len + 2);
+    return MCE_OK;
+}
+
+mce_status mce_create(const int32_t *offsets, const int32_t *adj, int32_t n, int is_device_ptr,
+                      const mce_config *cfg, void *stream, mce_graph **out)
+{
+    if (!out) return MCE_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (n < 0 || !offsets) return MCE_ERR_INVALID_ARG;
+    mce_graph *h = new (std::nothrow) mce_graph();
+    if (!h) return MCE_ERR_OUT_OF_MEMORY;
+    if (cfg) h->cfg = *cfg;
+    else mce_config_default(&h->cfg);
+    if (h->cfg.donate_min_p < 1) h->cfg.donate_min_p = 1;
+    if (h->cfg.spin_limit_ns <= 0) h->cfg.spin_limit_ns = 20LL * 1000 * 1000 * 1000;
+    mce_status st = create_impl(h, offsets, adj, n, is_device_ptr, (cudaStream_t)stream);
+    if (st != MCE_OK) {
+        cudaStreamSynchronize((cudaStream_t)stream);
+        cudaGetLastError();
+        free_all(h);
+        delete h;
+        return st;
+    }
+    *out = h;
+    return MCE_OK;
+}
+
+mce_status mce_order(mce_graph *h, void *stream)
+{
+    if (!h) return MCE_ERR_INVALID_ARG;
+    h->count_cache_valid = false;
+    MCE_TRY(launch_order(h->g, h->peel_blocks, h->cfg.spin_limit_ns, (cudaStream_t)stream));
+    return MCE_OK;
+}
+
+static mce_status count_impl(mce_graph *h, cudaStream_t s, const int32_t *d_roots,
+                             long long n_roots, uint64_t *d_out)
+{
+    if (h->n == 0) {
+        MCE_TRY(cudaMemsetAsync(d_out, 0, sizeof(uint64_t) * (2 + (size_t)h->hist_len), s));
+        return MCE_OK;
+    }
+    mce_status st = run_search(h, s, d_roots, n_roots, nullptr);
+    if (st != MCE_OK) return st;
+    DevOut o{};
+    o.hist = h->hist_acc;
+    o.hist_len = h->hist_len;
+    MCE_TRY(launch_finalize(h->g, o, (unsigned long long *)d_out, d_roots ? 0 : 1, s));
+    return MCE_OK;
+}
+
+mce_status mce_count(mce_graph *h, void *stream, uint64_t *d_out)
+{
+    if (!h || !d_out) return MCE_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    mce_status st = count_impl(h, s, nullptr, 0, d_out);
+    if (st != MCE_OK) return st;
+    MCE_TRY(cudaMemcpyAsync(h->count_cache, d_out, sizeof(uint64_t) * (2 + (size_t)h->hist_len),
+                            cudaMemcpyDeviceToDevice, s));
+    h->count_cache_valid = true;
+    return MCE_OK;
+}
+
+mce_status mce_count_roots(mce_graph *h, void *stream, const int32_t *d_roots, int32_t n_roots,
+                           uint64_t *d_out)
+{
+    if (!h || !d_out || n_roots < 0 || (n_roots > 0 && !d_roots)) return MCE_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (n_roots == 0) {
+        MCE_TRY(cudaMemsetAsync(d_out, 0, sizeof(uint64_t) * (2 + (size_t)h->hist_len), s));
+        return MCE_OK;
+    }
+    return count_impl(h, s, d_roots, n_roots, d_out);
+}
+
+mce_status mce_enumerate(mce_graph *h, void *stream, int32_t *d_ids, int64_t cap_ids,
+                         int64_t *d_offsets, int64_t cap_cliques, int64_t *h_sizes)
+{
+    if (!h || !h_sizes || cap_ids < 0 || cap_cliques < 0) return MCE_ERR_INVALID_ARG;
+    if ((cap_ids > 0 && !d_ids) || !d_offsets) return MCE_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (!h->count_cache_valid) {
+        mce_status st = mce_count(h, stream, (uint64_t *)h->count_cache);
+        if (st != MCE_OK) return st;
+    }
+    MCE_TRY(launch_enum_layout(h->g, h->count_cache, h->hist_len, h->region_ids, h->region_cl,
+                               h->cursor, h->totals, s));
+    long long tot[2] = {0, 0};
+    MCE_TRY(cudaMemcpyAsync(tot, h->totals, sizeof(tot), cudaMemcpyDeviceToHost, s));
+    MCE_TRY(cudaStreamSynchronize(s));
+    h_sizes[0] = tot[0];
+    h_sizes[1] = tot[1];
+    if (tot[0] > cap_cliques || tot[1] > cap_ids) return MCE_ERR_BUFFER_TOO_SMALL;
+    DevOut o{};
+    o.hist = h->hist_acc;
+    o.hist_len = h->hist_len;
+    o.ids = d_ids;
+    o.offsets = (long long *)d_offsets;
+    o.region_ids = h->region_ids;
+    o.region_cl = h->region_cl;
+    o.cursor = h->cursor;
+    if (h->n > 0) {
+        mce_status st = run_search(h, s, nullptr, 0, &o);
+        if (st != MCE_OK) return st;
+        MCE_TRY(launch_enum_isolated(h->g, o, s));
+    }
+    MCE_TRY(launch_enum_close(o, h->totals, s));
+    return MCE_OK;
+}
+
+mce_status mce_get_order(mce_graph *h, void *stream, int32_t *d_rank, int32_t *d_core)
+{
+    if (!h) return MCE_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (h->n == 0) return MCE_OK;
+    if (d_rank)
+        MCE_TRY(cudaMemcpyAsync(d_rank, h->g.rank, sizeof(int) * (size_t)h->n,
+                                cudaMemcpyDeviceToDevice, s));
+    if (d_core)
+        MCE_TRY(cudaMemcpyAsync(d_core, h->g.core, sizeof(int) * (size_t)h->n,
+                                cudaMemcpyDeviceToDevice, s));
+    return MCE_OK;
+}
+
+mce_status mce_last_error(mce_graph *h, void *stream)
+{
+    if (!h) return MCE_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    mce_status st = read_status(h, s);
+    if (st == MCE_ERR_CUDA) return st;
+    MCE_TRY(cudaMemsetAsync(&h->g.ctrl->status, 0, sizeof(int), s));
+    MCE_TRY(cudaStreamSynchronize(s));
+    return st;
+}
+
+mce_status mce_get_info(mce_graph *h, mce_info *info)
+{
+    if (!h || !info) return MCE_ERR_INVALID_ARG;
+    MCE_TRY(cudaDeviceSynchronize());
+    DevCtrl c{};
+    MCE_TRY(cudaMemcpy(&c, h->g.ctrl, sizeof(DevCtrl), cudaMemcpyDeviceToHost));
+    info->n = h->n;
+    info->degeneracy = h->degeneracy;
+    info->m = h->nnz / 2;
+    info->max_degree = h->max_degree;
+    info->hist_len = h->hist_len;
+    info->peel_rounds = c.rounds;
+    info->n_workers = h->n_workers;
+    info->workspace_bytes = (long long)(h->ws_words * 4ULL * (unsigned long long)h->n_workers);
+    info->tree_nodes = c.tree_nodes;
+    info->donations = c.donations;
+    return MCE_OK;
+}
+
+void mce_destroy(mce_graph *h)
+{
+    if (!h) return;
+    cudaDeviceSynchronize();
+    free_all(h);
+    delete h;
+}
+
+}  // extern "C"

@@ -1,0 +1,177 @@
+// Internal declarations shared by the CUDA sources of libmce_gb300.so (not installed).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mce.h"
+
+namespace mce {
+
+constexpr int kMaxP = 1024;            // largest |P| of a first-level subtree (32 words per row)
+constexpr int kMaxIdxBits = 21;        // pivot codes are packed as count << 21 | ~code
+constexpr int kMaxCode = (1 << kMaxIdxBits) - 1;
+constexpr int kPeelThreads = 512;
+constexpr int kPeelSoloVertices = 8192;  // the peel finishes in one CTA below this many vertices
+constexpr int kDefaultWarpsPerBlock = 4;
+
+// Device-resident control block of a handle.
+struct DevCtrl {
+    int status;                  // first device-side error (mce_status), 0 = none
+    int degeneracy;              // peel output
+    int rounds;                  // peel output
+    int max_pcount;              // max |P| over first-level subtrees
+    unsigned int bar_count;      // grid barrier arrival counter
+    unsigned int bar_gen;        // grid barrier generation
+    unsigned long long ws_words; // largest per-warp workspace need (words)
+    unsigned long long next_root;  // search: root claim counter
+    unsigned long long n_sched;    // search: number of scheduled roots
+    int busy;                    // worker list: warps holding work
+    int ring_head;               // worker list: pops
+    int ring_tail;               // worker list: pushes
+    int n_iso;                   // isolated vertices (cliques of size 1)
+    int max_degree;              // Delta
+    unsigned long long iso_hash; // hash contribution of the isolated vertices
+    unsigned long long tree_nodes;
+    unsigned long long donations;
+    unsigned long long result[2];  // count, hash of the last search
+};
+
+// Everything the kernels need about a handle's graph (device pointers).
+struct DevGraph {
+    int n;
+    long long nnz;
+    const int *offs;
+    const int *adj;
+    int *rank;        // id -> position in the degeneracy order
+    int *core;        // id -> core number
+    int *round_of;    // id -> peel round
+    int *order;       // position -> id
+    int *pcount;      // id -> |P| (later neighbours)
+    int *sched;       // first-level roots with |P| > 0, heavy first
+    int *deg;         // peel scratch
+    int *alive_a, *alive_b;
+    int *blk_cnt, *blk_min;   // peel per-CTA partials [2][grid]
+    int *bucket;      // orient: |P| histogram / cursors [kMaxP + 2]
+    DevCtrl *ctrl;
+};
+
+// Search output descriptors.
+struct DevOut {
+    unsigned long long *hist;       // [hist_len] histogram by clique size (device, accumulated)
+    int hist_len;
+    // enumeration (NULL when counting)
+    int *ids;
+    long long *offsets;
+    const long long *region_ids;     // [hist_len] first id slot of each size group
+    const long long *region_cl;      // [hist_len] first clique slot of each size group
+    unsigned long long *cursor;      // [hist_len] cliques written per size group
+};
+
+struct SearchArgs {
+    DevGraph g;
+    DevOut out;
+    const int *roots;        // NULL: g.sched (n_sched entries); else user roots (original ids)
+    long long n_roots;
+    unsigned int *ws;        // per-warp workspace, ws_words each
+    unsigned long long ws_words;
+    int *ring;               // worker list: ring of idle warp ids [n_workers]
+    int *flag;               // worker list: per-warp wake flag [n_workers]
+    int n_workers;
+    int worker_list;
+    int donate_min_p;
+    long long spin_limit_ns;
+};
+
+// Words per bitset row for a first-level subtree with np vertices in P (one bit per P vertex),
+// rounded up to 1, 2, 4, 8, 16 or 32 so that rows load as 4-, 8- or 16-byte vectors.
+__host__ __device__ inline int wclass(int np)
+{
+    return np <= 32 ? 1 : np <= 64 ? 2 : np <= 128 ? 4 : np <= 256 ? 8 : np <= 512 ? 16 : 32;
+}
+
+// Per-warp workspace layout (32-bit word offsets) for a root of degree `deg` with np later
+// neighbours.  The same layout serves a donated branch of such a root.
+struct WsLayout {
+    long long rowsP, rowsX, pids, pkey, loc, xx, spill, plist, stack, total;
+    int W, LV;
+};
+
+__host__ __device__ inline WsLayout ws_layout(int deg, int np)
+{
+    WsLayout l;
+    const int nx = deg - np;
+    l.W = wclass(np);
+    long long o = 0;
+    l.rowsP = o; o += (long long)np * l.W;       // rows of P vertices, columns over P
+    l.rowsX = o; o += (long long)nx * l.W;       // rows of X vertices, columns over P
+    l.pids = o; o += np;                         // original ids of P vertices (ascending)
+    o = (o + 1) & ~1LL;
+    l.pkey = o; o += 2LL * np;                   // vertex keys of P vertices (uint64)
+    l.loc = o; o += deg;                         // position in N(v) -> local row code
+    l.xx = o; o += nx;                           // compact X_X list (Section 3.5)
+    l.spill = o; o += nx;                        // partition scratch
+    l.plist = o; o += np;                        // pivot candidates from P u X_P
+    o = (o + 3) & ~3LL;
+    l.LV = (4 + 3 * l.W + 3) & ~3;               // level: S(2) lpX cursor | P0 | XP0 | C
+    l.stack = o; o += (long long)(np + 1) * l.LV;
+    l.total = (o + 3) & ~3LL;
+    return l;
+}
+
+// Launchers (each returns the CUDA error of its launch).
+cudaError_t launch_ingest_check(const DevGraph &g, int *d_unsorted_list, int *d_unsorted_n,
+                                cudaStream_t s);
+cudaError_t launch_ingest_sort(const DevGraph &g, int *adj_mut, const int *d_list, int n_list,
+                               int *scratch, long long scratch_len, cudaStream_t s);
+cudaError_t launch_ingest_sort_large(const DevGraph &g, int *adj_mut, int v, int *scratch,
+                                     cudaStream_t s);
+cudaError_t launch_ingest_validate(const DevGraph &g, cudaStream_t s);
+cudaError_t launch_order(const DevGraph &g, int peel_blocks, long long spin_limit_ns,
+                         cudaStream_t s);
+cudaError_t launch_search(const SearchArgs &a, int blocks, int threads, size_t smem,
+                          cudaStream_t s);
+cudaError_t search_occupancy(int threads, size_t smem, int *blocks_per_sm);
+cudaError_t launch_finalize(const DevGraph &g, const DevOut &o, unsigned long long *d_out,
+                            int include_isolated, cudaStream_t s);
+cudaError_t launch_enum_layout(const DevGraph &g, const unsigned long long *d_counts,
+                               int hist_len, long long *region_ids, long long *region_cl,
+                               unsigned long long *cursor, long long *d_totals, cudaStream_t s);
+cudaError_t launch_enum_isolated(const DevGraph &g, const DevOut &o, cudaStream_t s);
+cudaError_t launch_enum_close(const DevOut &o, const long long *d_totals, cudaStream_t s);
+
+// ------------------------------------------------------------------ device helpers
+
+__device__ __forceinline__ unsigned long long globaltimer_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void set_status(DevCtrl *c, int code)
+{
+    atomicCAS(&c->status, 0, code);
+}
+
+__device__ __forceinline__ int load_status(const DevCtrl *c)
+{
+    return *(volatile const int *)&c->status;
+}
+
+// SplitMix64 output function (Steele, Lea, Flood, "Fast splittable pseudorandom number
+// generators", OOPSLA 2014) -- the mixing step of the result hash.
+__device__ __forceinline__ unsigned long long mix64(unsigned long long z)
+{
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBULL;
+    return z ^ (z >> 31);
+}
+
+// key(v): the (v+1)-th output of SplitMix64 seeded with 0.
+__device__ __forceinline__ unsigned long long vertex_key(int v)
+{
+    return mix64((unsigned long long)((unsigned)v + 1u) * 0x9E3779B97F4A7C15ULL);
+}
+
+}  // namespace mce

@@ -1,0 +1,317 @@
+// Degeneracy order on the GPU ("Parallelizing Maximal Clique Enumeration on GPUs",
+// Section 2.4, "Degeneracy Ordering"; its time is part of the reported time, Section 4.1).
+//
+// The pages do not say how the order is computed.  This file computes one particular
+// degeneracy order, the "canonical peel": level k starts at 0; a round removes, all at once,
+// every remaining vertex with at most k remaining neighbours; when a round would be empty, k
+// rises to the smallest remaining degree.  A vertex's position is its (round, id) rank, and
+// its core number is the level at which it was removed.  Every vertex then has at most d
+// later neighbours, d being the degeneracy (largest level).
+//
+// One cooperative kernel runs all rounds: the remaining vertices stay in an id-ordered list
+// that is compacted stably every round, so each round's removals come out already in id
+// order and the order needs no sort.  Grid-wide barriers separate the phases of a round; once
+// at most kPeelSoloVertices vertices remain, CTA 0 finishes alone with CTA barriers.  Every
+// barrier wait is bounded by spin_limit_ns.
+//
+// Then three small kernels split every adjacency into earlier (X) and later (P) neighbours
+// (only |P| is stored: the search reclassifies neighbours by rank on the fly), count the
+// isolated vertices, and bucket the first-level roots by |P|, heaviest first.
+#include <climits>
+
+#include "mce_internal.cuh"
+
+namespace mce {
+
+namespace {
+
+__device__ __forceinline__ int block_sum(int v, int *sh)
+{
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    v = __reduce_add_sync(0xffffffffu, v);
+    if (lane == 0) sh[w] = v;
+    __syncthreads();
+    int t = 0;
+    for (int i = 0; i < nw; ++i) t += sh[i];
+    __syncthreads();
+    return t;
+}
+
+__device__ __forceinline__ int block_min(int v, int *sh)
+{
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    v = __reduce_min_sync(0xffffffffu, v);
+    if (lane == 0) sh[w] = v;
+    __syncthreads();
+    int t = INT_MAX;
+    for (int i = 0; i < nw; ++i) t = min(t, sh[i]);
+    __syncthreads();
+    return t;
+}
+
+// Exclusive prefix count of `flag` over the CTA (in thread order); *total = CTA-wide count.
+__device__ __forceinline__ int block_excl_scan(bool flag, int *total, int *sh)
+{
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const unsigned m = __ballot_sync(0xffffffffu, flag);
+    if (lane == 0) sh[w] = __popc(m);
+    __syncthreads();
+    int before = 0, t = 0;
+    for (int i = 0; i < nw; ++i) {
+        const int c = sh[i];
+        if (i < w) before += c;
+        t += c;
+    }
+    __syncthreads();
+    *total = t;
+    return before + __popc(m & ((1u << lane) - 1u));
+}
+
+// Grid-wide barrier for a cooperative launch.  Returns false if the wait exceeded the limit
+// (MCE_ERR_DEVICE_TIMEOUT recorded) or another CTA recorded an error.
+__device__ bool grid_barrier(DevCtrl *ctrl, long long limit_ns)
+{
+    __shared__ int s_ok;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int ok = 1;
+        volatile unsigned int *gen = &ctrl->bar_gen;
+        const unsigned int g0 = *gen;
+        __threadfence();
+        if (atomicAdd(&ctrl->bar_count, 1u) == gridDim.x - 1) {
+            atomicExch(&ctrl->bar_count, 0u);
+            __threadfence();
+            atomicAdd((unsigned int *)&ctrl->bar_gen, 1u);
+        } else {
+            const unsigned long long t0 = globaltimer_ns();
+            unsigned int ns = 32;
+            while (*gen == g0) {
+                if ((long long)(globaltimer_ns() - t0) > limit_ns) {
+                    set_status(ctrl, MCE_ERR_DEVICE_TIMEOUT);
+                    ok = 0;
+                    break;
+                }
+                __nanosleep(ns);
+                if (ns < 256) ns <<= 1;
+            }
+        }
+        __threadfence();
+        s_ok = ok && load_status(ctrl) == 0;
+    }
+    __syncthreads();
+    return s_ok != 0;
+}
+
+__global__ void __launch_bounds__(kPeelThreads) peel_kernel(DevGraph g, long long limit_ns)
+{
+    __shared__ int sh[32];
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    const int n = g.n;
+    for (int v = blockIdx.x * nthr + tid; v < n; v += gridDim.x * nthr) {
+        g.deg[v] = g.offs[v + 1] - g.offs[v];
+        g.round_of[v] = -1;
+        g.alive_a[v] = v;
+    }
+    if (!grid_barrier(g.ctrl, limit_ns)) return;
+
+    int *alive = g.alive_a, *alive_next = g.alive_b;
+    int n_alive = n, k = 0, r = 0, pos = 0, phase = 0, dmax = 0;
+    bool solo = false;
+    int nb = gridDim.x, b = blockIdx.x;
+    while (n_alive > 0) {
+        if (!solo && n_alive <= kPeelSoloVertices) {
+            if (blockIdx.x != 0) return;
+            solo = true;
+            nb = 1;
+            b = 0;
+        }
+        // -- count the vertices to remove at level k (and the smallest degree of the others)
+        const int chunk = (n_alive + nb - 1) / nb;
+        const int lo = min(b * chunk, n_alive), hi = min(lo + chunk, n_alive);
+        int cnt = 0, mn = INT_MAX;
+        for (int i = lo + tid; i < hi; i += nthr) {
+            const int dv = g.deg[alive[i]];
+            if (dv <= k) ++cnt;
+            else mn = min(mn, dv);
+        }
+        cnt = block_sum(cnt, sh);
+        mn = block_min(mn, sh);
+        int total, prefix, gmin;
+        if (solo) {
+            total = cnt;
+            prefix = 0;
+            gmin = mn;
+        } else {
+            if (tid == 0) {
+                g.blk_cnt[phase * nb + b] = cnt;
+                g.blk_min[phase * nb + b] = mn;
+            }
+            if (!grid_barrier(g.ctrl, limit_ns)) return;
+            int t = 0, p = 0, m = INT_MAX;
+            for (int i = tid; i < nb; i += nthr) {
+                const int c = g.blk_cnt[phase * nb + i];
+                t += c;
+                if (i < b) p += c;
+                m = min(m, g.blk_min[phase * nb + i]);
+            }
+            total = block_sum(t, sh);
+            prefix = block_sum(p, sh);
+            gmin = block_min(m, sh);
+            phase ^= 1;
+        }
+        if (total == 0) {            // nothing at level k: jump to the smallest remaining degree
+            k = max(k + 1, gmin);
+            continue;
+        }
+        dmax = k;
+        // -- write this round's removals (id order) and the stably compacted survivors
+        int bf = pos + prefix, bs = lo - prefix;
+        for (int i0 = lo; i0 < hi; i0 += nthr) {
+            const int i = i0 + tid;
+            const bool valid = i < hi;
+            const int v = valid ? alive[i] : 0;
+            const bool f = valid && g.deg[v] <= k;
+            int tot;
+            const int rf = block_excl_scan(f, &tot, sh);
+            if (f) {
+                const int p = bf + rf;
+                g.order[p] = v;
+                g.rank[v] = p;
+                g.round_of[v] = r;
+                g.core[v] = k;
+            } else if (valid) {
+                alive_next[bs + tid - rf] = v;
+            }
+            bf += tot;
+            bs += min(nthr, hi - i0) - tot;
+        }
+        if (solo) __syncthreads();
+        else if (!grid_barrier(g.ctrl, limit_ns)) return;
+        // -- remove them at once: every remaining neighbour loses one degree
+        const int lane = tid & 31, wib = tid >> 5, wpb = nthr >> 5;
+        for (int e = b * wpb + wib; e < total; e += nb * wpb) {
+            const int v = g.order[pos + e];
+            const int elo = g.offs[v], ehi = g.offs[v + 1];
+            for (int j = elo + lane; j < ehi; j += 32) {
+                const int u = g.adj[j];
+                if (g.round_of[u] < 0) atomicSub(&g.deg[u], 1);
+            }
+        }
+        if (solo) __syncthreads();
+        else if (!grid_barrier(g.ctrl, limit_ns)) return;
+        pos += total;
+        n_alive -= total;
+        ++r;
+        int *t = alive;
+        alive = alive_next;
+        alive_next = t;
+    }
+    if (blockIdx.x == 0 && tid == 0) {
+        g.ctrl->degeneracy = dmax;
+        g.ctrl->rounds = r;
+    }
+}
+
+constexpr int kOrientThreads = 256;
+
+// |P(v)| = number of neighbours later in the order; isolated vertices; |P| histogram; the
+// per-warp workspace bound; Delta.
+__global__ void __launch_bounds__(kOrientThreads) orient_count_kernel(DevGraph g)
+{
+    __shared__ int s_bucket[kMaxP + 2];
+    for (int i = threadIdx.x; i < kMaxP + 2; i += blockDim.x) s_bucket[i] = 0;
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int warps = gridDim.x * (blockDim.x >> 5);
+    int n_iso = 0, maxp = 0, maxdeg = 0;
+    unsigned long long iso_hash = 0, ws = 0;
+    for (int v = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; v < g.n; v += warps) {
+        const int lo = g.offs[v], hi = g.offs[v + 1];
+        const int rv = g.rank[v];
+        int c = 0;
+        for (int j = lo + lane; j < hi; j += 32) c += g.rank[g.adj[j]] > rv;
+        c = __reduce_add_sync(0xffffffffu, c);
+        if (lane == 0) {
+            g.pcount[v] = c;
+            const int deg = hi - lo;
+            maxdeg = max(maxdeg, deg);
+            if (deg == 0) {
+                ++n_iso;
+                iso_hash += mix64(vertex_key(v));
+            }
+            if (c > 0) {
+                atomicAdd(&s_bucket[min(c, kMaxP + 1)], 1);
+                maxp = max(maxp, c);
+                if (c <= kMaxP) {
+                    const unsigned long long need = (unsigned long long)ws_layout(deg, c).total;
+                    ws = need > ws ? need : ws;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < kMaxP + 2; i += blockDim.x)
+        if (s_bucket[i]) atomicAdd(&g.bucket[i], s_bucket[i]);
+    if (lane == 0) {
+        if (n_iso) {
+            atomicAdd(&g.ctrl->n_iso, n_iso);
+            atomicAdd(&g.ctrl->iso_hash, iso_hash);
+        }
+        atomicMax(&g.ctrl->max_pcount, maxp);
+        atomicMax(&g.ctrl->max_degree, maxdeg);
+        atomicMax(&g.ctrl->ws_words, ws);
+    }
+}
+
+// Turns the |P| histogram into bucket cursors, heaviest bucket first.
+__global__ void orient_scan_kernel(DevGraph g)
+{
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    unsigned long long run = 0;
+    for (int c = kMaxP + 1; c >= 1; --c) {
+        const int cnt = g.bucket[c];
+        g.bucket[c] = (int)run;
+        run += cnt;
+    }
+    g.ctrl->n_sched = run;
+}
+
+__global__ void __launch_bounds__(kOrientThreads) orient_scatter_kernel(DevGraph g)
+{
+    for (int v = blockIdx.x * blockDim.x + threadIdx.x; v < g.n; v += gridDim.x * blockDim.x) {
+        const int c = g.pcount[v];
+        if (c > 0) g.sched[atomicAdd(&g.bucket[min(c, kMaxP + 1)], 1)] = v;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_order(const DevGraph &g, int peel_blocks, long long spin_limit_ns,
+                         cudaStream_t s)
+{
+    if (g.n == 0) return cudaSuccess;
+    // reset the fields the kernels accumulate into
+    cudaError_t e = cudaMemsetAsync(&g.ctrl->bar_count, 0, sizeof(unsigned int), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(&g.ctrl->max_pcount, 0, sizeof(int), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(&g.ctrl->ws_words, 0, sizeof(unsigned long long), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(&g.ctrl->n_iso, 0, 2 * sizeof(int), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(&g.ctrl->iso_hash, 0, sizeof(unsigned long long), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(g.bucket, 0, sizeof(int) * (kMaxP + 2), s);
+    if (e != cudaSuccess) return e;
+    DevGraph gg = g;
+    long long lim = spin_limit_ns;
+    void *args[] = {&gg, &lim};
+    e = cudaLaunchCooperativeKernel((const void *)peel_kernel, dim3(peel_blocks),
+                                    dim3(kPeelThreads), args, 0, s);
+    if (e != cudaSuccess) return e;
+    int blocks = (int)((g.n + kOrientThreads / 32 - 1) / (kOrientThreads / 32));
+    if (blocks > 8192) blocks = 8192;
+    orient_count_kernel<<<blocks, kOrientThreads, 0, s>>>(g);
+    orient_scan_kernel<<<1, 32, 0, s>>>(g);
+    int sb = (g.n + kOrientThreads - 1) / kOrientThreads;
+    if (sb > 8192) sb = 8192;
+    orient_scatter_kernel<<<sb, kOrientThreads, 0, s>>>(g);
+    return cudaGetLastError();
+}
+
+}  // namespace mce

@@ -1,0 +1,690 @@
+// The search: Bron-Kerbosch with Tomita pivoting over independent first-level subtrees, one
+// subtree per warp ("Parallelizing Maximal Clique Enumeration on GPUs", Sections 2.3-2.4 and 3).
+//
+// GB300 mapping (the pages assign a subtree to a thread block; here a warp is the unit of
+// work, so that the many small subtrees of sparse graphs do not pay for block-wide barriers):
+//   * one persistent kernel, as many CTAs as can be resident (Section 3.3); every warp claims
+//     first-level roots from a global counter, heaviest |P| first;
+//   * per root v, the warp builds the binary-encoded induced subgraph over P u X
+//     (Sections 2.4 "Induced Subgraphs" and 3.4, the full variant): one bitset row per vertex
+//     of N(v), with one column per vertex of P = later neighbours;
+//   * X is kept compact (Section 3.5): X_P is a per-level bitset over the P columns, X_X a
+//     single list of X rows that is partitioned in place as the search descends, with the end
+//     of each level's part saved in its stack entry;
+//   * the depth-first search is iterative with an explicit stack in the warp's workspace;
+//     bitsets are spread over "sub-warps" of G lanes, each lane holding one 16-byte chunk of a
+//     row (W <= 4 words: G = 1, every lane holds a whole row), so that row loads are 128-bit
+//     and a pivot step scores 32/G rows at once; popcounts are reduced with shuffles.
+// Rows, lists and the stack live in global memory (served by L1/L2); each warp has its own
+// workspace sized at mce_create for the largest root of the graph.
+#include <climits>
+
+#include "mce_internal.cuh"
+
+namespace mce {
+
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+template <int W>
+struct Geo {
+    static constexpr int CH = W < 4 ? W : 4;   // words per lane chunk
+    static constexpr int G = W / CH;           // lanes per row
+    static constexpr int R = 32 / G;           // rows per warp step
+};
+
+template <int CH>
+struct Ck {
+    unsigned w[CH];
+};
+
+template <int CH>
+__device__ __forceinline__ Ck<CH> ck_zero()
+{
+    Ck<CH> c;
+#pragma unroll
+    for (int i = 0; i < CH; ++i) c.w[i] = 0u;
+    return c;
+}
+
+template <int CH>
+__device__ __forceinline__ Ck<CH> ck_load(const unsigned *p)
+{
+    Ck<CH> c;
+    if constexpr (CH == 4) {
+        const uint4 t = *reinterpret_cast<const uint4 *>(p);
+        c.w[0] = t.x; c.w[1] = t.y; c.w[2] = t.z; c.w[3] = t.w;
+    } else if constexpr (CH == 2) {
+        const uint2 t = *reinterpret_cast<const uint2 *>(p);
+        c.w[0] = t.x; c.w[1] = t.y;
+    } else {
+        c.w[0] = *p;
+    }
+    return c;
+}
+
+template <int CH>
+__device__ __forceinline__ void ck_store(unsigned *p, const Ck<CH> &c)
+{
+    if constexpr (CH == 4) {
+        *reinterpret_cast<uint4 *>(p) = make_uint4(c.w[0], c.w[1], c.w[2], c.w[3]);
+    } else if constexpr (CH == 2) {
+        *reinterpret_cast<uint2 *>(p) = make_uint2(c.w[0], c.w[1]);
+    } else {
+        *p = c.w[0];
+    }
+}
+
+template <int CH>
+__device__ __forceinline__ Ck<CH> ck_and(const Ck<CH> &a, const Ck<CH> &b)
+{
+    Ck<CH> c;
+#pragma unroll
+    for (int i = 0; i < CH; ++i) c.w[i] = a.w[i] & b.w[i];
+    return c;
+}
+
+template <int CH>
+__device__ __forceinline__ Ck<CH> ck_andnot(const Ck<CH> &a, const Ck<CH> &b)
+{
+    Ck<CH> c;
+#pragma unroll
+    for (int i = 0; i < CH; ++i) c.w[i] = a.w[i] & ~b.w[i];
+    return c;
+}
+
+template <int CH>
+__device__ __forceinline__ Ck<CH> ck_or(const Ck<CH> &a, const Ck<CH> &b)
+{
+    Ck<CH> c;
+#pragma unroll
+    for (int i = 0; i < CH; ++i) c.w[i] = a.w[i] | b.w[i];
+    return c;
+}
+
+template <int CH>
+__device__ __forceinline__ bool ck_nonzero(const Ck<CH> &a)
+{
+    unsigned t = 0;
+#pragma unroll
+    for (int i = 0; i < CH; ++i) t |= a.w[i];
+    return t != 0;
+}
+
+template <int CH>
+__device__ __forceinline__ int ck_popc(const Ck<CH> &a)
+{
+    int t = 0;
+#pragma unroll
+    for (int i = 0; i < CH; ++i) t += __popc(a.w[i]);
+    return t;
+}
+
+// Sum over the G lanes of a sub-warp (all lanes get the sum).
+template <int G>
+__device__ __forceinline__ int subwarp_sum(int x)
+{
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
+    return x;
+}
+
+template <int G>
+__device__ __forceinline__ int subwarp_min(int x)
+{
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) x = min(x, __shfl_xor_sync(kFull, x, o));
+    return x;
+}
+
+// The bitset with bits [0, np) set, in chunk layout (lane chunk q holds words q*CH ..).
+template <int W>
+__device__ __forceinline__ Ck<Geo<W>::CH> bits_prefix(int np, int q)
+{
+    constexpr int CH = Geo<W>::CH;
+    Ck<CH> c;
+#pragma unroll
+    for (int i = 0; i < CH; ++i) {
+        const int k = q * CH + i;
+        const int lo = k * 32;
+        c.w[i] = np >= lo + 32 ? kFull : (np > lo ? ((1u << (np - lo)) - 1u) : 0u);
+    }
+    return c;
+}
+
+// Bits of `c` with index < b.
+template <int W>
+__device__ __forceinline__ Ck<Geo<W>::CH> bits_below(const Ck<Geo<W>::CH> &c, int b, int q)
+{
+    constexpr int CH = Geo<W>::CH;
+    Ck<CH> r;
+    const int wb = b >> 5;
+    const unsigned m = (1u << (b & 31)) - 1u;
+#pragma unroll
+    for (int i = 0; i < CH; ++i) {
+        const int k = q * CH + i;
+        r.w[i] = k < wb ? c.w[i] : (k == wb ? (c.w[i] & m) : 0u);
+    }
+    return r;
+}
+
+// Index of the lowest set bit of `c` above `after` (after = -1: the lowest), or INT_MAX.
+template <int W>
+__device__ __forceinline__ int lowest_above(const Ck<Geo<W>::CH> &c, int after, int q)
+{
+    constexpr int CH = Geo<W>::CH;
+    int best = INT_MAX;
+#pragma unroll
+    for (int i = CH - 1; i >= 0; --i) {
+        const int k = q * CH + i;
+        unsigned w = c.w[i];
+        const int lo = k * 32;
+        if (after >= lo + 31) w = 0u;
+        else if (after >= lo) w &= ~((2u << (after - lo)) - 1u);
+        if (w) best = lo + __ffs(w) - 1;
+    }
+    return subwarp_min<Geo<W>::G>(best);
+}
+
+__device__ __forceinline__ int lower_bound_dev(const int *a, int len, int key)
+{
+    int lo = 0, hi = len;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(a + mid) < key) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
+}
+
+struct Acc {
+    unsigned long long count, hash, nodes;
+};
+
+struct RootCtx {
+    unsigned *rowsP, *rowsX;
+    int *pids;
+    unsigned long long *pkey;
+    int *loc, *xx, *spill, *plist;
+    unsigned *stack;
+    int np, nx, nxx, LV;
+    int root;
+};
+
+// Reports the maximal clique R u {c}: `size` vertices, hash input `hsum` (sum of keys).
+template <int W>
+__device__ void report(const SearchArgs &a, const RootCtx &r, int L, int c, int size,
+                       unsigned long long hsum, Acc &acc, unsigned long long *s_hist, int lane)
+{
+    if (a.out.ids == nullptr) {
+        if (lane == 0) {
+            acc.count++;
+            acc.hash += mix64(hsum);
+            atomicAdd(&s_hist[size], 1ULL);
+        }
+        return;
+    }
+    // enumeration: slot in the group of cliques of this size, then ids in ascending order
+    unsigned long long slot = 0;
+    if (lane == 0) slot = atomicAdd(&a.out.cursor[size], 1ULL);
+    slot = __shfl_sync(kFull, slot, 0);
+    const long long cl = a.out.region_cl[size] + (long long)slot;
+    if (cl >= a.out.region_cl[size + 1]) {          // more cliques than the counting pass saw
+        if (lane == 0) set_status(a.g.ctrl, MCE_ERR_BUFFER_TOO_SMALL);
+        return;
+    }
+    const long long base = a.out.region_ids[size] + (long long)slot * size;
+    if (lane == 0) a.out.offsets[cl] = base;
+    // element e: 0 = root, 1..L = chosen vertex of level e-1, L+1 = c
+    auto elem = [&](int e) -> int {
+        if (e == 0) return r.root;
+        const int loc = e <= L ? (int)r.stack[(long long)(e - 1) * r.LV + 3] : c;
+        return r.pids[loc];
+    };
+    for (int e = lane; e < size; e += 32) {
+        const int id = elem(e);
+        int rk = 0;
+        for (int f = 0; f < size; ++f) rk += elem(f) < id;
+        a.out.ids[base + rk] = id;
+    }
+}
+
+// Tomita pivot over P u X_P (bits of P | XP) and the live X_X rows xx[0..lpX): the row with
+// the most neighbours in P, ties to the smaller code.  Returns -1 when some vertex of X is
+// adjacent to all of P (no maximal clique below this node: every branch would be cut).
+template <int W>
+__device__ int choose_pivot(const RootCtx &r, const Ck<Geo<W>::CH> &P, const Ck<Geo<W>::CH> &PX,
+                            int npop, int lpX, int lane)
+{
+    constexpr int CH = Geo<W>::CH, G = Geo<W>::G, R = Geo<W>::R;
+    const int q = lane % G, sub = lane / G;
+    // list the members of P u X_P
+    int cntp = 0;
+#pragma unroll
+    for (int k = 0; k < W; ++k) {
+        const unsigned wk = __shfl_sync(kFull, PX.w[k % CH], k / CH);
+        const bool bit = (wk >> lane) & 1u;
+        const unsigned m = __ballot_sync(kFull, bit);
+        if (bit) r.plist[cntp + __popc(m & ((1u << lane) - 1u))] = k * 32 + lane;
+        cntp += __popc(m);
+    }
+    __syncwarp();
+    const int total = cntp + lpX;
+    unsigned best = 0;
+    for (int base = 0; base < total; base += R) {
+        const int t = base + sub;
+        const bool valid = t < total;
+        int code = 0;
+        const unsigned *row = r.rowsP;
+        if (valid) {
+            if (t < cntp) {
+                code = r.plist[t];
+                row = r.rowsP + (long long)code * W;
+            } else {
+                const int x = r.xx[t - cntp];
+                code = r.np + x;
+                row = r.rowsX + (long long)x * W;
+            }
+        }
+        const Ck<CH> rc = valid ? ck_load<CH>(row + q * CH) : ck_zero<CH>();
+        const int cnt = subwarp_sum<G>(ck_popc<CH>(ck_and<CH>(P, rc)));
+        if (valid) {
+            const unsigned key = ((unsigned)cnt << kMaxIdxBits) | (unsigned)(kMaxCode - code);
+            best = key > best ? key : best;
+        }
+        if (__any_sync(kFull, valid && cnt == npop)) return -1;
+    }
+    best = __reduce_max_sync(kFull, best);
+    return kMaxCode - (int)(best & (unsigned)kMaxCode);
+}
+
+// Does some live X_X row have bit c?  (X_X n N(c) non-empty)
+template <int W>
+__device__ __forceinline__ bool xx_hits(const RootCtx &r, int lpX, int c, int lane)
+{
+    const int wc = c >> 5;
+    const unsigned bit = 1u << (c & 31);
+    for (int base = 0; base < lpX; base += 32) {
+        const int i = base + lane;
+        bool hit = false;
+        if (i < lpX) hit = (r.rowsX[(long long)r.xx[i] * W + wc] & bit) != 0u;
+        if (__any_sync(kFull, hit)) return true;
+    }
+    return false;
+}
+
+// Moves the X_X rows adjacent to c to the front of xx[0..lpX) (order kept) and returns their
+// number; the others follow, so the parent's range xx[0..lpX) still holds the same set.
+template <int W>
+__device__ int xx_partition(const RootCtx &r, int lpX, int c, int lane)
+{
+    const int wc = c >> 5;
+    const unsigned bit = 1u << (c & 31);
+    const unsigned lt = (1u << lane) - 1u;
+    int kept = 0, rem = 0;
+    for (int base = 0; base < lpX; base += 32) {
+        const int i = base + lane;
+        const bool in = i < lpX;
+        const int x = in ? r.xx[i] : 0;
+        const bool keep = in && (r.rowsX[(long long)x * W + wc] & bit) != 0u;
+        const unsigned mk = __ballot_sync(kFull, keep);
+        const unsigned mr = __ballot_sync(kFull, in && !keep);
+        if (keep) r.xx[kept + __popc(mk & lt)] = x;
+        else if (in) r.spill[rem + __popc(mr & lt)] = x;
+        kept += __popc(mk);
+        rem += __popc(mr);
+        __syncwarp();
+    }
+    for (int t = lane; t < rem; t += 32) r.xx[kept + t] = r.spill[t];
+    __syncwarp();
+    return kept;
+}
+
+// Depth-first search of one first-level subtree from the node (P, XP, xx[0..lpX)) at level 0
+// whose clique R has `rsize` vertices and key sum `S`.
+template <int W>
+__device__ void dfs(const SearchArgs &a, const RootCtx &r, Ck<Geo<W>::CH> P, Ck<Geo<W>::CH> XP,
+                    int lpX, unsigned long long S, int rsize, Acc &acc,
+                    unsigned long long *s_hist, int lane)
+{
+    constexpr int CH = Geo<W>::CH, G = Geo<W>::G;
+    const int q = lane % G;
+    int L = 0;
+    bool enter = true;
+    Ck<CH> P0, XP0, C;
+    int cursor = -1;
+    while (true) {
+        if (enter) {
+            enter = false;
+            acc.nodes++;
+            const int npop = subwarp_sum<G>(ck_popc<CH>(P));
+            const int piv = choose_pivot<W>(r, P, ck_or<CH>(P, XP), npop, lpX, lane);
+            if (piv < 0) {
+                C = ck_zero<CH>();
+            } else {
+                const unsigned *row = piv < r.np ? r.rowsP + (long long)piv * W
+                                                 : r.rowsX + (long long)(piv - r.np) * W;
+                C = ck_andnot<CH>(P, ck_load<CH>(row + q * CH));
+            }
+            P0 = P;
+            XP0 = XP;
+            cursor = -1;
+            unsigned *lv = r.stack + (long long)L * r.LV;
+            if (lane < G) {
+                ck_store<CH>(lv + 4 + q * CH, P0);
+                ck_store<CH>(lv + 4 + W + q * CH, XP0);
+                ck_store<CH>(lv + 4 + 2 * W + q * CH, C);
+            }
+            if (lane == 0) {
+                *reinterpret_cast<unsigned long long *>(lv) = S;
+                lv[2] = (unsigned)lpX;
+                lv[3] = 0xffffffffu;
+            }
+            __syncwarp();
+        }
+        const int c = lowest_above<W>(C, cursor, q);
+        if (c == INT_MAX) {                       // level exhausted: back up
+            if (L == 0) return;
+            --L;
+            const unsigned *lv = r.stack + (long long)L * r.LV;
+            P0 = ck_load<CH>(lv + 4 + q * CH);
+            XP0 = ck_load<CH>(lv + 4 + W + q * CH);
+            C = ck_load<CH>(lv + 4 + 2 * W + q * CH);
+            S = *reinterpret_cast<const unsigned long long *>(lv);
+            lpX = (int)lv[2];
+            cursor = (int)lv[3];
+            continue;
+        }
+        cursor = c;
+        // branch on c: P at this point is P0 minus earlier candidates, X_P gained them
+        const Ck<CH> pre = bits_below<W>(C, c, q);
+        const Ck<CH> rc = ck_load<CH>(r.rowsP + (long long)c * W + q * CH);
+        const Ck<CH> Pc = ck_and<CH>(ck_andnot<CH>(P0, pre), rc);
+        const Ck<CH> XPc = ck_and<CH>(ck_or<CH>(XP0, pre), rc);
+        const unsigned long long Sc = S + r.pkey[c];
+        if (!__any_sync(kFull, ck_nonzero<CH>(Pc))) {
+            // leaf: R u {c} is maximal iff X n N(c) is empty (Algorithm 2, lines 2-3)
+            if (!__any_sync(kFull, ck_nonzero<CH>(XPc)) && !xx_hits<W>(r, lpX, c, lane)) {
+                report<W>(a, r, L, c, rsize + L + 1, Sc, acc, s_hist, lane);
+                acc.nodes++;
+            }
+            continue;
+        }
+        if (lane == 0) r.stack[(long long)L * r.LV + 3] = (unsigned)c;
+        lpX = xx_partition<W>(r, lpX, c, lane);
+        ++L;
+        P = Pc;
+        XP = XPc;
+        S = Sc;
+        enter = true;
+    }
+}
+
+// Builds the induced subgraph of root v into the warp's workspace and searches it.
+template <int W>
+__device__ void search_root(const SearchArgs &a, unsigned *ws, int v, int deg, int np, Acc &acc,
+                            unsigned long long *s_hist, int lane)
+{
+    constexpr int CH = Geo<W>::CH, G = Geo<W>::G;
+    const WsLayout lay = ws_layout(deg, np);
+    RootCtx r;
+    r.rowsP = ws + lay.rowsP;
+    r.rowsX = ws + lay.rowsX;
+    r.pids = reinterpret_cast<int *>(ws + lay.pids);
+    r.pkey = reinterpret_cast<unsigned long long *>(ws + lay.pkey);
+    r.loc = reinterpret_cast<int *>(ws + lay.loc);
+    r.xx = reinterpret_cast<int *>(ws + lay.xx);
+    r.spill = reinterpret_cast<int *>(ws + lay.spill);
+    r.plist = reinterpret_cast<int *>(ws + lay.plist);
+    r.stack = ws + lay.stack;
+    r.np = np;
+    r.nx = deg - np;
+    r.LV = lay.LV;
+    r.root = v;
+
+    const int *Nv = a.g.adj + a.g.offs[v];
+    const int rv = a.g.rank[v];
+    const unsigned lt = (1u << lane) - 1u;
+    // split N(v) into P (later) and X (earlier), numbering each part in id order
+    int pi = 0, xi = 0;
+    for (int base = 0; base < deg; base += 32) {
+        const int j = base + lane;
+        const bool in = j < deg;
+        const int w = in ? __ldg(Nv + j) : 0;
+        const bool isP = in && __ldg(a.g.rank + w) > rv;
+        const unsigned mp = __ballot_sync(kFull, isP);
+        const unsigned mx = __ballot_sync(kFull, in && !isP);
+        if (isP) {
+            const int idx = pi + __popc(mp & lt);
+            r.pids[idx] = w;
+            r.loc[j] = idx;
+        } else if (in) {
+            r.loc[j] = (xi + __popc(mx & lt)) | INT_MIN;
+        }
+        pi += __popc(mp);
+        xi += __popc(mx);
+    }
+    // zero the rows
+    {
+        const long long words = (long long)deg * W;
+        unsigned *rows = r.rowsP;   // rowsX follows rowsP directly
+        for (long long t = (long long)lane * CH; t < words; t += 32 * CH)
+            ck_store<CH>(rows + t, ck_zero<CH>());
+    }
+    __syncwarp();
+    // column i of every row: adjacency to the i-th P vertex (binary-encoded induced subgraph)
+    for (int i = 0; i < np; ++i) {
+        const int p = r.pids[i];
+        const int plo = __ldg(a.g.offs + p);
+        const int dp = __ldg(a.g.offs + p + 1) - plo;
+        const int wi = i >> 5;
+        const unsigned bi = 1u << (i & 31);
+        if (dp <= deg) {
+            for (int t = lane; t < dp; t += 32) {
+                const int w = __ldg(a.g.adj + plo + t);
+                const int j = lower_bound_dev(Nv, deg, w);
+                if (j < deg && __ldg(Nv + j) == w) {
+                    const int code = r.loc[j];
+                    unsigned *row = code < 0 ? r.rowsX + (long long)(code & INT_MAX) * W
+                                             : r.rowsP + (long long)code * W;
+                    row[wi] |= bi;
+                }
+            }
+        } else {
+            for (int t = lane; t < deg; t += 32) {
+                const int w = __ldg(Nv + t);
+                const int j = lower_bound_dev(a.g.adj + plo, dp, w);
+                if (j < dp && __ldg(a.g.adj + plo + j) == w) {
+                    const int code = r.loc[t];
+                    unsigned *row = code < 0 ? r.rowsX + (long long)(code & INT_MAX) * W
+                                             : r.rowsP + (long long)code * W;
+                    row[wi] |= bi;
+                }
+            }
+        }
+        __syncwarp();
+    }
+    for (int i = lane; i < np; i += 32) r.pkey[i] = vertex_key(r.pids[i]);
+    // X_X: the X vertices with at least one neighbour in P (the others leave X at the first
+    // branch and can never be a better pivot than a P vertex)
+    int nxx = 0;
+    for (int base = 0; base < r.nx; base += 32) {
+        const int x = base + lane;
+        bool keep = false;
+        if (x < r.nx) {
+            unsigned t = 0;
+            for (int k = 0; k < W; ++k) t |= r.rowsX[(long long)x * W + k];
+            keep = t != 0u;
+        }
+        const unsigned m = __ballot_sync(kFull, keep);
+        if (keep) r.xx[nxx + __popc(m & lt)] = x;
+        nxx += __popc(m);
+    }
+    r.nxx = nxx;
+    __syncwarp();
+    const int q = lane % G;
+    dfs<W>(a, r, bits_prefix<W>(np, q), ck_zero<CH>(), nxx, vertex_key(v), 1, acc, s_hist, lane);
+}
+
+__global__ void __launch_bounds__(128) search_kernel(SearchArgs a)
+{
+    extern __shared__ unsigned long long s_hist[];
+    for (int i = threadIdx.x; i < a.out.hist_len; i += blockDim.x) s_hist[i] = 0ULL;
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int wpb = blockDim.x >> 5;
+    const int warp = blockIdx.x * wpb + (threadIdx.x >> 5);
+    unsigned *ws = a.ws + (unsigned long long)warp * a.ws_words;
+    const unsigned long long n_roots = a.roots ? (unsigned long long)a.n_roots : a.g.ctrl->n_sched;
+    Acc acc{0, 0, 0};
+    while (load_status(a.g.ctrl) == 0) {
+        unsigned long long idx = 0;
+        if (lane == 0) idx = atomicAdd(&a.g.ctrl->next_root, 1ULL);
+        idx = __shfl_sync(kFull, idx, 0);
+        if (idx >= n_roots) break;
+        const int v = a.roots ? a.roots[idx] : a.g.sched[idx];
+        if (v < 0 || v >= a.g.n) {
+            if (lane == 0) set_status(a.g.ctrl, MCE_ERR_ID_RANGE);
+            break;
+        }
+        const int deg = a.g.offs[v + 1] - a.g.offs[v];
+        const int np = a.g.pcount[v];
+        if (np == 0) {
+            // R = {v}, P empty: maximal iff X is empty too, i.e. v is isolated
+            if (deg == 0) {
+                RootCtx single{};
+                single.root = v;
+                report<1>(a, single, 0, 0, 1, vertex_key(v), acc, s_hist, lane);
+            }
+            continue;
+        }
+        if (np > kMaxP) {
+            if (lane == 0) set_status(a.g.ctrl, MCE_ERR_LIMIT);
+            break;
+        }
+        switch (wclass(np)) {
+        case 1: search_root<1>(a, ws, v, deg, np, acc, s_hist, lane); break;
+        case 2: search_root<2>(a, ws, v, deg, np, acc, s_hist, lane); break;
+        case 4: search_root<4>(a, ws, v, deg, np, acc, s_hist, lane); break;
+        case 8: search_root<8>(a, ws, v, deg, np, acc, s_hist, lane); break;
+        case 16: search_root<16>(a, ws, v, deg, np, acc, s_hist, lane); break;
+        default: search_root<32>(a, ws, v, deg, np, acc, s_hist, lane); break;
+        }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < a.out.hist_len; i += blockDim.x)
+        if (s_hist[i]) atomicAdd(&a.out.hist[i], s_hist[i]);
+    if (lane == 0) {
+        atomicAdd(&a.g.ctrl->result[0], acc.count);
+        atomicAdd(&a.g.ctrl->result[1], acc.hash);
+        atomicAdd(&a.g.ctrl->tree_nodes, acc.nodes);
+    }
+}
+
+// Output: d_out = [count, hash, hist[0..hist_len)], adding the isolated vertices when the
+// search skipped them (full-graph count).
+__global__ void finalize_kernel(DevGraph g, DevOut o, unsigned long long *d_out,
+                                int include_isolated)
+{
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    const unsigned long long iso = include_isolated ? (unsigned long long)g.ctrl->n_iso : 0ULL;
+    if (i == 0) {
+        d_out[0] = g.ctrl->result[0] + iso;
+        d_out[1] = g.ctrl->result[1] + (include_isolated ? g.ctrl->iso_hash : 0ULL);
+    }
+    if (i < o.hist_len) d_out[2 + i] = o.hist[i] + (i == 1 ? iso : 0ULL);
+}
+
+// Enumeration layout from a count: cliques grouped by size, in ascending size.
+__global__ void enum_layout_kernel(const unsigned long long *counts, int hist_len,
+                                   long long *region_ids, long long *region_cl,
+                                   unsigned long long *cursor, long long *totals)
+{
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    long long ids = 0, cl = 0;
+    for (int k = 0; k < hist_len; ++k) {
+        region_ids[k] = ids;
+        region_cl[k] = cl;
+        cursor[k] = 0ULL;
+        const long long c = (long long)counts[2 + k];
+        cl += c;
+        ids += c * k;
+    }
+    region_ids[hist_len] = ids;
+    region_cl[hist_len] = cl;
+    totals[0] = cl;
+    totals[1] = ids;
+}
+
+// Isolated vertices (skipped by the full-graph search) as cliques of size 1.
+__global__ void enum_isolated_kernel(DevGraph g, DevOut o)
+{
+    for (int v = blockIdx.x * blockDim.x + threadIdx.x; v < g.n; v += gridDim.x * blockDim.x) {
+        if (g.offs[v + 1] != g.offs[v]) continue;
+        const unsigned long long slot = atomicAdd(&o.cursor[1], 1ULL);
+        const long long cl = o.region_cl[1] + (long long)slot;
+        if (cl >= o.region_cl[2]) {
+            set_status(g.ctrl, MCE_ERR_BUFFER_TOO_SMALL);
+            continue;
+        }
+        const long long base = o.region_ids[1] + (long long)slot;
+        o.offsets[cl] = base;
+        o.ids[base] = v;
+    }
+}
+
+__global__ void enum_close_kernel(DevOut o, const long long *totals)
+{
+    if (threadIdx.x == 0 && blockIdx.x == 0) o.offsets[totals[0]] = totals[1];
+}
+
+}  // namespace
+
+cudaError_t search_occupancy(int threads, size_t smem, int *blocks_per_sm)
+{
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, search_kernel, threads,
+                                                         smem);
+}
+
+cudaError_t launch_search(const SearchArgs &a, int blocks, int threads, size_t smem,
+                          cudaStream_t s)
+{
+    search_kernel<<<blocks, threads, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const DevGraph &g, const DevOut &o, unsigned long long *d_out,
+                            int include_isolated, cudaStream_t s)
+{
+    const int n = o.hist_len > 1 ? o.hist_len : 1;
+    finalize_kernel<<<(n + 255) / 256, 256, 0, s>>>(g, o, d_out, include_isolated);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_enum_layout(const DevGraph &g, const unsigned long long *d_counts,
+                               int hist_len, long long *region_ids, long long *region_cl,
+                               unsigned long long *cursor, long long *d_totals, cudaStream_t s)
+{
+    (void)g;
+    enum_layout_kernel<<<1, 32, 0, s>>>(d_counts, hist_len, region_ids, region_cl, cursor,
+                                        d_totals);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_enum_isolated(const DevGraph &g, const DevOut &o, cudaStream_t s)
+{
+    if (g.n == 0) return cudaSuccess;
+    int b = (g.n + 255) / 256;
+    if (b > 4096) b = 4096;
+    enum_isolated_kernel<<<b, 256, 0, s>>>(g, o);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_enum_close(const DevOut &o, const long long *d_totals, cudaStream_t s)
+{
+    enum_close_kernel<<<1, 32, 0, s>>>(o, d_totals);
+    return cudaGetLastError();
+}
+
+}  // namespace mce

@@ -67,14 +67,20 @@ def csr_from_edges(n: int, u, v, name: str = "") -> Graph:
         if u.min() < 0 or v.min() < 0 or u.max() >= n or v.max() >= n:
             raise ValueError("edge endpoint out of range")
     keep = u != v
-    u, v = u[keep], v[keep]
-    lo, hi = np.minimum(u, v), np.maximum(u, v)
-    key = np.unique(lo * n + hi)
-    lo, hi = key // n, key % n
-    src = np.concatenate([lo, hi])
-    dst = np.concatenate([hi, lo])
-    order = np.argsort(src * n + dst, kind="stable")
-    src, dst = src[order], dst[order]
+    lo = np.minimum(u[keep], v[keep])
+    hi = np.maximum(u[keep], v[keep])
+    fwd = lo * n + hi
+    fwd.sort()
+    if fwd.size:
+        fwd = fwd[np.concatenate(([True], fwd[1:] != fwd[:-1]))]     # drop repeated pairs
+    lo = fwd // n
+    hi = fwd - lo * n
+    rev = hi * n + lo
+    rev.sort()
+    both = np.concatenate([fwd, rev])
+    both.sort(kind="stable")                                          # merges two sorted runs
+    src = both // n
+    dst = both - src * n
     counts = np.bincount(src, minlength=n) if n else np.zeros(0, dtype=np.int64)
     offsets = np.zeros(n + 1, dtype=np.int64)
     np.cumsum(counts, out=offsets[1:])
@@ -239,8 +245,8 @@ def sbm_graph(n: int, n_comm: int, smin: int, smax: int, p_in: float, inter_edge
 
     Sizes are drawn uniform in [smin, smax], then random communities are nudged by +-1 (within
     the bounds) until they sum to n.  Inside a community every pair is an edge with probability
-    p_in; `inter_edges` distinct pairs with endpoints in different communities are drawn
-    uniformly.
+    p_in (drawn one community size at a time); `inter_edges` distinct pairs with endpoints in
+    different communities are drawn uniformly.
     """
     rng = _rng(seed)
     sizes = rng.integers(smin, smax + 1, n_comm).astype(np.int64)
@@ -257,15 +263,15 @@ def sbm_graph(n: int, n_comm: int, smin: int, smax: int, p_in: float, inter_edge
     np.cumsum(sizes, out=starts[1:])
     comm_of = np.repeat(np.arange(n_comm, dtype=np.int64), sizes)
     us, vs = [], []
-    tri_cache = {}
-    for ci in range(n_comm):
-        s = int(sizes[ci])
-        if s not in tri_cache:
-            tri_cache[s] = np.triu_indices(s, 1)
-        iu, ju = tri_cache[s]
-        keep = rng.random(iu.size) < p_in
-        us.append(iu[keep] + starts[ci])
-        vs.append(ju[keep] + starts[ci])
+    for s in np.unique(sizes):
+        s = int(s)
+        members = np.nonzero(sizes == s)[0]          # communities of this size, ascending
+        iu, ju = np.triu_indices(s, 1)
+        keep = rng.random((members.size, iu.size)) < p_in
+        ci, pj = np.nonzero(keep)
+        base = starts[members][ci]
+        us.append(iu[pj] + base)
+        vs.append(ju[pj] + base)
     iu, ju = _unique_pairs_uniform(rng, n, inter_edges,
                                    accept=lambda i, j: comm_of[i] != comm_of[j])
     us.append(iu)

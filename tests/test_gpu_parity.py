@@ -1,0 +1,268 @@
+"""GPU parity: the CUDA library against the CPU oracle, bit-exact on (count, hash, histogram),
+the degeneracy order, and the enumerated cliques.  Every call goes through the C ABI
+(libmce_gb300.so via the ctypes binding).
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+from maximal_clique_enumeration_gb300 import graphs as G
+from tests import pins
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from maximal_clique_enumeration_gb300 import build
+    build.build()
+
+
+def _mce():
+    import maximal_clique_enumeration_gb300 as mce
+    return mce
+
+
+def gpu_graph(g, **cfg):
+    mce = _mce()
+    return mce.Graph(torch.from_numpy(g.offsets).cuda(), torch.from_numpy(g.adj).cuda(), g.n,
+                     **cfg)
+
+
+def assert_count_parity(g, roots=None, threads=8, **cfg):
+    expect = O.count(g, roots=roots, threads=threads).key()
+    with gpu_graph(g, **cfg) as h:
+        got = h.count_result() if roots is None else h.count_roots_result(roots)
+    assert got == expect, g.name
+    return got
+
+
+# ---------------------------------------------------------------- worked example, closed forms
+
+def test_worked_example_figure_1():
+    n, edges, cliques, info = pins.load_golden("fig1_example.txt")
+    g = G.csr_from_edges(n, *zip(*edges))
+    mce = _mce()
+    with gpu_graph(g) as h:
+        assert h.count_result() == pins.summary(cliques)
+        ids, offs = h.enumerate()
+        assert sorted(mce.cliques_from(ids, offs)) == cliques
+        assert h.info["degeneracy"] == info["degeneracy"]
+        assert h.info["max_degree"] == info["max_degree"]
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 32, 33, 64, 65, 128, 129, 256, 257, 512, 513, 1000])
+def test_complete_graphs_every_row_width(n):
+    # K_n: the first vertex in the order has |P| = n - 1, so n spans every bitset width
+    with gpu_graph(G.complete_graph(n)) as h:
+        assert h.count_result() == pins.summary([tuple(range(n))])
+
+
+@pytest.mark.parametrize("g,count,size", [
+    (G.empty_graph(1), 1, 1), (G.empty_graph(777), 777, 1),
+    (G.moon_moser(1), 3, 1), (G.moon_moser(4), 81, 4), (G.moon_moser(8), 6561, 8),
+    (G.cocktail_party(12), 4096, 12), (G.path_graph(2), 1, 2), (G.path_graph(1000), 999, 2),
+    (G.cycle_graph(4), 4, 2), (G.cycle_graph(501), 501, 2),
+    (G.complete_multipartite([1] * 400 + [2] * 6), 64, 406),
+    (G.complete_multipartite([1] * 700 + [2] * 4), 16, 704),
+    (G.complete_multipartite([3, 1, 4, 1, 5, 9, 2, 6]), 3 * 4 * 5 * 9 * 2 * 6, 8),
+])
+def test_closed_forms(g, count, size):
+    with gpu_graph(g) as h:
+        c, hs, hist = h.count_result()
+    assert c == count
+    assert hist == tuple([0] * size + [count])
+    assert (c, hs, hist) == O.count(g).key()
+
+
+def test_zero_vertices():
+    with gpu_graph(G.empty_graph(0)) as h:
+        assert h.count_result() == (0, 0, ())
+
+
+# ---------------------------------------------------------------- random and structured graphs
+
+@pytest.mark.parametrize("n,p", [(10, 0.5), (40, 0.3), (64, 0.9), (100, 0.05), (100, 0.5),
+                                 (300, 0.05), (300, 0.2), (1000, 0.01), (45, 0.97)])
+def test_er_vs_oracle(n, p):
+    for seed in range(3):
+        assert_count_parity(G.er_graph(n, p, seed))
+
+
+@pytest.mark.parametrize("seed", [1, 2])
+def test_large_planted_cliques_wide_rows(seed):
+    # a few planted cliques of 300-600 vertices: subtrees with 16- and 32-word rows
+    assert_count_parity(G.planted_graph(3000, 6.0, 5, 300, 600, seed))
+
+
+@pytest.mark.parametrize("name", ["er200", "ba100k", "planted50k", "sbm_c20", "rmat_s10",
+                                  "rmat_s12"])
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_workloads_vs_oracle(name, seed):
+    assert_count_parity(G.config_graph(name, seed))
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_sbm_full_size_vs_oracle(seed):
+    g = G.config_graph("sbm1m", seed)
+    assert_count_parity(g, threads=16)
+
+
+def _light_roots(g, k, seed, max_p):
+    """k seeded roots whose first-level P (from the oracle's order) has fewer than max_p vertices."""
+    _, _, rank, _ = O.peel(g)
+    src = np.repeat(np.arange(g.n), g.degrees())
+    pc = np.bincount(src[rank[g.adj] > rank[src]], minlength=g.n)
+    cand = np.nonzero(pc < max_p)[0]
+    rng = np.random.default_rng(seed)
+    return np.sort(rng.choice(cand, size=min(k, cand.size), replace=False)).astype(np.int32)
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_rmat_s20_sampled_roots_vs_oracle(seed):
+    g = G.config_graph("rmat_s20", seed)
+    roots = _light_roots(g, 3000, seed, 160)
+    assert_count_parity(g, roots=roots, threads=16)
+
+
+# ---------------------------------------------------------------- root subsets, order, enumerate
+
+def test_root_partition_sums_to_full_count():
+    g = G.config_graph("planted50k", 4)
+    mce = _mce()
+    rng = np.random.default_rng(5)
+    label = rng.integers(0, 3, g.n)
+    with gpu_graph(g) as h:
+        full = mce.Graph.unpack(h.count())
+        parts = [h.count_roots(np.nonzero(label == i)[0].astype(np.int32)) for i in range(3)]
+        h.check()
+        tot = sum(p.cpu().numpy().view(np.uint64).astype(object) for p in parts)
+    assert int(tot[0]) == full[0]
+    assert int(tot[1]) % 2**64 == full[1]
+    assert tuple(int(x) for x in np.trim_zeros(np.array(tot[2:], dtype=np.uint64), "b")) == full[2]
+    roots = np.nonzero(label == 1)[0].astype(np.int32)
+    with gpu_graph(g) as h:
+        assert h.count_roots_result(roots) == O.count(g, roots=roots).key()
+
+
+@pytest.mark.parametrize("name,seed", [("er200", 1), ("ba100k", 2), ("rmat_s14", 1),
+                                       ("sbm_c50", 2), ("rmat_s20", 1)])
+def test_degeneracy_order_matches_oracle(name, seed):
+    g = G.config_graph(name, seed)
+    core, _, rank, d = O.peel(g)
+    with gpu_graph(g) as h:
+        r, c = h.order_arrays()
+        assert np.array_equal(r.cpu().numpy(), rank)
+        assert np.array_equal(c.cpu().numpy(), core)
+        assert h.info["degeneracy"] == d
+        h.order()                       # recomputing gives the same order
+        r2, _ = h.order_arrays()
+        assert np.array_equal(r2.cpu().numpy(), rank)
+
+
+@pytest.mark.parametrize("g", [G.config_graph("er200", 3), G.planted_graph(400, 4.0, 4, 8, 20, 1),
+                               G.moon_moser(6), G.disjoint_union([G.empty_graph(5),
+                                                                  G.er_graph(60, 0.3, 2)])])
+def test_enumerate_matches_oracle(g):
+    mce = _mce()
+    with gpu_graph(g) as h:
+        ids, offs = h.enumerate()
+        got = mce.cliques_from(ids, offs)
+    assert len(got) == len(set(got))
+    assert sorted(got) == sorted(O.enumerate_cliques(g))
+    sizes = [len(c) for c in got]
+    assert sizes == sorted(sizes)           # grouped by size, ascending
+
+
+def test_repeat_is_deterministic():
+    g = G.config_graph("ba100k", 3)
+    with gpu_graph(g) as h:
+        a = h.count_result()
+        h.order()
+        b = h.count_result()
+    assert a == b
+
+
+# ---------------------------------------------------------------- input handling and errors
+
+def _shuffled(g, seed):
+    rng = np.random.default_rng(seed)
+    adj = g.adj.copy()
+    for v in range(g.n):
+        lo, hi = g.offsets[v], g.offsets[v + 1]
+        adj[lo:hi] = rng.permutation(adj[lo:hi])
+    return G.Graph(g.n, g.offsets.copy(), adj, g.name + "_shuffled")
+
+
+def test_unsorted_adjacency_is_accepted():
+    star = G.csr_from_edges(5001, np.zeros(5000, int), np.arange(1, 5001))   # one 5000-list
+    for g in [G.config_graph("er200", 1), G.disjoint_union([star, G.er_graph(300, 0.05, 3)])]:
+        expect = O.count(g).key()
+        with gpu_graph(_shuffled(g, 1)) as h:
+            assert h.count_result() == expect
+
+
+def test_host_input_path():
+    mce = _mce()
+    g = G.config_graph("er200", 2)
+    with mce.Graph(g.offsets, g.adj) as h:          # numpy host arrays: copied by the library
+        assert h.count_result() == O.count(g).key()
+
+
+def _raw(n, lists):
+    offs = np.zeros(n + 1, np.int32)
+    offs[1:] = np.cumsum([len(x) for x in lists])
+    adj = np.asarray([y for x in lists for y in x] or [0], np.int32)[: offs[-1]]
+    return G.Graph(n, offs, adj)
+
+
+@pytest.mark.parametrize("lists,code", [
+    ([[0, 1], [0]], "MCE_ERR_NOT_SIMPLE"), ([[1, 1], [0, 0]], "MCE_ERR_NOT_SIMPLE"),
+    ([[1], [0, 2], []], "MCE_ERR_NOT_SYMMETRIC"), ([[5], [0]], "MCE_ERR_ID_RANGE"),
+    ([[-1], [0]], "MCE_ERR_ID_RANGE"),
+])
+def test_invalid_graphs_are_rejected(lists, code):
+    mce = _mce()
+    with pytest.raises(mce.MceError) as e:
+        gpu_graph(_raw(len(lists), lists))
+    assert e.value.name == code
+
+
+def test_bad_offsets_rejected():
+    mce = _mce()
+    g = G.Graph(3, np.asarray([0, 2, 1, 2], np.int32), np.asarray([1, 2], np.int32))
+    with pytest.raises(mce.MceError) as e:
+        gpu_graph(g)
+    assert e.value.name == "MCE_ERR_INVALID_ARG"
+
+
+def test_bad_root_id_is_reported():
+    mce = _mce()
+    g = G.config_graph("er200", 1)
+    with gpu_graph(g) as h:
+        h.count_roots(np.asarray([3, 999], np.int32))
+        assert h.last_error() == 4          # MCE_ERR_ID_RANGE
+        assert h.last_error() == 0          # cleared
+        assert h.count_result() == O.count(g).key()
+
+
+def test_enumerate_buffer_too_small():
+    import ctypes
+    mce = _mce()
+    g = G.config_graph("er200", 1)
+    with gpu_graph(g) as h:
+        sizes = np.zeros(2, np.int64)
+        ids = torch.empty(10, dtype=torch.int32, device="cuda")
+        offs = torch.empty(11, dtype=torch.int64, device="cuda")
+        code = mce.library().mce_enumerate(h._h, mce._stream_ptr(None),
+                                           ctypes.c_void_p(ids.data_ptr()), 10,
+                                           ctypes.c_void_p(offs.data_ptr()), 10,
+                                           sizes.ctypes.data_as(ctypes.c_void_p))
+        assert code == 6
+        r = O.count(g)
+        assert sizes[0] == r.count
+        assert sizes[1] == sum(k * int(c) for k, c in enumerate(r.hist))
