@@ -15,7 +15,10 @@ struct mce_graph {
     mce_config cfg{};
     int sm_count = 0;
     int peel_blocks = 0;
-    int search_blocks = 0, search_threads = 0, n_workers = 0;
+    int search_threads = 0, n_workers = 0;
+    int cls_blocks[kNumClasses] = {}, cls_workers[kNumClasses] = {}, cls_count[kNumClasses] = {};
+    unsigned long long cls_ws[kNumClasses] = {};
+    long long uroots_cap = 0;
     size_t search_smem = 0;
     int degeneracy = 0, max_degree = 0, hist_len = 2, rounds = 0;
     unsigned long long ws_words = 0;
@@ -24,6 +27,7 @@ struct mce_graph {
     unsigned long long *hist_acc = nullptr;     // [hist_len]
     unsigned int *ws = nullptr;
     int *ring = nullptr, *flag = nullptr;
+    unsigned *ring_seq = nullptr;
     long long *region_ids = nullptr, *region_cl = nullptr, *totals = nullptr;
     unsigned long long *cursor = nullptr;
     unsigned long long *count_cache = nullptr;  // [2 + hist_len], full-graph count
@@ -81,49 +85,49 @@ void free_all(mce_graph *h)
     h->allocs.clear();
 }
 
-// Resets the per-search fields of the control block.
+// Resets the per-search accumulators of the control block.
 mce_status reset_search(mce_graph *h, cudaStream_t s)
 {
     DevCtrl *c = h->g.ctrl;
-    MCE_TRY(cudaMemsetAsync(&c->next_root, 0, sizeof(unsigned long long), s));
-    MCE_TRY(cudaMemsetAsync(&c->busy, 0, 3 * sizeof(int), s));
     MCE_TRY(cudaMemsetAsync(&c->tree_nodes, 0, 4 * sizeof(unsigned long long), s));
     MCE_TRY(cudaMemsetAsync(h->hist_acc, 0, sizeof(unsigned long long) * h->hist_len, s));
-    MCE_TRY(cudaMemsetAsync(h->flag, 0, sizeof(int) * (h->n_workers > 0 ? h->n_workers : 1), s));
     return MCE_OK;
 }
 
-SearchArgs search_args(mce_graph *h, const int *roots, long long n_roots)
+// One launch per row-width class, widest first: the prep kernel empties the worker list and
+// the counters, then the persistent search kernel of that class runs.
+mce_status run_search(mce_graph *h, cudaStream_t s, bool user_roots, const DevOut *enum_out)
 {
+    mce_status st = reset_search(h, s);
+    if (st != MCE_OK) return st;
     SearchArgs a{};
     a.g = h->g;
     a.out.hist = h->hist_acc;
     a.out.hist_len = h->hist_len;
-    a.roots = roots;
-    a.n_roots = n_roots;
-    a.ws = h->ws;
-    a.ws_words = h->ws_words;
-    a.ring = h->ring;
-    a.flag = h->flag;
-    a.n_workers = h->n_workers;
-    a.worker_list = h->cfg.worker_list;
-    a.donate_min_p = h->cfg.donate_min_p;
-    a.spin_limit_ns = h->cfg.spin_limit_ns;
-    return a;
-}
-
-mce_status run_search(mce_graph *h, cudaStream_t s, const int *roots, long long n_roots,
-                      const DevOut *enum_out)
-{
-    mce_status st = reset_search(h, s);
-    if (st != MCE_OK) return st;
-    SearchArgs a = search_args(h, roots, n_roots);
     if (enum_out) {
         a.out = *enum_out;
         a.out.hist = h->hist_acc;
         a.out.hist_len = h->hist_len;
     }
-    MCE_TRY(launch_search(a, h->search_blocks, h->search_threads, h->search_smem, s));
+    a.roots = user_roots ? h->g.uroots : h->g.sched;
+    a.range = user_roots ? h->g.ctrl->ucls : h->g.ctrl->cls;
+    a.ws = h->ws;
+    a.ring = h->ring;
+    a.ring_seq = h->ring_seq;
+    a.flag = h->flag;
+    a.worker_list = h->cfg.worker_list;
+    a.donate_min_p = h->cfg.donate_min_p;
+    a.spin_limit_ns = h->cfg.spin_limit_ns;
+    for (int k = kNumClasses - 1; k >= 0; --k) {
+        if (h->cls_workers[k] == 0) continue;             // no vertex of the graph in this class
+        if (!user_roots && h->cls_count[k] == 0) continue;
+        a.cls = k;
+        a.ws_words = h->cls_ws[k];
+        a.n_workers = h->cls_workers[k];
+        MCE_TRY(cudaMemsetAsync(h->flag, 0, sizeof(int) * (size_t)a.n_workers, s));
+        MCE_TRY(launch_search_prep(a, s));
+        MCE_TRY(launch_search(a, h->cls_blocks[k], h->search_threads, h->search_smem, s));
+    }
     return MCE_OK;
 }
 
@@ -248,23 +252,35 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
     h->max_degree = c.max_degree;
     h->hist_len = c.degeneracy + 2;
     if (c.max_pcount > kMaxP || c.max_degree > kMaxCode) return MCE_ERR_LIMIT;
-    h->ws_words = (c.ws_words + 3) & ~3ULL;
-    if (h->ws_words == 0) h->ws_words = 4;
 
-    // search kernel geometry: as many CTAs as can be resident (Section 3.3)
+    // search kernel geometry, per row-width class: as many CTAs as can be resident
+    // (Section 3.3); each warp gets a workspace for the largest root of its class
     int wpb = h->cfg.warps_per_block > 0 ? h->cfg.warps_per_block : kDefaultWarpsPerBlock;
     if (wpb > 4) wpb = 4;
     h->search_threads = 32 * wpb;
     h->search_smem = sizeof(unsigned long long) * (size_t)(h->hist_len + 1);
-    int per_sm = 0;
-    MCE_TRY(search_occupancy(h->search_threads, h->search_smem, &per_sm));
-    if (per_sm < 1) return MCE_ERR_CUDA;
-    if (h->cfg.blocks_per_sm > 0 && h->cfg.blocks_per_sm < per_sm) per_sm = h->cfg.blocks_per_sm;
-    h->search_blocks = per_sm * h->sm_count;
-    h->n_workers = h->search_blocks * wpb;
-    MCE_ALLOC(h, h->ws, (size_t)h->n_workers * h->ws_words);
+    size_t ws_total = 4;
+    for (int k = 0; k < kNumClasses; ++k) {
+        h->cls_count[k] = c.cls[2 * k + 1] - c.cls[2 * k];
+        unsigned long long need = (c.ws_cls[k] + 3) & ~3ULL;
+        if (k == 0 && need < 4) need = 4;                 // isolated roots use 1 word
+        if (need == 0) continue;                          // no vertex of this class
+        int per_sm = 0;
+        MCE_TRY(search_occupancy(k, h->search_threads, h->search_smem, &per_sm));
+        if (per_sm < 1) return MCE_ERR_CUDA;
+        if (h->cfg.blocks_per_sm > 0 && h->cfg.blocks_per_sm < per_sm) per_sm = h->cfg.blocks_per_sm;
+        h->cls_blocks[k] = per_sm * h->sm_count;
+        h->cls_workers[k] = h->cls_blocks[k] * wpb;
+        h->cls_ws[k] = need;
+        if ((size_t)h->cls_workers[k] * need > ws_total) ws_total = (size_t)h->cls_workers[k] * need;
+        if (h->cls_workers[k] > h->n_workers) h->n_workers = h->cls_workers[k];
+    }
+    h->ws_words = ws_total;
+    MCE_ALLOC(h, h->ws, ws_total);
     MCE_ALLOC(h, h->ring, (size_t)h->n_workers);
     MCE_ALLOC(h, h->flag, (size_t)h->n_workers);
+    MCE_ALLOC(h, h->ring_seq, (size_t)h->n_workers);
+    MCE_ALLOC(h, g.ubucket, (size_t)kMaxP + 2);
     MCE_ALLOC(h, h->hist_acc, (size_t)h->hist_len + 1);
     MCE_ALLOC(h, h->region_ids, (size_t)h->hist_len + 2);
     MCE_ALLOC(h, h->region_cl, (size_t)h->hist_len + 2);
@@ -313,7 +329,16 @@ static mce_status count_impl(mce_graph *h, cudaStream_t s, const int32_t *d_root
         MCE_TRY(cudaMemsetAsync(d_out, 0, sizeof(uint64_t) * (2 + (size_t)h->hist_len), s));
         return MCE_OK;
     }
-    mce_status st = run_search(h, s, d_roots, n_roots, nullptr);
+    if (d_roots) {
+        if (n_roots > h->uroots_cap) {
+            int *buf = nullptr;
+            MCE_ALLOC(h, buf, (size_t)n_roots);
+            h->g.uroots = buf;
+            h->uroots_cap = n_roots;
+        }
+        MCE_TRY(launch_bin_roots(h->g, d_roots, (int)n_roots, s));
+    }
+    mce_status st = run_search(h, s, d_roots != nullptr, nullptr);
     if (st != MCE_OK) return st;
     DevOut o{};
     o.hist = h->hist_acc;
@@ -373,7 +398,7 @@ mce_status mce_enumerate(mce_graph *h, void *stream, int32_t *d_ids, int64_t cap
     o.region_cl = h->region_cl;
     o.cursor = h->cursor;
     if (h->n > 0) {
-        mce_status st = run_search(h, s, nullptr, 0, &o);
+        mce_status st = run_search(h, s, false, &o);
         if (st != MCE_OK) return st;
         MCE_TRY(launch_enum_isolated(h->g, o, s));
     }
@@ -419,7 +444,7 @@ mce_status mce_get_info(mce_graph *h, mce_info *info)
     info->hist_len = h->hist_len;
     info->peel_rounds = c.rounds;
     info->n_workers = h->n_workers;
-    info->workspace_bytes = (long long)(h->ws_words * 4ULL * (unsigned long long)h->n_workers);
+    info->workspace_bytes = (long long)(h->ws_words * 4ULL);
     info->tree_nodes = c.tree_nodes;
     info->donations = c.donations;
     return MCE_OK;

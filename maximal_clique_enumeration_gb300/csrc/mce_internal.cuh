@@ -14,6 +14,7 @@ constexpr int kMaxCode = (1 << kMaxIdxBits) - 1;
 constexpr int kPeelThreads = 512;
 constexpr int kPeelSoloVertices = 8192;  // the peel finishes in one CTA below this many vertices
 constexpr int kDefaultWarpsPerBlock = 4;
+constexpr int kNumClasses = 6;           // row widths W = 1, 2, 4, 8, 16, 32 words
 
 // Device-resident control block of a handle.
 struct DevCtrl {
@@ -23,7 +24,8 @@ struct DevCtrl {
     int max_pcount;              // max |P| over first-level subtrees
     unsigned int bar_count;      // grid barrier arrival counter
     unsigned int bar_gen;        // grid barrier generation
-    unsigned long long ws_words; // largest per-warp workspace need (words)
+    unsigned long long ws_words; // largest per-warp workspace need (words), all classes
+    unsigned long long ws_cls[kNumClasses];   // the same per row-width class
     unsigned long long next_root;  // search: root claim counter
     unsigned long long n_sched;    // search: number of scheduled roots
     int busy;                    // worker list: warps holding work
@@ -35,6 +37,11 @@ struct DevCtrl {
     unsigned long long tree_nodes;
     unsigned long long donations;
     unsigned long long result[2];  // count, hash of the last search
+    // first-level roots grouped by row width (class k: W = 1 << k), heaviest class first:
+    // sched[cls[2k] .. cls[2k+1]) for the full schedule, uroots[ucls[2k] .. ucls[2k+1])
+    // for a caller's root list
+    int cls[2 * kNumClasses];    // [begin, end) of class k at cls[2k], cls[2k+1]
+    int ucls[2 * kNumClasses];
 };
 
 // Everything the kernels need about a handle's graph (device pointers).
@@ -53,6 +60,8 @@ struct DevGraph {
     int *alive_a, *alive_b;
     int *blk_cnt, *blk_min;   // peel per-CTA partials [2][grid]
     int *bucket;      // orient: |P| histogram / cursors [kMaxP + 2]
+    int *ubucket;     // the same for a caller's root list [kMaxP + 2]
+    int *uroots;      // a caller's roots, grouped by row width, heaviest first
     DevCtrl *ctrl;
 };
 
@@ -71,12 +80,14 @@ struct DevOut {
 struct SearchArgs {
     DevGraph g;
     DevOut out;
-    const int *roots;        // NULL: g.sched (n_sched entries); else user roots (original ids)
-    long long n_roots;
+    const int *roots;        // g.sched or g.uroots
+    const int *range;        // roots[range[cls] .. range[cls+1]) belong to this launch
+    int cls;                 // row-width class of this launch (W = 1 << cls)
     unsigned int *ws;        // per-warp workspace, ws_words each
     unsigned long long ws_words;
     int *ring;               // worker list: ring of idle warp ids [n_workers]
-    int *flag;               // worker list: per-warp wake flag [n_workers]
+    unsigned *ring_seq;      // worker list: per-slot sequence numbers [n_workers]
+    int *flag;               // worker list: per-warp inbox state [n_workers]
     int n_workers;
     int worker_list;
     int donate_min_p;
@@ -90,10 +101,19 @@ __host__ __device__ inline int wclass(int np)
     return np <= 32 ? 1 : np <= 64 ? 2 : np <= 128 ? 4 : np <= 256 ? 8 : np <= 512 ? 16 : 32;
 }
 
+// Class index k of a |P| value (W = 1 << k); |P| = 0 joins class 0.
+__host__ __device__ inline int wclass_index(int np)
+{
+    return np <= 32 ? 0 : np <= 64 ? 1 : np <= 128 ? 2 : np <= 256 ? 3 : np <= 512 ? 4 : 5;
+}
+
 // Per-warp workspace layout (32-bit word offsets) for a root of degree `deg` with np later
-// neighbours.  The same layout serves a donated branch of such a root.
+// neighbours.  The same layout serves a branch of such a root donated through the worker list:
+// the donor writes the branch into the receiver's workspace at these offsets.
+constexpr int kWsHeader = 80;   // inbox: 16 scalar words, then P and X_P bitsets (32 words each)
+
 struct WsLayout {
-    long long rowsP, rowsX, pids, pkey, loc, xx, spill, plist, stack, total;
+    long long rowsP, rowsX, pids, pkey, rids, loc, xx, spill, plist, stack, total;
     int W, LV;
 };
 
@@ -102,18 +122,19 @@ __host__ __device__ inline WsLayout ws_layout(int deg, int np)
     WsLayout l;
     const int nx = deg - np;
     l.W = wclass(np);
-    long long o = 0;
+    long long o = kWsHeader;
     l.rowsP = o; o += (long long)np * l.W;       // rows of P vertices, columns over P
     l.rowsX = o; o += (long long)nx * l.W;       // rows of X vertices, columns over P
     l.pids = o; o += np;                         // original ids of P vertices (ascending)
     o = (o + 1) & ~1LL;
     l.pkey = o; o += 2LL * np;                   // vertex keys of P vertices (uint64)
+    l.rids = o; o += np + 1;                     // ids of R at level 0 (root, or donated R)
     l.loc = o; o += deg;                         // position in N(v) -> local row code
     l.xx = o; o += nx;                           // compact X_X list (Section 3.5)
     l.spill = o; o += nx;                        // partition scratch
     l.plist = o; o += np;                        // pivot candidates from P u X_P
     o = (o + 3) & ~3LL;
-    l.LV = (4 + 3 * l.W + 3) & ~3;               // level: S(2) lpX cursor | P0 | XP0 | C
+    l.LV = (8 + 3 * l.W + 3) & ~3;               // level: S(2) lpX cursor more pad(3) | P0 XP0 C
     l.stack = o; o += (long long)(np + 1) * l.LV;
     l.total = (o + 3) & ~3LL;
     return l;
@@ -131,7 +152,9 @@ cudaError_t launch_order(const DevGraph &g, int peel_blocks, long long spin_limi
                          cudaStream_t s);
 cudaError_t launch_search(const SearchArgs &a, int blocks, int threads, size_t smem,
                           cudaStream_t s);
-cudaError_t search_occupancy(int threads, size_t smem, int *blocks_per_sm);
+cudaError_t launch_search_prep(const SearchArgs &a, cudaStream_t s);
+cudaError_t search_occupancy(int cls, int threads, size_t smem, int *blocks_per_sm);
+cudaError_t launch_bin_roots(const DevGraph &g, const int *roots, int n_roots, cudaStream_t s);
 cudaError_t launch_finalize(const DevGraph &g, const DevOut &o, unsigned long long *d_out,
                             int include_isolated, cudaStream_t s);
 cudaError_t launch_enum_layout(const DevGraph &g, const unsigned long long *d_counts,

@@ -225,6 +225,7 @@ __global__ void __launch_bounds__(kOrientThreads) orient_count_kernel(DevGraph g
     const int warps = gridDim.x * (blockDim.x >> 5);
     int n_iso = 0, maxp = 0, maxdeg = 0;
     unsigned long long iso_hash = 0, ws = 0;
+    unsigned long long ws_cls[kNumClasses] = {0, 0, 0, 0, 0, 0};
     for (int v = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; v < g.n; v += warps) {
         const int lo = g.offs[v], hi = g.offs[v + 1];
         const int rv = g.rank[v];
@@ -245,6 +246,8 @@ __global__ void __launch_bounds__(kOrientThreads) orient_count_kernel(DevGraph g
                 if (c <= kMaxP) {
                     const unsigned long long need = (unsigned long long)ws_layout(deg, c).total;
                     ws = need > ws ? need : ws;
+                    const int k = wclass_index(c);
+                    ws_cls[k] = need > ws_cls[k] ? need : ws_cls[k];
                 }
             }
         }
@@ -260,20 +263,36 @@ __global__ void __launch_bounds__(kOrientThreads) orient_count_kernel(DevGraph g
         atomicMax(&g.ctrl->max_pcount, maxp);
         atomicMax(&g.ctrl->max_degree, maxdeg);
         atomicMax(&g.ctrl->ws_words, ws);
+        for (int k = 0; k < kNumClasses; ++k)
+            if (ws_cls[k]) atomicMax(&g.ctrl->ws_cls[k], ws_cls[k]);
     }
 }
 
-// Turns the |P| histogram into bucket cursors, heaviest bucket first.
+// Highest |P| of row-width class k (class 5 also takes the over-limit bucket).
+__device__ __forceinline__ int class_hi(int k) { return k == 5 ? kMaxP + 1 : 32 << k; }
+__device__ __forceinline__ int class_lo(int k, int lowest) { return k == 0 ? lowest : (16 << k) + 1; }
+
+// Turns a |P| histogram into bucket cursors, heaviest first, and records where each row-width
+// class starts and ends (buckets lowest .. kMaxP + 1).
+__device__ void buckets_to_cursors(int *bucket, int *cls, int lowest, unsigned long long *total)
+{
+    int run = 0;
+    for (int k = kNumClasses - 1; k >= 0; --k) {
+        cls[2 * k] = run;
+        for (int c = class_hi(k); c >= class_lo(k, lowest); --c) {
+            const int cnt = bucket[c];
+            bucket[c] = run;
+            run += cnt;
+        }
+        cls[2 * k + 1] = run;
+    }
+    if (total) *total = (unsigned long long)run;
+}
+
 __global__ void orient_scan_kernel(DevGraph g)
 {
     if (threadIdx.x != 0 || blockIdx.x != 0) return;
-    unsigned long long run = 0;
-    for (int c = kMaxP + 1; c >= 1; --c) {
-        const int cnt = g.bucket[c];
-        g.bucket[c] = (int)run;
-        run += cnt;
-    }
-    g.ctrl->n_sched = run;
+    buckets_to_cursors(g.bucket, g.ctrl->cls, 1, &g.ctrl->n_sched);
 }
 
 __global__ void __launch_bounds__(kOrientThreads) orient_scatter_kernel(DevGraph g)
@@ -284,7 +303,50 @@ __global__ void __launch_bounds__(kOrientThreads) orient_scatter_kernel(DevGraph
     }
 }
 
+// A caller's root list, grouped by row-width class and heaviest first (like the schedule).
+__global__ void __launch_bounds__(kOrientThreads) bin_count_kernel(DevGraph g, const int *roots,
+                                                                   int n_roots)
+{
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_roots; i += gridDim.x * blockDim.x) {
+        const int v = roots[i];
+        if (v < 0 || v >= g.n) {
+            set_status(g.ctrl, MCE_ERR_ID_RANGE);
+            continue;
+        }
+        atomicAdd(&g.ubucket[min(g.pcount[v], kMaxP + 1)], 1);
+    }
+}
+
+__global__ void bin_scan_kernel(DevGraph g)
+{
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    buckets_to_cursors(g.ubucket, g.ctrl->ucls, 0, nullptr);
+}
+
+__global__ void __launch_bounds__(kOrientThreads) bin_scatter_kernel(DevGraph g, const int *roots,
+                                                                     int n_roots)
+{
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_roots; i += gridDim.x * blockDim.x) {
+        const int v = roots[i];
+        if (v < 0 || v >= g.n) continue;
+        g.uroots[atomicAdd(&g.ubucket[min(g.pcount[v], kMaxP + 1)], 1)] = v;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_bin_roots(const DevGraph &g, const int *roots, int n_roots, cudaStream_t s)
+{
+    cudaError_t e = cudaMemsetAsync(g.ubucket, 0, sizeof(int) * (kMaxP + 2), s);
+    if (e != cudaSuccess) return e;
+    int b = (n_roots + kOrientThreads - 1) / kOrientThreads;
+    if (b < 1) b = 1;
+    if (b > 4096) b = 4096;
+    bin_count_kernel<<<b, kOrientThreads, 0, s>>>(g, roots, n_roots);
+    bin_scan_kernel<<<1, 32, 0, s>>>(g);
+    bin_scatter_kernel<<<b, kOrientThreads, 0, s>>>(g, roots, n_roots);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_order(const DevGraph &g, int peel_blocks, long long spin_limit_ns,
                          cudaStream_t s)
@@ -293,7 +355,8 @@ cudaError_t launch_order(const DevGraph &g, int peel_blocks, long long spin_limi
     // reset the fields the kernels accumulate into
     cudaError_t e = cudaMemsetAsync(&g.ctrl->bar_count, 0, sizeof(unsigned int), s);
     if (e == cudaSuccess) e = cudaMemsetAsync(&g.ctrl->max_pcount, 0, sizeof(int), s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(&g.ctrl->ws_words, 0, sizeof(unsigned long long), s);
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync(&g.ctrl->ws_words, 0, sizeof(unsigned long long) * (1 + kNumClasses), s);
     if (e == cudaSuccess) e = cudaMemsetAsync(&g.ctrl->n_iso, 0, 2 * sizeof(int), s);
     if (e == cudaSuccess) e = cudaMemsetAsync(&g.ctrl->iso_hash, 0, sizeof(unsigned long long), s);
     if (e == cudaSuccess) e = cudaMemsetAsync(g.bucket, 0, sizeof(int) * (kMaxP + 2), s);

@@ -19,6 +19,8 @@
 // workspace sized at mce_create for the largest root of the graph.
 #include <climits>
 
+#include <cuda/atomic>
+
 #include "mce_internal.cuh"
 
 namespace mce {
@@ -199,21 +201,60 @@ __device__ __forceinline__ int lower_bound_dev(const int *a, int len, int key)
 }
 
 struct Acc {
-    unsigned long long count, hash, nodes;
+    unsigned long long count, hash, nodes, donations;
 };
 
 struct RootCtx {
     unsigned *rowsP, *rowsX;
     int *pids;
     unsigned long long *pkey;
-    int *loc, *xx, *spill, *plist;
+    int *rids, *loc, *xx, *spill, *plist;
     unsigned *stack;
-    int np, nx, nxx, LV;
-    int root;
+    int deg, np, nx, LV;
+    int rsize;          // |R| at level 0 (1 for a first-level root)
 };
 
+// Inbox header of a warp workspace (word offsets) and inbox states.
+enum { kHdrDeg = 0, kHdrNp = 1, kHdrK = 2, kHdrRsize = 3, kHdrS = 4, kHdrP = 16, kHdrXP = 48 };
+enum : int { kInboxIdle = 0, kInboxFull = 1, kInboxRetired = 2, kInboxClaimed = 4 };
+constexpr long long kDonateCheckCycles = 2048;   // a donor looks at the worker list this often
+
+using dev_int = cuda::atomic_ref<int, cuda::thread_scope_device>;
+using dev_uint = cuda::atomic_ref<unsigned, cuda::thread_scope_device>;
+using dev_ull = cuda::atomic_ref<unsigned long long, cuda::thread_scope_device>;
+
+__device__ __forceinline__ RootCtx make_ctx(unsigned *ws, int deg, int np)
+{
+    const WsLayout lay = ws_layout(deg, np);
+    RootCtx r;
+    r.rowsP = ws + lay.rowsP;
+    r.rowsX = ws + lay.rowsX;
+    r.pids = reinterpret_cast<int *>(ws + lay.pids);
+    r.pkey = reinterpret_cast<unsigned long long *>(ws + lay.pkey);
+    r.rids = reinterpret_cast<int *>(ws + lay.rids);
+    r.loc = reinterpret_cast<int *>(ws + lay.loc);
+    r.xx = reinterpret_cast<int *>(ws + lay.xx);
+    r.spill = reinterpret_cast<int *>(ws + lay.spill);
+    r.plist = reinterpret_cast<int *>(ws + lay.plist);
+    r.stack = ws + lay.stack;
+    r.deg = deg;
+    r.np = np;
+    r.nx = deg - np;
+    r.LV = lay.LV;
+    r.rsize = 1;
+    return r;
+}
+
+// Id of element e of the clique R u {c} at level L: R's level-0 part, then the vertex chosen
+// at each level below L, then c.
+__device__ __forceinline__ int clique_elem(const RootCtx &r, int L, int c, int e)
+{
+    if (e < r.rsize) return r.rids[e];
+    const int loc = e < r.rsize + L ? (int)r.stack[(long long)(e - r.rsize) * r.LV + 3] : c;
+    return r.pids[loc];
+}
+
 // Reports the maximal clique R u {c}: `size` vertices, hash input `hsum` (sum of keys).
-template <int W>
 __device__ void report(const SearchArgs &a, const RootCtx &r, int L, int c, int size,
                        unsigned long long hsum, Acc &acc, unsigned long long *s_hist, int lane)
 {
@@ -236,16 +277,10 @@ __device__ void report(const SearchArgs &a, const RootCtx &r, int L, int c, int 
     }
     const long long base = a.out.region_ids[size] + (long long)slot * size;
     if (lane == 0) a.out.offsets[cl] = base;
-    // element e: 0 = root, 1..L = chosen vertex of level e-1, L+1 = c
-    auto elem = [&](int e) -> int {
-        if (e == 0) return r.root;
-        const int loc = e <= L ? (int)r.stack[(long long)(e - 1) * r.LV + 3] : c;
-        return r.pids[loc];
-    };
     for (int e = lane; e < size; e += 32) {
-        const int id = elem(e);
+        const int id = clique_elem(r, L, c, e);
         int rk = 0;
-        for (int f = 0; f < size; ++f) rk += elem(f) < id;
+        for (int f = 0; f < size; ++f) rk += clique_elem(r, L, c, f) < id;
         a.out.ids[base + rk] = id;
     }
 }
@@ -341,19 +376,121 @@ __device__ int xx_partition(const RootCtx &r, int lpX, int c, int lane)
     return kept;
 }
 
-// Depth-first search of one first-level subtree from the node (P, XP, xx[0..lpX)) at level 0
-// whose clique R has `rsize` vertices and key sum `S`.
+// ------------------------------------------------------------------ worker list (Section 3.3)
+//
+// Idle warps put their id in a bounded multi-producer multi-consumer ring (one slot per warp,
+// so it cannot overflow) and wait on their inbox flag.  A busy warp ("donor") that is about to
+// descend into a branch with |P| >= donate_min_p, with other branches left at the same level
+// and at an earlier level, pops an idle warp, claims its inbox (idle -> claimed), writes the
+// branch into the idle warp's workspace and publishes it (claimed -> full, release).  `busy`
+// counts warps holding work; an idle warp leaves when roots are exhausted and busy == 0.  An
+// idle warp that waited spin_limit_ns retires (idle -> retired); a donor that pops a retired
+// warp keeps the branch.  Ring slots carry sequence numbers, so a slot is never reused before
+// its previous value was taken.  Every wait is bounded.
+
+__device__ bool ring_push(const SearchArgs &a, int w)
+{
+    const int t = dev_int(a.g.ctrl->ring_tail).fetch_add(1, cuda::memory_order_relaxed);
+    const int slot = t % a.n_workers;
+    dev_uint seq(a.ring_seq[slot]);
+    const unsigned long long t0 = globaltimer_ns();
+    unsigned ns = 32;
+    while (seq.load(cuda::memory_order_acquire) != (unsigned)t) {
+        if ((long long)(globaltimer_ns() - t0) > a.spin_limit_ns) {
+            set_status(a.g.ctrl, MCE_ERR_DEVICE_TIMEOUT);
+            return false;
+        }
+        __nanosleep(ns);
+        if (ns < 1024) ns <<= 1;
+    }
+    a.ring[slot] = w;
+    seq.store((unsigned)t + 1u, cuda::memory_order_release);
+    return true;
+}
+
+// Pops an idle warp id, or -1 when the ring is empty (never waits).
+__device__ int ring_try_pop(const SearchArgs &a)
+{
+    dev_int head(a.g.ctrl->ring_head), tail(a.g.ctrl->ring_tail);
+    int h = head.load(cuda::memory_order_relaxed);
+    for (int attempt = 0; attempt < 16; ++attempt) {
+        if (h >= tail.load(cuda::memory_order_relaxed)) return -1;
+        const int slot = h % a.n_workers;
+        dev_uint seq(a.ring_seq[slot]);
+        const unsigned sq = seq.load(cuda::memory_order_acquire);
+        if (sq == (unsigned)h + 1u) {
+            if (head.compare_exchange_strong(h, h + 1, cuda::memory_order_relaxed)) {
+                const int w = a.ring[slot];
+                seq.store((unsigned)h + (unsigned)a.n_workers, cuda::memory_order_release);
+                return w;
+            }
+        } else if ((int)(sq - ((unsigned)h + 1u)) < 0) {
+            return -1;                           // its pusher has not written the slot yet
+        } else {
+            h = head.load(cuda::memory_order_relaxed);
+        }
+    }
+    return -1;
+}
+
+// Copies the branch R u {c} with sets (Pc, XPc, xx[0..k)) into the workspace `dst` of another
+// warp: the P rows, the k live X rows (renumbered 0..k-1), the P ids and keys, R's ids.
+template <int W>
+__device__ void write_branch(const RootCtx &r, unsigned *dst, int L, int c,
+                             const Ck<Geo<W>::CH> &Pc, const Ck<Geo<W>::CH> &XPc, int k,
+                             unsigned long long Sc, int lane)
+{
+    constexpr int CH = Geo<W>::CH, G = Geo<W>::G;
+    const int q = lane % G;
+    const WsLayout lay = ws_layout(r.deg, r.np);
+    const int rsize = r.rsize + L + 1;
+    if (lane == 0) {
+        dst[kHdrDeg] = (unsigned)r.deg;
+        dst[kHdrNp] = (unsigned)r.np;
+        dst[kHdrK] = (unsigned)k;
+        dst[kHdrRsize] = (unsigned)rsize;
+        *reinterpret_cast<unsigned long long *>(dst + kHdrS) = Sc;
+    }
+    if (lane < G) {
+        ck_store<CH>(dst + kHdrP + q * CH, Pc);
+        ck_store<CH>(dst + kHdrXP + q * CH, XPc);
+    }
+    const long long pw = (long long)r.np * W;
+    for (long long t = (long long)lane * CH; t < pw; t += 32 * CH)
+        ck_store<CH>(dst + lay.rowsP + t, ck_load<CH>(r.rowsP + t));
+    int *dxx = reinterpret_cast<int *>(dst + lay.xx);
+    for (long long t = lane; t < (long long)k * W; t += 32) {
+        const long long i = t / W;
+        const int x = r.xx[i];
+        dst[lay.rowsX + t] = r.rowsX[(long long)x * W + (t - i * W)];
+    }
+    for (int i = lane; i < k; i += 32) dxx[i] = i;
+    int *dp = reinterpret_cast<int *>(dst + lay.pids);
+    unsigned long long *dk = reinterpret_cast<unsigned long long *>(dst + lay.pkey);
+    for (int i = lane; i < r.np; i += 32) {
+        dp[i] = r.pids[i];
+        dk[i] = r.pkey[i];
+    }
+    int *dr = reinterpret_cast<int *>(dst + lay.rids);
+    for (int e = lane; e < rsize; e += 32) dr[e] = clique_elem(r, L, c, e);
+    __syncwarp();
+}
+
+// Depth-first search of one first-level subtree (or donated branch) from the node
+// (P, XP, xx[0..lpX)) at level 0 whose clique R has r.rsize vertices and key sum S.
 template <int W>
 __device__ void dfs(const SearchArgs &a, const RootCtx &r, Ck<Geo<W>::CH> P, Ck<Geo<W>::CH> XP,
-                    int lpX, unsigned long long S, int rsize, Acc &acc,
-                    unsigned long long *s_hist, int lane)
+                    int lpX, unsigned long long S, Acc &acc, unsigned long long *s_hist,
+                    int lane)
 {
     constexpr int CH = Geo<W>::CH, G = Geo<W>::G;
     const int q = lane % G;
     int L = 0;
     bool enter = true;
+    bool more_below = false;   // some level below L still has branches to explore
     Ck<CH> P0, XP0, C;
     int cursor = -1;
+    long long last_check = clock64();
     while (true) {
         if (enter) {
             enter = false;
@@ -372,14 +509,15 @@ __device__ void dfs(const SearchArgs &a, const RootCtx &r, Ck<Geo<W>::CH> P, Ck<
             cursor = -1;
             unsigned *lv = r.stack + (long long)L * r.LV;
             if (lane < G) {
-                ck_store<CH>(lv + 4 + q * CH, P0);
-                ck_store<CH>(lv + 4 + W + q * CH, XP0);
-                ck_store<CH>(lv + 4 + 2 * W + q * CH, C);
+                ck_store<CH>(lv + 8 + q * CH, P0);
+                ck_store<CH>(lv + 8 + W + q * CH, XP0);
+                ck_store<CH>(lv + 8 + 2 * W + q * CH, C);
             }
             if (lane == 0) {
                 *reinterpret_cast<unsigned long long *>(lv) = S;
                 lv[2] = (unsigned)lpX;
                 lv[3] = 0xffffffffu;
+                lv[4] = more_below ? 1u : 0u;
             }
             __syncwarp();
         }
@@ -388,12 +526,13 @@ __device__ void dfs(const SearchArgs &a, const RootCtx &r, Ck<Geo<W>::CH> P, Ck<
             if (L == 0) return;
             --L;
             const unsigned *lv = r.stack + (long long)L * r.LV;
-            P0 = ck_load<CH>(lv + 4 + q * CH);
-            XP0 = ck_load<CH>(lv + 4 + W + q * CH);
-            C = ck_load<CH>(lv + 4 + 2 * W + q * CH);
+            P0 = ck_load<CH>(lv + 8 + q * CH);
+            XP0 = ck_load<CH>(lv + 8 + W + q * CH);
+            C = ck_load<CH>(lv + 8 + 2 * W + q * CH);
             S = *reinterpret_cast<const unsigned long long *>(lv);
             lpX = (int)lv[2];
             cursor = (int)lv[3];
+            more_below = lv[4] != 0u;
             continue;
         }
         cursor = c;
@@ -406,13 +545,47 @@ __device__ void dfs(const SearchArgs &a, const RootCtx &r, Ck<Geo<W>::CH> P, Ck<
         if (!__any_sync(kFull, ck_nonzero<CH>(Pc))) {
             // leaf: R u {c} is maximal iff X n N(c) is empty (Algorithm 2, lines 2-3)
             if (!__any_sync(kFull, ck_nonzero<CH>(XPc)) && !xx_hits<W>(r, lpX, c, lane)) {
-                report<W>(a, r, L, c, rsize + L + 1, Sc, acc, s_hist, lane);
+                report(a, r, L, c, r.rsize + L + 1, Sc, acc, s_hist, lane);
                 acc.nodes++;
             }
             continue;
         }
+        const bool more_same = lowest_above<W>(C, c, q) != INT_MAX;
         if (lane == 0) r.stack[(long long)L * r.LV + 3] = (unsigned)c;
-        lpX = xx_partition<W>(r, lpX, c, lane);
+        const int lpXc = xx_partition<W>(r, lpX, c, lane);
+        // worker list: hand this branch to an idle warp instead of descending (Section 3.3)
+        if (a.worker_list && more_same && more_below) {
+            const long long now = clock64();
+            if (now - last_check > kDonateCheckCycles &&
+                subwarp_sum<G>(ck_popc<CH>(Pc)) >= a.donate_min_p) {
+                last_check = now;
+                int recv = -1;
+                if (lane == 0) {
+                    recv = ring_try_pop(a);
+                    if (recv >= 0) {
+                        int expect = kInboxIdle;
+                        if (!dev_int(a.flag[recv]).compare_exchange_strong(
+                                expect, kInboxClaimed, cuda::memory_order_acq_rel))
+                            recv = -1;                // it retired meanwhile
+                        else
+                            dev_int(a.g.ctrl->busy).fetch_add(1, cuda::memory_order_relaxed);
+                    }
+                }
+                recv = __shfl_sync(kFull, recv, 0);
+                if (recv >= 0) {
+                    unsigned *dst = a.ws + (unsigned long long)recv * a.ws_words;
+                    write_branch<W>(r, dst, L, c, Pc, XPc, lpXc, Sc, lane);
+                    if (lane == 0) {
+                        __threadfence();
+                        dev_int(a.flag[recv]).store(kInboxFull, cuda::memory_order_release);
+                        acc.donations++;
+                    }
+                    continue;
+                }
+            }
+        }
+        more_below = more_below || more_same;
+        lpX = lpXc;
         ++L;
         P = Pc;
         XP = XPc;
@@ -427,22 +600,7 @@ __device__ void search_root(const SearchArgs &a, unsigned *ws, int v, int deg, i
                             unsigned long long *s_hist, int lane)
 {
     constexpr int CH = Geo<W>::CH, G = Geo<W>::G;
-    const WsLayout lay = ws_layout(deg, np);
-    RootCtx r;
-    r.rowsP = ws + lay.rowsP;
-    r.rowsX = ws + lay.rowsX;
-    r.pids = reinterpret_cast<int *>(ws + lay.pids);
-    r.pkey = reinterpret_cast<unsigned long long *>(ws + lay.pkey);
-    r.loc = reinterpret_cast<int *>(ws + lay.loc);
-    r.xx = reinterpret_cast<int *>(ws + lay.xx);
-    r.spill = reinterpret_cast<int *>(ws + lay.spill);
-    r.plist = reinterpret_cast<int *>(ws + lay.plist);
-    r.stack = ws + lay.stack;
-    r.np = np;
-    r.nx = deg - np;
-    r.LV = lay.LV;
-    r.root = v;
-
+    RootCtx r = make_ctx(ws, deg, np);
     const int *Nv = a.g.adj + a.g.offs[v];
     const int rv = a.g.rank[v];
     const unsigned lt = (1u << lane) - 1u;
@@ -472,6 +630,7 @@ __device__ void search_root(const SearchArgs &a, unsigned *ws, int v, int deg, i
         for (long long t = (long long)lane * CH; t < words; t += 32 * CH)
             ck_store<CH>(rows + t, ck_zero<CH>());
     }
+    if (lane == 0) r.rids[0] = v;
     __syncwarp();
     // column i of every row: adjacency to the i-th P vertex (binary-encoded induced subgraph)
     for (int i = 0; i < np; ++i) {
@@ -521,13 +680,37 @@ __device__ void search_root(const SearchArgs &a, unsigned *ws, int v, int deg, i
         if (keep) r.xx[nxx + __popc(m & lt)] = x;
         nxx += __popc(m);
     }
-    r.nxx = nxx;
     __syncwarp();
     const int q = lane % G;
-    dfs<W>(a, r, bits_prefix<W>(np, q), ck_zero<CH>(), nxx, vertex_key(v), 1, acc, s_hist, lane);
+    dfs<W>(a, r, bits_prefix<W>(np, q), ck_zero<CH>(), nxx, vertex_key(v), acc, s_hist, lane);
 }
 
-__global__ void __launch_bounds__(128) search_kernel(SearchArgs a)
+// Searches a branch that another warp wrote into this warp's workspace.
+template <int W>
+__device__ void search_inbox(const SearchArgs &a, unsigned *ws, Acc &acc,
+                             unsigned long long *s_hist, int lane)
+{
+    constexpr int CH = Geo<W>::CH, G = Geo<W>::G;
+    const int q = lane % G;
+    RootCtx r = make_ctx(ws, (int)ws[kHdrDeg], (int)ws[kHdrNp]);
+    r.rsize = (int)ws[kHdrRsize];
+    const int k = (int)ws[kHdrK];
+    const unsigned long long S = *reinterpret_cast<const unsigned long long *>(ws + kHdrS);
+    const Ck<CH> P = ck_load<CH>(ws + kHdrP + q * CH);
+    const Ck<CH> XP = ck_load<CH>(ws + kHdrXP + q * CH);
+    dfs<W>(a, r, P, XP, k, S, acc, s_hist, lane);
+}
+
+// CTAs per SM the compiler should plan registers for, per row width (more for narrow rows).
+template <int W>
+struct MinBlocks {
+    static constexpr int value = W <= 2 ? 8 : (W <= 8 ? 6 : 4);
+};
+
+// One persistent launch per row width W: the roots of that class, heaviest first, then
+// donated branches of those roots (Section 3.3).
+template <int W>
+__global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(SearchArgs a)
 {
     extern __shared__ unsigned long long s_hist[];
     for (int i = threadIdx.x; i < a.out.hist_len; i += blockDim.x) s_hist[i] = 0ULL;
@@ -536,41 +719,82 @@ __global__ void __launch_bounds__(128) search_kernel(SearchArgs a)
     const int wpb = blockDim.x >> 5;
     const int warp = blockIdx.x * wpb + (threadIdx.x >> 5);
     unsigned *ws = a.ws + (unsigned long long)warp * a.ws_words;
-    const unsigned long long n_roots = a.roots ? (unsigned long long)a.n_roots : a.g.ctrl->n_sched;
-    Acc acc{0, 0, 0};
+    const unsigned long long begin = (unsigned long long)a.range[2 * a.cls];
+    const unsigned long long n_roots = (unsigned long long)a.range[2 * a.cls + 1] - begin;
+    dev_int busy(a.g.ctrl->busy);
+    Acc acc{0, 0, 0, 0};
+    // phase 1: first-level subtrees from the shared counter
     while (load_status(a.g.ctrl) == 0) {
         unsigned long long idx = 0;
-        if (lane == 0) idx = atomicAdd(&a.g.ctrl->next_root, 1ULL);
+        if (lane == 0) {
+            busy.fetch_add(1, cuda::memory_order_relaxed);
+            idx = atomicAdd(&a.g.ctrl->next_root, 1ULL);
+            if (idx >= n_roots) busy.fetch_sub(1, cuda::memory_order_acq_rel);
+        }
         idx = __shfl_sync(kFull, idx, 0);
         if (idx >= n_roots) break;
-        const int v = a.roots ? a.roots[idx] : a.g.sched[idx];
-        if (v < 0 || v >= a.g.n) {
-            if (lane == 0) set_status(a.g.ctrl, MCE_ERR_ID_RANGE);
-            break;
-        }
+        const int v = a.roots[begin + idx];
         const int deg = a.g.offs[v + 1] - a.g.offs[v];
         const int np = a.g.pcount[v];
         if (np == 0) {
             // R = {v}, P empty: maximal iff X is empty too, i.e. v is isolated
             if (deg == 0) {
                 RootCtx single{};
-                single.root = v;
-                report<1>(a, single, 0, 0, 1, vertex_key(v), acc, s_hist, lane);
+                single.rids = reinterpret_cast<int *>(ws);
+                single.rsize = 1;
+                if (lane == 0) single.rids[0] = v;
+                __syncwarp();
+                report(a, single, 0, 0, 1, vertex_key(v), acc, s_hist, lane);
             }
-            continue;
-        }
-        if (np > kMaxP) {
+        } else if (np > kMaxP) {
             if (lane == 0) set_status(a.g.ctrl, MCE_ERR_LIMIT);
-            break;
+        } else {
+            search_root<W>(a, ws, v, deg, np, acc, s_hist, lane);
         }
-        switch (wclass(np)) {
-        case 1: search_root<1>(a, ws, v, deg, np, acc, s_hist, lane); break;
-        case 2: search_root<2>(a, ws, v, deg, np, acc, s_hist, lane); break;
-        case 4: search_root<4>(a, ws, v, deg, np, acc, s_hist, lane); break;
-        case 8: search_root<8>(a, ws, v, deg, np, acc, s_hist, lane); break;
-        case 16: search_root<16>(a, ws, v, deg, np, acc, s_hist, lane); break;
-        default: search_root<32>(a, ws, v, deg, np, acc, s_hist, lane); break;
+        __syncwarp();
+        if (lane == 0) busy.fetch_sub(1, cuda::memory_order_acq_rel);
+    }
+    // phase 2: receive donated branches until no warp holds work
+    while (a.worker_list && load_status(a.g.ctrl) == 0) {
+        int state = 0;   // 1: a branch arrived, 2: leave
+        if (lane == 0) {
+            if (!ring_push(a, warp)) state = 2;
+            dev_int flag(a.flag[warp]);
+            const unsigned long long t0 = globaltimer_ns();
+            unsigned ns = 64;
+            while (state == 0) {
+                const int f = flag.load(cuda::memory_order_acquire);
+                const long long waited = (long long)(globaltimer_ns() - t0);
+                if (f == kInboxFull) {
+                    state = 1;
+                } else if (f == kInboxIdle) {
+                    if (busy.load(cuda::memory_order_acquire) == 0 || load_status(a.g.ctrl) != 0) {
+                        state = 2;                       // nothing left anywhere
+                    } else if (waited > a.spin_limit_ns) {
+                        int expect = kInboxIdle;
+                        if (flag.compare_exchange_strong(expect, kInboxRetired,
+                                                         cuda::memory_order_acq_rel))
+                            state = 2;                   // retire; donors skip this warp
+                    }
+                } else if (waited > a.spin_limit_ns + a.spin_limit_ns) {
+                    set_status(a.g.ctrl, MCE_ERR_DEVICE_TIMEOUT);   // claimed, never filled
+                    state = 2;
+                }
+                if (state == 0) {
+                    __nanosleep(ns);
+                    if (ns < 2048) ns <<= 1;
+                }
+            }
+            if (state == 1) flag.store(kInboxIdle, cuda::memory_order_relaxed);
         }
+        state = __shfl_sync(kFull, state, 0);
+        if (state != 1) break;
+        __syncwarp();
+        dev_int(a.flag[warp]).load(cuda::memory_order_acquire);
+        __threadfence();
+        search_inbox<W>(a, ws, acc, s_hist, lane);
+        __syncwarp();
+        if (lane == 0) busy.fetch_sub(1, cuda::memory_order_acq_rel);
     }
     __syncthreads();
     for (int i = threadIdx.x; i < a.out.hist_len; i += blockDim.x)
@@ -579,6 +803,20 @@ __global__ void __launch_bounds__(128) search_kernel(SearchArgs a)
         atomicAdd(&a.g.ctrl->result[0], acc.count);
         atomicAdd(&a.g.ctrl->result[1], acc.hash);
         atomicAdd(&a.g.ctrl->tree_nodes, acc.nodes);
+        atomicAdd(&a.g.ctrl->donations, acc.donations);
+    }
+}
+
+// Before each launch: empty worker list (slot i expects push number i) and fresh counters.
+__global__ void search_prep_kernel(unsigned *seq, int n, DevCtrl *ctrl)
+{
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    for (int i = t; i < n; i += gridDim.x * blockDim.x) seq[i] = (unsigned)i;
+    if (t == 0) {
+        ctrl->next_root = 0ULL;
+        ctrl->busy = 0;
+        ctrl->ring_head = 0;
+        ctrl->ring_tail = 0;
     }
 }
 
@@ -641,16 +879,39 @@ __global__ void enum_close_kernel(DevOut o, const long long *totals)
 
 }  // namespace
 
-cudaError_t search_occupancy(int threads, size_t smem, int *blocks_per_sm)
+template <int W>
+static const void *kernel_of() { return (const void *)search_kernel<W>; }
+
+static const void *search_kernel_ptr(int cls)
 {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, search_kernel, threads,
-                                                         smem);
+    switch (cls) {
+    case 0: return kernel_of<1>();
+    case 1: return kernel_of<2>();
+    case 2: return kernel_of<4>();
+    case 3: return kernel_of<8>();
+    case 4: return kernel_of<16>();
+    default: return kernel_of<32>();
+    }
+}
+
+cudaError_t search_occupancy(int cls, int threads, size_t smem, int *blocks_per_sm)
+{
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, search_kernel_ptr(cls),
+                                                         threads, smem);
 }
 
 cudaError_t launch_search(const SearchArgs &a, int blocks, int threads, size_t smem,
                           cudaStream_t s)
 {
-    search_kernel<<<blocks, threads, smem, s>>>(a);
+    SearchArgs aa = a;
+    void *args[] = {&aa};
+    return cudaLaunchKernel(search_kernel_ptr(a.cls), dim3(blocks), dim3(threads), args, smem, s);
+}
+
+cudaError_t launch_search_prep(const SearchArgs &a, cudaStream_t s)
+{
+    const int n = a.n_workers > 0 ? a.n_workers : 1;
+    search_prep_kernel<<<(n + 255) / 256, 256, 0, s>>>(a.ring_seq, n, a.g.ctrl);
     return cudaGetLastError();
 }
 

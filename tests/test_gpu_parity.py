@@ -266,3 +266,52 @@ def test_enumerate_buffer_too_small():
         r = O.count(g)
         assert sizes[0] == r.count
         assert sizes[1] == sum(k * int(c) for k, c in enumerate(r.hist))
+
+
+# ---------------------------------------------------------------- worker list and bounded waits
+
+@pytest.mark.parametrize("name", ["rmat_s12", "planted50k", "sbm_c20"])
+def test_worker_list_on_off_and_forced_donations(name):
+    g = G.config_graph(name, 2)
+    expect = O.count(g, threads=8).key()
+    for cfg in [dict(worker_list=0), dict(worker_list=1),
+                dict(worker_list=1, donate_min_p=1, blocks_per_sm=1)]:
+        with gpu_graph(g, **cfg) as h:
+            assert h.count_result() == expect, cfg
+            info = h.get_info()
+            if not cfg["worker_list"]:
+                assert info["donations"] == 0
+    # rmat: heavy subtrees must actually be split when donation is forced
+    if name == "rmat_s12":
+        with gpu_graph(g, donate_min_p=1, blocks_per_sm=1) as h:
+            h.count_result()
+            assert h.get_info()["donations"] > 0
+
+
+def test_rmat_s13_with_worker_list():
+    g = G.config_graph("rmat_s13", 1)
+    expect = O.count(g, threads=16).key()
+    with gpu_graph(g) as h:
+        assert h.count_result() == expect
+        assert h.get_info()["donations"] > 0
+
+
+def test_enumerate_with_forced_donations():
+    mce = _mce()
+    g = G.config_graph("rmat_s10", 3)
+    with gpu_graph(g, donate_min_p=1, blocks_per_sm=1) as h:
+        ids, offs = h.enumerate()
+        got = mce.cliques_from(ids, offs)
+    assert sorted(got) == sorted(O.enumerate_cliques(g))
+
+
+def test_device_wait_limit_returns_an_error_not_a_hang():
+    # a 1 ns limit makes the grid barrier of the peel give up at once: the kernel records
+    # MCE_ERR_DEVICE_TIMEOUT and returns; the context stays usable afterwards
+    mce = _mce()
+    g = G.config_graph("ba100k", 1)
+    with pytest.raises(mce.MceError) as e:
+        gpu_graph(g, spin_limit_ns=1)
+    assert e.value.name == "MCE_ERR_DEVICE_TIMEOUT"
+    with gpu_graph(g) as h:
+        assert h.count_result() == O.count(g, threads=8).key()
