@@ -47,7 +47,8 @@ typedef enum mce_status {
     MCE_ERR_BUFFER_TOO_SMALL = 6,  /* an output buffer cannot hold the result                  */
     MCE_ERR_DEVICE_TIMEOUT = 7,    /* a device-side wait exceeded mce_config.spin_limit_ns     */
     MCE_ERR_LIMIT = 8,             /* the graph exceeds a documented size limit of this build  */
-    MCE_ERR_CUDA = 9               /* any other CUDA runtime error                             */
+    MCE_ERR_CUDA = 9,              /* any other CUDA runtime error                             */
+    MCE_ERR_INTERNAL = 10          /* a device-side consistency check failed (a library bug)   */
 } mce_status;
 
 /*
@@ -57,19 +58,27 @@ typedef enum mce_status {
  *   donate_min_p     a branch is donated only if |P| >= this at its root (Section 3.3 uses 10).
  *   warps_per_block  warps per CTA of the search kernel (0 = library default).
  *   blocks_per_sm    CTAs per SM of the search kernel (0 = as many as can be resident).
+ *   profile          1: record CUDA events around the ordering and around every search launch,
+ *                    so that mce_get_info reports per-stage device times; 0 (default): none.
  *   spin_limit_ns    upper bound on any single device-side wait (grid barrier, idle warp
  *                    waiting for a donation); on expiry the kernel records
- *                    MCE_ERR_DEVICE_TIMEOUT and returns instead of hanging.
+ *                    MCE_ERR_DEVICE_TIMEOUT and returns instead of hanging (an idle warp
+ *                    that waited this long instead leaves the worker list, which is not an
+ *                    error).
  */
 typedef struct mce_config {
     int32_t worker_list;
     int32_t donate_min_p;
     int32_t warps_per_block;
     int32_t blocks_per_sm;
+    int32_t profile;
+    int32_t reserved;
     int64_t spin_limit_ns;
 } mce_config;
 
-/* Sizes and diagnostics of a handle (filled by mce_info). */
+#define MCE_NUM_WIDTHS 6   /* search kernels, one per bitset row width 1, 2, 4, 8, 16, 32 words */
+
+/* Sizes and diagnostics of a handle (filled by mce_get_info). */
 typedef struct mce_info {
     int32_t n;                 /* vertices                                                   */
     int32_t degeneracy;        /* d: largest core number (Section 2.4)                        */
@@ -81,6 +90,14 @@ typedef struct mce_info {
     int64_t workspace_bytes;   /* device workspace held by the handle                         */
     uint64_t tree_nodes;       /* search-tree nodes visited by the last count/enumerate       */
     uint64_t donations;        /* branches donated through the worker list, last call         */
+    /* last call, per row-width class k (row width 1 << k words): */
+    uint64_t words[MCE_NUM_WIDTHS];    /* bitset words scored or intersected (pivot scans,
+                                          child sets, X_X tests): the search's integer work  */
+    int32_t roots[MCE_NUM_WIDTHS];     /* first-level roots of the full schedule per class   */
+    int32_t workers[MCE_NUM_WIDTHS];   /* warps launched per class (0: class not launched)   */
+    float ms_search[MCE_NUM_WIDTHS];   /* device time per class launch (profile = 1 only)    */
+    float ms_order;                    /* device time of the last mce_order/mce_create order */
+    int32_t launches;                  /* kernels launched by the last order + count calls   */
 } mce_info;
 
 /* Writes the default configuration into *cfg.  Returns MCE_ERR_INVALID_ARG if cfg is NULL. */
@@ -158,6 +175,17 @@ mce_status mce_enumerate(mce_graph *g, void *stream, int32_t *d_ids, int64_t cap
  *   d_rank[v] = position of v in the order, d_core[v] = core number of v; either may be NULL.
  */
 mce_status mce_get_order(mce_graph *g, void *stream, int32_t *d_rank, int32_t *d_core);
+
+/*
+ * Activity profile of the last search (diagnostics).  Only a library built with MCE_PROFILE
+ * defined collects it (the normal build leaves it zero): SM clock cycles summed over warps, per
+ * row-width class k, at out[k * 8 + a] for activity a = 0 subtree build, 1 pivot selection,
+ * 2 child sets and leaf checks, 3 X_X partition, 4 donation, 5 waiting in the worker list,
+ * 6 the slowest single first-level root, 7 number of roots.  Section 4.5 of the pages breaks
+ * execution time down the same way from per-block SM clocks.
+ *   out  host uint64[8 * MCE_NUM_WIDTHS].  Synchronises the device.
+ */
+mce_status mce_get_profile(mce_graph *g, uint64_t *out);
 
 /* Synchronises `stream`, then returns (and clears) the device-side status of the handle. */
 mce_status mce_last_error(mce_graph *g, void *stream);

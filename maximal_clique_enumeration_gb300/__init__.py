@@ -22,11 +22,13 @@ __all__ = ["Graph", "MceError", "Config", "Info", "library", "STATUS", "graphs"]
 STATUS = {
     0: "MCE_OK", 1: "MCE_ERR_INVALID_ARG", 2: "MCE_ERR_NOT_SIMPLE", 3: "MCE_ERR_NOT_SYMMETRIC",
     4: "MCE_ERR_ID_RANGE", 5: "MCE_ERR_OUT_OF_MEMORY", 6: "MCE_ERR_BUFFER_TOO_SMALL",
-    7: "MCE_ERR_DEVICE_TIMEOUT", 8: "MCE_ERR_LIMIT", 9: "MCE_ERR_CUDA",
+    7: "MCE_ERR_DEVICE_TIMEOUT", 8: "MCE_ERR_LIMIT", 9: "MCE_ERR_CUDA", 10: "MCE_ERR_INTERNAL",
 }
 EXPORTS = ["mce_config_default", "mce_create", "mce_order", "mce_count", "mce_count_roots",
-           "mce_enumerate", "mce_get_order", "mce_last_error", "mce_get_info", "mce_destroy",
-           "mce_status_str"]
+           "mce_enumerate", "mce_get_order", "mce_last_error", "mce_get_info", "mce_get_profile",
+           "mce_destroy", "mce_status_str"]
+PROFILE_ACTIVITIES = ["build", "pivot", "child", "partition", "donate", "idle", "max_root",
+                      "roots"]
 
 
 class MceError(RuntimeError):
@@ -36,9 +38,13 @@ class MceError(RuntimeError):
         super().__init__(f"{what}: {self.name}" if what else self.name)
 
 
+NUM_WIDTHS = 6
+
+
 class Config(ctypes.Structure):
     _fields_ = [("worker_list", ctypes.c_int32), ("donate_min_p", ctypes.c_int32),
                 ("warps_per_block", ctypes.c_int32), ("blocks_per_sm", ctypes.c_int32),
+                ("profile", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("spin_limit_ns", ctypes.c_int64)]
 
 
@@ -47,20 +53,32 @@ class Info(ctypes.Structure):
                 ("max_degree", ctypes.c_int32), ("hist_len", ctypes.c_int32),
                 ("peel_rounds", ctypes.c_int32), ("n_workers", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_int64), ("tree_nodes", ctypes.c_uint64),
-                ("donations", ctypes.c_uint64)]
+                ("donations", ctypes.c_uint64), ("words", ctypes.c_uint64 * NUM_WIDTHS),
+                ("roots", ctypes.c_int32 * NUM_WIDTHS), ("workers", ctypes.c_int32 * NUM_WIDTHS),
+                ("ms_search", ctypes.c_float * NUM_WIDTHS), ("ms_order", ctypes.c_float),
+                ("launches", ctypes.c_int32)]
 
     def as_dict(self):
-        return {k: getattr(self, k) for k, _ in self._fields_}
+        out = {}
+        for k, _ in self._fields_:
+            v = getattr(self, k)
+            out[k] = list(v) if isinstance(v, ctypes.Array) else v
+        return out
 
 
 _lib = None
 
 
-def library(path: str = LIB_PATH):
-    """Loads libmce_gb300.so (raises if it has not been built)."""
+def library(path: str | None = None):
+    """Loads libmce_gb300.so (raises if it has not been built).
+
+    MCE_LIBRARY in the environment selects another build of the same library (for example the
+    MCE_PROFILE variant from build.build(profile=True)).
+    """
     global _lib
     if _lib is not None:
         return _lib
+    path = path or os.environ.get("MCE_LIBRARY") or LIB_PATH
     if not os.path.exists(path):
         raise RuntimeError(f"{path} is missing: build it with __graft_entry__.build() "
                            "(nvcc, sm_103a); there is no CPU fallback")
@@ -86,6 +104,8 @@ def library(path: str = LIB_PATH):
     lib.mce_last_error.argtypes = [P, P]
     lib.mce_get_info.restype = st
     lib.mce_get_info.argtypes = [P, ctypes.POINTER(Info)]
+    lib.mce_get_profile.restype = st
+    lib.mce_get_profile.argtypes = [P, P]
     lib.mce_destroy.restype = None
     lib.mce_destroy.argtypes = [P]
     lib.mce_status_str.restype = ctypes.c_char_p
@@ -174,6 +194,14 @@ class Graph:
         info = Info()
         _check(library().mce_get_info(self._h, ctypes.byref(info)), "mce_get_info")
         return info.as_dict()
+
+    def profile(self) -> dict:
+        """Per row width: cycles per activity of the last search (MCE_PROFILE builds only)."""
+        out = np.zeros(8 * NUM_WIDTHS, np.uint64)
+        _check(library().mce_get_profile(self._h, out.ctypes.data_as(ctypes.c_void_p)),
+               "mce_get_profile")
+        return {1 << k: dict(zip(PROFILE_ACTIVITIES, (int(x) for x in out[8 * k: 8 * k + 8])))
+                for k in range(NUM_WIDTHS)}
 
     def order(self, stream=None):
         _check(library().mce_order(self._h, _stream_ptr(stream)), "mce_order")

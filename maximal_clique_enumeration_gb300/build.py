@@ -12,6 +12,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libmce_gb300.so")
+PROBE_PATH = os.path.join(BUILD_DIR, "libmce_probe.so")
 SOURCES = ["api.cu", "ingest.cu", "order.cu", "search.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
@@ -26,20 +27,35 @@ def _nvcc() -> str:
 
 
 def _stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+    if not os.path.exists(LIB_PATH) or not os.path.exists(PROBE_PATH):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = min(os.path.getmtime(LIB_PATH), os.path.getmtime(PROBE_PATH))
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "mce.h")]
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile every CUDA source (in parallel) and link the shared library; returns its path."""
+PROFILE_LIB_PATH = os.path.join(BUILD_DIR, "profile", "libmce_gb300.so")
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags=(), profile: bool = False) -> str:
+    """Compile every CUDA source (in parallel) and link the shared library; returns its path.
+
+    profile=True builds the MCE_PROFILE variant (activity cycle counters) into
+    _build/profile/ instead; the normal library is left alone.
+    """
+    if profile:
+        return _build_variant(os.path.dirname(PROFILE_LIB_PATH), ["-DMCE_PROFILE", *extra_flags],
+                              verbose)
     if not force and not extra_flags and not _stale():
         return LIB_PATH
     nvcc = _nvcc()
     os.makedirs(BUILD_DIR, exist_ok=True)
     procs, objs = [], []
+    probe_tmp = PROBE_PATH + f".tmp{os.getpid()}"
+    probe_cmd = [nvcc, *ARCH, *FLAGS, *extra_flags, "-shared", "-cudart", "static",
+                 os.path.join(CSRC, "probe.cu"), "-o", probe_tmp]
+    procs.append(("probe.cu", subprocess.Popen(probe_cmd, stdout=subprocess.PIPE,
+                                               stderr=subprocess.STDOUT)))
     for src in SOURCES:
         obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
         objs.append(obj)
@@ -62,7 +78,29 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + r.stdout + r.stderr)
     os.replace(tmp, LIB_PATH)
+    os.replace(probe_tmp, PROBE_PATH)
     return LIB_PATH
+
+
+def _build_variant(out_dir: str, flags, verbose: bool) -> str:
+    nvcc = _nvcc()
+    os.makedirs(out_dir, exist_ok=True)
+    procs, objs = [], []
+    for src in SOURCES:
+        obj = os.path.join(out_dir, src.replace(".cu", ".o"))
+        objs.append(obj)
+        cmd = [nvcc, *ARCH, *FLAGS, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
+        procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
+    errors = [f"--- {src}\n{p.communicate()[0].decode(errors='replace')}" for src, p in procs
+              if p.wait() != 0]
+    if errors:
+        raise RuntimeError("nvcc failed:\n" + "\n".join(errors))
+    out = os.path.join(out_dir, "libmce_gb300.so")
+    r = subprocess.run([nvcc, *ARCH, "-shared", "-cudart", "static", "-o", out, *objs],
+                       capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("link failed:\n" + r.stdout + r.stderr)
+    return out
 
 
 if __name__ == "__main__":

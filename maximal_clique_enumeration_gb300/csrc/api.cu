@@ -17,9 +17,9 @@ struct mce_graph {
     int peel_blocks = 0;
     int search_threads = 0, n_workers = 0;
     int cls_blocks[kNumClasses] = {}, cls_workers[kNumClasses] = {}, cls_count[kNumClasses] = {};
+    size_t cls_smem[kNumClasses] = {};
     unsigned long long cls_ws[kNumClasses] = {};
     long long uroots_cap = 0;
-    size_t search_smem = 0;
     int degeneracy = 0, max_degree = 0, hist_len = 2, rounds = 0;
     unsigned long long ws_words = 0;
     std::vector<void *> allocs;
@@ -32,6 +32,12 @@ struct mce_graph {
     unsigned long long *cursor = nullptr;
     unsigned long long *count_cache = nullptr;  // [2 + hist_len], full-graph count
     bool count_cache_valid = false;
+    // profiling: events around the order and around each class launch
+    cudaEvent_t ev_order[2] = {nullptr, nullptr};
+    cudaEvent_t ev_cls[kNumClasses][2] = {};
+    bool cls_timed[kNumClasses] = {};
+    bool order_timed = false;
+    int launches_order = 0, launches_count = 0;
 };
 
 namespace {
@@ -83,6 +89,11 @@ void free_all(mce_graph *h)
 {
     for (void *p : h->allocs) cudaFree(p);
     h->allocs.clear();
+    for (int i = 0; i < 2; ++i)
+        if (h->ev_order[i]) cudaEventDestroy(h->ev_order[i]);
+    for (int k = 0; k < kNumClasses; ++k)
+        for (int i = 0; i < 2; ++i)
+            if (h->ev_cls[k][i]) cudaEventDestroy(h->ev_cls[k][i]);
 }
 
 // Resets the per-search accumulators of the control block.
@@ -90,6 +101,9 @@ mce_status reset_search(mce_graph *h, cudaStream_t s)
 {
     DevCtrl *c = h->g.ctrl;
     MCE_TRY(cudaMemsetAsync(&c->tree_nodes, 0, 4 * sizeof(unsigned long long), s));
+    MCE_TRY(cudaMemsetAsync(c->words, 0, sizeof(c->words), s));
+    MCE_TRY(cudaMemsetAsync(c->prof, 0, sizeof(c->prof), s));
+    for (int k = 0; k < kNumClasses; ++k) h->cls_timed[k] = false;
     MCE_TRY(cudaMemsetAsync(h->hist_acc, 0, sizeof(unsigned long long) * h->hist_len, s));
     return MCE_OK;
 }
@@ -126,7 +140,13 @@ mce_status run_search(mce_graph *h, cudaStream_t s, bool user_roots, const DevOu
         a.n_workers = h->cls_workers[k];
         MCE_TRY(cudaMemsetAsync(h->flag, 0, sizeof(int) * (size_t)a.n_workers, s));
         MCE_TRY(launch_search_prep(a, s));
-        MCE_TRY(launch_search(a, h->cls_blocks[k], h->search_threads, h->search_smem, s));
+        if (h->cfg.profile) MCE_TRY(cudaEventRecord(h->ev_cls[k][0], s));
+        MCE_TRY(launch_search(a, h->cls_blocks[k], h->search_threads, h->cls_smem[k], s));
+        if (h->cfg.profile) {
+            MCE_TRY(cudaEventRecord(h->ev_cls[k][1], s));
+            h->cls_timed[k] = true;
+        }
+        h->launches_count += 2;
     }
     return MCE_OK;
 }
@@ -142,6 +162,8 @@ mce_status mce_config_default(mce_config *cfg)
     cfg->donate_min_p = 10;
     cfg->warps_per_block = kDefaultWarpsPerBlock;
     cfg->blocks_per_sm = 0;
+    cfg->profile = 0;
+    cfg->reserved = 0;
     cfg->spin_limit_ns = 20LL * 1000 * 1000 * 1000;
     return MCE_OK;
 }
@@ -159,9 +181,12 @@ const char *mce_status_str(mce_status s)
     case MCE_ERR_DEVICE_TIMEOUT: return "device-side wait exceeded the spin limit";
     case MCE_ERR_LIMIT: return "graph exceeds a size limit of this build";
     case MCE_ERR_CUDA: return "CUDA error";
+    case MCE_ERR_INTERNAL: return "internal consistency check failed on the device";
     }
     return "unknown status";
 }
+
+static mce_status order_impl(mce_graph *h, cudaStream_t s);
 
 static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_t *adj, int32_t n,
                               int is_device_ptr, cudaStream_t s)
@@ -235,14 +260,28 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
     MCE_ALLOC(h, g.deg, (size_t)n);
     MCE_ALLOC(h, g.alive_a, (size_t)n);
     MCE_ALLOC(h, g.alive_b, (size_t)n);
-    MCE_ALLOC(h, g.bucket, (size_t)kMaxP + 2);
+    MCE_ALLOC(h, g.bucket, (size_t)kNumBuckets);
+    MCE_ALLOC(h, g.poffs, (size_t)n + 1);
+    MCE_ALLOC(h, g.padj, (size_t)(h->nnz / 2 > 0 ? h->nnz / 2 : 1));
+    MCE_ALLOC(h, g.scan_tmp, (size_t)n / kScanBlock + 2);
     int coop = 0;
     MCE_TRY(cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, h->device));
     if (!coop) return MCE_ERR_CUDA;
     h->peel_blocks = h->sm_count;
     MCE_ALLOC(h, g.blk_cnt, (size_t)2 * h->peel_blocks);
     MCE_ALLOC(h, g.blk_min, (size_t)2 * h->peel_blocks);
-    MCE_TRY(launch_order(g, h->peel_blocks, h->cfg.spin_limit_ns, s));
+    if (h->cfg.profile) {
+        MCE_TRY(cudaEventCreate(&h->ev_order[0]));
+        MCE_TRY(cudaEventCreate(&h->ev_order[1]));
+        for (int k = 0; k < kNumClasses; ++k) {
+            MCE_TRY(cudaEventCreate(&h->ev_cls[k][0]));
+            MCE_TRY(cudaEventCreate(&h->ev_cls[k][1]));
+        }
+    }
+    {
+        mce_status so = order_impl(h, s);
+        if (so != MCE_OK) return so;
+    }
     st = read_status(h, s);
     if (st != MCE_OK) return st;
     DevCtrl c{};
@@ -258,15 +297,17 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
     int wpb = h->cfg.warps_per_block > 0 ? h->cfg.warps_per_block : kDefaultWarpsPerBlock;
     if (wpb > 4) wpb = 4;
     h->search_threads = 32 * wpb;
-    h->search_smem = sizeof(unsigned long long) * (size_t)(h->hist_len + 1);
     size_t ws_total = 4;
     for (int k = 0; k < kNumClasses; ++k) {
         h->cls_count[k] = c.cls[2 * k + 1] - c.cls[2 * k];
-        unsigned long long need = (c.ws_cls[k] + 3) & ~3ULL;
-        if (k == 0 && need < 4) need = 4;                 // isolated roots use 1 word
+        // whole 128-byte lines per warp: no two warps share an L1 line of workspace
+        unsigned long long need = (c.ws_cls[k] + 31) & ~31ULL;
+        if (k == 0 && need < 32) need = 32;               // isolated roots use 1 word
         if (need == 0) continue;                          // no vertex of this class
+        h->cls_smem[k] = search_smem_bytes(k, h->hist_len, wpb);
+        MCE_TRY(search_configure(k, h->cls_smem[k]));
         int per_sm = 0;
-        MCE_TRY(search_occupancy(k, h->search_threads, h->search_smem, &per_sm));
+        MCE_TRY(search_occupancy(k, h->search_threads, h->cls_smem[k], &per_sm));
         if (per_sm < 1) return MCE_ERR_CUDA;
         if (h->cfg.blocks_per_sm > 0 && h->cfg.blocks_per_sm < per_sm) per_sm = h->cfg.blocks_per_sm;
         h->cls_blocks[k] = per_sm * h->sm_count;
@@ -280,7 +321,7 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
     MCE_ALLOC(h, h->ring, (size_t)h->n_workers);
     MCE_ALLOC(h, h->flag, (size_t)h->n_workers);
     MCE_ALLOC(h, h->ring_seq, (size_t)h->n_workers);
-    MCE_ALLOC(h, g.ubucket, (size_t)kMaxP + 2);
+    MCE_ALLOC(h, g.ubucket, (size_t)kNumBuckets);
     MCE_ALLOC(h, h->hist_acc, (size_t)h->hist_len + 1);
     MCE_ALLOC(h, h->region_ids, (size_t)h->hist_len + 2);
     MCE_ALLOC(h, h->region_cl, (size_t)h->hist_len + 2);
@@ -314,12 +355,23 @@ mce_status mce_create(const int32_t *offsets, const int32_t *adj, int32_t n, int
     return MCE_OK;
 }
 
+static mce_status order_impl(mce_graph *h, cudaStream_t s)
+{
+    h->count_cache_valid = false;
+    if (h->cfg.profile) MCE_TRY(cudaEventRecord(h->ev_order[0], s));
+    MCE_TRY(launch_order(h->g, h->peel_blocks, h->cfg.spin_limit_ns, s));
+    if (h->cfg.profile) {
+        MCE_TRY(cudaEventRecord(h->ev_order[1], s));
+        h->order_timed = true;
+    }
+    h->launches_order = h->n > 0 ? 4 : 0;                   // peel + 3 orient kernels
+    return MCE_OK;
+}
+
 mce_status mce_order(mce_graph *h, void *stream)
 {
     if (!h) return MCE_ERR_INVALID_ARG;
-    h->count_cache_valid = false;
-    MCE_TRY(launch_order(h->g, h->peel_blocks, h->cfg.spin_limit_ns, (cudaStream_t)stream));
-    return MCE_OK;
+    return order_impl(h, (cudaStream_t)stream);
 }
 
 static mce_status count_impl(mce_graph *h, cudaStream_t s, const int32_t *d_roots,
@@ -329,7 +381,9 @@ static mce_status count_impl(mce_graph *h, cudaStream_t s, const int32_t *d_root
         MCE_TRY(cudaMemsetAsync(d_out, 0, sizeof(uint64_t) * (2 + (size_t)h->hist_len), s));
         return MCE_OK;
     }
+    h->launches_count = 1;                                  // finalize
     if (d_roots) {
+        h->launches_count += 3;                             // root binning
         if (n_roots > h->uroots_cap) {
             int *buf = nullptr;
             MCE_ALLOC(h, buf, (size_t)n_roots);
@@ -437,6 +491,7 @@ mce_status mce_get_info(mce_graph *h, mce_info *info)
     MCE_TRY(cudaDeviceSynchronize());
     DevCtrl c{};
     MCE_TRY(cudaMemcpy(&c, h->g.ctrl, sizeof(DevCtrl), cudaMemcpyDeviceToHost));
+    memset(info, 0, sizeof(*info));
     info->n = h->n;
     info->degeneracy = h->degeneracy;
     info->m = h->nnz / 2;
@@ -447,6 +502,24 @@ mce_status mce_get_info(mce_graph *h, mce_info *info)
     info->workspace_bytes = (long long)(h->ws_words * 4ULL);
     info->tree_nodes = c.tree_nodes;
     info->donations = c.donations;
+    for (int k = 0; k < kNumClasses; ++k) {
+        info->words[k] = c.words[k];
+        info->roots[k] = h->cls_count[k];
+        info->workers[k] = h->cls_workers[k];
+        if (h->cls_timed[k]) MCE_TRY(cudaEventElapsedTime(&info->ms_search[k], h->ev_cls[k][0],
+                                                          h->ev_cls[k][1]));
+    }
+    if (h->order_timed)
+        MCE_TRY(cudaEventElapsedTime(&info->ms_order, h->ev_order[0], h->ev_order[1]));
+    info->launches = h->launches_order + h->launches_count;
+    return MCE_OK;
+}
+
+mce_status mce_get_profile(mce_graph *h, uint64_t *out)
+{
+    if (!h || !out) return MCE_ERR_INVALID_ARG;
+    MCE_TRY(cudaDeviceSynchronize());
+    MCE_TRY(cudaMemcpy(out, h->g.ctrl->prof, sizeof(h->g.ctrl->prof), cudaMemcpyDeviceToHost));
     return MCE_OK;
 }
 

@@ -15,6 +15,7 @@ constexpr int kPeelThreads = 512;
 constexpr int kPeelSoloVertices = 8192;  // the peel finishes in one CTA below this many vertices
 constexpr int kDefaultWarpsPerBlock = 4;
 constexpr int kNumClasses = 6;           // row widths W = 1, 2, 4, 8, 16, 32 words
+constexpr int kScanBlock = 1024;         // elements per CTA of the exclusive scan
 
 // Device-resident control block of a handle.
 struct DevCtrl {
@@ -37,6 +38,8 @@ struct DevCtrl {
     unsigned long long tree_nodes;
     unsigned long long donations;
     unsigned long long result[2];  // count, hash of the last search
+    unsigned long long words[kNumClasses];  // bitset words processed per row-width class
+    unsigned long long prof[kNumClasses][8];  // MCE_PROFILE builds: cycles per activity
     // first-level roots grouped by row width (class k: W = 1 << k), heaviest class first:
     // sched[cls[2k] .. cls[2k+1]) for the full schedule, uroots[ucls[2k] .. ucls[2k+1])
     // for a caller's root list
@@ -55,12 +58,15 @@ struct DevGraph {
     int *round_of;    // id -> peel round
     int *order;       // position -> id
     int *pcount;      // id -> |P| (later neighbours)
+    int *poffs;       // [n+1] CSR offsets of the later-neighbour lists N+(v)
+    int *padj;        // [m] N+(v) in id order (Section 2.4: P of the first-level subtree)
+    int *scan_tmp;    // exclusive-scan partials
     int *sched;       // first-level roots with |P| > 0, heavy first
     int *deg;         // peel scratch
     int *alive_a, *alive_b;
     int *blk_cnt, *blk_min;   // peel per-CTA partials [2][grid]
-    int *bucket;      // orient: |P| histogram / cursors [kMaxP + 2]
-    int *ubucket;     // the same for a caller's root list [kMaxP + 2]
+    int *bucket;      // orient: schedule bucket histogram / cursors [kNumBuckets]
+    int *ubucket;     // the same for a caller's root list [kNumBuckets]
     int *uroots;      // a caller's roots, grouped by row width, heaviest first
     DevCtrl *ctrl;
 };
@@ -107,13 +113,36 @@ __host__ __device__ inline int wclass_index(int np)
     return np <= 32 ? 0 : np <= 64 ? 1 : np <= 128 ? 2 : np <= 256 ? 3 : np <= 512 ? 4 : 5;
 }
 
+// Schedule buckets: row-width classes widest first and, inside a class, roots with a larger
+// estimated cost deg(v) * (|P| + 1) first (log2 buckets).  Bucket 0 holds over-limit roots.
+constexpr int kCostBuckets = 48;
+constexpr int kNumBuckets = 1 + kNumClasses * kCostBuckets;
+
+__host__ __device__ inline int class_first_bucket(int k)
+{
+    return k == kNumClasses - 1 ? 0 : 1 + (kNumClasses - 1 - k) * kCostBuckets;
+}
+__host__ __device__ inline int class_end_bucket(int k)
+{
+    return 1 + (kNumClasses - k) * kCostBuckets;
+}
+
+__device__ inline int sched_bucket(int np, int deg)
+{
+    if (np > kMaxP) return 0;
+    const unsigned long long est = (unsigned long long)deg * (unsigned long long)(np + 1);
+    int lb = est ? 63 - __clzll((long long)est) : 0;
+    lb = lb < kCostBuckets - 1 ? lb : kCostBuckets - 1;
+    return 1 + (kNumClasses - 1 - wclass_index(np)) * kCostBuckets + (kCostBuckets - 1 - lb);
+}
+
 // Per-warp workspace layout (32-bit word offsets) for a root of degree `deg` with np later
 // neighbours.  The same layout serves a branch of such a root donated through the worker list:
 // the donor writes the branch into the receiver's workspace at these offsets.
 constexpr int kWsHeader = 80;   // inbox: 16 scalar words, then P and X_P bitsets (32 words each)
 
 struct WsLayout {
-    long long rowsP, rowsX, pids, pkey, rids, loc, xx, spill, plist, stack, total;
+    long long rowsP, rowsX, pids, pkey, rids, xids, xx, spill, plist, stack, total;
     int W, LV;
 };
 
@@ -129,7 +158,7 @@ __host__ __device__ inline WsLayout ws_layout(int deg, int np)
     o = (o + 1) & ~1LL;
     l.pkey = o; o += 2LL * np;                   // vertex keys of P vertices (uint64)
     l.rids = o; o += np + 1;                     // ids of R at level 0 (root, or donated R)
-    l.loc = o; o += deg;                         // position in N(v) -> local row code
+    l.xids = o; o += nx;                         // original ids of X vertices (ascending)
     l.xx = o; o += nx;                           // compact X_X list (Section 3.5)
     l.spill = o; o += nx;                        // partition scratch
     l.plist = o; o += np;                        // pivot candidates from P u X_P
@@ -154,6 +183,15 @@ cudaError_t launch_search(const SearchArgs &a, int blocks, int threads, size_t s
                           cudaStream_t s);
 cudaError_t launch_search_prep(const SearchArgs &a, cudaStream_t s);
 cudaError_t search_occupancy(int cls, int threads, size_t smem, int *blocks_per_sm);
+// Shared memory of the search kernel of class k: the size histogram, then per warp a hash of
+// P(v) (ids and local indices) and a staging row.
+__host__ __device__ inline int hash_slots(int k) { return 64 << k; }
+__host__ __device__ inline size_t search_smem_bytes(int k, int hist_len, int warps)
+{
+    const size_t hist = ((size_t)(hist_len + 1) * 8 + 15) & ~(size_t)15;
+    return hist + (size_t)warps * ((size_t)hash_slots(k) * 8 + 32 * 4);
+}
+cudaError_t search_configure(int cls, size_t smem);
 cudaError_t launch_bin_roots(const DevGraph &g, const int *roots, int n_roots, cudaStream_t s);
 cudaError_t launch_finalize(const DevGraph &g, const DevOut &o, unsigned long long *d_out,
                             int include_isolated, cudaStream_t s);

@@ -14,9 +14,9 @@
 // at most kPeelSoloVertices vertices remain, CTA 0 finishes alone with CTA barriers.  Every
 // barrier wait is bounded by spin_limit_ns.
 //
-// Then three small kernels split every adjacency into earlier (X) and later (P) neighbours
-// (only |P| is stored: the search reclassifies neighbours by rank on the fly), count the
-// isolated vertices, and bucket the first-level roots by |P|, heaviest first.
+// Then small kernels count every vertex's later neighbours |P| (Algorithm 3's P), count the
+// isolated vertices, bucket the first-level roots by |P|, heaviest first, and store the
+// later-neighbour lists N+(v) as a CSR (scan of |P|, then a stable split of each adjacency).
 #include <climits>
 
 #include "mce_internal.cuh"
@@ -218,8 +218,8 @@ constexpr int kOrientThreads = 256;
 // per-warp workspace bound; Delta.
 __global__ void __launch_bounds__(kOrientThreads) orient_count_kernel(DevGraph g)
 {
-    __shared__ int s_bucket[kMaxP + 2];
-    for (int i = threadIdx.x; i < kMaxP + 2; i += blockDim.x) s_bucket[i] = 0;
+    __shared__ int s_bucket[kNumBuckets];
+    for (int i = threadIdx.x; i < kNumBuckets; i += blockDim.x) s_bucket[i] = 0;
     __syncthreads();
     const int lane = threadIdx.x & 31;
     const int warps = gridDim.x * (blockDim.x >> 5);
@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(kOrientThreads) orient_count_kernel(DevGraph g
                 iso_hash += mix64(vertex_key(v));
             }
             if (c > 0) {
-                atomicAdd(&s_bucket[min(c, kMaxP + 1)], 1);
+                atomicAdd(&s_bucket[sched_bucket(c, deg)], 1);
                 maxp = max(maxp, c);
                 if (c <= kMaxP) {
                     const unsigned long long need = (unsigned long long)ws_layout(deg, c).total;
@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(kOrientThreads) orient_count_kernel(DevGraph g
         }
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < kMaxP + 2; i += blockDim.x)
+    for (int i = threadIdx.x; i < kNumBuckets; i += blockDim.x)
         if (s_bucket[i]) atomicAdd(&g.bucket[i], s_bucket[i]);
     if (lane == 0) {
         if (n_iso) {
@@ -268,20 +268,16 @@ __global__ void __launch_bounds__(kOrientThreads) orient_count_kernel(DevGraph g
     }
 }
 
-// Highest |P| of row-width class k (class 5 also takes the over-limit bucket).
-__device__ __forceinline__ int class_hi(int k) { return k == 5 ? kMaxP + 1 : 32 << k; }
-__device__ __forceinline__ int class_lo(int k, int lowest) { return k == 0 ? lowest : (16 << k) + 1; }
-
-// Turns a |P| histogram into bucket cursors, heaviest first, and records where each row-width
-// class starts and ends (buckets lowest .. kMaxP + 1).
-__device__ void buckets_to_cursors(int *bucket, int *cls, int lowest, unsigned long long *total)
+// Turns a schedule-bucket histogram into bucket cursors and records where each row-width
+// class starts and ends in the resulting order.
+__device__ void buckets_to_cursors(int *bucket, int *cls, unsigned long long *total)
 {
     int run = 0;
     for (int k = kNumClasses - 1; k >= 0; --k) {
         cls[2 * k] = run;
-        for (int c = class_hi(k); c >= class_lo(k, lowest); --c) {
-            const int cnt = bucket[c];
-            bucket[c] = run;
+        for (int b = class_first_bucket(k); b < class_end_bucket(k); ++b) {
+            const int cnt = bucket[b];
+            bucket[b] = run;
             run += cnt;
         }
         cls[2 * k + 1] = run;
@@ -292,14 +288,111 @@ __device__ void buckets_to_cursors(int *bucket, int *cls, int lowest, unsigned l
 __global__ void orient_scan_kernel(DevGraph g)
 {
     if (threadIdx.x != 0 || blockIdx.x != 0) return;
-    buckets_to_cursors(g.bucket, g.ctrl->cls, 1, &g.ctrl->n_sched);
+    buckets_to_cursors(g.bucket, g.ctrl->cls, &g.ctrl->n_sched);
 }
 
 __global__ void __launch_bounds__(kOrientThreads) orient_scatter_kernel(DevGraph g)
 {
     for (int v = blockIdx.x * blockDim.x + threadIdx.x; v < g.n; v += gridDim.x * blockDim.x) {
         const int c = g.pcount[v];
-        if (c > 0) g.sched[atomicAdd(&g.bucket[min(c, kMaxP + 1)], 1)] = v;
+        if (c > 0) g.sched[atomicAdd(&g.bucket[sched_bucket(c, g.offs[v + 1] - g.offs[v])], 1)] = v;
+    }
+}
+
+// ---- exclusive scan of an int array (three passes: CTA sums, scan of the sums, final)
+
+__device__ __forceinline__ int warp_incl_scan(int v, int lane)
+{
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += t;
+    }
+    return v;
+}
+
+// Exclusive scan of one value per thread over the CTA; *total = CTA sum.
+__device__ __forceinline__ int block_excl_scan_int(int v, int *total, int *sh)
+{
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int inc = warp_incl_scan(v, lane);
+    if (lane == 31) sh[w] = inc;
+    __syncthreads();
+    int before = 0, t = 0;
+    for (int i = 0; i < nw; ++i) {
+        const int c = sh[i];
+        if (i < w) before += c;
+        t += c;
+    }
+    __syncthreads();
+    *total = t;
+    return before + inc - v;
+}
+
+constexpr int kScanThreads = 256;   // 4 elements per thread
+
+__global__ void __launch_bounds__(kScanThreads) scan_partial_kernel(const int *in, int n, int *sums)
+{
+    __shared__ int sh[32];
+    const int base = blockIdx.x * kScanBlock + threadIdx.x * 4;
+    int v = 0;
+    for (int i = 0; i < 4; ++i) v += base + i < n ? in[base + i] : 0;
+    int tot;
+    block_excl_scan_int(v, &tot, sh);
+    if (threadIdx.x == 0) sums[blockIdx.x] = tot;
+}
+
+__global__ void __launch_bounds__(1024) scan_sums_kernel(int *sums, int nb)
+{
+    __shared__ int sh[32];
+    int carry = 0;
+    for (int c0 = 0; c0 < nb; c0 += blockDim.x) {
+        const int i = c0 + threadIdx.x;
+        const int v = i < nb ? sums[i] : 0;
+        int tot;
+        const int ex = block_excl_scan_int(v, &tot, sh);
+        if (i < nb) sums[i] = carry + ex;
+        carry += tot;
+    }
+}
+
+__global__ void __launch_bounds__(kScanThreads) scan_final_kernel(const int *in, int n,
+                                                                  const int *sums, int *out)
+{
+    __shared__ int sh[32];
+    const int base = blockIdx.x * kScanBlock + threadIdx.x * 4;
+    int x[4], v = 0;
+    for (int i = 0; i < 4; ++i) {
+        x[i] = base + i < n ? in[base + i] : 0;
+        v += x[i];
+    }
+    int tot;
+    int run = sums[blockIdx.x] + block_excl_scan_int(v, &tot, sh);
+    for (int i = 0; i < 4; ++i) {
+        if (base + i < n) out[base + i] = run;
+        run += x[i];
+        if (base + i == n - 1) out[n] = run;
+    }
+}
+
+// N+(v): the neighbours of v later in the order, kept in id order (stable ballot compaction).
+__global__ void __launch_bounds__(kOrientThreads) orient_split_kernel(DevGraph g)
+{
+    const int lane = threadIdx.x & 31;
+    const int warps = gridDim.x * (blockDim.x >> 5);
+    const unsigned lt = (1u << lane) - 1u;
+    for (int v = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; v < g.n; v += warps) {
+        const int lo = g.offs[v], hi = g.offs[v + 1];
+        const int rv = g.rank[v];
+        int out = g.poffs[v];
+        for (int j0 = lo; j0 < hi; j0 += 32) {
+            const int j = j0 + lane;
+            const int w = j < hi ? g.adj[j] : 0;
+            const bool later = j < hi && g.rank[w] > rv;
+            const unsigned m = __ballot_sync(0xffffffffu, later);
+            if (later) g.padj[out + __popc(m & lt)] = w;
+            out += __popc(m);
+        }
     }
 }
 
@@ -313,14 +406,14 @@ __global__ void __launch_bounds__(kOrientThreads) bin_count_kernel(DevGraph g, c
             set_status(g.ctrl, MCE_ERR_ID_RANGE);
             continue;
         }
-        atomicAdd(&g.ubucket[min(g.pcount[v], kMaxP + 1)], 1);
+        atomicAdd(&g.ubucket[sched_bucket(g.pcount[v], g.offs[v + 1] - g.offs[v])], 1);
     }
 }
 
 __global__ void bin_scan_kernel(DevGraph g)
 {
     if (threadIdx.x != 0 || blockIdx.x != 0) return;
-    buckets_to_cursors(g.ubucket, g.ctrl->ucls, 0, nullptr);
+    buckets_to_cursors(g.ubucket, g.ctrl->ucls, nullptr);
 }
 
 __global__ void __launch_bounds__(kOrientThreads) bin_scatter_kernel(DevGraph g, const int *roots,
@@ -329,7 +422,7 @@ __global__ void __launch_bounds__(kOrientThreads) bin_scatter_kernel(DevGraph g,
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_roots; i += gridDim.x * blockDim.x) {
         const int v = roots[i];
         if (v < 0 || v >= g.n) continue;
-        g.uroots[atomicAdd(&g.ubucket[min(g.pcount[v], kMaxP + 1)], 1)] = v;
+        g.uroots[atomicAdd(&g.ubucket[sched_bucket(g.pcount[v], g.offs[v + 1] - g.offs[v])], 1)] = v;
     }
 }
 
@@ -337,7 +430,7 @@ __global__ void __launch_bounds__(kOrientThreads) bin_scatter_kernel(DevGraph g,
 
 cudaError_t launch_bin_roots(const DevGraph &g, const int *roots, int n_roots, cudaStream_t s)
 {
-    cudaError_t e = cudaMemsetAsync(g.ubucket, 0, sizeof(int) * (kMaxP + 2), s);
+    cudaError_t e = cudaMemsetAsync(g.ubucket, 0, sizeof(int) * kNumBuckets, s);
     if (e != cudaSuccess) return e;
     int b = (n_roots + kOrientThreads - 1) / kOrientThreads;
     if (b < 1) b = 1;
@@ -359,7 +452,7 @@ cudaError_t launch_order(const DevGraph &g, int peel_blocks, long long spin_limi
         e = cudaMemsetAsync(&g.ctrl->ws_words, 0, sizeof(unsigned long long) * (1 + kNumClasses), s);
     if (e == cudaSuccess) e = cudaMemsetAsync(&g.ctrl->n_iso, 0, 2 * sizeof(int), s);
     if (e == cudaSuccess) e = cudaMemsetAsync(&g.ctrl->iso_hash, 0, sizeof(unsigned long long), s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(g.bucket, 0, sizeof(int) * (kMaxP + 2), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(g.bucket, 0, sizeof(int) * kNumBuckets, s);
     if (e != cudaSuccess) return e;
     DevGraph gg = g;
     long long lim = spin_limit_ns;
@@ -374,6 +467,12 @@ cudaError_t launch_order(const DevGraph &g, int peel_blocks, long long spin_limi
     int sb = (g.n + kOrientThreads - 1) / kOrientThreads;
     if (sb > 8192) sb = 8192;
     orient_scatter_kernel<<<sb, kOrientThreads, 0, s>>>(g);
+    // CSR of the later-neighbour lists
+    const int nb = (g.n + kScanBlock - 1) / kScanBlock;
+    scan_partial_kernel<<<nb, kScanThreads, 0, s>>>(g.pcount, g.n, g.scan_tmp);
+    scan_sums_kernel<<<1, 1024, 0, s>>>(g.scan_tmp, nb);
+    scan_final_kernel<<<nb, kScanThreads, 0, s>>>(g.pcount, g.n, g.scan_tmp, g.poffs);
+    orient_split_kernel<<<blocks, kOrientThreads, 0, s>>>(g);
     return cudaGetLastError();
 }
 

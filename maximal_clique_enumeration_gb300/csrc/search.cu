@@ -189,26 +189,30 @@ __device__ __forceinline__ int lowest_above(const Ck<Geo<W>::CH> &c, int after, 
     return subwarp_min<Geo<W>::G>(best);
 }
 
-__device__ __forceinline__ int lower_bound_dev(const int *a, int len, int key)
-{
-    int lo = 0, hi = len;
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (__ldg(a + mid) < key) lo = mid + 1;
-        else hi = mid;
-    }
-    return lo;
-}
-
 struct Acc {
     unsigned long long count, hash, nodes, donations;
+    unsigned long long words;   // bitset words scored / intersected / tested (lane 0 counts)
+#ifdef MCE_PROFILE
+    unsigned long long prof[8];
+#endif
 };
+
+// Activity timers of the MCE_PROFILE build (no code otherwise).
+#ifdef MCE_PROFILE
+#define PROF_START(var) const long long var = clock64()
+#define PROF_ADD(acc, slot, var) ((acc).prof[slot] += (unsigned long long)(clock64() - (var)))
+#else
+#define PROF_START(var) (void)0
+#define PROF_ADD(acc, slot, var) (void)0
+#endif
+enum { kProfBuild = 0, kProfPivot, kProfChild, kProfPartition, kProfDonate, kProfIdle,
+       kProfMaxRoot, kProfRoots };
 
 struct RootCtx {
     unsigned *rowsP, *rowsX;
     int *pids;
     unsigned long long *pkey;
-    int *rids, *loc, *xx, *spill, *plist;
+    int *rids, *xids, *xx, *spill, *plist;
     unsigned *stack;
     int deg, np, nx, LV;
     int rsize;          // |R| at level 0 (1 for a first-level root)
@@ -232,7 +236,7 @@ __device__ __forceinline__ RootCtx make_ctx(unsigned *ws, int deg, int np)
     r.pids = reinterpret_cast<int *>(ws + lay.pids);
     r.pkey = reinterpret_cast<unsigned long long *>(ws + lay.pkey);
     r.rids = reinterpret_cast<int *>(ws + lay.rids);
-    r.loc = reinterpret_cast<int *>(ws + lay.loc);
+    r.xids = reinterpret_cast<int *>(ws + lay.xids);
     r.xx = reinterpret_cast<int *>(ws + lay.xx);
     r.spill = reinterpret_cast<int *>(ws + lay.spill);
     r.plist = reinterpret_cast<int *>(ws + lay.plist);
@@ -258,6 +262,10 @@ __device__ __forceinline__ int clique_elem(const RootCtx &r, int L, int c, int e
 __device__ void report(const SearchArgs &a, const RootCtx &r, int L, int c, int size,
                        unsigned long long hsum, Acc &acc, unsigned long long *s_hist, int lane)
 {
+    if (size >= a.out.hist_len) {                   // cannot happen: size <= d + 1
+        if (lane == 0) set_status(a.g.ctrl, MCE_ERR_INTERNAL);
+        return;
+    }
     if (a.out.ids == nullptr) {
         if (lane == 0) {
             acc.count++;
@@ -290,7 +298,7 @@ __device__ void report(const SearchArgs &a, const RootCtx &r, int L, int c, int 
 // adjacent to all of P (no maximal clique below this node: every branch would be cut).
 template <int W>
 __device__ int choose_pivot(const RootCtx &r, const Ck<Geo<W>::CH> &P, const Ck<Geo<W>::CH> &PX,
-                            int npop, int lpX, int lane)
+                            int npop, int lpX, Acc &acc, int lane)
 {
     constexpr int CH = Geo<W>::CH, G = Geo<W>::G, R = Geo<W>::R;
     const int q = lane % G, sub = lane / G;
@@ -328,6 +336,7 @@ __device__ int choose_pivot(const RootCtx &r, const Ck<Geo<W>::CH> &P, const Ck<
             const unsigned key = ((unsigned)cnt << kMaxIdxBits) | (unsigned)(kMaxCode - code);
             best = key > best ? key : best;
         }
+        if (lane == 0) acc.words += (unsigned long long)W * (unsigned)min(R, total - base);
         if (__any_sync(kFull, valid && cnt == npop)) return -1;
     }
     best = __reduce_max_sync(kFull, best);
@@ -336,7 +345,7 @@ __device__ int choose_pivot(const RootCtx &r, const Ck<Geo<W>::CH> &P, const Ck<
 
 // Does some live X_X row have bit c?  (X_X n N(c) non-empty)
 template <int W>
-__device__ __forceinline__ bool xx_hits(const RootCtx &r, int lpX, int c, int lane)
+__device__ __forceinline__ bool xx_hits(const RootCtx &r, int lpX, int c, Acc &acc, int lane)
 {
     const int wc = c >> 5;
     const unsigned bit = 1u << (c & 31);
@@ -344,6 +353,7 @@ __device__ __forceinline__ bool xx_hits(const RootCtx &r, int lpX, int c, int la
         const int i = base + lane;
         bool hit = false;
         if (i < lpX) hit = (r.rowsX[(long long)r.xx[i] * W + wc] & bit) != 0u;
+        if (lane == 0) acc.words += (unsigned)min(32, lpX - base);
         if (__any_sync(kFull, hit)) return true;
     }
     return false;
@@ -473,7 +483,8 @@ __device__ void write_branch(const RootCtx &r, unsigned *dst, int L, int c,
     }
     int *dr = reinterpret_cast<int *>(dst + lay.rids);
     for (int e = lane; e < rsize; e += 32) dr[e] = clique_elem(r, L, c, e);
-    __syncwarp();
+    __threadfence();          // every lane's part of the branch is visible GPU-wide ...
+    __syncwarp();             // ... before lane 0 publishes it
 }
 
 // Depth-first search of one first-level subtree (or donated branch) from the node
@@ -490,13 +501,15 @@ __device__ void dfs(const SearchArgs &a, const RootCtx &r, Ck<Geo<W>::CH> P, Ck<
     bool more_below = false;   // some level below L still has branches to explore
     Ck<CH> P0, XP0, C;
     int cursor = -1;
-    long long last_check = clock64();
+    long long last_check = __shfl_sync(kFull, (long long)clock64(), 0);
     while (true) {
         if (enter) {
             enter = false;
             acc.nodes++;
+            PROF_START(t_piv);
             const int npop = subwarp_sum<G>(ck_popc<CH>(P));
-            const int piv = choose_pivot<W>(r, P, ck_or<CH>(P, XP), npop, lpX, lane);
+            const int piv = choose_pivot<W>(r, P, ck_or<CH>(P, XP), npop, lpX, acc, lane);
+            PROF_ADD(acc, kProfPivot, t_piv);
             if (piv < 0) {
                 C = ck_zero<CH>();
             } else {
@@ -536,26 +549,35 @@ __device__ void dfs(const SearchArgs &a, const RootCtx &r, Ck<Geo<W>::CH> P, Ck<
             continue;
         }
         cursor = c;
+        PROF_START(t_child);
         // branch on c: P at this point is P0 minus earlier candidates, X_P gained them
         const Ck<CH> pre = bits_below<W>(C, c, q);
         const Ck<CH> rc = ck_load<CH>(r.rowsP + (long long)c * W + q * CH);
         const Ck<CH> Pc = ck_and<CH>(ck_andnot<CH>(P0, pre), rc);
         const Ck<CH> XPc = ck_and<CH>(ck_or<CH>(XP0, pre), rc);
         const unsigned long long Sc = S + r.pkey[c];
+        if (lane == 0) acc.words += 2 * W;
         if (!__any_sync(kFull, ck_nonzero<CH>(Pc))) {
             // leaf: R u {c} is maximal iff X n N(c) is empty (Algorithm 2, lines 2-3)
-            if (!__any_sync(kFull, ck_nonzero<CH>(XPc)) && !xx_hits<W>(r, lpX, c, lane)) {
+            if (!__any_sync(kFull, ck_nonzero<CH>(XPc)) && !xx_hits<W>(r, lpX, c, acc, lane)) {
                 report(a, r, L, c, r.rsize + L + 1, Sc, acc, s_hist, lane);
                 acc.nodes++;
             }
+            PROF_ADD(acc, kProfChild, t_child);
             continue;
         }
         const bool more_same = lowest_above<W>(C, c, q) != INT_MAX;
         if (lane == 0) r.stack[(long long)L * r.LV + 3] = (unsigned)c;
+        PROF_ADD(acc, kProfChild, t_child);
+        PROF_START(t_part);
         const int lpXc = xx_partition<W>(r, lpX, c, lane);
-        // worker list: hand this branch to an idle warp instead of descending (Section 3.3)
-        if (a.worker_list && more_same && more_below) {
-            const long long now = clock64();
+        PROF_ADD(acc, kProfPartition, t_part);
+        if (lane == 0) acc.words += (unsigned)lpX;
+        // worker list: hand this branch to an idle warp instead of descending (Section 3.3).
+        // The pages ask for unexplored branches both at this level and at an earlier one; a
+        // warp-sized worker has far less to lose by giving work away, so either suffices here.
+        if (a.worker_list && (more_same || more_below)) {
+            const long long now = __shfl_sync(kFull, (long long)clock64(), 0);
             if (now - last_check > kDonateCheckCycles &&
                 subwarp_sum<G>(ck_popc<CH>(Pc)) >= a.donate_min_p) {
                 last_check = now;
@@ -572,6 +594,7 @@ __device__ void dfs(const SearchArgs &a, const RootCtx &r, Ck<Geo<W>::CH> P, Ck<
                     }
                 }
                 recv = __shfl_sync(kFull, recv, 0);
+                PROF_START(t_don);
                 if (recv >= 0) {
                     unsigned *dst = a.ws + (unsigned long long)recv * a.ws_words;
                     write_branch<W>(r, dst, L, c, Pc, XPc, lpXc, Sc, lane);
@@ -580,12 +603,17 @@ __device__ void dfs(const SearchArgs &a, const RootCtx &r, Ck<Geo<W>::CH> P, Ck<
                         dev_int(a.flag[recv]).store(kInboxFull, cuda::memory_order_release);
                         acc.donations++;
                     }
+                    PROF_ADD(acc, kProfDonate, t_don);
                     continue;
                 }
             }
         }
         more_below = more_below || more_same;
         lpX = lpXc;
+        if (L + 1 > r.np) {                       // cannot happen: |P| shrinks at every level
+            if (lane == 0) set_status(a.g.ctrl, MCE_ERR_INTERNAL);
+            return;
+        }
         ++L;
         P = Pc;
         XP = XPc;
@@ -594,12 +622,45 @@ __device__ void dfs(const SearchArgs &a, const RootCtx &r, Ck<Geo<W>::CH> P, Ck<
     }
 }
 
+// Per-warp shared memory of the build: open-addressing hash of P(v) (id -> local index) and
+// a staging row.
+struct WarpSmem {
+    int *hkey, *hval;
+    unsigned *stage;
+    int slots;
+};
+
+__device__ __forceinline__ unsigned hash_slot(int id, int mask)
+{
+    return ((unsigned)id * 0x9E3779B1u >> 7) & (unsigned)mask;
+}
+
+__device__ __forceinline__ int hash_find(const WarpSmem &sm, int id)
+{
+    const int mask = sm.slots - 1;
+    unsigned s = hash_slot(id, mask);
+    while (true) {
+        const int k = sm.hkey[s];
+        if (k == id) return sm.hval[s];
+        if (k < 0) return -1;
+        s = (s + 1) & (unsigned)mask;
+    }
+}
+
 // Builds the induced subgraph of root v into the warp's workspace and searches it.
+//
+// Rows: for u in N(v), row(u) has bit i set iff u is adjacent to the i-th vertex of P (the
+// binary-encoded induced subgraph over P u X, Section 3.4's full variant).  Every such
+// adjacency u - p with p in P is found by streaming the later-neighbour list N+(u): a vertex of
+// X precedes v and so precedes every p in P, hence p is in N+(u); a pair of P vertices is found
+// from the earlier of the two.  Membership in P is a shared-memory hash lookup, so the build
+// reads the bounded lists N+(u) (each at most d long) with coalesced loads and no search.
 template <int W>
-__device__ void search_root(const SearchArgs &a, unsigned *ws, int v, int deg, int np, Acc &acc,
-                            unsigned long long *s_hist, int lane)
+__device__ void search_root(const SearchArgs &a, unsigned *ws, const WarpSmem &sm, int v, int deg,
+                            int np, Acc &acc, unsigned long long *s_hist, int lane)
 {
     constexpr int CH = Geo<W>::CH, G = Geo<W>::G;
+    PROF_START(t_build);
     RootCtx r = make_ctx(ws, deg, np);
     const int *Nv = a.g.adj + a.g.offs[v];
     const int rv = a.g.rank[v];
@@ -613,74 +674,110 @@ __device__ void search_root(const SearchArgs &a, unsigned *ws, int v, int deg, i
         const bool isP = in && __ldg(a.g.rank + w) > rv;
         const unsigned mp = __ballot_sync(kFull, isP);
         const unsigned mx = __ballot_sync(kFull, in && !isP);
-        if (isP) {
-            const int idx = pi + __popc(mp & lt);
-            r.pids[idx] = w;
-            r.loc[j] = idx;
-        } else if (in) {
-            r.loc[j] = (xi + __popc(mx & lt)) | INT_MIN;
-        }
+        if (isP) r.pids[pi + __popc(mp & lt)] = w;
+        else if (in) r.xids[xi + __popc(mx & lt)] = w;
         pi += __popc(mp);
         xi += __popc(mx);
     }
-    // zero the rows
+    // hash P(v); zero the P rows (X rows are written whole below, or zeroed for wide rows)
     {
-        const long long words = (long long)deg * W;
-        unsigned *rows = r.rowsP;   // rowsX follows rowsP directly
+        const long long words = (long long)(W <= 4 ? np : deg) * W;
         for (long long t = (long long)lane * CH; t < words; t += 32 * CH)
-            ck_store<CH>(rows + t, ck_zero<CH>());
+            ck_store<CH>(r.rowsP + t, ck_zero<CH>());
     }
+    int slots = 32;
+    while (slots < 2 * np) slots <<= 1;
+    WarpSmem h = sm;
+    h.slots = slots;
+    for (int i = lane; i < slots; i += 32) h.hkey[i] = -1;
     if (lane == 0) r.rids[0] = v;
     __syncwarp();
-    // column i of every row: adjacency to the i-th P vertex (binary-encoded induced subgraph)
-    for (int i = 0; i < np; ++i) {
-        const int p = r.pids[i];
-        const int plo = __ldg(a.g.offs + p);
-        const int dp = __ldg(a.g.offs + p + 1) - plo;
-        const int wi = i >> 5;
-        const unsigned bi = 1u << (i & 31);
-        if (dp <= deg) {
-            for (int t = lane; t < dp; t += 32) {
-                const int w = __ldg(a.g.adj + plo + t);
-                const int j = lower_bound_dev(Nv, deg, w);
-                if (j < deg && __ldg(Nv + j) == w) {
-                    const int code = r.loc[j];
-                    unsigned *row = code < 0 ? r.rowsX + (long long)(code & INT_MAX) * W
-                                             : r.rowsP + (long long)code * W;
-                    row[wi] |= bi;
-                }
-            }
-        } else {
-            for (int t = lane; t < deg; t += 32) {
-                const int w = __ldg(Nv + t);
-                const int j = lower_bound_dev(a.g.adj + plo, dp, w);
-                if (j < dp && __ldg(a.g.adj + plo + j) == w) {
-                    const int code = r.loc[t];
-                    unsigned *row = code < 0 ? r.rowsX + (long long)(code & INT_MAX) * W
-                                             : r.rowsP + (long long)code * W;
-                    row[wi] |= bi;
-                }
-            }
-        }
-        __syncwarp();
-    }
-    for (int i = lane; i < np; i += 32) r.pkey[i] = vertex_key(r.pids[i]);
-    // X_X: the X vertices with at least one neighbour in P (the others leave X at the first
-    // branch and can never be a better pivot than a P vertex)
-    int nxx = 0;
-    for (int base = 0; base < r.nx; base += 32) {
-        const int x = base + lane;
-        bool keep = false;
-        if (x < r.nx) {
-            unsigned t = 0;
-            for (int k = 0; k < W; ++k) t |= r.rowsX[(long long)x * W + k];
-            keep = t != 0u;
-        }
-        const unsigned m = __ballot_sync(kFull, keep);
-        if (keep) r.xx[nxx + __popc(m & lt)] = x;
-        nxx += __popc(m);
+    for (int i = lane; i < np; i += 32) {
+        const int id = r.pids[i];
+        unsigned sl = hash_slot(id, slots - 1);
+        while (atomicCAS(&h.hkey[sl], -1, id) != -1) sl = (sl + 1) & (unsigned)(slots - 1);
+        h.hval[sl] = i;
     }
     __syncwarp();
+    // X rows, one vertex per lane.  A vertex of X adjacent to all of P makes every clique of
+    // this subtree extendable (it is the Tomita pivot of the root with P - N(pivot) empty):
+    // the subtree holds no maximal clique and is abandoned as soon as one is seen.
+    int nxx = 0;
+    bool covered = false;
+    for (int base = 0; base < r.nx && !covered; base += 32) {
+        const int xi = base + lane;
+        int hits = 0;
+        unsigned reg[W <= 4 ? W : 1];
+#pragma unroll
+        for (int k = 0; k < (W <= 4 ? W : 1); ++k) reg[k] = 0u;
+        unsigned *row = r.rowsX + (long long)xi * W;
+        if (xi < r.nx) {
+            const int u = r.xids[xi];
+            const int s1 = __ldg(a.g.poffs + u + 1);
+            for (int e = __ldg(a.g.poffs + u); e < s1; ++e) {
+                const int j = hash_find(h, __ldg(a.g.padj + e));
+                if (j < 0) continue;
+                ++hits;
+                if constexpr (W <= 4) {
+#pragma unroll
+                    for (int k = 0; k < W; ++k) reg[k] |= (j >> 5) == k ? 1u << (j & 31) : 0u;
+                } else {
+                    row[j >> 5] |= 1u << (j & 31);
+                }
+            }
+            if constexpr (W <= 4) {
+                Ck<CH> c;
+#pragma unroll
+                for (int k = 0; k < CH; ++k) c.w[k] = reg[k];
+                ck_store<CH>(row, c);
+            }
+        }
+        covered = __any_sync(kFull, hits == np && xi < r.nx);
+        const unsigned m = __ballot_sync(kFull, hits > 0);
+        if (hits > 0) r.xx[nxx + __popc(m & lt)] = xi;
+        nxx += __popc(m);
+    }
+    if (covered) {
+        acc.nodes++;
+        PROF_ADD(acc, kProfBuild, t_build);
+        return;
+    }
+    // P rows, one vertex per lane: the later P neighbours of p_i come from N+(p_i) ...
+    for (int base = 0; base < np; base += 32) {
+        const int i = base + lane;
+        if (i < np) {
+            const int u = r.pids[i];
+            unsigned *row = r.rowsP + (long long)i * W;
+            const int s1 = __ldg(a.g.poffs + u + 1);
+            for (int e = __ldg(a.g.poffs + u); e < s1; ++e) {
+                const int j = hash_find(h, __ldg(a.g.padj + e));
+                if (j >= 0) row[j >> 5] |= 1u << (j & 31);
+            }
+        }
+    }
+    __syncwarp();
+    // ... and the earlier ones by symmetry: transpose 32 x 32 bit blocks with ballots
+    const int nb = (np + 31) >> 5;
+    for (int bi = 0; bi < nb; ++bi) {
+        for (int bj = 0; bj < nb; ++bj) {
+            const int ri = bi * 32 + lane;                 // this lane's row in block row bi
+            const unsigned word = ri < np ? r.rowsP[(long long)ri * W + bj] : 0u;
+            unsigned tr = 0;
+#pragma unroll 4
+            for (int k = 0; k < 32; ++k) {
+                const unsigned col = __ballot_sync(kFull, (word >> k) & 1u);
+                if (lane == k) tr = col;
+            }
+            // tr = word bi of row (bj * 32 + lane), as seen from the block (bi, bj)
+            const int rj = bj * 32 + lane;
+            __syncwarp();
+            if (rj < np && tr) r.rowsP[(long long)rj * W + bi] |= tr;
+            __syncwarp();
+        }
+    }
+    for (int i = lane; i < np; i += 32) r.pkey[i] = vertex_key(r.pids[i]);
+    __syncwarp();
+    PROF_ADD(acc, kProfBuild, t_build);
     const int q = lane % G;
     dfs<W>(a, r, bits_prefix<W>(np, q), ck_zero<CH>(), nxx, vertex_key(v), acc, s_hist, lane);
 }
@@ -692,9 +789,18 @@ __device__ void search_inbox(const SearchArgs &a, unsigned *ws, Acc &acc,
 {
     constexpr int CH = Geo<W>::CH, G = Geo<W>::G;
     const int q = lane % G;
-    RootCtx r = make_ctx(ws, (int)ws[kHdrDeg], (int)ws[kHdrNp]);
-    r.rsize = (int)ws[kHdrRsize];
-    const int k = (int)ws[kHdrK];
+    const int deg = (int)ws[kHdrDeg], np = (int)ws[kHdrNp];
+    const int k = (int)ws[kHdrK], rsize = (int)ws[kHdrRsize];
+    // a branch always comes from a root of this kernel's class, within its workspace
+    const bool sane = np >= 1 && np <= kMaxP && wclass(np) == W && deg >= np && k >= 0 &&
+                      k <= deg - np && rsize >= 2 && rsize <= np + 1 &&
+                      (unsigned long long)ws_layout(deg, np).total <= a.ws_words;
+    if (!sane) {
+        if (lane == 0) set_status(a.g.ctrl, MCE_ERR_INTERNAL);
+        return;
+    }
+    RootCtx r = make_ctx(ws, deg, np);
+    r.rsize = rsize;
     const unsigned long long S = *reinterpret_cast<const unsigned long long *>(ws + kHdrS);
     const Ck<CH> P = ck_load<CH>(ws + kHdrP + q * CH);
     const Ck<CH> XP = ck_load<CH>(ws + kHdrXP + q * CH);
@@ -712,17 +818,29 @@ struct MinBlocks {
 template <int W>
 __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(SearchArgs a)
 {
-    extern __shared__ unsigned long long s_hist[];
+    extern __shared__ __align__(16) unsigned char s_raw[];
+    unsigned long long *s_hist = reinterpret_cast<unsigned long long *>(s_raw);
     for (int i = threadIdx.x; i < a.out.hist_len; i += blockDim.x) s_hist[i] = 0ULL;
-    __syncthreads();
     const int lane = threadIdx.x & 31;
     const int wpb = blockDim.x >> 5;
     const int warp = blockIdx.x * wpb + (threadIdx.x >> 5);
+    WarpSmem sm;
+    {
+        constexpr int k = W == 1 ? 0 : W == 2 ? 1 : W == 4 ? 2 : W == 8 ? 3 : W == 16 ? 4 : 5;
+        const size_t hist = ((size_t)(a.out.hist_len + 1) * 8 + 15) & ~(size_t)15;
+        unsigned char *mine = s_raw + hist +
+                              (size_t)(threadIdx.x >> 5) * ((size_t)hash_slots(k) * 8 + 128);
+        sm.hkey = reinterpret_cast<int *>(mine);
+        sm.hval = sm.hkey + hash_slots(k);
+        sm.stage = reinterpret_cast<unsigned *>(sm.hval + hash_slots(k));
+        sm.slots = hash_slots(k);
+    }
+    __syncthreads();
     unsigned *ws = a.ws + (unsigned long long)warp * a.ws_words;
     const unsigned long long begin = (unsigned long long)a.range[2 * a.cls];
     const unsigned long long n_roots = (unsigned long long)a.range[2 * a.cls + 1] - begin;
     dev_int busy(a.g.ctrl->busy);
-    Acc acc{0, 0, 0, 0};
+    Acc acc{};
     // phase 1: first-level subtrees from the shared counter
     while (load_status(a.g.ctrl) == 0) {
         unsigned long long idx = 0;
@@ -733,6 +851,7 @@ __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(Search
         }
         idx = __shfl_sync(kFull, idx, 0);
         if (idx >= n_roots) break;
+        PROF_START(t_root);
         const int v = a.roots[begin + idx];
         const int deg = a.g.offs[v + 1] - a.g.offs[v];
         const int np = a.g.pcount[v];
@@ -749,14 +868,22 @@ __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(Search
         } else if (np > kMaxP) {
             if (lane == 0) set_status(a.g.ctrl, MCE_ERR_LIMIT);
         } else {
-            search_root<W>(a, ws, v, deg, np, acc, s_hist, lane);
+            search_root<W>(a, ws, sm, v, deg, np, acc, s_hist, lane);
         }
         __syncwarp();
         if (lane == 0) busy.fetch_sub(1, cuda::memory_order_acq_rel);
+#ifdef MCE_PROFILE
+        {
+            const unsigned long long dt = (unsigned long long)(clock64() - t_root);
+            acc.prof[kProfMaxRoot] = dt > acc.prof[kProfMaxRoot] ? dt : acc.prof[kProfMaxRoot];
+            acc.prof[kProfRoots]++;
+        }
+#endif
     }
     // phase 2: receive donated branches until no warp holds work
     while (a.worker_list && load_status(a.g.ctrl) == 0) {
         int state = 0;   // 1: a branch arrived, 2: leave
+        PROF_START(t_idle);
         if (lane == 0) {
             if (!ring_push(a, warp)) state = 2;
             dev_int flag(a.flag[warp]);
@@ -785,13 +912,13 @@ __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(Search
                     if (ns < 2048) ns <<= 1;
                 }
             }
-            if (state == 1) flag.store(kInboxIdle, cuda::memory_order_relaxed);
+            if (state == 1) flag.store(kInboxIdle, cuda::memory_order_release);
         }
         state = __shfl_sync(kFull, state, 0);
+        PROF_ADD(acc, kProfIdle, t_idle);
         if (state != 1) break;
         __syncwarp();
-        dev_int(a.flag[warp]).load(cuda::memory_order_acquire);
-        __threadfence();
+        cuda::atomic_thread_fence(cuda::memory_order_acquire, cuda::thread_scope_device);
         search_inbox<W>(a, ws, acc, s_hist, lane);
         __syncwarp();
         if (lane == 0) busy.fetch_sub(1, cuda::memory_order_acq_rel);
@@ -804,6 +931,13 @@ __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(Search
         atomicAdd(&a.g.ctrl->result[1], acc.hash);
         atomicAdd(&a.g.ctrl->tree_nodes, acc.nodes);
         atomicAdd(&a.g.ctrl->donations, acc.donations);
+        atomicAdd(&a.g.ctrl->words[a.cls], acc.words);
+#ifdef MCE_PROFILE
+        for (int i = 0; i < 8; ++i) {
+            if (i == kProfMaxRoot) atomicMax(&a.g.ctrl->prof[a.cls][i], acc.prof[i]);
+            else atomicAdd(&a.g.ctrl->prof[a.cls][i], acc.prof[i]);
+        }
+#endif
     }
 }
 
@@ -892,6 +1026,12 @@ static const void *search_kernel_ptr(int cls)
     case 4: return kernel_of<16>();
     default: return kernel_of<32>();
     }
+}
+
+cudaError_t search_configure(int cls, size_t smem)
+{
+    return cudaFuncSetAttribute(search_kernel_ptr(cls), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)smem);
 }
 
 cudaError_t search_occupancy(int cls, int threads, size_t smem, int *blocks_per_sm)
