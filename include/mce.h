@@ -187,6 +187,33 @@ mce_status mce_get_order(mce_graph *g, void *stream, int32_t *d_rank, int32_t *d
  */
 mce_status mce_get_profile(mce_graph *g, uint64_t *out);
 
+/*
+ * Degeneracy order of a small graph without allocating anything.
+ *
+ * The paper has no counterpart: this is a packaging of mce_order's peel for callers that are
+ * not allowed to allocate device memory -- code that runs inside a framework whose caching
+ * allocator owns all of the GPU's memory, plug-ins that are only ever handed buffers, or
+ * latency-critical paths that must not pay for cudaMalloc and the synchronisation it implies.
+ * It neither creates a handle nor calls cudaMalloc, cudaFree or any allocating library routine;
+ * its scratch space is one fixed array of about 5.3 MiB in device memory, which every GPU that
+ * loads the library holds until the process exits.
+ *   d_offsets, d_adj  device pointers to a simple undirected graph as a CSR (the same layout as
+ *                     mce_create).  The input is NOT checked: validate it with mce_create first
+ *                     if it may be malformed.
+ *   n                 0 <= n <= 262144; larger graphs return MCE_ERR_LIMIT and nothing runs.
+ *   d_rank, d_core    device int32[n]: position in the canonical degeneracy order and core
+ *                     number, identical to what mce_get_order reports for the same graph.
+ *   d_result          device int32[2]: {degeneracy d, device-side status (0 or an mce_status)}.
+ *   stream            the work is enqueued on it; the call returns without waiting.
+ * The first call on each device looks up the device address of the scratch array
+ * (cudaGetSymbolAddress); make that first call before any stream capture starts.  All calls
+ * share the one array, so calls that can overlap on the GPU (different streams or host
+ * threads) race with each other: keep them in one stream, one at a time.  Each call clears
+ * the part of the array that must start at zero.
+ */
+mce_status mce_order_noalloc(const int32_t *d_offsets, const int32_t *d_adj, int32_t n,
+                             int32_t *d_rank, int32_t *d_core, int32_t *d_result, void *stream);
+
 /* Synchronises `stream`, then returns (and clears) the device-side status of the handle. */
 mce_status mce_last_error(mce_graph *g, void *stream);
 

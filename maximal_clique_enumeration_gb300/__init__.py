@@ -26,7 +26,7 @@ STATUS = {
 }
 EXPORTS = ["mce_config_default", "mce_create", "mce_order", "mce_count", "mce_count_roots",
            "mce_enumerate", "mce_get_order", "mce_last_error", "mce_get_info", "mce_get_profile",
-           "mce_destroy", "mce_status_str"]
+           "mce_destroy", "mce_status_str", "mce_order_noalloc"]
 PROFILE_ACTIVITIES = ["build", "pivot", "child", "partition", "donate", "idle", "max_root",
                       "roots"]
 

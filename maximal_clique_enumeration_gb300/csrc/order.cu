@@ -477,3 +477,100 @@ cudaError_t launch_order(const DevGraph &g, int peel_blocks, long long spin_limi
 }
 
 }  // namespace mce
+
+// ------------------------------------------------------------------ allocation-free order
+//
+// mce_order_noalloc: the degeneracy order of a small graph with no allocation at all, for
+// callers that may not call cudaMalloc (see include/mce.h).  The peel kernel above runs
+// unchanged; only its scratch (degrees, live lists, the removal order, the barrier counters)
+// lives in one fixed array in device memory instead of a handle's buffers.
+
+namespace mce {
+
+namespace {
+
+constexpr int kNoAllocMaxN = 1 << 18;        // vertices
+constexpr int kNoAllocMaxBlocks = 1024;      // CTAs of the cooperative peel
+constexpr int kNoAllocCtrlWords = (int)((sizeof(DevCtrl) + 255) / 256 * 64);
+constexpr int kNoAllocWords = kNoAllocCtrlWords + 4 * kNoAllocMaxBlocks + 5 * kNoAllocMaxN;
+constexpr int kNoAllocMaxDevices = 64;
+
+// The whole scratch area: 5 MiB + a few KiB, held by every device that loads the library.
+static __device__ __align__(256) int g_noalloc_scratch[kNoAllocWords];
+
+int *g_noalloc_ptr[kNoAllocMaxDevices];      // device address of the array, per device
+
+// Clears what the peel reads before writing: the status word and the barrier counter.
+__global__ void noalloc_prep_kernel()
+{
+    DevCtrl *c = reinterpret_cast<DevCtrl *>(g_noalloc_scratch);
+    c->status = 0;
+    c->bar_count = 0u;
+    c->degeneracy = 0;
+    c->rounds = 0;
+}
+
+__global__ void noalloc_result_kernel(int *d_result)
+{
+    const DevCtrl *c = reinterpret_cast<const DevCtrl *>(g_noalloc_scratch);
+    d_result[0] = c->degeneracy;
+    d_result[1] = c->status;
+}
+
+}  // namespace
+
+}  // namespace mce
+
+extern "C" mce_status mce_order_noalloc(const int32_t *d_offsets, const int32_t *d_adj, int32_t n,
+                                        int32_t *d_rank, int32_t *d_core, int32_t *d_result,
+                                        void *stream)
+{
+    using namespace mce;
+    if (n < 0 || !d_result) return MCE_ERR_INVALID_ARG;
+    if (n > kNoAllocMaxN) return MCE_ERR_LIMIT;          // checked first: the size is the news
+    if (n > 0 && (!d_offsets || !d_adj || !d_rank || !d_core)) return MCE_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MCE_ERR_CUDA;
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return MCE_ERR_LIMIT;
+    if (!g_noalloc_ptr[dev]) {                    // set-up, once per device
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return MCE_ERR_CUDA;
+        }
+        g_noalloc_ptr[dev] = static_cast<int *>(p);
+    }
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return MCE_ERR_CUDA;
+    const int blocks = sms < kNoAllocMaxBlocks ? sms : kNoAllocMaxBlocks;
+    int *base = g_noalloc_ptr[dev];
+    cudaStream_t s = (cudaStream_t)stream;
+    DevGraph g{};
+    g.n = n;
+    g.offs = d_offsets;
+    g.adj = d_adj;
+    g.rank = d_rank;
+    g.core = d_core;
+    g.ctrl = reinterpret_cast<DevCtrl *>(base);
+    g.blk_cnt = base + kNoAllocCtrlWords;
+    g.blk_min = g.blk_cnt + 2 * kNoAllocMaxBlocks;
+    g.deg = g.blk_min + 2 * kNoAllocMaxBlocks;
+    g.round_of = g.deg + kNoAllocMaxN;
+    g.alive_a = g.round_of + kNoAllocMaxN;
+    g.alive_b = g.alive_a + kNoAllocMaxN;
+    g.order = g.alive_b + kNoAllocMaxN;
+    noalloc_prep_kernel<<<1, 1, 0, s>>>();
+    if (cudaGetLastError() != cudaSuccess) return MCE_ERR_CUDA;
+    if (n > 0) {
+        long long lim = 20LL * 1000 * 1000 * 1000;
+        void *args[] = {&g, &lim};
+        if (cudaLaunchCooperativeKernel((const void *)peel_kernel, dim3(blocks),
+                                        dim3(kPeelThreads), args, 0, s) != cudaSuccess) {
+            cudaGetLastError();
+            return MCE_ERR_CUDA;
+        }
+    }
+    noalloc_result_kernel<<<1, 1, 0, s>>>(d_result);
+    return cudaGetLastError() == cudaSuccess ? MCE_OK : MCE_ERR_CUDA;
+}
