@@ -33,6 +33,24 @@ if ROOT not in sys.path:
 METRIC = "maximal cliques/sec (R-MAT s20 ef16)"
 UNIT = "cliques/s"
 
+# DRAM traffic of the dominant search launch, from the last ncu capture summarised in
+# profiles/search_kernel_w4_rmat_s20_sample.md (a 10 % root sample; dram bytes read + written
+# = 82.4 MB for 86,953,769 counted words).  It is scaled to a full launch by the counted words
+# and only reported while the kernel sources are the ones it was measured on.
+TRAFFIC_CAPTURE = {"sources": "d4006426136c7cdf", "width_class": 2,
+                   "bytes_per_word": 82.4e6 / 86953769.0}
+KERNEL_SOURCES = ["maximal_clique_enumeration_gb300/csrc/search.cu",
+                  "maximal_clique_enumeration_gb300/csrc/mce_internal.cuh"]
+
+
+def kernel_sources_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
 
 def parse_args():
     p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
@@ -44,6 +62,8 @@ def parse_args():
     p.add_argument("--scale", type=int, default=20)
     p.add_argument("--max-p", type=int, default=128,
                    help="first-level subtrees whose root has |P| < max_p form the workload")
+    p.add_argument("--root-fraction", type=float, default=1.0,
+                   help="profiling aid: keep only this seeded share of the workload roots")
     p.add_argument("--cpu-fraction", type=float, default=0.2,
                    help="share of the workload roots the oracle baseline counts")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -104,6 +124,7 @@ def workload_config(args, g, roots, pc, d):
         "n": g.n, "m": g.m, "max_degree": g.max_degree(), "degeneracy": d,
         "roots": int(len(roots)), "roots_total": g.n, "max_p": args.max_p,
         "roots_left_out": int((pc >= args.max_p).sum()),
+        "root_fraction": args.root_fraction,
         "l2": "flushed between steps (256 MiB write, untimed)",
     }
 
@@ -192,6 +213,10 @@ def run_gb300(args, rank, world, local):
     h = mce.Graph(dev_offs, dev_adj, g.n, profile=1)
     rank_arr, _ = h.order_arrays()
     roots, pc = light_roots(g, rank_arr.cpu().numpy(), args.max_p)
+    if args.root_fraction < 1.0:
+        rng = np.random.default_rng(args.seed + 3000)
+        keep = max(1, int(len(roots) * args.root_fraction))
+        roots = np.sort(rng.choice(roots, size=keep, replace=False)).astype(np.int32)
     roots_dev = torch.from_numpy(roots).cuda()
     out = h.new_output()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
@@ -251,7 +276,10 @@ def run_gb300(args, rank, world, local):
         "bound": "alu", "kernel": f"search_kernel<W={1 << dom}>",
         "achieved": rate / 1e9, "peak": pr["words_per_s"] / 1e9, "unit": "Gword/s",
         "frac": rate / pr["words_per_s"] if pr["words_per_s"] else None,
-        "traffic": None,
+        "traffic": (TRAFFIC_CAPTURE["bytes_per_word"] * words_cls[dom] / args.steps
+                    if kernel_sources_hash() == TRAFFIC_CAPTURE["sources"]
+                    and dom == TRAFFIC_CAPTURE["width_class"] else None),
+        "traffic_unit": "bytes per launch (ncu capture, scaled by counted words)",
         "peak_source": "measured: AND+POPC+ADD word rate of a register-only kernel on this GPU "
                        f"({pr['ms']:.2f} ms probe)",
         "share_of_step": float(ms_cls[dom] / max(sum(step_ms), 1e-9)),

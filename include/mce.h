@@ -60,6 +60,8 @@ typedef enum mce_status {
  *   blocks_per_sm    CTAs per SM of the search kernel (0 = as many as can be resident).
  *   profile          1: record CUDA events around the ordering and around every search launch,
  *                    so that mce_get_info reports per-stage device times; 0 (default): none.
+ *   donate_rule      0 (default): donate only when unexplored branches remain both at the
+ *                    donor's level and at an earlier level (Section 3.3); 1: when either holds.
  *   spin_limit_ns    upper bound on any single device-side wait (grid barrier, idle warp
  *                    waiting for a donation); on expiry the kernel records
  *                    MCE_ERR_DEVICE_TIMEOUT and returns instead of hanging (an idle warp
@@ -72,7 +74,7 @@ typedef struct mce_config {
     int32_t warps_per_block;
     int32_t blocks_per_sm;
     int32_t profile;
-    int32_t reserved;
+    int32_t donate_rule;
     int64_t spin_limit_ns;
 } mce_config;
 

@@ -44,7 +44,7 @@ NUM_WIDTHS = 6
 class Config(ctypes.Structure):
     _fields_ = [("worker_list", ctypes.c_int32), ("donate_min_p", ctypes.c_int32),
                 ("warps_per_block", ctypes.c_int32), ("blocks_per_sm", ctypes.c_int32),
-                ("profile", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("profile", ctypes.c_int32), ("donate_rule", ctypes.c_int32),
                 ("spin_limit_ns", ctypes.c_int64)]
 
 

@@ -16,9 +16,10 @@ struct mce_graph {
     int sm_count = 0;
     int peel_blocks = 0;
     int search_threads = 0, n_workers = 0;
-    int cls_blocks[kNumClasses] = {}, cls_workers[kNumClasses] = {}, cls_count[kNumClasses] = {};
+    // per launch group g = 2k + b (row width 1 << k; b = 0 big-workspace roots, 1 the rest)
+    int grp_blocks[kNumGroups] = {}, grp_workers[kNumGroups] = {}, grp_count[kNumGroups] = {};
+    unsigned long long grp_ws[kNumGroups] = {};
     size_t cls_smem[kNumClasses] = {};
-    unsigned long long cls_ws[kNumClasses] = {};
     long long uroots_cap = 0;
     int degeneracy = 0, max_degree = 0, hist_len = 2, rounds = 0;
     unsigned long long ws_words = 0;
@@ -34,8 +35,8 @@ struct mce_graph {
     bool count_cache_valid = false;
     // profiling: events around the order and around each class launch
     cudaEvent_t ev_order[2] = {nullptr, nullptr};
-    cudaEvent_t ev_cls[kNumClasses][2] = {};
-    bool cls_timed[kNumClasses] = {};
+    cudaEvent_t ev_grp[kNumGroups][2] = {};
+    bool grp_timed[kNumGroups] = {};
     bool order_timed = false;
     int launches_order = 0, launches_count = 0;
 };
@@ -91,9 +92,9 @@ void free_all(mce_graph *h)
     h->allocs.clear();
     for (int i = 0; i < 2; ++i)
         if (h->ev_order[i]) cudaEventDestroy(h->ev_order[i]);
-    for (int k = 0; k < kNumClasses; ++k)
+    for (int k = 0; k < kNumGroups; ++k)
         for (int i = 0; i < 2; ++i)
-            if (h->ev_cls[k][i]) cudaEventDestroy(h->ev_cls[k][i]);
+            if (h->ev_grp[k][i]) cudaEventDestroy(h->ev_grp[k][i]);
 }
 
 // Resets the per-search accumulators of the control block.
@@ -103,7 +104,7 @@ mce_status reset_search(mce_graph *h, cudaStream_t s)
     MCE_TRY(cudaMemsetAsync(&c->tree_nodes, 0, 4 * sizeof(unsigned long long), s));
     MCE_TRY(cudaMemsetAsync(c->words, 0, sizeof(c->words), s));
     MCE_TRY(cudaMemsetAsync(c->prof, 0, sizeof(c->prof), s));
-    for (int k = 0; k < kNumClasses; ++k) h->cls_timed[k] = false;
+    for (int k = 0; k < kNumGroups; ++k) h->grp_timed[k] = false;
     MCE_TRY(cudaMemsetAsync(h->hist_acc, 0, sizeof(unsigned long long) * h->hist_len, s));
     return MCE_OK;
 }
@@ -131,20 +132,23 @@ mce_status run_search(mce_graph *h, cudaStream_t s, bool user_roots, const DevOu
     a.flag = h->flag;
     a.worker_list = h->cfg.worker_list;
     a.donate_min_p = h->cfg.donate_min_p;
+    a.donate_rule = h->cfg.donate_rule;
     a.spin_limit_ns = h->cfg.spin_limit_ns;
-    for (int k = kNumClasses - 1; k >= 0; --k) {
-        if (h->cls_workers[k] == 0) continue;             // no vertex of the graph in this class
-        if (!user_roots && h->cls_count[k] == 0) continue;
+    for (int o = 0; o < kNumGroups; ++o) {
+        const int gi = group_at(o), k = gi / 2;
+        if (h->grp_workers[gi] == 0) continue;            // no vertex of the graph in this group
+        if (!user_roots && h->grp_count[gi] == 0) continue;
         a.cls = k;
-        a.ws_words = h->cls_ws[k];
-        a.n_workers = h->cls_workers[k];
+        a.group = gi;
+        a.ws_words = h->grp_ws[gi];
+        a.n_workers = h->grp_workers[gi];
         MCE_TRY(cudaMemsetAsync(h->flag, 0, sizeof(int) * (size_t)a.n_workers, s));
         MCE_TRY(launch_search_prep(a, s));
-        if (h->cfg.profile) MCE_TRY(cudaEventRecord(h->ev_cls[k][0], s));
-        MCE_TRY(launch_search(a, h->cls_blocks[k], h->search_threads, h->cls_smem[k], s));
+        if (h->cfg.profile) MCE_TRY(cudaEventRecord(h->ev_grp[gi][0], s));
+        MCE_TRY(launch_search(a, h->grp_blocks[gi], h->search_threads, h->cls_smem[k], s));
         if (h->cfg.profile) {
-            MCE_TRY(cudaEventRecord(h->ev_cls[k][1], s));
-            h->cls_timed[k] = true;
+            MCE_TRY(cudaEventRecord(h->ev_grp[gi][1], s));
+            h->grp_timed[gi] = true;
         }
         h->launches_count += 2;
     }
@@ -163,7 +167,7 @@ mce_status mce_config_default(mce_config *cfg)
     cfg->warps_per_block = kDefaultWarpsPerBlock;
     cfg->blocks_per_sm = 0;
     cfg->profile = 0;
-    cfg->reserved = 0;
+    cfg->donate_rule = 0;
     cfg->spin_limit_ns = 20LL * 1000 * 1000 * 1000;
     return MCE_OK;
 }
@@ -273,9 +277,9 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
     if (h->cfg.profile) {
         MCE_TRY(cudaEventCreate(&h->ev_order[0]));
         MCE_TRY(cudaEventCreate(&h->ev_order[1]));
-        for (int k = 0; k < kNumClasses; ++k) {
-            MCE_TRY(cudaEventCreate(&h->ev_cls[k][0]));
-            MCE_TRY(cudaEventCreate(&h->ev_cls[k][1]));
+        for (int k = 0; k < kNumGroups; ++k) {
+            MCE_TRY(cudaEventCreate(&h->ev_grp[k][0]));
+            MCE_TRY(cudaEventCreate(&h->ev_grp[k][1]));
         }
     }
     {
@@ -297,24 +301,36 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
     int wpb = h->cfg.warps_per_block > 0 ? h->cfg.warps_per_block : kDefaultWarpsPerBlock;
     if (wpb > 4) wpb = 4;
     h->search_threads = 32 * wpb;
-    size_t ws_total = 4;
+    size_t ws_total = 32;
+    int class_per_sm[kNumClasses] = {};
     for (int k = 0; k < kNumClasses; ++k) {
-        h->cls_count[k] = c.cls[2 * k + 1] - c.cls[2 * k];
-        // whole 128-byte lines per warp: no two warps share an L1 line of workspace
-        unsigned long long need = (c.ws_cls[k] + 31) & ~31ULL;
-        if (k == 0 && need < 32) need = 32;               // isolated roots use 1 word
-        if (need == 0) continue;                          // no vertex of this class
         h->cls_smem[k] = search_smem_bytes(k, h->hist_len, wpb);
         MCE_TRY(search_configure(k, h->cls_smem[k]));
-        int per_sm = 0;
-        MCE_TRY(search_occupancy(k, h->search_threads, h->cls_smem[k], &per_sm));
-        if (per_sm < 1) return MCE_ERR_CUDA;
-        if (h->cfg.blocks_per_sm > 0 && h->cfg.blocks_per_sm < per_sm) per_sm = h->cfg.blocks_per_sm;
-        h->cls_blocks[k] = per_sm * h->sm_count;
-        h->cls_workers[k] = h->cls_blocks[k] * wpb;
-        h->cls_ws[k] = need;
-        if ((size_t)h->cls_workers[k] * need > ws_total) ws_total = (size_t)h->cls_workers[k] * need;
-        if (h->cls_workers[k] > h->n_workers) h->n_workers = h->cls_workers[k];
+        MCE_TRY(search_occupancy(k, h->search_threads, h->cls_smem[k], &class_per_sm[k]));
+        if (class_per_sm[k] < 1) return MCE_ERR_CUDA;
+        if (h->cfg.blocks_per_sm > 0 && h->cfg.blocks_per_sm < class_per_sm[k])
+            class_per_sm[k] = h->cfg.blocks_per_sm;
+    }
+    for (int gi = 0; gi < kNumGroups; ++gi) {
+        const int k = gi / 2;
+        const bool big = (gi & 1) == 0;
+        h->grp_count[gi] = c.cls[2 * gi + 1] - c.cls[2 * gi];
+        // whole 128-byte lines per warp: no two warps share an L1 line of workspace
+        unsigned long long need = (c.ws_grp[gi] + 31) & ~31ULL;
+        if (gi == 1 && need < 32) need = 32;              // isolated roots use 1 word
+        if (need == 0) continue;                          // no vertex of the graph in this group
+        int blocks = class_per_sm[k] * h->sm_count;
+        if (big) {
+            // as many warps as the big-workspace budget allows, at most one launch's worth
+            long long warps = kBigBudgetWords / (long long)need;
+            if (warps < wpb) warps = wpb;
+            if (warps / wpb < blocks) blocks = (int)(warps / wpb);
+        }
+        h->grp_blocks[gi] = blocks;
+        h->grp_workers[gi] = blocks * wpb;
+        h->grp_ws[gi] = need;
+        if ((size_t)h->grp_workers[gi] * need > ws_total) ws_total = (size_t)h->grp_workers[gi] * need;
+        if (h->grp_workers[gi] > h->n_workers) h->n_workers = h->grp_workers[gi];
     }
     h->ws_words = ws_total;
     MCE_ALLOC(h, h->ws, ws_total);
@@ -504,10 +520,17 @@ mce_status mce_get_info(mce_graph *h, mce_info *info)
     info->donations = c.donations;
     for (int k = 0; k < kNumClasses; ++k) {
         info->words[k] = c.words[k];
-        info->roots[k] = h->cls_count[k];
-        info->workers[k] = h->cls_workers[k];
-        if (h->cls_timed[k]) MCE_TRY(cudaEventElapsedTime(&info->ms_search[k], h->ev_cls[k][0],
-                                                          h->ev_cls[k][1]));
+        info->roots[k] = h->grp_count[2 * k] + h->grp_count[2 * k + 1];
+        info->workers[k] = h->grp_workers[2 * k + 1] > h->grp_workers[2 * k]
+                               ? h->grp_workers[2 * k + 1] : h->grp_workers[2 * k];
+        info->ms_search[k] = 0.f;
+        for (int b = 0; b < 2; ++b) {
+            const int gi = 2 * k + b;
+            if (!h->grp_timed[gi]) continue;
+            float ms = 0.f;
+            MCE_TRY(cudaEventElapsedTime(&ms, h->ev_grp[gi][0], h->ev_grp[gi][1]));
+            info->ms_search[k] += ms;
+        }
     }
     if (h->order_timed)
         MCE_TRY(cudaEventElapsedTime(&info->ms_order, h->ev_order[0], h->ev_order[1]));

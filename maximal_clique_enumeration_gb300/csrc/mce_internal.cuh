@@ -15,6 +15,9 @@ constexpr int kPeelThreads = 512;
 constexpr int kPeelSoloVertices = 8192;  // the peel finishes in one CTA below this many vertices
 constexpr int kDefaultWarpsPerBlock = 4;
 constexpr int kNumClasses = 6;           // row widths W = 1, 2, 4, 8, 16, 32 words
+constexpr int kNumGroups = 2 * kNumClasses;   // per width: big-workspace roots, then the rest
+constexpr long long kWsCapWords = 16384;     // workspace per warp of a "normal" launch (64 KiB)
+constexpr long long kBigBudgetWords = 256LL << 20;   // workspace of a "big" launch (1 GiB)
 constexpr int kScanBlock = 1024;         // elements per CTA of the exclusive scan
 
 // Device-resident control block of a handle.
@@ -26,7 +29,7 @@ struct DevCtrl {
     unsigned int bar_count;      // grid barrier arrival counter
     unsigned int bar_gen;        // grid barrier generation
     unsigned long long ws_words; // largest per-warp workspace need (words), all classes
-    unsigned long long ws_cls[kNumClasses];   // the same per row-width class
+    unsigned long long ws_grp[kNumGroups];    // the same per launch group
     unsigned long long next_root;  // search: root claim counter
     unsigned long long n_sched;    // search: number of scheduled roots
     int busy;                    // worker list: warps holding work
@@ -40,11 +43,11 @@ struct DevCtrl {
     unsigned long long result[2];  // count, hash of the last search
     unsigned long long words[kNumClasses];  // bitset words processed per row-width class
     unsigned long long prof[kNumClasses][8];  // MCE_PROFILE builds: cycles per activity
-    // first-level roots grouped by row width (class k: W = 1 << k), heaviest class first:
-    // sched[cls[2k] .. cls[2k+1]) for the full schedule, uroots[ucls[2k] .. ucls[2k+1])
-    // for a caller's root list
-    int cls[2 * kNumClasses];    // [begin, end) of class k at cls[2k], cls[2k+1]
-    int ucls[2 * kNumClasses];
+    // first-level roots in launch groups g = 2k + b (row width W = 1 << k; b = 0: roots
+    // whose workspace exceeds kWsCapWords, b = 1: the others): sched[cls[2g] .. cls[2g+1])
+    // for the full schedule, uroots[ucls[2g] .. ucls[2g+1]) for a caller's root list
+    int cls[2 * kNumGroups];     // [begin, end) of launch group g at cls[2g], cls[2g+1]
+    int ucls[2 * kNumGroups];
 };
 
 // Everything the kernels need about a handle's graph (device pointers).
@@ -87,8 +90,9 @@ struct SearchArgs {
     DevGraph g;
     DevOut out;
     const int *roots;        // g.sched or g.uroots
-    const int *range;        // roots[range[cls] .. range[cls+1]) belong to this launch
+    const int *range;        // roots[range[2 group] .. range[2 group + 1]) are this launch's
     int cls;                 // row-width class of this launch (W = 1 << cls)
+    int group;               // launch group (2 cls + 0 for big-workspace roots, + 1 otherwise)
     unsigned int *ws;        // per-warp workspace, ws_words each
     unsigned long long ws_words;
     int *ring;               // worker list: ring of idle warp ids [n_workers]
@@ -97,6 +101,7 @@ struct SearchArgs {
     int n_workers;
     int worker_list;
     int donate_min_p;
+    int donate_rule;         // 0: siblings at this level and at an earlier one; 1: either
     long long spin_limit_ns;
 };
 
@@ -111,29 +116,6 @@ __host__ __device__ inline int wclass(int np)
 __host__ __device__ inline int wclass_index(int np)
 {
     return np <= 32 ? 0 : np <= 64 ? 1 : np <= 128 ? 2 : np <= 256 ? 3 : np <= 512 ? 4 : 5;
-}
-
-// Schedule buckets: row-width classes widest first and, inside a class, roots with a larger
-// estimated cost deg(v) * (|P| + 1) first (log2 buckets).  Bucket 0 holds over-limit roots.
-constexpr int kCostBuckets = 48;
-constexpr int kNumBuckets = 1 + kNumClasses * kCostBuckets;
-
-__host__ __device__ inline int class_first_bucket(int k)
-{
-    return k == kNumClasses - 1 ? 0 : 1 + (kNumClasses - 1 - k) * kCostBuckets;
-}
-__host__ __device__ inline int class_end_bucket(int k)
-{
-    return 1 + (kNumClasses - k) * kCostBuckets;
-}
-
-__device__ inline int sched_bucket(int np, int deg)
-{
-    if (np > kMaxP) return 0;
-    const unsigned long long est = (unsigned long long)deg * (unsigned long long)(np + 1);
-    int lb = est ? 63 - __clzll((long long)est) : 0;
-    lb = lb < kCostBuckets - 1 ? lb : kCostBuckets - 1;
-    return 1 + (kNumClasses - 1 - wclass_index(np)) * kCostBuckets + (kCostBuckets - 1 - lb);
 }
 
 // Per-warp workspace layout (32-bit word offsets) for a root of degree `deg` with np later
@@ -167,6 +149,27 @@ __host__ __device__ inline WsLayout ws_layout(int deg, int np)
     l.stack = o; o += (long long)(np + 1) * l.LV;
     l.total = (o + 3) & ~3LL;
     return l;
+}
+
+// Schedule buckets: launch groups in launch order (widest rows first; per width the roots with
+// a big workspace, then the rest) and, inside a group, roots with a larger estimated cost
+// deg(v) * (|P| + 1) first (log2 buckets).  Bucket 0 holds over-limit roots (group of W = 32).
+constexpr int kCostBuckets = 48;
+constexpr int kNumBuckets = 1 + kNumGroups * kCostBuckets;
+
+// Launch position o = 0 .. kNumGroups-1 <-> group g = 2k + b.
+__host__ __device__ inline int group_at(int o) { return 2 * (kNumClasses - 1 - o / 2) + (o & 1); }
+__host__ __device__ inline int position_of(int g) { return 2 * (kNumClasses - 1 - g / 2) + (g & 1); }
+
+__device__ inline int sched_bucket(int np, int deg)
+{
+    if (np > kMaxP) return 0;
+    const int k = wclass_index(np);
+    const int b = np > 0 && ws_layout(deg, np).total > kWsCapWords ? 0 : 1;
+    const unsigned long long est = (unsigned long long)deg * (unsigned long long)(np + 1);
+    int lb = est ? 63 - __clzll((long long)est) : 0;
+    lb = lb < kCostBuckets - 1 ? lb : kCostBuckets - 1;
+    return 1 + position_of(2 * k + b) * kCostBuckets + (kCostBuckets - 1 - lb);
 }
 
 // Launchers (each returns the CUDA error of its launch).

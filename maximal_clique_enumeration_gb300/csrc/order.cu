@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(kOrientThreads) orient_count_kernel(DevGraph g
     const int warps = gridDim.x * (blockDim.x >> 5);
     int n_iso = 0, maxp = 0, maxdeg = 0;
     unsigned long long iso_hash = 0, ws = 0;
-    unsigned long long ws_cls[kNumClasses] = {0, 0, 0, 0, 0, 0};
+    unsigned long long ws_grp[kNumGroups] = {};
     for (int v = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; v < g.n; v += warps) {
         const int lo = g.offs[v], hi = g.offs[v + 1];
         const int rv = g.rank[v];
@@ -246,8 +246,8 @@ __global__ void __launch_bounds__(kOrientThreads) orient_count_kernel(DevGraph g
                 if (c <= kMaxP) {
                     const unsigned long long need = (unsigned long long)ws_layout(deg, c).total;
                     ws = need > ws ? need : ws;
-                    const int k = wclass_index(c);
-                    ws_cls[k] = need > ws_cls[k] ? need : ws_cls[k];
+                    const int gi = 2 * wclass_index(c) + (need > (unsigned long long)kWsCapWords ? 0 : 1);
+                    ws_grp[gi] = need > ws_grp[gi] ? need : ws_grp[gi];
                 }
             }
         }
@@ -263,24 +263,25 @@ __global__ void __launch_bounds__(kOrientThreads) orient_count_kernel(DevGraph g
         atomicMax(&g.ctrl->max_pcount, maxp);
         atomicMax(&g.ctrl->max_degree, maxdeg);
         atomicMax(&g.ctrl->ws_words, ws);
-        for (int k = 0; k < kNumClasses; ++k)
-            if (ws_cls[k]) atomicMax(&g.ctrl->ws_cls[k], ws_cls[k]);
+        for (int k = 0; k < kNumGroups; ++k)
+            if (ws_grp[k]) atomicMax(&g.ctrl->ws_grp[k], ws_grp[k]);
     }
 }
 
-// Turns a schedule-bucket histogram into bucket cursors and records where each row-width
-// class starts and ends in the resulting order.
+// Turns a schedule-bucket histogram into bucket cursors and records where each launch group
+// starts and ends in the resulting order.
 __device__ void buckets_to_cursors(int *bucket, int *cls, unsigned long long *total)
 {
     int run = 0;
-    for (int k = kNumClasses - 1; k >= 0; --k) {
-        cls[2 * k] = run;
-        for (int b = class_first_bucket(k); b < class_end_bucket(k); ++b) {
+    for (int o = 0; o < kNumGroups; ++o) {
+        const int gi = group_at(o);
+        cls[2 * gi] = run;
+        for (int b = o == 0 ? 0 : 1 + o * kCostBuckets; b < 1 + (o + 1) * kCostBuckets; ++b) {
             const int cnt = bucket[b];
             bucket[b] = run;
             run += cnt;
         }
-        cls[2 * k + 1] = run;
+        cls[2 * gi + 1] = run;
     }
     if (total) *total = (unsigned long long)run;
 }
@@ -449,7 +450,7 @@ cudaError_t launch_order(const DevGraph &g, int peel_blocks, long long spin_limi
     cudaError_t e = cudaMemsetAsync(&g.ctrl->bar_count, 0, sizeof(unsigned int), s);
     if (e == cudaSuccess) e = cudaMemsetAsync(&g.ctrl->max_pcount, 0, sizeof(int), s);
     if (e == cudaSuccess)
-        e = cudaMemsetAsync(&g.ctrl->ws_words, 0, sizeof(unsigned long long) * (1 + kNumClasses), s);
+        e = cudaMemsetAsync(&g.ctrl->ws_words, 0, sizeof(unsigned long long) * (1 + kNumGroups), s);
     if (e == cudaSuccess) e = cudaMemsetAsync(&g.ctrl->n_iso, 0, 2 * sizeof(int), s);
     if (e == cudaSuccess) e = cudaMemsetAsync(&g.ctrl->iso_hash, 0, sizeof(unsigned long long), s);
     if (e == cudaSuccess) e = cudaMemsetAsync(g.bucket, 0, sizeof(int) * kNumBuckets, s);

@@ -293,6 +293,24 @@ __device__ void report(const SearchArgs &a, const RootCtx &r, int L, int c, int 
     }
 }
 
+// Writes the indices of the set bits of a chunked bitset to out[], ascending; returns how many.
+template <int W>
+__device__ __forceinline__ int list_bits(const Ck<Geo<W>::CH> &b, int *out, int lane)
+{
+    constexpr int CH = Geo<W>::CH;
+    int cnt = 0;
+#pragma unroll
+    for (int k = 0; k < W; ++k) {
+        const unsigned wk = __shfl_sync(kFull, b.w[k % CH], k / CH);
+        const bool bit = (wk >> lane) & 1u;
+        const unsigned m = __ballot_sync(kFull, bit);
+        if (bit) out[cnt + __popc(m & ((1u << lane) - 1u))] = k * 32 + lane;
+        cnt += __popc(m);
+    }
+    __syncwarp();
+    return cnt;
+}
+
 // Tomita pivot over P u X_P (bits of P | XP) and the live X_X rows xx[0..lpX): the row with
 // the most neighbours in P, ties to the smaller code.  Returns -1 when some vertex of X is
 // adjacent to all of P (no maximal clique below this node: every branch would be cut).
@@ -303,16 +321,7 @@ __device__ int choose_pivot(const RootCtx &r, const Ck<Geo<W>::CH> &P, const Ck<
     constexpr int CH = Geo<W>::CH, G = Geo<W>::G, R = Geo<W>::R;
     const int q = lane % G, sub = lane / G;
     // list the members of P u X_P
-    int cntp = 0;
-#pragma unroll
-    for (int k = 0; k < W; ++k) {
-        const unsigned wk = __shfl_sync(kFull, PX.w[k % CH], k / CH);
-        const bool bit = (wk >> lane) & 1u;
-        const unsigned m = __ballot_sync(kFull, bit);
-        if (bit) r.plist[cntp + __popc(m & ((1u << lane) - 1u))] = k * 32 + lane;
-        cntp += __popc(m);
-    }
-    __syncwarp();
+    const int cntp = list_bits<W>(PX, r.plist, lane);
     const int total = cntp + lpX;
     unsigned best = 0;
     for (int base = 0; base < total; base += R) {
@@ -465,9 +474,13 @@ __device__ void write_branch(const RootCtx &r, unsigned *dst, int L, int c,
         ck_store<CH>(dst + kHdrP + q * CH, Pc);
         ck_store<CH>(dst + kHdrXP + q * CH, XPc);
     }
-    const long long pw = (long long)r.np * W;
-    for (long long t = (long long)lane * CH; t < pw; t += 32 * CH)
-        ck_store<CH>(dst + lay.rowsP + t, ck_load<CH>(r.rowsP + t));
+    // the branch only ever touches rows (and ids, keys) of vertices in P' u X_P'
+    const int nl = list_bits<W>(ck_or<CH>(Pc, XPc), r.plist, lane);
+    for (long long t = lane; t < (long long)nl * W; t += 32) {
+        const long long i = t / W;
+        const long long off = (long long)r.plist[i] * W + (t - i * W);
+        dst[lay.rowsP + off] = r.rowsP[off];
+    }
     int *dxx = reinterpret_cast<int *>(dst + lay.xx);
     for (long long t = lane; t < (long long)k * W; t += 32) {
         const long long i = t / W;
@@ -477,7 +490,8 @@ __device__ void write_branch(const RootCtx &r, unsigned *dst, int L, int c,
     for (int i = lane; i < k; i += 32) dxx[i] = i;
     int *dp = reinterpret_cast<int *>(dst + lay.pids);
     unsigned long long *dk = reinterpret_cast<unsigned long long *>(dst + lay.pkey);
-    for (int i = lane; i < r.np; i += 32) {
+    for (int t = lane; t < nl; t += 32) {
+        const int i = r.plist[t];
         dp[i] = r.pids[i];
         dk[i] = r.pkey[i];
     }
@@ -573,10 +587,11 @@ __device__ void dfs(const SearchArgs &a, const RootCtx &r, Ck<Geo<W>::CH> P, Ck<
         const int lpXc = xx_partition<W>(r, lpX, c, lane);
         PROF_ADD(acc, kProfPartition, t_part);
         if (lane == 0) acc.words += (unsigned)lpX;
-        // worker list: hand this branch to an idle warp instead of descending (Section 3.3).
-        // The pages ask for unexplored branches both at this level and at an earlier one; a
-        // warp-sized worker has far less to lose by giving work away, so either suffices here.
-        if (a.worker_list && (more_same || more_below)) {
+        // worker list: hand this branch to an idle warp instead of descending (Section 3.3:
+        // only when the donor keeps unexplored branches at this level and an earlier one;
+        // donate_rule 1 accepts either)
+        if (a.worker_list && (a.donate_rule ? (more_same || more_below)
+                                            : (more_same && more_below))) {
             const long long now = __shfl_sync(kFull, (long long)clock64(), 0);
             if (now - last_check > kDonateCheckCycles &&
                 subwarp_sum<G>(ck_popc<CH>(Pc)) >= a.donate_min_p) {
@@ -837,8 +852,8 @@ __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(Search
     }
     __syncthreads();
     unsigned *ws = a.ws + (unsigned long long)warp * a.ws_words;
-    const unsigned long long begin = (unsigned long long)a.range[2 * a.cls];
-    const unsigned long long n_roots = (unsigned long long)a.range[2 * a.cls + 1] - begin;
+    const unsigned long long begin = (unsigned long long)a.range[2 * a.group];
+    const unsigned long long n_roots = (unsigned long long)a.range[2 * a.group + 1] - begin;
     dev_int busy(a.g.ctrl->busy);
     Acc acc{};
     // phase 1: first-level subtrees from the shared counter

@@ -275,7 +275,8 @@ def test_worker_list_on_off_and_forced_donations(name):
     g = G.config_graph(name, 2)
     expect = O.count(g, threads=8).key()
     for cfg in [dict(worker_list=0), dict(worker_list=1),
-                dict(worker_list=1, donate_min_p=1, blocks_per_sm=1)]:
+                dict(worker_list=1, donate_min_p=1, blocks_per_sm=1),
+                dict(worker_list=1, donate_min_p=1, blocks_per_sm=1, donate_rule=1)]:
         with gpu_graph(g, **cfg) as h:
             assert h.count_result() == expect, cfg
             info = h.get_info()
