@@ -274,6 +274,7 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
     h->peel_blocks = h->sm_count;
     MCE_ALLOC(h, g.blk_cnt, (size_t)2 * h->peel_blocks);
     MCE_ALLOC(h, g.blk_min, (size_t)2 * h->peel_blocks);
+    MCE_ALLOC(h, g.blk_cm, (size_t)2 * h->peel_blocks);
     if (h->cfg.profile) {
         MCE_TRY(cudaEventCreate(&h->ev_order[0]));
         MCE_TRY(cudaEventCreate(&h->ev_order[1]));

@@ -11,7 +11,7 @@ namespace mce {
 constexpr int kMaxP = 1024;            // largest |P| of a first-level subtree (32 words per row)
 constexpr int kMaxIdxBits = 21;        // pivot codes are packed as count << 21 | ~code
 constexpr int kMaxCode = (1 << kMaxIdxBits) - 1;
-constexpr int kPeelThreads = 512;
+constexpr int kPeelThreads = 1024;
 constexpr int kPeelSoloVertices = 8192;  // the peel finishes in one CTA below this many vertices
 constexpr int kDefaultWarpsPerBlock = 4;
 constexpr int kNumClasses = 6;           // row widths W = 1, 2, 4, 8, 16, 32 words
@@ -67,7 +67,7 @@ struct DevGraph {
     int *sched;       // first-level roots with |P| > 0, heavy first
     int *deg;         // peel scratch
     int *alive_a, *alive_b;
-    int *blk_cnt, *blk_min;   // peel per-CTA partials [2][grid]
+    int *blk_cnt, *blk_min, *blk_cm;   // peel per-CTA reports [2][grid]
     int *bucket;      // orient: schedule bucket histogram / cursors [kNumBuckets]
     int *ubucket;     // the same for a caller's root list [kNumBuckets]
     int *uroots;      // a caller's roots, grouped by row width, heaviest first

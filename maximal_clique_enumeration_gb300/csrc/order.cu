@@ -10,9 +10,9 @@
 //
 // One cooperative kernel runs all rounds: the remaining vertices stay in an id-ordered list
 // that is compacted stably every round, so each round's removals come out already in id
-// order and the order needs no sort.  Grid-wide barriers separate the phases of a round; once
-// at most kPeelSoloVertices vertices remain, CTA 0 finishes alone with CTA barriers.  Every
-// barrier wait is bounded by spin_limit_ns.
+// order and the order needs no sort.  Two grid-wide barriers separate the phases of a round;
+// once at most kPeelSoloVertices vertices remain, CTA 0 finishes alone with CTA barriers.
+// Every barrier wait is bounded by spin_limit_ns.
 //
 // Then small kernels count every vertex's later neighbours |P| (Algorithm 3's P), count the
 // isolated vertices, bucket the first-level roots by |P|, heaviest first, and store the
@@ -24,48 +24,6 @@
 namespace mce {
 
 namespace {
-
-__device__ __forceinline__ int block_sum(int v, int *sh)
-{
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    v = __reduce_add_sync(0xffffffffu, v);
-    if (lane == 0) sh[w] = v;
-    __syncthreads();
-    int t = 0;
-    for (int i = 0; i < nw; ++i) t += sh[i];
-    __syncthreads();
-    return t;
-}
-
-__device__ __forceinline__ int block_min(int v, int *sh)
-{
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    v = __reduce_min_sync(0xffffffffu, v);
-    if (lane == 0) sh[w] = v;
-    __syncthreads();
-    int t = INT_MAX;
-    for (int i = 0; i < nw; ++i) t = min(t, sh[i]);
-    __syncthreads();
-    return t;
-}
-
-// Exclusive prefix count of `flag` over the CTA (in thread order); *total = CTA-wide count.
-__device__ __forceinline__ int block_excl_scan(bool flag, int *total, int *sh)
-{
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    const unsigned m = __ballot_sync(0xffffffffu, flag);
-    if (lane == 0) sh[w] = __popc(m);
-    __syncthreads();
-    int before = 0, t = 0;
-    for (int i = 0; i < nw; ++i) {
-        const int c = sh[i];
-        if (i < w) before += c;
-        t += c;
-    }
-    __syncthreads();
-    *total = t;
-    return before + __popc(m & ((1u << lane) - 1u));
-}
 
 // Grid-wide barrier for a cooperative launch.  Returns false if the wait exceeded the limit
 // (MCE_ERR_DEVICE_TIMEOUT recorded) or another CTA recorded an error.
@@ -84,15 +42,16 @@ __device__ bool grid_barrier(DevCtrl *ctrl, long long limit_ns)
             atomicAdd((unsigned int *)&ctrl->bar_gen, 1u);
         } else {
             const unsigned long long t0 = globaltimer_ns();
-            unsigned int ns = 32;
+            unsigned int polls = 0;
             while (*gen == g0) {
-                if ((long long)(globaltimer_ns() - t0) > limit_ns) {
-                    set_status(ctrl, MCE_ERR_DEVICE_TIMEOUT);
-                    ok = 0;
-                    break;
+                if ((++polls & 63u) == 1) {              // check the clock now and then
+                    if ((long long)(globaltimer_ns() - t0) > limit_ns) {
+                        set_status(ctrl, MCE_ERR_DEVICE_TIMEOUT);
+                        ok = 0;
+                        break;
+                    }
+                    if (polls > 4096) __nanosleep(128);  // a long wait: stop hammering L2
                 }
-                __nanosleep(ns);
-                if (ns < 256) ns <<= 1;
             }
         }
         __threadfence();
@@ -102,10 +61,52 @@ __device__ bool grid_barrier(DevCtrl *ctrl, long long limit_ns)
     return s_ok != 0;
 }
 
-__global__ void __launch_bounds__(kPeelThreads) peel_kernel(DevGraph g, long long limit_ns)
+__device__ __forceinline__ int warp_incl_scan(int v, int lane)
+{
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += t;
+    }
+    return v;
+}
+
+// Exclusive scan of one value per thread over the CTA; *total = CTA sum.
+__device__ __forceinline__ int block_excl_scan_int(int v, int *total, int *sh)
+{
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int inc = warp_incl_scan(v, lane);
+    if (lane == 31) sh[w] = inc;
+    __syncthreads();
+    int before = 0, t = 0;
+    for (int i = 0; i < nw; ++i) {
+        const int c = sh[i];
+        if (i < w) before += c;
+        t += c;
+    }
+    __syncthreads();
+    *total = t;
+    return before + inc - v;
+}
+
+// Each thread holds up to kPeelItems consecutive entries of its CTA's part of the live list.
+constexpr int kPeelItems = 8;
+
+// One round of the peel, in a CTA that owns live[lo, hi):
+//   scan   -- load ids and current degrees once (kept in registers across the exchange) and
+//             report (#deg <= k, least degree above k, #vertices at that degree);
+//   decide -- from every CTA's report: if some vertex has deg <= k the round removes those,
+//             else the level rises to the least degree d' and the round removes deg == d';
+//   write  -- stable compaction: removed vertices get their rank (round, id order), round and
+//             core number; survivors go to the next live list;
+//   remove -- the CTA subtracts one degree from every neighbour of its own removed vertices
+//             (degrees of vertices already removed are never read again).
+// Grid barriers: after the scan (reports) and after the removal (degrees, next live list).
+__global__ void __launch_bounds__(kPeelThreads, 1) peel_kernel(DevGraph g, long long limit_ns)
 {
     __shared__ int sh[32];
     const int tid = threadIdx.x, nthr = blockDim.x;
+    const int lane = tid & 31, wib = tid >> 5, wpb = nthr >> 5;
     const int n = g.n;
     for (int v = blockIdx.x * nthr + tid; v < n; v += gridDim.x * nthr) {
         g.deg[v] = g.offs[v + 1] - g.offs[v];
@@ -118,6 +119,7 @@ __global__ void __launch_bounds__(kPeelThreads) peel_kernel(DevGraph g, long lon
     int n_alive = n, k = 0, r = 0, pos = 0, phase = 0, dmax = 0;
     bool solo = false;
     int nb = gridDim.x, b = blockIdx.x;
+    const int tile = nthr * kPeelItems;
     while (n_alive > 0) {
         if (!solo && n_alive <= kPeelSoloVertices) {
             if (blockIdx.x != 0) return;
@@ -125,77 +127,151 @@ __global__ void __launch_bounds__(kPeelThreads) peel_kernel(DevGraph g, long lon
             nb = 1;
             b = 0;
         }
-        // -- count the vertices to remove at level k (and the smallest degree of the others)
         const int chunk = (n_alive + nb - 1) / nb;
         const int lo = min(b * chunk, n_alive), hi = min(lo + chunk, n_alive);
-        int cnt = 0, mn = INT_MAX;
-        for (int i = lo + tid; i < hi; i += nthr) {
-            const int dv = g.deg[alive[i]];
-            if (dv <= k) ++cnt;
-            else mn = min(mn, dv);
+        const bool in_regs = chunk <= tile;        // the same in every CTA
+        int vid[kPeelItems], vdg[kPeelItems];
+        // -- scan
+        int cnt_le = 0, mmin = INT_MAX, cnt_m = 0;
+        for (int t0 = lo; t0 < hi; t0 += tile) {
+#pragma unroll
+            for (int j = 0; j < kPeelItems; ++j) {
+                const int i = t0 + tid * kPeelItems + j;
+                vid[j] = i < hi ? alive[i] : -1;
+            }
+#pragma unroll
+            for (int j = 0; j < kPeelItems; ++j) vdg[j] = vid[j] >= 0 ? g.deg[vid[j]] : INT_MAX;
+#pragma unroll
+            for (int j = 0; j < kPeelItems; ++j) {
+                const int d = vdg[j];
+                if (vid[j] < 0) continue;
+                if (d <= k) ++cnt_le;
+                else if (d < mmin) { mmin = d; cnt_m = 1; }
+                else if (d == mmin) ++cnt_m;
+            }
         }
-        cnt = block_sum(cnt, sh);
-        mn = block_min(mn, sh);
-        int total, prefix, gmin;
+        // CTA report in one exchange: (#deg <= k, least degree above k, #at that degree)
+        __shared__ int s_rep[3][32];
+        __shared__ int s_dec[3];
+        {
+            const int wle = __reduce_add_sync(0xffffffffu, cnt_le);
+            const int wmin = __reduce_min_sync(0xffffffffu, mmin);
+            const int wcm = __reduce_add_sync(0xffffffffu, mmin == wmin ? cnt_m : 0);
+            if (lane == 0) { s_rep[0][wib] = wle; s_rep[1][wib] = wmin; s_rep[2][wib] = wcm; }
+            __syncthreads();
+            if (wib == 0) {
+                const int a0 = lane < wpb ? s_rep[0][lane] : 0;
+                const int a1 = lane < wpb ? s_rep[1][lane] : INT_MAX;
+                const int a2 = lane < wpb ? s_rep[2][lane] : 0;
+                const int bm = __reduce_min_sync(0xffffffffu, a1);
+                const int t_le = __reduce_add_sync(0xffffffffu, a0);
+                const int t_cm = __reduce_add_sync(0xffffffffu, a1 == bm ? a2 : 0);
+                if (lane == 0) { s_dec[0] = t_le; s_dec[1] = bm; s_dec[2] = t_cm; }
+            }
+            __syncthreads();
+        }
+        cnt_le = s_dec[0];
+        const int bmin = s_dec[1];
+        cnt_m = s_dec[2];
+        // -- decide (identically in every CTA)
+        int total, prefix, newk;
         if (solo) {
-            total = cnt;
+            if (cnt_le > 0) { newk = k; total = cnt_le; }
+            else { newk = bmin; total = cnt_m; }
             prefix = 0;
-            gmin = mn;
         } else {
             if (tid == 0) {
-                g.blk_cnt[phase * nb + b] = cnt;
-                g.blk_min[phase * nb + b] = mn;
+                g.blk_cnt[phase * nb + b] = cnt_le;
+                g.blk_min[phase * nb + b] = bmin;
+                g.blk_cm[phase * nb + b] = cnt_m;
             }
             if (!grid_barrier(g.ctrl, limit_ns)) return;
-            int t = 0, p = 0, m = INT_MAX;
-            for (int i = tid; i < nb; i += nthr) {
-                const int c = g.blk_cnt[phase * nb + i];
-                t += c;
-                if (i < b) p += c;
-                m = min(m, g.blk_min[phase * nb + i]);
+            // warp 0 reads every CTA's report
+            __shared__ int s_glob[3];
+            if (wib == 0) {
+                int tle = 0, ple = 0, gm = INT_MAX;
+                for (int i = lane; i < nb; i += 32) {
+                    const int c = g.blk_cnt[phase * nb + i];
+                    tle += c;
+                    if (i < b) ple += c;
+                    gm = min(gm, g.blk_min[phase * nb + i]);
+                }
+                tle = __reduce_add_sync(0xffffffffu, tle);
+                ple = __reduce_add_sync(0xffffffffu, ple);
+                gm = __reduce_min_sync(0xffffffffu, gm);
+                if (tle == 0) {
+                    int tm = 0, pm = 0;
+                    for (int i = lane; i < nb; i += 32) {
+                        const int c = g.blk_min[phase * nb + i] == gm ? g.blk_cm[phase * nb + i] : 0;
+                        tm += c;
+                        if (i < b) pm += c;
+                    }
+                    tle = __reduce_add_sync(0xffffffffu, tm);
+                    ple = __reduce_add_sync(0xffffffffu, pm);
+                } else {
+                    gm = k;
+                }
+                if (lane == 0) { s_glob[0] = tle; s_glob[1] = ple; s_glob[2] = gm; }
             }
-            total = block_sum(t, sh);
-            prefix = block_sum(p, sh);
-            gmin = block_min(m, sh);
+            __syncthreads();
+            total = s_glob[0];
+            prefix = s_glob[1];
+            newk = s_glob[2];
             phase ^= 1;
         }
-        if (total == 0) {            // nothing at level k: jump to the smallest remaining degree
-            k = max(k + 1, gmin);
-            continue;
-        }
+        k = newk;
         dmax = k;
-        // -- write this round's removals (id order) and the stably compacted survivors
-        int bf = pos + prefix, bs = lo - prefix;
-        for (int i0 = lo; i0 < hi; i0 += nthr) {
-            const int i = i0 + tid;
-            const bool valid = i < hi;
-            const int v = valid ? alive[i] : 0;
-            const bool f = valid && g.deg[v] <= k;
+        // -- write: this round's removals in id order, and the stably compacted survivors
+        __shared__ int s_front[kPeelThreads * kPeelItems];   // this CTA's removed vertices
+        const int my_first = pos + prefix;
+        int bf = my_first, bs = lo - prefix;
+        for (int t0 = lo; t0 < hi; t0 += tile) {
+            if (!in_regs) {
+#pragma unroll
+                for (int j = 0; j < kPeelItems; ++j) {
+                    const int i = t0 + tid * kPeelItems + j;
+                    vid[j] = i < hi ? alive[i] : -1;
+                    vdg[j] = vid[j] >= 0 ? g.deg[vid[j]] : INT_MAX;
+                }
+            }
+            int nf = 0, nv = 0;
+#pragma unroll
+            for (int j = 0; j < kPeelItems; ++j) {
+                nv += vid[j] >= 0;
+                nf += vid[j] >= 0 && vdg[j] <= k;
+            }
             int tot;
-            const int rf = block_excl_scan(f, &tot, sh);
-            if (f) {
-                const int p = bf + rf;
-                g.order[p] = v;
-                g.rank[v] = p;
-                g.round_of[v] = r;
-                g.core[v] = k;
-            } else if (valid) {
-                alive_next[bs + tid - rf] = v;
+            const int ex = block_excl_scan_int((nv << 16) | nf, &tot, sh);  // both < 2^16
+            const int rf = ex & 0xffff, rv = ex >> 16;
+            const int tf = tot & 0xffff, tv = tot >> 16;
+            int of = bf + rf, os = bs + (rv - rf);
+#pragma unroll
+            for (int j = 0; j < kPeelItems; ++j) {
+                const int v = vid[j];
+                if (v < 0) continue;
+                if (vdg[j] <= k) {
+                    g.order[of] = v;
+                    g.rank[v] = of;
+                    g.round_of[v] = r;
+                    g.core[v] = k;
+                    if (in_regs) s_front[of - my_first] = v;
+                    ++of;
+                } else {
+                    alive_next[os++] = v;
+                }
             }
-            bf += tot;
-            bs += min(nthr, hi - i0) - tot;
+            bf += tf;
+            bs += tv - tf;
         }
-        if (solo) __syncthreads();
+        // degrees re-read by the write step (slices longer than one tile) must not move before
+        // every CTA has written
+        if (in_regs || solo) __syncthreads();
         else if (!grid_barrier(g.ctrl, limit_ns)) return;
-        // -- remove them at once: every remaining neighbour loses one degree
-        const int lane = tid & 31, wib = tid >> 5, wpb = nthr >> 5;
-        for (int e = b * wpb + wib; e < total; e += nb * wpb) {
-            const int v = g.order[pos + e];
+        // -- remove this CTA's vertices: one warp per vertex, lanes over its neighbours
+        for (int e = wib; e < bf - my_first; e += wpb) {
+            const int v = in_regs ? s_front[e] : g.order[my_first + e];
             const int elo = g.offs[v], ehi = g.offs[v + 1];
-            for (int j = elo + lane; j < ehi; j += 32) {
-                const int u = g.adj[j];
-                if (g.round_of[u] < 0) atomicSub(&g.deg[u], 1);
-            }
+            for (int j = elo + lane; j < ehi; j += 32) atomicSub(&g.deg[g.adj[j]], 1);
         }
         if (solo) __syncthreads();
         else if (!grid_barrier(g.ctrl, limit_ns)) return;
@@ -301,34 +377,6 @@ __global__ void __launch_bounds__(kOrientThreads) orient_scatter_kernel(DevGraph
 }
 
 // ---- exclusive scan of an int array (three passes: CTA sums, scan of the sums, final)
-
-__device__ __forceinline__ int warp_incl_scan(int v, int lane)
-{
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += t;
-    }
-    return v;
-}
-
-// Exclusive scan of one value per thread over the CTA; *total = CTA sum.
-__device__ __forceinline__ int block_excl_scan_int(int v, int *total, int *sh)
-{
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    const int inc = warp_incl_scan(v, lane);
-    if (lane == 31) sh[w] = inc;
-    __syncthreads();
-    int before = 0, t = 0;
-    for (int i = 0; i < nw; ++i) {
-        const int c = sh[i];
-        if (i < w) before += c;
-        t += c;
-    }
-    __syncthreads();
-    *total = t;
-    return before + inc - v;
-}
 
 constexpr int kScanThreads = 256;   // 4 elements per thread
 
@@ -493,7 +541,7 @@ namespace {
 constexpr int kNoAllocMaxN = 1 << 18;        // vertices
 constexpr int kNoAllocMaxBlocks = 1024;      // CTAs of the cooperative peel
 constexpr int kNoAllocCtrlWords = (int)((sizeof(DevCtrl) + 255) / 256 * 64);
-constexpr int kNoAllocWords = kNoAllocCtrlWords + 4 * kNoAllocMaxBlocks + 5 * kNoAllocMaxN;
+constexpr int kNoAllocWords = kNoAllocCtrlWords + 6 * kNoAllocMaxBlocks + 5 * kNoAllocMaxN;
 constexpr int kNoAllocMaxDevices = 64;
 
 // The whole scratch area: 5 MiB + a few KiB, held by every device that loads the library.
@@ -556,7 +604,8 @@ extern "C" mce_status mce_order_noalloc(const int32_t *d_offsets, const int32_t 
     g.ctrl = reinterpret_cast<DevCtrl *>(base);
     g.blk_cnt = base + kNoAllocCtrlWords;
     g.blk_min = g.blk_cnt + 2 * kNoAllocMaxBlocks;
-    g.deg = g.blk_min + 2 * kNoAllocMaxBlocks;
+    g.blk_cm = g.blk_min + 2 * kNoAllocMaxBlocks;
+    g.deg = g.blk_cm + 2 * kNoAllocMaxBlocks;
     g.round_of = g.deg + kNoAllocMaxN;
     g.alive_a = g.round_of + kNoAllocMaxN;
     g.alive_b = g.alive_a + kNoAllocMaxN;
