@@ -639,6 +639,8 @@ __device__ void dfs(const SearchArgs &a, const RootCtx &r, Ck<Geo<W>::CH> P, Ck<
 
 // Per-warp shared memory of the build: open-addressing hash of P(v) (id -> local index) and
 // a staging row.
+constexpr int kBatch = 8;   // N+ entries a lane loads before probing them
+
 struct WarpSmem {
     int *hkey, *hval;
     unsigned *stage;
@@ -729,15 +731,21 @@ __device__ void search_root(const SearchArgs &a, unsigned *ws, const WarpSmem &s
         if (xi < r.nx) {
             const int u = r.xids[xi];
             const int s1 = __ldg(a.g.poffs + u + 1);
-            for (int e = __ldg(a.g.poffs + u); e < s1; ++e) {
-                const int j = hash_find(h, __ldg(a.g.padj + e));
-                if (j < 0) continue;
-                ++hits;
-                if constexpr (W <= 4) {
+            for (int e0 = __ldg(a.g.poffs + u); e0 < s1; e0 += kBatch) {
+                int w[kBatch];                           // independent loads in flight
 #pragma unroll
-                    for (int k = 0; k < W; ++k) reg[k] |= (j >> 5) == k ? 1u << (j & 31) : 0u;
-                } else {
-                    row[j >> 5] |= 1u << (j & 31);
+                for (int b = 0; b < kBatch; ++b) w[b] = e0 + b < s1 ? __ldg(a.g.padj + e0 + b) : -1;
+#pragma unroll
+                for (int b = 0; b < kBatch; ++b) {
+                    const int j = w[b] < 0 ? -1 : hash_find(h, w[b]);
+                    if (j < 0) continue;
+                    ++hits;
+                    if constexpr (W <= 4) {
+#pragma unroll
+                        for (int k = 0; k < W; ++k) reg[k] |= (j >> 5) == k ? 1u << (j & 31) : 0u;
+                    } else {
+                        row[j >> 5] |= 1u << (j & 31);
+                    }
                 }
             }
             if constexpr (W <= 4) {
@@ -764,9 +772,15 @@ __device__ void search_root(const SearchArgs &a, unsigned *ws, const WarpSmem &s
             const int u = r.pids[i];
             unsigned *row = r.rowsP + (long long)i * W;
             const int s1 = __ldg(a.g.poffs + u + 1);
-            for (int e = __ldg(a.g.poffs + u); e < s1; ++e) {
-                const int j = hash_find(h, __ldg(a.g.padj + e));
-                if (j >= 0) row[j >> 5] |= 1u << (j & 31);
+            for (int e0 = __ldg(a.g.poffs + u); e0 < s1; e0 += kBatch) {
+                int w[kBatch];
+#pragma unroll
+                for (int b = 0; b < kBatch; ++b) w[b] = e0 + b < s1 ? __ldg(a.g.padj + e0 + b) : -1;
+#pragma unroll
+                for (int b = 0; b < kBatch; ++b) {
+                    const int j = w[b] < 0 ? -1 : hash_find(h, w[b]);
+                    if (j >= 0) row[j >> 5] |= 1u << (j & 31);
+                }
             }
         }
     }
@@ -823,9 +837,12 @@ __device__ void search_inbox(const SearchArgs &a, unsigned *ws, Acc &acc,
 }
 
 // CTAs per SM the compiler should plan registers for, per row width (more for narrow rows).
+#ifndef MCE_MIN_BLOCKS_MID
+#define MCE_MIN_BLOCKS_MID 6
+#endif
 template <int W>
 struct MinBlocks {
-    static constexpr int value = W <= 2 ? 8 : (W <= 8 ? 6 : 4);
+    static constexpr int value = W <= 2 ? 8 : (W <= 8 ? MCE_MIN_BLOCKS_MID : 4);
 };
 
 // One persistent launch per row width W: the roots of that class, heaviest first, then
