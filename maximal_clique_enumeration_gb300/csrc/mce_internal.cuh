@@ -189,10 +189,18 @@ cudaError_t search_occupancy(int cls, int threads, size_t smem, int *blocks_per_
 // Shared memory of the search kernel of class k: the size histogram, then per warp a hash of
 // P(v) (ids and local indices) and a staging row.
 __host__ __device__ inline int hash_slots(int k) { return 64 << k; }
+// Rows of a root with deg * W <= smem_row_words(k) are built and searched in shared memory.
+__host__ __device__ inline int smem_row_words(int k) { return k <= 2 ? 1024 : 0; }
+// Per warp: hash keys and values, staging row (32 words), build cursor arrays (2 x 33 words),
+// rows.
+__host__ __device__ inline size_t warp_smem_bytes(int k)
+{
+    return (size_t)hash_slots(k) * 8 + 32 * 4 + 2 * 36 * 4 + (size_t)smem_row_words(k) * 4;
+}
 __host__ __device__ inline size_t search_smem_bytes(int k, int hist_len, int warps)
 {
     const size_t hist = ((size_t)(hist_len + 1) * 8 + 15) & ~(size_t)15;
-    return hist + (size_t)warps * ((size_t)hash_slots(k) * 8 + 32 * 4);
+    return hist + (size_t)warps * warp_smem_bytes(k);
 }
 cudaError_t search_configure(int cls, size_t smem);
 cudaError_t launch_bin_roots(const DevGraph &g, const int *roots, int n_roots, cudaStream_t s);

@@ -645,6 +645,9 @@ struct WarpSmem {
     int *hkey, *hval;
     unsigned *stage;
     int slots;
+    int *cur_start, *cur_base;   // build: per group of 32 neighbours, list starts and bases
+    unsigned *rows;              // rows of a root small enough for shared memory
+    int rows_words;
 };
 
 __device__ __forceinline__ unsigned hash_slot(int id, int mask)
@@ -664,6 +667,62 @@ __device__ __forceinline__ int hash_find(const WarpSmem &sm, int id)
     }
 }
 
+// Load-balanced build of all rows (normal roots).  The neighbours u_t of v (P first, then X)
+// are taken 32 at a time; the warp walks the concatenation of their lists N+(u_t) with
+// consecutive lanes on consecutive entries (coalesced), kBatch entries per lane in flight.  A
+// hit on p_j sets bit j of row t, and, when u_t = p_t is in P, bit t of row j as well.
+template <int W>
+__device__ void build_flat(const SearchArgs &a, const RootCtx &r, const WarpSmem &h, int deg,
+                           int np, int lane)
+{
+    unsigned *rows = r.rowsP;   // rowsX follows rowsP directly
+    for (int g0 = 0; g0 < deg; g0 += 32) {
+        const int t = g0 + lane;
+        int base = 0, len = 0;
+        if (t < deg) {
+            const int u = t < np ? r.pids[t] : r.xids[t - np];
+            base = __ldg(a.g.poffs + u);
+            len = __ldg(a.g.poffs + u + 1) - base;
+        }
+        int incl = len;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const int total = __shfl_sync(kFull, incl, 31);
+        h.cur_start[lane] = incl - len;
+        h.cur_base[lane] = base;
+        if (lane == 0) h.cur_start[32] = total;
+        __syncwarp();
+        int own = 0;
+        for (int f0 = 0; f0 < total; f0 += 32 * kBatch) {
+            int w[kBatch], ow[kBatch];
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+                const int f = f0 + b * 32 + lane;
+                ow[b] = -1;
+                w[b] = -1;
+                if (f < total) {
+                    while (h.cur_start[own + 1] <= f) ++own;
+                    ow[b] = own;
+                    w[b] = __ldg(a.g.padj + h.cur_base[own] + (f - h.cur_start[own]));
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+                if (ow[b] < 0) continue;
+                const int j = hash_find(h, w[b]);
+                if (j < 0) continue;
+                const int tt = g0 + ow[b];
+                atomicOr(rows + (long long)tt * W + (j >> 5), 1u << (j & 31));
+                if (tt < np) atomicOr(rows + (long long)j * W + (tt >> 5), 1u << (tt & 31));
+            }
+        }
+        __syncwarp();
+    }
+}
+
 // Builds the induced subgraph of root v into the warp's workspace and searches it.
 //
 // Rows: for u in N(v), row(u) has bit i set iff u is adjacent to the i-th vertex of P (the
@@ -674,7 +733,7 @@ __device__ __forceinline__ int hash_find(const WarpSmem &sm, int id)
 // reads the bounded lists N+(u) (each at most d long) with coalesced loads and no search.
 template <int W>
 __device__ void search_root(const SearchArgs &a, unsigned *ws, const WarpSmem &sm, int v, int deg,
-                            int np, Acc &acc, unsigned long long *s_hist, int lane)
+                            int np, bool big, Acc &acc, unsigned long long *s_hist, int lane)
 {
     constexpr int CH = Geo<W>::CH, G = Geo<W>::G;
     PROF_START(t_build);
@@ -696,9 +755,14 @@ __device__ void search_root(const SearchArgs &a, unsigned *ws, const WarpSmem &s
         pi += __popc(mp);
         xi += __popc(mx);
     }
-    // hash P(v); zero the P rows (X rows are written whole below, or zeroed for wide rows)
+    // rows in shared memory when they fit (normal roots only), else in the workspace; zero the
+    // rows (the big-root build writes X rows whole when they are at most 4 words wide)
+    if (!big && (long long)deg * W <= sm.rows_words) {
+        r.rowsP = sm.rows;
+        r.rowsX = sm.rows + (long long)np * W;
+    }
     {
-        const long long words = (long long)(W <= 4 ? np : deg) * W;
+        const long long words = (long long)(big && W <= 4 ? np : deg) * W;
         for (long long t = (long long)lane * CH; t < words; t += 32 * CH)
             ck_store<CH>(r.rowsP + t, ck_zero<CH>());
     }
@@ -716,11 +780,32 @@ __device__ void search_root(const SearchArgs &a, unsigned *ws, const WarpSmem &s
         h.hval[sl] = i;
     }
     __syncwarp();
+    int nxx = 0;
+    bool covered = false;
+    if (!big) {
+        build_flat<W>(a, r, h, deg, np, lane);
+        // X_X and the coverage test: a vertex of X adjacent to all of P makes every clique of
+        // this subtree extendable (it is the Tomita pivot of the root with P - N(pivot) empty),
+        // so the subtree holds no maximal clique
+        for (int base = 0; base < r.nx; base += 32) {
+            const int xi = base + lane;
+            int cnt = 0;
+            if (xi < r.nx)
+                for (int k = 0; k < W; ++k) cnt += __popc(r.rowsX[(long long)xi * W + k]);
+            covered = covered || __any_sync(kFull, cnt == np);
+            const unsigned m = __ballot_sync(kFull, cnt > 0);
+            if (cnt > 0) r.xx[nxx + __popc(m & lt)] = xi;
+            nxx += __popc(m);
+        }
+        if (covered) {
+            acc.nodes++;
+            PROF_ADD(acc, kProfBuild, t_build);
+            return;
+        }
+    } else {
     // X rows, one vertex per lane.  A vertex of X adjacent to all of P makes every clique of
     // this subtree extendable (it is the Tomita pivot of the root with P - N(pivot) empty):
     // the subtree holds no maximal clique and is abandoned as soon as one is seen.
-    int nxx = 0;
-    bool covered = false;
     for (int base = 0; base < r.nx && !covered; base += 32) {
         const int xi = base + lane;
         int hits = 0;
@@ -804,6 +889,7 @@ __device__ void search_root(const SearchArgs &a, unsigned *ws, const WarpSmem &s
             __syncwarp();
         }
     }
+    }
     for (int i = lane; i < np; i += 32) r.pkey[i] = vertex_key(r.pids[i]);
     __syncwarp();
     PROF_ADD(acc, kProfBuild, t_build);
@@ -860,12 +946,15 @@ __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(Search
     {
         constexpr int k = W == 1 ? 0 : W == 2 ? 1 : W == 4 ? 2 : W == 8 ? 3 : W == 16 ? 4 : 5;
         const size_t hist = ((size_t)(a.out.hist_len + 1) * 8 + 15) & ~(size_t)15;
-        unsigned char *mine = s_raw + hist +
-                              (size_t)(threadIdx.x >> 5) * ((size_t)hash_slots(k) * 8 + 128);
+        unsigned char *mine = s_raw + hist + (size_t)(threadIdx.x >> 5) * warp_smem_bytes(k);
         sm.hkey = reinterpret_cast<int *>(mine);
         sm.hval = sm.hkey + hash_slots(k);
         sm.stage = reinterpret_cast<unsigned *>(sm.hval + hash_slots(k));
         sm.slots = hash_slots(k);
+        sm.cur_start = reinterpret_cast<int *>(sm.stage + 32);
+        sm.cur_base = sm.cur_start + 36;
+        sm.rows = reinterpret_cast<unsigned *>(sm.cur_base + 36);   // 16-byte aligned
+        sm.rows_words = smem_row_words(k);
     }
     __syncthreads();
     unsigned *ws = a.ws + (unsigned long long)warp * a.ws_words;
@@ -900,7 +989,7 @@ __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(Search
         } else if (np > kMaxP) {
             if (lane == 0) set_status(a.g.ctrl, MCE_ERR_LIMIT);
         } else {
-            search_root<W>(a, ws, sm, v, deg, np, acc, s_hist, lane);
+            search_root<W>(a, ws, sm, v, deg, np, (a.group & 1) == 0, acc, s_hist, lane);
         }
         __syncwarp();
         if (lane == 0) busy.fetch_sub(1, cuda::memory_order_acq_rel);
