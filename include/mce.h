@@ -55,7 +55,9 @@ typedef enum mce_status {
  * Tuning knobs.  Fill with mce_config_default() and change fields; pass NULL for defaults.
  *   worker_list      1: warps that run out of first-level subtrees receive branches donated by
  *                    busy warps (Section 3.3); 0: static first-level distribution only.
- *   donate_min_p     a branch is donated only if |P| >= this at its root (Section 3.3 uses 10).
+ *   donate_min_p     a branch is donated only if |P| at its root is at least this (Section 3.3
+ *                    uses 10) and at least a quarter of |P| of its first-level subtree (copying
+ *                    a branch into another warp's workspace is not free).
  *   warps_per_block  warps per CTA of the search kernel (0 = library default).
  *   blocks_per_sm    CTAs per SM of the search kernel (0 = as many as can be resident).
  *   profile          1: record CUDA events around the ordering and around every search launch,

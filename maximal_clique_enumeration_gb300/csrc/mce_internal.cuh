@@ -32,10 +32,12 @@ struct DevCtrl {
     unsigned long long ws_grp[kNumGroups];    // the same per launch group
     unsigned long long next_root;  // search: root claim counter
     unsigned long long n_sched;    // search: number of scheduled roots
-    int busy;                    // worker list: warps holding work
-    int ring_head;               // worker list: pops
-    int ring_tail;               // worker list: pushes
-    int n_iso;                   // isolated vertices (cliques of size 1)
+    // worker list counters, each on its own 128-byte line: idle warps poll `busy` while donors
+    // update the ring
+    alignas(128) int busy;       // warps holding work
+    alignas(128) int ring_head;  // pops
+    alignas(128) int ring_tail;  // pushes
+    alignas(128) int n_iso;      // isolated vertices (cliques of size 1)
     int max_degree;              // Delta
     unsigned long long iso_hash; // hash contribution of the isolated vertices
     unsigned long long tree_nodes;

@@ -593,8 +593,10 @@ __device__ void dfs(const SearchArgs &a, const RootCtx &r, Ck<Geo<W>::CH> P, Ck<
         if (a.worker_list && (a.donate_rule ? (more_same || more_below)
                                             : (more_same && more_below))) {
             const long long now = __shfl_sync(kFull, (long long)clock64(), 0);
+            // a branch worth the copy: |P'| at least donate_min_p and a quarter of the root's P
+            const int min_p = a.donate_min_p > (r.np >> 2) ? a.donate_min_p : (r.np >> 2);
             if (now - last_check > kDonateCheckCycles &&
-                subwarp_sum<G>(ck_popc<CH>(Pc)) >= a.donate_min_p) {
+                subwarp_sum<G>(ck_popc<CH>(Pc)) >= min_p) {
                 last_check = now;
                 int recv = -1;
                 if (lane == 0) {
@@ -1009,14 +1011,16 @@ __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(Search
             if (!ring_push(a, warp)) state = 2;
             dev_int flag(a.flag[warp]);
             const unsigned long long t0 = globaltimer_ns();
-            unsigned ns = 64;
+            unsigned ns = 64, polls = 0;
             while (state == 0) {
                 const int f = flag.load(cuda::memory_order_acquire);
                 const long long waited = (long long)(globaltimer_ns() - t0);
                 if (f == kInboxFull) {
                     state = 1;
                 } else if (f == kInboxIdle) {
-                    if (busy.load(cuda::memory_order_acquire) == 0 || load_status(a.g.ctrl) != 0) {
+                    // the shared counters are read on every 8th poll only (own flag every time)
+                    if ((polls++ & 7u) == 0 &&
+                        (busy.load(cuda::memory_order_acquire) == 0 || load_status(a.g.ctrl) != 0)) {
                         state = 2;                       // nothing left anywhere
                     } else if (waited > a.spin_limit_ns) {
                         int expect = kInboxIdle;
