@@ -186,8 +186,12 @@ mce_status mce_get_order(mce_graph *g, void *stream, int32_t *d_rank, int32_t *d
  * row-width class k, at out[k * 8 + a] for activity a = 0 subtree build, 1 pivot selection,
  * 2 child sets and leaf checks, 3 X_X partition, 4 donation, 5 waiting in the worker list,
  * 6 the slowest single first-level root, 7 number of roots.  Section 4.5 of the pages breaks
- * execution time down the same way from per-block SM clocks.
- *   out  host uint64[8 * MCE_NUM_WIDTHS].  Synchronises the device.
+ * execution time down the same way from per-block SM clocks.  Then 16 values for the last
+ * ordering, as seen by its first CTA, in nanoseconds: out[48 + p] for rounds run by all CTAs and
+ * out[56 + p] for rounds run by one CTA, phase p = 0 scan, 1 report exchange, 2 decide and
+ * write, 3 edge removal, 4 end-of-round barrier, 5 number of rounds; out[54] is the largest
+ * degree of a vertex removed by the first CTA.
+ *   out  host uint64[8 * MCE_NUM_WIDTHS + 16].  Synchronises the device.
  */
 mce_status mce_get_profile(mce_graph *g, uint64_t *out);
 

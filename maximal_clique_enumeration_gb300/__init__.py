@@ -197,11 +197,17 @@ class Graph:
 
     def profile(self) -> dict:
         """Per row width: cycles per activity of the last search (MCE_PROFILE builds only)."""
-        out = np.zeros(8 * NUM_WIDTHS, np.uint64)
+        out = np.zeros(8 * NUM_WIDTHS + 16, np.uint64)
         _check(library().mce_get_profile(self._h, out.ctypes.data_as(ctypes.c_void_p)),
                "mce_get_profile")
-        return {1 << k: dict(zip(PROFILE_ACTIVITIES, (int(x) for x in out[8 * k: 8 * k + 8])))
-                for k in range(NUM_WIDTHS)}
+        res = {1 << k: dict(zip(PROFILE_ACTIVITIES, (int(x) for x in out[8 * k: 8 * k + 8])))
+               for k in range(NUM_WIDTHS)}
+        phases = ["scan_ns", "exchange_ns", "write_ns", "edges_ns", "barrier_ns", "rounds"]
+        base = 8 * NUM_WIDTHS
+        res["peel"] = {"multi": dict(zip(phases, (int(x) for x in out[base: base + 6]))),
+                       "single": dict(zip(phases, (int(x) for x in out[base + 8: base + 14]))),
+                       "max_removed_degree": int(out[base + 6])}
+        return res
 
     def order(self, stream=None):
         _check(library().mce_order(self._h, _stream_ptr(stream)), "mce_order")

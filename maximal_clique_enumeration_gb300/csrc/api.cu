@@ -275,6 +275,7 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
     MCE_ALLOC(h, g.blk_cnt, (size_t)2 * h->peel_blocks);
     MCE_ALLOC(h, g.blk_min, (size_t)2 * h->peel_blocks);
     MCE_ALLOC(h, g.blk_cm, (size_t)2 * h->peel_blocks);
+    MCE_ALLOC(h, g.blk_rd, (size_t)h->peel_blocks);
     if (h->cfg.profile) {
         MCE_TRY(cudaEventCreate(&h->ev_order[0]));
         MCE_TRY(cudaEventCreate(&h->ev_order[1]));
@@ -375,6 +376,7 @@ mce_status mce_create(const int32_t *offsets, const int32_t *adj, int32_t n, int
 static mce_status order_impl(mce_graph *h, cudaStream_t s)
 {
     h->count_cache_valid = false;
+    MCE_TRY(cudaMemsetAsync(h->g.ctrl->peel_prof, 0, sizeof(h->g.ctrl->peel_prof), s));
     if (h->cfg.profile) MCE_TRY(cudaEventRecord(h->ev_order[0], s));
     MCE_TRY(launch_order(h->g, h->peel_blocks, h->cfg.spin_limit_ns, s));
     if (h->cfg.profile) {
@@ -544,6 +546,8 @@ mce_status mce_get_profile(mce_graph *h, uint64_t *out)
     if (!h || !out) return MCE_ERR_INVALID_ARG;
     MCE_TRY(cudaDeviceSynchronize());
     MCE_TRY(cudaMemcpy(out, h->g.ctrl->prof, sizeof(h->g.ctrl->prof), cudaMemcpyDeviceToHost));
+    MCE_TRY(cudaMemcpy(out + 8 * kNumClasses, h->g.ctrl->peel_prof, sizeof(h->g.ctrl->peel_prof),
+                       cudaMemcpyDeviceToHost));
     return MCE_OK;
 }
 

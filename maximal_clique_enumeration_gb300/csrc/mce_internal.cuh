@@ -45,6 +45,7 @@ struct DevCtrl {
     unsigned long long result[2];  // count, hash of the last search
     unsigned long long words[kNumClasses];  // bitset words processed per row-width class
     unsigned long long prof[kNumClasses][8];  // MCE_PROFILE builds: cycles per activity
+    unsigned long long peel_prof[16];         // MCE_PROFILE builds: peel phases (ns, CTA 0)
     // first-level roots in launch groups g = 2k + b (row width W = 1 << k; b = 0: roots
     // whose workspace exceeds kWsCapWords, b = 1: the others): sched[cls[2g] .. cls[2g+1])
     // for the full schedule, uroots[ucls[2g] .. ucls[2g+1]) for a caller's root list
@@ -70,6 +71,7 @@ struct DevGraph {
     int *deg;         // peel scratch
     int *alive_a, *alive_b;
     int *blk_cnt, *blk_min, *blk_cm;   // peel per-CTA reports [2][grid]
+    long long *blk_rd;                 // peel: adjacency entries removed per CTA [grid]
     int *bucket;      // orient: schedule bucket histogram / cursors [kNumBuckets]
     int *ubucket;     // the same for a caller's root list [kNumBuckets]
     int *uroots;      // a caller's roots, grouped by row width, heaviest first

@@ -89,8 +89,29 @@ __device__ __forceinline__ int block_excl_scan_int(int v, int *total, int *sh)
     return before + inc - v;
 }
 
+// Phase timers of the MCE_PROFILE build (CTA 0, thread 0; nanoseconds): slot = phase, +8 when
+// the round runs in a single CTA.  Phases: 0 scan, 1 report exchange (barrier), 2 decide and
+// write, 3 edge removal, 4 end-of-round barrier, 5 rounds, 6 max edges of one removed vertex.
+#ifdef MCE_PROFILE
+#define PEEL_MARK(var) unsigned long long var = globaltimer_ns()
+#define PEEL_ADD(slot, var)                                                            \
+    do {                                                                               \
+        if (blockIdx.x == 0 && threadIdx.x == 0) {                                     \
+            const unsigned long long now_ = globaltimer_ns();                          \
+            g.ctrl->peel_prof[(slot) + (solo ? 8 : 0)] += now_ - (var);                \
+            var = now_;                                                                \
+        }                                                                              \
+    } while (0)
+#else
+#define PEEL_MARK(var) (void)0
+#define PEEL_ADD(slot, var) (void)0
+#endif
+
 // Each thread holds up to kPeelItems consecutive entries of its CTA's part of the live list.
 constexpr int kPeelItems = 8;
+constexpr int kPeelBigDegree = 1024;   // removed vertices this wide are handled by a whole CTA
+constexpr int kPeelBigQueue = 256;     // ... up to this many per round and CTA (then by warps)
+constexpr long long kPeelSoloEntries = 1 << 20;   // and the single-CTA finish needs few edges left
 
 // One round of the peel, in a CTA that owns live[lo, hi):
 //   scan   -- load ids and current degrees once (kept in registers across the exchange) and
@@ -117,16 +138,32 @@ __global__ void __launch_bounds__(kPeelThreads, 1) peel_kernel(DevGraph g, long 
 
     int *alive = g.alive_a, *alive_next = g.alive_b;
     int n_alive = n, k = 0, r = 0, pos = 0, phase = 0, dmax = 0;
+    long long live_entries = g.nnz;   // adjacency entries of the remaining vertices
     bool solo = false;
     int nb = gridDim.x, b = blockIdx.x;
     const int tile = nthr * kPeelItems;
+    __shared__ long long s_removed;
     while (n_alive > 0) {
-        if (!solo && n_alive <= kPeelSoloVertices) {
+        if (!solo && r > 0) {
+            // every CTA learns how many adjacency entries the last round removed
+            if (wib == 0) {
+                long long t = 0;
+                for (int i = lane; i < nb; i += 32) t += g.blk_rd[i];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+                if (lane == 0) s_removed = t;
+            }
+            __syncthreads();
+            live_entries -= s_removed;
+        }
+        // one CTA finishes once few vertices and few edges remain (a dense core keeps the grid)
+        if (!solo && n_alive <= kPeelSoloVertices && live_entries <= kPeelSoloEntries) {
             if (blockIdx.x != 0) return;
             solo = true;
             nb = 1;
             b = 0;
         }
+        PEEL_MARK(t_ph);
         const int chunk = (n_alive + nb - 1) / nb;
         const int lo = min(b * chunk, n_alive), hi = min(lo + chunk, n_alive);
         const bool in_regs = chunk <= tile;        // the same in every CTA
@@ -173,6 +210,7 @@ __global__ void __launch_bounds__(kPeelThreads, 1) peel_kernel(DevGraph g, long 
         cnt_le = s_dec[0];
         const int bmin = s_dec[1];
         cnt_m = s_dec[2];
+        PEEL_ADD(0, t_ph);
         // -- decide (identically in every CTA)
         int total, prefix, newk;
         if (solo) {
@@ -186,6 +224,7 @@ __global__ void __launch_bounds__(kPeelThreads, 1) peel_kernel(DevGraph g, long 
                 g.blk_cm[phase * nb + b] = cnt_m;
             }
             if (!grid_barrier(g.ctrl, limit_ns)) return;
+            PEEL_ADD(1, t_ph);
             // warp 0 reads every CTA's report
             __shared__ int s_glob[3];
             if (wib == 0) {
@@ -267,14 +306,56 @@ __global__ void __launch_bounds__(kPeelThreads, 1) peel_kernel(DevGraph g, long 
         // every CTA has written
         if (in_regs || solo) __syncthreads();
         else if (!grid_barrier(g.ctrl, limit_ns)) return;
-        // -- remove this CTA's vertices: one warp per vertex, lanes over its neighbours
+        PEEL_ADD(2, t_ph);
+        // -- remove this CTA's vertices: one warp per vertex, lanes over its neighbours; a vertex
+        // with kPeelBigDegree or more neighbours is queued and then handled by the whole CTA
+        __shared__ int s_big[kPeelBigQueue];
+        __shared__ int s_nbig;
+        __shared__ unsigned long long s_rd;       // adjacency entries this CTA removes
+        if (tid == 0) {
+            s_nbig = 0;
+            s_rd = 0ULL;
+        }
+        __syncthreads();
         for (int e = wib; e < bf - my_first; e += wpb) {
             const int v = in_regs ? s_front[e] : g.order[my_first + e];
             const int elo = g.offs[v], ehi = g.offs[v + 1];
+            if (lane == 0) atomicAdd(&s_rd, (unsigned long long)(ehi - elo));
+            if (ehi - elo >= kPeelBigDegree) {
+                int slot = 0;
+                if (lane == 0) slot = atomicAdd(&s_nbig, 1);
+                slot = __shfl_sync(0xffffffffu, slot, 0);
+                if (slot < kPeelBigQueue) {
+                    if (lane == 0) s_big[slot] = v;
+                    continue;
+                }
+            }
             for (int j = elo + lane; j < ehi; j += 32) atomicSub(&g.deg[g.adj[j]], 1);
+#ifdef MCE_PROFILE
+            if (lane == 0 && blockIdx.x == 0)
+                atomicMax(&g.ctrl->peel_prof[6], (unsigned long long)(ehi - elo));
+#endif
         }
+        __syncthreads();
+        const int nbig = min(s_nbig, kPeelBigQueue);
+        for (int i = 0; i < nbig; ++i) {
+            const int v = s_big[i];
+            const int elo = g.offs[v], ehi = g.offs[v + 1];
+            for (int j = elo + tid; j < ehi; j += nthr) atomicSub(&g.deg[g.adj[j]], 1);
+#ifdef MCE_PROFILE
+            if (tid == 0 && blockIdx.x == 0)
+                atomicMax(&g.ctrl->peel_prof[6], (unsigned long long)(ehi - elo));
+#endif
+        }
+        if (!solo && tid == 0) g.blk_rd[b] = (long long)s_rd;
+        __syncthreads();
+        PEEL_ADD(3, t_ph);
         if (solo) __syncthreads();
         else if (!grid_barrier(g.ctrl, limit_ns)) return;
+        PEEL_ADD(4, t_ph);
+#ifdef MCE_PROFILE
+        if (blockIdx.x == 0 && tid == 0) g.ctrl->peel_prof[5 + (solo ? 8 : 0)]++;
+#endif
         pos += total;
         n_alive -= total;
         ++r;
@@ -541,7 +622,7 @@ namespace {
 constexpr int kNoAllocMaxN = 1 << 18;        // vertices
 constexpr int kNoAllocMaxBlocks = 1024;      // CTAs of the cooperative peel
 constexpr int kNoAllocCtrlWords = (int)((sizeof(DevCtrl) + 255) / 256 * 64);
-constexpr int kNoAllocWords = kNoAllocCtrlWords + 6 * kNoAllocMaxBlocks + 5 * kNoAllocMaxN;
+constexpr int kNoAllocWords = kNoAllocCtrlWords + 8 * kNoAllocMaxBlocks + 5 * kNoAllocMaxN;
 constexpr int kNoAllocMaxDevices = 64;
 
 // The whole scratch area: 5 MiB + a few KiB, held by every device that loads the library.
@@ -605,7 +686,8 @@ extern "C" mce_status mce_order_noalloc(const int32_t *d_offsets, const int32_t 
     g.blk_cnt = base + kNoAllocCtrlWords;
     g.blk_min = g.blk_cnt + 2 * kNoAllocMaxBlocks;
     g.blk_cm = g.blk_min + 2 * kNoAllocMaxBlocks;
-    g.deg = g.blk_cm + 2 * kNoAllocMaxBlocks;
+    g.blk_rd = reinterpret_cast<long long *>(g.blk_cm + 2 * kNoAllocMaxBlocks);
+    g.deg = g.blk_cm + 4 * kNoAllocMaxBlocks;
     g.round_of = g.deg + kNoAllocMaxN;
     g.alive_a = g.round_of + kNoAllocMaxN;
     g.alive_b = g.alive_a + kNoAllocMaxN;
