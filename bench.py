@@ -68,6 +68,8 @@ def parse_args():
                    help="share of the workload roots the oracle baseline counts")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--induced", type=int, default=0, choices=[0, 1, 2],
+                   help="induced subgraphs: 0 the Delta/d rule (default), 1 full, 2 partial")
     return p.parse_args()
 
 
@@ -126,6 +128,7 @@ def workload_config(args, g, roots, pc, d):
         "roots_left_out": int((pc >= args.max_p).sum()),
         "root_fraction": args.root_fraction,
         "l2": "flushed between steps (256 MiB write, untimed)",
+        "induced": {0: "Delta/d rule", 1: "full", 2: "partial"}[getattr(args, "induced", 0)],
     }
 
 
@@ -210,7 +213,7 @@ def run_gb300(args, rank, world, local):
     g = workload_graph(args)
     dev_offs = torch.from_numpy(g.offsets).cuda()
     dev_adj = torch.from_numpy(g.adj).cuda()
-    h = mce.Graph(dev_offs, dev_adj, g.n, profile=1)
+    h = mce.Graph(dev_offs, dev_adj, g.n, profile=1, induced=args.induced)
     rank_arr, _ = h.order_arrays()
     roots, pc = light_roots(g, rank_arr.cpu().numpy(), args.max_p)
     if args.root_fraction < 1.0:
@@ -291,7 +294,8 @@ def run_gb300(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "ms_per_graph": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
         "data": "synthetic (seeded R-MAT generator)",
-        "config": workload_config(args, g, roots, pc, h.info["degeneracy"]),
+        "config": dict(workload_config(args, g, roots, pc, h.info["degeneracy"]),
+                       induced={1: "full", 2: "partial"}[h.info["induced"]]),
         "result": {"cliques": res[0], "hash": f"{res[1]:#018x}", "max_size": len(res[2]) - 1},
         "stage_ms": {"order": ms_order / args.steps,
                      "search_by_width": {str(1 << i): float(ms_cls[i] / args.steps)
@@ -332,7 +336,7 @@ def e2e_leg(args, g, roots, world):
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        h = mce.Graph(offs, adj, g.n)                 # host pointers: the library copies them in
+        h = mce.Graph(offs, adj, g.n, induced=args.induced)   # host pointers: copied in
         r = roots_h.to("cuda", non_blocking=True)
         out = h.count_roots(r)
         res_h = out.to("cpu", non_blocking=True)

@@ -69,6 +69,13 @@ typedef enum mce_status {
  *                    MCE_ERR_DEVICE_TIMEOUT and returns instead of hanging (an idle warp
  *                    that waited this long instead leaves the worker list, which is not an
  *                    error).
+ *   induced          induced subgraph of a subtree (Section 3.4): 1 = full (bitset rows for
+ *                    every vertex of P u X; pivot from P u X), 2 = partial (rows for P only;
+ *                    P-X adjacencies are binary searches in the graph; pivot from P u X_P),
+ *                    0 (default) = the rule of Section 4.5: partial iff Delta / d > 200.
+ *   subtree_level    1 (default): independent first-level subtrees, one per vertex
+ *                    (Algorithm 3); 2: independent second-level subtrees, one per edge
+ *                    (Algorithm 4, Section 3.2).  Other values: MCE_ERR_INVALID_ARG.
  */
 typedef struct mce_config {
     int32_t worker_list;
@@ -78,6 +85,8 @@ typedef struct mce_config {
     int32_t profile;
     int32_t donate_rule;
     int64_t spin_limit_ns;
+    int32_t induced;
+    int32_t subtree_level;
 } mce_config;
 
 #define MCE_NUM_WIDTHS 6   /* search kernels, one per bitset row width 1, 2, 4, 8, 16, 32 words */
@@ -102,6 +111,8 @@ typedef struct mce_info {
     float ms_search[MCE_NUM_WIDTHS];   /* device time per class launch (profile = 1 only)    */
     float ms_order;                    /* device time of the last mce_order/mce_create order */
     int32_t launches;                  /* kernels launched by the last order + count calls   */
+    int32_t induced;                   /* induced subgraph in use: 1 full, 2 partial         */
+    int32_t subtree_level;             /* 1: first-level subtrees, 2: second-level subtrees  */
 } mce_info;
 
 /* Writes the default configuration into *cfg.  Returns MCE_ERR_INVALID_ARG if cfg is NULL. */

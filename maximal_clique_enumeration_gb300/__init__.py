@@ -45,7 +45,8 @@ class Config(ctypes.Structure):
     _fields_ = [("worker_list", ctypes.c_int32), ("donate_min_p", ctypes.c_int32),
                 ("warps_per_block", ctypes.c_int32), ("blocks_per_sm", ctypes.c_int32),
                 ("profile", ctypes.c_int32), ("donate_rule", ctypes.c_int32),
-                ("spin_limit_ns", ctypes.c_int64)]
+                ("spin_limit_ns", ctypes.c_int64), ("induced", ctypes.c_int32),
+                ("subtree_level", ctypes.c_int32)]
 
 
 class Info(ctypes.Structure):
@@ -56,7 +57,8 @@ class Info(ctypes.Structure):
                 ("donations", ctypes.c_uint64), ("words", ctypes.c_uint64 * NUM_WIDTHS),
                 ("roots", ctypes.c_int32 * NUM_WIDTHS), ("workers", ctypes.c_int32 * NUM_WIDTHS),
                 ("ms_search", ctypes.c_float * NUM_WIDTHS), ("ms_order", ctypes.c_float),
-                ("launches", ctypes.c_int32)]
+                ("launches", ctypes.c_int32), ("induced", ctypes.c_int32),
+                ("subtree_level", ctypes.c_int32)]
 
     def as_dict(self):
         out = {}

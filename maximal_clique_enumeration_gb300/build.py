@@ -13,7 +13,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libmce_gb300.so")
 PROBE_PATH = os.path.join(BUILD_DIR, "libmce_probe.so")
-SOURCES = ["api.cu", "ingest.cu", "order.cu", "search.cu"]
+SOURCES = ["api.cu", "ingest.cu", "order.cu", "search.cu", "search_full.cu", "search_partial.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          f"-I{INCLUDE}", f"-I{CSRC}"]
@@ -91,8 +91,8 @@ def _build_variant(out_dir: str, flags, verbose: bool) -> str:
         objs.append(obj)
         cmd = [nvcc, *ARCH, *FLAGS, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
         procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
-    errors = [f"--- {src}\n{p.communicate()[0].decode(errors='replace')}" for src, p in procs
-              if p.wait() != 0]
+    outs = [(src, p.communicate()[0], p.returncode) for src, p in procs]
+    errors = [f"--- {src}\n{out.decode(errors='replace')}" for src, out, rc in outs if rc != 0]
     if errors:
         raise RuntimeError("nvcc failed:\n" + "\n".join(errors))
     out = os.path.join(out_dir, "libmce_gb300.so")

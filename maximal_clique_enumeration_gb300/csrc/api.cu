@@ -169,6 +169,8 @@ mce_status mce_config_default(mce_config *cfg)
     cfg->profile = 0;
     cfg->donate_rule = 0;
     cfg->spin_limit_ns = 20LL * 1000 * 1000 * 1000;
+    cfg->induced = 0;
+    cfg->subtree_level = 1;
     return MCE_OK;
 }
 
@@ -284,6 +286,7 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
             MCE_TRY(cudaEventCreate(&h->ev_grp[k][1]));
         }
     }
+    g.ip = h->cfg.induced == 2 ? 1 : 0;
     {
         mce_status so = order_impl(h, s);
         if (so != MCE_OK) return so;
@@ -292,6 +295,19 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
     if (st != MCE_OK) return st;
     DevCtrl c{};
     MCE_TRY(cudaMemcpy(&c, g.ctrl, sizeof(DevCtrl), cudaMemcpyDeviceToHost));
+    // induced subgraphs (Section 4.5): partial when Delta / d > 200, full otherwise, unless the
+    // configuration fixes one; the schedule and workspace sizes depend on it, so a change of
+    // mode orders once more
+    const int ip = h->cfg.induced == 2 ||
+                   (h->cfg.induced == 0 && (long long)c.max_degree > 200LL * c.degeneracy);
+    if (ip != g.ip) {
+        g.ip = ip;
+        mce_status so = order_impl(h, s);
+        if (so != MCE_OK) return so;
+        st = read_status(h, s);
+        if (st != MCE_OK) return st;
+        MCE_TRY(cudaMemcpy(&c, g.ctrl, sizeof(DevCtrl), cudaMemcpyDeviceToHost));
+    }
     h->degeneracy = c.degeneracy;
     h->rounds = c.rounds;
     h->max_degree = c.max_degree;
@@ -307,8 +323,8 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
     int class_per_sm[kNumClasses] = {};
     for (int k = 0; k < kNumClasses; ++k) {
         h->cls_smem[k] = search_smem_bytes(k, h->hist_len, wpb);
-        MCE_TRY(search_configure(k, h->cls_smem[k]));
-        MCE_TRY(search_occupancy(k, h->search_threads, h->cls_smem[k], &class_per_sm[k]));
+        MCE_TRY(search_configure(k, g.ip, h->cls_smem[k]));
+        MCE_TRY(search_occupancy(k, g.ip, h->search_threads, h->cls_smem[k], &class_per_sm[k]));
         if (class_per_sm[k] < 1) return MCE_ERR_CUDA;
         if (h->cfg.blocks_per_sm > 0 && h->cfg.blocks_per_sm < class_per_sm[k])
             class_per_sm[k] = h->cfg.blocks_per_sm;
@@ -360,6 +376,10 @@ mce_status mce_create(const int32_t *offsets, const int32_t *adj, int32_t n, int
     if (cfg) h->cfg = *cfg;
     else mce_config_default(&h->cfg);
     if (h->cfg.donate_min_p < 1) h->cfg.donate_min_p = 1;
+    if (h->cfg.induced < 0 || h->cfg.induced > 2 || h->cfg.subtree_level != 1) {
+        delete h;
+        return MCE_ERR_INVALID_ARG;
+    }
     if (h->cfg.spin_limit_ns <= 0) h->cfg.spin_limit_ns = 20LL * 1000 * 1000 * 1000;
     mce_status st = create_impl(h, offsets, adj, n, is_device_ptr, (cudaStream_t)stream);
     if (st != MCE_OK) {
@@ -519,6 +539,8 @@ mce_status mce_get_info(mce_graph *h, mce_info *info)
     info->peel_rounds = c.rounds;
     info->n_workers = h->n_workers;
     info->workspace_bytes = (long long)(h->ws_words * 4ULL);
+    info->induced = h->g.ip ? 2 : 1;
+    info->subtree_level = 1;
     info->tree_nodes = c.tree_nodes;
     info->donations = c.donations;
     for (int k = 0; k < kNumClasses; ++k) {

@@ -72,6 +72,7 @@ struct DevGraph {
     int *alive_a, *alive_b;
     int *blk_cnt, *blk_min, *blk_cm;   // peel per-CTA reports [2][grid]
     long long *blk_rd;                 // peel: adjacency entries removed per CTA [grid]
+    int ip;           // search over partial induced subgraphs (rows for P only), Section 3.4
     int *bucket;      // orient: schedule bucket histogram / cursors [kNumBuckets]
     int *ubucket;     // the same for a caller's root list [kNumBuckets]
     int *uroots;      // a caller's roots, grouped by row width, heaviest first
@@ -132,14 +133,14 @@ struct WsLayout {
     int W, LV;
 };
 
-__host__ __device__ inline WsLayout ws_layout(int deg, int np)
+__host__ __device__ inline WsLayout ws_layout(int deg, int np, bool ip)
 {
     WsLayout l;
     const int nx = deg - np;
     l.W = wclass(np);
     long long o = kWsHeader;
     l.rowsP = o; o += (long long)np * l.W;       // rows of P vertices, columns over P
-    l.rowsX = o; o += (long long)nx * l.W;       // rows of X vertices, columns over P
+    l.rowsX = o; o += ip ? 0 : (long long)nx * l.W;   // rows of X vertices (full subgraphs only)
     l.pids = o; o += np;                         // original ids of P vertices (ascending)
     o = (o + 1) & ~1LL;
     l.pkey = o; o += 2LL * np;                   // vertex keys of P vertices (uint64)
@@ -165,11 +166,11 @@ constexpr int kNumBuckets = 1 + kNumGroups * kCostBuckets;
 __host__ __device__ inline int group_at(int o) { return 2 * (kNumClasses - 1 - o / 2) + (o & 1); }
 __host__ __device__ inline int position_of(int g) { return 2 * (kNumClasses - 1 - g / 2) + (g & 1); }
 
-__device__ inline int sched_bucket(int np, int deg)
+__device__ inline int sched_bucket(int np, int deg, bool ip)
 {
     if (np > kMaxP) return 0;
     const int k = wclass_index(np);
-    const int b = np > 0 && ws_layout(deg, np).total > kWsCapWords ? 0 : 1;
+    const int b = np > 0 && ws_layout(deg, np, ip).total > kWsCapWords ? 0 : 1;
     const unsigned long long est = (unsigned long long)deg * (unsigned long long)(np + 1);
     int lb = est ? 63 - __clzll((long long)est) : 0;
     lb = lb < kCostBuckets - 1 ? lb : kCostBuckets - 1;
@@ -189,7 +190,7 @@ cudaError_t launch_order(const DevGraph &g, int peel_blocks, long long spin_limi
 cudaError_t launch_search(const SearchArgs &a, int blocks, int threads, size_t smem,
                           cudaStream_t s);
 cudaError_t launch_search_prep(const SearchArgs &a, cudaStream_t s);
-cudaError_t search_occupancy(int cls, int threads, size_t smem, int *blocks_per_sm);
+cudaError_t search_occupancy(int cls, int ip, int threads, size_t smem, int *blocks_per_sm);
 // Shared memory of the search kernel of class k: the size histogram, then per warp a hash of
 // P(v) (ids and local indices) and a staging row.
 __host__ __device__ inline int hash_slots(int k) { return 64 << k; }
@@ -206,7 +207,7 @@ __host__ __device__ inline size_t search_smem_bytes(int k, int hist_len, int war
     const size_t hist = ((size_t)(hist_len + 1) * 8 + 15) & ~(size_t)15;
     return hist + (size_t)warps * warp_smem_bytes(k);
 }
-cudaError_t search_configure(int cls, size_t smem);
+cudaError_t search_configure(int cls, int ip, size_t smem);
 cudaError_t launch_bin_roots(const DevGraph &g, const int *roots, int n_roots, cudaStream_t s);
 cudaError_t launch_finalize(const DevGraph &g, const DevOut &o, unsigned long long *d_out,
                             int include_isolated, cudaStream_t s);

@@ -398,10 +398,10 @@ __global__ void __launch_bounds__(kOrientThreads) orient_count_kernel(DevGraph g
                 iso_hash += mix64(vertex_key(v));
             }
             if (c > 0) {
-                atomicAdd(&s_bucket[sched_bucket(c, deg)], 1);
+                atomicAdd(&s_bucket[sched_bucket(c, deg, g.ip)], 1);
                 maxp = max(maxp, c);
                 if (c <= kMaxP) {
-                    const unsigned long long need = (unsigned long long)ws_layout(deg, c).total;
+                    const unsigned long long need = (unsigned long long)ws_layout(deg, c, g.ip).total;
                     ws = need > ws ? need : ws;
                     const int gi = 2 * wclass_index(c) + (need > (unsigned long long)kWsCapWords ? 0 : 1);
                     ws_grp[gi] = need > ws_grp[gi] ? need : ws_grp[gi];
@@ -453,7 +453,7 @@ __global__ void __launch_bounds__(kOrientThreads) orient_scatter_kernel(DevGraph
 {
     for (int v = blockIdx.x * blockDim.x + threadIdx.x; v < g.n; v += gridDim.x * blockDim.x) {
         const int c = g.pcount[v];
-        if (c > 0) g.sched[atomicAdd(&g.bucket[sched_bucket(c, g.offs[v + 1] - g.offs[v])], 1)] = v;
+        if (c > 0) g.sched[atomicAdd(&g.bucket[sched_bucket(c, g.offs[v + 1] - g.offs[v], g.ip)], 1)] = v;
     }
 }
 
@@ -536,7 +536,7 @@ __global__ void __launch_bounds__(kOrientThreads) bin_count_kernel(DevGraph g, c
             set_status(g.ctrl, MCE_ERR_ID_RANGE);
             continue;
         }
-        atomicAdd(&g.ubucket[sched_bucket(g.pcount[v], g.offs[v + 1] - g.offs[v])], 1);
+        atomicAdd(&g.ubucket[sched_bucket(g.pcount[v], g.offs[v + 1] - g.offs[v], g.ip)], 1);
     }
 }
 
@@ -552,7 +552,7 @@ __global__ void __launch_bounds__(kOrientThreads) bin_scatter_kernel(DevGraph g,
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_roots; i += gridDim.x * blockDim.x) {
         const int v = roots[i];
         if (v < 0 || v >= g.n) continue;
-        g.uroots[atomicAdd(&g.ubucket[sched_bucket(g.pcount[v], g.offs[v + 1] - g.offs[v])], 1)] = v;
+        g.uroots[atomicAdd(&g.ubucket[sched_bucket(g.pcount[v], g.offs[v + 1] - g.offs[v], g.ip)], 1)] = v;
     }
 }
 

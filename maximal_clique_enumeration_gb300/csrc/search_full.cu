@@ -1,0 +1,19 @@
+// Search kernels over full induced subgraphs, one per row width.
+#define MCE_SEARCH_IP 0
+#include "search_impl.cuh"
+
+namespace mce {
+
+const void *search_kernel_full(int cls)
+{
+    switch (cls) {
+    case 0: return (const void *)search_kernel<1>;
+    case 1: return (const void *)search_kernel<2>;
+    case 2: return (const void *)search_kernel<4>;
+    case 3: return (const void *)search_kernel<8>;
+    case 4: return (const void *)search_kernel<16>;
+    default: return (const void *)search_kernel<32>;
+    }
+}
+
+}  // namespace mce

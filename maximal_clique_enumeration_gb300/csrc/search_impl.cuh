@@ -1,0 +1,1122 @@
+// Device code of the search (included by search_full.cu and search_partial.cu, which
+// instantiate its kernels).
+//
+// The search: Bron-Kerbosch with Tomita pivoting over independent first-level subtrees, one
+// subtree per warp ("Parallelizing Maximal Clique Enumeration on GPUs", Sections 2.3-2.4 and 3).
+//
+// GB300 mapping (the pages assign a subtree to a thread block; here a warp is the unit of
+// work, so that the many small subtrees of sparse graphs do not pay for block-wide barriers):
+//   * one persistent kernel, as many CTAs as can be resident (Section 3.3); every warp claims
+//     first-level roots from a global counter, heaviest |P| first;
+//   * per root v, the warp builds the binary-encoded induced subgraph over P u X
+//     (Sections 2.4 "Induced Subgraphs" and 3.4, the full variant): one bitset row per vertex
+//     of N(v), with one column per vertex of P = later neighbours;
+//   * X is kept compact (Section 3.5): X_P is a per-level bitset over the P columns, X_X a
+//     single list of X rows that is partitioned in place as the search descends, with the end
+//     of each level's part saved in its stack entry;
+//   * the depth-first search is iterative with an explicit stack in the warp's workspace;
+//     bitsets are spread over "sub-warps" of G lanes, each lane holding one 16-byte chunk of a
+//     row (W <= 4 words: G = 1, every lane holds a whole row), so that row loads are 128-bit
+//     and a pivot step scores 32/G rows at once; popcounts are reduced with shuffles.
+// Rows, lists and the stack live in global memory (served by L1/L2); each warp has its own
+// workspace sized at mce_create for the largest root of the graph.
+#pragma once
+
+#include <climits>
+
+#include <cuda/atomic>
+
+#include "mce_internal.cuh"
+
+// Which induced subgraph the including translation unit builds (Section 3.4): 0 = full (rows
+// for every vertex of P u X), 1 = partial (rows for P only; P-X adjacencies are looked up in
+// the original graph, and the pivot comes from P u X_P).
+#ifndef MCE_SEARCH_IP
+#error "define MCE_SEARCH_IP before including search_impl.cuh"
+#endif
+
+namespace mce {
+
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr bool kIP = MCE_SEARCH_IP != 0;
+
+template <int W>
+struct Geo {
+    static constexpr int CH = W < 4 ? W : 4;   // words per lane chunk
+    static constexpr int G = W / CH;           // lanes per row
+    static constexpr int R = 32 / G;           // rows per warp step
+};
+
+template <int CH>
+struct Ck {
+    unsigned w[CH];
+};
+
+template <int CH>
+__device__ __forceinline__ Ck<CH> ck_zero()
+{
+    Ck<CH> c;
+#pragma unroll
+    for (int i = 0; i < CH; ++i) c.w[i] = 0u;
+    return c;
+}
+
+template <int CH>
+__device__ __forceinline__ Ck<CH> ck_load(const unsigned *p)
+{
+    Ck<CH> c;
+    if constexpr (CH == 4) {
+        const uint4 t = *reinterpret_cast<const uint4 *>(p);
+        c.w[0] = t.x; c.w[1] = t.y; c.w[2] = t.z; c.w[3] = t.w;
+    } else if constexpr (CH == 2) {
+        const uint2 t = *reinterpret_cast<const uint2 *>(p);
+        c.w[0] = t.x; c.w[1] = t.y;
+    } else {
+        c.w[0] = *p;
+    }
+    return c;
+}
+
+template <int CH>
+__device__ __forceinline__ void ck_store(unsigned *p, const Ck<CH> &c)
+{
+    if constexpr (CH == 4) {
+        *reinterpret_cast<uint4 *>(p) = make_uint4(c.w[0], c.w[1], c.w[2], c.w[3]);
+    } else if constexpr (CH == 2) {
+        *reinterpret_cast<uint2 *>(p) = make_uint2(c.w[0], c.w[1]);
+    } else {
+        *p = c.w[0];
+    }
+}
+
+template <int CH>
+__device__ __forceinline__ Ck<CH> ck_and(const Ck<CH> &a, const Ck<CH> &b)
+{
+    Ck<CH> c;
+#pragma unroll
+    for (int i = 0; i < CH; ++i) c.w[i] = a.w[i] & b.w[i];
+    return c;
+}
+
+template <int CH>
+__device__ __forceinline__ Ck<CH> ck_andnot(const Ck<CH> &a, const Ck<CH> &b)
+{
+    Ck<CH> c;
+#pragma unroll
+    for (int i = 0; i < CH; ++i) c.w[i] = a.w[i] & ~b.w[i];
+    return c;
+}
+
+template <int CH>
+__device__ __forceinline__ Ck<CH> ck_or(const Ck<CH> &a, const Ck<CH> &b)
+{
+    Ck<CH> c;
+#pragma unroll
+    for (int i = 0; i < CH; ++i) c.w[i] = a.w[i] | b.w[i];
+    return c;
+}
+
+template <int CH>
+__device__ __forceinline__ bool ck_nonzero(const Ck<CH> &a)
+{
+    unsigned t = 0;
+#pragma unroll
+    for (int i = 0; i < CH; ++i) t |= a.w[i];
+    return t != 0;
+}
+
+template <int CH>
+__device__ __forceinline__ int ck_popc(const Ck<CH> &a)
+{
+    int t = 0;
+#pragma unroll
+    for (int i = 0; i < CH; ++i) t += __popc(a.w[i]);
+    return t;
+}
+
+// Sum over the G lanes of a sub-warp (all lanes get the sum).
+template <int G>
+__device__ __forceinline__ int subwarp_sum(int x)
+{
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
+    return x;
+}
+
+template <int G>
+__device__ __forceinline__ int subwarp_min(int x)
+{
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) x = min(x, __shfl_xor_sync(kFull, x, o));
+    return x;
+}
+
+// The bitset with bits [0, np) set, in chunk layout (lane chunk q holds words q*CH ..).
+template <int W>
+__device__ __forceinline__ Ck<Geo<W>::CH> bits_prefix(int np, int q)
+{
+    constexpr int CH = Geo<W>::CH;
+    Ck<CH> c;
+#pragma unroll
+    for (int i = 0; i < CH; ++i) {
+        const int k = q * CH + i;
+        const int lo = k * 32;
+        c.w[i] = np >= lo + 32 ? kFull : (np > lo ? ((1u << (np - lo)) - 1u) : 0u);
+    }
+    return c;
+}
+
+// Bits of `c` with index < b.
+template <int W>
+__device__ __forceinline__ Ck<Geo<W>::CH> bits_below(const Ck<Geo<W>::CH> &c, int b, int q)
+{
+    constexpr int CH = Geo<W>::CH;
+    Ck<CH> r;
+    const int wb = b >> 5;
+    const unsigned m = (1u << (b & 31)) - 1u;
+#pragma unroll
+    for (int i = 0; i < CH; ++i) {
+        const int k = q * CH + i;
+        r.w[i] = k < wb ? c.w[i] : (k == wb ? (c.w[i] & m) : 0u);
+    }
+    return r;
+}
+
+// Index of the lowest set bit of `c` above `after` (after = -1: the lowest), or INT_MAX.
+template <int W>
+__device__ __forceinline__ int lowest_above(const Ck<Geo<W>::CH> &c, int after, int q)
+{
+    constexpr int CH = Geo<W>::CH;
+    int best = INT_MAX;
+#pragma unroll
+    for (int i = CH - 1; i >= 0; --i) {
+        const int k = q * CH + i;
+        unsigned w = c.w[i];
+        const int lo = k * 32;
+        if (after >= lo + 31) w = 0u;
+        else if (after >= lo) w &= ~((2u << (after - lo)) - 1u);
+        if (w) best = lo + __ffs(w) - 1;
+    }
+    return subwarp_min<Geo<W>::G>(best);
+}
+
+struct Acc {
+    unsigned long long count, hash, nodes, donations;
+    unsigned long long words;   // bitset words scored / intersected / tested (lane 0 counts)
+#ifdef MCE_PROFILE
+    unsigned long long prof[8];
+#endif
+};
+
+// Activity timers of the MCE_PROFILE build (no code otherwise).
+#ifdef MCE_PROFILE
+#define PROF_START(var) const long long var = clock64()
+#define PROF_ADD(acc, slot, var) ((acc).prof[slot] += (unsigned long long)(clock64() - (var)))
+#else
+#define PROF_START(var) (void)0
+#define PROF_ADD(acc, slot, var) (void)0
+#endif
+enum { kProfBuild = 0, kProfPivot, kProfChild, kProfPartition, kProfDonate, kProfIdle,
+       kProfMaxRoot, kProfRoots };
+
+struct RootCtx {
+    unsigned *rowsP, *rowsX;
+    int *pids;
+    unsigned long long *pkey;
+    int *rids, *xids, *xx, *spill, *plist;
+    unsigned *stack;
+    int deg, np, nx, LV;
+    int rsize;          // |R| at level 0 (1 for a first-level root)
+};
+
+// Inbox header of a warp workspace (word offsets) and inbox states.
+enum { kHdrDeg = 0, kHdrNp = 1, kHdrK = 2, kHdrRsize = 3, kHdrS = 4, kHdrP = 16, kHdrXP = 48 };
+enum : int { kInboxIdle = 0, kInboxFull = 1, kInboxRetired = 2, kInboxClaimed = 4 };
+constexpr long long kDonateCheckCycles = 2048;   // a donor looks at the worker list this often
+
+using dev_int = cuda::atomic_ref<int, cuda::thread_scope_device>;
+using dev_uint = cuda::atomic_ref<unsigned, cuda::thread_scope_device>;
+using dev_ull = cuda::atomic_ref<unsigned long long, cuda::thread_scope_device>;
+
+__device__ __forceinline__ RootCtx make_ctx(unsigned *ws, int deg, int np)
+{
+    const WsLayout lay = ws_layout(deg, np, kIP);
+    RootCtx r;
+    r.rowsP = ws + lay.rowsP;
+    r.rowsX = ws + lay.rowsX;
+    r.pids = reinterpret_cast<int *>(ws + lay.pids);
+    r.pkey = reinterpret_cast<unsigned long long *>(ws + lay.pkey);
+    r.rids = reinterpret_cast<int *>(ws + lay.rids);
+    r.xids = reinterpret_cast<int *>(ws + lay.xids);
+    r.xx = reinterpret_cast<int *>(ws + lay.xx);
+    r.spill = reinterpret_cast<int *>(ws + lay.spill);
+    r.plist = reinterpret_cast<int *>(ws + lay.plist);
+    r.stack = ws + lay.stack;
+    r.deg = deg;
+    r.np = np;
+    r.nx = deg - np;
+    r.LV = lay.LV;
+    r.rsize = 1;
+    return r;
+}
+
+// Id of element e of the clique R u {c} at level L: R's level-0 part, then the vertex chosen
+// at each level below L, then c.
+__device__ __forceinline__ int clique_elem(const RootCtx &r, int L, int c, int e)
+{
+    if (e < r.rsize) return r.rids[e];
+    const int loc = e < r.rsize + L ? (int)r.stack[(long long)(e - r.rsize) * r.LV + 3] : c;
+    return r.pids[loc];
+}
+
+// Reports the maximal clique R u {c}: `size` vertices, hash input `hsum` (sum of keys).
+__device__ void report(const SearchArgs &a, const RootCtx &r, int L, int c, int size,
+                       unsigned long long hsum, Acc &acc, unsigned long long *s_hist, int lane)
+{
+    if (size >= a.out.hist_len) {                   // cannot happen: size <= d + 1
+        if (lane == 0) set_status(a.g.ctrl, MCE_ERR_INTERNAL);
+        return;
+    }
+    if (a.out.ids == nullptr) {
+        if (lane == 0) {
+            acc.count++;
+            acc.hash += mix64(hsum);
+            atomicAdd(&s_hist[size], 1ULL);
+        }
+        return;
+    }
+    // enumeration: slot in the group of cliques of this size, then ids in ascending order
+    unsigned long long slot = 0;
+    if (lane == 0) slot = atomicAdd(&a.out.cursor[size], 1ULL);
+    slot = __shfl_sync(kFull, slot, 0);
+    const long long cl = a.out.region_cl[size] + (long long)slot;
+    if (cl >= a.out.region_cl[size + 1]) {          // more cliques than the counting pass saw
+        if (lane == 0) set_status(a.g.ctrl, MCE_ERR_BUFFER_TOO_SMALL);
+        return;
+    }
+    const long long base = a.out.region_ids[size] + (long long)slot * size;
+    if (lane == 0) a.out.offsets[cl] = base;
+    for (int e = lane; e < size; e += 32) {
+        const int id = clique_elem(r, L, c, e);
+        int rk = 0;
+        for (int f = 0; f < size; ++f) rk += clique_elem(r, L, c, f) < id;
+        a.out.ids[base + rk] = id;
+    }
+}
+
+// Writes the indices of the set bits of a chunked bitset to out[], ascending; returns how many.
+template <int W>
+__device__ __forceinline__ int list_bits(const Ck<Geo<W>::CH> &b, int *out, int lane)
+{
+    constexpr int CH = Geo<W>::CH;
+    int cnt = 0;
+#pragma unroll
+    for (int k = 0; k < W; ++k) {
+        const unsigned wk = __shfl_sync(kFull, b.w[k % CH], k / CH);
+        const bool bit = (wk >> lane) & 1u;
+        const unsigned m = __ballot_sync(kFull, bit);
+        if (bit) out[cnt + __popc(m & ((1u << lane) - 1u))] = k * 32 + lane;
+        cnt += __popc(m);
+    }
+    __syncwarp();
+    return cnt;
+}
+
+// Partial induced subgraphs: is the X vertex x adjacent to the P vertex p?  p comes after x in
+// the order, so it is in x's later-neighbour list N+(x), which is sorted by id: a binary search
+// of the original graph (Section 3.4).
+__device__ __forceinline__ bool x_adjacent(const DevGraph &g, int x, int p)
+{
+    const int end = __ldg(g.poffs + x + 1);
+    int lo = __ldg(g.poffs + x), hi = end;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(g.padj + mid) < p) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo < end && __ldg(g.padj + lo) == p;
+}
+
+// Tomita pivot over P u X_P (bits of P | XP) and the live X_X rows xx[0..lpX): the row with
+// the most neighbours in P, ties to the smaller code.  Returns -1 when some vertex of X is
+// adjacent to all of P (no maximal clique below this node: every branch would be cut).  With
+// partial induced subgraphs X_X has no rows, and the pivot comes from P u X_P only (Section 3.5,
+// last paragraph).
+template <int W>
+__device__ int choose_pivot(const RootCtx &r, const Ck<Geo<W>::CH> &P, const Ck<Geo<W>::CH> &PX,
+                            int npop, int lpX, Acc &acc, int lane)
+{
+    constexpr int CH = Geo<W>::CH, G = Geo<W>::G, R = Geo<W>::R;
+    const int q = lane % G, sub = lane / G;
+    // list the members of P u X_P
+    const int cntp = list_bits<W>(PX, r.plist, lane);
+    const int total = kIP ? cntp : cntp + lpX;
+    unsigned best = 0;
+    for (int base = 0; base < total; base += R) {
+        const int t = base + sub;
+        const bool valid = t < total;
+        int code = 0;
+        const unsigned *row = r.rowsP;
+        if (valid) {
+            if (t < cntp) {
+                code = r.plist[t];
+                row = r.rowsP + (long long)code * W;
+            } else {
+                const int x = r.xx[t - cntp];
+                code = r.np + x;
+                row = r.rowsX + (long long)x * W;
+            }
+        }
+        const Ck<CH> rc = valid ? ck_load<CH>(row + q * CH) : ck_zero<CH>();
+        const int cnt = subwarp_sum<G>(ck_popc<CH>(ck_and<CH>(P, rc)));
+        if (valid) {
+            const unsigned key = ((unsigned)cnt << kMaxIdxBits) | (unsigned)(kMaxCode - code);
+            best = key > best ? key : best;
+        }
+        if (lane == 0) acc.words += (unsigned long long)W * (unsigned)min(R, total - base);
+        if (__any_sync(kFull, valid && cnt == npop)) return -1;
+    }
+    best = __reduce_max_sync(kFull, best);
+    return kMaxCode - (int)(best & (unsigned)kMaxCode);
+}
+
+// Does some live X_X row have bit c?  (X_X n N(c) non-empty)
+template <int W>
+__device__ __forceinline__ bool xx_hits(const DevGraph &g, const RootCtx &r, int lpX, int c,
+                                        Acc &acc, int lane)
+{
+    const int wc = c >> 5;
+    const unsigned bit = 1u << (c & 31);
+    const int pc = kIP ? r.pids[c] : 0;
+    for (int base = 0; base < lpX; base += 32) {
+        const int i = base + lane;
+        bool hit = false;
+        if (i < lpX) {
+            if constexpr (kIP) hit = x_adjacent(g, r.xids[r.xx[i]], pc);
+            else hit = (r.rowsX[(long long)r.xx[i] * W + wc] & bit) != 0u;
+        }
+        if (lane == 0) acc.words += (unsigned)min(32, lpX - base);
+        if (__any_sync(kFull, hit)) return true;
+    }
+    return false;
+}
+
+// Moves the X_X rows adjacent to c to the front of xx[0..lpX) (order kept) and returns their
+// number; the others follow, so the parent's range xx[0..lpX) still holds the same set.
+template <int W>
+__device__ int xx_partition(const DevGraph &g, const RootCtx &r, int lpX, int c, int lane)
+{
+    const int wc = c >> 5;
+    const unsigned bit = 1u << (c & 31);
+    const int pc = kIP ? r.pids[c] : 0;
+    const unsigned lt = (1u << lane) - 1u;
+    int kept = 0, rem = 0;
+    for (int base = 0; base < lpX; base += 32) {
+        const int i = base + lane;
+        const bool in = i < lpX;
+        const int x = in ? r.xx[i] : 0;
+        bool keep = false;
+        if (in) {
+            if constexpr (kIP) keep = x_adjacent(g, r.xids[x], pc);
+            else keep = (r.rowsX[(long long)x * W + wc] & bit) != 0u;
+        }
+        const unsigned mk = __ballot_sync(kFull, keep);
+        const unsigned mr = __ballot_sync(kFull, in && !keep);
+        if (keep) r.xx[kept + __popc(mk & lt)] = x;
+        else if (in) r.spill[rem + __popc(mr & lt)] = x;
+        kept += __popc(mk);
+        rem += __popc(mr);
+        __syncwarp();
+    }
+    for (int t = lane; t < rem; t += 32) r.xx[kept + t] = r.spill[t];
+    __syncwarp();
+    return kept;
+}
+
+// ------------------------------------------------------------------ worker list (Section 3.3)
+//
+// Idle warps put their id in a bounded multi-producer multi-consumer ring (one slot per warp,
+// so it cannot overflow) and wait on their inbox flag.  A busy warp ("donor") that is about to
+// descend into a branch with |P| >= donate_min_p, with other branches left at the same level
+// and at an earlier level, pops an idle warp, claims its inbox (idle -> claimed), writes the
+// branch into the idle warp's workspace and publishes it (claimed -> full, release).  `busy`
+// counts warps holding work; an idle warp leaves when roots are exhausted and busy == 0.  An
+// idle warp that waited spin_limit_ns retires (idle -> retired); a donor that pops a retired
+// warp keeps the branch.  Ring slots carry sequence numbers, so a slot is never reused before
+// its previous value was taken.  Every wait is bounded.
+
+__device__ bool ring_push(const SearchArgs &a, int w)
+{
+    const int t = dev_int(a.g.ctrl->ring_tail).fetch_add(1, cuda::memory_order_relaxed);
+    const int slot = t % a.n_workers;
+    dev_uint seq(a.ring_seq[slot]);
+    const unsigned long long t0 = globaltimer_ns();
+    unsigned ns = 32;
+    while (seq.load(cuda::memory_order_acquire) != (unsigned)t) {
+        if ((long long)(globaltimer_ns() - t0) > a.spin_limit_ns) {
+            set_status(a.g.ctrl, MCE_ERR_DEVICE_TIMEOUT);
+            return false;
+        }
+        __nanosleep(ns);
+        if (ns < 1024) ns <<= 1;
+    }
+    a.ring[slot] = w;
+    seq.store((unsigned)t + 1u, cuda::memory_order_release);
+    return true;
+}
+
+// Pops an idle warp id, or -1 when the ring is empty (never waits).
+__device__ int ring_try_pop(const SearchArgs &a)
+{
+    dev_int head(a.g.ctrl->ring_head), tail(a.g.ctrl->ring_tail);
+    int h = head.load(cuda::memory_order_relaxed);
+    for (int attempt = 0; attempt < 16; ++attempt) {
+        if (h >= tail.load(cuda::memory_order_relaxed)) return -1;
+        const int slot = h % a.n_workers;
+        dev_uint seq(a.ring_seq[slot]);
+        const unsigned sq = seq.load(cuda::memory_order_acquire);
+        if (sq == (unsigned)h + 1u) {
+            if (head.compare_exchange_strong(h, h + 1, cuda::memory_order_relaxed)) {
+                const int w = a.ring[slot];
+                seq.store((unsigned)h + (unsigned)a.n_workers, cuda::memory_order_release);
+                return w;
+            }
+        } else if ((int)(sq - ((unsigned)h + 1u)) < 0) {
+            return -1;                           // its pusher has not written the slot yet
+        } else {
+            h = head.load(cuda::memory_order_relaxed);
+        }
+    }
+    return -1;
+}
+
+// Copies the branch R u {c} with sets (Pc, XPc, xx[0..k)) into the workspace `dst` of another
+// warp: the P rows, the k live X rows (renumbered 0..k-1), the P ids and keys, R's ids.
+template <int W>
+__device__ void write_branch(const RootCtx &r, unsigned *dst, int L, int c,
+                             const Ck<Geo<W>::CH> &Pc, const Ck<Geo<W>::CH> &XPc, int k,
+                             unsigned long long Sc, int lane)
+{
+    constexpr int CH = Geo<W>::CH, G = Geo<W>::G;
+    const int q = lane % G;
+    const WsLayout lay = ws_layout(r.deg, r.np, kIP);
+    const int rsize = r.rsize + L + 1;
+    if (lane == 0) {
+        dst[kHdrDeg] = (unsigned)r.deg;
+        dst[kHdrNp] = (unsigned)r.np;
+        dst[kHdrK] = (unsigned)k;
+        dst[kHdrRsize] = (unsigned)rsize;
+        *reinterpret_cast<unsigned long long *>(dst + kHdrS) = Sc;
+    }
+    if (lane < G) {
+        ck_store<CH>(dst + kHdrP + q * CH, Pc);
+        ck_store<CH>(dst + kHdrXP + q * CH, XPc);
+    }
+    // the branch only ever touches rows (and ids, keys) of vertices in P' u X_P'
+    const int nl = list_bits<W>(ck_or<CH>(Pc, XPc), r.plist, lane);
+    for (long long t = lane; t < (long long)nl * W; t += 32) {
+        const long long i = t / W;
+        const long long off = (long long)r.plist[i] * W + (t - i * W);
+        dst[lay.rowsP + off] = r.rowsP[off];
+    }
+    int *dxx = reinterpret_cast<int *>(dst + lay.xx);
+    if constexpr (kIP) {
+        // no X rows: the ids of the live X_X vertices, renumbered
+        int *dxi = reinterpret_cast<int *>(dst + lay.xids);
+        for (int i = lane; i < k; i += 32) dxi[i] = r.xids[r.xx[i]];
+    } else {
+        for (long long t = lane; t < (long long)k * W; t += 32) {
+            const long long i = t / W;
+            const int x = r.xx[i];
+            dst[lay.rowsX + t] = r.rowsX[(long long)x * W + (t - i * W)];
+        }
+    }
+    for (int i = lane; i < k; i += 32) dxx[i] = i;
+    int *dp = reinterpret_cast<int *>(dst + lay.pids);
+    unsigned long long *dk = reinterpret_cast<unsigned long long *>(dst + lay.pkey);
+    for (int t = lane; t < nl; t += 32) {
+        const int i = r.plist[t];
+        dp[i] = r.pids[i];
+        dk[i] = r.pkey[i];
+    }
+    int *dr = reinterpret_cast<int *>(dst + lay.rids);
+    for (int e = lane; e < rsize; e += 32) dr[e] = clique_elem(r, L, c, e);
+    __threadfence();          // every lane's part of the branch is visible GPU-wide ...
+    __syncwarp();             // ... before lane 0 publishes it
+}
+
+// Depth-first search of one first-level subtree (or donated branch) from the node
+// (P, XP, xx[0..lpX)) at level 0 whose clique R has r.rsize vertices and key sum S.
+template <int W>
+__device__ void dfs(const SearchArgs &a, const RootCtx &r, Ck<Geo<W>::CH> P, Ck<Geo<W>::CH> XP,
+                    int lpX, unsigned long long S, Acc &acc, unsigned long long *s_hist,
+                    int lane)
+{
+    constexpr int CH = Geo<W>::CH, G = Geo<W>::G;
+    const int q = lane % G;
+    int L = 0;
+    bool enter = true;
+    bool more_below = false;   // some level below L still has branches to explore
+    Ck<CH> P0, XP0, C;
+    int cursor = -1;
+    long long last_check = __shfl_sync(kFull, (long long)clock64(), 0);
+    while (true) {
+        if (enter) {
+            enter = false;
+            acc.nodes++;
+            PROF_START(t_piv);
+            const int npop = subwarp_sum<G>(ck_popc<CH>(P));
+            const int piv = choose_pivot<W>(r, P, ck_or<CH>(P, XP), npop, lpX, acc, lane);
+            PROF_ADD(acc, kProfPivot, t_piv);
+            if (piv < 0) {
+                C = ck_zero<CH>();
+            } else {
+                const unsigned *row = piv < r.np ? r.rowsP + (long long)piv * W
+                                                 : r.rowsX + (long long)(piv - r.np) * W;
+                C = ck_andnot<CH>(P, ck_load<CH>(row + q * CH));
+            }
+            P0 = P;
+            XP0 = XP;
+            cursor = -1;
+            unsigned *lv = r.stack + (long long)L * r.LV;
+            if (lane < G) {
+                ck_store<CH>(lv + 8 + q * CH, P0);
+                ck_store<CH>(lv + 8 + W + q * CH, XP0);
+                ck_store<CH>(lv + 8 + 2 * W + q * CH, C);
+            }
+            if (lane == 0) {
+                *reinterpret_cast<unsigned long long *>(lv) = S;
+                lv[2] = (unsigned)lpX;
+                lv[3] = 0xffffffffu;
+                lv[4] = more_below ? 1u : 0u;
+            }
+            __syncwarp();
+        }
+        const int c = lowest_above<W>(C, cursor, q);
+        if (c == INT_MAX) {                       // level exhausted: back up
+            if (L == 0) return;
+            --L;
+            const unsigned *lv = r.stack + (long long)L * r.LV;
+            P0 = ck_load<CH>(lv + 8 + q * CH);
+            XP0 = ck_load<CH>(lv + 8 + W + q * CH);
+            C = ck_load<CH>(lv + 8 + 2 * W + q * CH);
+            S = *reinterpret_cast<const unsigned long long *>(lv);
+            lpX = (int)lv[2];
+            cursor = (int)lv[3];
+            more_below = lv[4] != 0u;
+            continue;
+        }
+        cursor = c;
+        PROF_START(t_child);
+        // branch on c: P at this point is P0 minus earlier candidates, X_P gained them
+        const Ck<CH> pre = bits_below<W>(C, c, q);
+        const Ck<CH> rc = ck_load<CH>(r.rowsP + (long long)c * W + q * CH);
+        const Ck<CH> Pc = ck_and<CH>(ck_andnot<CH>(P0, pre), rc);
+        const Ck<CH> XPc = ck_and<CH>(ck_or<CH>(XP0, pre), rc);
+        const unsigned long long Sc = S + r.pkey[c];
+        if (lane == 0) acc.words += 2 * W;
+        if (!__any_sync(kFull, ck_nonzero<CH>(Pc))) {
+            // leaf: R u {c} is maximal iff X n N(c) is empty (Algorithm 2, lines 2-3)
+            if (!__any_sync(kFull, ck_nonzero<CH>(XPc)) && !xx_hits<W>(a.g, r, lpX, c, acc, lane)) {
+                report(a, r, L, c, r.rsize + L + 1, Sc, acc, s_hist, lane);
+                acc.nodes++;
+            }
+            PROF_ADD(acc, kProfChild, t_child);
+            continue;
+        }
+        const bool more_same = lowest_above<W>(C, c, q) != INT_MAX;
+        if (lane == 0) r.stack[(long long)L * r.LV + 3] = (unsigned)c;
+        PROF_ADD(acc, kProfChild, t_child);
+        PROF_START(t_part);
+        const int lpXc = xx_partition<W>(a.g, r, lpX, c, lane);
+        PROF_ADD(acc, kProfPartition, t_part);
+        if (lane == 0) acc.words += (unsigned)lpX;
+        // worker list: hand this branch to an idle warp instead of descending (Section 3.3:
+        // only when the donor keeps unexplored branches at this level and an earlier one;
+        // donate_rule 1 accepts either)
+        if (a.worker_list && (a.donate_rule ? (more_same || more_below)
+                                            : (more_same && more_below))) {
+            const long long now = __shfl_sync(kFull, (long long)clock64(), 0);
+            // a branch worth the copy: |P'| at least donate_min_p and a quarter of the root's P
+            const int min_p = a.donate_min_p > (r.np >> 2) ? a.donate_min_p : (r.np >> 2);
+            if (now - last_check > kDonateCheckCycles &&
+                subwarp_sum<G>(ck_popc<CH>(Pc)) >= min_p) {
+                last_check = now;
+                int recv = -1;
+                if (lane == 0) {
+                    recv = ring_try_pop(a);
+                    if (recv >= 0) {
+                        int expect = kInboxIdle;
+                        if (!dev_int(a.flag[recv]).compare_exchange_strong(
+                                expect, kInboxClaimed, cuda::memory_order_acq_rel))
+                            recv = -1;                // it retired meanwhile
+                        else
+                            dev_int(a.g.ctrl->busy).fetch_add(1, cuda::memory_order_relaxed);
+                    }
+                }
+                recv = __shfl_sync(kFull, recv, 0);
+                PROF_START(t_don);
+                if (recv >= 0) {
+                    unsigned *dst = a.ws + (unsigned long long)recv * a.ws_words;
+                    write_branch<W>(r, dst, L, c, Pc, XPc, lpXc, Sc, lane);
+                    if (lane == 0) {
+                        __threadfence();
+                        dev_int(a.flag[recv]).store(kInboxFull, cuda::memory_order_release);
+                        acc.donations++;
+                    }
+                    PROF_ADD(acc, kProfDonate, t_don);
+                    continue;
+                }
+            }
+        }
+        more_below = more_below || more_same;
+        lpX = lpXc;
+        if (L + 1 > r.np) {                       // cannot happen: |P| shrinks at every level
+            if (lane == 0) set_status(a.g.ctrl, MCE_ERR_INTERNAL);
+            return;
+        }
+        ++L;
+        P = Pc;
+        XP = XPc;
+        S = Sc;
+        enter = true;
+    }
+}
+
+// Per-warp shared memory of the build: open-addressing hash of P(v) (id -> local index) and
+// a staging row.
+constexpr int kBatch = 8;   // N+ entries a lane loads before probing them
+
+struct WarpSmem {
+    int *hkey, *hval;
+    unsigned *stage;
+    int slots;
+    int *cur_start, *cur_base;   // build: per group of 32 neighbours, list starts and bases
+    unsigned *rows;              // rows of a root small enough for shared memory
+    int rows_words;
+};
+
+__device__ __forceinline__ unsigned hash_slot(int id, int mask)
+{
+    return ((unsigned)id * 0x9E3779B1u >> 7) & (unsigned)mask;
+}
+
+__device__ __forceinline__ int hash_find(const WarpSmem &sm, int id)
+{
+    const int mask = sm.slots - 1;
+    unsigned s = hash_slot(id, mask);
+    while (true) {
+        const int k = sm.hkey[s];
+        if (k == id) return sm.hval[s];
+        if (k < 0) return -1;
+        s = (s + 1) & (unsigned)mask;
+    }
+}
+
+// Load-balanced build of all rows (normal roots).  The neighbours u_t of v (P first, then X)
+// are taken 32 at a time; the warp walks the concatenation of their lists N+(u_t) with
+// consecutive lanes on consecutive entries (coalesced), kBatch entries per lane in flight.  A
+// hit on p_j sets bit j of row t, and, when u_t = p_t is in P, bit t of row j as well.
+template <int W>
+__device__ void build_flat(const SearchArgs &a, const RootCtx &r, const WarpSmem &h, int deg,
+                           int np, int lane)
+{
+    unsigned *rows = r.rowsP;   // rowsX follows rowsP directly
+    for (int g0 = 0; g0 < deg; g0 += 32) {
+        const int t = g0 + lane;
+        int base = 0, len = 0;
+        if (t < deg) {
+            const int u = t < np ? r.pids[t] : r.xids[t - np];
+            base = __ldg(a.g.poffs + u);
+            len = __ldg(a.g.poffs + u + 1) - base;
+        }
+        int incl = len;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const int total = __shfl_sync(kFull, incl, 31);
+        h.cur_start[lane] = incl - len;
+        h.cur_base[lane] = base;
+        if (lane == 0) h.cur_start[32] = total;
+        __syncwarp();
+        int own = 0;
+        for (int f0 = 0; f0 < total; f0 += 32 * kBatch) {
+            int w[kBatch], ow[kBatch];
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+                const int f = f0 + b * 32 + lane;
+                ow[b] = -1;
+                w[b] = -1;
+                if (f < total) {
+                    while (h.cur_start[own + 1] <= f) ++own;
+                    ow[b] = own;
+                    w[b] = __ldg(a.g.padj + h.cur_base[own] + (f - h.cur_start[own]));
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+                if (ow[b] < 0) continue;
+                const int j = hash_find(h, w[b]);
+                if (j < 0) continue;
+                const int tt = g0 + ow[b];
+                atomicOr(rows + (long long)tt * W + (j >> 5), 1u << (j & 31));
+                if (tt < np) atomicOr(rows + (long long)j * W + (tt >> 5), 1u << (tt & 31));
+            }
+        }
+        __syncwarp();
+    }
+}
+
+// Builds the induced subgraph of root v into the warp's workspace and searches it.
+//
+// Rows: for u in N(v), row(u) has bit i set iff u is adjacent to the i-th vertex of P (the
+// binary-encoded induced subgraph over P u X, Section 3.4's full variant).  Every such
+// adjacency u - p with p in P is found by streaming the later-neighbour list N+(u): a vertex of
+// X precedes v and so precedes every p in P, hence p is in N+(u); a pair of P vertices is found
+// from the earlier of the two.  Membership in P is a shared-memory hash lookup, so the build
+// reads the bounded lists N+(u) (each at most d long) with coalesced loads and no search.
+template <int W>
+__device__ void search_root(const SearchArgs &a, unsigned *ws, const WarpSmem &sm, int v, int deg,
+                            int np, bool big, Acc &acc, unsigned long long *s_hist, int lane)
+{
+    constexpr int CH = Geo<W>::CH, G = Geo<W>::G;
+    PROF_START(t_build);
+    RootCtx r = make_ctx(ws, deg, np);
+    const int *Nv = a.g.adj + a.g.offs[v];
+    const int rv = a.g.rank[v];
+    const unsigned lt = (1u << lane) - 1u;
+    // split N(v) into P (later) and X (earlier), numbering each part in id order
+    int pi = 0, xi = 0;
+    for (int base = 0; base < deg; base += 32) {
+        const int j = base + lane;
+        const bool in = j < deg;
+        const int w = in ? __ldg(Nv + j) : 0;
+        const bool isP = in && __ldg(a.g.rank + w) > rv;
+        const unsigned mp = __ballot_sync(kFull, isP);
+        const unsigned mx = __ballot_sync(kFull, in && !isP);
+        if (isP) r.pids[pi + __popc(mp & lt)] = w;
+        else if (in) r.xids[xi + __popc(mx & lt)] = w;
+        pi += __popc(mp);
+        xi += __popc(mx);
+    }
+    // rows in shared memory when they fit (normal roots only), else in the workspace; zero the
+    // rows (the big-root build writes X rows whole when they are at most 4 words wide)
+    if (!big && (long long)(kIP ? np : deg) * W <= sm.rows_words) {
+        r.rowsP = sm.rows;
+        r.rowsX = sm.rows + (long long)np * W;
+    }
+    {
+        const long long words = (long long)(kIP || (big && W <= 4) ? np : deg) * W;
+        for (long long t = (long long)lane * CH; t < words; t += 32 * CH)
+            ck_store<CH>(r.rowsP + t, ck_zero<CH>());
+    }
+    int slots = 32;
+    while (slots < 2 * np) slots <<= 1;
+    WarpSmem h = sm;
+    h.slots = slots;
+    for (int i = lane; i < slots; i += 32) h.hkey[i] = -1;
+    if (lane == 0) r.rids[0] = v;
+    __syncwarp();
+    for (int i = lane; i < np; i += 32) {
+        const int id = r.pids[i];
+        unsigned sl = hash_slot(id, slots - 1);
+        while (atomicCAS(&h.hkey[sl], -1, id) != -1) sl = (sl + 1) & (unsigned)(slots - 1);
+        h.hval[sl] = i;
+    }
+    __syncwarp();
+    int nxx = 0;
+    bool covered = false;
+    if constexpr (kIP) {
+        // partial induced subgraph: P x P rows only; X_X starts as the whole of X
+        build_flat<W>(a, r, h, np, np, lane);
+        for (int i = lane; i < r.nx; i += 32) r.xx[i] = i;
+        nxx = r.nx;
+    } else if (!big) {
+        build_flat<W>(a, r, h, deg, np, lane);
+        // X_X and the coverage test: a vertex of X adjacent to all of P makes every clique of
+        // this subtree extendable (it is the Tomita pivot of the root with P - N(pivot) empty),
+        // so the subtree holds no maximal clique
+        for (int base = 0; base < r.nx; base += 32) {
+            const int xi = base + lane;
+            int cnt = 0;
+            if (xi < r.nx)
+                for (int k = 0; k < W; ++k) cnt += __popc(r.rowsX[(long long)xi * W + k]);
+            covered = covered || __any_sync(kFull, cnt == np);
+            const unsigned m = __ballot_sync(kFull, cnt > 0);
+            if (cnt > 0) r.xx[nxx + __popc(m & lt)] = xi;
+            nxx += __popc(m);
+        }
+        if (covered) {
+            acc.nodes++;
+            PROF_ADD(acc, kProfBuild, t_build);
+            return;
+        }
+    } else {
+    // X rows, one vertex per lane.  A vertex of X adjacent to all of P makes every clique of
+    // this subtree extendable (it is the Tomita pivot of the root with P - N(pivot) empty):
+    // the subtree holds no maximal clique and is abandoned as soon as one is seen.
+    for (int base = 0; base < r.nx && !covered; base += 32) {
+        const int xi = base + lane;
+        int hits = 0;
+        unsigned reg[W <= 4 ? W : 1];
+#pragma unroll
+        for (int k = 0; k < (W <= 4 ? W : 1); ++k) reg[k] = 0u;
+        unsigned *row = r.rowsX + (long long)xi * W;
+        if (xi < r.nx) {
+            const int u = r.xids[xi];
+            const int s1 = __ldg(a.g.poffs + u + 1);
+            for (int e0 = __ldg(a.g.poffs + u); e0 < s1; e0 += kBatch) {
+                int w[kBatch];                           // independent loads in flight
+#pragma unroll
+                for (int b = 0; b < kBatch; ++b) w[b] = e0 + b < s1 ? __ldg(a.g.padj + e0 + b) : -1;
+#pragma unroll
+                for (int b = 0; b < kBatch; ++b) {
+                    const int j = w[b] < 0 ? -1 : hash_find(h, w[b]);
+                    if (j < 0) continue;
+                    ++hits;
+                    if constexpr (W <= 4) {
+#pragma unroll
+                        for (int k = 0; k < W; ++k) reg[k] |= (j >> 5) == k ? 1u << (j & 31) : 0u;
+                    } else {
+                        row[j >> 5] |= 1u << (j & 31);
+                    }
+                }
+            }
+            if constexpr (W <= 4) {
+                Ck<CH> c;
+#pragma unroll
+                for (int k = 0; k < CH; ++k) c.w[k] = reg[k];
+                ck_store<CH>(row, c);
+            }
+        }
+        covered = __any_sync(kFull, hits == np && xi < r.nx);
+        const unsigned m = __ballot_sync(kFull, hits > 0);
+        if (hits > 0) r.xx[nxx + __popc(m & lt)] = xi;
+        nxx += __popc(m);
+    }
+    if (covered) {
+        acc.nodes++;
+        PROF_ADD(acc, kProfBuild, t_build);
+        return;
+    }
+    // P rows, one vertex per lane: the later P neighbours of p_i come from N+(p_i) ...
+    for (int base = 0; base < np; base += 32) {
+        const int i = base + lane;
+        if (i < np) {
+            const int u = r.pids[i];
+            unsigned *row = r.rowsP + (long long)i * W;
+            const int s1 = __ldg(a.g.poffs + u + 1);
+            for (int e0 = __ldg(a.g.poffs + u); e0 < s1; e0 += kBatch) {
+                int w[kBatch];
+#pragma unroll
+                for (int b = 0; b < kBatch; ++b) w[b] = e0 + b < s1 ? __ldg(a.g.padj + e0 + b) : -1;
+#pragma unroll
+                for (int b = 0; b < kBatch; ++b) {
+                    const int j = w[b] < 0 ? -1 : hash_find(h, w[b]);
+                    if (j >= 0) row[j >> 5] |= 1u << (j & 31);
+                }
+            }
+        }
+    }
+    __syncwarp();
+    // ... and the earlier ones by symmetry: transpose 32 x 32 bit blocks with ballots
+    const int nb = (np + 31) >> 5;
+    for (int bi = 0; bi < nb; ++bi) {
+        for (int bj = 0; bj < nb; ++bj) {
+            const int ri = bi * 32 + lane;                 // this lane's row in block row bi
+            const unsigned word = ri < np ? r.rowsP[(long long)ri * W + bj] : 0u;
+            unsigned tr = 0;
+#pragma unroll 4
+            for (int k = 0; k < 32; ++k) {
+                const unsigned col = __ballot_sync(kFull, (word >> k) & 1u);
+                if (lane == k) tr = col;
+            }
+            // tr = word bi of row (bj * 32 + lane), as seen from the block (bi, bj)
+            const int rj = bj * 32 + lane;
+            __syncwarp();
+            if (rj < np && tr) r.rowsP[(long long)rj * W + bi] |= tr;
+            __syncwarp();
+        }
+    }
+    }
+    for (int i = lane; i < np; i += 32) r.pkey[i] = vertex_key(r.pids[i]);
+    __syncwarp();
+    PROF_ADD(acc, kProfBuild, t_build);
+    const int q = lane % G;
+    dfs<W>(a, r, bits_prefix<W>(np, q), ck_zero<CH>(), nxx, vertex_key(v), acc, s_hist, lane);
+}
+
+// Searches a branch that another warp wrote into this warp's workspace.
+template <int W>
+__device__ void search_inbox(const SearchArgs &a, unsigned *ws, Acc &acc,
+                             unsigned long long *s_hist, int lane)
+{
+    constexpr int CH = Geo<W>::CH, G = Geo<W>::G;
+    const int q = lane % G;
+    const int deg = (int)ws[kHdrDeg], np = (int)ws[kHdrNp];
+    const int k = (int)ws[kHdrK], rsize = (int)ws[kHdrRsize];
+    // a branch always comes from a root of this kernel's class, within its workspace
+    const bool sane = np >= 1 && np <= kMaxP && wclass(np) == W && deg >= np && k >= 0 &&
+                      k <= deg - np && rsize >= 2 && rsize <= np + 1 &&
+                      (unsigned long long)ws_layout(deg, np, kIP).total <= a.ws_words;
+    if (!sane) {
+        if (lane == 0) set_status(a.g.ctrl, MCE_ERR_INTERNAL);
+        return;
+    }
+    RootCtx r = make_ctx(ws, deg, np);
+    r.rsize = rsize;
+    const unsigned long long S = *reinterpret_cast<const unsigned long long *>(ws + kHdrS);
+    const Ck<CH> P = ck_load<CH>(ws + kHdrP + q * CH);
+    const Ck<CH> XP = ck_load<CH>(ws + kHdrXP + q * CH);
+    dfs<W>(a, r, P, XP, k, S, acc, s_hist, lane);
+}
+
+// CTAs per SM the compiler should plan registers for, per row width (more for narrow rows).
+#ifndef MCE_MIN_BLOCKS_MID
+#define MCE_MIN_BLOCKS_MID 6
+#endif
+template <int W>
+struct MinBlocks {
+    static constexpr int value = W <= 2 ? 8 : (W <= 8 ? MCE_MIN_BLOCKS_MID : 4);
+};
+
+// One persistent launch per row width W: the roots of that class, heaviest first, then
+// donated branches of those roots (Section 3.3).
+template <int W>
+__global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(SearchArgs a)
+{
+    extern __shared__ __align__(16) unsigned char s_raw[];
+    unsigned long long *s_hist = reinterpret_cast<unsigned long long *>(s_raw);
+    for (int i = threadIdx.x; i < a.out.hist_len; i += blockDim.x) s_hist[i] = 0ULL;
+    const int lane = threadIdx.x & 31;
+    const int wpb = blockDim.x >> 5;
+    const int warp = blockIdx.x * wpb + (threadIdx.x >> 5);
+    WarpSmem sm;
+    {
+        constexpr int k = W == 1 ? 0 : W == 2 ? 1 : W == 4 ? 2 : W == 8 ? 3 : W == 16 ? 4 : 5;
+        const size_t hist = ((size_t)(a.out.hist_len + 1) * 8 + 15) & ~(size_t)15;
+        unsigned char *mine = s_raw + hist + (size_t)(threadIdx.x >> 5) * warp_smem_bytes(k);
+        sm.hkey = reinterpret_cast<int *>(mine);
+        sm.hval = sm.hkey + hash_slots(k);
+        sm.stage = reinterpret_cast<unsigned *>(sm.hval + hash_slots(k));
+        sm.slots = hash_slots(k);
+        sm.cur_start = reinterpret_cast<int *>(sm.stage + 32);
+        sm.cur_base = sm.cur_start + 36;
+        sm.rows = reinterpret_cast<unsigned *>(sm.cur_base + 36);   // 16-byte aligned
+        sm.rows_words = smem_row_words(k);
+    }
+    __syncthreads();
+    unsigned *ws = a.ws + (unsigned long long)warp * a.ws_words;
+    const unsigned long long begin = (unsigned long long)a.range[2 * a.group];
+    const unsigned long long n_roots = (unsigned long long)a.range[2 * a.group + 1] - begin;
+    dev_int busy(a.g.ctrl->busy);
+    Acc acc{};
+    // phase 1: first-level subtrees from the shared counter
+    while (load_status(a.g.ctrl) == 0) {
+        unsigned long long idx = 0;
+        if (lane == 0) {
+            busy.fetch_add(1, cuda::memory_order_relaxed);
+            idx = atomicAdd(&a.g.ctrl->next_root, 1ULL);
+            if (idx >= n_roots) busy.fetch_sub(1, cuda::memory_order_acq_rel);
+        }
+        idx = __shfl_sync(kFull, idx, 0);
+        if (idx >= n_roots) break;
+        PROF_START(t_root);
+        const int v = a.roots[begin + idx];
+        const int deg = a.g.offs[v + 1] - a.g.offs[v];
+        const int np = a.g.pcount[v];
+        if (np == 0) {
+            // R = {v}, P empty: maximal iff X is empty too, i.e. v is isolated
+            if (deg == 0) {
+                RootCtx single{};
+                single.rids = reinterpret_cast<int *>(ws);
+                single.rsize = 1;
+                if (lane == 0) single.rids[0] = v;
+                __syncwarp();
+                report(a, single, 0, 0, 1, vertex_key(v), acc, s_hist, lane);
+            }
+        } else if (np > kMaxP) {
+            if (lane == 0) set_status(a.g.ctrl, MCE_ERR_LIMIT);
+        } else {
+            search_root<W>(a, ws, sm, v, deg, np, (a.group & 1) == 0, acc, s_hist, lane);
+        }
+        __syncwarp();
+        if (lane == 0) busy.fetch_sub(1, cuda::memory_order_acq_rel);
+#ifdef MCE_PROFILE
+        {
+            const unsigned long long dt = (unsigned long long)(clock64() - t_root);
+            acc.prof[kProfMaxRoot] = dt > acc.prof[kProfMaxRoot] ? dt : acc.prof[kProfMaxRoot];
+            acc.prof[kProfRoots]++;
+        }
+#endif
+    }
+    // phase 2: receive donated branches until no warp holds work
+    while (a.worker_list && load_status(a.g.ctrl) == 0) {
+        int state = 0;   // 1: a branch arrived, 2: leave
+        PROF_START(t_idle);
+        if (lane == 0) {
+            if (!ring_push(a, warp)) state = 2;
+            dev_int flag(a.flag[warp]);
+            const unsigned long long t0 = globaltimer_ns();
+            unsigned ns = 64, polls = 0;
+            while (state == 0) {
+                const int f = flag.load(cuda::memory_order_acquire);
+                const long long waited = (long long)(globaltimer_ns() - t0);
+                if (f == kInboxFull) {
+                    state = 1;
+                } else if (f == kInboxIdle) {
+                    // the shared counters are read on every 8th poll only (own flag every time)
+                    if ((polls++ & 7u) == 0 &&
+                        (busy.load(cuda::memory_order_acquire) == 0 || load_status(a.g.ctrl) != 0)) {
+                        state = 2;                       // nothing left anywhere
+                    } else if (waited > a.spin_limit_ns) {
+                        int expect = kInboxIdle;
+                        if (flag.compare_exchange_strong(expect, kInboxRetired,
+                                                         cuda::memory_order_acq_rel))
+                            state = 2;                   // retire; donors skip this warp
+                    }
+                } else if (waited > a.spin_limit_ns + a.spin_limit_ns) {
+                    set_status(a.g.ctrl, MCE_ERR_DEVICE_TIMEOUT);   // claimed, never filled
+                    state = 2;
+                }
+                if (state == 0) {
+                    __nanosleep(ns);
+                    if (ns < 2048) ns <<= 1;
+                }
+            }
+            if (state == 1) flag.store(kInboxIdle, cuda::memory_order_release);
+        }
+        state = __shfl_sync(kFull, state, 0);
+        PROF_ADD(acc, kProfIdle, t_idle);
+        if (state != 1) break;
+        __syncwarp();
+        cuda::atomic_thread_fence(cuda::memory_order_acquire, cuda::thread_scope_device);
+        search_inbox<W>(a, ws, acc, s_hist, lane);
+        __syncwarp();
+        if (lane == 0) busy.fetch_sub(1, cuda::memory_order_acq_rel);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < a.out.hist_len; i += blockDim.x)
+        if (s_hist[i]) atomicAdd(&a.out.hist[i], s_hist[i]);
+    if (lane == 0) {
+        atomicAdd(&a.g.ctrl->result[0], acc.count);
+        atomicAdd(&a.g.ctrl->result[1], acc.hash);
+        atomicAdd(&a.g.ctrl->tree_nodes, acc.nodes);
+        atomicAdd(&a.g.ctrl->donations, acc.donations);
+        atomicAdd(&a.g.ctrl->words[a.cls], acc.words);
+#ifdef MCE_PROFILE
+        for (int i = 0; i < 8; ++i) {
+            if (i == kProfMaxRoot) atomicMax(&a.g.ctrl->prof[a.cls][i], acc.prof[i]);
+            else atomicAdd(&a.g.ctrl->prof[a.cls][i], acc.prof[i]);
+        }
+#endif
+    }
+}
+
+}  // namespace
+
+}  // namespace mce

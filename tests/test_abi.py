@@ -48,6 +48,15 @@ def test_calls_that_need_no_gpu(lib):
     # argument errors are caught before any CUDA call
     assert lib.mce_create(None, None, 5, 0, None, None, ctypes.byref(out)) == 1
     assert lib.mce_create(None, None, 0, 0, None, None, None) == 1
+    assert (cfg.induced, cfg.subtree_level) == (0, 1)
+    offs = (ctypes.c_int32 * 2)(0, 0)
+    for field, value in [("induced", 3), ("induced", -1), ("subtree_level", 0),
+                         ("subtree_level", 3)]:
+        bad = mce.Config()
+        lib.mce_config_default(ctypes.byref(bad))
+        setattr(bad, field, value)
+        assert lib.mce_create(offs, None, 1, 0, ctypes.byref(bad), None, ctypes.byref(out)) == 1
+        assert out.value is None
     assert lib.mce_count(None, None, None) == 1
     assert lib.mce_count_roots(None, None, None, 0, None) == 1
     assert lib.mce_order(None, None) == 1
