@@ -70,6 +70,8 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--induced", type=int, default=0, choices=[0, 1, 2],
                    help="induced subgraphs: 0 the Delta/d rule (default), 1 full, 2 partial")
+    p.add_argument("--subtree-level", type=int, default=1, choices=[1, 2],
+                   help="independent subtrees: 1 first-level (default), 2 second-level (per edge)")
     return p.parse_args()
 
 
@@ -129,6 +131,7 @@ def workload_config(args, g, roots, pc, d):
         "root_fraction": args.root_fraction,
         "l2": "flushed between steps (256 MiB write, untimed)",
         "induced": {0: "Delta/d rule", 1: "full", 2: "partial"}[getattr(args, "induced", 0)],
+        "subtree_level": getattr(args, "subtree_level", 1),
     }
 
 
@@ -213,7 +216,8 @@ def run_gb300(args, rank, world, local):
     g = workload_graph(args)
     dev_offs = torch.from_numpy(g.offsets).cuda()
     dev_adj = torch.from_numpy(g.adj).cuda()
-    h = mce.Graph(dev_offs, dev_adj, g.n, profile=1, induced=args.induced)
+    h = mce.Graph(dev_offs, dev_adj, g.n, profile=1, induced=args.induced,
+                  subtree_level=args.subtree_level)
     rank_arr, _ = h.order_arrays()
     roots, pc = light_roots(g, rank_arr.cpu().numpy(), args.max_p)
     if args.root_fraction < 1.0:
@@ -336,7 +340,8 @@ def e2e_leg(args, g, roots, world):
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        h = mce.Graph(offs, adj, g.n, induced=args.induced)   # host pointers: copied in
+        h = mce.Graph(offs, adj, g.n, induced=args.induced,   # host pointers: copied in
+                      subtree_level=args.subtree_level)
         r = roots_h.to("cuda", non_blocking=True)
         out = h.count_roots(r)
         res_h = out.to("cpu", non_blocking=True)

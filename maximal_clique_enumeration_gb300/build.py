@@ -13,7 +13,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libmce_gb300.so")
 PROBE_PATH = os.path.join(BUILD_DIR, "libmce_probe.so")
-SOURCES = ["api.cu", "ingest.cu", "order.cu", "search.cu", "search_full.cu", "search_partial.cu"]
+SOURCES = ["api.cu", "ingest.cu", "order.cu", "search.cu", "search_full.cu", "search_partial.cu",
+           "search_full_l2.cu", "search_partial_l2.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          f"-I{INCLUDE}", f"-I{CSRC}"]

@@ -126,6 +126,7 @@ mce_status run_search(mce_graph *h, cudaStream_t s, bool user_roots, const DevOu
     }
     a.roots = user_roots ? h->g.uroots : h->g.sched;
     a.range = user_roots ? h->g.ctrl->ucls : h->g.ctrl->cls;
+    a.uoff = user_roots ? h->g.uroots_uoff : h->g.sched_uoff;
     a.ws = h->ws;
     a.ring = h->ring;
     a.ring_seq = h->ring_seq;
@@ -287,6 +288,12 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
         }
     }
     g.ip = h->cfg.induced == 2 ? 1 : 0;
+    g.l2 = h->cfg.subtree_level == 2 ? 1 : 0;
+    if (g.l2) {
+        MCE_ALLOC(h, g.unit_cnt, (size_t)n + 1);
+        MCE_ALLOC(h, g.sched_uoff, (size_t)n + 1);
+        MCE_ALLOC(h, g.unit_scan, (size_t)n / kScanBlock + 2);
+    }
     {
         mce_status so = order_impl(h, s);
         if (so != MCE_OK) return so;
@@ -323,8 +330,8 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
     int class_per_sm[kNumClasses] = {};
     for (int k = 0; k < kNumClasses; ++k) {
         h->cls_smem[k] = search_smem_bytes(k, h->hist_len, wpb);
-        MCE_TRY(search_configure(k, g.ip, h->cls_smem[k]));
-        MCE_TRY(search_occupancy(k, g.ip, h->search_threads, h->cls_smem[k], &class_per_sm[k]));
+        MCE_TRY(search_configure(k, g.ip, g.l2, h->cls_smem[k]));
+        MCE_TRY(search_occupancy(k, g.ip, g.l2, h->search_threads, h->cls_smem[k], &class_per_sm[k]));
         if (class_per_sm[k] < 1) return MCE_ERR_CUDA;
         if (h->cfg.blocks_per_sm > 0 && h->cfg.blocks_per_sm < class_per_sm[k])
             class_per_sm[k] = h->cfg.blocks_per_sm;
@@ -376,7 +383,8 @@ mce_status mce_create(const int32_t *offsets, const int32_t *adj, int32_t n, int
     if (cfg) h->cfg = *cfg;
     else mce_config_default(&h->cfg);
     if (h->cfg.donate_min_p < 1) h->cfg.donate_min_p = 1;
-    if (h->cfg.induced < 0 || h->cfg.induced > 2 || h->cfg.subtree_level != 1) {
+    if (h->cfg.induced < 0 || h->cfg.induced > 2 || h->cfg.subtree_level < 1 ||
+        h->cfg.subtree_level > 2) {
         delete h;
         return MCE_ERR_INVALID_ARG;
     }
@@ -403,7 +411,8 @@ static mce_status order_impl(mce_graph *h, cudaStream_t s)
         MCE_TRY(cudaEventRecord(h->ev_order[1], s));
         h->order_timed = true;
     }
-    h->launches_order = h->n > 0 ? 4 : 0;                   // peel + 3 orient kernels
+    // peel, orient count/scan/scatter, 3-pass scan, split (+ subtree count and its scan)
+    h->launches_order = h->n > 0 ? (h->g.l2 ? 12 : 8) : 0;
     return MCE_OK;
 }
 
@@ -427,9 +436,20 @@ static mce_status count_impl(mce_graph *h, cudaStream_t s, const int32_t *d_root
             int *buf = nullptr;
             MCE_ALLOC(h, buf, (size_t)n_roots);
             h->g.uroots = buf;
+            if (h->g.l2) {
+                // second-level subtrees: their prefix over the caller's roots, and scan scratch
+                const size_t len = (size_t)(n_roots > h->n ? n_roots : h->n);
+                MCE_ALLOC(h, h->g.uroots_uoff, (size_t)n_roots + 1);
+                MCE_ALLOC(h, h->g.unit_cnt, len + 1);
+                MCE_ALLOC(h, h->g.unit_scan, len / kScanBlock + 2);
+            }
             h->uroots_cap = n_roots;
         }
         MCE_TRY(launch_bin_roots(h->g, d_roots, (int)n_roots, s));
+        if (h->g.l2) {
+            MCE_TRY(launch_unit_offsets(h->g, h->g.uroots, (int)n_roots, h->g.uroots_uoff, s));
+            h->launches_count += 4;
+        }
     }
     mce_status st = run_search(h, s, d_roots != nullptr, nullptr);
     if (st != MCE_OK) return st;
@@ -540,7 +560,7 @@ mce_status mce_get_info(mce_graph *h, mce_info *info)
     info->n_workers = h->n_workers;
     info->workspace_bytes = (long long)(h->ws_words * 4ULL);
     info->induced = h->g.ip ? 2 : 1;
-    info->subtree_level = 1;
+    info->subtree_level = h->g.l2 ? 2 : 1;
     info->tree_nodes = c.tree_nodes;
     info->donations = c.donations;
     for (int k = 0; k < kNumClasses; ++k) {

@@ -73,6 +73,11 @@ struct DevGraph {
     int *blk_cnt, *blk_min, *blk_cm;   // peel per-CTA reports [2][grid]
     long long *blk_rd;                 // peel: adjacency entries removed per CTA [grid]
     int ip;           // search over partial induced subgraphs (rows for P only), Section 3.4
+    int l2;           // independent second-level subtrees, one per edge (Section 3.2)
+    int *unit_cnt;    // l2: subtrees per root, in schedule order (scan input) [n]
+    int *sched_uoff;  // l2: exclusive prefix of subtrees over sched [n+1]
+    int *uroots_uoff; // l2: the same over uroots [n+1]
+    int *unit_scan;   // l2: exclusive-scan partials of unit_cnt
     int *bucket;      // orient: schedule bucket histogram / cursors [kNumBuckets]
     int *ubucket;     // the same for a caller's root list [kNumBuckets]
     int *uroots;      // a caller's roots, grouped by row width, heaviest first
@@ -96,6 +101,7 @@ struct SearchArgs {
     DevOut out;
     const int *roots;        // g.sched or g.uroots
     const int *range;        // roots[range[2 group] .. range[2 group + 1]) are this launch's
+    const int *uoff;         // second-level subtrees: prefix of subtree counts over roots[]
     int cls;                 // row-width class of this launch (W = 1 << cls)
     int group;               // launch group (2 cls + 0 for big-workspace roots, + 1 otherwise)
     unsigned int *ws;        // per-warp workspace, ws_words each
@@ -126,6 +132,11 @@ __host__ __device__ inline int wclass_index(int np)
 // Per-warp workspace layout (32-bit word offsets) for a root of degree `deg` with np later
 // neighbours.  The same layout serves a branch of such a root donated through the worker list:
 // the donor writes the branch into the receiver's workspace at these offsets.
+//
+// ip: partial induced subgraphs (no X rows).  l2: the layout also holds every second-level
+// subtree {v, w} of the root v (Algorithm 4): its P (at most |P(v)|) and X (at most deg(v) - 1
+// vertices, some of them later than v) fit once the X lists are sized by deg rather than by
+// deg - np; its rows (P rows, then X rows) fit in the deg * W words of rows.
 constexpr int kWsHeader = 80;   // inbox: 16 scalar words, then P and X_P bitsets (32 words each)
 
 struct WsLayout {
@@ -133,14 +144,14 @@ struct WsLayout {
     int W, LV;
 };
 
-__host__ __device__ inline WsLayout ws_layout(int deg, int np, bool ip)
+__host__ __device__ inline WsLayout ws_layout(int deg, int np, bool ip, bool l2)
 {
     WsLayout l;
-    const int nx = deg - np;
+    const int nx = l2 ? deg : deg - np;
     l.W = wclass(np);
     long long o = kWsHeader;
     l.rowsP = o; o += (long long)np * l.W;       // rows of P vertices, columns over P
-    l.rowsX = o; o += ip ? 0 : (long long)nx * l.W;   // rows of X vertices (full subgraphs only)
+    l.rowsX = o; o += ip ? 0 : (long long)(deg - np) * l.W;   // X rows (full subgraphs only)
     l.pids = o; o += np;                         // original ids of P vertices (ascending)
     o = (o + 1) & ~1LL;
     l.pkey = o; o += 2LL * np;                   // vertex keys of P vertices (uint64)
@@ -166,11 +177,11 @@ constexpr int kNumBuckets = 1 + kNumGroups * kCostBuckets;
 __host__ __device__ inline int group_at(int o) { return 2 * (kNumClasses - 1 - o / 2) + (o & 1); }
 __host__ __device__ inline int position_of(int g) { return 2 * (kNumClasses - 1 - g / 2) + (g & 1); }
 
-__device__ inline int sched_bucket(int np, int deg, bool ip)
+__device__ inline int sched_bucket(int np, int deg, bool ip, bool l2)
 {
     if (np > kMaxP) return 0;
     const int k = wclass_index(np);
-    const int b = np > 0 && ws_layout(deg, np, ip).total > kWsCapWords ? 0 : 1;
+    const int b = np > 0 && ws_layout(deg, np, ip, l2).total > kWsCapWords ? 0 : 1;
     const unsigned long long est = (unsigned long long)deg * (unsigned long long)(np + 1);
     int lb = est ? 63 - __clzll((long long)est) : 0;
     lb = lb < kCostBuckets - 1 ? lb : kCostBuckets - 1;
@@ -190,7 +201,8 @@ cudaError_t launch_order(const DevGraph &g, int peel_blocks, long long spin_limi
 cudaError_t launch_search(const SearchArgs &a, int blocks, int threads, size_t smem,
                           cudaStream_t s);
 cudaError_t launch_search_prep(const SearchArgs &a, cudaStream_t s);
-cudaError_t search_occupancy(int cls, int ip, int threads, size_t smem, int *blocks_per_sm);
+cudaError_t search_occupancy(int cls, int ip, int l2, int threads, size_t smem,
+                             int *blocks_per_sm);
 // Shared memory of the search kernel of class k: the size histogram, then per warp a hash of
 // P(v) (ids and local indices) and a staging row.
 __host__ __device__ inline int hash_slots(int k) { return 64 << k; }
@@ -207,8 +219,13 @@ __host__ __device__ inline size_t search_smem_bytes(int k, int hist_len, int war
     const size_t hist = ((size_t)(hist_len + 1) * 8 + 15) & ~(size_t)15;
     return hist + (size_t)warps * warp_smem_bytes(k);
 }
-cudaError_t search_configure(int cls, int ip, size_t smem);
+cudaError_t search_configure(int cls, int ip, int l2, size_t smem);
 cudaError_t launch_bin_roots(const DevGraph &g, const int *roots, int n_roots, cudaStream_t s);
+// Second-level subtrees: uoff[i] = number of subtrees of roots[0 .. i) (edges to later
+// neighbours; 1 for an isolated root), i <= n_roots; n_roots < 0 reads the schedule length
+// from the control block.
+cudaError_t launch_unit_offsets(const DevGraph &g, const int *roots, int n_roots, int *uoff,
+                                cudaStream_t s);
 cudaError_t launch_finalize(const DevGraph &g, const DevOut &o, unsigned long long *d_out,
                             int include_isolated, cudaStream_t s);
 cudaError_t launch_enum_layout(const DevGraph &g, const unsigned long long *d_counts,

@@ -398,10 +398,10 @@ __global__ void __launch_bounds__(kOrientThreads) orient_count_kernel(DevGraph g
                 iso_hash += mix64(vertex_key(v));
             }
             if (c > 0) {
-                atomicAdd(&s_bucket[sched_bucket(c, deg, g.ip)], 1);
+                atomicAdd(&s_bucket[sched_bucket(c, deg, g.ip, g.l2)], 1);
                 maxp = max(maxp, c);
                 if (c <= kMaxP) {
-                    const unsigned long long need = (unsigned long long)ws_layout(deg, c, g.ip).total;
+                    const unsigned long long need = (unsigned long long)ws_layout(deg, c, g.ip, g.l2).total;
                     ws = need > ws ? need : ws;
                     const int gi = 2 * wclass_index(c) + (need > (unsigned long long)kWsCapWords ? 0 : 1);
                     ws_grp[gi] = need > ws_grp[gi] ? need : ws_grp[gi];
@@ -453,7 +453,7 @@ __global__ void __launch_bounds__(kOrientThreads) orient_scatter_kernel(DevGraph
 {
     for (int v = blockIdx.x * blockDim.x + threadIdx.x; v < g.n; v += gridDim.x * blockDim.x) {
         const int c = g.pcount[v];
-        if (c > 0) g.sched[atomicAdd(&g.bucket[sched_bucket(c, g.offs[v + 1] - g.offs[v], g.ip)], 1)] = v;
+        if (c > 0) g.sched[atomicAdd(&g.bucket[sched_bucket(c, g.offs[v + 1] - g.offs[v], g.ip, g.l2)], 1)] = v;
     }
 }
 
@@ -536,7 +536,7 @@ __global__ void __launch_bounds__(kOrientThreads) bin_count_kernel(DevGraph g, c
             set_status(g.ctrl, MCE_ERR_ID_RANGE);
             continue;
         }
-        atomicAdd(&g.ubucket[sched_bucket(g.pcount[v], g.offs[v + 1] - g.offs[v], g.ip)], 1);
+        atomicAdd(&g.ubucket[sched_bucket(g.pcount[v], g.offs[v + 1] - g.offs[v], g.ip, g.l2)], 1);
     }
 }
 
@@ -552,7 +552,7 @@ __global__ void __launch_bounds__(kOrientThreads) bin_scatter_kernel(DevGraph g,
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_roots; i += gridDim.x * blockDim.x) {
         const int v = roots[i];
         if (v < 0 || v >= g.n) continue;
-        g.uroots[atomicAdd(&g.ubucket[sched_bucket(g.pcount[v], g.offs[v + 1] - g.offs[v], g.ip)], 1)] = v;
+        g.uroots[atomicAdd(&g.ubucket[sched_bucket(g.pcount[v], g.offs[v + 1] - g.offs[v], g.ip, g.l2)], 1)] = v;
     }
 }
 
@@ -568,6 +568,39 @@ cudaError_t launch_bin_roots(const DevGraph &g, const int *roots, int n_roots, c
     bin_count_kernel<<<b, kOrientThreads, 0, s>>>(g, roots, n_roots);
     bin_scan_kernel<<<1, 32, 0, s>>>(g);
     bin_scatter_kernel<<<b, kOrientThreads, 0, s>>>(g, roots, n_roots);
+    return cudaGetLastError();
+}
+
+// Second-level subtrees of each root (Algorithm 4): one per later neighbour w, i.e. per edge
+// {v, w} ordered v before w; an isolated root has one, which reports the clique {v}.
+__global__ void __launch_bounds__(kOrientThreads) unit_count_kernel(DevGraph g, const int *roots,
+                                                                   int n_roots, int n_slots)
+{
+    const int len = n_roots >= 0 ? n_roots : (int)g.ctrl->n_sched;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_slots; i += gridDim.x * blockDim.x) {
+        int c = 0;
+        if (i < len) {
+            const int v = roots[i];
+            const int p = g.pcount[v];
+            c = p > 0 ? p : (g.offs[v + 1] == g.offs[v] ? 1 : 0);
+        }
+        g.unit_cnt[i] = c;
+    }
+}
+
+cudaError_t launch_unit_offsets(const DevGraph &g, const int *roots, int n_roots, int *uoff,
+                                cudaStream_t s)
+{
+    const int n_slots = n_roots >= 0 ? n_roots : g.n;
+    cudaError_t e = cudaMemsetAsync(uoff, 0, sizeof(int), s);
+    if (e != cudaSuccess || n_slots == 0) return e;
+    int b = (n_slots + kOrientThreads - 1) / kOrientThreads;
+    if (b > 4096) b = 4096;
+    unit_count_kernel<<<b, kOrientThreads, 0, s>>>(g, roots, n_roots, n_slots);
+    const int nb = (n_slots + kScanBlock - 1) / kScanBlock;
+    scan_partial_kernel<<<nb, kScanThreads, 0, s>>>(g.unit_cnt, n_slots, g.unit_scan);
+    scan_sums_kernel<<<1, 1024, 0, s>>>(g.unit_scan, nb);
+    scan_final_kernel<<<nb, kScanThreads, 0, s>>>(g.unit_cnt, n_slots, g.unit_scan, uoff);
     return cudaGetLastError();
 }
 
@@ -603,6 +636,11 @@ cudaError_t launch_order(const DevGraph &g, int peel_blocks, long long spin_limi
     scan_sums_kernel<<<1, 1024, 0, s>>>(g.scan_tmp, nb);
     scan_final_kernel<<<nb, kScanThreads, 0, s>>>(g.pcount, g.n, g.scan_tmp, g.poffs);
     orient_split_kernel<<<blocks, kOrientThreads, 0, s>>>(g);
+    if (g.l2) {
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        return launch_unit_offsets(g, g.sched, -1, g.sched_uoff, s);
+    }
     return cudaGetLastError();
 }
 

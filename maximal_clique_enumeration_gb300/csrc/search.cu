@@ -79,24 +79,28 @@ __global__ void enum_close_kernel(DevOut o, const long long *totals)
 
 }  // namespace
 
-// Kernel instances, one translation unit per induced-subgraph variant (built in parallel).
+// Kernel instances, one translation unit per variant (built in parallel): full or partial
+// induced subgraphs, first- or second-level subtrees.
 const void *search_kernel_full(int cls);
 const void *search_kernel_partial(int cls);
+const void *search_kernel_full_l2(int cls);
+const void *search_kernel_partial_l2(int cls);
 
-static const void *search_kernel_ptr(int cls, int ip)
+static const void *search_kernel_ptr(int cls, int ip, int l2)
 {
+    if (l2) return ip ? search_kernel_partial_l2(cls) : search_kernel_full_l2(cls);
     return ip ? search_kernel_partial(cls) : search_kernel_full(cls);
 }
 
-cudaError_t search_configure(int cls, int ip, size_t smem)
+cudaError_t search_configure(int cls, int ip, int l2, size_t smem)
 {
-    return cudaFuncSetAttribute(search_kernel_ptr(cls, ip),
+    return cudaFuncSetAttribute(search_kernel_ptr(cls, ip, l2),
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
 }
 
-cudaError_t search_occupancy(int cls, int ip, int threads, size_t smem, int *blocks_per_sm)
+cudaError_t search_occupancy(int cls, int ip, int l2, int threads, size_t smem, int *blocks_per_sm)
 {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, search_kernel_ptr(cls, ip),
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, search_kernel_ptr(cls, ip, l2),
                                                          threads, smem);
 }
 
@@ -105,7 +109,7 @@ cudaError_t launch_search(const SearchArgs &a, int blocks, int threads, size_t s
 {
     SearchArgs aa = a;
     void *args[] = {&aa};
-    return cudaLaunchKernel(search_kernel_ptr(a.cls, a.g.ip), dim3(blocks), dim3(threads), args,
+    return cudaLaunchKernel(search_kernel_ptr(a.cls, a.g.ip, a.g.l2), dim3(blocks), dim3(threads), args,
                             smem, s);
 }
 

@@ -1,5 +1,6 @@
-// Search kernels over full induced subgraphs, one per row width.
+// Search kernels over full induced subgraphs of first-level subtrees, one per row width.
 #define MCE_SEARCH_IP 0
+#define MCE_SEARCH_L2 0
 #include "search_impl.cuh"
 
 namespace mce {

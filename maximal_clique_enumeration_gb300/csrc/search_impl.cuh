@@ -31,8 +31,10 @@
 // Which induced subgraph the including translation unit builds (Section 3.4): 0 = full (rows
 // for every vertex of P u X), 1 = partial (rows for P only; P-X adjacencies are looked up in
 // the original graph, and the pivot comes from P u X_P).
-#ifndef MCE_SEARCH_IP
-#error "define MCE_SEARCH_IP before including search_impl.cuh"
+// And which subtrees it searches: 0 = first-level (one per vertex, Algorithm 3), 1 =
+// second-level (one per edge, Algorithm 4).
+#if !defined(MCE_SEARCH_IP) || !defined(MCE_SEARCH_L2)
+#error "define MCE_SEARCH_IP and MCE_SEARCH_L2 before including search_impl.cuh"
 #endif
 
 namespace mce {
@@ -41,6 +43,7 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr bool kIP = MCE_SEARCH_IP != 0;
+constexpr bool kL2 = MCE_SEARCH_L2 != 0;
 
 template <int W>
 struct Geo {
@@ -228,11 +231,13 @@ struct RootCtx {
     int *rids, *xids, *xx, *spill, *plist;
     unsigned *stack;
     int deg, np, nx, LV;
-    int rsize;          // |R| at level 0 (1 for a first-level root)
+    int rsize;          // |R| at level 0 (1 for a first-level root, 2 for a second-level one)
+    int lay_deg, lay_np;   // the workspace layout in use: that of a root of this degree and |P|
 };
 
 // Inbox header of a warp workspace (word offsets) and inbox states.
-enum { kHdrDeg = 0, kHdrNp = 1, kHdrK = 2, kHdrRsize = 3, kHdrS = 4, kHdrP = 16, kHdrXP = 48 };
+enum { kHdrDeg = 0, kHdrNp = 1, kHdrK = 2, kHdrRsize = 3, kHdrS = 4, kHdrLayDeg = 6,
+       kHdrLayNp = 7, kHdrP = 16, kHdrXP = 48 };
 enum : int { kInboxIdle = 0, kInboxFull = 1, kInboxRetired = 2, kInboxClaimed = 4 };
 constexpr long long kDonateCheckCycles = 2048;   // a donor looks at the worker list this often
 
@@ -240,12 +245,16 @@ using dev_int = cuda::atomic_ref<int, cuda::thread_scope_device>;
 using dev_uint = cuda::atomic_ref<unsigned, cuda::thread_scope_device>;
 using dev_ull = cuda::atomic_ref<unsigned long long, cuda::thread_scope_device>;
 
-__device__ __forceinline__ RootCtx make_ctx(unsigned *ws, int deg, int np)
+// Regions of a workspace laid out for a root of degree lay_deg with lay_np later neighbours,
+// holding a subtree with np vertices in P and nx in X (the same sizes for a first-level root;
+// at most those for a second-level subtree of that root).  X rows follow the P rows.
+template <int W>
+__device__ __forceinline__ RootCtx make_ctx(unsigned *ws, int lay_deg, int lay_np, int np, int nx)
 {
-    const WsLayout lay = ws_layout(deg, np, kIP);
+    const WsLayout lay = ws_layout(lay_deg, lay_np, kIP, kL2);
     RootCtx r;
     r.rowsP = ws + lay.rowsP;
-    r.rowsX = ws + lay.rowsX;
+    r.rowsX = r.rowsP + (long long)np * W;
     r.pids = reinterpret_cast<int *>(ws + lay.pids);
     r.pkey = reinterpret_cast<unsigned long long *>(ws + lay.pkey);
     r.rids = reinterpret_cast<int *>(ws + lay.rids);
@@ -254,11 +263,13 @@ __device__ __forceinline__ RootCtx make_ctx(unsigned *ws, int deg, int np)
     r.spill = reinterpret_cast<int *>(ws + lay.spill);
     r.plist = reinterpret_cast<int *>(ws + lay.plist);
     r.stack = ws + lay.stack;
-    r.deg = deg;
+    r.deg = np + nx;
     r.np = np;
-    r.nx = deg - np;
+    r.nx = nx;
     r.LV = lay.LV;
     r.rsize = 1;
+    r.lay_deg = lay_deg;
+    r.lay_np = lay_np;
     return r;
 }
 
@@ -322,6 +333,18 @@ __device__ __forceinline__ int list_bits(const Ck<Geo<W>::CH> &b, int *out, int 
     }
     __syncwarp();
     return cnt;
+}
+
+// Is id in the id-sorted list a[lo .. hi)?
+__device__ __forceinline__ bool sorted_has(const int *a, int lo, int hi, int id)
+{
+    const int end = hi;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(a + mid) < id) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo < end && __ldg(a + lo) == id;
 }
 
 // Partial induced subgraphs: is the X vertex x adjacent to the P vertex p?  p comes after x in
@@ -501,11 +524,13 @@ __device__ void write_branch(const RootCtx &r, unsigned *dst, int L, int c,
 {
     constexpr int CH = Geo<W>::CH, G = Geo<W>::G;
     const int q = lane % G;
-    const WsLayout lay = ws_layout(r.deg, r.np, kIP);
+    const WsLayout lay = ws_layout(r.lay_deg, r.lay_np, kIP, kL2);
     const int rsize = r.rsize + L + 1;
     if (lane == 0) {
         dst[kHdrDeg] = (unsigned)r.deg;
         dst[kHdrNp] = (unsigned)r.np;
+        dst[kHdrLayDeg] = (unsigned)r.lay_deg;
+        dst[kHdrLayNp] = (unsigned)r.lay_np;
         dst[kHdrK] = (unsigned)k;
         dst[kHdrRsize] = (unsigned)rsize;
         *reinterpret_cast<unsigned long long *>(dst + kHdrS) = Sc;
@@ -530,7 +555,7 @@ __device__ void write_branch(const RootCtx &r, unsigned *dst, int L, int c,
         for (long long t = lane; t < (long long)k * W; t += 32) {
             const long long i = t / W;
             const int x = r.xx[i];
-            dst[lay.rowsX + t] = r.rowsX[(long long)x * W + (t - i * W)];
+            dst[lay.rowsP + (long long)r.np * W + t] = r.rowsX[(long long)x * W + (t - i * W)];
         }
     }
     for (int i = lane; i < k; i += 32) dxx[i] = i;
@@ -779,30 +804,18 @@ __device__ void build_flat(const SearchArgs &a, const RootCtx &r, const WarpSmem
 // X precedes v and so precedes every p in P, hence p is in N+(u); a pair of P vertices is found
 // from the earlier of the two.  Membership in P is a shared-memory hash lookup, so the build
 // reads the bounded lists N+(u) (each at most d long) with coalesced loads and no search.
+// Builds the induced subgraph of the subtree in r (its P and X ids already in r.pids, r.xids;
+// R in r.rids) into the warp's workspace, or into shared memory when the rows fit, and searches
+// it from R's key sum S.
 template <int W>
-__device__ void search_root(const SearchArgs &a, unsigned *ws, const WarpSmem &sm, int v, int deg,
-                            int np, bool big, Acc &acc, unsigned long long *s_hist, int lane)
+__device__ void build_and_search(const SearchArgs &a, RootCtx r, const WarpSmem &sm, bool big,
+                                 unsigned long long S, Acc &acc, unsigned long long *s_hist,
+                                 int lane)
 {
     constexpr int CH = Geo<W>::CH, G = Geo<W>::G;
     PROF_START(t_build);
-    RootCtx r = make_ctx(ws, deg, np);
-    const int *Nv = a.g.adj + a.g.offs[v];
-    const int rv = a.g.rank[v];
+    const int np = r.np, deg = r.deg;
     const unsigned lt = (1u << lane) - 1u;
-    // split N(v) into P (later) and X (earlier), numbering each part in id order
-    int pi = 0, xi = 0;
-    for (int base = 0; base < deg; base += 32) {
-        const int j = base + lane;
-        const bool in = j < deg;
-        const int w = in ? __ldg(Nv + j) : 0;
-        const bool isP = in && __ldg(a.g.rank + w) > rv;
-        const unsigned mp = __ballot_sync(kFull, isP);
-        const unsigned mx = __ballot_sync(kFull, in && !isP);
-        if (isP) r.pids[pi + __popc(mp & lt)] = w;
-        else if (in) r.xids[xi + __popc(mx & lt)] = w;
-        pi += __popc(mp);
-        xi += __popc(mx);
-    }
     // rows in shared memory when they fit (normal roots only), else in the workspace; zero the
     // rows (the big-root build writes X rows whole when they are at most 4 words wide)
     if (!big && (long long)(kIP ? np : deg) * W <= sm.rows_words) {
@@ -819,7 +832,6 @@ __device__ void search_root(const SearchArgs &a, unsigned *ws, const WarpSmem &s
     WarpSmem h = sm;
     h.slots = slots;
     for (int i = lane; i < slots; i += 32) h.hkey[i] = -1;
-    if (lane == 0) r.rids[0] = v;
     __syncwarp();
     for (int i = lane; i < np; i += 32) {
         const int id = r.pids[i];
@@ -947,7 +959,96 @@ __device__ void search_root(const SearchArgs &a, unsigned *ws, const WarpSmem &s
     __syncwarp();
     PROF_ADD(acc, kProfBuild, t_build);
     const int q = lane % G;
-    dfs<W>(a, r, bits_prefix<W>(np, q), ck_zero<CH>(), nxx, vertex_key(v), acc, s_hist, lane);
+    dfs<W>(a, r, bits_prefix<W>(np, q), ck_zero<CH>(), nxx, S, acc, s_hist, lane);
+}
+
+// First-level subtree of root v (Algorithm 3): P = later neighbours, X = earlier ones.
+//
+// Rows: for u in N(v), row(u) has bit i set iff u is adjacent to the i-th vertex of P (the
+// binary-encoded induced subgraph over P u X, Section 3.4's full variant).  Every such
+// adjacency u - p with p in P is found by streaming the later-neighbour list N+(u): a vertex of
+// X precedes v and so precedes every p in P, hence p is in N+(u); a pair of P vertices is found
+// from the earlier of the two.  Membership in P is a shared-memory hash lookup, so the build
+// reads the bounded lists N+(u) (each at most d long) with coalesced loads and no search.
+template <int W>
+__device__ void search_root(const SearchArgs &a, unsigned *ws, const WarpSmem &sm, int v, int deg,
+                            int np, bool big, Acc &acc, unsigned long long *s_hist, int lane)
+{
+    RootCtx r = make_ctx<W>(ws, deg, np, np, deg - np);
+    const int *Nv = a.g.adj + a.g.offs[v];
+    const int rv = a.g.rank[v];
+    const unsigned lt = (1u << lane) - 1u;
+    // split N(v) into P (later) and X (earlier), numbering each part in id order
+    int pi = 0, xi = 0;
+    for (int base = 0; base < deg; base += 32) {
+        const int j = base + lane;
+        const bool in = j < deg;
+        const int w = in ? __ldg(Nv + j) : 0;
+        const bool isP = in && __ldg(a.g.rank + w) > rv;
+        const unsigned mp = __ballot_sync(kFull, isP);
+        const unsigned mx = __ballot_sync(kFull, in && !isP);
+        if (isP) r.pids[pi + __popc(mp & lt)] = w;
+        else if (in) r.xids[xi + __popc(mx & lt)] = w;
+        pi += __popc(mp);
+        xi += __popc(mx);
+    }
+    if (lane == 0) r.rids[0] = v;
+    build_and_search<W>(a, r, sm, big, vertex_key(v), acc, s_hist, lane);
+}
+
+// Second-level subtree of the edge {v, w}, v before w (Algorithm 4): R = {v, w},
+// P = N(v) n N(w) after w = N+(v) n N+(w), X = N(v) n N(w) before w.  The workspace keeps the
+// layout of root v, which holds any of its second-level subtrees.
+template <int W>
+__device__ void search_edge(const SearchArgs &a, unsigned *ws, const WarpSmem &sm, int v, int w,
+                            bool big, Acc &acc, unsigned long long *s_hist, int lane)
+{
+    const DevGraph &g = a.g;
+    const int degv = g.offs[v + 1] - g.offs[v];
+    RootCtx r = make_ctx<W>(ws, degv, g.pcount[v], 0, 0);
+    const unsigned lt = (1u << lane) - 1u;
+    // P: the later neighbours of v that are later neighbours of w too (both lists id-sorted)
+    const int pv1 = g.poffs[v + 1], pw0 = g.poffs[w], pw1 = g.poffs[w + 1];
+    int np = 0;
+    for (int j0 = g.poffs[v]; j0 < pv1; j0 += 32) {
+        const int j = j0 + lane;
+        const int u = j < pv1 ? __ldg(g.padj + j) : -1;
+        const bool in = u >= 0 && sorted_has(g.padj, pw0, pw1, u);
+        const unsigned m = __ballot_sync(kFull, in);
+        if (in) r.pids[np + __popc(m & lt)] = u;
+        np += __popc(m);
+    }
+    // X: walk the shorter of N(v), N(w) and search the other; keep what comes before w
+    const int rw = g.rank[w];
+    const int degw = g.offs[w + 1] - g.offs[w];
+    const bool walk_v = degv <= degw;
+    const int a0 = walk_v ? g.offs[v] : g.offs[w], a1 = walk_v ? g.offs[v + 1] : g.offs[w + 1];
+    const int b0 = walk_v ? g.offs[w] : g.offs[v], b1 = walk_v ? g.offs[w + 1] : g.offs[v + 1];
+    int nx = 0;
+    for (int j0 = a0; j0 < a1; j0 += 32) {
+        const int j = j0 + lane;
+        const int u = j < a1 ? __ldg(g.adj + j) : -1;
+        const bool in = u >= 0 && u != v && u != w && __ldg(g.rank + u) < rw &&
+                        sorted_has(g.adj, b0, b1, u);
+        const unsigned m = __ballot_sync(kFull, in);
+        if (in) r.xids[nx + __popc(m & lt)] = u;
+        nx += __popc(m);
+    }
+    r = make_ctx<W>(ws, degv, g.pcount[v], np, nx);
+    r.rsize = 2;
+    if (lane == 0) {
+        r.rids[0] = v;
+        r.rids[1] = w;
+    }
+    __syncwarp();
+    const unsigned long long S = vertex_key(v) + vertex_key(w);
+    if (np == 0) {
+        // P empty: {v, w} is maximal iff X is empty too
+        if (nx == 0) report(a, r, 0, 0, 2, S, acc, s_hist, lane);
+        acc.nodes++;
+        return;
+    }
+    build_and_search<W>(a, r, sm, big, S, acc, s_hist, lane);
 }
 
 // Searches a branch that another warp wrote into this warp's workspace.
@@ -959,20 +1060,40 @@ __device__ void search_inbox(const SearchArgs &a, unsigned *ws, Acc &acc,
     const int q = lane % G;
     const int deg = (int)ws[kHdrDeg], np = (int)ws[kHdrNp];
     const int k = (int)ws[kHdrK], rsize = (int)ws[kHdrRsize];
-    // a branch always comes from a root of this kernel's class, within its workspace
-    const bool sane = np >= 1 && np <= kMaxP && wclass(np) == W && deg >= np && k >= 0 &&
-                      k <= deg - np && rsize >= 2 && rsize <= np + 1 &&
-                      (unsigned long long)ws_layout(deg, np, kIP).total <= a.ws_words;
+    const int lay_deg = (int)ws[kHdrLayDeg], lay_np = (int)ws[kHdrLayNp];
+    constexpr bool l2 = kL2;
+    // a branch always comes from a root of this kernel's class, within its workspace (a
+    // second-level subtree is at most as large as its root's first-level one)
+    const bool sane = lay_np >= 1 && lay_np <= kMaxP && wclass(lay_np) == W &&
+                      lay_deg >= lay_np && np >= 1 && np <= lay_np && deg >= np &&
+                      deg <= lay_deg && (l2 || (np == lay_np && deg == lay_deg)) && k >= 0 &&
+                      k <= deg - np && rsize >= 2 && rsize <= np + 2 &&
+                      (unsigned long long)ws_layout(lay_deg, lay_np, kIP, l2).total <= a.ws_words;
     if (!sane) {
         if (lane == 0) set_status(a.g.ctrl, MCE_ERR_INTERNAL);
         return;
     }
-    RootCtx r = make_ctx(ws, deg, np);
+    RootCtx r = make_ctx<W>(ws, lay_deg, lay_np, np, deg - np);
     r.rsize = rsize;
     const unsigned long long S = *reinterpret_cast<const unsigned long long *>(ws + kHdrS);
     const Ck<CH> P = ck_load<CH>(ws + kHdrP + q * CH);
     const Ck<CH> XP = ck_load<CH>(ws + kHdrXP + q * CH);
     dfs<W>(a, r, P, XP, k, S, acc, s_hist, lane);
+}
+
+// The last i in [lo, hi) with a[i] <= t, for a non-decreasing a with a[lo] <= t: 32 probes
+// per step, so a schedule of n roots takes about log32(n) rounds of loads.
+__device__ __forceinline__ int last_at_most(const int *a, int lo, int hi, int t, int lane)
+{
+    while (hi - lo > 32) {
+        const int step = (hi - lo + 31) >> 5;
+        const int p = lo + lane * step;
+        const unsigned m = __ballot_sync(kFull, p < hi && __ldg(a + p) <= t);
+        lo += (31 - __clz(m)) * step;
+        hi = min(hi, lo + step);
+    }
+    const unsigned m = __ballot_sync(kFull, lo + lane < hi && __ldg(a + lo + lane) <= t);
+    return lo + 31 - __clz(m);
 }
 
 // CTAs per SM the compiler should plan registers for, per row width (more for narrow rows).
@@ -1012,7 +1133,11 @@ __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(Search
     __syncthreads();
     unsigned *ws = a.ws + (unsigned long long)warp * a.ws_words;
     const unsigned long long begin = (unsigned long long)a.range[2 * a.group];
-    const unsigned long long n_roots = (unsigned long long)a.range[2 * a.group + 1] - begin;
+    const int end = a.range[2 * a.group + 1];
+    // work items: the roots of this launch, or with second-level subtrees their edges
+    const int ubase = kL2 ? a.uoff[begin] : 0;
+    const unsigned long long n_roots = kL2 ? (unsigned long long)(a.uoff[end] - ubase)
+                                           : (unsigned long long)end - begin;
     dev_int busy(a.g.ctrl->busy);
     Acc acc{};
     // phase 1: first-level subtrees from the shared counter
@@ -1026,7 +1151,15 @@ __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(Search
         idx = __shfl_sync(kFull, idx, 0);
         if (idx >= n_roots) break;
         PROF_START(t_root);
-        const int v = a.roots[begin + idx];
+        int pos = (int)(begin + idx), w = -1;
+        if constexpr (kL2) {
+            // the root whose edges hold item idx, and the edge's later end w
+            const int t = ubase + (int)idx;
+            pos = last_at_most(a.uoff, (int)begin, end, t, lane);
+            const int v0 = a.roots[pos];
+            if (a.g.pcount[v0] > 0) w = a.g.padj[a.g.poffs[v0] + (t - a.uoff[pos])];
+        }
+        const int v = a.roots[pos];
         const int deg = a.g.offs[v + 1] - a.g.offs[v];
         const int np = a.g.pcount[v];
         if (np == 0) {
@@ -1041,6 +1174,8 @@ __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(Search
             }
         } else if (np > kMaxP) {
             if (lane == 0) set_status(a.g.ctrl, MCE_ERR_LIMIT);
+        } else if (kL2) {
+            if (w >= 0) search_edge<W>(a, ws, sm, v, w, (a.group & 1) == 0, acc, s_hist, lane);
         } else {
             search_root<W>(a, ws, sm, v, deg, np, (a.group & 1) == 0, acc, s_hist, lane);
         }
