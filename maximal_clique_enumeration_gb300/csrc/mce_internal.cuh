@@ -26,8 +26,8 @@ struct DevCtrl {
     int degeneracy;              // peel output
     int rounds;                  // peel output
     int max_pcount;              // max |P| over first-level subtrees
-    unsigned int bar_count;      // grid barrier arrival counter
-    unsigned int bar_gen;        // grid barrier generation
+    unsigned int bar_count;      // grid barrier arrivals (grows by the grid size per barrier)
+    unsigned int bar_pad;
     unsigned long long ws_words; // largest per-warp workspace need (words), all classes
     unsigned long long ws_grp[kNumGroups];    // the same per launch group
     unsigned long long next_root;  // search: root claim counter

@@ -19,6 +19,8 @@
 // later-neighbour lists N+(v) as a CSR (scan of |P|, then a stable split of each adjacency).
 #include <climits>
 
+#include <cuda/atomic>
+
 #include "mce_internal.cuh"
 
 namespace mce {
@@ -26,36 +28,42 @@ namespace mce {
 namespace {
 
 // Grid-wide barrier for a cooperative launch.  Returns false if the wait exceeded the limit
-// (MCE_ERR_DEVICE_TIMEOUT recorded) or another CTA recorded an error.
+// (MCE_ERR_DEVICE_TIMEOUT recorded) or some CTA recorded an error.
+//
+// The arrival counter only grows: a CTA adds 1 with release order, and the barrier it joined is
+// complete once the counter reaches the next multiple of the grid size (acquire order), so no
+// CTA has to reset anything and the last arrival frees every waiter at once.  The status word is
+// polled beside the counter, so an error elsewhere ends the wait early.
 __device__ bool grid_barrier(DevCtrl *ctrl, long long limit_ns)
 {
     __shared__ int s_ok;
     __syncthreads();
     if (threadIdx.x == 0) {
         int ok = 1;
-        volatile unsigned int *gen = &ctrl->bar_gen;
-        const unsigned int g0 = *gen;
-        __threadfence();
-        if (atomicAdd(&ctrl->bar_count, 1u) == gridDim.x - 1) {
-            atomicExch(&ctrl->bar_count, 0u);
-            __threadfence();
-            atomicAdd((unsigned int *)&ctrl->bar_gen, 1u);
-        } else {
-            const unsigned long long t0 = globaltimer_ns();
-            unsigned int polls = 0;
-            while (*gen == g0) {
-                if ((++polls & 63u) == 1) {              // check the clock now and then
-                    if ((long long)(globaltimer_ns() - t0) > limit_ns) {
-                        set_status(ctrl, MCE_ERR_DEVICE_TIMEOUT);
-                        ok = 0;
-                        break;
-                    }
-                    if (polls > 4096) __nanosleep(128);  // a long wait: stop hammering L2
+        cuda::atomic_ref<unsigned int, cuda::thread_scope_device> count(ctrl->bar_count);
+        const unsigned int nb = gridDim.x;
+        const unsigned int old = count.fetch_add(1u, cuda::memory_order_release);
+        const unsigned int target = (old / nb + 1u) * nb;
+        const volatile int *status = &ctrl->status;
+        const unsigned long long t0 = globaltimer_ns();
+        unsigned int polls = 0;
+        while (true) {
+            const unsigned int c = count.load(cuda::memory_order_acquire);
+            if (*status != 0) {
+                ok = 0;
+                break;
+            }
+            if ((int)(c - target) >= 0) break;
+            if ((++polls & 63u) == 1) {                  // check the clock now and then
+                if ((long long)(globaltimer_ns() - t0) > limit_ns) {
+                    set_status(ctrl, MCE_ERR_DEVICE_TIMEOUT);
+                    ok = 0;
+                    break;
                 }
+                if (polls > 4096) __nanosleep(128);      // a long wait: stop hammering L2
             }
         }
-        __threadfence();
-        s_ok = ok && load_status(ctrl) == 0;
+        s_ok = ok;
     }
     __syncthreads();
     return s_ok != 0;
