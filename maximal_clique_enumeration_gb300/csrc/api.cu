@@ -224,15 +224,21 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
     g.adj = adjm;
 
     // input checks: offsets, id range, sortedness
-    int *d_list = nullptr, *d_nlist = nullptr;
+    // (stats: unsorted lists, long lists, largest degree; fb: forward and backward entries)
+    int *d_list = nullptr, *d_stats = nullptr, *d_big = nullptr;
+    unsigned long long *d_fb = nullptr;
     MCE_ALLOC(h, d_list, (size_t)n + 1);
-    MCE_ALLOC(h, d_nlist, 1);
-    MCE_TRY(cudaMemsetAsync(d_nlist, 0, sizeof(int), s));
-    MCE_TRY(launch_ingest_check(g, d_list, d_nlist, s));
+    MCE_ALLOC(h, d_big, (size_t)n + 1);
+    MCE_ALLOC(h, d_stats, 4);
+    MCE_ALLOC(h, d_fb, 2);
+    MCE_TRY(cudaMemsetAsync(d_stats, 0, 4 * sizeof(int), s));
+    MCE_TRY(cudaMemsetAsync(d_fb, 0, 2 * sizeof(unsigned long long), s));
+    MCE_TRY(launch_ingest_check(g, d_list, d_stats, d_big, s));
     mce_status st = read_status(h, s);
     if (st != MCE_OK) return st;
-    int n_unsorted = 0;
-    MCE_TRY(cudaMemcpy(&n_unsorted, d_nlist, sizeof(int), cudaMemcpyDeviceToHost));
+    int stats[4] = {0, 0, 0, 0};
+    MCE_TRY(cudaMemcpy(stats, d_stats, sizeof(stats), cudaMemcpyDeviceToHost));
+    const int n_unsorted = stats[0];
     if (n_unsorted > 0) {
         MCE_TRY(launch_ingest_sort(g, adjm, d_list, n_unsorted, nullptr, 0, s));
         std::vector<int> list(n_unsorted), hoffs((size_t)n + 1);
@@ -253,9 +259,12 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
             MCE_TRY(launch_ingest_sort_large(g, adjm, v, scratch, s));
         }
     }
-    MCE_TRY(launch_ingest_validate(g, s));
+    MCE_TRY(launch_ingest_validate(g, d_big, stats[1], stats[2], d_fb, s));
     st = read_status(h, s);
     if (st != MCE_OK) return st;
+    unsigned long long fb[2] = {0ULL, 0ULL};
+    MCE_TRY(cudaMemcpy(fb, d_fb, sizeof(fb), cudaMemcpyDeviceToHost));
+    if (fb[0] != fb[1]) return MCE_ERR_NOT_SYMMETRIC;
 
     // degeneracy order buffers
     MCE_ALLOC(h, g.rank, (size_t)n);

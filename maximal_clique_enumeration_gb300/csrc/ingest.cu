@@ -14,11 +14,17 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// Lists longer than this are validated by many CTAs each (validate_big_kernel).
+constexpr int kValidateSplit = 1024;
+constexpr int kValidateChunk = 4096;   // entries per CTA of a long list
+
 // Offsets must be non-decreasing and inside [0, nnz]; adjacency ids inside [0, n).  Lists that
-// are not sorted ascending are appended to `unsorted_list`.
+// are not sorted ascending are appended to `unsorted_list`; stats[1] counts, and big_list
+// receives, the lists longer than kValidateSplit, stats[2] is the largest degree.
 __global__ void __launch_bounds__(kThreads) check_kernel(DevGraph g, int *unsorted_list,
-                                                         int *unsorted_n)
+                                                         int *stats, int *big_list)
 {
+    int *unsorted_n = stats;
     const int lane = threadIdx.x & 31;
     const int warps = gridDim.x * (blockDim.x >> 5);
     for (int v = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; v < g.n; v += warps) {
@@ -37,6 +43,10 @@ __global__ void __launch_bounds__(kThreads) check_kernel(DevGraph g, int *unsort
             if (lane == 0) set_status(g.ctrl, MCE_ERR_ID_RANGE);
         } else if (__any_sync(0xffffffffu, unsorted)) {
             if (lane == 0) unsorted_list[atomicAdd(unsorted_n, 1)] = v;
+        }
+        if (lane == 0 && hi - lo > kValidateSplit) {
+            big_list[atomicAdd(&stats[1], 1)] = v;
+            atomicMax(&stats[2], hi - lo);
         }
     }
 }
@@ -110,25 +120,65 @@ __device__ __forceinline__ bool sorted_contains(const int *a, int len, int key)
     return lo < len && a[lo] == key;
 }
 
-// On sorted lists: no self-loop, no repeated neighbour, and v in N(u) for every u in N(v).
-__global__ void __launch_bounds__(kThreads) validate_kernel(DevGraph g)
+// On sorted lists: no self-loop and no repeated neighbour; and symmetry.  Symmetry is checked on
+// the forward entries only (u in N(v) with u > v: is v in N(u)?), and the forward and backward
+// entries are counted into fb[0], fb[1].  With no repeats, reversal maps forward entries into
+// backward ones injectively, so equal counts make it a bijection: every backward entry has its
+// reverse too.  A warp takes a list of at most kValidateSplit entries (longer ones: below).
+__device__ __forceinline__ void validate_range(const DevGraph &g, int v, int lo, int hi, int first,
+                                               int step, unsigned long long *fb)
+{
+    const int lane = threadIdx.x & 31;
+    bool not_simple = false, asym = false;
+    unsigned nf = 0, nbk = 0;
+    for (int i = first; i < hi; i += step) {
+        const int u = g.adj[i];
+        not_simple |= (u == v) || (i > lo && g.adj[i - 1] == u);
+        if (u > v) {
+            ++nf;
+            const int ulo = g.offs[u];
+            asym |= !sorted_contains(g.adj + ulo, g.offs[u + 1] - ulo, v);
+        } else if (u < v) {
+            ++nbk;
+        }
+    }
+    const unsigned wf = __reduce_add_sync(0xffffffffu, nf);
+    const unsigned wb = __reduce_add_sync(0xffffffffu, nbk);
+    if (lane == 0) {
+        if (wf) atomicAdd(&fb[0], (unsigned long long)wf);
+        if (wb) atomicAdd(&fb[1], (unsigned long long)wb);
+    }
+    if (__any_sync(0xffffffffu, not_simple)) {
+        if (lane == 0) set_status(g.ctrl, MCE_ERR_NOT_SIMPLE);
+    } else if (__any_sync(0xffffffffu, asym)) {
+        if (lane == 0) set_status(g.ctrl, MCE_ERR_NOT_SYMMETRIC);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) validate_kernel(DevGraph g, unsigned long long *fb)
 {
     const int lane = threadIdx.x & 31;
     const int warps = gridDim.x * (blockDim.x >> 5);
     for (int v = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; v < g.n; v += warps) {
         const int lo = g.offs[v], hi = g.offs[v + 1];
-        bool not_simple = false, asym = false;
-        for (int i = lo + lane; i < hi; i += 32) {
-            const int u = g.adj[i];
-            not_simple |= (u == v) || (i > lo && g.adj[i - 1] == u);
-            const int ulo = g.offs[u];
-            asym |= !sorted_contains(g.adj + ulo, g.offs[u + 1] - ulo, v);
-        }
-        if (__any_sync(0xffffffffu, not_simple)) {
-            if (lane == 0) set_status(g.ctrl, MCE_ERR_NOT_SIMPLE);
-        } else if (__any_sync(0xffffffffu, asym)) {
-            if (lane == 0) set_status(g.ctrl, MCE_ERR_NOT_SYMMETRIC);
-        }
+        if (hi - lo > kValidateSplit) continue;
+        validate_range(g, v, lo, hi, lo + lane, 32, fb);
+    }
+}
+
+// A long list: CTA (x, y) takes chunks y, y + gridDim.y, ... of kValidateChunk entries of the
+// list of big_list[x].
+__global__ void __launch_bounds__(kThreads) validate_big_kernel(DevGraph g, const int *big_list,
+                                                                unsigned long long *fb)
+{
+    const int v = big_list[blockIdx.x];
+    const int lo = g.offs[v], hi = g.offs[v + 1];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (long long c0 = lo + (long long)blockIdx.y * kValidateChunk; c0 < hi;
+         c0 += (long long)gridDim.y * kValidateChunk) {
+        const int c1 = (int)(c0 + kValidateChunk < hi ? c0 + kValidateChunk : hi);
+        // warps interleave over the chunk; the repeat test reads the entry before, as above
+        validate_range(g, v, lo, c1, (int)c0 + warp * 32 + lane, kThreads, fb);
     }
 }
 
@@ -142,12 +192,12 @@ int grid_for(long long work_items, int per_block)
 
 }  // namespace
 
-cudaError_t launch_ingest_check(const DevGraph &g, int *d_unsorted_list, int *d_unsorted_n,
-                                cudaStream_t s)
+cudaError_t launch_ingest_check(const DevGraph &g, int *d_unsorted_list, int *d_stats,
+                                int *d_big_list, cudaStream_t s)
 {
     if (g.n == 0) return cudaSuccess;
-    check_kernel<<<grid_for(g.n, kThreads / 32), kThreads, 0, s>>>(g, d_unsorted_list,
-                                                                   d_unsorted_n);
+    check_kernel<<<grid_for(g.n, kThreads / 32), kThreads, 0, s>>>(g, d_unsorted_list, d_stats,
+                                                                   d_big_list);
     return cudaGetLastError();
 }
 
@@ -170,10 +220,16 @@ cudaError_t launch_ingest_sort_large(const DevGraph &g, int *adj_mut, int v, int
     return cudaGetLastError();
 }
 
-cudaError_t launch_ingest_validate(const DevGraph &g, cudaStream_t s)
+cudaError_t launch_ingest_validate(const DevGraph &g, const int *d_big_list, int n_big,
+                                   int max_degree, unsigned long long *d_fb, cudaStream_t s)
 {
     if (g.n == 0) return cudaSuccess;
-    validate_kernel<<<grid_for(g.n, kThreads / 32), kThreads, 0, s>>>(g);
+    validate_kernel<<<grid_for(g.n, kThreads / 32), kThreads, 0, s>>>(g, d_fb);
+    if (n_big > 0) {
+        int chunks = (max_degree + kValidateChunk - 1) / kValidateChunk;
+        if (chunks > 65535) chunks = 65535;
+        validate_big_kernel<<<dim3(n_big, chunks), kThreads, 0, s>>>(g, d_big_list, d_fb);
+    }
     return cudaGetLastError();
 }
 

@@ -189,13 +189,14 @@ __device__ inline int sched_bucket(int np, int deg, bool ip, bool l2)
 }
 
 // Launchers (each returns the CUDA error of its launch).
-cudaError_t launch_ingest_check(const DevGraph &g, int *d_unsorted_list, int *d_unsorted_n,
-                                cudaStream_t s);
+cudaError_t launch_ingest_check(const DevGraph &g, int *d_unsorted_list, int *d_stats,
+                                int *d_big_list, cudaStream_t s);
 cudaError_t launch_ingest_sort(const DevGraph &g, int *adj_mut, const int *d_list, int n_list,
                                int *scratch, long long scratch_len, cudaStream_t s);
 cudaError_t launch_ingest_sort_large(const DevGraph &g, int *adj_mut, int v, int *scratch,
                                      cudaStream_t s);
-cudaError_t launch_ingest_validate(const DevGraph &g, cudaStream_t s);
+cudaError_t launch_ingest_validate(const DevGraph &g, const int *d_big_list, int n_big,
+                                   int max_degree, unsigned long long *d_fb, cudaStream_t s);
 cudaError_t launch_order(const DevGraph &g, int peel_blocks, long long spin_limit_ns,
                          cudaStream_t s);
 cudaError_t launch_search(const SearchArgs &a, int blocks, int threads, size_t smem,

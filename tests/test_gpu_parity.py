@@ -224,12 +224,46 @@ def _raw(n, lists):
     ([[0, 1], [0]], "MCE_ERR_NOT_SIMPLE"), ([[1, 1], [0, 0]], "MCE_ERR_NOT_SIMPLE"),
     ([[1], [0, 2], []], "MCE_ERR_NOT_SYMMETRIC"), ([[5], [0]], "MCE_ERR_ID_RANGE"),
     ([[-1], [0]], "MCE_ERR_ID_RANGE"),
+    # only a backward entry (1 lists 0, 0 lists nothing): caught by the entry counts
+    ([[], [0]], "MCE_ERR_NOT_SYMMETRIC"), ([[2], [0], [1]], "MCE_ERR_NOT_SYMMETRIC"),
 ])
 def test_invalid_graphs_are_rejected(lists, code):
     mce = _mce()
     with pytest.raises(mce.MceError) as e:
         gpu_graph(_raw(len(lists), lists))
     assert e.value.name == code
+
+
+def _star(n_leaves, centre_last):
+    # a star whose centre list is longer than one validation chunk of a warp
+    c = n_leaves if centre_last else 0
+    leaves = [i for i in range(n_leaves + 1) if i != c]
+    lists = [[c] for _ in range(n_leaves + 1)]
+    lists[c] = list(leaves)
+    return lists
+
+
+@pytest.mark.parametrize("centre_last", [False, True])
+@pytest.mark.parametrize("defect", ["none", "missing_reverse", "repeat"])
+def test_long_lists_are_validated(centre_last, defect):
+    mce = _mce()
+    lists = _star(9000, centre_last)
+    c = 9000 if centre_last else 0
+    if defect == "missing_reverse":
+        leaf = 4097 if not centre_last else 4095     # inside the second chunk of the centre
+        lists[leaf] = []
+    elif defect == "repeat":
+        k = 4096                                      # a repeat across two chunks
+        lists[c].insert(k, lists[c][k - 1])
+    g = _raw(len(lists), lists)
+    if defect == "none":
+        with gpu_graph(g) as h:
+            assert h.count_result() == O.count(g).key()
+        return
+    with pytest.raises(mce.MceError) as e:
+        gpu_graph(g)
+    want = "MCE_ERR_NOT_SIMPLE" if defect == "repeat" else "MCE_ERR_NOT_SYMMETRIC"
+    assert e.value.name == want
 
 
 def test_bad_offsets_rejected():
