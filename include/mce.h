@@ -186,6 +186,21 @@ mce_status mce_enumerate(mce_graph *g, void *stream, int32_t *d_ids, int64_t cap
                          int64_t *d_offsets, int64_t cap_cliques, int64_t *h_sizes);
 
 /*
+ * mce_enumerate restricted to the subtrees of the given roots (the cliques mce_count_roots
+ * counts for them), so that an enumeration larger than device memory can be written in pieces:
+ * the caller takes the roots in batches, and copies each batch's output out (for example to a
+ * pinned host buffer, overlapping the next batch) before reusing the buffers.
+ *   d_roots    device int32[n_roots], original vertex ids; n_roots = 0 writes nothing.
+ *   d_ids, d_offsets, h_sizes  as for mce_enumerate (d_offsets[0 .. count] is written).
+ * Runs a counting pass over the roots, then the writing pass.  Synchronises `stream` once.
+ * Errors: MCE_ERR_BUFFER_TOO_SMALL with the required sizes in h_sizes (nothing is written),
+ * MCE_ERR_ID_RANGE for a root id outside [0, n), and those of mce_count_roots.
+ */
+mce_status mce_enumerate_roots(mce_graph *g, void *stream, const int32_t *d_roots,
+                               int32_t n_roots, int32_t *d_ids, int64_t cap_ids,
+                               int64_t *d_offsets, int64_t cap_cliques, int64_t *h_sizes);
+
+/*
  * Copies the current degeneracy order to device buffers (diagnostics and tests):
  *   d_rank[v] = position of v in the order, d_core[v] = core number of v; either may be NULL.
  */

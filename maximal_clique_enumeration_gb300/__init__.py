@@ -26,7 +26,7 @@ STATUS = {
 }
 EXPORTS = ["mce_config_default", "mce_create", "mce_order", "mce_count", "mce_count_roots",
            "mce_enumerate", "mce_get_order", "mce_last_error", "mce_get_info", "mce_get_profile",
-           "mce_destroy", "mce_status_str", "mce_order_noalloc"]
+           "mce_destroy", "mce_status_str", "mce_order_noalloc", "mce_enumerate_roots"]
 PROFILE_ACTIVITIES = ["build", "pivot", "child", "partition", "donate", "idle", "max_root",
                       "roots"]
 
@@ -100,6 +100,8 @@ def library(path: str | None = None):
     lib.mce_count_roots.argtypes = [P, P, P, i32, P]
     lib.mce_enumerate.restype = st
     lib.mce_enumerate.argtypes = [P, P, P, i64, P, i64, P]
+    lib.mce_enumerate_roots.restype = st
+    lib.mce_enumerate_roots.argtypes = [P, P, P, i32, P, i64, P, i64, P]
     lib.mce_get_order.restype = st
     lib.mce_get_order.argtypes = [P, P, P, P]
     lib.mce_last_error.restype = st
@@ -262,6 +264,81 @@ class Graph:
         self.check(stream)
         return self.unpack(out)
 
+    def enumerate_roots(self, roots, stream=None):
+        """The maximal cliques of the given roots' subtrees: (ids, offsets) device tensors."""
+        import torch
+        roots = torch.as_tensor(np.asarray(roots, dtype=np.int32)).cuda()
+        dummy_i = torch.zeros(1, dtype=torch.int32, device="cuda")
+        dummy_o = torch.zeros(1, dtype=torch.int64, device="cuda")
+        code, (nc, ni) = _enumerate_roots_into(self._h, roots, dummy_i[:0], dummy_o, stream)
+        if code not in (0, 6):
+            raise MceError(code, "mce_enumerate_roots (sizing)")
+        ids = torch.empty(max(ni, 1), dtype=torch.int32, device="cuda")
+        offs = torch.empty(nc + 1, dtype=torch.int64, device="cuda")
+        code, _ = _enumerate_roots_into(self._h, roots, ids, offs, stream)
+        _check(code, "mce_enumerate_roots")
+        return ids[:ni], offs
+
+    def enumerate_stream(self, roots=None, max_cliques: int = 1 << 22, max_ids: int = 1 << 25,
+                         batch_roots: int = 1 << 16, stream=None):
+        """Yields the enumeration in host pieces (ids, offsets), numpy, piece by piece.
+
+        Roots (all vertices by default) are taken in batches whose output fits device buffers of
+        max_cliques cliques and max_ids ids; a batch that does not fit is halved, and one that
+        fills little of them lets the next batch grow.  Two buffer pairs alternate: while one
+        batch is enumerated, the previous one is copied to pinned host memory on a side stream.
+        Each piece's offsets start at 0.  A single root whose cliques exceed the buffers raises
+        MceError(MCE_ERR_BUFFER_TOO_SMALL).
+        """
+        import torch
+        if roots is None:
+            roots = np.arange(self.n, dtype=np.int32)
+        roots = np.asarray(roots, dtype=np.int32)
+        dev_roots = torch.as_tensor(roots).cuda()
+        main = stream if stream is not None else torch.cuda.current_stream()
+        side = torch.cuda.Stream()
+        bufs = [(torch.empty(max_ids, dtype=torch.int32, device="cuda"),
+                 torch.empty(max_cliques + 1, dtype=torch.int64, device="cuda"),
+                 torch.empty(max_ids, dtype=torch.int32).pin_memory(),
+                 torch.empty(max_cliques + 1, dtype=torch.int64).pin_memory(),
+                 torch.cuda.Event()) for _ in range(2)]
+        pending = None          # (slot, cliques, ids) being copied to the host
+        start, b, slot = 0, max(1, int(batch_roots)), 0
+        while start < len(roots):
+            n_b = min(b, len(roots) - start)
+            d_ids, d_offs, h_ids, h_offs, done = bufs[slot]
+            done.synchronize()                       # this slot's last copy has landed
+            with torch.cuda.stream(main):
+                code, (nc, ni) = _enumerate_roots_into(self._h, dev_roots[start:start + n_b],
+                                                       d_ids, d_offs, main)
+            if code == 6:
+                if n_b == 1:
+                    raise MceError(code, f"mce_enumerate_roots: root {int(roots[start])} needs "
+                                         f"{nc} cliques / {ni} ids")
+                b = max(1, n_b // 2)
+                continue
+            _check(code, "mce_enumerate_roots")
+            ready = torch.cuda.Event()
+            ready.record(main)
+            with torch.cuda.stream(side):
+                side.wait_event(ready)
+                h_ids[:ni].copy_(d_ids[:ni], non_blocking=True)
+                h_offs[:nc + 1].copy_(d_offs[:nc + 1], non_blocking=True)
+                done.record(side)
+            if pending is not None:
+                p_slot, p_nc, p_ni = pending
+                bufs[p_slot][4].synchronize()
+                yield bufs[p_slot][2][:p_ni].numpy().copy(), bufs[p_slot][3][:p_nc + 1].numpy().copy()
+            pending = (slot, nc, ni)
+            slot ^= 1
+            start += n_b
+            if 4 * nc < max_cliques and 4 * ni < max_ids:
+                b = min(2 * b, 1 << 24)
+        if pending is not None:
+            p_slot, p_nc, p_ni = pending
+            bufs[p_slot][4].synchronize()
+            yield bufs[p_slot][2][:p_ni].numpy().copy(), bufs[p_slot][3][:p_nc + 1].numpy().copy()
+
     def enumerate(self, stream=None):
         """All maximal cliques: (ids int32 tensor, offsets int64 tensor) on the device."""
         import torch
@@ -290,6 +367,17 @@ class Graph:
                                        ctypes.c_void_p(rank.data_ptr()),
                                        ctypes.c_void_p(core.data_ptr())), "mce_get_order")
         return rank[: self.n], core[: self.n]
+
+
+def _enumerate_roots_into(h, roots, ids, offs, stream):
+    """One mce_enumerate_roots call: returns (status code, (cliques, ids) needed or written)."""
+    sizes = np.zeros(2, np.int64)
+    code = library().mce_enumerate_roots(
+        h, _stream_ptr(stream), ctypes.c_void_p(roots.data_ptr() if roots.numel() else 0),
+        int(roots.numel()), ctypes.c_void_p(ids.data_ptr()), int(ids.numel()),
+        ctypes.c_void_p(offs.data_ptr()), int(offs.numel()) - 1,
+        sizes.ctypes.data_as(ctypes.c_void_p))
+    return int(code), (int(sizes[0]), int(sizes[1]))
 
 
 def cliques_from(ids, offsets):

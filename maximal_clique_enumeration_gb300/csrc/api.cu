@@ -32,6 +32,7 @@ struct mce_graph {
     long long *region_ids = nullptr, *region_cl = nullptr, *totals = nullptr;
     unsigned long long *cursor = nullptr;
     unsigned long long *count_cache = nullptr;  // [2 + hist_len], full-graph count
+    unsigned long long *roots_count = nullptr;  // [2 + hist_len], count of a root batch
     bool count_cache_valid = false;
     // profiling: events around the order and around each class launch
     cudaEvent_t ev_order[2] = {nullptr, nullptr};
@@ -378,6 +379,7 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
     MCE_ALLOC(h, h->cursor, (size_t)h->hist_len + 1);
     MCE_ALLOC(h, h->totals, 2);
     MCE_ALLOC(h, h->count_cache, (size_t)h->hist_len + 2);
+    MCE_ALLOC(h, h->roots_count, (size_t)h->hist_len + 2);
     return MCE_OK;
 }
 
@@ -523,6 +525,49 @@ mce_status mce_enumerate(mce_graph *h, void *stream, int32_t *d_ids, int64_t cap
         mce_status st = run_search(h, s, false, &o);
         if (st != MCE_OK) return st;
         MCE_TRY(launch_enum_isolated(h->g, o, s));
+    }
+    MCE_TRY(launch_enum_close(o, h->totals, s));
+    return MCE_OK;
+}
+
+mce_status mce_enumerate_roots(mce_graph *h, void *stream, const int32_t *d_roots,
+                               int32_t n_roots, int32_t *d_ids, int64_t cap_ids,
+                               int64_t *d_offsets, int64_t cap_cliques, int64_t *h_sizes)
+{
+    if (!h || !h_sizes || n_roots < 0 || (n_roots > 0 && !d_roots) || cap_ids < 0 ||
+        cap_cliques < 0)
+        return MCE_ERR_INVALID_ARG;
+    if ((cap_ids > 0 && !d_ids) || !d_offsets) return MCE_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    const bool search = n_roots > 0 && h->n > 0;
+    if (search) {
+        mce_status st = count_impl(h, s, d_roots, n_roots, (uint64_t *)h->roots_count);
+        if (st != MCE_OK) return st;
+    } else {
+        MCE_TRY(cudaMemsetAsync(h->roots_count, 0, sizeof(uint64_t) * (2 + (size_t)h->hist_len),
+                                s));
+    }
+    MCE_TRY(launch_enum_layout(h->g, h->roots_count, h->hist_len, h->region_ids, h->region_cl,
+                               h->cursor, h->totals, s));
+    long long tot[2] = {0, 0};
+    MCE_TRY(cudaMemcpyAsync(tot, h->totals, sizeof(tot), cudaMemcpyDeviceToHost, s));
+    mce_status st = read_status(h, s);                  // synchronises s
+    if (st != MCE_OK) return st;
+    h_sizes[0] = tot[0];
+    h_sizes[1] = tot[1];
+    if (tot[0] > cap_cliques || tot[1] > cap_ids) return MCE_ERR_BUFFER_TOO_SMALL;
+    DevOut o{};
+    o.hist = h->hist_acc;
+    o.hist_len = h->hist_len;
+    o.ids = d_ids;
+    o.offsets = (long long *)d_offsets;
+    o.region_ids = h->region_ids;
+    o.region_cl = h->region_cl;
+    o.cursor = h->cursor;
+    if (search) {
+        // the roots are still binned from the counting pass
+        st = run_search(h, s, true, &o);
+        if (st != MCE_OK) return st;
     }
     MCE_TRY(launch_enum_close(o, h->totals, s));
     return MCE_OK;
