@@ -209,11 +209,14 @@ cudaError_t search_occupancy(int cls, int ip, int l2, int threads, size_t smem,
 __host__ __device__ inline int hash_slots(int k) { return 64 << k; }
 // Rows of a root with deg * W <= smem_row_words(k) are built and searched in shared memory.
 __host__ __device__ inline int smem_row_words(int k) { return k <= 2 ? 1024 : 0; }
-// Per warp: hash keys and values, staging row (32 words), build cursor arrays (2 x 33 words),
-// rows.
+// Per warp: hash keys and values, the bit filter in front of the hash, build cursor arrays
+// (2 x 36 words), rows.
+constexpr int kFilterLog2Bits = 12;
+constexpr int kFilterWords = (1 << kFilterLog2Bits) / 32;
 __host__ __device__ inline size_t warp_smem_bytes(int k)
 {
-    return (size_t)hash_slots(k) * 8 + 32 * 4 + 2 * 36 * 4 + (size_t)smem_row_words(k) * 4;
+    return (size_t)hash_slots(k) * 8 + kFilterWords * 4 + 2 * 36 * 4 +
+           (size_t)smem_row_words(k) * 4;
 }
 __host__ __device__ inline size_t search_smem_bytes(int k, int hist_len, int warps)
 {

@@ -710,13 +710,13 @@ __device__ void dfs(const SearchArgs &a, const RootCtx &r, Ck<Geo<W>::CH> P, Ck<
     }
 }
 
-// Per-warp shared memory of the build: open-addressing hash of P(v) (id -> local index) and
-// a staging row.
+// Per-warp shared memory of the build: open-addressing hash of P(v) (id -> local index), a
+// one-hash bit filter of P(v) in front of it, cursors of the walk, and small roots' rows.
 constexpr int kBatch = 8;   // N+ entries a lane loads before probing them
 
 struct WarpSmem {
     int *hkey, *hval;
-    unsigned *stage;
+    unsigned *filter;            // kFilterWords words: bit f(id) set for every id of P(v)
     int slots;
     int *cur_start, *cur_base;   // build: per group of 32 neighbours, list starts and bases
     unsigned *rows;              // rows of a root small enough for shared memory
@@ -728,8 +728,18 @@ __device__ __forceinline__ unsigned hash_slot(int id, int mask)
     return ((unsigned)id * 0x9E3779B1u >> 7) & (unsigned)mask;
 }
 
+// The filter's bit of an id (a hash independent of the slot hash).
+__device__ __forceinline__ unsigned filter_bit(int id)
+{
+    return ((unsigned)id * 0x85EBCA6Bu) >> (32 - kFilterLog2Bits);
+}
+
+// Local index of id in P(v), or -1.  Most walked ids are not in P: the filter answers for
+// almost all of them with one shared-memory load.
 __device__ __forceinline__ int hash_find(const WarpSmem &sm, int id)
 {
+    const unsigned f = filter_bit(id);
+    if (!((sm.filter[f >> 5] >> (f & 31)) & 1u)) return -1;
     const int mask = sm.slots - 1;
     unsigned s = hash_slot(id, mask);
     while (true) {
@@ -832,12 +842,15 @@ __device__ void build_and_search(const SearchArgs &a, RootCtx r, const WarpSmem 
     WarpSmem h = sm;
     h.slots = slots;
     for (int i = lane; i < slots; i += 32) h.hkey[i] = -1;
+    for (int i = lane; i < kFilterWords; i += 32) h.filter[i] = 0u;
     __syncwarp();
     for (int i = lane; i < np; i += 32) {
         const int id = r.pids[i];
         unsigned sl = hash_slot(id, slots - 1);
         while (atomicCAS(&h.hkey[sl], -1, id) != -1) sl = (sl + 1) & (unsigned)(slots - 1);
         h.hval[sl] = i;
+        const unsigned f = filter_bit(id);
+        atomicOr(&h.filter[f >> 5], 1u << (f & 31));
     }
     __syncwarp();
     int nxx = 0;
@@ -1123,9 +1136,9 @@ __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(Search
         unsigned char *mine = s_raw + hist + (size_t)(threadIdx.x >> 5) * warp_smem_bytes(k);
         sm.hkey = reinterpret_cast<int *>(mine);
         sm.hval = sm.hkey + hash_slots(k);
-        sm.stage = reinterpret_cast<unsigned *>(sm.hval + hash_slots(k));
+        sm.filter = reinterpret_cast<unsigned *>(sm.hval + hash_slots(k));
         sm.slots = hash_slots(k);
-        sm.cur_start = reinterpret_cast<int *>(sm.stage + 32);
+        sm.cur_start = reinterpret_cast<int *>(sm.filter + kFilterWords);
         sm.cur_base = sm.cur_start + 36;
         sm.rows = reinterpret_cast<unsigned *>(sm.cur_base + 36);   // 16-byte aligned
         sm.rows_words = smem_row_words(k);
