@@ -778,7 +778,10 @@ __device__ void build_flat(const SearchArgs &a, const RootCtx &r, const WarpSmem
         h.cur_base[lane] = base;
         if (lane == 0) h.cur_start[32] = total;
         __syncwarp();
-        int own = 0;
+        // the list this lane is in, kept in registers for W >= 2: a lane's entries only move
+        // forward, and long lists are crossed rarely (measured: the narrowest class, whose roots
+        // see many short lists, runs faster reading the cursors from shared memory each time)
+        int own = 0, own_start = 0, own_next = h.cur_start[1], own_base = h.cur_base[0];
         for (int f0 = 0; f0 < total; f0 += 32 * kBatch) {
             int w[kBatch], ow[kBatch];
 #pragma unroll
@@ -787,9 +790,20 @@ __device__ void build_flat(const SearchArgs &a, const RootCtx &r, const WarpSmem
                 ow[b] = -1;
                 w[b] = -1;
                 if (f < total) {
-                    while (h.cur_start[own + 1] <= f) ++own;
+                    if constexpr (W == 1) {
+                        while (h.cur_start[own + 1] <= f) ++own;
+                        own_start = h.cur_start[own];
+                        own_base = h.cur_base[own];
+                    } else if (own_next <= f) {
+                        do {
+                            ++own;
+                            own_start = own_next;
+                            own_next = h.cur_start[own + 1];
+                        } while (own_next <= f);
+                        own_base = h.cur_base[own];
+                    }
                     ow[b] = own;
-                    w[b] = __ldg(a.g.padj + h.cur_base[own] + (f - h.cur_start[own]));
+                    w[b] = __ldg(a.g.padj + own_base + (f - own_start));
                 }
             }
 #pragma unroll
