@@ -278,9 +278,7 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
     MCE_ALLOC(h, g.alive_a, (size_t)n);
     MCE_ALLOC(h, g.alive_b, (size_t)n);
     MCE_ALLOC(h, g.bucket, (size_t)kNumBuckets);
-    MCE_ALLOC(h, g.poffs, (size_t)n + 1);
-    MCE_ALLOC(h, g.padj, (size_t)(h->nnz / 2 > 0 ? h->nnz / 2 : 1));
-    MCE_ALLOC(h, g.scan_tmp, (size_t)n / kScanBlock + 2);
+    MCE_ALLOC(h, g.padj, (size_t)(h->nnz > 0 ? h->nnz : 1));
     int coop = 0;
     MCE_TRY(cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, h->device));
     if (!coop) return MCE_ERR_CUDA;
@@ -422,8 +420,8 @@ static mce_status order_impl(mce_graph *h, cudaStream_t s)
         MCE_TRY(cudaEventRecord(h->ev_order[1], s));
         h->order_timed = true;
     }
-    // peel, orient count/scan/scatter, 3-pass scan, split (+ subtree count and its scan)
-    h->launches_order = h->n > 0 ? (h->g.l2 ? 12 : 8) : 0;
+    // peel, orient count (with the split) / scan / scatter (+ subtree count and its scan)
+    h->launches_order = h->n > 0 ? (h->g.l2 ? 8 : 4) : 0;
     return MCE_OK;
 }
 

@@ -64,9 +64,8 @@ struct DevGraph {
     int *round_of;    // id -> peel round
     int *order;       // position -> id
     int *pcount;      // id -> |P| (later neighbours)
-    int *poffs;       // [n+1] CSR offsets of the later-neighbour lists N+(v)
-    int *padj;        // [m] N+(v) in id order (Section 2.4: P of the first-level subtree)
-    int *scan_tmp;    // exclusive-scan partials
+    int *padj;        // [2m] N+(v) in id order at padj[offs[v] .. offs[v] + pcount[v])
+                      // (Section 2.4: P of the first-level subtree)
     int *sched;       // first-level roots with |P| > 0, heavy first
     int *deg;         // peel scratch
     int *alive_a, *alive_b;

@@ -379,8 +379,9 @@ __global__ void __launch_bounds__(kPeelThreads, 1) peel_kernel(DevGraph g, long 
 
 constexpr int kOrientThreads = 256;
 
-// |P(v)| = number of neighbours later in the order; isolated vertices; |P| histogram; the
-// per-warp workspace bound; Delta.
+// |P(v)| = number of neighbours later in the order, and N+(v) itself: the later neighbours, in
+// id order, at the front of v's own slot of padj (padj[offs[v] .. offs[v] + |P(v)|)); isolated
+// vertices; |P| histogram; the per-warp workspace bound; Delta.
 __global__ void __launch_bounds__(kOrientThreads) orient_count_kernel(DevGraph g)
 {
     __shared__ int s_bucket[kNumBuckets];
@@ -394,9 +395,16 @@ __global__ void __launch_bounds__(kOrientThreads) orient_count_kernel(DevGraph g
     for (int v = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; v < g.n; v += warps) {
         const int lo = g.offs[v], hi = g.offs[v + 1];
         const int rv = g.rank[v];
+        const unsigned lt = (1u << lane) - 1u;
         int c = 0;
-        for (int j = lo + lane; j < hi; j += 32) c += g.rank[g.adj[j]] > rv;
-        c = __reduce_add_sync(0xffffffffu, c);
+        for (int j0 = lo; j0 < hi; j0 += 32) {
+            const int j = j0 + lane;
+            const int w = j < hi ? g.adj[j] : 0;
+            const bool later = j < hi && g.rank[w] > rv;
+            const unsigned m = __ballot_sync(0xffffffffu, later);
+            if (later) g.padj[lo + c + __popc(m & lt)] = w;
+            c += __popc(m);
+        }
         if (lane == 0) {
             g.pcount[v] = c;
             const int deg = hi - lo;
@@ -513,27 +521,6 @@ __global__ void __launch_bounds__(kScanThreads) scan_final_kernel(const int *in,
     }
 }
 
-// N+(v): the neighbours of v later in the order, kept in id order (stable ballot compaction).
-__global__ void __launch_bounds__(kOrientThreads) orient_split_kernel(DevGraph g)
-{
-    const int lane = threadIdx.x & 31;
-    const int warps = gridDim.x * (blockDim.x >> 5);
-    const unsigned lt = (1u << lane) - 1u;
-    for (int v = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; v < g.n; v += warps) {
-        const int lo = g.offs[v], hi = g.offs[v + 1];
-        const int rv = g.rank[v];
-        int out = g.poffs[v];
-        for (int j0 = lo; j0 < hi; j0 += 32) {
-            const int j = j0 + lane;
-            const int w = j < hi ? g.adj[j] : 0;
-            const bool later = j < hi && g.rank[w] > rv;
-            const unsigned m = __ballot_sync(0xffffffffu, later);
-            if (later) g.padj[out + __popc(m & lt)] = w;
-            out += __popc(m);
-        }
-    }
-}
-
 // A caller's root list, grouped by row-width class and heaviest first (like the schedule).
 __global__ void __launch_bounds__(kOrientThreads) bin_count_kernel(DevGraph g, const int *roots,
                                                                    int n_roots)
@@ -638,12 +625,6 @@ cudaError_t launch_order(const DevGraph &g, int peel_blocks, long long spin_limi
     int sb = (g.n + kOrientThreads - 1) / kOrientThreads;
     if (sb > 8192) sb = 8192;
     orient_scatter_kernel<<<sb, kOrientThreads, 0, s>>>(g);
-    // CSR of the later-neighbour lists
-    const int nb = (g.n + kScanBlock - 1) / kScanBlock;
-    scan_partial_kernel<<<nb, kScanThreads, 0, s>>>(g.pcount, g.n, g.scan_tmp);
-    scan_sums_kernel<<<1, 1024, 0, s>>>(g.scan_tmp, nb);
-    scan_final_kernel<<<nb, kScanThreads, 0, s>>>(g.pcount, g.n, g.scan_tmp, g.poffs);
-    orient_split_kernel<<<blocks, kOrientThreads, 0, s>>>(g);
     if (g.l2) {
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;

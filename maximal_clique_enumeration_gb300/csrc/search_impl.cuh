@@ -352,8 +352,9 @@ __device__ __forceinline__ bool sorted_has(const int *a, int lo, int hi, int id)
 // of the original graph (Section 3.4).
 __device__ __forceinline__ bool x_adjacent(const DevGraph &g, int x, int p)
 {
-    const int end = __ldg(g.poffs + x + 1);
-    int lo = __ldg(g.poffs + x), hi = end;
+    int lo = __ldg(g.offs + x);
+    const int end = lo + __ldg(g.pcount + x);
+    int hi = end;
     while (lo < hi) {
         const int mid = (lo + hi) >> 1;
         if (__ldg(g.padj + mid) < p) lo = mid + 1;
@@ -764,8 +765,8 @@ __device__ void build_flat(const SearchArgs &a, const RootCtx &r, const WarpSmem
         int base = 0, len = 0;
         if (t < deg) {
             const int u = t < np ? r.pids[t] : r.xids[t - np];
-            base = __ldg(a.g.poffs + u);
-            len = __ldg(a.g.poffs + u + 1) - base;
+            base = __ldg(a.g.offs + u);
+            len = __ldg(a.g.pcount + u);
         }
         int incl = len;
 #pragma unroll
@@ -907,8 +908,8 @@ __device__ void build_and_search(const SearchArgs &a, RootCtx r, const WarpSmem 
         unsigned *row = r.rowsX + (long long)xi * W;
         if (xi < r.nx) {
             const int u = r.xids[xi];
-            const int s1 = __ldg(a.g.poffs + u + 1);
-            for (int e0 = __ldg(a.g.poffs + u); e0 < s1; e0 += kBatch) {
+            const int s0 = __ldg(a.g.offs + u), s1 = s0 + __ldg(a.g.pcount + u);
+            for (int e0 = s0; e0 < s1; e0 += kBatch) {
                 int w[kBatch];                           // independent loads in flight
 #pragma unroll
                 for (int b = 0; b < kBatch; ++b) w[b] = e0 + b < s1 ? __ldg(a.g.padj + e0 + b) : -1;
@@ -948,8 +949,8 @@ __device__ void build_and_search(const SearchArgs &a, RootCtx r, const WarpSmem 
         if (i < np) {
             const int u = r.pids[i];
             unsigned *row = r.rowsP + (long long)i * W;
-            const int s1 = __ldg(a.g.poffs + u + 1);
-            for (int e0 = __ldg(a.g.poffs + u); e0 < s1; e0 += kBatch) {
+            const int s0 = __ldg(a.g.offs + u), s1 = s0 + __ldg(a.g.pcount + u);
+            for (int e0 = s0; e0 < s1; e0 += kBatch) {
                 int w[kBatch];
 #pragma unroll
                 for (int b = 0; b < kBatch; ++b) w[b] = e0 + b < s1 ? __ldg(a.g.padj + e0 + b) : -1;
@@ -1035,9 +1036,10 @@ __device__ void search_edge(const SearchArgs &a, unsigned *ws, const WarpSmem &s
     RootCtx r = make_ctx<W>(ws, degv, g.pcount[v], 0, 0);
     const unsigned lt = (1u << lane) - 1u;
     // P: the later neighbours of v that are later neighbours of w too (both lists id-sorted)
-    const int pv1 = g.poffs[v + 1], pw0 = g.poffs[w], pw1 = g.poffs[w + 1];
+    const int pv0 = g.offs[v], pv1 = pv0 + g.pcount[v];
+    const int pw0 = g.offs[w], pw1 = pw0 + g.pcount[w];
     int np = 0;
-    for (int j0 = g.poffs[v]; j0 < pv1; j0 += 32) {
+    for (int j0 = pv0; j0 < pv1; j0 += 32) {
         const int j = j0 + lane;
         const int u = j < pv1 ? __ldg(g.padj + j) : -1;
         const bool in = u >= 0 && sorted_has(g.padj, pw0, pw1, u);
@@ -1184,7 +1186,7 @@ __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(Search
             const int t = ubase + (int)idx;
             pos = last_at_most(a.uoff, (int)begin, end, t, lane);
             const int v0 = a.roots[pos];
-            if (a.g.pcount[v0] > 0) w = a.g.padj[a.g.poffs[v0] + (t - a.uoff[pos])];
+            if (a.g.pcount[v0] > 0) w = a.g.padj[a.g.offs[v0] + (t - a.uoff[pos])];
         }
         const int v = a.roots[pos];
         const int deg = a.g.offs[v + 1] - a.g.offs[v];
