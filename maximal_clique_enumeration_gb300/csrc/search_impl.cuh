@@ -325,7 +325,8 @@ __device__ __forceinline__ int list_bits(const Ck<Geo<W>::CH> &b, int *out, int 
     int cnt = 0;
 #pragma unroll
     for (int k = 0; k < W; ++k) {
-        const unsigned wk = __shfl_sync(kFull, b.w[k % CH], k / CH);
+        // with whole rows per lane (G = 1) every lane already holds word k
+        const unsigned wk = Geo<W>::G == 1 ? b.w[k % CH] : __shfl_sync(kFull, b.w[k % CH], k / CH);
         const bool bit = (wk >> lane) & 1u;
         const unsigned m = __ballot_sync(kFull, bit);
         if (bit) out[cnt + __popc(m & ((1u << lane) - 1u))] = k * 32 + lane;
@@ -436,6 +437,24 @@ __device__ int xx_partition(const DevGraph &g, const RootCtx &r, int lpX, int c,
     const unsigned bit = 1u << (c & 31);
     const int pc = kIP ? r.pids[c] : 0;
     const unsigned lt = (1u << lane) - 1u;
+    if (lpX <= 32) {
+        // one row per lane: every lane has read its row before any lane writes, so the rows go
+        // straight to their places (kept first, then the others, each in the old order)
+        const bool in = lane < lpX;
+        const int x = in ? r.xx[lane] : 0;
+        bool keep = false;
+        if (in) {
+            if constexpr (kIP) keep = x_adjacent(g, r.xids[x], pc);
+            else keep = (r.rowsX[(long long)x * W + wc] & bit) != 0u;
+        }
+        const unsigned mk = __ballot_sync(kFull, keep);
+        const unsigned mr = __ballot_sync(kFull, in && !keep);
+        __syncwarp();
+        if (keep) r.xx[__popc(mk & lt)] = x;
+        else if (in) r.xx[__popc(mk) + __popc(mr & lt)] = x;
+        __syncwarp();
+        return __popc(mk);
+    }
     int kept = 0, rem = 0;
     for (int base = 0; base < lpX; base += 32) {
         const int i = base + lane;
