@@ -266,6 +266,44 @@ def test_long_lists_are_validated(centre_last, defect):
     assert e.value.name == want
 
 
+def test_widest_rows_and_the_p_limit():
+    # K_1025: the first vertex has |P| = 1024, the widest rows (32 words); K_1026 is over
+    mce = _mce()
+    with gpu_graph(G.complete_graph(1025)) as h:
+        assert h.count_result() == pins.summary([tuple(range(1025))])
+    with pytest.raises(mce.MceError) as e:
+        gpu_graph(G.complete_graph(1026))
+    assert e.value.name == "MCE_ERR_LIMIT"
+
+
+def _star(leaves):
+    return G.csr_from_edges(leaves + 1, np.zeros(leaves, np.int64), np.arange(1, leaves + 1))
+
+
+def test_degree_limit():
+    # a degree of 2^21 - 1 is the largest a pivot code can hold; one more is refused
+    mce = _mce()
+    g = _star((1 << 21) - 1)
+    with gpu_graph(g) as h:
+        got = h.count_result()
+    assert got == O.count(g).key()
+    assert got[0] == (1 << 21) - 1 and got[2] == (0, 0, (1 << 21) - 1)
+    with pytest.raises(mce.MceError) as e:
+        gpu_graph(_star(1 << 21))
+    assert e.value.name == "MCE_ERR_LIMIT"
+
+
+def test_duplicate_roots_count_twice():
+    g = G.config_graph("planted50k", 2)
+    roots = np.arange(0, g.n, 5, dtype=np.int32)
+    with gpu_graph(g) as h:
+        one = h.count_roots_result(roots)
+        two = h.count_roots_result(np.concatenate([roots, roots[::-1]]))
+    assert two[0] == 2 * one[0]
+    assert two[1] == (2 * one[1]) % (1 << 64)
+    assert two[2] == tuple(2 * x for x in one[2])
+
+
 def test_bad_offsets_rejected():
     mce = _mce()
     g = G.Graph(3, np.asarray([0, 2, 1, 2], np.int32), np.asarray([1, 2], np.int32))
