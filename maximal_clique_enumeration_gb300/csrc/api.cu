@@ -335,24 +335,26 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
     if (wpb > 4) wpb = 4;
     h->search_threads = 32 * wpb;
     size_t ws_total = 32;
-    int class_per_sm[kNumClasses] = {};
+    int group_per_sm[kNumGroups] = {};
     for (int k = 0; k < kNumClasses; ++k) {
         h->cls_smem[k] = search_smem_bytes(k, h->hist_len, wpb);
         MCE_TRY(search_configure(k, g.ip, g.l2, h->cls_smem[k]));
-        MCE_TRY(search_occupancy(k, g.ip, g.l2, h->search_threads, h->cls_smem[k], &class_per_sm[k]));
-        if (class_per_sm[k] < 1) return MCE_ERR_CUDA;
-        if (h->cfg.blocks_per_sm > 0 && h->cfg.blocks_per_sm < class_per_sm[k])
-            class_per_sm[k] = h->cfg.blocks_per_sm;
+        for (int gi = 2 * k; gi < 2 * k + 2; ++gi) {
+            MCE_TRY(search_occupancy(gi, g.ip, g.l2, h->search_threads, h->cls_smem[k],
+                                     &group_per_sm[gi]));
+            if (group_per_sm[gi] < 1) return MCE_ERR_CUDA;
+            if (h->cfg.blocks_per_sm > 0 && h->cfg.blocks_per_sm < group_per_sm[gi])
+                group_per_sm[gi] = h->cfg.blocks_per_sm;
+        }
     }
     for (int gi = 0; gi < kNumGroups; ++gi) {
-        const int k = gi / 2;
         const bool big = (gi & 1) == 0;
         h->grp_count[gi] = c.cls[2 * gi + 1] - c.cls[2 * gi];
         // whole 128-byte lines per warp: no two warps share an L1 line of workspace
         unsigned long long need = (c.ws_grp[gi] + 31) & ~31ULL;
         if (gi == 1 && need < 32) need = 32;              // isolated roots use 1 word
         if (need == 0) continue;                          // no vertex of the graph in this group
-        int blocks = class_per_sm[k] * h->sm_count;
+        int blocks = group_per_sm[gi] * h->sm_count;
         if (big) {
             // as many warps as the big-workspace budget allows, at most one launch's worth
             long long warps = kBigBudgetWords / (long long)need;

@@ -201,7 +201,8 @@ cudaError_t launch_order(const DevGraph &g, int peel_blocks, long long spin_limi
 cudaError_t launch_search(const SearchArgs &a, int blocks, int threads, size_t smem,
                           cudaStream_t s);
 cudaError_t launch_search_prep(const SearchArgs &a, cudaStream_t s);
-cudaError_t search_occupancy(int cls, int ip, int l2, int threads, size_t smem,
+// CTAs per SM of the kernel of launch group `group` (row-width class group / 2).
+cudaError_t search_occupancy(int group, int ip, int l2, int threads, size_t smem,
                              int *blocks_per_sm);
 // Shared memory of the search kernel of class k: the size histogram, then per warp a hash of
 // P(v) (ids and local indices) and a staging row.

@@ -81,27 +81,33 @@ __global__ void enum_close_kernel(DevOut o, const long long *totals)
 
 // Kernel instances, one translation unit per variant (built in parallel): full or partial
 // induced subgraphs, first- or second-level subtrees.
-const void *search_kernel_full(int cls);
-const void *search_kernel_partial(int cls);
-const void *search_kernel_full_l2(int cls);
-const void *search_kernel_partial_l2(int cls);
+const void *search_kernel_full(int cls, bool big);
+const void *search_kernel_partial(int cls, bool big);
+const void *search_kernel_full_l2(int cls, bool big);
+const void *search_kernel_partial_l2(int cls, bool big);
 
-static const void *search_kernel_ptr(int cls, int ip, int l2)
+static const void *search_kernel_ptr(int cls, int ip, int l2, bool big)
 {
-    if (l2) return ip ? search_kernel_partial_l2(cls) : search_kernel_full_l2(cls);
-    return ip ? search_kernel_partial(cls) : search_kernel_full(cls);
+    if (l2) return ip ? search_kernel_partial_l2(cls, big) : search_kernel_full_l2(cls, big);
+    return ip ? search_kernel_partial(cls, big) : search_kernel_full(cls, big);
 }
 
 cudaError_t search_configure(int cls, int ip, int l2, size_t smem)
 {
-    return cudaFuncSetAttribute(search_kernel_ptr(cls, ip, l2),
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    for (int big = 0; big < 2; ++big) {
+        const cudaError_t e = cudaFuncSetAttribute(search_kernel_ptr(cls, ip, l2, big != 0),
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
-cudaError_t search_occupancy(int cls, int ip, int l2, int threads, size_t smem, int *blocks_per_sm)
+cudaError_t search_occupancy(int group, int ip, int l2, int threads, size_t smem,
+                             int *blocks_per_sm)
 {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, search_kernel_ptr(cls, ip, l2),
-                                                         threads, smem);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        blocks_per_sm, search_kernel_ptr(group / 2, ip, l2, (group & 1) == 0), threads, smem);
 }
 
 cudaError_t launch_search(const SearchArgs &a, int blocks, int threads, size_t smem,
@@ -109,7 +115,7 @@ cudaError_t launch_search(const SearchArgs &a, int blocks, int threads, size_t s
 {
     SearchArgs aa = a;
     void *args[] = {&aa};
-    return cudaLaunchKernel(search_kernel_ptr(a.cls, a.g.ip, a.g.l2), dim3(blocks), dim3(threads), args,
+    return cudaLaunchKernel(search_kernel_ptr(a.cls, a.g.ip, a.g.l2, (a.group & 1) == 0), dim3(blocks), dim3(threads), args,
                             smem, s);
 }
 

@@ -1,19 +1,20 @@
-// Search kernels over full induced subgraphs of second-level subtrees, one per row width.
+// Search kernels over full induced subgraphs of second-level subtrees, one per row width and
+// launch group.
 #define MCE_SEARCH_IP 0
 #define MCE_SEARCH_L2 1
 #include "search_impl.cuh"
 
 namespace mce {
 
-const void *search_kernel_full_l2(int cls)
+const void *search_kernel_full_l2(int cls, bool big)
 {
     switch (cls) {
-    case 0: return (const void *)search_kernel<1>;
-    case 1: return (const void *)search_kernel<2>;
-    case 2: return (const void *)search_kernel<4>;
-    case 3: return (const void *)search_kernel<8>;
-    case 4: return (const void *)search_kernel<16>;
-    default: return (const void *)search_kernel<32>;
+    case 0: return big ? (const void *)search_kernel<1, true> : (const void *)search_kernel<1, false>;
+    case 1: return big ? (const void *)search_kernel<2, true> : (const void *)search_kernel<2, false>;
+    case 2: return big ? (const void *)search_kernel<4, true> : (const void *)search_kernel<4, false>;
+    case 3: return big ? (const void *)search_kernel<8, true> : (const void *)search_kernel<8, false>;
+    case 4: return big ? (const void *)search_kernel<16, true> : (const void *)search_kernel<16, false>;
+    default: return big ? (const void *)search_kernel<32, true> : (const void *)search_kernel<32, false>;
     }
 }
 

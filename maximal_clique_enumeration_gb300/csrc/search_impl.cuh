@@ -848,11 +848,61 @@ __device__ void build_flat(const SearchArgs &a, const RootCtx &r, const WarpSmem
 // X precedes v and so precedes every p in P, hence p is in N+(u); a pair of P vertices is found
 // from the earlier of the two.  Membership in P is a shared-memory hash lookup, so the build
 // reads the bounded lists N+(u) (each at most d long) with coalesced loads and no search.
+// Is some vertex of X adjacent to all of P?  Only an x with |N+(x)| >= |P| can be: per chunk of
+// 32 * kBatch vertices of X the candidates are listed (kBatch gathers of |N+(x)| in flight per
+// lane) and their lists walked, so a covering vertex early in X ends the test early (big
+// roots only).
+__device__ __forceinline__ bool x_covers_p(const DevGraph &g, const RootCtx &r, const WarpSmem &h,
+                                        int np, int lane)
+{
+    const unsigned lt = (1u << lane) - 1u;
+    bool covered = false;
+    for (int base = 0; base < r.nx && !covered; base += 32 * kBatch) {
+        int ncand = 0;
+        {
+            int x[kBatch], c[kBatch];
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+                const int xi = base + b * 32 + lane;
+                x[b] = xi < r.nx ? r.xids[xi] : -1;
+            }
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) c[b] = x[b] >= 0 ? __ldg(g.pcount + x[b]) : 0;
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+                const bool cand = x[b] >= 0 && c[b] >= np;
+                const unsigned m = __ballot_sync(kFull, cand);
+                if (cand) r.spill[ncand + __popc(m & lt)] = x[b];
+                ncand += __popc(m);
+            }
+        }
+        __syncwarp();
+        for (int cb = 0; cb < ncand && !covered; cb += 32) {
+            const int ci = cb + lane;
+            int hits = 0;
+            if (ci < ncand) {
+                const int u = r.spill[ci];
+                const int s0 = __ldg(g.offs + u), s1 = s0 + __ldg(g.pcount + u);
+                for (int e0 = s0; e0 < s1; e0 += kBatch) {
+                    int w[kBatch];
+#pragma unroll
+                    for (int b = 0; b < kBatch; ++b) w[b] = e0 + b < s1 ? __ldg(g.padj + e0 + b) : -1;
+#pragma unroll
+                    for (int b = 0; b < kBatch; ++b) hits += w[b] >= 0 && hash_find(h, w[b]) >= 0;
+                }
+            }
+            covered = __any_sync(kFull, ci < ncand && hits == np);
+        }
+        __syncwarp();
+    }
+    return covered;
+}
+
 // Builds the induced subgraph of the subtree in r (its P and X ids already in r.pids, r.xids;
 // R in r.rids) into the warp's workspace, or into shared memory when the rows fit, and searches
 // it from R's key sum S.
-template <int W>
-__device__ void build_and_search(const SearchArgs &a, RootCtx r, const WarpSmem &sm, bool big,
+template <int W, bool big>
+__device__ void build_and_search(const SearchArgs &a, RootCtx r, const WarpSmem &sm,
                                  unsigned long long S, Acc &acc, unsigned long long *s_hist,
                                  int lane)
 {
@@ -862,7 +912,7 @@ __device__ void build_and_search(const SearchArgs &a, RootCtx r, const WarpSmem 
     const unsigned lt = (1u << lane) - 1u;
     // rows in shared memory when they fit (normal roots only), else in the workspace; zero the
     // rows (the big-root build writes X rows whole when they are at most 4 words wide)
-    if (!big && (long long)(kIP ? np : deg) * W <= sm.rows_words) {
+    if (!big && (long long)(kIP ? np : deg) * W <= sm.rows_words) {   // (big: a constant)
         r.rowsP = sm.rows;
         r.rowsX = sm.rows + (long long)np * W;
     }
@@ -894,7 +944,7 @@ __device__ void build_and_search(const SearchArgs &a, RootCtx r, const WarpSmem 
         build_flat<W>(a, r, h, np, np, lane);
         for (int i = lane; i < r.nx; i += 32) r.xx[i] = i;
         nxx = r.nx;
-    } else if (!big) {
+    } else if constexpr (!big) {
         build_flat<W>(a, r, h, deg, np, lane);
         // X_X and the coverage test: a vertex of X adjacent to all of P makes every clique of
         // this subtree extendable (it is the Tomita pivot of the root with P - N(pivot) empty),
@@ -915,9 +965,19 @@ __device__ void build_and_search(const SearchArgs &a, RootCtx r, const WarpSmem 
             return;
         }
     } else {
-    // X rows, one vertex per lane.  A vertex of X adjacent to all of P makes every clique of
-    // this subtree extendable (it is the Tomita pivot of the root with P - N(pivot) empty):
-    // the subtree holds no maximal clique and is abandoned as soon as one is seen.
+    // A vertex of X adjacent to all of P makes every clique of this subtree extendable (it is
+    // the Tomita pivot of the root with P - N(pivot) empty): the subtree holds no maximal
+    // clique.  Such a vertex x has all of P in N+(x), so only those with |N+(x)| >= |P| can be
+    // one.  A big root's X is mostly vertices with short lists: per chunk of 32 * kBatch
+    // vertices of X, the candidates are listed (kBatch gathers of |N+(x)| in flight per lane)
+    // and their lists walked, so a covering vertex early in X ends the root early.
+    covered = x_covers_p(a.g, r, h, np, lane);
+    if (covered) {
+        acc.nodes++;
+        PROF_ADD(acc, kProfBuild, t_build);
+        return;
+    }
+    // X rows, one vertex per lane
     for (int base = 0; base < r.nx && !covered; base += 32) {
         const int xi = base + lane;
         int hits = 0;
@@ -1009,6 +1069,37 @@ __device__ void build_and_search(const SearchArgs &a, RootCtx r, const WarpSmem 
     dfs<W>(a, r, bits_prefix<W>(np, q), ck_zero<CH>(), nxx, S, acc, s_hist, lane);
 }
 
+// The split of a wide root's N(v) into P (later) and X (earlier), in id order, with kBatch rank
+// gathers in flight per lane (big-workspace roots only).
+__device__ __forceinline__ void split_wide(const DevGraph &g, const int *Nv, int deg, int rv, int *pids,
+                                        int *xids, int lane)
+{
+    const unsigned lt = (1u << lane) - 1u;
+    int pi = 0, xi = 0;
+    for (int base = 0; base < deg; base += 32 * kBatch) {
+        int w[kBatch], rk[kBatch];
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const int j = base + b * 32 + lane;
+            w[b] = j < deg ? __ldg(Nv + j) : -1;
+        }
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) rk[b] = w[b] >= 0 ? __ldg(g.rank + w[b]) : 0;
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const bool in = w[b] >= 0;
+            const bool isP = in && rk[b] > rv;
+            const unsigned mp = __ballot_sync(kFull, isP);
+            const unsigned mx = __ballot_sync(kFull, in && !isP);
+            if (isP) pids[pi + __popc(mp & lt)] = w[b];
+            else if (in) xids[xi + __popc(mx & lt)] = w[b];
+            pi += __popc(mp);
+            xi += __popc(mx);
+        }
+    }
+    __syncwarp();
+}
+
 // First-level subtree of root v (Algorithm 3): P = later neighbours, X = earlier ones.
 //
 // Rows: for u in N(v), row(u) has bit i set iff u is adjacent to the i-th vertex of P (the
@@ -1017,16 +1108,20 @@ __device__ void build_and_search(const SearchArgs &a, RootCtx r, const WarpSmem 
 // X precedes v and so precedes every p in P, hence p is in N+(u); a pair of P vertices is found
 // from the earlier of the two.  Membership in P is a shared-memory hash lookup, so the build
 // reads the bounded lists N+(u) (each at most d long) with coalesced loads and no search.
-template <int W>
+template <int W, bool big>
 __device__ void search_root(const SearchArgs &a, unsigned *ws, const WarpSmem &sm, int v, int deg,
-                            int np, bool big, Acc &acc, unsigned long long *s_hist, int lane)
+                            int np, Acc &acc, unsigned long long *s_hist, int lane)
 {
     RootCtx r = make_ctx<W>(ws, deg, np, np, deg - np);
     const int *Nv = a.g.adj + a.g.offs[v];
     const int rv = a.g.rank[v];
     const unsigned lt = (1u << lane) - 1u;
-    // split N(v) into P (later) and X (earlier), numbering each part in id order
+    // split N(v) into P (later) and X (earlier), numbering each part in id order; a wide
+    // root keeps kBatch rank gathers in flight per lane
     int pi = 0, xi = 0;
+    if (big && deg > 32 * kBatch) {
+        split_wide(a.g, Nv, deg, rv, r.pids, r.xids, lane);
+    } else
     for (int base = 0; base < deg; base += 32) {
         const int j = base + lane;
         const bool in = j < deg;
@@ -1040,15 +1135,15 @@ __device__ void search_root(const SearchArgs &a, unsigned *ws, const WarpSmem &s
         xi += __popc(mx);
     }
     if (lane == 0) r.rids[0] = v;
-    build_and_search<W>(a, r, sm, big, vertex_key(v), acc, s_hist, lane);
+    build_and_search<W, big>(a, r, sm, vertex_key(v), acc, s_hist, lane);
 }
 
 // Second-level subtree of the edge {v, w}, v before w (Algorithm 4): R = {v, w},
 // P = N(v) n N(w) after w = N+(v) n N+(w), X = N(v) n N(w) before w.  The workspace keeps the
 // layout of root v, which holds any of its second-level subtrees.
-template <int W>
+template <int W, bool big>
 __device__ void search_edge(const SearchArgs &a, unsigned *ws, const WarpSmem &sm, int v, int w,
-                            bool big, Acc &acc, unsigned long long *s_hist, int lane)
+                            Acc &acc, unsigned long long *s_hist, int lane)
 {
     const DevGraph &g = a.g;
     const int degv = g.offs[v + 1] - g.offs[v];
@@ -1096,7 +1191,7 @@ __device__ void search_edge(const SearchArgs &a, unsigned *ws, const WarpSmem &s
         acc.nodes++;
         return;
     }
-    build_and_search<W>(a, r, sm, big, S, acc, s_hist, lane);
+    build_and_search<W, big>(a, r, sm, S, acc, s_hist, lane);
 }
 
 // Searches a branch that another warp wrote into this warp's workspace.
@@ -1148,14 +1243,16 @@ __device__ __forceinline__ int last_at_most(const int *a, int lo, int hi, int t,
 #ifndef MCE_MIN_BLOCKS_MID
 #define MCE_MIN_BLOCKS_MID 6
 #endif
+// (measured: 2-word rows run best at 7, which leaves them 72 registers instead of 64)
 template <int W>
 struct MinBlocks {
-    static constexpr int value = W <= 2 ? 8 : (W <= 8 ? MCE_MIN_BLOCKS_MID : 4);
+    static constexpr int value = W == 1 ? 8 : (W == 2 ? 7 : (W <= 8 ? MCE_MIN_BLOCKS_MID : 4));
 };
 
-// One persistent launch per row width W: the roots of that class, heaviest first, then
-// donated branches of those roots (Section 3.3).
-template <int W>
+// One persistent launch per row width W and launch group: the roots of that class, heaviest
+// first, then donated branches of those roots (Section 3.3).  Big: the group of roots whose
+// workspace exceeds kWsCapWords (their build code is compiled into these instances only).
+template <int W, bool Big>
 __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(SearchArgs a)
 {
     extern __shared__ __align__(16) unsigned char s_raw[];
@@ -1223,9 +1320,9 @@ __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(Search
         } else if (np > kMaxP) {
             if (lane == 0) set_status(a.g.ctrl, MCE_ERR_LIMIT);
         } else if (kL2) {
-            if (w >= 0) search_edge<W>(a, ws, sm, v, w, (a.group & 1) == 0, acc, s_hist, lane);
+            if (w >= 0) search_edge<W, Big>(a, ws, sm, v, w, acc, s_hist, lane);
         } else {
-            search_root<W>(a, ws, sm, v, deg, np, (a.group & 1) == 0, acc, s_hist, lane);
+            search_root<W, Big>(a, ws, sm, v, deg, np, acc, s_hist, lane);
         }
         __syncwarp();
         if (lane == 0) busy.fetch_sub(1, cuda::memory_order_acq_rel);

@@ -276,20 +276,20 @@ def test_widest_rows_and_the_p_limit():
     assert e.value.name == "MCE_ERR_LIMIT"
 
 
-def _star(leaves):
+def _star_graph(leaves):
     return G.csr_from_edges(leaves + 1, np.zeros(leaves, np.int64), np.arange(1, leaves + 1))
 
 
 def test_degree_limit():
     # a degree of 2^21 - 1 is the largest a pivot code can hold; one more is refused
     mce = _mce()
-    g = _star((1 << 21) - 1)
+    g = _star_graph((1 << 21) - 1)
     with gpu_graph(g) as h:
         got = h.count_result()
     assert got == O.count(g).key()
     assert got[0] == (1 << 21) - 1 and got[2] == (0, 0, (1 << 21) - 1)
     with pytest.raises(mce.MceError) as e:
-        gpu_graph(_star(1 << 21))
+        gpu_graph(_star_graph(1 << 21))
     assert e.value.name == "MCE_ERR_LIMIT"
 
 
