@@ -168,7 +168,8 @@ __host__ __device__ inline WsLayout ws_layout(int deg, int np, bool ip, bool l2)
 
 // Schedule buckets: launch groups in launch order (widest rows first; per width the roots with
 // a big workspace, then the rest) and, inside a group, roots with a larger estimated cost
-// deg(v) * (|P| + 1) first (log2 buckets).  Bucket 0 holds over-limit roots (group of W = 32).
+// (|P| + 1)^2 * (core(v) + 1) first (log2 buckets).  Bucket 0 holds over-limit roots (group of
+// W = 32).
 constexpr int kCostBuckets = 48;
 constexpr int kNumBuckets = 1 + kNumGroups * kCostBuckets;
 
@@ -176,12 +177,14 @@ constexpr int kNumBuckets = 1 + kNumGroups * kCostBuckets;
 __host__ __device__ inline int group_at(int o) { return 2 * (kNumClasses - 1 - o / 2) + (o & 1); }
 __host__ __device__ inline int position_of(int g) { return 2 * (kNumClasses - 1 - g / 2) + (g & 1); }
 
-__device__ inline int sched_bucket(int np, int deg, bool ip, bool l2)
+__device__ inline int sched_bucket(int np, int deg, bool ip, bool l2, int core)
 {
     if (np > kMaxP) return 0;
     const int k = wclass_index(np);
     const int b = np > 0 && ws_layout(deg, np, ip, l2).total > kWsCapWords ? 0 : 1;
-    const unsigned long long est = (unsigned long long)deg * (unsigned long long)(np + 1);
+    // the subtree's cost grows with |P| and with how dense the region is (its core number)
+    const unsigned long long est = (unsigned long long)(np + 1) * (unsigned long long)(np + 1) *
+                                   (unsigned long long)(core + 1);
     int lb = est ? 63 - __clzll((long long)est) : 0;
     lb = lb < kCostBuckets - 1 ? lb : kCostBuckets - 1;
     return 1 + position_of(2 * k + b) * kCostBuckets + (kCostBuckets - 1 - lb);

@@ -414,7 +414,7 @@ __global__ void __launch_bounds__(kOrientThreads) orient_count_kernel(DevGraph g
                 iso_hash += mix64(vertex_key(v));
             }
             if (c > 0) {
-                atomicAdd(&s_bucket[sched_bucket(c, deg, g.ip, g.l2)], 1);
+                atomicAdd(&s_bucket[sched_bucket(c, deg, g.ip, g.l2, g.core[v])], 1);
                 maxp = max(maxp, c);
                 if (c <= kMaxP) {
                     const unsigned long long need = (unsigned long long)ws_layout(deg, c, g.ip, g.l2).total;
@@ -469,7 +469,7 @@ __global__ void __launch_bounds__(kOrientThreads) orient_scatter_kernel(DevGraph
 {
     for (int v = blockIdx.x * blockDim.x + threadIdx.x; v < g.n; v += gridDim.x * blockDim.x) {
         const int c = g.pcount[v];
-        if (c > 0) g.sched[atomicAdd(&g.bucket[sched_bucket(c, g.offs[v + 1] - g.offs[v], g.ip, g.l2)], 1)] = v;
+        if (c > 0) g.sched[atomicAdd(&g.bucket[sched_bucket(c, g.offs[v + 1] - g.offs[v], g.ip, g.l2, g.core[v])], 1)] = v;
     }
 }
 
@@ -531,7 +531,7 @@ __global__ void __launch_bounds__(kOrientThreads) bin_count_kernel(DevGraph g, c
             set_status(g.ctrl, MCE_ERR_ID_RANGE);
             continue;
         }
-        atomicAdd(&g.ubucket[sched_bucket(g.pcount[v], g.offs[v + 1] - g.offs[v], g.ip, g.l2)], 1);
+        atomicAdd(&g.ubucket[sched_bucket(g.pcount[v], g.offs[v + 1] - g.offs[v], g.ip, g.l2, g.core[v])], 1);
     }
 }
 
@@ -547,7 +547,7 @@ __global__ void __launch_bounds__(kOrientThreads) bin_scatter_kernel(DevGraph g,
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_roots; i += gridDim.x * blockDim.x) {
         const int v = roots[i];
         if (v < 0 || v >= g.n) continue;
-        g.uroots[atomicAdd(&g.ubucket[sched_bucket(g.pcount[v], g.offs[v + 1] - g.offs[v], g.ip, g.l2)], 1)] = v;
+        g.uroots[atomicAdd(&g.ubucket[sched_bucket(g.pcount[v], g.offs[v + 1] - g.offs[v], g.ip, g.l2, g.core[v])], 1)] = v;
     }
 }
 
