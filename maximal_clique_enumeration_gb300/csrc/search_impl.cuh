@@ -734,6 +734,13 @@ __device__ void dfs(const SearchArgs &a, const RootCtx &r, Ck<Geo<W>::CH> P, Ck<
 // one-hash bit filter of P(v) in front of it, cursors of the walk, and small roots' rows.
 constexpr int kBatch = 8;   // N+ entries a lane loads before probing them
 
+// The same for the normal roots' load-balanced walk, per row width (measured on R-MAT: 2-word
+// rows run best with 4 loads in flight, 4-word rows with 12).
+template <int W>
+struct WalkBatch {
+    static constexpr int value = W == 2 ? 4 : (W == 4 ? 12 : kBatch);
+};
+
 struct WarpSmem {
     int *hkey, *hval;
     unsigned *filter;            // kFilterWords words: bit f(id) set for every id of P(v)
@@ -772,12 +779,13 @@ __device__ __forceinline__ int hash_find(const WarpSmem &sm, int id)
 
 // Load-balanced build of all rows (normal roots).  The neighbours u_t of v (P first, then X)
 // are taken 32 at a time; the warp walks the concatenation of their lists N+(u_t) with
-// consecutive lanes on consecutive entries (coalesced), kBatch entries per lane in flight.  A
+// consecutive lanes on consecutive entries (coalesced), WalkBatch entries per lane in flight.  A
 // hit on p_j sets bit j of row t, and, when u_t = p_t is in P, bit t of row j as well.
 template <int W>
 __device__ void build_flat(const SearchArgs &a, const RootCtx &r, const WarpSmem &h, int deg,
                            int np, int lane)
 {
+    constexpr int kB = WalkBatch<W>::value;
     unsigned *rows = r.rowsP;   // rowsX follows rowsP directly
     for (int g0 = 0; g0 < deg; g0 += 32) {
         const int t = g0 + lane;
@@ -802,10 +810,10 @@ __device__ void build_flat(const SearchArgs &a, const RootCtx &r, const WarpSmem
         // forward, and long lists are crossed rarely (measured: the narrowest class, whose roots
         // see many short lists, runs faster reading the cursors from shared memory each time)
         int own = 0, own_start = 0, own_next = h.cur_start[1], own_base = h.cur_base[0];
-        for (int f0 = 0; f0 < total; f0 += 32 * kBatch) {
-            int w[kBatch], ow[kBatch];
+        for (int f0 = 0; f0 < total; f0 += 32 * kB) {
+            int w[kB], ow[kB];
 #pragma unroll
-            for (int b = 0; b < kBatch; ++b) {
+            for (int b = 0; b < kB; ++b) {
                 const int f = f0 + b * 32 + lane;
                 ow[b] = -1;
                 w[b] = -1;
@@ -827,7 +835,7 @@ __device__ void build_flat(const SearchArgs &a, const RootCtx &r, const WarpSmem
                 }
             }
 #pragma unroll
-            for (int b = 0; b < kBatch; ++b) {
+            for (int b = 0; b < kB; ++b) {
                 if (ow[b] < 0) continue;
                 const int j = hash_find(h, w[b]);
                 if (j < 0) continue;
