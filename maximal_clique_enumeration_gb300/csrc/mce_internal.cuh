@@ -208,7 +208,7 @@ cudaError_t launch_search_prep(const SearchArgs &a, cudaStream_t s);
 cudaError_t search_occupancy(int group, int ip, int l2, int threads, size_t smem,
                              int *blocks_per_sm);
 // Shared memory of the search kernel of class k: the size histogram, then per warp a hash of
-// P(v) (ids and local indices) and a staging row.
+// P(v) (ids and local indices), its bit filter, the build cursors and (W <= 4) a row area.
 __host__ __device__ inline int hash_slots(int k) { return 64 << k; }
 // Rows of a root with deg * W <= smem_row_words(k) are built and searched in shared memory.
 __host__ __device__ inline int smem_row_words(int k) { return k <= 2 ? 1024 : 0; }
