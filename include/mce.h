@@ -11,7 +11,9 @@
  * (Section 2.4, Algorithm 3) taken in degeneracy order (Section 2.4, "Degeneracy Ordering"),
  * each solved on a binary-encoded induced subgraph over P u X (Sections 2.4 and 3.4, "full"
  * induced subgraph) with the compact X representation of Section 3.5 and the worker list of
- * Section 3.3.  Everything runs on one GPU.
+ * Section 3.3.  mce_config selects the alternatives of the same pages: partial induced
+ * subgraphs (Section 3.4, and the rule of Section 4.5 that picks them) and independent
+ * second-level subtrees (Section 3.2, Algorithm 4).  Everything runs on one GPU.
  *
  * Conventions shared by every entry point
  *   - Streams are passed as `void *` holding a cudaStream_t (NULL = the legacy default
@@ -140,7 +142,7 @@ mce_status mce_create(const int32_t *offsets, const int32_t *adj, int32_t n, int
 /*
  * Recomputes the degeneracy order (Section 2.4, "Degeneracy Ordering"): a parallel k-core peel
  * on the GPU, then the split of every adjacency into earlier (X) and later (P) neighbours and
- * the heavy-first schedule of first-level subtrees.  mce_count, mce_count_roots and
+ * the heavy-first schedule of the subtrees.  mce_count, mce_count_roots and
  * mce_enumerate use the order computed last; mce_create computes it once.  This entry point
  * exists so that a timing loop can include the preprocessing, as Section 4.1 ("Reporting of
  * Measurements") does.  Asynchronous on `stream`.
@@ -163,6 +165,8 @@ mce_status mce_count(mce_graph *g, void *stream, uint64_t *d_out);
 /*
  * Same as mce_count, restricted to the first-level subtrees (Algorithm 3) of the given roots:
  * the maximal cliques whose earliest vertex in the current degeneracy order is one of them.
+ * With second-level subtrees (mce_config.subtree_level = 2) the same cliques are found through
+ * the subtrees of each root's edges to its later neighbours (Algorithm 4).
  * Summing the outputs over a partition of V gives mce_count's output, which makes runs
  * resumable and lets large graphs be processed in pieces.
  *   d_roots  device pointer to int32[n_roots], original vertex ids (duplicates count twice).
