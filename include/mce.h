@@ -133,8 +133,8 @@ mce_status mce_config_default(mce_config *cfg);
  *   out      receives the handle; *out is NULL on failure.
  * Synchronises `stream` (the input checks and the workspace size are read back to the host).
  * Errors: MCE_ERR_INVALID_ARG, MCE_ERR_ID_RANGE, MCE_ERR_NOT_SIMPLE, MCE_ERR_NOT_SYMMETRIC,
- * MCE_ERR_OUT_OF_MEMORY, MCE_ERR_LIMIT (a first-level P larger than 1024 vertices, or a degree
- * of 2^21 or more), MCE_ERR_CUDA.
+ * MCE_ERR_OUT_OF_MEMORY, MCE_ERR_LIMIT (a first-level P larger than 1024 vertices, a degree of
+ * 2^21 or more, or with second-level subtrees n + m of 2^31 or more), MCE_ERR_CUDA.
  */
 mce_status mce_create(const int32_t *offsets, const int32_t *adj, int32_t n, int is_device_ptr,
                       const mce_config *cfg, void *stream, mce_graph **out);

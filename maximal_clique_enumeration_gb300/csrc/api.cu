@@ -297,6 +297,8 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
     }
     g.ip = h->cfg.induced == 2 ? 1 : 0;
     g.l2 = h->cfg.subtree_level == 2 ? 1 : 0;
+    // second-level subtrees are counted in int32 prefixes: at most one per edge and vertex
+    if (g.l2 && (long long)n + h->nnz / 2 >= (1LL << 31)) return MCE_ERR_LIMIT;
     if (g.l2) {
         MCE_ALLOC(h, g.unit_cnt, (size_t)n + 1);
         MCE_ALLOC(h, g.sched_uoff, (size_t)n + 1);
