@@ -23,7 +23,7 @@ _LIB_PATH = os.path.join(_HERE, "_build", "liboracle.so")
 _lib = None
 
 OK, INVALID_ARG, NOT_SIMPLE, NOT_SYMMETRIC, ID_RANGE, NOMEM, BUFFER = range(7)
-ALG3_TOMITA, ALG2_TOMITA, ALG2_PIVOT_P, ALG1_PLAIN = range(4)
+ALG3_TOMITA, ALG2_TOMITA, ALG2_PIVOT_P, ALG1_PLAIN, ALG4_TOMITA = range(5)
 
 
 class OracleError(RuntimeError):

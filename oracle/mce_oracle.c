@@ -53,7 +53,8 @@ enum {
     OR_ALG3_TOMITA = 0,   /* Algorithm 3 over degeneracy order, Algorithm 2 pivot over P u X */
     OR_ALG2_TOMITA = 1,   /* Algorithm 2 from R = {}, P = V, X = {}, pivot over P u X */
     OR_ALG2_PIVOT_P = 2,  /* Algorithm 2 from R = {}, P = V, X = {}, pivot over P only */
-    OR_ALG1_PLAIN = 3     /* Algorithm 1: no pivot */
+    OR_ALG1_PLAIN = 3,    /* Algorithm 1: no pivot */
+    OR_ALG4_TOMITA = 4    /* Algorithm 4 over degeneracy order (one subtree per edge), pivot as 0 */
 };
 
 /* ------------------------------------------------------------------ hashing */
@@ -463,6 +464,42 @@ static void first_level(bk_ctx *c, int32_t p)
     c->r_len = 0;
 }
 
+/*
+ * Algorithm 4 for the edges of the vertex at position p to later vertices q: R = {p, q},
+ * P = common neighbours after q, X = common neighbours before q.  An isolated vertex has no
+ * edge, so Algorithm 4 alone would miss its clique {p}; it is reported here (as Algorithm 3
+ * reports it for p).
+ */
+static void second_level(bk_ctx *c, int32_t p)
+{
+    const rgraph *g = c->g;
+    const int32_t *np_ = g->adj + g->offs[p];
+    int64_t dp = g->offs[p + 1] - g->offs[p];
+    if (dp == 0) {
+        c->R[0] = p;
+        c->r_len = 1;
+        bk(c, NULL, 0, NULL, 0);
+        c->r_len = 0;
+        return;
+    }
+    arena_mark m = arena_save(&c->mem);
+    int32_t *common = arena_alloc(&c->mem, dp);
+    if (!common) { c->err = OR_ERR_NOMEM; return; }
+    for (int64_t e = 0; e < dp && !c->err; ++e) {
+        int32_t q = np_[e];
+        if (q < p) continue;
+        int64_t k = intersect(np_, dp, g->adj + g->offs[q], g->offs[q + 1] - g->offs[q], common);
+        int64_t split = 0;
+        while (split < k && common[split] < q) ++split;
+        c->R[0] = p;
+        c->R[1] = q;
+        c->r_len = 2;
+        bk(c, common + split, k - split, common, split);
+    }
+    c->r_len = 0;
+    arena_restore(&c->mem, m);
+}
+
 static void whole_graph(bk_ctx *c)
 {
     arena_mark m = arena_save(&c->mem);
@@ -477,8 +514,9 @@ static void whole_graph(bk_ctx *c)
 /*
  * Counts the maximal cliques.  out[0] = count, out[1] = hash, out[2 + k] = number of maximal
  * cliques with k vertices for k < hist_len.  roots (original ids, may be NULL = every vertex)
- * restricts Algorithm 3 to those first-level subtrees; it is only meaningful for
- * OR_ALG3_TOMITA.  threads > 1 splits the first-level subtrees over OpenMP threads.
+ * restricts Algorithm 3 to those first-level subtrees (Algorithm 4 to those vertices' edges to
+ * later ones); it is only meaningful for OR_ALG3_TOMITA and OR_ALG4_TOMITA.  threads > 1 splits
+ * the roots over OpenMP threads.
  * nodes_out (optional) receives the number of search-tree nodes visited.
  */
 int oracle_count(int32_t n, const int32_t *offs, const int32_t *adj,
@@ -496,7 +534,7 @@ int oracle_count(int32_t n, const int32_t *offs, const int32_t *adj,
     memset(out, 0, sizeof(uint64_t) * (size_t)(2 + hist_len));
     uint64_t nodes = 0;
     int64_t work = roots ? n_roots : n;
-    if (variant != OR_ALG3_TOMITA) {
+    if (variant != OR_ALG3_TOMITA && variant != OR_ALG4_TOMITA) {
         bk_ctx c;
         rc = ctx_init(&c, &g, variant, hist_len);
         if (rc == OR_OK) {
@@ -525,7 +563,9 @@ int oracle_count(int32_t n, const int32_t *offs, const int32_t *adj,
 #endif
             for (int64_t i = 0; i < work; ++i) {
                 if (lrc != OR_OK || c.err) continue;
-                first_level(&c, roots ? rank[roots[i]] : (int32_t)i);
+                const int32_t p = roots ? rank[roots[i]] : (int32_t)i;
+                if (variant == OR_ALG4_TOMITA) second_level(&c, p);
+                else first_level(&c, p);
             }
             if (lrc == OR_OK && c.err) lrc = c.err;
             if (lrc == OR_OK && c.overflow) lrc = OR_ERR_BUFFER;
@@ -571,18 +611,24 @@ int oracle_enumerate(int32_t n, const int32_t *offs, const int32_t *adj,
     if (rc == OR_OK) {
         c.ids = ids; c.cap_ids = cap_ids;
         c.offsets = offsets; c.cap_cl = cap_cliques;   /* offsets has cap_cliques + 1 slots */
-        if (variant != OR_ALG3_TOMITA) {
+        if (variant != OR_ALG3_TOMITA && variant != OR_ALG4_TOMITA) {
             whole_graph(&c);
         } else if (roots) {
             int32_t *rank = (int32_t *)malloc(sizeof(int32_t) * (size_t)(n + 1));
             if (!rank) c.err = OR_ERR_NOMEM;
             else {
                 for (int32_t p = 0; p < n; ++p) rank[g.orig[p]] = p;
-                for (int64_t i = 0; i < n_roots && !c.err; ++i) first_level(&c, rank[roots[i]]);
+                for (int64_t i = 0; i < n_roots && !c.err; ++i) {
+                    if (variant == OR_ALG4_TOMITA) second_level(&c, rank[roots[i]]);
+                    else first_level(&c, rank[roots[i]]);
+                }
                 free(rank);
             }
         } else {
-            for (int32_t p = 0; p < n && !c.err; ++p) first_level(&c, p);
+            for (int32_t p = 0; p < n && !c.err; ++p) {
+                if (variant == OR_ALG4_TOMITA) second_level(&c, p);
+                else first_level(&c, p);
+            }
         }
         if (!c.overflow) offsets[c.n_cl] = c.n_ids;
         sizes_out[0] = c.n_cl;

@@ -207,6 +207,30 @@ def test_search_variants_agree():
             sorted(O.enumerate_cliques(g))
 
 
+@pytest.mark.parametrize("n", [0, 1, 2, 5, 9, 13])
+def test_second_level_decomposition_brute_force(n):
+    # Algorithm 4 (one subtree per edge, plus isolated vertices) reaches exactly the maximal
+    # cliques that brute force finds
+    for seed, p in itertools.product(range(3), [0.1, 0.4, 0.7, 0.95]):
+        g = G.er_graph(n, p, seed + 7)
+        expect = pins.brute_subsets(g)
+        assert sorted(O.enumerate_cliques(g, variant=O.ALG4_TOMITA)) == expect
+        assert O.count(g, variant=O.ALG4_TOMITA).key() == pins.summary(expect)
+
+
+def test_second_level_decomposition_per_root():
+    # per root, Algorithm 4 over the root's edges to later vertices gives the same cliques as
+    # the root's first-level subtree (the first level of Algorithm 3 takes no pivot)
+    g = G.config_graph("planted50k", 3)
+    rng = np.random.default_rng(9)
+    roots = np.sort(rng.choice(g.n, 3000, replace=False)).astype(np.int32)
+    assert O.count(g, roots=roots, variant=O.ALG4_TOMITA).key() == O.count(g, roots=roots).key()
+    for h in [G.moon_moser(5), G.cocktail_party(8), G.empty_graph(7), G.path_graph(30),
+              G.complete_graph(12), G.ba_graph(300, 5, 2)]:
+        assert sorted(O.enumerate_cliques(h, variant=O.ALG4_TOMITA)) == \
+            sorted(O.enumerate_cliques(h))
+
+
 def test_root_subsets_are_additive_and_threads_agree():
     g = G.config_graph("planted50k", 2)
     full = O.count(g, threads=4)

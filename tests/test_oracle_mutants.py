@@ -36,6 +36,12 @@ BATTERY = textwrap.dedent("""
                       (G.empty_graph(5), 5, 1), (G.path_graph(5), 4, 2)]:
         r = o.count(g)
         assert r.count == cnt and r.key()[2] == tuple([0] * k + [cnt])
+        r = o.count(g, variant=O.ALG4_TOMITA)
+        assert r.count == cnt and r.key()[2] == tuple([0] * k + [cnt])
+    for seed in range(2):
+        for p in (0.3, 0.6, 0.9):
+            g = G.er_graph(10, p, seed)
+            assert sorted(o.enumerate_cliques(g, variant=O.ALG4_TOMITA)) == pins.brute_subsets(g)
     import networkx as nx
     for name in ("er200", "rmat_s9"):
         g = G.config_graph(name, 1)
@@ -70,6 +76,11 @@ MUTANTS = {
                                 "rnd[batch[i]] = r; core[batch[i]] = r;"),
     "rank_counting_sort_shift": ("for (int32_t v = 0; v < n; ++v) start[rnd[v] + 1]++;",
                                  "for (int32_t v = 0; v < n; ++v) start[rnd[v]]++;"),
+    "second_level_X_split_at_first_vertex": ("while (split < k && common[split] < q) ++split;",
+                                             "while (split < k && common[split] < p) ++split;"),
+    "second_level_drops_X": ("bk(c, common + split, k - split, common, split);",
+                             "bk(c, common + split, k - split, common, 0);"),
+    "second_level_misses_isolated": ("        bk(c, NULL, 0, NULL, 0);\n", "\n"),
 }
 
 
