@@ -132,6 +132,9 @@ mce_status mce_config_default(mce_config *cfg);
  *   stream   the copy, the input checks and the first degeneracy ordering run on it.
  *   out      receives the handle; *out is NULL on failure.
  * Synchronises `stream` (the input checks and the workspace size are read back to the host).
+ * Device memory comes from a memory pool the library keeps per device (stream-ordered, on
+ * `stream`); mce_destroy returns it to that pool, which keeps it for later handles until the
+ * process ends.
  * Errors: MCE_ERR_INVALID_ARG, MCE_ERR_ID_RANGE, MCE_ERR_NOT_SIMPLE, MCE_ERR_NOT_SYMMETRIC,
  * MCE_ERR_OUT_OF_MEMORY, MCE_ERR_LIMIT (a first-level P larger than 1024 vertices, a degree of
  * 2^21 or more, or with second-level subtrees n + m of 2^31 or more), MCE_ERR_CUDA.
@@ -258,7 +261,8 @@ mce_status mce_last_error(mce_graph *g, void *stream);
 /* Fills *info; the diagnostics refer to the last completed call (synchronises the device). */
 mce_status mce_get_info(mce_graph *g, mce_info *info);
 
-/* Frees the handle and its device memory (synchronises the device first).  NULL is a no-op. */
+/* Frees the handle and returns its device memory to the library's pool (synchronises the
+ * device first).  NULL is a no-op. */
 void mce_destroy(mce_graph *g);
 
 /* Static English description of a status code. */

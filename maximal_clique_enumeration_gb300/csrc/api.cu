@@ -1,6 +1,8 @@
 // Host side of the C ABI declared in include/mce.h.
+#include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -24,6 +26,7 @@ struct mce_graph {
     int degeneracy = 0, max_degree = 0, hist_len = 2, rounds = 0;
     unsigned long long ws_words = 0;
     std::vector<void *> allocs;
+    cudaStream_t alloc_stream = nullptr;   // stream the next allocations are ordered on
     DevGraph g{};
     unsigned long long *hist_acc = nullptr;     // [hist_len]
     unsigned int *ws = nullptr;
@@ -57,12 +60,44 @@ mce_status from_cuda(cudaError_t e)
         if (_st != MCE_OK) return _st;                       \
     } while (0)
 
+// Device memory comes from one stream-ordered pool per device, owned by the library, that keeps
+// freed memory instead of returning it to the driver: a handle created after another one was
+// destroyed reuses its memory without a cudaMalloc / cudaFree round trip each time.
+constexpr int kMaxDevices = 64;
+cudaMemPool_t g_pool[kMaxDevices];
+std::mutex g_pool_lock;
+
+cudaMemPool_t device_pool(int device)
+{
+    if (device < 0 || device >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_pool_lock);
+    if (!g_pool[device]) {
+        cudaMemPoolProps props{};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = device;
+        cudaMemPool_t pool = nullptr;
+        if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        uint64_t keep = UINT64_MAX;
+        cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        g_pool[device] = pool;
+    }
+    return g_pool[device];
+}
+
 template <typename T>
 mce_status dev_alloc(mce_graph *h, T **p, size_t count)
 {
     void *q = nullptr;
     const size_t bytes = count * sizeof(T) > 0 ? count * sizeof(T) : 16;
-    cudaError_t e = cudaMalloc(&q, bytes);
+    cudaMemPool_t pool = device_pool(h->device);
+    // ordered on the stream of the call that allocates; that call synchronises it or uses the
+    // memory on it before any other stream can
+    cudaError_t e = pool ? cudaMallocFromPoolAsync(&q, bytes, pool, h->alloc_stream)
+                         : cudaMalloc(&q, bytes);
     if (e != cudaSuccess) {
         cudaGetLastError();
         *p = nullptr;
@@ -89,7 +124,17 @@ mce_status read_status(mce_graph *h, cudaStream_t s)
 
 void free_all(mce_graph *h)
 {
-    for (void *p : h->allocs) cudaFree(p);
+    if (!h->allocs.empty()) {
+        // no work of this handle may still be running on any stream (as cudaFree would wait)
+        cudaDeviceSynchronize();
+        cudaGetLastError();
+        for (void *p : h->allocs) {
+            if (device_pool(h->device)) cudaFreeAsync(p, 0);
+            else cudaFree(p);
+        }
+        cudaStreamSynchronize(0);
+        cudaGetLastError();
+    }
     h->allocs.clear();
     for (int i = 0; i < 2; ++i)
         if (h->ev_order[i]) cudaEventDestroy(h->ev_order[i]);
@@ -201,6 +246,7 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
 {
     MCE_TRY(cudaGetDevice(&h->device));
     MCE_TRY(cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, h->device));
+    h->alloc_stream = s;
     h->n = n;
     // offsets[0] and offsets[n] (= number of adjacency entries)
     int first = 0, last = 0;
@@ -382,6 +428,8 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
     MCE_ALLOC(h, h->totals, 2);
     MCE_ALLOC(h, h->count_cache, (size_t)h->hist_len + 2);
     MCE_ALLOC(h, h->roots_count, (size_t)h->hist_len + 2);
+    // the allocations are ordered on s: complete them before the handle is used on any stream
+    MCE_TRY(cudaStreamSynchronize(s));
     return MCE_OK;
 }
 
@@ -443,6 +491,7 @@ static mce_status count_impl(mce_graph *h, cudaStream_t s, const int32_t *d_root
         return MCE_OK;
     }
     h->launches_count = 1;                                  // finalize
+    h->alloc_stream = s;
     if (d_roots) {
         h->launches_count += 3;                             // root binning
         if (n_roots > h->uroots_cap) {
