@@ -134,7 +134,7 @@ mce_status mce_config_default(mce_config *cfg);
  * Synchronises `stream` (the input checks and the workspace size are read back to the host).
  * Device memory comes from a memory pool the library keeps per device (stream-ordered, on
  * `stream`); mce_destroy returns it to that pool, which keeps it for later handles until the
- * process ends.
+ * process ends or mce_trim_memory hands it back to the driver.
  * Errors: MCE_ERR_INVALID_ARG, MCE_ERR_ID_RANGE, MCE_ERR_NOT_SIMPLE, MCE_ERR_NOT_SYMMETRIC,
  * MCE_ERR_OUT_OF_MEMORY, MCE_ERR_LIMIT (a first-level P larger than 1024 vertices, a degree of
  * 2^21 or more, or with second-level subtrees n + m of 2^31 or more), MCE_ERR_CUDA.
@@ -264,6 +264,16 @@ mce_status mce_get_info(mce_graph *g, mce_info *info);
 /* Frees the handle and returns its device memory to the library's pool (synchronises the
  * device first).  NULL is a no-op. */
 void mce_destroy(mce_graph *g);
+
+/*
+ * Returns the device memory that the library's pool for the current device keeps cached (the
+ * memory of destroyed handles) to the driver; memory of live handles stays.  The library keeps
+ * freed memory so that creating a handle after destroying another one needs no cudaMalloc; a
+ * caller that shares the GPU with another allocator (for example a framework's caching
+ * allocator) calls this once it has destroyed its handles.  Synchronises the device.
+ * Errors: MCE_ERR_CUDA.
+ */
+mce_status mce_trim_memory(void);
 
 /* Static English description of a status code. */
 const char *mce_status_str(mce_status s);

@@ -26,7 +26,8 @@ STATUS = {
 }
 EXPORTS = ["mce_config_default", "mce_create", "mce_order", "mce_count", "mce_count_roots",
            "mce_enumerate", "mce_get_order", "mce_last_error", "mce_get_info", "mce_get_profile",
-           "mce_destroy", "mce_status_str", "mce_order_noalloc", "mce_enumerate_roots"]
+           "mce_destroy", "mce_status_str", "mce_order_noalloc", "mce_enumerate_roots",
+           "mce_trim_memory"]
 PROFILE_ACTIVITIES = ["build", "pivot", "child", "partition", "donate", "idle", "max_root",
                       "roots"]
 
@@ -112,6 +113,8 @@ def library(path: str | None = None):
     lib.mce_get_profile.argtypes = [P, P]
     lib.mce_destroy.restype = None
     lib.mce_destroy.argtypes = [P]
+    lib.mce_trim_memory.restype = st
+    lib.mce_trim_memory.argtypes = []
     lib.mce_status_str.restype = ctypes.c_char_p
     lib.mce_status_str.argtypes = [st]
     _lib = lib
@@ -367,6 +370,11 @@ class Graph:
                                        ctypes.c_void_p(rank.data_ptr()),
                                        ctypes.c_void_p(core.data_ptr())), "mce_get_order")
         return rank[: self.n], core[: self.n]
+
+
+def trim_memory():
+    """Hands the device memory cached by the library's pool (current device) back to the driver."""
+    _check(library().mce_trim_memory(), "mce_trim_memory")
 
 
 def _enumerate_roots_into(h, roots, ids, offs, stream):

@@ -23,6 +23,7 @@ struct mce_graph {
     unsigned long long grp_ws[kNumGroups] = {};
     size_t cls_smem[kNumClasses] = {};
     long long uroots_cap = 0;
+    bool unit_own = false;    // unit_cnt / unit_scan were reallocated for a caller's root list
     int degeneracy = 0, max_degree = 0, hist_len = 2, rounds = 0;
     unsigned long long ws_words = 0;
     std::vector<void *> allocs;
@@ -122,8 +123,43 @@ mce_status read_status(mce_graph *h, cudaStream_t s)
     return (mce_status)st;
 }
 
+// Makes the handle's device current for the lifetime of this object (and restores the caller's
+// device afterwards), so that synchronisation and frees act on the device that owns the memory.
+struct OnDevice {
+    int saved = -1;
+    explicit OnDevice(int device)
+    {
+        if (cudaGetDevice(&saved) != cudaSuccess) {
+            cudaGetLastError();
+            saved = -1;
+        }
+        if (saved != device) cudaSetDevice(device);
+    }
+    ~OnDevice()
+    {
+        int cur = -1;
+        if (saved >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != saved) cudaSetDevice(saved);
+        cudaGetLastError();
+    }
+};
+
+// Returns one allocation of the handle to the pool (ordered on stream s) and forgets it.
+void dev_free(mce_graph *h, void *p, cudaStream_t s)
+{
+    if (!p) return;
+    for (size_t i = 0; i < h->allocs.size(); ++i) {
+        if (h->allocs[i] != p) continue;
+        h->allocs[i] = h->allocs.back();
+        h->allocs.pop_back();
+        if (device_pool(h->device)) cudaFreeAsync(p, s);
+        else cudaFree(p);
+        return;
+    }
+}
+
 void free_all(mce_graph *h)
 {
+    OnDevice on(h->device);
     if (!h->allocs.empty()) {
         // no work of this handle may still be running on any stream (as cudaFree would wait)
         cudaDeviceSynchronize();
@@ -495,17 +531,32 @@ static mce_status count_impl(mce_graph *h, cudaStream_t s, const int32_t *d_root
     if (d_roots) {
         h->launches_count += 3;                             // root binning
         if (n_roots > h->uroots_cap) {
+            // grow geometrically, and give the replaced buffers back to the pool (in stream
+            // order: work already queued on s still reads them)
+            long long cap = h->uroots_cap * 2 > n_roots ? h->uroots_cap * 2 : n_roots;
+            if (cap > INT32_MAX) cap = INT32_MAX;
+            dev_free(h, h->g.uroots, s);
+            h->g.uroots = nullptr;
+            h->uroots_cap = 0;
             int *buf = nullptr;
-            MCE_ALLOC(h, buf, (size_t)n_roots);
+            MCE_ALLOC(h, buf, (size_t)cap);
             h->g.uroots = buf;
             if (h->g.l2) {
                 // second-level subtrees: their prefix over the caller's roots, and scan scratch
-                const size_t len = (size_t)(n_roots > h->n ? n_roots : h->n);
-                MCE_ALLOC(h, h->g.uroots_uoff, (size_t)n_roots + 1);
+                // (the schedule's own buffers stay: mce_order uses them)
+                dev_free(h, h->g.uroots_uoff, s);
+                h->g.uroots_uoff = nullptr;
+                if (h->unit_own) {
+                    dev_free(h, h->g.unit_cnt, s);
+                    dev_free(h, h->g.unit_scan, s);
+                }
+                const size_t len = (size_t)(cap > h->n ? cap : h->n);
+                MCE_ALLOC(h, h->g.uroots_uoff, (size_t)cap + 1);
                 MCE_ALLOC(h, h->g.unit_cnt, len + 1);
                 MCE_ALLOC(h, h->g.unit_scan, len / kScanBlock + 2);
+                h->unit_own = true;
             }
-            h->uroots_cap = n_roots;
+            h->uroots_cap = cap;
         }
         MCE_TRY(launch_bin_roots(h->g, d_roots, (int)n_roots, s));
         if (h->g.l2) {
@@ -701,9 +752,23 @@ mce_status mce_get_profile(mce_graph *h, uint64_t *out)
 void mce_destroy(mce_graph *h)
 {
     if (!h) return;
-    cudaDeviceSynchronize();
+    {
+        OnDevice on(h->device);
+        cudaDeviceSynchronize();
+    }
     free_all(h);
     delete h;
+}
+
+mce_status mce_trim_memory(void)
+{
+    int dev = 0;
+    MCE_TRY(cudaGetDevice(&dev));
+    cudaMemPool_t pool = device_pool(dev);
+    if (!pool) return MCE_OK;
+    MCE_TRY(cudaDeviceSynchronize());
+    MCE_TRY(cudaMemPoolTrimTo(pool, 0));
+    return MCE_OK;
 }
 
 }  // extern "C"

@@ -146,7 +146,9 @@ __global__ void __launch_bounds__(kPeelThreads, 1) peel_kernel(DevGraph g, long 
 
     int *alive = g.alive_a, *alive_next = g.alive_b;
     int n_alive = n, k = 0, r = 0, pos = 0, phase = 0, dmax = 0;
-    long long live_entries = g.nnz;   // adjacency entries of the remaining vertices
+    // adjacency entries of the remaining vertices, read from the offsets themselves (callers of
+    // the allocation-free entry point pass no edge count)
+    long long live_entries = n > 0 ? (long long)g.offs[n] - (long long)g.offs[0] : 0;
     bool solo = false;
     int nb = gridDim.x, b = blockIdx.x;
     const int tile = nthr * kPeelItems;

@@ -107,5 +107,28 @@ def load_golden(name: str):
     return n, edges, sorted(cliques), info
 
 
+def load_peel_golden(name: str):
+    """(n, edges, {vertex: (round, core, rank)}, info) of a hand-derived peel fixture."""
+    path = os.path.join(HERE, "golden", name)
+    edges, peel, info = [], {}, {}
+    n = 0
+    with open(path) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            key, *vals = line.split()
+            if key == "vertices":
+                n = int(vals[0])
+            elif key == "edge":
+                edges.append((int(vals[0]), int(vals[1])))
+            elif key == "peel":
+                v, rnd, core, rank = (int(x) for x in vals)
+                peel[v] = (rnd, core, rank)
+            else:
+                info[key] = int(vals[0])
+    return n, edges, peel, info
+
+
 def csr_arrays(g):
     return np.asarray(g.offsets, np.int32), np.asarray(g.adj, np.int32)

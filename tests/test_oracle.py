@@ -286,6 +286,51 @@ def test_peel_core_numbers_and_order(name, seed):
         assert all(cn[v] == core[v] for v in range(g.n))
 
 
+@pytest.mark.parametrize("fixture", ["peel_fig1.txt", "peel_k4_tails.txt"])
+def test_peel_rounds_match_hand_derivation(fixture):
+    # round, core number and rank of every vertex, derived by hand from the canonical peel's
+    # definition (the fixture headers show the derivation)
+    n, edges, expect, info = pins.load_peel_golden(fixture)
+    g = G.csr_from_edges(n, *zip(*edges))
+    core, rnd, rank, d = O.peel(g)
+    assert d == info["degeneracy"]
+    assert int(rnd.max()) + 1 == info["rounds"]
+    for v, (r, c, k) in expect.items():
+        assert (int(rnd[v]), int(core[v]), int(rank[v])) == (r, c, k), v
+
+
+def canonical_peel_violations(g, rnd, core):
+    """Checks (round, core) against the definition of the canonical peel, round by round.
+
+    With A_r the vertices whose round is >= r (those left at the start of round r) and deg_r(v)
+    the number of neighbours of v in A_r, round r at level k_r must remove exactly
+    {v in A_r : deg_r(v) <= k_r}, where k_r = max(k_{r-1}, min over A_r of deg_r) and k_{-1} = 0
+    (the level only rises when nothing qualifies, and then to the least remaining degree).
+    Returns the list of rounds that break it.
+    """
+    src = np.repeat(np.arange(g.n), g.degrees())
+    dst = g.adj.astype(np.int64)
+    bad = []
+    k_prev = 0
+    for r in range(int(rnd.max()) + 1 if g.n else 0):
+        alive = rnd >= r
+        keep = alive[src] & alive[dst]
+        deg_r = np.bincount(src[keep], minlength=g.n)
+        k_r = max(k_prev, int(deg_r[alive].min()))
+        removed = alive & (deg_r <= k_r)
+        if not np.array_equal(removed, rnd == r) or np.any(core[rnd == r] != k_r):
+            bad.append(r)
+        k_prev = k_r
+    return bad
+
+
+@pytest.mark.parametrize("name,seed", [("er200", 2), ("rmat_s10", 1), ("ba100k", 1)])
+def test_peel_rounds_satisfy_the_definition(name, seed):
+    g = G.config_graph(name, seed)
+    core, rnd, rank, d = O.peel(g)
+    assert canonical_peel_violations(g, rnd, core) == []
+
+
 # ---------------------------------------------------------------- input checks
 
 def _raw(n, lists):

@@ -42,6 +42,11 @@ BATTERY = textwrap.dedent("""
         for p in (0.3, 0.6, 0.9):
             g = G.er_graph(10, p, seed)
             assert sorted(o.enumerate_cliques(g, variant=O.ALG4_TOMITA)) == pins.brute_subsets(g)
+    for fx in ("peel_fig1.txt", "peel_k4_tails.txt"):
+        n, edges, expect, info = pins.load_peel_golden(fx)
+        core, rnd, rank, d = o.peel(G.csr_from_edges(n, *zip(*edges)))
+        assert d == info["degeneracy"] and int(rnd.max()) + 1 == info["rounds"]
+        assert all((int(rnd[v]), int(core[v]), int(rank[v])) == e for v, e in expect.items())
     import networkx as nx
     for name in ("er200", "rmat_s9"):
         g = G.config_graph(name, 1)
@@ -74,6 +79,26 @@ MUTANTS = {
                               "if (curdeg[alive[i]] < k) batch[nb++] = alive[i];"),
     "core_is_round_not_level": ("rnd[batch[i]] = r; core[batch[i]] = k;",
                                 "rnd[batch[i]] = r; core[batch[i]] = r;"),
+    # a level's vertices removed one at a time in id order (each removal updating its
+    # neighbours at once, so a neighbour later in the sweep can join the same round)
+    "peel_one_at_a_time_within_a_round": (
+        "        for (int32_t i = 0; i < n_alive; ++i)\n"
+        "            if (curdeg[alive[i]] <= k) batch[nb++] = alive[i];\n"
+        "        if (nb == 0) { ++k; continue; }\n"
+        "        for (int32_t i = 0; i < nb; ++i) { rnd[batch[i]] = r; core[batch[i]] = k; }\n"
+        "        for (int32_t i = 0; i < nb; ++i) {\n"
+        "            int32_t v = batch[i];\n"
+        "            for (int64_t e = offs[v]; e < offs[v + 1]; ++e)\n"
+        "                if (rnd[adj[e]] < 0) curdeg[adj[e]]--;\n"
+        "        }\n",
+        "        for (int32_t i = 0; i < n_alive; ++i) {\n"
+        "            int32_t v = alive[i];\n"
+        "            if (curdeg[v] > k) continue;\n"
+        "            batch[nb++] = v; rnd[v] = r; core[v] = k;\n"
+        "            for (int64_t e = offs[v]; e < offs[v + 1]; ++e)\n"
+        "                if (rnd[adj[e]] < 0) curdeg[adj[e]]--;\n"
+        "        }\n"
+        "        if (nb == 0) { ++k; continue; }\n"),
     "rank_counting_sort_shift": ("for (int32_t v = 0; v < n; ++v) start[rnd[v] + 1]++;",
                                  "for (int32_t v = 0; v < n; ++v) start[rnd[v]]++;"),
     "second_level_X_split_at_first_vertex": ("while (split < k && common[split] < q) ++split;",

@@ -1,22 +1,28 @@
-"""The allocation-free ordering entry point (mce_order_noalloc) against the regular one.
+"""The allocation-free ordering entry point (mce_order_noalloc), through the C ABI.
 
-Some callers cannot allocate device memory (a framework's allocator owns the GPU, or the call
-sits on a path that must not synchronise for cudaMalloc); mce_order_noalloc serves them from a
-fixed scratch array.  This test calls it through the C ABI twice in a row, on two different
-graphs, and checks that rank, core numbers and degeneracy equal what mce_create +
-mce_get_order report -- exactly, as these are integers.  The second call also shows that state
-left in the shared scratch array by the first call does not leak into the next result.
+Some callers cannot allocate device memory: code running under a framework whose caching
+allocator owns the GPU, plug-ins that are only handed buffers, or paths that must not stall on
+cudaMalloc.  mce_order_noalloc serves them from one fixed scratch array in device memory.
+
+Its rank, core numbers and degeneracy are compared exactly (they are integers) with the CPU
+oracle's canonical peel and with the regular entry point (mce_create + mce_get_order), on calls
+made back to back, so that anything the shared scratch array keeps from one call cannot leak
+into the next result.  The cases cover the largest graph the scratch admits (n = 2^18), a dense
+core that the peel must not finish in a single CTA, and the graph with no vertices.
 """
 import ctypes
 
 import numpy as np
 import pytest
 
+import oracle as O
 from maximal_clique_enumeration_gb300 import graphs as G
 
 pytestmark = pytest.mark.gpu
 
 torch = pytest.importorskip("torch")
+
+NOALLOC_MAX_N = 1 << 18
 
 
 @pytest.fixture(scope="module")
@@ -42,7 +48,7 @@ def _regular(g):
 
 def _noalloc(lib, g):
     offs = torch.from_numpy(g.offsets).cuda()
-    adj = torch.from_numpy(g.adj).cuda()
+    adj = torch.from_numpy(g.adj if g.adj.size else np.zeros(1, np.int32)).cuda()
     rank = torch.full((max(g.n, 1),), -7, dtype=torch.int32, device="cuda")
     core = torch.full((max(g.n, 1),), -7, dtype=torch.int32, device="cuda")
     res = torch.full((2,), -7, dtype=torch.int32, device="cuda")
@@ -58,18 +64,52 @@ def _noalloc(lib, g):
     return rank.cpu().numpy()[: g.n], core.cpu().numpy()[: g.n], int(r[0])
 
 
-def test_noalloc_order_matches_regular_entry_point_twice(lib):
+def _check_against_oracle(g, got):
+    core, _, rank, d = O.peel(g)
+    got_rank, got_core, got_d = got
+    assert np.array_equal(got_rank, rank), g.name
+    assert np.array_equal(got_core, core), g.name
+    assert got_d == d, g.name
+
+
+def test_noalloc_order_matches_oracle_and_regular_entry_point_twice(lib):
     graphs = [G.config_graph("ba100k", 1), G.config_graph("planted50k", 2)]
     expected = [_regular(g) for g in graphs]
     for g, (rank, core, d) in zip(graphs, expected):          # two calls in a row
-        got_rank, got_core, got_d = _noalloc(lib, g)
-        assert np.array_equal(got_rank, rank), g.name
-        assert np.array_equal(got_core, core), g.name
-        assert got_d == d, g.name
+        got = _noalloc(lib, g)
+        _check_against_oracle(g, got)
+        assert np.array_equal(got[0], rank), g.name
+        assert np.array_equal(got[1], core), g.name
+        assert got[2] == d, g.name
+
+
+def test_noalloc_at_the_size_limit_and_with_a_dense_core(lib):
+    # n at the limit fills every per-vertex array of the scratch to its end; the dense core
+    # (4,000 vertices, about 1.6M adjacency entries) keeps the peel on the whole grid
+    big = G.er_graph(NOALLOC_MAX_N, 8.0 / (NOALLOC_MAX_N - 1), 5, "er_noalloc_max")
+    dense = G.er_graph(4000, 0.1, 6, "er_dense_core")
+    assert big.n == NOALLOC_MAX_N and dense.offsets[-1] > (1 << 20)
+    for g in (big, dense, big):
+        _check_against_oracle(g, _noalloc(lib, g))
+
+
+def test_noalloc_empty_graph(lib):
+    g = G.empty_graph(0)
+    res = torch.full((2,), -7, dtype=torch.int32, device="cuda")
+    offs = torch.zeros(1, dtype=torch.int32, device="cuda")
+    code = lib.mce_order_noalloc(ctypes.c_void_p(offs.data_ptr()), None, 0, None, None,
+                                 ctypes.c_void_p(res.data_ptr()),
+                                 ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert code == 0
+    torch.cuda.synchronize()
+    assert res.cpu().tolist() == [0, 0]
+    # and a regular graph right after it still comes out right
+    g = G.config_graph("er200", 3)
+    _check_against_oracle(g, _noalloc(lib, g))
 
 
 def test_noalloc_rejects_oversize_graph(lib):
     res = torch.zeros(2, dtype=torch.int32, device="cuda")
-    code = lib.mce_order_noalloc(None, None, (1 << 18) + 1, None, None,
+    code = lib.mce_order_noalloc(None, None, NOALLOC_MAX_N + 1, None, None,
                                  ctypes.c_void_p(res.data_ptr()), None)
     assert code == 8                                           # MCE_ERR_LIMIT
