@@ -11,6 +11,15 @@ first-level subtrees each take minutes to hours), so the workload is every first
 subtree whose root has fewer than --max-p later neighbours (98% of the roots); the order is
 always computed for the whole graph.
 
+Beside the headline the same JSON line carries:
+  configs       the other four workloads (ER, BA, planted cliques, SBM), each timed whole
+                (order + count) with the oracle timed beside it;
+  graph_stages  achieved GB/s of the peel, the orientation and the subtree build against the
+                measured HBM bandwidth, from their algorithmic bytes;
+  heavy         a seeded sample of the R-MAT roots with 128 <= |P| < 256 (8-word rows);
+  activity      per-activity split of the search's warp time (MCE_PROFILE build, in a child
+                process), which also times the subtree build.
+
 Lines printed: one JSON object (rank 0).  `--impl reference` times the CPU oracle instead.
 """
 from __future__ import annotations
@@ -32,11 +41,13 @@ if ROOT not in sys.path:
 
 METRIC = "maximal cliques/sec (R-MAT s20 ef16)"
 UNIT = "cliques/s"
+OTHER_CONFIGS = ["er200", "ba100k", "planted50k", "sbm1m"]
+WIDTHS = [1, 2, 4, 8, 16, 32]
 
-# DRAM traffic of the dominant search launch, from the last ncu capture summarised in
-# profiles/search_kernel_w4_rmat_s20_sample.md (a 10 % root sample; dram bytes read + written
-# = 82.4 MB for 86,953,769 counted words).  It is scaled to a full launch by the counted words
-# and only reported while the kernel sources are the ones it was measured on.
+# DRAM traffic of the dominant search launch from an ncu capture of a 10 % root sample of this
+# workload (dram bytes read + written per counted bitset word).  It is scaled to a full launch
+# by the counted words, and only reported while the kernel sources hash to the version that
+# was captured.
 TRAFFIC_CAPTURE = {"sources": "b4a4ad260dfd7168", "width_class": 2,
                    "bytes_per_word": 93.36e6 / 86953769.0}
 KERNEL_SOURCES = ["maximal_clique_enumeration_gb300/csrc/search_impl.cuh",
@@ -53,7 +64,16 @@ def kernel_sources_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def parse_args():
+def hbm_peak():
+    """(GB/s, source) of the HBM roofline: the measured copy bandwidth, else fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "of measured (MEASURED_PEAKS.json hbm_gbs)"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "of fallback (6.8 TB/s)"
+
+
+def parse_args(argv=None):
     p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=5)
@@ -65,15 +85,23 @@ def parse_args():
                    help="first-level subtrees whose root has |P| < max_p form the workload")
     p.add_argument("--root-fraction", type=float, default=1.0,
                    help="profiling aid: keep only this seeded share of the workload roots")
-    p.add_argument("--cpu-fraction", type=float, default=0.2,
-                   help="share of the workload roots the oracle baseline counts")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--configs", default=",".join(OTHER_CONFIGS),
+                   help="other workloads timed beside the headline ('' for none)")
+    p.add_argument("--heavy-fraction", type=float, default=1 / 16,
+                   help="seeded share of the roots with 128 <= |P| < 256 timed as 'heavy' (0: off)")
+    p.add_argument("--no-activity", action="store_true",
+                   help="skip the activity profile (MCE_PROFILE build, child process)")
     p.add_argument("--induced", type=int, default=0, choices=[0, 1, 2],
                    help="induced subgraphs: 0 the Delta/d rule (default), 1 full, 2 partial")
     p.add_argument("--subtree-level", type=int, default=1, choices=[1, 2],
                    help="independent subtrees: 1 first-level (default), 2 second-level (per edge)")
-    return p.parse_args()
+    p.add_argument("--imbalance", action="store_true",
+                   help="diagnostic: per-SM load max/avg with and without the worker list "
+                        "(planted50k, rmat_s14), MCE_PROFILE build; prints one JSON line")
+    p.add_argument("--activity-child", default=None, help=argparse.SUPPRESS)
+    return p.parse_args(argv)
 
 
 # ---------------------------------------------------------------- process group (replicas)
@@ -114,11 +142,26 @@ def workload_graph(args):
     return G.config_graph(name, args.seed)
 
 
+def later_counts(g, rank):
+    """|P(v)| for every v: neighbours later in the order `rank`."""
+    src = np.repeat(np.arange(g.n), g.degrees())
+    return np.bincount(src[rank[g.adj] > rank[src]], minlength=g.n)
+
+
 def light_roots(g, rank, max_p):
     """Roots v with |P(v)| < max_p, where P(v) = neighbours later in the order `rank`."""
-    src = np.repeat(np.arange(g.n), g.degrees())
-    pc = np.bincount(src[rank[g.adj] > rank[src]], minlength=g.n)
+    pc = later_counts(g, rank)
     return np.nonzero(pc < max_p)[0].astype(np.int32), pc
+
+
+def heavy_roots(pc, fraction, seed):
+    """A seeded share of the roots with 128 <= |P| < 256 (the 8-word row class)."""
+    cand = np.nonzero((pc >= 128) & (pc < 256))[0]
+    if fraction <= 0 or cand.size == 0:
+        return np.zeros(0, np.int32), int(cand.size)
+    rng = np.random.default_rng(seed)
+    k = max(1, int(round(cand.size * fraction)))
+    return np.sort(rng.choice(cand, size=k, replace=False)).astype(np.int32), int(cand.size)
 
 
 def workload_config(args, g, roots, pc, d):
@@ -134,6 +177,41 @@ def workload_config(args, g, roots, pc, d):
         "induced": {0: "Delta/d rule", 1: "full", 2: "partial"}[getattr(args, "induced", 0)],
         "subtree_level": getattr(args, "subtree_level", 1),
     }
+
+
+# ---------------------------------------------------------------- algorithmic bytes (roofline)
+
+def stage_bytes(g, rank, roots, peel_live):
+    """Algorithmic bytes of the graph stages, from the graph (int32 everywhere).
+
+    peel (a1):   8m   every adjacency list read once, when its vertex is removed
+               + 8m   one 4-byte degree update per adjacency entry
+               + 8 L  id and degree of every live vertex in every round (L = live vertices
+                      summed over rounds, counted by the peel)
+               + 16n  rank, core number, round and order written
+    orient (a2): 8m + 8m + 4m + 16n: adjacency read, the rank of every entry gathered, every
+                 edge written once into a later-neighbour list N+; offsets and ranks read,
+                 |P| and the schedule written
+    build (a3):  per workload root v (|P| > 0), with W(v) words per row:
+                 16 deg(v)  N(v) read, the rank of each neighbour, |N+(u)| and offset of each
+               + 4 sum_{u in N(v)} |N+(u)|  the later-neighbour lists walked
+               + 4 deg(v) W(v)              the rows written
+    """
+    n, m = g.n, g.m
+    deg = g.degrees()
+    pc = later_counts(g, rank)
+    src = np.repeat(np.arange(n), deg)
+    walk = np.bincount(src, weights=pc[g.adj].astype(np.float64), minlength=n)
+    w = np.select([pc <= 32, pc <= 64, pc <= 128, pc <= 256, pc <= 512], [1, 2, 4, 8, 16], 32)
+    per_root = 16.0 * deg + 4.0 * walk + 4.0 * deg * w
+    sel = np.zeros(n, bool)
+    sel[roots] = True
+    sel &= pc > 0
+    k = np.log2(w).astype(int)
+    a3_cls = [float(per_root[sel & (k == c)].sum()) for c in range(6)]
+    return {"peel": 16.0 * m + 8.0 * peel_live + 16.0 * n,
+            "orient": 20.0 * m + 16.0 * n,
+            "build": float(sum(a3_cls)), "build_by_width": a3_cls}
 
 
 # ---------------------------------------------------------------- clocks
@@ -188,21 +266,222 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- CPU oracle baseline
 
-def oracle_sample(g, roots, fraction, seed, threads):
-    """Times the oracle (as it stands) on a seeded sample of the workload roots."""
+def oracle_count_timed(g, roots, threads, hist_len=1026):
+    """Times the oracle (as it stands) on the given roots (None = the whole graph)."""
     import oracle
     oracle.build()
-    rng = np.random.default_rng(seed)
-    k = max(1, int(len(roots) * fraction))
-    sample = np.sort(rng.choice(roots, size=k, replace=False)).astype(np.int32)
     t0 = time.perf_counter()
-    res = oracle.count(g, roots=sample, threads=threads, hist_len=1026)
-    dt = time.perf_counter() - t0
-    return sample, res, dt
+    res = oracle.count(g, roots=roots, threads=threads, hist_len=hist_len)
+    return res, time.perf_counter() - t0
 
 
-def cpu_block(value, cores, sample_desc):
-    return {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample_desc}
+def oracle_preprocessing_s(g):
+    """The oracle's own input checks and peel, timed alone (context for its rates)."""
+    import oracle
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.validate(g)
+    oracle.peel(g)
+    return time.perf_counter() - t0
+
+
+def cpu_block(value, cores, sample_desc, **extra):
+    return dict({"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                 "sample": sample_desc}, **extra)
+
+
+# ---------------------------------------------------------------- GPU helpers
+
+def timed_steps(step, steps, warmup, flush, stream, info_fn=None):
+    """W untimed steps, then K steps each bracketed by CUDA events on `stream` (L2 flushed
+    before each, untimed); returns (per-step ms list, summed info deltas)."""
+    import torch
+    for _ in range(max(warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+    ms, infos = [], []
+    for k in range(steps):
+        flush.fill_(k & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+        if info_fn is not None:
+            infos.append(info_fn())
+    return ms, infos
+
+
+def dominant_class(infos, steps):
+    ms_cls = np.sum([np.asarray(i["ms_search"]) for i in infos], axis=0) / steps
+    words = np.sum([np.asarray(i["words"], dtype=np.float64) for i in infos], axis=0) / steps
+    dom = int(np.argmax(ms_cls))
+    return dom, ms_cls, words
+
+
+def run_other_config(name, seed, args, flush, word_peak, threads, want_cpu, hbm):
+    """One of the other workloads, whole: W + K steps of (order + count), oracle beside it."""
+    import torch
+    import maximal_clique_enumeration_gb300 as mce
+    from maximal_clique_enumeration_gb300 import graphs as G
+    g = G.config_graph(name, seed)
+    h = mce.Graph(torch.from_numpy(g.offsets).cuda(), torch.from_numpy(g.adj).cuda(), g.n,
+                  profile=1)
+    out = h.new_output()
+    stream = torch.cuda.current_stream()
+
+    def step():
+        h.order()
+        h.count(out=out)
+
+    ms, infos = timed_steps(step, args.steps, args.warmup, flush, stream, h.get_info)
+    h.check()
+    res = mce.Graph.unpack(out)
+    step_ms = float(np.mean(ms))
+    dom, ms_cls, words = dominant_class(infos, args.steps)
+    order_ms = float(np.mean([i["ms_order"] for i in infos]))
+    peel_ms = float(np.mean([i["ms_peel"] for i in infos]))
+    info = infos[-1]
+    rank, _ = h.order_arrays()
+    rank = rank.cpu().numpy()
+    entry = {
+        "workload": G.CONFIGS[name] + f", seed {seed}",
+        "n": g.n, "m": g.m, "max_degree": g.max_degree(), "degeneracy": info["degeneracy"],
+        "induced": {1: "full", 2: "partial"}[info["induced"]],
+        "cliques": res[0], "hash": f"{res[1]:#018x}", "max_size": len(res[2]) - 1,
+        "ms_per_graph": step_ms, "value": res[0] / (step_ms * 1e-3), "unit": UNIT,
+        "stage_ms": {"order": order_ms, "peel": peel_ms,
+                     "search_by_width": {str(WIDTHS[i]): float(ms_cls[i])
+                                         for i in range(6) if ms_cls[i] > 0}},
+        "search_roofline": {"bound": "alu", "kernel": f"search_kernel<W={WIDTHS[dom]}>",
+                            "achieved_gword_s": words[dom] / max(ms_cls[dom], 1e-9) * 1e-6,
+                            "frac": (words[dom] / max(ms_cls[dom], 1e-9) * 1e3) / word_peak},
+        "tree_nodes": info["tree_nodes"], "donations": info["donations"],
+    }
+    sb = stage_bytes(g, rank, np.arange(g.n, dtype=np.int32), info["peel_live"])
+    entry["graph_stages"] = {
+        "peel": _gbs(sb["peel"], peel_ms, hbm),
+        "orient": _gbs(sb["orient"], order_ms - peel_ms, hbm)}
+    if want_cpu:
+        if name == "sbm1m":
+            # a seeded tenth of the roots keeps the oracle near 10 s; the GPU counts the same
+            from maximal_clique_enumeration_gb300.graphs import sample_roots
+            roots = sample_roots(g.n, g.n // 10, seed + 4000)
+            ores, dt = oracle_count_timed(g, roots, threads, hist_len=h.hist_len)
+            got = h.count_roots_result(roots)
+            desc = (f"oracle on a seeded 10% of the roots ({len(roots)}): {ores.count} cliques "
+                    f"in {dt:.1f} s, including its input checks, peel and relabelling")
+        else:
+            ores, dt = oracle_count_timed(g, None, threads, hist_len=h.hist_len)
+            got = res
+            desc = (f"oracle on the whole graph: {ores.count} cliques in {dt:.2f} s, including "
+                    f"its input checks, peel and relabelling")
+        entry["cpu_baseline"] = cpu_block(ores.count / dt, threads, desc)
+        entry["parity"] = "ok" if got == ores.key() else f"MISMATCH {got} {ores.key()}"
+    h.close()
+    return entry
+
+
+def _gbs(nbytes, ms, hbm):
+    if ms <= 0:
+        return {"bytes": nbytes, "ms": ms, "achieved_gbs": None, "frac": None}
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"bytes": nbytes, "ms": ms, "achieved_gbs": gbs, "frac": gbs / hbm[0],
+            "peak_gbs": hbm[0], "peak": hbm[1]}
+
+
+# ---------------------------------------------------------------- activity profile (child)
+
+def activity_profile(g, roots, args):
+    """Runs the MCE_PROFILE build on the same graph and roots in a child process; returns its
+    per-class activity split (SM cycles summed over warps) and per-SM loads."""
+    with tempfile.TemporaryDirectory() as d:
+        path = os.path.join(d, "w.npz")
+        np.savez(path, offsets=g.offsets, adj=g.adj, roots=roots)
+        cmd = [sys.executable, os.path.abspath(__file__), "--activity-child", path,
+               "--induced", str(args.induced), "--subtree-level", str(args.subtree_level)]
+        r = subprocess.run(cmd, capture_output=True, text=True, timeout=900)
+    if r.returncode != 0:
+        return {"error": (r.stderr or r.stdout)[-500:]}
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def _load_stats(sm_busy, n_sms):
+    x = np.asarray(sm_busy[:n_sms], dtype=np.float64)
+    if x.sum() <= 0:
+        return None
+    return {"max_over_avg": float(x.max() / x.mean()), "min_over_avg": float(x.min() / x.mean())}
+
+
+def activity_child(args):
+    """Child process: load the MCE_PROFILE library (MCE_LIBRARY) and profile one search."""
+    import torch
+    from maximal_clique_enumeration_gb300 import build
+    os.environ["MCE_LIBRARY"] = build.build(profile=True)
+    import maximal_clique_enumeration_gb300 as mce
+    z = np.load(args.activity_child)
+    offs, adj, roots = z["offsets"], z["adj"], z["roots"]
+    n = len(offs) - 1
+    h = mce.Graph(torch.from_numpy(offs).cuda(), torch.from_numpy(adj).cuda(), n, profile=1,
+                  induced=args.induced, subtree_level=args.subtree_level)
+    r = torch.from_numpy(roots).cuda()
+    out = h.count_roots(r)
+    torch.cuda.synchronize()
+    h.count_roots(r, out=out)
+    h.check()
+    info = h.get_info()
+    prof = h.profile()
+    n_sms = torch.cuda.get_device_properties(0).multi_processor_count
+    acts = ["build", "pivot", "child", "partition", "donate", "idle"]
+    res = {"ms_search": info["ms_search"], "workers": info["workers"], "n_sms": n_sms}
+    for k in range(6):
+        p = prof[1 << k]
+        tot = sum(p[a] for a in acts)
+        if tot == 0:
+            continue
+        res[str(1 << k)] = {"cycles": {a: int(p[a]) for a in acts},
+                            "share": {a: p[a] / tot for a in acts},
+                            "roots": int(p["roots"]), "slowest_root_cycles": int(p["max_root"]),
+                            "sm_load": _load_stats(p["sm_busy"], n_sms)}
+    h.close()
+    print(json.dumps(res), flush=True)
+
+
+def imbalance_run(args):
+    """Per-SM load (max / average) with and without the worker list, per row-width class."""
+    import torch
+    from maximal_clique_enumeration_gb300 import build
+    os.environ["MCE_LIBRARY"] = build.build(profile=True)
+    import maximal_clique_enumeration_gb300 as mce
+    from maximal_clique_enumeration_gb300 import graphs as G
+    n_sms = torch.cuda.get_device_properties(0).multi_processor_count
+    out = {"kind": "imbalance", "n_sms": n_sms, "graphs": {}}
+    for name in ["planted50k", "rmat_s14"]:
+        g = G.config_graph(name, 1)
+        per = {}
+        for wl in (0, 1):
+            h = mce.Graph(torch.from_numpy(g.offsets).cuda(), torch.from_numpy(g.adj).cuda(),
+                          g.n, profile=1, worker_list=wl)
+            h.count_result()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            o = h.count()
+            e1.record()
+            torch.cuda.synchronize()
+            h.check()
+            info = h.get_info()
+            prof = h.profile()
+            per["worker_list" if wl else "static"] = {
+                "ms": e0.elapsed_time(e1), "cliques": int(mce.Graph.unpack(o)[0]),
+                "donations": info["donations"], "tree_nodes": info["tree_nodes"],
+                "sm_load_by_width": {str(1 << k): _load_stats(prof[1 << k]["sm_busy"], n_sms)
+                                     for k in range(6) if prof[1 << k]["sm_busy"].sum() > 0},
+                "sm_load_all": _load_stats(sum(prof[1 << k]["sm_busy"] for k in range(6)),
+                                           n_sms)}
+            h.close()
+        out["graphs"][name] = per
+    print(json.dumps(out), flush=True)
 
 
 # ---------------------------------------------------------------- GPU arm
@@ -214,13 +493,14 @@ def run_gb300(args, rank, world, local):
 
     torch.cuda.set_device(local)
     build.build()
+    hbm = hbm_peak()
     g = workload_graph(args)
     dev_offs = torch.from_numpy(g.offsets).cuda()
     dev_adj = torch.from_numpy(g.adj).cuda()
     h = mce.Graph(dev_offs, dev_adj, g.n, profile=1, induced=args.induced,
                   subtree_level=args.subtree_level)
-    rank_arr, _ = h.order_arrays()
-    roots, pc = light_roots(g, rank_arr.cpu().numpy(), args.max_p)
+    rank_arr = h.order_arrays()[0].cpu().numpy()
+    roots, pc = light_roots(g, rank_arr, args.max_p)
     if args.root_fraction < 1.0:
         rng = np.random.default_rng(args.seed + 3000)
         keep = max(1, int(len(roots) * args.root_fraction))
@@ -245,7 +525,7 @@ def run_gb300(args, rank, world, local):
           for _ in range(args.steps)]
     ms_cls = np.zeros(mce.NUM_WIDTHS)
     words_cls = np.zeros(mce.NUM_WIDTHS)
-    ms_order = 0.0
+    ms_order = ms_peel = 0.0
     launches = 0
     barrier(world)
     torch.cuda.synchronize()
@@ -261,6 +541,7 @@ def run_gb300(args, rank, world, local):
         ms_cls += np.asarray(info["ms_search"])
         words_cls += np.asarray(info["words"], dtype=np.float64)
         ms_order += info["ms_order"]
+        ms_peel += info["ms_peel"]
         launches += info["launches"]
     wall = time.perf_counter() - wall0
     torch.cuda.synchronize()
@@ -273,6 +554,7 @@ def run_gb300(args, rank, world, local):
     total_ms = max_over_ranks(sum(step_ms), world)
     ms_per_step = total_ms / args.steps
     value = world * res[0] * args.steps / (total_ms * 1e-3)
+    info = h.get_info()
 
     # roofline of the dominant kernel: the search launch with the largest device time
     dom = int(np.argmax(ms_cls))
@@ -302,25 +584,95 @@ def run_gb300(args, rank, world, local):
         "config": dict(workload_config(args, g, roots, pc, h.info["degeneracy"]),
                        induced={1: "full", 2: "partial"}[h.info["induced"]]),
         "result": {"cliques": res[0], "hash": f"{res[1]:#018x}", "max_size": len(res[2]) - 1},
-        "stage_ms": {"order": ms_order / args.steps,
+        "stage_ms": {"order": ms_order / args.steps, "peel": ms_peel / args.steps,
                      "search_by_width": {str(1 << i): float(ms_cls[i] / args.steps)
                                          for i in range(mce.NUM_WIDTHS) if ms_cls[i] > 0}},
         "roofline": roofline, "clocks": clocks, "gpu_launches": launches,
         "wall_s_timed": wall,
     }
 
+    # graph stages against HBM: peel, orientation, and (from the activity profile) the build
+    sb = stage_bytes(g, rank_arr, roots, info["peel_live"])
+    peel_ms = ms_peel / args.steps
+    stages = {"peel": _gbs(sb["peel"], peel_ms, hbm),
+              "orient": _gbs(sb["orient"], ms_order / args.steps - peel_ms, hbm),
+              "peel_live_vertices": info["peel_live"], "rounds": info["peel_rounds"],
+              "bytes_formulas": "see stage_bytes() in bench.py"}
+    if rank == 0 and world == 1 and not args.no_activity:
+        act = activity_profile(g, roots, args)
+        line["activity"] = act
+        # the build's device time: its SM cycles summed over warps, spread over the launch's
+        # warps, at the sampled clock
+        mhz = (clocks or {}).get("sm_mhz") or 2070.0
+        build_ms, build_bytes = 0.0, 0.0
+        for c in range(6):
+            a = act.get(str(1 << c)) if isinstance(act, dict) else None
+            if not a or not act["workers"][c]:
+                continue
+            build_ms += a["cycles"]["build"] / (mhz * 1e3) / act["workers"][c]
+            build_bytes += sb["build_by_width"][c]
+        if build_ms > 0:
+            stages["build"] = dict(_gbs(build_bytes, build_ms, hbm),
+                                   time_source="MCE_PROFILE activity cycles of the subtree "
+                                               "build, spread over each launch's warps")
+    line["graph_stages"] = stages
+
+    if args.heavy_fraction > 0 and args.scale == 20:
+        hv, n_heavy = heavy_roots(pc, args.heavy_fraction, args.seed + 5000)
+        hv_dev = torch.from_numpy(hv).cuda()
+        hout = h.new_output()
+        hms, hinfos = timed_steps(lambda: h.count_roots(hv_dev, out=hout), args.steps,
+                                  args.warmup, flush, stream, h.get_info)
+        h.check()
+        hres = mce.Graph.unpack(hout)
+        hdom, hcls, hwords = dominant_class(hinfos, args.steps)
+        hstep = float(np.mean(hms))
+        line["heavy"] = {
+            "roots": int(len(hv)), "roots_in_class": n_heavy,
+            "sample": f"seeded {args.heavy_fraction:.4g} of the roots with 128 <= |P| < 256",
+            "cliques": hres[0], "hash": f"{hres[1]:#018x}", "ms": hstep,
+            "value": hres[0] / (hstep * 1e-3), "unit": UNIT,
+            "search_by_width": {str(WIDTHS[i]): float(hcls[i]) for i in range(6) if hcls[i] > 0},
+            "search_roofline": {"kernel": f"search_kernel<W={WIDTHS[hdom]}>",
+                                "achieved_gword_s": hwords[hdom] / max(hcls[hdom], 1e-9) * 1e-6,
+                                "frac": hwords[hdom] / max(hcls[hdom], 1e-9) * 1e3
+                                / pr["words_per_s"]},
+        }
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            cores = len(os.sched_getaffinity(0))
+            # the oracle on every 16th root of the sample keeps it near 10-30 s
+            sub = hv[::16]
+            ores, dt = oracle_count_timed(g, sub, cores)
+            got = h.count_roots_result(sub)
+            line["heavy"]["cpu_baseline"] = cpu_block(
+                ores.count / dt, cores, f"oracle on every 16th root of the heavy sample "
+                f"({len(sub)} roots): {ores.count} cliques in {dt:.1f} s, including its input "
+                f"checks, peel and relabelling of the whole graph")
+            line["heavy"]["parity"] = ("ok" if got == ores.key()
+                                       else f"MISMATCH {got} {ores.key()}")
+
     if not args.no_e2e:
         line["e2e"] = e2e_leg(args, g, roots, world)
+    threads = len(os.sched_getaffinity(0))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        threads = len(os.sched_getaffinity(0))
-        sample, ores, dt = oracle_sample(g, roots, args.cpu_fraction, args.seed + 1000, threads)
-        got = h.count_roots_result(sample)
+        ores, dt = oracle_count_timed(g, roots, threads)
+        pre = oracle_preprocessing_s(g)
         line["cpu_baseline"] = cpu_block(
             ores.count / dt, threads,
-            f"oracle on {len(sample)} seeded roots ({args.cpu_fraction:.0%} of the workload "
-            f"roots): {ores.count} cliques in {dt:.1f} s, including its own input checks, "
-            f"peel and relabelling of the whole graph")
-        line["parity_on_cpu_sample"] = "ok" if got == ores.key() else f"MISMATCH {got} {ores.key()}"
+            f"oracle on the whole workload ({len(roots)} roots): {ores.count} cliques in "
+            f"{dt:.1f} s, including its own input checks, peel and relabelling of the whole "
+            f"graph (those alone: {pre:.1f} s)", preprocessing_s=pre, seconds=dt)
+        line["parity_on_cpu_sample"] = "ok" if res == ores.key() else \
+            f"MISMATCH {res} {ores.key()}"
+        line["parity_scope"] = "the whole workload"
+
+    names = [c for c in args.configs.split(",") if c]
+    if names:
+        line["configs"] = {}
+        for name in names:
+            line["configs"][name] = run_other_config(
+                name, args.seed, args, flush, pr["words_per_s"], threads,
+                rank == 0 and world == 1 and not args.no_cpu_baseline, hbm)
     h.close()
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -365,6 +717,9 @@ def e2e_leg(args, g, roots, world):
 # ---------------------------------------------------------------- reference arm (CPU oracle)
 
 def run_reference(args, rank, world):
+    """The oracle, as it stands, on the host cores: each timed step counts the whole workload
+    (every root with |P| < max_p, with the oracle's own input checks, peel and relabelling);
+    the untimed warm-up steps count a 1 % seeded sample."""
     if rank != 0:
         return
     import oracle
@@ -373,17 +728,19 @@ def run_reference(args, rank, world):
     _, _, orank, d = oracle.peel(g)
     roots, pc = light_roots(g, orank, args.max_p)
     threads = len(os.sched_getaffinity(0))
-    frac = min(args.cpu_fraction, 1.0) / 2
+    rng = np.random.default_rng(args.seed + 2000)
+    warm = np.sort(rng.choice(roots, size=max(1, len(roots) // 100), replace=False))
+    for _ in range(args.warmup):
+        oracle_count_timed(g, warm.astype(np.int32), threads)
     total_cl = 0
     total_s = 0.0
-    for k in range(args.warmup + args.steps):
-        _, res, dt = oracle_sample(g, roots, frac, args.seed + 2000 + k, threads)
-        if k >= args.warmup:
-            total_cl += res.count
-            total_s += dt
+    for _ in range(args.steps):
+        res, dt = oracle_count_timed(g, roots, threads)
+        total_cl += res.count
+        total_s += dt
     value = total_cl / total_s
-    desc = (f"oracle, each step {frac:.0%} of the workload roots (seeded), with its own input "
-            f"checks, peel and relabelling of the whole graph")
+    desc = ("oracle, each step the whole workload (all roots with |P| < max_p), with its own "
+            "input checks, peel and relabelling of the whole graph")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
@@ -397,6 +754,12 @@ def run_reference(args, rank, world):
 
 def main():
     args = parse_args()
+    if args.activity_child:
+        activity_child(args)
+        return
+    if args.imbalance:
+        imbalance_run(args)
+        return
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     rank, world, local = dist_init(args)

@@ -115,6 +115,9 @@ typedef struct mce_info {
     int32_t launches;                  /* kernels launched by the last order + count calls   */
     int32_t induced;                   /* induced subgraph in use: 1 full, 2 partial         */
     int32_t subtree_level;             /* 1: first-level subtrees, 2: second-level subtrees  */
+    float ms_peel;                     /* the peel's part of ms_order (profile = 1 only)     */
+    int64_t peel_live;                 /* vertices still in the graph, summed over the peel's
+                                          rounds (the live lists its rounds scan)            */
 } mce_info;
 
 /* Writes the default configuration into *cfg.  Returns MCE_ERR_INVALID_ARG if cfg is NULL. */
@@ -223,8 +226,11 @@ mce_status mce_get_order(mce_graph *g, void *stream, int32_t *d_rank, int32_t *d
  * ordering, as seen by its first CTA, in nanoseconds: out[48 + p] for rounds run by all CTAs and
  * out[56 + p] for rounds run by one CTA, phase p = 0 scan, 1 report exchange, 2 decide and
  * write, 3 edge removal, 4 end-of-round barrier, 5 number of rounds; out[54] is the largest
- * degree of a vertex removed by the first CTA.
- *   out  host uint64[8 * MCE_NUM_WIDTHS + 16].  Synchronises the device.
+ * degree of a vertex removed by the first CTA.  Then, per row-width class k, the load of every
+ * SM in the last search (Section 4.3 judges the worker list by per-block loads): at
+ * out[64 + k * 256 + s] the SM clock cycles that warps on SM s spent holding work (time in the
+ * kernel minus time waiting in the worker list), for s < 256.
+ *   out  host uint64[8 * MCE_NUM_WIDTHS + 16 + 256 * MCE_NUM_WIDTHS].  Synchronises the device.
  */
 mce_status mce_get_profile(mce_graph *g, uint64_t *out);
 

@@ -40,6 +40,7 @@ class MceError(RuntimeError):
 
 
 NUM_WIDTHS = 6
+PROF_SMS = 256
 
 
 class Config(ctypes.Structure):
@@ -59,7 +60,8 @@ class Info(ctypes.Structure):
                 ("roots", ctypes.c_int32 * NUM_WIDTHS), ("workers", ctypes.c_int32 * NUM_WIDTHS),
                 ("ms_search", ctypes.c_float * NUM_WIDTHS), ("ms_order", ctypes.c_float),
                 ("launches", ctypes.c_int32), ("induced", ctypes.c_int32),
-                ("subtree_level", ctypes.c_int32)]
+                ("subtree_level", ctypes.c_int32), ("ms_peel", ctypes.c_float),
+                ("peel_live", ctypes.c_int64)]
 
     def as_dict(self):
         out = {}
@@ -204,7 +206,7 @@ class Graph:
 
     def profile(self) -> dict:
         """Per row width: cycles per activity of the last search (MCE_PROFILE builds only)."""
-        out = np.zeros(8 * NUM_WIDTHS + 16, np.uint64)
+        out = np.zeros(8 * NUM_WIDTHS + 16 + PROF_SMS * NUM_WIDTHS, np.uint64)
         _check(library().mce_get_profile(self._h, out.ctypes.data_as(ctypes.c_void_p)),
                "mce_get_profile")
         res = {1 << k: dict(zip(PROFILE_ACTIVITIES, (int(x) for x in out[8 * k: 8 * k + 8])))
@@ -214,6 +216,9 @@ class Graph:
         res["peel"] = {"multi": dict(zip(phases, (int(x) for x in out[base: base + 6]))),
                        "single": dict(zip(phases, (int(x) for x in out[base + 8: base + 14]))),
                        "max_removed_degree": int(out[base + 6])}
+        sm = out[base + 16:].reshape(NUM_WIDTHS, PROF_SMS)
+        for k in range(NUM_WIDTHS):
+            res[1 << k]["sm_busy"] = sm[k].astype(np.int64)
         return res
 
     def order(self, stream=None):

@@ -27,10 +27,11 @@ def _nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libmce_gb300.so")
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB_PATH) or not os.path.exists(PROBE_PATH):
+def _stale(*outputs) -> bool:
+    outputs = outputs or (LIB_PATH, PROBE_PATH)
+    if not all(os.path.exists(o) for o in outputs):
         return True
-    t = min(os.path.getmtime(LIB_PATH), os.path.getmtime(PROBE_PATH))
+    t = min(os.path.getmtime(o) for o in outputs)
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "mce.h")]
     return any(os.path.getmtime(d) > t for d in deps)
 
@@ -45,6 +46,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=(), profile: b
     _build/profile/ instead; the normal library is left alone.
     """
     if profile:
+        if not force and not extra_flags and not _stale(PROFILE_LIB_PATH):
+            return PROFILE_LIB_PATH
         return _build_variant(os.path.dirname(PROFILE_LIB_PATH), ["-DMCE_PROFILE", *extra_flags],
                               verbose)
     if not force and not extra_flags and not _stale():
@@ -97,10 +100,12 @@ def _build_variant(out_dir: str, flags, verbose: bool) -> str:
     if errors:
         raise RuntimeError("nvcc failed:\n" + "\n".join(errors))
     out = os.path.join(out_dir, "libmce_gb300.so")
-    r = subprocess.run([nvcc, *ARCH, "-shared", "-cudart", "static", "-o", out, *objs],
+    tmp = out + f".tmp{os.getpid()}"
+    r = subprocess.run([nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs],
                        capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + r.stdout + r.stderr)
+    os.replace(tmp, out)
     return out
 
 

@@ -39,7 +39,7 @@ struct mce_graph {
     unsigned long long *roots_count = nullptr;  // [2 + hist_len], count of a root batch
     bool count_cache_valid = false;
     // profiling: events around the order and around each class launch
-    cudaEvent_t ev_order[2] = {nullptr, nullptr};
+    cudaEvent_t ev_order[3] = {nullptr, nullptr, nullptr};   // start, end, after the peel
     cudaEvent_t ev_grp[kNumGroups][2] = {};
     bool grp_timed[kNumGroups] = {};
     bool order_timed = false;
@@ -172,7 +172,7 @@ void free_all(mce_graph *h)
         cudaGetLastError();
     }
     h->allocs.clear();
-    for (int i = 0; i < 2; ++i)
+    for (int i = 0; i < 3; ++i)
         if (h->ev_order[i]) cudaEventDestroy(h->ev_order[i]);
     for (int k = 0; k < kNumGroups; ++k)
         for (int i = 0; i < 2; ++i)
@@ -186,6 +186,8 @@ mce_status reset_search(mce_graph *h, cudaStream_t s)
     MCE_TRY(cudaMemsetAsync(&c->tree_nodes, 0, 4 * sizeof(unsigned long long), s));
     MCE_TRY(cudaMemsetAsync(c->words, 0, sizeof(c->words), s));
     MCE_TRY(cudaMemsetAsync(c->prof, 0, sizeof(c->prof), s));
+    MCE_TRY(cudaMemsetAsync(h->g.prof_sm, 0, sizeof(unsigned long long) * kNumClasses * kProfSms,
+                            s));
     for (int k = 0; k < kNumGroups; ++k) h->grp_timed[k] = false;
     MCE_TRY(cudaMemsetAsync(h->hist_acc, 0, sizeof(unsigned long long) * h->hist_len, s));
     return MCE_OK;
@@ -370,8 +372,7 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
     MCE_ALLOC(h, g.blk_cm, (size_t)2 * h->peel_blocks);
     MCE_ALLOC(h, g.blk_rd, (size_t)h->peel_blocks);
     if (h->cfg.profile) {
-        MCE_TRY(cudaEventCreate(&h->ev_order[0]));
-        MCE_TRY(cudaEventCreate(&h->ev_order[1]));
+        for (int i = 0; i < 3; ++i) MCE_TRY(cudaEventCreate(&h->ev_order[i]));
         for (int k = 0; k < kNumGroups; ++k) {
             MCE_TRY(cudaEventCreate(&h->ev_grp[k][0]));
             MCE_TRY(cudaEventCreate(&h->ev_grp[k][1]));
@@ -457,6 +458,7 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
     MCE_ALLOC(h, h->flag, (size_t)h->n_workers);
     MCE_ALLOC(h, h->ring_seq, (size_t)h->n_workers);
     MCE_ALLOC(h, g.ubucket, (size_t)kNumBuckets);
+    MCE_ALLOC(h, g.prof_sm, (size_t)kNumClasses * kProfSms);
     MCE_ALLOC(h, h->hist_acc, (size_t)h->hist_len + 1);
     MCE_ALLOC(h, h->region_ids, (size_t)h->hist_len + 2);
     MCE_ALLOC(h, h->region_cl, (size_t)h->hist_len + 2);
@@ -503,7 +505,8 @@ static mce_status order_impl(mce_graph *h, cudaStream_t s)
     h->count_cache_valid = false;
     MCE_TRY(cudaMemsetAsync(h->g.ctrl->peel_prof, 0, sizeof(h->g.ctrl->peel_prof), s));
     if (h->cfg.profile) MCE_TRY(cudaEventRecord(h->ev_order[0], s));
-    MCE_TRY(launch_order(h->g, h->peel_blocks, h->cfg.spin_limit_ns, s));
+    MCE_TRY(launch_order(h->g, h->peel_blocks, h->cfg.spin_limit_ns, s,
+                         h->cfg.profile && h->n > 0 ? h->ev_order[2] : nullptr));
     if (h->cfg.profile) {
         MCE_TRY(cudaEventRecord(h->ev_order[1], s));
         h->order_timed = true;
@@ -733,8 +736,11 @@ mce_status mce_get_info(mce_graph *h, mce_info *info)
             info->ms_search[k] += ms;
         }
     }
-    if (h->order_timed)
+    if (h->order_timed && h->n > 0) {
         MCE_TRY(cudaEventElapsedTime(&info->ms_order, h->ev_order[0], h->ev_order[1]));
+        MCE_TRY(cudaEventElapsedTime(&info->ms_peel, h->ev_order[0], h->ev_order[2]));
+    }
+    info->peel_live = c.peel_live;
     info->launches = h->launches_order + h->launches_count;
     return MCE_OK;
 }
@@ -745,6 +751,9 @@ mce_status mce_get_profile(mce_graph *h, uint64_t *out)
     MCE_TRY(cudaDeviceSynchronize());
     MCE_TRY(cudaMemcpy(out, h->g.ctrl->prof, sizeof(h->g.ctrl->prof), cudaMemcpyDeviceToHost));
     MCE_TRY(cudaMemcpy(out + 8 * kNumClasses, h->g.ctrl->peel_prof, sizeof(h->g.ctrl->peel_prof),
+                       cudaMemcpyDeviceToHost));
+    MCE_TRY(cudaMemcpy(out + 8 * kNumClasses + 16, h->g.prof_sm,
+                       sizeof(unsigned long long) * kNumClasses * kProfSms,
                        cudaMemcpyDeviceToHost));
     return MCE_OK;
 }

@@ -19,12 +19,14 @@ constexpr int kNumGroups = 2 * kNumClasses;   // per width: big-workspace roots,
 constexpr long long kWsCapWords = 16384;     // workspace per warp of a "normal" launch (64 KiB)
 constexpr long long kBigBudgetWords = 256LL << 20;   // workspace of a "big" launch (1 GiB)
 constexpr int kScanBlock = 1024;         // elements per CTA of the exclusive scan
+constexpr int kProfSms = 256;            // MCE_PROFILE builds: per-SM load slots per class
 
 // Device-resident control block of a handle.
 struct DevCtrl {
     int status;                  // first device-side error (mce_status), 0 = none
     int degeneracy;              // peel output
     int rounds;                  // peel output
+    long long peel_live;         // peel output: live vertices summed over rounds
     int max_pcount;              // max |P| over first-level subtrees
     unsigned int bar_count;      // grid barrier arrivals (grows by the grid size per barrier)
     unsigned int bar_pad;
@@ -80,6 +82,7 @@ struct DevGraph {
     int *bucket;      // orient: schedule bucket histogram / cursors [kNumBuckets]
     int *ubucket;     // the same for a caller's root list [kNumBuckets]
     int *uroots;      // a caller's roots, grouped by row width, heaviest first
+    unsigned long long *prof_sm;   // MCE_PROFILE builds: busy warp cycles [kNumClasses][kProfSms]
     DevCtrl *ctrl;
 };
 
@@ -199,8 +202,9 @@ cudaError_t launch_ingest_sort_large(const DevGraph &g, int *adj_mut, int v, int
                                      cudaStream_t s);
 cudaError_t launch_ingest_validate(const DevGraph &g, const int *d_big_list, int n_big,
                                    int max_degree, unsigned long long *d_fb, cudaStream_t s);
+// ev_peel (may be null) is recorded on s between the peel and the orientation kernels.
 cudaError_t launch_order(const DevGraph &g, int peel_blocks, long long spin_limit_ns,
-                         cudaStream_t s);
+                         cudaStream_t s, cudaEvent_t ev_peel);
 cudaError_t launch_search(const SearchArgs &a, int blocks, int threads, size_t smem,
                           cudaStream_t s);
 cudaError_t launch_search_prep(const SearchArgs &a, cudaStream_t s);

@@ -149,6 +149,7 @@ __global__ void __launch_bounds__(kPeelThreads, 1) peel_kernel(DevGraph g, long 
     // adjacency entries of the remaining vertices, read from the offsets themselves (callers of
     // the allocation-free entry point pass no edge count)
     long long live_entries = n > 0 ? (long long)g.offs[n] - (long long)g.offs[0] : 0;
+    long long live_sum = 0;           // live vertices summed over rounds (CTA 0 keeps it)
     bool solo = false;
     int nb = gridDim.x, b = blockIdx.x;
     const int tile = nthr * kPeelItems;
@@ -366,6 +367,7 @@ __global__ void __launch_bounds__(kPeelThreads, 1) peel_kernel(DevGraph g, long 
 #ifdef MCE_PROFILE
         if (blockIdx.x == 0 && tid == 0) g.ctrl->peel_prof[5 + (solo ? 8 : 0)]++;
 #endif
+        live_sum += n_alive;
         pos += total;
         n_alive -= total;
         ++r;
@@ -376,6 +378,7 @@ __global__ void __launch_bounds__(kPeelThreads, 1) peel_kernel(DevGraph g, long 
     if (blockIdx.x == 0 && tid == 0) {
         g.ctrl->degeneracy = dmax;
         g.ctrl->rounds = r;
+        g.ctrl->peel_live = live_sum;
     }
 }
 
@@ -602,7 +605,7 @@ cudaError_t launch_unit_offsets(const DevGraph &g, const int *roots, int n_roots
 }
 
 cudaError_t launch_order(const DevGraph &g, int peel_blocks, long long spin_limit_ns,
-                         cudaStream_t s)
+                         cudaStream_t s, cudaEvent_t ev_peel)
 {
     if (g.n == 0) return cudaSuccess;
     // reset the fields the kernels accumulate into
@@ -620,6 +623,7 @@ cudaError_t launch_order(const DevGraph &g, int peel_blocks, long long spin_limi
     e = cudaLaunchCooperativeKernel((const void *)peel_kernel, dim3(peel_blocks),
                                     dim3(kPeelThreads), args, 0, s);
     if (e != cudaSuccess) return e;
+    if (ev_peel && (e = cudaEventRecord(ev_peel, s)) != cudaSuccess) return e;
     int blocks = (int)((g.n + kOrientThreads / 32 - 1) / (kOrientThreads / 32));
     if (blocks > 8192) blocks = 8192;
     orient_count_kernel<<<blocks, kOrientThreads, 0, s>>>(g);

@@ -1294,6 +1294,9 @@ __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(Search
                                            : (unsigned long long)end - begin;
     dev_int busy(a.g.ctrl->busy);
     Acc acc{};
+#ifdef MCE_PROFILE
+    const long long t_kernel = clock64();
+#endif
     // phase 1: first-level subtrees from the shared counter
     while (load_status(a.g.ctrl) == 0) {
         unsigned long long idx = 0;
@@ -1402,6 +1405,14 @@ __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(Search
             if (i == kProfMaxRoot) atomicMax(&a.g.ctrl->prof[a.cls][i], acc.prof[i]);
             else atomicAdd(&a.g.ctrl->prof[a.cls][i], acc.prof[i]);
         }
+        // this warp's load: its time in the kernel minus its time waiting in the worker list,
+        // added to the slot of the SM it ran on (Section 4.3 compares per-block loads)
+        unsigned smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        const unsigned long long span = (unsigned long long)(clock64() - t_kernel);
+        const unsigned long long idle = acc.prof[kProfIdle];
+        if (a.g.prof_sm && smid < (unsigned)kProfSms)
+            atomicAdd(&a.g.prof_sm[a.cls * kProfSms + smid], span > idle ? span - idle : 0ULL);
 #endif
     }
 }
