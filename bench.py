@@ -164,6 +164,39 @@ def heavy_roots(pc, fraction, seed):
     return np.sort(rng.choice(cand, size=k, replace=False)).astype(np.int32), int(cand.size)
 
 
+HEAVY_GOLDEN = os.path.join(ROOT, "tests", "golden", "rmat_s20_heavy_roots.txt")
+
+
+def graph_fingerprint(g) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    h.update(np.ascontiguousarray(g.offsets, np.int32).tobytes())
+    h.update(np.ascontiguousarray(g.adj, np.int32).tobytes())
+    return h.hexdigest()[:16]
+
+
+def heavy_golden(g):
+    """Roots of the stored heavy sample that the oracle finished, with its (count, hash, hist)
+    for each (written by tests/golden/make_rmat_s20_heavy.py from the oracle alone), or None
+    when the file is missing or was made from another graph."""
+    try:
+        lines = open(HEAVY_GOLDEN).read().splitlines()
+    except OSError:
+        return None
+    roots, keys, pcs = [], [], []
+    for line in lines:
+        f = line.split()
+        if not f or f[0].startswith("#"):
+            continue
+        if f[0] == "graph" and f[5] != graph_fingerprint(g):
+            return None
+        if f[0] == "root":
+            roots.append(int(f[1]))
+            pcs.append(int(f[2]))
+            keys.append((int(f[3]), int(f[4], 16), tuple(int(x) for x in f[6:])))
+    return np.asarray(roots, np.int32), keys, np.asarray(pcs)
+
+
 def workload_config(args, g, roots, pc, d):
     return {
         "workload": f"R-MAT scale {args.scale}, edge factor 16, (a,b,c,d)=(0.57,0.19,0.19,0.05), "
@@ -638,18 +671,32 @@ def run_gb300(args, rank, world, local):
                                 "frac": hwords[hdom] / max(hcls[hdom], 1e-9) * 1e3
                                 / pr["words_per_s"]},
         }
-        if rank == 0 and world == 1 and not args.no_cpu_baseline:
-            cores = len(os.sched_getaffinity(0))
-            # the oracle on every 16th root of the sample keeps it near 10-30 s
-            sub = hv[::16]
-            ores, dt = oracle_count_timed(g, sub, cores)
-            got = h.count_roots_result(sub)
-            line["heavy"]["cpu_baseline"] = cpu_block(
-                ores.count / dt, cores, f"oracle on every 16th root of the heavy sample "
-                f"({len(sub)} roots): {ores.count} cliques in {dt:.1f} s, including its input "
-                f"checks, peel and relabelling of the whole graph")
-            line["heavy"]["parity"] = ("ok" if got == ores.key()
-                                       else f"MISMATCH {got} {ores.key()}")
+        # the stored sample the oracle can finish (its per-root results): GPU parity root by
+        # root, and the oracle timed on the same roots
+        gold = heavy_golden(g)
+        if gold is not None and len(gold[0]):
+            groots, gkeys, gpc = gold
+            bad = [int(v) for v, key in zip(groots, gkeys)
+                   if h.count_roots_result(np.array([v], np.int32)) != key]
+            gdev = torch.from_numpy(groots).cuda()
+            gout = h.new_output()
+            gms, _ = timed_steps(lambda: h.count_roots(gdev, out=gout), args.steps,
+                                 args.warmup, flush, stream)
+            h.check()
+            gres = mce.Graph.unpack(gout)
+            gstep = float(np.mean(gms))
+            entry = {"roots": int(len(groots)), "p_range": [int(gpc.min()), int(gpc.max())],
+                     "cliques": gres[0], "ms": gstep, "value": gres[0] / (gstep * 1e-3),
+                     "parity_per_root": "ok" if not bad else f"MISMATCH at roots {bad[:8]}"}
+            if rank == 0 and world == 1 and not args.no_cpu_baseline:
+                cores = len(os.sched_getaffinity(0))
+                ores, dt = oracle_count_timed(g, groots, cores)
+                entry["cpu_baseline"] = cpu_block(
+                    ores.count / dt, cores, f"oracle on the same {len(groots)} roots: "
+                    f"{ores.count} cliques in {dt:.1f} s, including its input checks, peel and "
+                    f"relabelling of the whole graph")
+                entry["parity"] = "ok" if gres == ores.key() else f"MISMATCH {gres} {ores.key()}"
+            line["heavy"]["oracle_sample"] = entry
 
     if not args.no_e2e:
         line["e2e"] = e2e_leg(args, g, roots, world)

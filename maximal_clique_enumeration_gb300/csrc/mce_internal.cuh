@@ -27,6 +27,9 @@ struct DevCtrl {
     int degeneracy;              // peel output
     int rounds;                  // peel output
     long long peel_live;         // peel output: live vertices summed over rounds
+    // peel state handed from the grid-wide rounds to the cluster that runs the last ones
+    int ph_n_alive, ph_k, ph_r, ph_pos, ph_dmax, ph_alive_b;
+    long long ph_live;
     int max_pcount;              // max |P| over first-level subtrees
     unsigned int bar_count;      // grid barrier arrivals (grows by the grid size per barrier)
     unsigned int bar_pad;

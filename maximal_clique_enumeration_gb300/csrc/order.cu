@@ -8,11 +8,14 @@
 // its core number is the level at which it was removed.  Every vertex then has at most d
 // later neighbours, d being the degeneracy (largest level).
 //
-// One cooperative kernel runs all rounds: the remaining vertices stay in an id-ordered list
-// that is compacted stably every round, so each round's removals come out already in id
-// order and the order needs no sort.  Two grid-wide barriers separate the phases of a round;
-// once at most kPeelSoloVertices vertices remain, CTA 0 finishes alone with CTA barriers.
-// Every barrier wait is bounded by spin_limit_ns.
+// The remaining vertices stay in an id-ordered list that is compacted stably every round, so
+// each round's removals come out already in id order and the order needs no sort.  A
+// cooperative kernel over the whole GPU runs the rounds while many vertices remain, with two
+// grid-wide barriers per round.  Most rounds remove few vertices from a small remainder (the
+// dense cores), and there a round is dominated by its barriers: once the remainder fits one
+// thread-block cluster's registers (16 CTAs x 8192 vertices), a second kernel, launched as one
+// cluster, runs the rest with barriers in distributed shared memory (mbarriers that every
+// CTA of the cluster arrives on remotely).  Every barrier wait is bounded by spin_limit_ns.
 //
 // Then small kernels count every vertex's later neighbours |P| (Algorithm 3's P), count the
 // isolated vertices, bucket the first-level roots by |P|, heaviest first, and store the
@@ -131,7 +134,10 @@ constexpr long long kPeelSoloEntries = 1 << 20;   // and the single-CTA finish n
 //   remove -- the CTA subtracts one degree from every neighbour of its own removed vertices
 //             (degrees of vertices already removed are never read again).
 // Grid barriers: after the scan (reports) and after the removal (degrees, next live list).
-__global__ void __launch_bounds__(kPeelThreads, 1) peel_kernel(DevGraph g, long long limit_ns)
+// tail_at > 0: stop once at most tail_at vertices remain, and leave the state for the cluster
+// kernel below (peel_tail_kernel).
+__global__ void __launch_bounds__(kPeelThreads, 1) peel_kernel(DevGraph g, long long limit_ns,
+                                                               int tail_at)
 {
     __shared__ int sh[32];
     const int tid = threadIdx.x, nthr = blockDim.x;
@@ -167,6 +173,7 @@ __global__ void __launch_bounds__(kPeelThreads, 1) peel_kernel(DevGraph g, long 
             __syncthreads();
             live_entries -= s_removed;
         }
+        if (n_alive <= tail_at) break;            // the same in every CTA: the cluster goes on
         // one CTA finishes once few vertices and few edges remain (a dense core keeps the grid)
         if (!solo && n_alive <= kPeelSoloVertices && live_entries <= kPeelSoloEntries) {
             if (blockIdx.x != 0) return;
@@ -379,7 +386,301 @@ __global__ void __launch_bounds__(kPeelThreads, 1) peel_kernel(DevGraph g, long 
         g.ctrl->degeneracy = dmax;
         g.ctrl->rounds = r;
         g.ctrl->peel_live = live_sum;
+        g.ctrl->ph_n_alive = n_alive;
+        g.ctrl->ph_k = k;
+        g.ctrl->ph_r = r;
+        g.ctrl->ph_pos = pos;
+        g.ctrl->ph_dmax = dmax;
+        g.ctrl->ph_alive_b = alive == g.alive_b ? 1 : 0;
+        g.ctrl->ph_live = live_sum;
     }
+}
+
+// ---- the last rounds, in one thread-block cluster
+
+constexpr int kTailMaxCtas = 16;
+
+__device__ __forceinline__ unsigned cluster_rank()
+{
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ unsigned cluster_size()
+{
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ unsigned smem_u32(const void *p)
+{
+    return (unsigned)__cvta_generic_to_shared(p);
+}
+
+// The address of the same shared-memory variable in CTA `rank` of the cluster.
+__device__ __forceinline__ unsigned cluster_map(unsigned addr, unsigned rank)
+{
+    unsigned r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void st_cluster(unsigned addr, int v)
+{
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Hardware barrier of the whole cluster (every thread of every CTA takes part).  Used only
+// where every CTA gets unconditionally: at the start and at the very end of the kernel.
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release;\n\t"
+                 "barrier.cluster.wait.acquire;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_init(unsigned addr, unsigned count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(addr), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_remote(unsigned cluster_addr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
+                 ::"r"(cluster_addr) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(unsigned addr, unsigned parity)
+{
+    unsigned ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(addr), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// Barrier of the cluster's CTAs through two mbarriers per CTA, used alternately (episode e
+// uses bars[e & 1], whose phase parity is then (e >> 1) & 1): thread 0 of every CTA arrives
+// on the barrier of every CTA (release, cluster scope), then waits on its own (acquire), at
+// most limit_ns.  Alternating keeps an early arrival for the next episode from completing a
+// CTA's current one.  Returns false after a timeout (MCE_ERR_DEVICE_TIMEOUT recorded).
+__device__ bool tail_barrier(unsigned long long *bars, int &episode, unsigned nb,
+                             long long limit_ns, DevCtrl *ctrl, int *s_ok)
+{
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const unsigned laddr = smem_u32(bars + (episode & 1));
+        for (unsigned j = 0; j < nb; ++j) mbar_arrive_remote(cluster_map(laddr, j));
+        const unsigned parity = (unsigned)(episode >> 1) & 1u;
+        int ok = 1;
+        const unsigned long long t0 = globaltimer_ns();
+        unsigned polls = 0;
+        while (!mbar_try_wait(laddr, parity)) {
+            if ((++polls & 15u) == 0 && (long long)(globaltimer_ns() - t0) > limit_ns) {
+                set_status(ctrl, MCE_ERR_DEVICE_TIMEOUT);
+                ok = 0;
+                break;
+            }
+        }
+        *s_ok = ok;
+    }
+    ++episode;
+    __syncthreads();
+    return *s_ok != 0;
+}
+
+// The rounds after the handoff, in one cluster of nb <= kTailMaxCtas CTAs (one launch).  The
+// same round as peel_kernel's, with every CTA's report written into every CTA's shared memory
+// and the two barriers of a round taken in distributed shared memory.  The remainder is at
+// most nb * kPeelThreads * kPeelItems vertices, so every thread keeps its entries of the live
+// list in registers through the round.  Data written by other CTAs in this kernel (live lists,
+// degrees) is read past L1.
+__global__ void __launch_bounds__(kPeelThreads, 1) peel_tail_kernel(DevGraph g, long long limit_ns)
+{
+    __shared__ unsigned long long s_bar[2];
+    __shared__ int s_rep[kTailMaxCtas][4];     // report of CTA j (written by CTA j)
+    __shared__ int sh[32];
+    __shared__ int s_ok;
+    __shared__ int s_red[3][32];
+    __shared__ int s_glob[3];
+    __shared__ int s_front[kPeelThreads * kPeelItems];
+    __shared__ int s_big[kPeelBigQueue];
+    __shared__ int s_nbig;
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    const int lane = tid & 31, wib = tid >> 5, wpb = nthr >> 5;
+    const unsigned b = cluster_rank(), nb = cluster_size();
+    const bool solo = true;                   // profile slots of the last rounds
+    (void)solo;
+    DevCtrl *c = g.ctrl;
+    // read before the first cluster barrier, so that every CTA sees the same value
+    const bool run = load_status(c) == 0 && nb <= (unsigned)kTailMaxCtas;
+    if (tid == 0) {
+        mbar_init(smem_u32(&s_bar[0]), nb);
+        mbar_init(smem_u32(&s_bar[1]), nb);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    cluster_sync_all();                       // every CTA's barriers exist before any arrival
+    int n_alive = run ? c->ph_n_alive : 0;
+    int k = c->ph_k, r = c->ph_r, pos = c->ph_pos, dmax = c->ph_dmax;
+    long long live_sum = c->ph_live;
+    int *alive = c->ph_alive_b ? g.alive_b : g.alive_a;
+    int *alive_next = c->ph_alive_b ? g.alive_a : g.alive_b;
+    int episode = 0;
+    const int tile = nthr * kPeelItems;
+    if (n_alive > (int)nb * tile) {           // cannot happen: the handoff threshold fits
+        if (b == 0 && tid == 0) set_status(c, MCE_ERR_INTERNAL);
+        n_alive = 0;
+    }
+    while (n_alive > 0) {
+        PEEL_MARK(t_ph);
+        const int chunk = (n_alive + (int)nb - 1) / (int)nb;
+        const int lo = min((int)b * chunk, n_alive), hi = min(lo + chunk, n_alive);
+        int vid[kPeelItems], vdg[kPeelItems];
+        // -- scan (chunk <= tile: one pass, kept in registers)
+        int cnt_le = 0, mmin = INT_MAX, cnt_m = 0;
+#pragma unroll
+        for (int j = 0; j < kPeelItems; ++j) {
+            const int i = lo + tid * kPeelItems + j;
+            vid[j] = i < hi ? __ldcg(alive + i) : -1;
+        }
+#pragma unroll
+        for (int j = 0; j < kPeelItems; ++j) vdg[j] = vid[j] >= 0 ? __ldcg(g.deg + vid[j]) : INT_MAX;
+#pragma unroll
+        for (int j = 0; j < kPeelItems; ++j) {
+            const int d = vdg[j];
+            if (vid[j] < 0) continue;
+            if (d <= k) ++cnt_le;
+            else if (d < mmin) { mmin = d; cnt_m = 1; }
+            else if (d == mmin) ++cnt_m;
+        }
+        {
+            const int wle = __reduce_add_sync(0xffffffffu, cnt_le);
+            const int wmin = __reduce_min_sync(0xffffffffu, mmin);
+            const int wcm = __reduce_add_sync(0xffffffffu, mmin == wmin ? cnt_m : 0);
+            if (lane == 0) { s_red[0][wib] = wle; s_red[1][wib] = wmin; s_red[2][wib] = wcm; }
+            __syncthreads();
+            if (wib == 0) {
+                const int a0 = lane < wpb ? s_red[0][lane] : 0;
+                const int a1 = lane < wpb ? s_red[1][lane] : INT_MAX;
+                const int a2 = lane < wpb ? s_red[2][lane] : 0;
+                const int bm = __reduce_min_sync(0xffffffffu, a1);
+                const int t_le = __reduce_add_sync(0xffffffffu, a0);
+                const int t_cm = __reduce_add_sync(0xffffffffu, a1 == bm ? a2 : 0);
+                // this CTA's report, into slot b of every CTA of the cluster
+                if (lane < (int)nb) {
+                    const unsigned base = cluster_map(smem_u32(&s_rep[b][0]), (unsigned)lane);
+                    st_cluster(base, t_le);
+                    st_cluster(base + 4, bm);
+                    st_cluster(base + 8, t_cm);
+                }
+            }
+        }
+        PEEL_ADD(0, t_ph);
+        if (!tail_barrier(s_bar, episode, nb, limit_ns, c, &s_ok)) break;
+        PEEL_ADD(1, t_ph);
+        // -- decide (identically in every CTA, from the same reports)
+        if (wib == 0) {
+            const int cle = lane < (int)nb ? s_rep[lane][0] : 0;
+            const int cmn = lane < (int)nb ? s_rep[lane][1] : INT_MAX;
+            const int ccm = lane < (int)nb ? s_rep[lane][2] : 0;
+            int tle = __reduce_add_sync(0xffffffffu, cle);
+            int ple = __reduce_add_sync(0xffffffffu, lane < (int)b ? cle : 0);
+            int gm = __reduce_min_sync(0xffffffffu, cmn);
+            if (tle == 0) {
+                tle = __reduce_add_sync(0xffffffffu, cmn == gm ? ccm : 0);
+                ple = __reduce_add_sync(0xffffffffu, lane < (int)b && cmn == gm ? ccm : 0);
+            } else {
+                gm = k;
+            }
+            if (lane == 0) { s_glob[0] = tle; s_glob[1] = ple; s_glob[2] = gm; }
+        }
+        __syncthreads();
+        const int total = s_glob[0], prefix = s_glob[1];
+        k = s_glob[2];
+        dmax = k;
+        // -- write: this round's removals in id order, and the stably compacted survivors
+        const int my_first = pos + prefix;
+        int nf = 0, nv = 0;
+#pragma unroll
+        for (int j = 0; j < kPeelItems; ++j) {
+            nv += vid[j] >= 0;
+            nf += vid[j] >= 0 && vdg[j] <= k;
+        }
+        int tot;
+        const int ex = block_excl_scan_int((nv << 16) | nf, &tot, sh);   // both < 2^16
+        const int rf = ex & 0xffff, rv = ex >> 16;
+        int of = my_first + rf, os = lo - prefix + (rv - rf);
+#pragma unroll
+        for (int j = 0; j < kPeelItems; ++j) {
+            const int v = vid[j];
+            if (v < 0) continue;
+            if (vdg[j] <= k) {
+                g.order[of] = v;
+                g.rank[v] = of;
+                g.round_of[v] = r;
+                g.core[v] = k;
+                s_front[of - my_first] = v;
+                ++of;
+            } else {
+                alive_next[os++] = v;
+            }
+        }
+        const int n_front = tot & 0xffff;
+        if (tid == 0) s_nbig = 0;
+        __syncthreads();
+        PEEL_ADD(2, t_ph);
+        // -- remove this CTA's vertices (one warp per vertex; wide ones by the whole CTA)
+        for (int e = wib; e < n_front; e += wpb) {
+            const int v = s_front[e];
+            const int elo = __ldg(g.offs + v), ehi = __ldg(g.offs + v + 1);
+            if (ehi - elo >= kPeelBigDegree) {
+                int slot = 0;
+                if (lane == 0) slot = atomicAdd(&s_nbig, 1);
+                slot = __shfl_sync(0xffffffffu, slot, 0);
+                if (slot < kPeelBigQueue) {
+                    if (lane == 0) s_big[slot] = v;
+                    continue;
+                }
+            }
+            for (int j = elo + lane; j < ehi; j += 32) atomicSub(&g.deg[__ldg(g.adj + j)], 1);
+#ifdef MCE_PROFILE
+            if (lane == 0 && b == 0)
+                atomicMax(&g.ctrl->peel_prof[6], (unsigned long long)(ehi - elo));
+#endif
+        }
+        __syncthreads();
+        const int nbig = min(s_nbig, kPeelBigQueue);
+        for (int i = 0; i < nbig; ++i) {
+            const int v = s_big[i];
+            const int elo = __ldg(g.offs + v), ehi = __ldg(g.offs + v + 1);
+            for (int j = elo + tid; j < ehi; j += nthr) atomicSub(&g.deg[__ldg(g.adj + j)], 1);
+#ifdef MCE_PROFILE
+            if (tid == 0 && b == 0)
+                atomicMax(&g.ctrl->peel_prof[6], (unsigned long long)(ehi - elo));
+#endif
+        }
+        PEEL_ADD(3, t_ph);
+        if (!tail_barrier(s_bar, episode, nb, limit_ns, c, &s_ok)) break;
+        PEEL_ADD(4, t_ph);
+#ifdef MCE_PROFILE
+        if (b == 0 && tid == 0) g.ctrl->peel_prof[5 + 8]++;
+#endif
+        live_sum += n_alive;
+        pos += total;
+        n_alive -= total;
+        ++r;
+        int *t = alive;
+        alive = alive_next;
+        alive_next = t;
+    }
+    if (run && b == 0 && tid == 0 && load_status(c) == 0) {
+        c->degeneracy = dmax;
+        c->rounds = r;
+        c->peel_live = live_sum;
+    }
+    cluster_sync_all();   // no CTA leaves while another may still address its shared memory
 }
 
 constexpr int kOrientThreads = 256;
@@ -604,6 +905,71 @@ cudaError_t launch_unit_offsets(const DevGraph &g, const int *roots, int n_roots
     return cudaGetLastError();
 }
 
+// CTAs of the peel's tail cluster on the current device: 16 where a 16-CTA cluster of this
+// kernel fits, else 8, else 0 (then the grid-wide kernel runs every round).  Cached per device.
+int tail_cluster_ctas()
+{
+    constexpr int kMaxDev = 64;
+    static int cached[kMaxDev] = {};            // 0 = unknown, else ctas + 1
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) {
+        cudaGetLastError();
+        return 0;
+    }
+    if (cached[dev]) return cached[dev] - 1;
+    int best = 0;
+    if (cudaFuncSetAttribute((const void *)peel_tail_kernel,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+        cudaGetLastError();
+    for (int ctas = kTailMaxCtas; ctas >= 8 && !best; ctas /= 2) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = ctas;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(ctas);
+        cfg.blockDim = dim3(kPeelThreads);
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, (const void *)peel_tail_kernel, &cfg) ==
+                cudaSuccess && clusters >= 1)
+            best = ctas;
+        else
+            cudaGetLastError();
+    }
+    cached[dev] = best + 1;
+    return best;
+}
+
+// The whole peel: the grid-wide kernel, then (if the device runs the tail cluster) the cluster
+// kernel for the rounds after the handoff.
+cudaError_t launch_peel(const DevGraph &g, int peel_blocks, long long spin_limit_ns,
+                        cudaStream_t s)
+{
+    const int ctas = tail_cluster_ctas();
+    DevGraph gg = g;
+    long long lim = spin_limit_ns;
+    int tail_at = ctas * kPeelThreads * kPeelItems;
+    void *args[] = {&gg, &lim, &tail_at};
+    cudaError_t e = cudaLaunchCooperativeKernel((const void *)peel_kernel, dim3(peel_blocks),
+                                                dim3(kPeelThreads), args, 0, s);
+    if (e != cudaSuccess || ctas == 0) return e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = ctas;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(ctas);
+    cfg.blockDim = dim3(kPeelThreads);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, peel_tail_kernel, gg, lim);
+}
+
 cudaError_t launch_order(const DevGraph &g, int peel_blocks, long long spin_limit_ns,
                          cudaStream_t s, cudaEvent_t ev_peel)
 {
@@ -617,11 +983,7 @@ cudaError_t launch_order(const DevGraph &g, int peel_blocks, long long spin_limi
     if (e == cudaSuccess) e = cudaMemsetAsync(&g.ctrl->iso_hash, 0, sizeof(unsigned long long), s);
     if (e == cudaSuccess) e = cudaMemsetAsync(g.bucket, 0, sizeof(int) * kNumBuckets, s);
     if (e != cudaSuccess) return e;
-    DevGraph gg = g;
-    long long lim = spin_limit_ns;
-    void *args[] = {&gg, &lim};
-    e = cudaLaunchCooperativeKernel((const void *)peel_kernel, dim3(peel_blocks),
-                                    dim3(kPeelThreads), args, 0, s);
+    e = launch_peel(g, peel_blocks, spin_limit_ns, s);
     if (e != cudaSuccess) return e;
     if (ev_peel && (e = cudaEventRecord(ev_peel, s)) != cudaSuccess) return e;
     int blocks = (int)((g.n + kOrientThreads / 32 - 1) / (kOrientThreads / 32));
@@ -727,14 +1089,9 @@ extern "C" mce_status mce_order_noalloc(const int32_t *d_offsets, const int32_t 
     g.order = g.alive_b + kNoAllocMaxN;
     noalloc_prep_kernel<<<1, 1, 0, s>>>();
     if (cudaGetLastError() != cudaSuccess) return MCE_ERR_CUDA;
-    if (n > 0) {
-        long long lim = 20LL * 1000 * 1000 * 1000;
-        void *args[] = {&g, &lim};
-        if (cudaLaunchCooperativeKernel((const void *)peel_kernel, dim3(blocks),
-                                        dim3(kPeelThreads), args, 0, s) != cudaSuccess) {
-            cudaGetLastError();
-            return MCE_ERR_CUDA;
-        }
+    if (n > 0 && launch_peel(g, blocks, 20LL * 1000 * 1000 * 1000, s) != cudaSuccess) {
+        cudaGetLastError();
+        return MCE_ERR_CUDA;
     }
     noalloc_result_kernel<<<1, 1, 0, s>>>(d_result);
     return cudaGetLastError() == cudaSuccess ? MCE_OK : MCE_ERR_CUDA;

@@ -130,5 +130,50 @@ def load_peel_golden(name: str):
     return n, edges, peel, info
 
 
+def load_root_golden(name: str):
+    """Per-root oracle results written by a committed script under tests/golden/:
+    (graph fields, [(root, |P|, (count, hash, hist))], skipped roots)."""
+    path = os.path.join(HERE, "golden", name)
+    graph, roots, skipped = None, [], []
+    with open(path) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            key, *vals = line.split()
+            if key == "graph":
+                graph = {"name": vals[0], "seed": int(vals[1]), "n": int(vals[2]),
+                         "m": int(vals[3]), "fingerprint": vals[4]}
+            elif key == "root":
+                hist = tuple(int(x) for x in vals[5:])
+                roots.append((int(vals[0]), int(vals[1]),
+                              (int(vals[2]), int(vals[3], 16), hist)))
+            elif key == "skipped":
+                skipped.append((int(vals[0]), int(vals[1])))
+    return graph, roots, skipped
+
+
+def graph_fingerprint(g) -> str:
+    """First 16 hex digits of the SHA-256 of a graph's int32 offsets and adjacency."""
+    import hashlib
+    h = hashlib.sha256()
+    h.update(np.ascontiguousarray(g.offsets, np.int32).tobytes())
+    h.update(np.ascontiguousarray(g.adj, np.int32).tobytes())
+    return h.hexdigest()[:16]
+
+
+def add_keys(keys):
+    """Sum of (count, hash, hist) summaries over disjoint sets of cliques."""
+    count, h, hist = 0, 0, []
+    for c, hh, hs in keys:
+        count += c
+        h = (h + hh) & M64
+        hist = [x + y for x, y in zip(hist + [0] * (len(hs) - len(hist)),
+                                      list(hs) + [0] * (len(hist) - len(hs)))]
+    while hist and hist[-1] == 0:
+        hist.pop()
+    return count, h, tuple(hist)
+
+
 def csr_arrays(g):
     return np.asarray(g.offsets, np.int32), np.asarray(g.adj, np.int32)
