@@ -223,6 +223,7 @@ struct Acc {
 #endif
 enum { kProfBuild = 0, kProfPivot, kProfChild, kProfPartition, kProfDonate, kProfIdle,
        kProfMaxRoot, kProfRoots };
+constexpr int kProfSmall = kProfPivot;   // small subtrees solved whole are part of the pivot work
 
 struct RootCtx {
     unsigned *rowsP, *rowsX;
@@ -478,6 +479,185 @@ __device__ int xx_partition(const DevGraph &g, const RootCtx &r, int lpX, int c,
     return kept;
 }
 
+// ------------------------------------------------------------------ small subtrees
+//
+// Most nodes of a search tree sit near its leaves: on R-MAT, four in five internal nodes have
+// |P| <= 8.  Below a node (R, P, X) the search reports exactly the cliques R u C with C a
+// nonempty subset of P that is a clique, that no other vertex of P extends, and that no vertex
+// of X extends (the invariant of Algorithm 2: every vertex adjacent to all of R is in R, P or
+// X).  Which pivots the search would pick below the node changes only the path to these
+// cliques, not the set.  So for |P| = k <= kSmallP the warp decides all 2^k subsets at once
+// instead of walking the subtree:
+//   * P's members p_0 .. p_{k-1} (ascending) renumber the node's columns; N_i is the closed
+//     neighbourhood of p_i inside P, as a k-bit mask;
+//   * C is a maximal clique of G[P] iff, for every i < k, C is a subset of N_i exactly when i is
+//     in C;
+//   * C is extended by a vertex of X iff some X vertex's k-bit mask of neighbours in P contains
+//     C: the masks of X_P and X_X are collected as a 256-bit set and closed under subsets;
+//   * the 256 subsets are bit-sliced over lanes 0-7 (lane l holds subsets 32 l .. 32 l + 31), so
+//     each test is a handful of word operations.
+// Count mode only (enumeration walks the subtree, so that every clique is written as before).
+constexpr int kSmallP = 8;
+
+// kSubsets5[m]: bit t set iff the 5-bit value t is a subset of the 5-bit value m.
+struct Subsets5 {
+    unsigned v[32];
+    constexpr Subsets5() : v()
+    {
+        for (int m = 0; m < 32; ++m) {
+            unsigned w = 0;
+            for (int t = 0; t < 32; ++t)
+                if ((t & ~m) == 0) w |= 1u << t;
+            v[m] = w;
+        }
+    }
+};
+__constant__ Subsets5 kSubsets5 = Subsets5();
+
+// Subsets C (of 8 bits) that lane l's word holds, C = 32 l + t: the bits t with C a subset of m.
+__device__ __forceinline__ unsigned subsets_of(unsigned m, int lane)
+{
+    return kSubsets5.v[m & 31u] & ((((unsigned)lane & ~(m >> 5)) & 7u) ? 0u : 0xffffffffu);
+}
+
+// The same word's subsets that contain element i.
+__device__ __forceinline__ unsigned subsets_with(int i, int lane)
+{
+    constexpr unsigned kZ[5] = {0xAAAAAAAAu, 0xCCCCCCCCu, 0xF0F0F0F0u, 0xFF00FF00u, 0xFFFF0000u};
+    return i < 5 ? kZ[i] : (((unsigned)lane >> (i - 5)) & 1u ? 0xffffffffu : 0u);
+}
+
+// The bits of v at the positions of the set bits of m, packed in ascending order (m is the same
+// in every lane, so the loop is uniform).
+template <int W>
+__device__ __forceinline__ unsigned gather_bits(const Ck<W> &v, const Ck<W> &m)
+{
+    unsigned out = 0;
+    int j = 0;
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+        unsigned pm = m.w[w];
+        const unsigned vw = v.w[w];
+        while (pm) {
+            const int b = __ffs(pm) - 1;
+            out |= ((vw >> b) & 1u) << j;
+            ++j;
+            pm &= pm - 1u;
+        }
+    }
+    return out;
+}
+
+// Reports every maximal clique below the node (R, P, X_P u X_X) at level L, |P| = k <= kSmallP
+// (rows of whole words per lane, W <= 4).  scratch: 24 words of the warp's shared memory.
+template <int W>
+__device__ void solve_small(const SearchArgs &a, const RootCtx &r, const Ck<W> &P,
+                            const Ck<W> &XP, int lpX, unsigned long long S, int L, int k,
+                            Acc &acc, unsigned long long *s_hist, unsigned *scratch, int lane)
+{
+    unsigned *T = scratch;                                    // 256-bit set of X masks
+    unsigned long long *keys = reinterpret_cast<unsigned long long *>(scratch + 8);
+    // lane j < k: the column of p_j
+    int my_p = 0;
+    {
+        int j = 0;
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+            unsigned pm = P.w[w];
+            while (pm) {
+                const int b = __ffs(pm) - 1;
+                if (lane == j) my_p = w * 32 + b;
+                ++j;
+                pm &= pm - 1u;
+            }
+        }
+    }
+    if (lane < 8) T[lane] = 0u;
+    unsigned adj = 0;                                         // lane i < k: N(p_i) n P, packed
+    if (lane < k) {
+        adj = gather_bits<W>(ck_load<W>(r.rowsP + (long long)my_p * W), P);
+        keys[lane] = r.pkey[my_p];
+    }
+    // the X vertices' masks: members of X_P (P rows), then the live X_X rows
+    const int nxp = list_bits<W>(XP, r.plist, lane);          // ends with __syncwarp
+    const int nx = nxp + lpX;
+    for (int base = 0; base < nx; base += 32) {
+        const int t = base + lane;
+        unsigned m = 0;
+        if (t < nxp) {
+            m = gather_bits<W>(ck_load<W>(r.rowsP + (long long)r.plist[t] * W), P);
+        } else if (t < nx) {
+            const int x = r.xx[t - nxp];
+            if constexpr (kIP) {
+                // no X rows: one search of the graph per member of P
+                const int xid = r.xids[x];
+                int j = 0;
+#pragma unroll
+                for (int w = 0; w < W; ++w) {
+                    unsigned pm = P.w[w];
+                    while (pm) {
+                        const int b = __ffs(pm) - 1;
+                        m |= (x_adjacent(a.g, xid, r.pids[w * 32 + b]) ? 1u : 0u) << j;
+                        ++j;
+                        pm &= pm - 1u;
+                    }
+                }
+            } else {
+                m = gather_bits<W>(ck_load<W>(r.rowsX + (long long)x * W), P);
+            }
+        }
+        if (m) atomicOr(&T[m >> 5], 1u << (m & 31u));
+    }
+    __syncwarp();
+    // subsets covered by some X mask: closure of T under subsets (lanes 0-7 hold 32 subsets
+    // each; bits 0-4 of a subset inside the word, bits 5-7 in the lane number)
+    unsigned D = lane < 8 ? T[lane] : 0u;
+    D |= (D >> 1) & 0x55555555u;
+    D |= (D >> 2) & 0x33333333u;
+    D |= (D >> 4) & 0x0F0F0F0Fu;
+    D |= (D >> 8) & 0x00FF00FFu;
+    D |= (D >> 16) & 0x0000FFFFu;
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+        const unsigned up = __shfl_xor_sync(kFull, D, o);
+        if (!(lane & o)) D |= up;
+    }
+    // maximal cliques of G[P]: subsets of {0..k-1} with [C subset of N_i] == [i in C] for all i
+    unsigned V = subsets_of((1u << k) - 1u, lane);
+    for (int i = 0; i < k; ++i) {
+        const unsigned ni = __shfl_sync(kFull, adj, i) | (1u << i);
+        V &= ~(subsets_of(ni, lane) ^ subsets_with(i, lane));
+    }
+    V = lane < 8 ? V & ~D : 0u;
+    if (lane == 0) acc.words += (unsigned long long)(k + nx) * W + 8ULL * (unsigned)k;
+    const int total = __reduce_add_sync(kFull, __popc(V));
+    if (total == 0) return;
+    const int rsize = r.rsize + L;
+    unsigned long long hs = 0;
+    for (unsigned v = V; v; v &= v - 1u) {
+        const unsigned C = (unsigned)lane * 32u + (unsigned)(__ffs(v) - 1);
+        unsigned long long sum = S;
+        int size = rsize;
+        for (unsigned cm = C; cm; cm &= cm - 1u) {
+            sum += keys[__ffs(cm) - 1];
+            ++size;
+        }
+        if (size >= a.out.hist_len) {                         // cannot happen: size <= d + 1
+            set_status(a.g.ctrl, MCE_ERR_INTERNAL);
+            continue;
+        }
+        hs += mix64(sum);
+        atomicAdd(&s_hist[size], 1ULL);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) hs += __shfl_xor_sync(kFull, hs, o);
+    if (lane == 0) {
+        acc.count += (unsigned)total;
+        acc.hash += hs;
+        acc.nodes += (unsigned)total;
+    }
+}
+
 // ------------------------------------------------------------------ worker list (Section 3.3)
 //
 // Idle warps put their id in a bounded multi-producer multi-consumer ring (one slot per warp,
@@ -597,7 +777,7 @@ __device__ void write_branch(const RootCtx &r, unsigned *dst, int L, int c,
 template <int W>
 __device__ void dfs(const SearchArgs &a, const RootCtx &r, Ck<Geo<W>::CH> P, Ck<Geo<W>::CH> XP,
                     int lpX, unsigned long long S, Acc &acc, unsigned long long *s_hist,
-                    int lane)
+                    unsigned *scratch, int lane)
 {
     constexpr int CH = Geo<W>::CH, G = Geo<W>::G;
     const int q = lane % G;
@@ -613,6 +793,16 @@ __device__ void dfs(const SearchArgs &a, const RootCtx &r, Ck<Geo<W>::CH> P, Ck<
             acc.nodes++;
             PROF_START(t_piv);
             const int npop = subwarp_sum<G>(ck_popc<CH>(P));
+            if constexpr (G == 1) {
+                if (npop <= kSmallP && a.out.ids == nullptr) {
+                    // the whole subtree at once; no stack entry, so the search backs up next
+                    solve_small<W>(a, r, P, XP, lpX, S, L, npop, acc, s_hist, scratch, lane);
+                    PROF_ADD(acc, kProfSmall, t_piv);
+                    C = ck_zero<CH>();
+                    cursor = -1;
+                    goto next_candidate;
+                }
+            }
             const int piv = choose_pivot<W>(r, P, ck_or<CH>(P, XP), npop, lpX, acc, lane);
             PROF_ADD(acc, kProfPivot, t_piv);
             if (piv < 0) {
@@ -639,6 +829,7 @@ __device__ void dfs(const SearchArgs &a, const RootCtx &r, Ck<Geo<W>::CH> P, Ck<
             }
             __syncwarp();
         }
+    next_candidate:
         const int c = lowest_above<W>(C, cursor, q);
         if (c == INT_MAX) {                       // level exhausted: back up
             if (L == 0) return;
@@ -1074,7 +1265,7 @@ __device__ void build_and_search(const SearchArgs &a, RootCtx r, const WarpSmem 
     __syncwarp();
     PROF_ADD(acc, kProfBuild, t_build);
     const int q = lane % G;
-    dfs<W>(a, r, bits_prefix<W>(np, q), ck_zero<CH>(), nxx, S, acc, s_hist, lane);
+    dfs<W>(a, r, bits_prefix<W>(np, q), ck_zero<CH>(), nxx, S, acc, s_hist, reinterpret_cast<unsigned *>(sm.cur_start), lane);
 }
 
 // The split of a wide root's N(v) into P (later) and X (earlier), in id order, with kBatch rank
@@ -1205,7 +1396,7 @@ __device__ void search_edge(const SearchArgs &a, unsigned *ws, const WarpSmem &s
 
 // Searches a branch that another warp wrote into this warp's workspace.
 template <int W>
-__device__ void search_inbox(const SearchArgs &a, unsigned *ws, Acc &acc,
+__device__ void search_inbox(const SearchArgs &a, unsigned *ws, const WarpSmem &sm, Acc &acc,
                              unsigned long long *s_hist, int lane)
 {
     constexpr int CH = Geo<W>::CH, G = Geo<W>::G;
@@ -1230,7 +1421,7 @@ __device__ void search_inbox(const SearchArgs &a, unsigned *ws, Acc &acc,
     const unsigned long long S = *reinterpret_cast<const unsigned long long *>(ws + kHdrS);
     const Ck<CH> P = ck_load<CH>(ws + kHdrP + q * CH);
     const Ck<CH> XP = ck_load<CH>(ws + kHdrXP + q * CH);
-    dfs<W>(a, r, P, XP, k, S, acc, s_hist, lane);
+    dfs<W>(a, r, P, XP, k, S, acc, s_hist, reinterpret_cast<unsigned *>(sm.cur_start), lane);
 }
 
 // The last i in [lo, hi) with a[i] <= t, for a non-decreasing a with a[lo] <= t: 32 probes
@@ -1387,7 +1578,7 @@ __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(Search
         if (state != 1) break;
         __syncwarp();
         cuda::atomic_thread_fence(cuda::memory_order_acquire, cuda::thread_scope_device);
-        search_inbox<W>(a, ws, acc, s_hist, lane);
+        search_inbox<W>(a, ws, sm, acc, s_hist, lane);
         __syncwarp();
         if (lane == 0) busy.fetch_sub(1, cuda::memory_order_acq_rel);
     }
