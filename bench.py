@@ -16,7 +16,8 @@ Beside the headline the same JSON line carries:
                 (order + count) with the oracle timed beside it;
   graph_stages  achieved GB/s of the peel, the orientation and the subtree build against the
                 measured HBM bandwidth, from their algorithmic bytes;
-  heavy         a seeded sample of the R-MAT roots with 128 <= |P| < 256 (8-word rows);
+  heavy         the R-MAT roots with 128 <= |P| < 512 of a stored seeded sample, with
+                parity root by root against the oracle's stored results;
   activity      per-activity split of the search's warp time (MCE_PROFILE build, in a child
                 process), which also times the subtree build.
 
@@ -64,6 +65,14 @@ def kernel_sources_hash() -> str:
     return h.hexdigest()[:16]
 
 
+_T0 = time.perf_counter()
+
+
+def progress(msg: str):
+    """One line on stderr per bench section (so that a cut-off run shows where it was)."""
+    print(f"[bench {time.perf_counter() - _T0:7.1f}s] {msg}", file=sys.stderr, flush=True)
+
+
 def hbm_peak():
     """(GB/s, source) of the HBM roofline: the measured copy bandwidth, else fallback."""
     try:
@@ -89,8 +98,8 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--configs", default=",".join(OTHER_CONFIGS),
                    help="other workloads timed beside the headline ('' for none)")
-    p.add_argument("--heavy-fraction", type=float, default=1 / 16,
-                   help="seeded share of the roots with 128 <= |P| < 256 timed as 'heavy' (0: off)")
+    p.add_argument("--no-heavy", action="store_true",
+                   help="skip the heavy-root tier (stored sample of roots with |P| >= 128)")
     p.add_argument("--no-activity", action="store_true",
                    help="skip the activity profile (MCE_PROFILE build, child process)")
     p.add_argument("--induced", type=int, default=0, choices=[0, 1, 2],
@@ -152,16 +161,6 @@ def light_roots(g, rank, max_p):
     """Roots v with |P(v)| < max_p, where P(v) = neighbours later in the order `rank`."""
     pc = later_counts(g, rank)
     return np.nonzero(pc < max_p)[0].astype(np.int32), pc
-
-
-def heavy_roots(pc, fraction, seed):
-    """A seeded share of the roots with 128 <= |P| < 256 (the 8-word row class)."""
-    cand = np.nonzero((pc >= 128) & (pc < 256))[0]
-    if fraction <= 0 or cand.size == 0:
-        return np.zeros(0, np.int32), int(cand.size)
-    rng = np.random.default_rng(seed)
-    k = max(1, int(round(cand.size * fraction)))
-    return np.sort(rng.choice(cand, size=k, replace=False)).astype(np.int32), int(cand.size)
 
 
 HEAVY_GOLDEN = os.path.join(ROOT, "tests", "golden", "rmat_s20_heavy_roots.txt")
@@ -494,6 +493,7 @@ def imbalance_run(args):
         g = G.config_graph(name, 1)
         per = {}
         for wl in (0, 1):
+            progress(f"imbalance {name} worker_list={wl}")
             h = mce.Graph(torch.from_numpy(g.offsets).cuda(), torch.from_numpy(g.adj).cuda(),
                           g.n, profile=1, worker_list=wl)
             h.count_result()
@@ -528,6 +528,7 @@ def run_gb300(args, rank, world, local):
     build.build()
     hbm = hbm_peak()
     g = workload_graph(args)
+    progress(f"graph n={g.n} m={g.m}")
     dev_offs = torch.from_numpy(g.offsets).cuda()
     dev_adj = torch.from_numpy(g.adj).cuda()
     h = mce.Graph(dev_offs, dev_adj, g.n, profile=1, induced=args.induced,
@@ -553,6 +554,7 @@ def run_gb300(args, rank, world, local):
     h.check()
     ref = mce.Graph.unpack(out)
 
+    progress("warm-up done")
     sampler = ClockSampler()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
@@ -589,6 +591,7 @@ def run_gb300(args, rank, world, local):
     value = world * res[0] * args.steps / (total_ms * 1e-3)
     info = h.get_info()
 
+    progress(f"timed steps done: {ms_per_step:.2f} ms/step")
     # roofline of the dominant kernel: the search launch with the largest device time
     dom = int(np.argmax(ms_cls))
     rate = 0.0
@@ -632,6 +635,7 @@ def run_gb300(args, rank, world, local):
               "peel_live_vertices": info["peel_live"], "rounds": info["peel_rounds"],
               "bytes_formulas": "see stage_bytes() in bench.py"}
     if rank == 0 and world == 1 and not args.no_activity:
+        progress("activity profile")
         act = activity_profile(g, roots, args)
         line["activity"] = act
         # the build's device time: its SM cycles summed over warps, spread over the launch's
@@ -650,61 +654,62 @@ def run_gb300(args, rank, world, local):
                                                "build, spread over each launch's warps")
     line["graph_stages"] = stages
 
-    if args.heavy_fraction > 0 and args.scale == 20:
-        hv, n_heavy = heavy_roots(pc, args.heavy_fraction, args.seed + 5000)
-        hv_dev = torch.from_numpy(hv).cuda()
-        hout = h.new_output()
-        hms, hinfos = timed_steps(lambda: h.count_roots(hv_dev, out=hout), args.steps,
-                                  args.warmup, flush, stream, h.get_info)
-        h.check()
-        hres = mce.Graph.unpack(hout)
-        hdom, hcls, hwords = dominant_class(hinfos, args.steps)
-        hstep = float(np.mean(hms))
-        line["heavy"] = {
-            "roots": int(len(hv)), "roots_in_class": n_heavy,
-            "sample": f"seeded {args.heavy_fraction:.4g} of the roots with 128 <= |P| < 256",
-            "cliques": hres[0], "hash": f"{hres[1]:#018x}", "ms": hstep,
-            "value": hres[0] / (hstep * 1e-3), "unit": UNIT,
-            "search_by_width": {str(WIDTHS[i]): float(hcls[i]) for i in range(6) if hcls[i] > 0},
-            "search_roofline": {"kernel": f"search_kernel<W={WIDTHS[hdom]}>",
-                                "achieved_gword_s": hwords[hdom] / max(hcls[hdom], 1e-9) * 1e-6,
-                                "frac": hwords[hdom] / max(hcls[hdom], 1e-9) * 1e3
-                                / pr["words_per_s"]},
-        }
-        # the stored sample the oracle can finish (its per-root results): GPU parity root by
-        # root, and the oracle timed on the same roots
+    if not args.no_heavy and args.scale == 20 and args.seed == 1:
+        # heavy roots (|P| >= 128, left out of the headline): the stored seeded sample that the
+        # oracle finished root by root (tests/golden/rmat_s20_heavy_roots.txt); parity root by
+        # root against the stored results, timing of the whole sample, and the oracle timed on
+        # its 8-word roots (the 16-word ones take it minutes each)
+        progress("heavy roots")
         gold = heavy_golden(g)
-        if gold is not None and len(gold[0]):
-            # the 8-word class only: the stored 16-word roots take the oracle minutes each
-            keep = gold[2] < 256
-            groots, gkeys, gpc = gold[0][keep], [k for k, t in zip(gold[1], keep) if t], \
-                gold[2][keep]
+        if gold is None:
+            line["heavy"] = {"error": "stored heavy-root results missing or made on another graph"}
+        else:
+            groots, gkeys, gpc = gold
             bad = [int(v) for v, key in zip(groots, gkeys)
                    if h.count_roots_result(np.array([v], np.int32)) != key]
             gdev = torch.from_numpy(groots).cuda()
             gout = h.new_output()
-            gms, _ = timed_steps(lambda: h.count_roots(gdev, out=gout), args.steps,
-                                 args.warmup, flush, stream)
+            gms, ginfos = timed_steps(lambda: h.count_roots(gdev, out=gout), args.steps,
+                                      args.warmup, flush, stream, h.get_info)
             h.check()
             gres = mce.Graph.unpack(gout)
+            gdom, gcls, gwords = dominant_class(ginfos, args.steps)
             gstep = float(np.mean(gms))
-            entry = {"roots": int(len(groots)), "p_range": [int(gpc.min()), int(gpc.max())],
-                     "cliques": gres[0], "ms": gstep, "value": gres[0] / (gstep * 1e-3),
-                     "parity_per_root": "ok" if not bad else f"MISMATCH at roots {bad[:8]}"}
+            entry = {
+                "sample": "stored seeded sample of R-MAT s20 roots with 128 <= |P| < 512 that "
+                          "the oracle finished (tests/golden/rmat_s20_heavy_roots.txt)",
+                "roots": int(len(groots)), "roots_8_word": int((gpc < 256).sum()),
+                "roots_16_word": int((gpc >= 256).sum()),
+                "cliques": gres[0], "hash": f"{gres[1]:#018x}", "ms": gstep,
+                "value": gres[0] / (gstep * 1e-3), "unit": UNIT,
+                "search_by_width": {str(WIDTHS[i]): float(gcls[i]) for i in range(6)
+                                    if gcls[i] > 0},
+                "search_roofline": {"kernel": f"search_kernel<W={WIDTHS[gdom]}>",
+                                    "achieved_gword_s": gwords[gdom] / max(gcls[gdom], 1e-9)
+                                    * 1e-6,
+                                    "frac": gwords[gdom] / max(gcls[gdom], 1e-9) * 1e3
+                                    / pr["words_per_s"]},
+                "parity_per_root": "ok" if not bad else f"MISMATCH at roots {bad[:8]}"}
             if rank == 0 and world == 1 and not args.no_cpu_baseline:
+                keep = gpc < 256
+                sub = groots[keep]
                 cores = len(os.sched_getaffinity(0))
-                ores, dt = oracle_count_timed(g, groots, cores)
+                ores, dt = oracle_count_timed(g, sub, cores)
+                got = h.count_roots_result(sub)
                 entry["cpu_baseline"] = cpu_block(
-                    ores.count / dt, cores, f"oracle on the same {len(groots)} roots: "
+                    ores.count / dt, cores, f"oracle on the sample's {len(sub)} 8-word roots: "
                     f"{ores.count} cliques in {dt:.1f} s, including its input checks, peel and "
                     f"relabelling of the whole graph")
-                entry["parity"] = "ok" if gres == ores.key() else f"MISMATCH {gres} {ores.key()}"
-            line["heavy"]["oracle_sample"] = entry
+                entry["parity_8_word_roots"] = ("ok" if got == ores.key()
+                                                else f"MISMATCH {got} {ores.key()}")
+            line["heavy"] = entry
 
     if not args.no_e2e:
+        progress("e2e")
         line["e2e"] = e2e_leg(args, g, roots, world)
     threads = len(os.sched_getaffinity(0))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        progress("oracle on the workload")
         ores, dt = oracle_count_timed(g, roots, threads)
         pre = oracle_preprocessing_s(g)
         line["cpu_baseline"] = cpu_block(
@@ -720,6 +725,7 @@ def run_gb300(args, rank, world, local):
     if names:
         line["configs"] = {}
         for name in names:
+            progress(f"config {name}")
             line["configs"][name] = run_other_config(
                 name, args.seed, args, flush, pr["words_per_s"], threads,
                 rank == 0 and world == 1 and not args.no_cpu_baseline, hbm)
