@@ -462,17 +462,19 @@ __device__ __forceinline__ bool mbar_try_wait(unsigned addr, unsigned parity)
 }
 
 // Barrier of the cluster's CTAs through two mbarriers per CTA, used alternately (episode e
-// uses bars[e & 1], whose phase parity is then (e >> 1) & 1): thread 0 of every CTA arrives
-// on the barrier of every CTA (release, cluster scope), then waits on its own (acquire), at
-// most limit_ns.  Alternating keeps an early arrival for the next episode from completing a
+// uses bars[e & 1], whose phase parity is then (e >> 1) & 1): every CTA arrives on the barrier
+// of every CTA (release, cluster scope; thread j of the CTA on CTA j's, after the CTA's own
+// barrier), then thread 0 waits on its own (acquire), at most limit_ns.  Alternating keeps an early arrival for the next episode from completing a
 // CTA's current one.  Returns false after a timeout (MCE_ERR_DEVICE_TIMEOUT recorded).
 __device__ bool tail_barrier(unsigned long long *bars, int &episode, unsigned nb,
                              long long limit_ns, DevCtrl *ctrl, int *s_ok)
 {
     __syncthreads();
+    const unsigned laddr = smem_u32(bars + (episode & 1));
+    // lane j of warp 0 arrives on CTA j's barrier: the arrivals (each a release) run side by
+    // side instead of one after another
+    if (threadIdx.x < nb) mbar_arrive_remote(cluster_map(laddr, threadIdx.x));
     if (threadIdx.x == 0) {
-        const unsigned laddr = smem_u32(bars + (episode & 1));
-        for (unsigned j = 0; j < nb; ++j) mbar_arrive_remote(cluster_map(laddr, j));
         const unsigned parity = (unsigned)(episode >> 1) & 1u;
         int ok = 1;
         const unsigned long long t0 = globaltimer_ns();
@@ -909,6 +911,9 @@ cudaError_t launch_unit_offsets(const DevGraph &g, const int *roots, int n_roots
 // kernel fits, else 8, else 0 (then the grid-wide kernel runs every round).  Cached per device.
 int tail_cluster_ctas()
 {
+#ifdef MCE_NO_PEEL_TAIL
+    return 0;
+#endif
     constexpr int kMaxDev = 64;
     static int cached[kMaxDev] = {};            // 0 = unknown, else ctas + 1
     int dev = 0;

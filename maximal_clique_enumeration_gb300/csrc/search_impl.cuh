@@ -491,13 +491,15 @@ __device__ int xx_partition(const DevGraph &g, const RootCtx &r, int lpX, int c,
 //   * P's members p_0 .. p_{k-1} (ascending) renumber the node's columns; N_i is the closed
 //     neighbourhood of p_i inside P, as a k-bit mask;
 //   * C is a maximal clique of G[P] iff, for every i < k, C is a subset of N_i exactly when i is
-//     in C;
-//   * C is extended by a vertex of X iff some X vertex's k-bit mask of neighbours in P contains
-//     C: the masks of X_P and X_X are collected as a 256-bit set and closed under subsets;
-//   * the 256 subsets are bit-sliced over lanes 0-7 (lane l holds subsets 32 l .. 32 l + 31), so
-//     each test is a handful of word operations.
+//     in C; the 256 subsets are bit-sliced over lanes 0-7 (lane l holds subsets
+//     32 l .. 32 l + 31), so each of the k tests is a handful of word operations;
+//   * each such C (there are few) is reported unless some row of X_P or X_X contains it: the
+//     lanes test 32 rows at a time, as the pivot scan would.
 // Count mode only (enumeration walks the subtree, so that every clique is written as before).
-constexpr int kSmallP = 8;
+#ifndef MCE_SMALL_P
+#define MCE_SMALL_P 8
+#endif
+constexpr int kSmallP = MCE_SMALL_P;   // 0 turns the whole-subtree solver off
 
 // kSubsets5[m]: bit t set iff the 5-bit value t is a subset of the 5-bit value m.
 struct Subsets5 {
@@ -555,9 +557,9 @@ __device__ void solve_small(const SearchArgs &a, const RootCtx &r, const Ck<W> &
                             const Ck<W> &XP, int lpX, unsigned long long S, int L, int k,
                             Acc &acc, unsigned long long *s_hist, unsigned *scratch, int lane)
 {
-    unsigned *T = scratch;                                    // 256-bit set of X masks
+    int *mem = reinterpret_cast<int *>(scratch);                          // columns of P
     unsigned long long *keys = reinterpret_cast<unsigned long long *>(scratch + 8);
-    // lane j < k: the column of p_j
+    // lane j < k: the column of p_j (the j-th member of P, ascending)
     int my_p = 0;
     {
         int j = 0;
@@ -572,55 +574,11 @@ __device__ void solve_small(const SearchArgs &a, const RootCtx &r, const Ck<W> &
             }
         }
     }
-    if (lane < 8) T[lane] = 0u;
     unsigned adj = 0;                                         // lane i < k: N(p_i) n P, packed
     if (lane < k) {
+        mem[lane] = my_p;
         adj = gather_bits<W>(ck_load<W>(r.rowsP + (long long)my_p * W), P);
         keys[lane] = r.pkey[my_p];
-    }
-    // the X vertices' masks: members of X_P (P rows), then the live X_X rows
-    const int nxp = list_bits<W>(XP, r.plist, lane);          // ends with __syncwarp
-    const int nx = nxp + lpX;
-    for (int base = 0; base < nx; base += 32) {
-        const int t = base + lane;
-        unsigned m = 0;
-        if (t < nxp) {
-            m = gather_bits<W>(ck_load<W>(r.rowsP + (long long)r.plist[t] * W), P);
-        } else if (t < nx) {
-            const int x = r.xx[t - nxp];
-            if constexpr (kIP) {
-                // no X rows: one search of the graph per member of P
-                const int xid = r.xids[x];
-                int j = 0;
-#pragma unroll
-                for (int w = 0; w < W; ++w) {
-                    unsigned pm = P.w[w];
-                    while (pm) {
-                        const int b = __ffs(pm) - 1;
-                        m |= (x_adjacent(a.g, xid, r.pids[w * 32 + b]) ? 1u : 0u) << j;
-                        ++j;
-                        pm &= pm - 1u;
-                    }
-                }
-            } else {
-                m = gather_bits<W>(ck_load<W>(r.rowsX + (long long)x * W), P);
-            }
-        }
-        if (m) atomicOr(&T[m >> 5], 1u << (m & 31u));
-    }
-    __syncwarp();
-    // subsets covered by some X mask: closure of T under subsets (lanes 0-7 hold 32 subsets
-    // each; bits 0-4 of a subset inside the word, bits 5-7 in the lane number)
-    unsigned D = lane < 8 ? T[lane] : 0u;
-    D |= (D >> 1) & 0x55555555u;
-    D |= (D >> 2) & 0x33333333u;
-    D |= (D >> 4) & 0x0F0F0F0Fu;
-    D |= (D >> 8) & 0x00FF00FFu;
-    D |= (D >> 16) & 0x0000FFFFu;
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) {
-        const unsigned up = __shfl_xor_sync(kFull, D, o);
-        if (!(lane & o)) D |= up;
     }
     // maximal cliques of G[P]: subsets of {0..k-1} with [C subset of N_i] == [i in C] for all i
     unsigned V = subsets_of((1u << k) - 1u, lane);
@@ -628,34 +586,67 @@ __device__ void solve_small(const SearchArgs &a, const RootCtx &r, const Ck<W> &
         const unsigned ni = __shfl_sync(kFull, adj, i) | (1u << i);
         V &= ~(subsets_of(ni, lane) ^ subsets_with(i, lane));
     }
-    V = lane < 8 ? V & ~D : 0u;
-    if (lane == 0) acc.words += (unsigned long long)(k + nx) * W + 8ULL * (unsigned)k;
-    const int total = __reduce_add_sync(kFull, __popc(V));
-    if (total == 0) return;
+    if (lane >= 8) V = 0u;
+    // X: the members of X_P (their rows are P rows), then the live X_X rows
+    const int nxp = list_bits<W>(XP, r.plist, lane);          // ends with __syncwarp
+    const int nx = nxp + lpX;
     const int rsize = r.rsize + L;
-    unsigned long long hs = 0;
-    for (unsigned v = V; v; v &= v - 1u) {
-        const unsigned C = (unsigned)lane * 32u + (unsigned)(__ffs(v) - 1);
+    unsigned long long words = (unsigned long long)k * W + 8ULL * (unsigned)k;
+    unsigned cand = __ballot_sync(kFull, V != 0u);
+    while (cand) {
+        // the next candidate C (the same in every lane), as a set of columns
+        const int src = __ffs(cand) - 1;
+        const unsigned vs = __shfl_sync(kFull, V, src);
+        const unsigned C = (unsigned)src * 32u + (unsigned)(__ffs(vs) - 1);
+        if (lane == src) V &= V - 1u;
+        cand = __ballot_sync(kFull, V != 0u);
+        Ck<W> cb = ck_zero<W>();
         unsigned long long sum = S;
-        int size = rsize;
         for (unsigned cm = C; cm; cm &= cm - 1u) {
-            sum += keys[__ffs(cm) - 1];
-            ++size;
-        }
-        if (size >= a.out.hist_len) {                         // cannot happen: size <= d + 1
-            set_status(a.g.ctrl, MCE_ERR_INTERNAL);
-            continue;
-        }
-        hs += mix64(sum);
-        atomicAdd(&s_hist[size], 1ULL);
-    }
+            const int j = __ffs(cm) - 1;
+            const int col = mem[j];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) hs += __shfl_xor_sync(kFull, hs, o);
-    if (lane == 0) {
-        acc.count += (unsigned)total;
-        acc.hash += hs;
-        acc.nodes += (unsigned)total;
+            for (int w = 0; w < W; ++w) cb.w[w] |= (col >> 5) == w ? 1u << (col & 31) : 0u;
+            sum += keys[j];
+        }
+        // extended by a vertex of X: some X row containing all of C
+        bool dominated = false;
+        for (int base = 0; base < nx && !dominated; base += 32) {
+            const int t = base + lane;
+            bool hit = false;
+            if (t < nxp) {
+                const Ck<W> rc = ck_load<W>(r.rowsP + (long long)r.plist[t] * W);
+                hit = !ck_nonzero<W>(ck_andnot<W>(cb, rc));
+            } else if (t < nx) {
+                const int x = r.xx[t - nxp];
+                if constexpr (kIP) {
+                    hit = true;
+                    const int xid = r.xids[x];
+                    for (unsigned cm = C; cm && hit; cm &= cm - 1u)
+                        hit = x_adjacent(a.g, xid, r.pids[mem[__ffs(cm) - 1]]);
+                } else {
+                    const Ck<W> rc = ck_load<W>(r.rowsX + (long long)x * W);
+                    hit = !ck_nonzero<W>(ck_andnot<W>(cb, rc));
+                }
+            }
+            dominated = __any_sync(kFull, hit);
+            words += (unsigned long long)W * (unsigned)min(32, nx - base);
+        }
+        if (dominated) continue;
+        const int size = rsize + __popc(C);
+        if (lane == 0) {
+            if (size >= a.out.hist_len) {                     // cannot happen: size <= d + 1
+                set_status(a.g.ctrl, MCE_ERR_INTERNAL);
+            } else {
+                acc.count++;
+                acc.hash += mix64(sum);
+                acc.nodes++;
+                atomicAdd(&s_hist[size], 1ULL);
+            }
+        }
     }
+    if (lane == 0) acc.words += words;
+    __syncwarp();
 }
 
 // ------------------------------------------------------------------ worker list (Section 3.3)
@@ -1444,26 +1435,48 @@ __device__ __forceinline__ int last_at_most(const int *a, int lo, int hi, int t,
 #define MCE_MIN_BLOCKS_MID 6
 #endif
 // (measured: 2-word rows run best at 7, which leaves them 72 registers instead of 64)
+// W = 0: the merged launch of the normal roots of W = 1, 2 and 4 (planned as W = 4).
 template <int W>
 struct MinBlocks {
-    static constexpr int value = W == 1 ? 8 : (W == 2 ? 7 : (W <= 8 ? MCE_MIN_BLOCKS_MID : 4));
+    static constexpr int value =
+        W == 1 ? 8 : (W == 2 ? 7 : (W <= 8 ? MCE_MIN_BLOCKS_MID : 4));
 };
+
+// First-level subtree of root v (or, with second-level subtrees, the subtree of its edge to w),
+// searched with rows of W words.
+template <int W, bool Big>
+__device__ __forceinline__ void search_unit(const SearchArgs &a, unsigned *ws, const WarpSmem &sm,
+                                            int v, int w, int deg, int np, Acc &acc,
+                                            unsigned long long *s_hist, int lane)
+{
+    if constexpr (kL2) {
+        if (w >= 0) search_edge<W, Big>(a, ws, sm, v, w, acc, s_hist, lane);
+    } else {
+        search_root<W, Big>(a, ws, sm, v, deg, np, acc, s_hist, lane);
+    }
+}
 
 // One persistent launch per row width W and launch group: the roots of that class, heaviest
 // first, then donated branches of those roots (Section 3.3).  Big: the group of roots whose
 // workspace exceeds kWsCapWords (their build code is compiled into these instances only).
+// W = 0: one launch for the normal roots of W = 4, then 2, then 1 (each root and each donated
+// branch searched with its own row width), so that warps that run out of 4-word roots go on
+// with narrower ones instead of idling until the launch's longest roots end.
 template <int W, bool Big>
 __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(SearchArgs a)
 {
+    static_assert(W != 0 || !Big, "the merged launch takes normal roots only");
     extern __shared__ __align__(16) unsigned char s_raw[];
+    __shared__ unsigned long long s_cls_words[3];     // merged launch: words per row width
     unsigned long long *s_hist = reinterpret_cast<unsigned long long *>(s_raw);
     for (int i = threadIdx.x; i < a.out.hist_len; i += blockDim.x) s_hist[i] = 0ULL;
+    if (threadIdx.x < 3) s_cls_words[threadIdx.x] = 0ULL;
     const int lane = threadIdx.x & 31;
     const int wpb = blockDim.x >> 5;
     const int warp = blockIdx.x * wpb + (threadIdx.x >> 5);
     WarpSmem sm;
     {
-        constexpr int k = W == 1 ? 0 : W == 2 ? 1 : W == 4 ? 2 : W == 8 ? 3 : W == 16 ? 4 : 5;
+        constexpr int k = W == 1 ? 0 : W == 2 ? 1 : W == 4 || W == 0 ? 2 : W == 8 ? 3 : W == 16 ? 4 : 5;
         const size_t hist = ((size_t)(a.out.hist_len + 1) * 8 + 15) & ~(size_t)15;
         unsigned char *mine = s_raw + hist + (size_t)(threadIdx.x >> 5) * warp_smem_bytes(k);
         sm.hkey = reinterpret_cast<int *>(mine);
@@ -1478,7 +1491,7 @@ __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(Search
     __syncthreads();
     unsigned *ws = a.ws + (unsigned long long)warp * a.ws_words;
     const unsigned long long begin = (unsigned long long)a.range[2 * a.group];
-    const int end = a.range[2 * a.group + 1];
+    const int end = a.range[2 * a.group_end + 1];
     // work items: the roots of this launch, or with second-level subtrees their edges
     const int ubase = kL2 ? a.uoff[begin] : 0;
     const unsigned long long n_roots = kL2 ? (unsigned long long)(a.uoff[end] - ubase)
@@ -1522,10 +1535,16 @@ __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(Search
             }
         } else if (np > kMaxP) {
             if (lane == 0) set_status(a.g.ctrl, MCE_ERR_LIMIT);
-        } else if (kL2) {
-            if (w >= 0) search_edge<W, Big>(a, ws, sm, v, w, acc, s_hist, lane);
+        } else if constexpr (W == 0) {
+            const int k = wclass_index(np);
+            if (k == 0) search_unit<1, false>(a, ws, sm, v, w, deg, np, acc, s_hist, lane);
+            else if (k == 1) search_unit<2, false>(a, ws, sm, v, w, deg, np, acc, s_hist, lane);
+            else if (k == 2) search_unit<4, false>(a, ws, sm, v, w, deg, np, acc, s_hist, lane);
+            else if (lane == 0) set_status(a.g.ctrl, MCE_ERR_INTERNAL);
+            if (lane == 0 && k <= 2) atomicAdd(&s_cls_words[k], acc.words);
+            acc.words = 0;
         } else {
-            search_root<W, Big>(a, ws, sm, v, deg, np, acc, s_hist, lane);
+            search_unit<W, Big>(a, ws, sm, v, w, deg, np, acc, s_hist, lane);
         }
         __syncwarp();
         if (lane == 0) busy.fetch_sub(1, cuda::memory_order_acq_rel);
@@ -1578,19 +1597,32 @@ __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(Search
         if (state != 1) break;
         __syncwarp();
         cuda::atomic_thread_fence(cuda::memory_order_acquire, cuda::thread_scope_device);
-        search_inbox<W>(a, ws, sm, acc, s_hist, lane);
+        if constexpr (W == 0) {
+            // the donor's root, and so the row width, is in the inbox header
+            const int k = wclass_index((int)ws[kHdrLayNp]);
+            if (k == 0) search_inbox<1>(a, ws, sm, acc, s_hist, lane);
+            else if (k == 1) search_inbox<2>(a, ws, sm, acc, s_hist, lane);
+            else if (k == 2) search_inbox<4>(a, ws, sm, acc, s_hist, lane);
+            else if (lane == 0) set_status(a.g.ctrl, MCE_ERR_INTERNAL);
+            if (lane == 0 && k <= 2) atomicAdd(&s_cls_words[k], acc.words);
+            acc.words = 0;
+        } else {
+            search_inbox<W>(a, ws, sm, acc, s_hist, lane);
+        }
         __syncwarp();
         if (lane == 0) busy.fetch_sub(1, cuda::memory_order_acq_rel);
     }
     __syncthreads();
     for (int i = threadIdx.x; i < a.out.hist_len; i += blockDim.x)
         if (s_hist[i]) atomicAdd(&a.out.hist[i], s_hist[i]);
+    if (W == 0 && threadIdx.x < 3 && s_cls_words[threadIdx.x])
+        atomicAdd(&a.g.ctrl->words[threadIdx.x], s_cls_words[threadIdx.x]);
     if (lane == 0) {
         atomicAdd(&a.g.ctrl->result[0], acc.count);
         atomicAdd(&a.g.ctrl->result[1], acc.hash);
         atomicAdd(&a.g.ctrl->tree_nodes, acc.nodes);
         atomicAdd(&a.g.ctrl->donations, acc.donations);
-        atomicAdd(&a.g.ctrl->words[a.cls], acc.words);
+        if (W != 0) atomicAdd(&a.g.ctrl->words[a.cls], acc.words);
 #ifdef MCE_PROFILE
         for (int i = 0; i < 8; ++i) {
             if (i == kProfMaxRoot) atomicMax(&a.g.ctrl->prof[a.cls][i], acc.prof[i]);
