@@ -110,8 +110,7 @@ typedef struct mce_info {
                                           child sets, X_X tests): the search's integer work  */
     int32_t roots[MCE_NUM_WIDTHS];     /* first-level roots of the full schedule per class   */
     int32_t workers[MCE_NUM_WIDTHS];   /* warps launched per class (0: class not launched)   */
-    float ms_search[MCE_NUM_WIDTHS];   /* device time of each class's launches (profile = 1
-                                          only); see narrow_merged                           */
+    float ms_search[MCE_NUM_WIDTHS];   /* device time per class launch (profile = 1 only)    */
     float ms_order;                    /* device time of the last mce_order/mce_create order */
     int32_t launches;                  /* kernels launched by the last order + count calls   */
     int32_t induced;                   /* induced subgraph in use: 1 full, 2 partial         */
@@ -119,10 +118,6 @@ typedef struct mce_info {
     float ms_peel;                     /* the peel's part of ms_order (profile = 1 only)     */
     int64_t peel_live;                 /* vertices still in the graph, summed over the peel's
                                           rounds (the live lists its rounds scan)            */
-    int32_t narrow_merged;             /* 1: the roots of row width 1, 2 and 4 words that fit
-                                          the normal workspace ran in one launch, whose time
-                                          ms_search[2] holds (ms_search[0], [1] then hold
-                                          only the big-workspace launches of those widths)   */
 } mce_info;
 
 /* Writes the default configuration into *cfg.  Returns MCE_ERR_INVALID_ARG if cfg is NULL. */

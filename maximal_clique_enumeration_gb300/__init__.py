@@ -61,7 +61,7 @@ class Info(ctypes.Structure):
                 ("ms_search", ctypes.c_float * NUM_WIDTHS), ("ms_order", ctypes.c_float),
                 ("launches", ctypes.c_int32), ("induced", ctypes.c_int32),
                 ("subtree_level", ctypes.c_int32), ("ms_peel", ctypes.c_float),
-                ("peel_live", ctypes.c_int64), ("narrow_merged", ctypes.c_int32)]
+                ("peel_live", ctypes.c_int64)]
 
     def as_dict(self):
         out = {}

@@ -23,6 +23,7 @@ struct mce_graph {
     unsigned long long grp_ws[kNumGroups] = {};
     size_t cls_smem[kNumClasses] = {};
     long long uroots_cap = 0;
+    int small_lo = 1, small_hi = kSmallP;     // |P| range of the nodes solved whole
     bool unit_own = false;    // unit_cnt / unit_scan were reallocated for a caller's root list
     int degeneracy = 0, max_degree = 0, hist_len = 2, rounds = 0;
     unsigned long long ws_words = 0;
@@ -219,21 +220,14 @@ mce_status run_search(mce_graph *h, cudaStream_t s, bool user_roots, const DevOu
     a.donate_min_p = h->cfg.donate_min_p;
     a.donate_rule = h->cfg.donate_rule;
     a.spin_limit_ns = h->cfg.spin_limit_ns;
+    a.small_lo = h->small_lo;
+    a.small_hi = h->small_hi;
     for (int o = 0; o < kNumGroups; ++o) {
         const int gi = group_at(o), k = gi / 2;
-        // the normal roots of W = 4, 2, 1 (positions kMergedFirstPos ..) share one launch
-        const bool merged = kMergeNarrow && o == kMergedFirstPos;
-        if (kMergeNarrow && o > kMergedFirstPos) break;
-        const int gend = merged ? group_at(kNumGroups - 1) : gi;
         if (h->grp_workers[gi] == 0) continue;            // no vertex of the graph in this group
-        if (!user_roots) {
-            int count = 0;
-            for (int p = o; p <= (merged ? kNumGroups - 1 : o); ++p) count += h->grp_count[group_at(p)];
-            if (count == 0) continue;
-        }
+        if (!user_roots && h->grp_count[gi] == 0) continue;
         a.cls = k;
         a.group = gi;
-        a.group_end = gend;
         a.ws_words = h->grp_ws[gi];
         a.n_workers = h->grp_workers[gi];
         MCE_TRY(cudaMemsetAsync(h->flag, 0, sizeof(int) * (size_t)a.n_workers, s));
@@ -461,28 +455,6 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
         if ((size_t)h->grp_workers[gi] * need > ws_total) ws_total = (size_t)h->grp_workers[gi] * need;
         if (h->grp_workers[gi] > h->n_workers) h->n_workers = h->grp_workers[gi];
     }
-    if (kMergeNarrow) {
-        // the normal roots of W = 4, 2, 1 share one launch: its warps hold the largest root of
-        // the three groups
-        unsigned long long need = 0;
-        for (int gi = 1; gi <= 5; gi += 2) need = h->grp_ws[gi] > need ? h->grp_ws[gi] : need;
-        if (need > 0) {
-            int per_sm = 0;
-            MCE_TRY(search_configure(-1, g.ip, g.l2, h->cls_smem[2]));
-            MCE_TRY(search_occupancy(-1, g.ip, g.l2, h->search_threads, h->cls_smem[2], &per_sm));
-            if (per_sm < 1) return MCE_ERR_CUDA;
-            if (h->cfg.blocks_per_sm > 0 && h->cfg.blocks_per_sm < per_sm)
-                per_sm = h->cfg.blocks_per_sm;
-            for (int gi = 1; gi <= 5; gi += 2) {
-                h->grp_blocks[gi] = per_sm * h->sm_count;
-                h->grp_workers[gi] = per_sm * h->sm_count * wpb;
-                h->grp_ws[gi] = need;
-            }
-            const int workers = per_sm * h->sm_count * wpb;
-            if ((size_t)workers * need > ws_total) ws_total = (size_t)workers * need;
-            if (workers > h->n_workers) h->n_workers = workers;
-        }
-    }
     h->ws_words = ws_total;
     MCE_ALLOC(h, h->ws, ws_total);
     MCE_ALLOC(h, h->ring, (size_t)h->n_workers);
@@ -519,6 +491,12 @@ mce_status mce_create(const int32_t *offsets, const int32_t *adj, int32_t n, int
         return MCE_ERR_INVALID_ARG;
     }
     if (h->cfg.spin_limit_ns <= 0) h->cfg.spin_limit_ns = 20LL * 1000 * 1000 * 1000;
+#ifdef MCE_AB_ENV
+    // measurement builds only: the solver's |P| range from the environment
+    if (const char *e = getenv("MCE_AB_SMALL_LO")) h->small_lo = atoi(e);
+    if (const char *e = getenv("MCE_AB_SMALL_HI")) h->small_hi = atoi(e);
+    if (h->small_hi > kSmallP) h->small_hi = kSmallP;
+#endif
     mce_status st = create_impl(h, offsets, adj, n, is_device_ptr, (cudaStream_t)stream);
     if (st != MCE_OK) {
         cudaStreamSynchronize((cudaStream_t)stream);
@@ -772,7 +750,6 @@ mce_status mce_get_info(mce_graph *h, mce_info *info)
         MCE_TRY(cudaEventElapsedTime(&info->ms_peel, h->ev_order[0], h->ev_order[2]));
     }
     info->peel_live = c.peel_live;
-    info->narrow_merged = kMergeNarrow ? 1 : 0;
     info->launches = h->launches_order + h->launches_count;
     return MCE_OK;
 }

@@ -20,6 +20,7 @@ constexpr long long kWsCapWords = 16384;     // workspace per warp of a "normal"
 constexpr long long kBigBudgetWords = 256LL << 20;   // workspace of a "big" launch (1 GiB)
 constexpr int kScanBlock = 1024;         // elements per CTA of the exclusive scan
 constexpr int kProfSms = 256;            // MCE_PROFILE builds: per-SM load slots per class
+constexpr int kSmallP = 8;               // largest |P| of a search-tree node solved whole
 
 // Device-resident control block of a handle.
 struct DevCtrl {
@@ -105,12 +106,11 @@ struct SearchArgs {
     DevGraph g;
     DevOut out;
     const int *roots;        // g.sched or g.uroots
-    const int *range;        // begin/end of each launch group's roots in `roots`
+    const int *range;        // roots[range[2 group] .. range[2 group + 1]) are this launch's
     const int *uoff;         // second-level subtrees: prefix of subtree counts over roots[]
     int cls;                 // row-width class of this launch (W = 1 << cls)
     int group;               // launch group (2 cls + 0 for big-workspace roots, + 1 otherwise)
-    int group_end;           // last group of the launch: roots[range[2 group] ..
-                             // range[2 group_end + 1]); != group for the merged narrow launch
+    int small_lo, small_hi;  // nodes with small_lo <= |P| <= small_hi are solved whole
     unsigned int *ws;        // per-warp workspace, ws_words each
     unsigned long long ws_words;
     int *ring;               // worker list: ring of idle warp ids [n_workers]
@@ -181,28 +181,9 @@ __host__ __device__ inline WsLayout ws_layout(int deg, int np, bool ip, bool l2)
 constexpr int kCostBuckets = 48;
 constexpr int kNumBuckets = 1 + kNumGroups * kCostBuckets;
 
-// Launch position o = 0 .. kNumGroups-1 <-> group g = 2k + b.  Widest rows first; for W <= 4
-// the big-workspace groups come before the normal ones (positions 6-8: W = 4, 2, 1), so that the
-// normal roots of W = 4, 2 and 1 are consecutive in the schedule (positions 9-11) and one launch
-// takes them all: the idle warps at the end of the 4-word roots go on with the narrower ones
-// instead of waiting for the launch's last roots.
-#ifndef MCE_SEPARATE_NARROW
-constexpr bool kMergeNarrow = true;
-#else
-constexpr bool kMergeNarrow = false;
-#endif
-constexpr int kMergedFirstPos = 9;
-__host__ __device__ inline int group_at(int o)
-{
-    return o <= 6 ? 2 * (kNumClasses - 1 - o / 2) + (o & 1) : o <= 8 ? 2 * (8 - o)
-                                                                      : 2 * (11 - o) + 1;
-}
-__host__ __device__ inline int position_of(int g)
-{
-    if (g >= 6) return 2 * (kNumClasses - 1 - g / 2) + (g & 1);
-    if (g == 4) return 6;
-    return (g & 1) == 0 ? 8 - g / 2 : 11 - g / 2;
-}
+// Launch position o = 0 .. kNumGroups-1 <-> group g = 2k + b.
+__host__ __device__ inline int group_at(int o) { return 2 * (kNumClasses - 1 - o / 2) + (o & 1); }
+__host__ __device__ inline int position_of(int g) { return 2 * (kNumClasses - 1 - g / 2) + (g & 1); }
 
 __device__ inline int sched_bucket(int np, int deg, bool ip, bool l2, int core)
 {
@@ -232,8 +213,7 @@ cudaError_t launch_order(const DevGraph &g, int peel_blocks, long long spin_limi
 cudaError_t launch_search(const SearchArgs &a, int blocks, int threads, size_t smem,
                           cudaStream_t s);
 cudaError_t launch_search_prep(const SearchArgs &a, cudaStream_t s);
-// CTAs per SM of the kernel of launch group `group` (row-width class group / 2; -1: the
-// merged launch of the normal roots of W <= 4).
+// CTAs per SM of the kernel of launch group `group` (row-width class group / 2).
 cudaError_t search_occupancy(int group, int ip, int l2, int threads, size_t smem,
                              int *blocks_per_sm);
 // Shared memory of the search kernel of class k: the size histogram, then per warp a hash of
@@ -255,7 +235,6 @@ __host__ __device__ inline size_t search_smem_bytes(int k, int hist_len, int war
     const size_t hist = ((size_t)(hist_len + 1) * 8 + 15) & ~(size_t)15;
     return hist + (size_t)warps * warp_smem_bytes(k);
 }
-// cls = -1: the merged launch of the normal roots of W <= 4 (shared memory of class 2).
 cudaError_t search_configure(int cls, int ip, int l2, size_t smem);
 cudaError_t launch_bin_roots(const DevGraph &g, const int *roots, int n_roots, cudaStream_t s);
 // Second-level subtrees: uoff[i] = number of subtrees of roots[0 .. i) (edges to later

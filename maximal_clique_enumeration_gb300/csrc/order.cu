@@ -21,6 +21,7 @@
 // isolated vertices, bucket the first-level roots by |P|, heaviest first, and store the
 // later-neighbour lists N+(v) as a CSR (scan of |P|, then a stable split of each adjacency).
 #include <climits>
+#include <cstdlib>
 
 #include <cuda/atomic>
 
@@ -911,8 +912,8 @@ cudaError_t launch_unit_offsets(const DevGraph &g, const int *roots, int n_roots
 // kernel fits, else 8, else 0 (then the grid-wide kernel runs every round).  Cached per device.
 int tail_cluster_ctas()
 {
-#ifdef MCE_NO_PEEL_TAIL
-    return 0;
+#ifdef MCE_AB_ENV
+    if (getenv("MCE_AB_NO_TAIL")) return 0;   // measurement builds only
 #endif
     constexpr int kMaxDev = 64;
     static int cached[kMaxDev] = {};            // 0 = unknown, else ctas + 1

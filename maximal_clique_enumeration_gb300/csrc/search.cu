@@ -81,7 +81,6 @@ __global__ void enum_close_kernel(DevOut o, const long long *totals)
 
 // Kernel instances, one translation unit per variant (built in parallel): full or partial
 // induced subgraphs, first- or second-level subtrees.
-// cls = -1: the merged launch of the normal roots of W = 1, 2 and 4.
 const void *search_kernel_full(int cls, bool big);
 const void *search_kernel_partial(int cls, bool big);
 const void *search_kernel_full_l2(int cls, bool big);
@@ -95,9 +94,6 @@ static const void *search_kernel_ptr(int cls, int ip, int l2, bool big)
 
 cudaError_t search_configure(int cls, int ip, int l2, size_t smem)
 {
-    if (cls < 0)
-        return cudaFuncSetAttribute(search_kernel_ptr(-1, ip, l2, false),
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     for (int big = 0; big < 2; ++big) {
         const cudaError_t e = cudaFuncSetAttribute(search_kernel_ptr(cls, ip, l2, big != 0),
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -110,9 +106,6 @@ cudaError_t search_configure(int cls, int ip, int l2, size_t smem)
 cudaError_t search_occupancy(int group, int ip, int l2, int threads, size_t smem,
                              int *blocks_per_sm)
 {
-    if (group < 0)
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            blocks_per_sm, search_kernel_ptr(-1, ip, l2, false), threads, smem);
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
         blocks_per_sm, search_kernel_ptr(group / 2, ip, l2, (group & 1) == 0), threads, smem);
 }
@@ -122,9 +115,7 @@ cudaError_t launch_search(const SearchArgs &a, int blocks, int threads, size_t s
 {
     SearchArgs aa = a;
     void *args[] = {&aa};
-    const bool merged = a.group_end != a.group;
-    return cudaLaunchKernel(search_kernel_ptr(merged ? -1 : a.cls, a.g.ip, a.g.l2,
-                                              !merged && (a.group & 1) == 0),
+    return cudaLaunchKernel(search_kernel_ptr(a.cls, a.g.ip, a.g.l2, (a.group & 1) == 0),
                             dim3(blocks), dim3(threads), args, smem, s);
 }
 

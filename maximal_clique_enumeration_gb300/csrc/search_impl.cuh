@@ -496,10 +496,7 @@ __device__ int xx_partition(const DevGraph &g, const RootCtx &r, int lpX, int c,
 //   * each such C (there are few) is reported unless some row of X_P or X_X contains it: the
 //     lanes test 32 rows at a time, as the pivot scan would.
 // Count mode only (enumeration walks the subtree, so that every clique is written as before).
-#ifndef MCE_SMALL_P
-#define MCE_SMALL_P 8
-#endif
-constexpr int kSmallP = MCE_SMALL_P;   // 0 turns the whole-subtree solver off
+
 
 // kSubsets5[m]: bit t set iff the 5-bit value t is a subset of the 5-bit value m.
 struct Subsets5 {
@@ -785,7 +782,7 @@ __device__ void dfs(const SearchArgs &a, const RootCtx &r, Ck<Geo<W>::CH> P, Ck<
             PROF_START(t_piv);
             const int npop = subwarp_sum<G>(ck_popc<CH>(P));
             if constexpr (G == 1) {
-                if (npop <= kSmallP && a.out.ids == nullptr) {
+                if (npop <= a.small_hi && npop >= a.small_lo && a.out.ids == nullptr) {
                     // the whole subtree at once; no stack entry, so the search backs up next
                     solve_small<W>(a, r, P, XP, lpX, S, L, npop, acc, s_hist, scratch, lane);
                     PROF_ADD(acc, kProfSmall, t_piv);
@@ -1435,11 +1432,9 @@ __device__ __forceinline__ int last_at_most(const int *a, int lo, int hi, int t,
 #define MCE_MIN_BLOCKS_MID 6
 #endif
 // (measured: 2-word rows run best at 7, which leaves them 72 registers instead of 64)
-// W = 0: the merged launch of the normal roots of W = 1, 2 and 4 (planned as W = 4).
 template <int W>
 struct MinBlocks {
-    static constexpr int value =
-        W == 1 ? 8 : (W == 2 ? 7 : (W <= 8 ? MCE_MIN_BLOCKS_MID : 4));
+    static constexpr int value = W == 1 ? 8 : (W == 2 ? 7 : (W <= 8 ? MCE_MIN_BLOCKS_MID : 4));
 };
 
 // First-level subtree of root v (or, with second-level subtrees, the subtree of its edge to w),
@@ -1459,24 +1454,18 @@ __device__ __forceinline__ void search_unit(const SearchArgs &a, unsigned *ws, c
 // One persistent launch per row width W and launch group: the roots of that class, heaviest
 // first, then donated branches of those roots (Section 3.3).  Big: the group of roots whose
 // workspace exceeds kWsCapWords (their build code is compiled into these instances only).
-// W = 0: one launch for the normal roots of W = 4, then 2, then 1 (each root and each donated
-// branch searched with its own row width), so that warps that run out of 4-word roots go on
-// with narrower ones instead of idling until the launch's longest roots end.
 template <int W, bool Big>
 __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(SearchArgs a)
 {
-    static_assert(W != 0 || !Big, "the merged launch takes normal roots only");
     extern __shared__ __align__(16) unsigned char s_raw[];
-    __shared__ unsigned long long s_cls_words[3];     // merged launch: words per row width
     unsigned long long *s_hist = reinterpret_cast<unsigned long long *>(s_raw);
     for (int i = threadIdx.x; i < a.out.hist_len; i += blockDim.x) s_hist[i] = 0ULL;
-    if (threadIdx.x < 3) s_cls_words[threadIdx.x] = 0ULL;
     const int lane = threadIdx.x & 31;
     const int wpb = blockDim.x >> 5;
     const int warp = blockIdx.x * wpb + (threadIdx.x >> 5);
     WarpSmem sm;
     {
-        constexpr int k = W == 1 ? 0 : W == 2 ? 1 : W == 4 || W == 0 ? 2 : W == 8 ? 3 : W == 16 ? 4 : 5;
+        constexpr int k = W == 1 ? 0 : W == 2 ? 1 : W == 4 ? 2 : W == 8 ? 3 : W == 16 ? 4 : 5;
         const size_t hist = ((size_t)(a.out.hist_len + 1) * 8 + 15) & ~(size_t)15;
         unsigned char *mine = s_raw + hist + (size_t)(threadIdx.x >> 5) * warp_smem_bytes(k);
         sm.hkey = reinterpret_cast<int *>(mine);
@@ -1491,7 +1480,7 @@ __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(Search
     __syncthreads();
     unsigned *ws = a.ws + (unsigned long long)warp * a.ws_words;
     const unsigned long long begin = (unsigned long long)a.range[2 * a.group];
-    const int end = a.range[2 * a.group_end + 1];
+    const int end = a.range[2 * a.group + 1];
     // work items: the roots of this launch, or with second-level subtrees their edges
     const int ubase = kL2 ? a.uoff[begin] : 0;
     const unsigned long long n_roots = kL2 ? (unsigned long long)(a.uoff[end] - ubase)
@@ -1535,14 +1524,6 @@ __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(Search
             }
         } else if (np > kMaxP) {
             if (lane == 0) set_status(a.g.ctrl, MCE_ERR_LIMIT);
-        } else if constexpr (W == 0) {
-            const int k = wclass_index(np);
-            if (k == 0) search_unit<1, false>(a, ws, sm, v, w, deg, np, acc, s_hist, lane);
-            else if (k == 1) search_unit<2, false>(a, ws, sm, v, w, deg, np, acc, s_hist, lane);
-            else if (k == 2) search_unit<4, false>(a, ws, sm, v, w, deg, np, acc, s_hist, lane);
-            else if (lane == 0) set_status(a.g.ctrl, MCE_ERR_INTERNAL);
-            if (lane == 0 && k <= 2) atomicAdd(&s_cls_words[k], acc.words);
-            acc.words = 0;
         } else {
             search_unit<W, Big>(a, ws, sm, v, w, deg, np, acc, s_hist, lane);
         }
@@ -1597,32 +1578,19 @@ __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(Search
         if (state != 1) break;
         __syncwarp();
         cuda::atomic_thread_fence(cuda::memory_order_acquire, cuda::thread_scope_device);
-        if constexpr (W == 0) {
-            // the donor's root, and so the row width, is in the inbox header
-            const int k = wclass_index((int)ws[kHdrLayNp]);
-            if (k == 0) search_inbox<1>(a, ws, sm, acc, s_hist, lane);
-            else if (k == 1) search_inbox<2>(a, ws, sm, acc, s_hist, lane);
-            else if (k == 2) search_inbox<4>(a, ws, sm, acc, s_hist, lane);
-            else if (lane == 0) set_status(a.g.ctrl, MCE_ERR_INTERNAL);
-            if (lane == 0 && k <= 2) atomicAdd(&s_cls_words[k], acc.words);
-            acc.words = 0;
-        } else {
-            search_inbox<W>(a, ws, sm, acc, s_hist, lane);
-        }
+        search_inbox<W>(a, ws, sm, acc, s_hist, lane);
         __syncwarp();
         if (lane == 0) busy.fetch_sub(1, cuda::memory_order_acq_rel);
     }
     __syncthreads();
     for (int i = threadIdx.x; i < a.out.hist_len; i += blockDim.x)
         if (s_hist[i]) atomicAdd(&a.out.hist[i], s_hist[i]);
-    if (W == 0 && threadIdx.x < 3 && s_cls_words[threadIdx.x])
-        atomicAdd(&a.g.ctrl->words[threadIdx.x], s_cls_words[threadIdx.x]);
     if (lane == 0) {
         atomicAdd(&a.g.ctrl->result[0], acc.count);
         atomicAdd(&a.g.ctrl->result[1], acc.hash);
         atomicAdd(&a.g.ctrl->tree_nodes, acc.nodes);
         atomicAdd(&a.g.ctrl->donations, acc.donations);
-        if (W != 0) atomicAdd(&a.g.ctrl->words[a.cls], acc.words);
+        atomicAdd(&a.g.ctrl->words[a.cls], acc.words);
 #ifdef MCE_PROFILE
         for (int i = 0; i < 8; ++i) {
             if (i == kProfMaxRoot) atomicMax(&a.g.ctrl->prof[a.cls][i], acc.prof[i]);

@@ -9,7 +9,6 @@ namespace mce {
 const void *search_kernel_partial_l2(int cls, bool big)
 {
     switch (cls) {
-    case -1: return (const void *)search_kernel<0, false>;
     case 0: return big ? (const void *)search_kernel<1, true> : (const void *)search_kernel<1, false>;
     case 1: return big ? (const void *)search_kernel<2, true> : (const void *)search_kernel<2, false>;
     case 2: return big ? (const void *)search_kernel<4, true> : (const void *)search_kernel<4, false>;
