@@ -374,6 +374,8 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
     MCE_ALLOC(h, g.blk_min, (size_t)2 * h->peel_blocks);
     MCE_ALLOC(h, g.blk_cm, (size_t)2 * h->peel_blocks);
     MCE_ALLOC(h, g.blk_rd, (size_t)h->peel_blocks);
+    MCE_ALLOC(h, g.blk_gone, (size_t)2 * h->peel_blocks);
+    MCE_ALLOC(h, g.front, (size_t)kFrontCap);
     if (h->cfg.profile) {
         for (int i = 0; i < 3; ++i) MCE_TRY(cudaEventCreate(&h->ev_order[i]));
         for (int k = 0; k < kNumGroups; ++k) {

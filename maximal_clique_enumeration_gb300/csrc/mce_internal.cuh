@@ -21,6 +21,7 @@ constexpr long long kBigBudgetWords = 256LL << 20;   // workspace of a "big" lau
 constexpr int kScanBlock = 1024;         // elements per CTA of the exclusive scan
 constexpr int kProfSms = 256;            // MCE_PROFILE builds: per-SM load slots per class
 constexpr int kSmallP = 8;               // largest |P| of a search-tree node solved whole
+constexpr int kFrontCap = 4096;          // largest frontier the peel removes without a scan
 
 // Device-resident control block of a handle.
 struct DevCtrl {
@@ -28,9 +29,11 @@ struct DevCtrl {
     int degeneracy;              // peel output
     int rounds;                  // peel output
     long long peel_live;         // peel output: live vertices summed over rounds
-    // peel state handed from the grid-wide rounds to the cluster that runs the last ones
-    int ph_n_alive, ph_k, ph_r, ph_pos, ph_dmax, ph_alive_b;
-    long long ph_live;
+    // peel: frontier appends of the last two scan rounds, and the state a run of frontier
+    // rounds (first CTA alone) hands back to the grid
+    int front_cnt[2];
+    int fr_r, fr_pos, fr_n_alive;
+    long long fr_live_sum, fr_entries;
     int max_pcount;              // max |P| over first-level subtrees
     unsigned int bar_count;      // grid barrier arrivals (grows by the grid size per barrier)
     unsigned int bar_pad;
@@ -77,6 +80,8 @@ struct DevGraph {
     int *alive_a, *alive_b;
     int *blk_cnt, *blk_min, *blk_cm;   // peel per-CTA reports [2][grid]
     long long *blk_rd;                 // peel: adjacency entries removed per CTA [grid]
+    int *blk_gone;                     // peel per-CTA reports: live entries removed [2][grid]
+    int *front;                        // peel: next round's vertices [kFrontCap]
     int ip;           // search over partial induced subgraphs (rows for P only), Section 3.4
     int l2;           // independent second-level subtrees, one per edge (Section 3.2)
     int *unit_cnt;    // l2: subtrees per root, in schedule order (scan input) [n]
