@@ -497,7 +497,7 @@ mce_status mce_create(const int32_t *offsets, const int32_t *adj, int32_t n, int
     // measurement builds only: the solver's |P| range from the environment
     if (const char *e = getenv("MCE_AB_SMALL_LO")) h->small_lo = atoi(e);
     if (const char *e = getenv("MCE_AB_SMALL_HI")) h->small_hi = atoi(e);
-    if (h->small_hi > kSmallP) h->small_hi = kSmallP;
+    if (h->small_hi > kSmallPMax) h->small_hi = kSmallPMax;
 #endif
     mce_status st = create_impl(h, offsets, adj, n, is_device_ptr, (cudaStream_t)stream);
     if (st != MCE_OK) {

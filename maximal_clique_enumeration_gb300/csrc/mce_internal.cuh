@@ -21,6 +21,7 @@ constexpr long long kBigBudgetWords = 256LL << 20;   // workspace of a "big" lau
 constexpr int kScanBlock = 1024;         // elements per CTA of the exclusive scan
 constexpr int kProfSms = 256;            // MCE_PROFILE builds: per-SM load slots per class
 constexpr int kSmallP = 8;               // largest |P| of a search-tree node solved whole
+constexpr int kSmallPMax = 10;           // ... and the most its bit-sliced test allows
 constexpr int kFrontCap = 4096;          // largest frontier the peel removes without a scan
 
 // Device-resident control block of a handle.

@@ -121,7 +121,8 @@ __device__ __forceinline__ int block_excl_scan_int(int v, int *total, int *sh)
 // Each thread holds up to kPeelItems consecutive entries of its CTA's part of the live list.
 constexpr int kPeelItems = 8;
 constexpr int kPeelTile = kPeelThreads * kPeelItems;
-constexpr size_t kPeelSmemBytes = (size_t)(kPeelTile + 2 * kFrontCap) * sizeof(int);
+constexpr size_t kPeelSmemBytes = (size_t)(kPeelTile + 64 + 2 * kFrontCap) * sizeof(int);
+static_assert(2 * kFrontCap + 8 <= kPeelTile + 64, "frontier offsets and bases fit s_front");
 constexpr int kPeelBigDegree = 1024;   // removed vertices this wide are handled by a whole CTA
 constexpr int kPeelBigQueue = 256;     // ... up to this many per round and CTA (then by warps)
 constexpr long long kPeelSoloEntries = 1 << 20;   // and the single-CTA finish needs few edges left
@@ -130,19 +131,35 @@ constexpr long long kPeelSoloEntries = 1 << 20;   // and the single-CTA finish n
 // and appends to front[] each neighbour whose degree falls from k + 1 to k: at level k those
 // are exactly the vertices the next round removes.  A vertex removed earlier, or in this round,
 // already has degree <= k and is never appended.  Appends beyond cap are counted, not stored.
+constexpr int kPeelInFlight = 8;    // neighbours a thread has in flight while removing edges
+
 __device__ __forceinline__ long long remove_edges(const DevGraph &g, int v, int k, int first,
                                                   int stride, int *front, int *front_cnt)
 {
     const int elo = __ldg(g.offs + v), ehi = __ldg(g.offs + v + 1);
-    for (int j = elo + first; j < ehi; j += stride) {
-        const int u = __ldg(g.adj + j);
-        if (atomicSub(&g.deg[u], 1) == k + 1) {
-            const int at = atomicAdd(front_cnt, 1);
-            if (at < kFrontCap) front[at] = u;
+    for (int j0 = elo + first; j0 < ehi; j0 += stride * kPeelInFlight) {
+        int u[kPeelInFlight], old[kPeelInFlight];
+#pragma unroll
+        for (int t = 0; t < kPeelInFlight; ++t) {
+            const int j = j0 + t * stride;
+            u[t] = j < ehi ? __ldg(g.adj + j) : -1;
+        }
+#pragma unroll
+        for (int t = 0; t < kPeelInFlight; ++t) old[t] = u[t] >= 0 ? atomicSub(&g.deg[u[t]], 1) : 0;
+#pragma unroll
+        for (int t = 0; t < kPeelInFlight; ++t) {
+            if (u[t] >= 0 && old[t] == k + 1) {
+                const int at = atomicAdd(front_cnt, 1);
+                if (at < kFrontCap) front[at] = u[t];
+            }
         }
     }
     return ehi - elo;
 }
+
+// Frontier rounds whose vertices have more adjacency entries than this go back to the grid (a
+// scan round at the same level finds the same vertices): one CTA removes them too slowly.
+constexpr int kFrontEdges = 32768;
 
 // Sorts s[0 .. cnt) ascending, cnt <= kFrontCap (s has room for the next power of two):
 // bitonic sort, in one warp's registers up to 32 entries, else by the whole CTA in shared memory.
@@ -211,8 +228,10 @@ __device__ void block_sort(int *s, int cnt)
 __global__ void __launch_bounds__(kPeelThreads, 1) peel_kernel(DevGraph g, long long limit_ns)
 {
     extern __shared__ int s_dyn[];
-    int *s_front = s_dyn;                     // this CTA's removed vertices of a scan round
-    int *s_fa = s_dyn + kPeelTile;            // frontiers of CTA 0 (current, next)
+    // this CTA's removed vertices of a scan round; in frontier rounds, the frontier's entry
+    // offsets (kFrontCap + 1) and adjacency bases (kFrontCap)
+    int *s_front = s_dyn;
+    int *s_fa = s_dyn + kPeelTile + 64;       // frontiers of CTA 0 (current, next)
     int *s_fb = s_fa + kFrontCap;
     __shared__ int sh[32];
     __shared__ int s_rep[4][32];
@@ -506,11 +525,42 @@ __global__ void __launch_bounds__(kPeelThreads, 1) peel_kernel(DevGraph g, long 
             if (tid == 0) s_rd = 0ULL;
             int cnt = fc;
             __syncthreads();
+            // the frontier's adjacency entries, flattened: s_off[i] = entries of cur[0 .. i)
+            int *s_off = s_front, *s_base = s_front + kFrontCap + 8;
             while (true) {
 #ifdef MCE_PROFILE
                 unsigned long long t_fr = globaltimer_ns();
 #endif
                 block_sort(cur, cnt);                       // ends with __syncthreads
+                {
+                    // 4 consecutive frontier entries per thread (cnt <= kFrontCap = 4 * threads)
+                    int d4[4], dsum = 0;
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const int i = tid * 4 + t;
+                        d4[t] = 0;
+                        if (i < cnt) {
+                            const int v = cur[i];
+                            const int lo_v = g.offs[v];
+                            s_base[i] = lo_v;
+                            d4[t] = g.offs[v + 1] - lo_v;
+                        }
+                        dsum += d4[t];
+                    }
+                    int tot;
+                    int run = block_excl_scan_int(dsum, &tot, sh);
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const int i = tid * 4 + t;
+                        if (i < cnt) s_off[i] = run;
+                        run += d4[t];
+                    }
+                    if (tid == 0) s_off[cnt] = tot;
+                }
+                __syncthreads();
+                const int edges = s_off[cnt];
+                // too many edges for one CTA: the grid takes this round (nothing written yet)
+                if (edges > kFrontEdges) break;
                 for (int i = tid; i < cnt; i += nthr) {
                     const int v = cur[i];
                     g.order[pos + i] = v;
@@ -518,10 +568,7 @@ __global__ void __launch_bounds__(kPeelThreads, 1) peel_kernel(DevGraph g, long 
                     g.round_of[v] = r;
                     g.core[v] = k;
                 }
-                if (tid == 0) {
-                    s_fcnt = 0;
-                    s_nbig = 0;
-                }
+                if (tid == 0) s_fcnt = 0;
                 __syncthreads();
 #ifdef MCE_PROFILE
                 if (tid == 0) {
@@ -530,27 +577,41 @@ __global__ void __launch_bounds__(kPeelThreads, 1) peel_kernel(DevGraph g, long 
                     t_fr = now;
                 }
 #endif
-                for (int e = wib; e < cnt; e += wpb) {
-                    const int v = cur[e];
-                    const int deg_v = g.offs[v + 1] - g.offs[v];
-                    if (deg_v >= kPeelBigDegree) {
-                        int slot = 0;
-                        if (lane == 0) slot = atomicAdd(&s_nbig, 1);
-                        slot = __shfl_sync(0xffffffffu, slot, 0);
-                        if (slot < kPeelBigQueue) {
-                            if (lane == 0) s_big[slot] = v;
-                            continue;
+                // every thread takes a contiguous share of the entries, kPeelInFlight at a time
+                {
+                    const int f_begin = (int)((long long)edges * tid / nthr);
+                    const int f_end = (int)((long long)edges * (tid + 1) / nthr);
+                    int lo_i = 0, hi_i = cnt;                  // owner of f_begin: last i with
+                    while (hi_i - lo_i > 1) {                  // s_off[i] <= f_begin
+                        const int mid = (lo_i + hi_i) >> 1;
+                        if (s_off[mid] <= f_begin) lo_i = mid;
+                        else hi_i = mid;
+                    }
+                    int own = lo_i;
+                    for (int f0 = f_begin; f0 < f_end; f0 += kPeelInFlight) {
+                        int u[kPeelInFlight], old[kPeelInFlight];
+#pragma unroll
+                        for (int t = 0; t < kPeelInFlight; ++t) {
+                            const int f = f0 + t;
+                            u[t] = -1;
+                            if (f < f_end) {
+                                while (s_off[own + 1] <= f) ++own;
+                                u[t] = __ldg(g.adj + s_base[own] + (f - s_off[own]));
+                            }
+                        }
+#pragma unroll
+                        for (int t = 0; t < kPeelInFlight; ++t)
+                            old[t] = u[t] >= 0 ? atomicSub(&g.deg[u[t]], 1) : 0;
+#pragma unroll
+                        for (int t = 0; t < kPeelInFlight; ++t) {
+                            if (u[t] >= 0 && old[t] == k + 1) {
+                                const int at = atomicAdd(&s_fcnt, 1);
+                                if (at < kFrontCap) nxt[at] = u[t];
+                            }
                         }
                     }
-                    remove_edges(g, v, k, lane, 32, nxt, &s_fcnt);
-                    if (lane == 0) atomicAdd(&s_rd, (unsigned long long)deg_v);
                 }
-                __syncthreads();
-                const int nbig = min(s_nbig, kPeelBigQueue);
-                for (int i = 0; i < nbig; ++i) {
-                    const long long dv = remove_edges(g, s_big[i], k, tid, nthr, nxt, &s_fcnt);
-                    if (tid == 0) atomicAdd(&s_rd, (unsigned long long)dv);
-                }
+                if (tid == 0) s_rd += (unsigned long long)edges;
                 __syncthreads();
                 const int next = s_fcnt;
                 live_sum += cnt;

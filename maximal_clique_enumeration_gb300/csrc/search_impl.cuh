@@ -491,10 +491,11 @@ __device__ int xx_partition(const DevGraph &g, const RootCtx &r, int lpX, int c,
 //   * P's members p_0 .. p_{k-1} (ascending) renumber the node's columns; N_i is the closed
 //     neighbourhood of p_i inside P, as a k-bit mask;
 //   * C is a maximal clique of G[P] iff, for every i < k, C is a subset of N_i exactly when i is
-//     in C; the 256 subsets are bit-sliced over lanes 0-7 (lane l holds subsets
+//     in C; the 2^k subsets are bit-sliced over the lanes (lane l holds subsets
 //     32 l .. 32 l + 31), so each of the k tests is a handful of word operations;
-//   * each such C (there are few) is reported unless some row of X_P or X_X contains it: the
-//     lanes test 32 rows at a time, as the pivot scan would.
+//   * each such C (there are few) is reported unless some vertex of X is adjacent to all of it:
+//     for X_P that is one AND of C's own rows (the rows are symmetric on the columns of P), for
+//     X_X the lanes test 32 rows at a time, as the pivot scan would.
 // Count mode only (enumeration walks the subtree, so that every clique is written as before).
 
 
@@ -513,10 +514,11 @@ struct Subsets5 {
 };
 __constant__ Subsets5 kSubsets5 = Subsets5();
 
-// Subsets C (of 8 bits) that lane l's word holds, C = 32 l + t: the bits t with C a subset of m.
+// Subsets C (of up to 10 bits) that lane l's word holds, C = 32 l + t: the bits t with C a
+// subset of m.
 __device__ __forceinline__ unsigned subsets_of(unsigned m, int lane)
 {
-    return kSubsets5.v[m & 31u] & ((((unsigned)lane & ~(m >> 5)) & 7u) ? 0u : 0xffffffffu);
+    return kSubsets5.v[m & 31u] & ((((unsigned)lane & ~(m >> 5)) & 31u) ? 0u : 0xffffffffu);
 }
 
 // The same word's subsets that contain element i.
@@ -548,14 +550,14 @@ __device__ __forceinline__ unsigned gather_bits(const Ck<W> &v, const Ck<W> &m)
 }
 
 // Reports every maximal clique below the node (R, P, X_P u X_X) at level L, |P| = k <= kSmallP
-// (rows of whole words per lane, W <= 4).  scratch: 24 words of the warp's shared memory.
+// (rows of whole words per lane, W <= 4).  scratch: 36 words of the warp's shared memory.
 template <int W>
 __device__ void solve_small(const SearchArgs &a, const RootCtx &r, const Ck<W> &P,
                             const Ck<W> &XP, int lpX, unsigned long long S, int L, int k,
                             Acc &acc, unsigned long long *s_hist, unsigned *scratch, int lane)
 {
     int *mem = reinterpret_cast<int *>(scratch);                          // columns of P
-    unsigned long long *keys = reinterpret_cast<unsigned long long *>(scratch + 8);
+    unsigned long long *keys = reinterpret_cast<unsigned long long *>(scratch + 16);
     // lane j < k: the column of p_j (the j-th member of P, ascending)
     int my_p = 0;
     {
@@ -583,12 +585,9 @@ __device__ void solve_small(const SearchArgs &a, const RootCtx &r, const Ck<W> &
         const unsigned ni = __shfl_sync(kFull, adj, i) | (1u << i);
         V &= ~(subsets_of(ni, lane) ^ subsets_with(i, lane));
     }
-    if (lane >= 8) V = 0u;
-    // X: the members of X_P (their rows are P rows), then the live X_X rows
-    const int nxp = list_bits<W>(XP, r.plist, lane);          // ends with __syncwarp
-    const int nx = nxp + lpX;
+    __syncwarp();                                             // mem[], keys[] written
     const int rsize = r.rsize + L;
-    unsigned long long words = (unsigned long long)k * W + 8ULL * (unsigned)k;
+    unsigned long long words = (unsigned long long)k * W + (unsigned long long)k * ((1u << k) + 31u) / 32u;
     unsigned cand = __ballot_sync(kFull, V != 0u);
     while (cand) {
         // the next candidate C (the same in every lane), as a set of columns
@@ -597,25 +596,29 @@ __device__ void solve_small(const SearchArgs &a, const RootCtx &r, const Ck<W> &
         const unsigned C = (unsigned)src * 32u + (unsigned)(__ffs(vs) - 1);
         if (lane == src) V &= V - 1u;
         cand = __ballot_sync(kFull, V != 0u);
-        Ck<W> cb = ck_zero<W>();
+        // C as columns, and the columns adjacent to every member of C (rows are symmetric on
+        // the columns of P, so X_P's members adjacent to all of C are XP & AND of C's rows)
+        Ck<W> cb = ck_zero<W>(), common;
+#pragma unroll
+        for (int w = 0; w < W; ++w) common.w[w] = 0xffffffffu;
         unsigned long long sum = S;
         for (unsigned cm = C; cm; cm &= cm - 1u) {
             const int j = __ffs(cm) - 1;
             const int col = mem[j];
 #pragma unroll
             for (int w = 0; w < W; ++w) cb.w[w] |= (col >> 5) == w ? 1u << (col & 31) : 0u;
+            common = ck_and<W>(common, ck_load<W>(r.rowsP + (long long)col * W));
             sum += keys[j];
         }
-        // extended by a vertex of X: some X row containing all of C
-        bool dominated = false;
-        for (int base = 0; base < nx && !dominated; base += 32) {
+        words += (unsigned long long)__popc(C) * W;
+        // extended by a vertex of X: a member of X_P adjacent to all of C, or an X_X row
+        // containing all of C
+        bool dominated = ck_nonzero<W>(ck_and<W>(XP, common));
+        for (int base = 0; base < lpX && !dominated; base += 32) {
             const int t = base + lane;
             bool hit = false;
-            if (t < nxp) {
-                const Ck<W> rc = ck_load<W>(r.rowsP + (long long)r.plist[t] * W);
-                hit = !ck_nonzero<W>(ck_andnot<W>(cb, rc));
-            } else if (t < nx) {
-                const int x = r.xx[t - nxp];
+            if (t < lpX) {
+                const int x = r.xx[t];
                 if constexpr (kIP) {
                     hit = true;
                     const int xid = r.xids[x];
@@ -627,7 +630,7 @@ __device__ void solve_small(const SearchArgs &a, const RootCtx &r, const Ck<W> &
                 }
             }
             dominated = __any_sync(kFull, hit);
-            words += (unsigned long long)W * (unsigned)min(32, nx - base);
+            words += (unsigned long long)W * (unsigned)min(32, lpX - base);
         }
         if (dominated) continue;
         const int size = rsize + __popc(C);
