@@ -465,15 +465,17 @@ def activity_child(args):
     info = h.get_info()
     prof = h.profile()
     n_sms = torch.cuda.get_device_properties(0).multi_processor_count
-    acts = ["build", "pivot", "child", "partition", "donate", "idle"]
+    acts = ["split", "build", "pivot", "small", "child", "partition", "donate", "idle"]
+    sub = ["hash", "walk", "xlist"]
     res = {"ms_search": info["ms_search"], "workers": info["workers"], "n_sms": n_sms}
     for k in range(6):
         p = prof[1 << k]
         tot = sum(p[a] for a in acts)
         if tot == 0:
             continue
-        res[str(1 << k)] = {"cycles": {a: int(p[a]) for a in acts},
+        res[str(1 << k)] = {"cycles": {a: int(p[a]) for a in acts + sub},
                             "share": {a: p[a] / tot for a in acts},
+                            "build_parts_share": {a: p[a] / max(p["build"], 1) for a in sub},
                             "roots": int(p["roots"]), "slowest_root_cycles": int(p["max_root"]),
                             "sm_load": _load_stats(p["sm_busy"], n_sms)}
     h.close()
@@ -646,7 +648,8 @@ def run_gb300(args, rank, world, local):
             a = act.get(str(1 << c)) if isinstance(act, dict) else None
             if not a or not act["workers"][c]:
                 continue
-            build_ms += a["cycles"]["build"] / (mhz * 1e3) / act["workers"][c]
+            build_ms += (a["cycles"]["build"] + a["cycles"]["split"]) / (mhz * 1e3) \
+                / act["workers"][c]
             build_bytes += sb["build_by_width"][c]
         if build_ms > 0:
             stages["build"] = dict(_gbs(build_bytes, build_ms, hbm),

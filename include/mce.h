@@ -219,18 +219,20 @@ mce_status mce_get_order(mce_graph *g, void *stream, int32_t *d_rank, int32_t *d
 /*
  * Activity profile of the last search (diagnostics).  Only a library built with MCE_PROFILE
  * defined collects it (the normal build leaves it zero): SM clock cycles summed over warps, per
- * row-width class k, at out[k * 8 + a] for activity a = 0 subtree build, 1 pivot selection,
- * 2 child sets and leaf checks, 3 X_X partition, 4 donation, 5 waiting in the worker list,
- * 6 the slowest single first-level root, 7 number of roots.  Section 4.5 of the pages breaks
+ * row-width class k, at out[k * 16 + a] for activity a = 0 subtree build (rows and X_X list),
+ * 1 pivot selection, 2 child sets and leaf checks, 3 X_X partition, 4 donation, 5 waiting in the
+ * worker list, 6 the slowest single first-level root, 7 number of roots, 8 small subtrees solved
+ * whole, 9 split of N(v) into P and X, and inside a = 0: 10 hash and row set-up, 11 the walk of
+ * the later-neighbour lists, 12 the X_X list and vertex keys.  Section 4.5 of the pages breaks
  * execution time down the same way from per-block SM clocks.  Then 16 values for the last
- * ordering, as seen by its first CTA, in nanoseconds: out[48 + p] for rounds run by all CTAs and
- * out[56 + p] for rounds run by one CTA, phase p = 0 scan, 1 report exchange, 2 decide and
- * write, 3 edge removal, 4 end-of-round barrier, 5 number of rounds; out[54] is the largest
+ * ordering, as seen by its first CTA, in nanoseconds: out[96 + p] for rounds run by all CTAs and
+ * out[104 + p] for rounds run by one CTA, phase p = 0 scan, 1 report exchange, 2 decide and
+ * write, 3 edge removal, 4 end-of-round barrier, 5 number of rounds; out[102] is the largest
  * degree of a vertex removed by the first CTA.  Then, per row-width class k, the load of every
  * SM in the last search (Section 4.3 judges the worker list by per-block loads): at
- * out[64 + k * 256 + s] the SM clock cycles that warps on SM s spent holding work (time in the
+ * out[112 + k * 256 + s] the SM clock cycles that warps on SM s spent holding work (time in the
  * kernel minus time waiting in the worker list), for s < 256.
- *   out  host uint64[8 * MCE_NUM_WIDTHS + 16 + 256 * MCE_NUM_WIDTHS].  Synchronises the device.
+ *   out  host uint64[16 * MCE_NUM_WIDTHS + 16 + 256 * MCE_NUM_WIDTHS].  Synchronises the device.
  */
 mce_status mce_get_profile(mce_graph *g, uint64_t *out);
 

@@ -29,7 +29,8 @@ EXPORTS = ["mce_config_default", "mce_create", "mce_order", "mce_count", "mce_co
            "mce_destroy", "mce_status_str", "mce_order_noalloc", "mce_enumerate_roots",
            "mce_trim_memory"]
 PROFILE_ACTIVITIES = ["build", "pivot", "child", "partition", "donate", "idle", "max_root",
-                      "roots"]
+                      "roots", "small", "split", "hash", "walk", "xlist"]
+PROF_SLOTS = 16
 
 
 class MceError(RuntimeError):
@@ -206,13 +207,14 @@ class Graph:
 
     def profile(self) -> dict:
         """Per row width: cycles per activity of the last search (MCE_PROFILE builds only)."""
-        out = np.zeros(8 * NUM_WIDTHS + 16 + PROF_SMS * NUM_WIDTHS, np.uint64)
+        out = np.zeros(PROF_SLOTS * NUM_WIDTHS + 16 + PROF_SMS * NUM_WIDTHS, np.uint64)
         _check(library().mce_get_profile(self._h, out.ctypes.data_as(ctypes.c_void_p)),
                "mce_get_profile")
-        res = {1 << k: dict(zip(PROFILE_ACTIVITIES, (int(x) for x in out[8 * k: 8 * k + 8])))
+        res = {1 << k: dict(zip(PROFILE_ACTIVITIES,
+                                (int(x) for x in out[PROF_SLOTS * k: PROF_SLOTS * k + 13])))
                for k in range(NUM_WIDTHS)}
         phases = ["scan_ns", "exchange_ns", "write_ns", "edges_ns", "barrier_ns", "rounds"]
-        base = 8 * NUM_WIDTHS
+        base = PROF_SLOTS * NUM_WIDTHS
         res["peel"] = {"multi": dict(zip(phases, (int(x) for x in out[base: base + 6]))),
                        "single": dict(zip(phases, (int(x) for x in out[base + 8: base + 14]))),
                        "max_removed_degree": int(out[base + 6])}

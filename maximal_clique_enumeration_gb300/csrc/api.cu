@@ -374,8 +374,6 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
     MCE_ALLOC(h, g.blk_min, (size_t)2 * h->peel_blocks);
     MCE_ALLOC(h, g.blk_cm, (size_t)2 * h->peel_blocks);
     MCE_ALLOC(h, g.blk_rd, (size_t)h->peel_blocks);
-    MCE_ALLOC(h, g.blk_gone, (size_t)2 * h->peel_blocks);
-    MCE_ALLOC(h, g.front, (size_t)kFrontCap);
     if (h->cfg.profile) {
         for (int i = 0; i < 3; ++i) MCE_TRY(cudaEventCreate(&h->ev_order[i]));
         for (int k = 0; k < kNumGroups; ++k) {
@@ -761,9 +759,9 @@ mce_status mce_get_profile(mce_graph *h, uint64_t *out)
     if (!h || !out) return MCE_ERR_INVALID_ARG;
     MCE_TRY(cudaDeviceSynchronize());
     MCE_TRY(cudaMemcpy(out, h->g.ctrl->prof, sizeof(h->g.ctrl->prof), cudaMemcpyDeviceToHost));
-    MCE_TRY(cudaMemcpy(out + 8 * kNumClasses, h->g.ctrl->peel_prof, sizeof(h->g.ctrl->peel_prof),
-                       cudaMemcpyDeviceToHost));
-    MCE_TRY(cudaMemcpy(out + 8 * kNumClasses + 16, h->g.prof_sm,
+    MCE_TRY(cudaMemcpy(out + kProfSlots * kNumClasses, h->g.ctrl->peel_prof,
+                       sizeof(h->g.ctrl->peel_prof), cudaMemcpyDeviceToHost));
+    MCE_TRY(cudaMemcpy(out + kProfSlots * kNumClasses + 16, h->g.prof_sm,
                        sizeof(unsigned long long) * kNumClasses * kProfSms,
                        cudaMemcpyDeviceToHost));
     return MCE_OK;

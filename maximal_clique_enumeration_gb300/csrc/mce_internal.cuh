@@ -20,9 +20,9 @@ constexpr long long kWsCapWords = 16384;     // workspace per warp of a "normal"
 constexpr long long kBigBudgetWords = 256LL << 20;   // workspace of a "big" launch (1 GiB)
 constexpr int kScanBlock = 1024;         // elements per CTA of the exclusive scan
 constexpr int kProfSms = 256;            // MCE_PROFILE builds: per-SM load slots per class
-constexpr int kSmallP = 8;               // largest |P| of a search-tree node solved whole
+constexpr int kProfSlots = 16;           // MCE_PROFILE builds: activity counters per class
+constexpr int kSmallP = 10;              // largest |P| of a search-tree node solved whole
 constexpr int kSmallPMax = 10;           // ... and the most its bit-sliced test allows
-constexpr int kFrontCap = 4096;          // largest frontier the peel removes without a scan
 
 // Device-resident control block of a handle.
 struct DevCtrl {
@@ -30,11 +30,6 @@ struct DevCtrl {
     int degeneracy;              // peel output
     int rounds;                  // peel output
     long long peel_live;         // peel output: live vertices summed over rounds
-    // peel: frontier appends of the last two scan rounds, and the state a run of frontier
-    // rounds (first CTA alone) hands back to the grid
-    int front_cnt[2];
-    int fr_r, fr_pos, fr_n_alive;
-    long long fr_live_sum, fr_entries;
     int max_pcount;              // max |P| over first-level subtrees
     unsigned int bar_count;      // grid barrier arrivals (grows by the grid size per barrier)
     unsigned int bar_pad;
@@ -54,7 +49,7 @@ struct DevCtrl {
     unsigned long long donations;
     unsigned long long result[2];  // count, hash of the last search
     unsigned long long words[kNumClasses];  // bitset words processed per row-width class
-    unsigned long long prof[kNumClasses][8];  // MCE_PROFILE builds: cycles per activity
+    unsigned long long prof[kNumClasses][kProfSlots];  // MCE_PROFILE builds: cycles per activity
     unsigned long long peel_prof[16];         // MCE_PROFILE builds: peel phases (ns, CTA 0)
     // first-level roots in launch groups g = 2k + b (row width W = 1 << k; b = 0: roots
     // whose workspace exceeds kWsCapWords, b = 1: the others): sched[cls[2g] .. cls[2g+1])
@@ -81,8 +76,6 @@ struct DevGraph {
     int *alive_a, *alive_b;
     int *blk_cnt, *blk_min, *blk_cm;   // peel per-CTA reports [2][grid]
     long long *blk_rd;                 // peel: adjacency entries removed per CTA [grid]
-    int *blk_gone;                     // peel per-CTA reports: live entries removed [2][grid]
-    int *front;                        // peel: next round's vertices [kFrontCap]
     int ip;           // search over partial induced subgraphs (rows for P only), Section 3.4
     int l2;           // independent second-level subtrees, one per edge (Section 3.2)
     int *unit_cnt;    // l2: subtrees per root, in schedule order (scan input) [n]
@@ -216,6 +209,8 @@ cudaError_t launch_ingest_validate(const DevGraph &g, const int *d_big_list, int
 // ev_peel (may be null) is recorded on s between the peel and the orientation kernels.
 cudaError_t launch_order(const DevGraph &g, int peel_blocks, long long spin_limit_ns,
                          cudaStream_t s, cudaEvent_t ev_peel);
+cudaError_t launch_peel(const DevGraph &g, int peel_blocks, long long spin_limit_ns,
+                        cudaStream_t s);
 cudaError_t launch_search(const SearchArgs &a, int blocks, int threads, size_t smem,
                           cudaStream_t s);
 cudaError_t launch_search_prep(const SearchArgs &a, cudaStream_t s);

@@ -8,19 +8,16 @@
 // its core number is the level at which it was removed.  Every vertex then has at most d
 // later neighbours, d being the degeneracy (largest level).
 //
-// The remaining vertices stay in an id-ordered list that is compacted stably in every round that
-// scans it, so that round's removals come out already in id order.  Most rounds need no scan at
-// all: at level k, a round that does not raise the level removes exactly the vertices whose
-// degree fell to k during the round before, which that round's edge removal collects.  One
-// cooperative kernel runs the peel: scan rounds over the whole GPU with two grid-wide barriers,
-// runs of such frontier rounds on one CTA in between.  Every barrier wait is bounded by
-// spin_limit_ns.
+// One cooperative kernel runs all rounds: the remaining vertices stay in an id-ordered list
+// that is compacted stably every round, so each round's removals come out already in id
+// order and the order needs no sort.  Two grid-wide barriers separate the phases of a round;
+// once at most kPeelSoloVertices vertices remain, CTA 0 finishes alone with CTA barriers.
+// Every barrier wait is bounded by spin_limit_ns.
 //
 // Then small kernels count every vertex's later neighbours |P| (Algorithm 3's P), count the
 // isolated vertices, bucket the first-level roots by |P|, heaviest first, and store the
 // later-neighbour lists N+(v) as a CSR (scan of |P|, then a stable split of each adjacency).
 #include <climits>
-#include <cstdlib>
 
 #include <cuda/atomic>
 
@@ -120,315 +117,188 @@ __device__ __forceinline__ int block_excl_scan_int(int v, int *total, int *sh)
 
 // Each thread holds up to kPeelItems consecutive entries of its CTA's part of the live list.
 constexpr int kPeelItems = 8;
-constexpr int kPeelTile = kPeelThreads * kPeelItems;
-constexpr size_t kPeelSmemBytes = (size_t)(kPeelTile + 64 + 2 * kFrontCap) * sizeof(int);
-static_assert(2 * kFrontCap + 8 <= kPeelTile + 64, "frontier offsets and bases fit s_front");
 constexpr int kPeelBigDegree = 1024;   // removed vertices this wide are handled by a whole CTA
 constexpr int kPeelBigQueue = 256;     // ... up to this many per round and CTA (then by warps)
 constexpr long long kPeelSoloEntries = 1 << 20;   // and the single-CTA finish needs few edges left
 
-// Subtracts one from the degree of every neighbour of v (threads first, first + stride, ...),
-// and appends to front[] each neighbour whose degree falls from k + 1 to k: at level k those
-// are exactly the vertices the next round removes.  A vertex removed earlier, or in this round,
-// already has degree <= k and is never appended.  Appends beyond cap are counted, not stored.
-constexpr int kPeelInFlight = 8;    // neighbours a thread has in flight while removing edges
-
-__device__ __forceinline__ long long remove_edges(const DevGraph &g, int v, int k, int first,
-                                                  int stride, int *front, int *front_cnt)
-{
-    const int elo = __ldg(g.offs + v), ehi = __ldg(g.offs + v + 1);
-    for (int j0 = elo + first; j0 < ehi; j0 += stride * kPeelInFlight) {
-        int u[kPeelInFlight], old[kPeelInFlight];
-#pragma unroll
-        for (int t = 0; t < kPeelInFlight; ++t) {
-            const int j = j0 + t * stride;
-            u[t] = j < ehi ? __ldg(g.adj + j) : -1;
-        }
-#pragma unroll
-        for (int t = 0; t < kPeelInFlight; ++t) old[t] = u[t] >= 0 ? atomicSub(&g.deg[u[t]], 1) : 0;
-#pragma unroll
-        for (int t = 0; t < kPeelInFlight; ++t) {
-            if (u[t] >= 0 && old[t] == k + 1) {
-                const int at = atomicAdd(front_cnt, 1);
-                if (at < kFrontCap) front[at] = u[t];
-            }
-        }
-    }
-    return ehi - elo;
-}
-
-// Frontier rounds whose vertices have more adjacency entries than this go back to the grid (a
-// scan round at the same level finds the same vertices): one CTA removes them too slowly.
-constexpr int kFrontEdges = 32768;
-
-// Sorts s[0 .. cnt) ascending, cnt <= kFrontCap (s has room for the next power of two):
-// bitonic sort, in one warp's registers up to 32 entries, else by the whole CTA in shared memory.
-__device__ void block_sort(int *s, int cnt)
-{
-    const int lane = threadIdx.x & 31;
-    if (cnt <= 32) {
-        if (threadIdx.x < 32) {
-            int x = lane < cnt ? s[lane] : INT_MAX;
-#pragma unroll
-            for (int kk = 2; kk <= 32; kk <<= 1) {
-#pragma unroll
-                for (int j = kk >> 1; j > 0; j >>= 1) {
-                    const int y = __shfl_xor_sync(0xffffffffu, x, j);
-                    const bool take_min = ((lane & j) == 0) == ((lane & kk) == 0);
-                    x = take_min ? min(x, y) : max(x, y);
-                }
-            }
-            if (lane < cnt) s[lane] = x;
-        }
-        __syncthreads();
-        return;
-    }
-    int p2 = 64;
-    while (p2 < cnt) p2 <<= 1;
-    for (int i = cnt + (int)threadIdx.x; i < p2; i += blockDim.x) s[i] = INT_MAX;
-    __syncthreads();
-    for (int kk = 2; kk <= p2; kk <<= 1) {
-        for (int j = kk >> 1; j > 0; j >>= 1) {
-            for (int i = threadIdx.x; i < p2; i += blockDim.x) {
-                const int ixj = i ^ j;
-                if (ixj > i) {
-                    const int a = s[i], b = s[ixj];
-                    if ((a > b) == ((i & kk) == 0)) {
-                        s[i] = b;
-                        s[ixj] = a;
-                    }
-                }
-            }
-            __syncthreads();
-        }
-    }
-}
-
-// The canonical peel (see the top of this file), in one cooperative kernel with two kinds of
-// round:
-//   scan round (all CTAs; the first round, every round that raises the level, and every round
-//   whose vertex set did not fit a frontier) -- a CTA owns live[lo, hi):
-//     scan   -- load ids, current degrees and removal marks once (kept in registers across the
-//               exchange) and report (#deg <= k, least degree above k, #vertices at that degree,
-//               #entries removed since the last compaction);
-//     decide -- from every CTA's report: if some vertex has deg <= k the round removes those,
-//               else the level rises to the least degree d' and the round removes deg == d';
-//     write  -- stable compaction: removed vertices get their rank (round, id order), round and
-//               core number; survivors go to the next live list;
-//     remove -- the CTA subtracts one degree from every neighbour of its own removed vertices,
-//               collecting the vertices whose degree falls to the level (the next frontier);
-//   frontier rounds (CTA 0 alone, while the other CTAs wait at the next grid barrier) -- at
-//   level k a round that does not raise the level removes exactly the vertices that fell to k
-//   in the round before, so as long as they fit in shared memory the round needs no scan: the
-//   frontier is sorted by id (ranks are (round, id)), its vertices written, their edges removed
-//   (collecting the next frontier).  Most rounds of a peel are of this kind.
-// Grid barriers: after the scan (reports) and after the removal (degrees, next live list), and
-// one after each run of frontier rounds.  Once few vertices and few edges remain, CTA 0 goes on
-// alone (CTA barriers only).
+// One round of the peel, in a CTA that owns live[lo, hi):
+//   scan   -- load ids and current degrees once (kept in registers across the exchange) and
+//             report (#deg <= k, least degree above k, #vertices at that degree);
+//   decide -- from every CTA's report: if some vertex has deg <= k the round removes those,
+//             else the level rises to the least degree d' and the round removes deg == d';
+//   write  -- stable compaction: removed vertices get their rank (round, id order), round and
+//             core number; survivors go to the next live list;
+//   remove -- the CTA subtracts one degree from every neighbour of its own removed vertices
+//             (degrees of vertices already removed are never read again).
+// Grid barriers: after the scan (reports) and after the removal (degrees, next live list).
 __global__ void __launch_bounds__(kPeelThreads, 1) peel_kernel(DevGraph g, long long limit_ns)
 {
-    extern __shared__ int s_dyn[];
-    // this CTA's removed vertices of a scan round; in frontier rounds, the frontier's entry
-    // offsets (kFrontCap + 1) and adjacency bases (kFrontCap)
-    int *s_front = s_dyn;
-    int *s_fa = s_dyn + kPeelTile + 64;       // frontiers of CTA 0 (current, next)
-    int *s_fb = s_fa + kFrontCap;
     __shared__ int sh[32];
-    __shared__ int s_rep[4][32];
-    __shared__ int s_dec[4];
-    __shared__ int s_glob[5];
-    __shared__ int s_big[kPeelBigQueue];
-    __shared__ int s_nbig, s_fcnt;
-    __shared__ unsigned long long s_rd;       // adjacency entries removed (this CTA)
-    __shared__ long long s_removed;
     const int tid = threadIdx.x, nthr = blockDim.x;
     const int lane = tid & 31, wib = tid >> 5, wpb = nthr >> 5;
     const int n = g.n;
-    DevCtrl *c = g.ctrl;
     for (int v = blockIdx.x * nthr + tid; v < n; v += gridDim.x * nthr) {
         g.deg[v] = g.offs[v + 1] - g.offs[v];
         g.round_of[v] = -1;
         g.alive_a[v] = v;
     }
-    if (blockIdx.x == 0 && tid == 0) {
-        c->front_cnt[0] = 0;
-        c->front_cnt[1] = 0;
-    }
-    if (!grid_barrier(c, limit_ns)) return;
+    if (!grid_barrier(g.ctrl, limit_ns)) return;
 
     int *alive = g.alive_a, *alive_next = g.alive_b;
-    int n_live = n;     // entries of the live list (frontier rounds remove without compacting)
-    int n_alive = n;    // vertices not removed yet
-    int k = 0, r = 0, pos = 0, phase = 0, dmax = 0, scans = 0;
+    int n_alive = n, k = 0, r = 0, pos = 0, phase = 0, dmax = 0;
     // adjacency entries of the remaining vertices, read from the offsets themselves (callers of
     // the allocation-free entry point pass no edge count)
     long long live_entries = n > 0 ? (long long)g.offs[n] - (long long)g.offs[0] : 0;
-    long long live_sum = 0;   // live-list entries scanned plus frontier vertices, over rounds
+    long long live_sum = 0;           // live vertices summed over rounds (CTA 0 keeps it)
     bool solo = false;
     int nb = gridDim.x, b = blockIdx.x;
+    const int tile = nthr * kPeelItems;
+    __shared__ long long s_removed;
     while (n_alive > 0) {
-        // ======================================================== scan round
+        if (!solo && r > 0) {
+            // every CTA learns how many adjacency entries the last round removed
+            if (wib == 0) {
+                long long t = 0;
+                for (int i = lane; i < nb; i += 32) t += g.blk_rd[i];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+                if (lane == 0) s_removed = t;
+            }
+            __syncthreads();
+            live_entries -= s_removed;
+        }
         // one CTA finishes once few vertices and few edges remain (a dense core keeps the grid)
-        if (!solo && n_live <= kPeelSoloVertices && live_entries <= kPeelSoloEntries) {
+        if (!solo && n_alive <= kPeelSoloVertices && live_entries <= kPeelSoloEntries) {
             if (blockIdx.x != 0) return;
             solo = true;
             nb = 1;
             b = 0;
         }
         PEEL_MARK(t_ph);
-        int *front_cnt = &c->front_cnt[scans & 1];
-        const int chunk = (n_live + nb - 1) / nb;
-        const int lo = min(b * chunk, n_live), hi = min(lo + chunk, n_live);
-        const bool in_regs = chunk <= kPeelTile;   // the same in every CTA
+        const int chunk = (n_alive + nb - 1) / nb;
+        const int lo = min(b * chunk, n_alive), hi = min(lo + chunk, n_alive);
+        const bool in_regs = chunk <= tile;        // the same in every CTA
         int vid[kPeelItems], vdg[kPeelItems];
-        // -- scan (an entry removed by a frontier round gets vdg = -1)
-        int cnt_le = 0, mmin = INT_MAX, cnt_m = 0, cnt_gone = 0;
-        for (int t0 = lo; t0 < hi; t0 += kPeelTile) {
+        // -- scan
+        int cnt_le = 0, mmin = INT_MAX, cnt_m = 0;
+        for (int t0 = lo; t0 < hi; t0 += tile) {
 #pragma unroll
             for (int j = 0; j < kPeelItems; ++j) {
                 const int i = t0 + tid * kPeelItems + j;
                 vid[j] = i < hi ? alive[i] : -1;
             }
 #pragma unroll
-            for (int j = 0; j < kPeelItems; ++j) {
-                if (vid[j] < 0) {
-                    vdg[j] = INT_MAX;
-                    continue;
-                }
-                const int d = g.deg[vid[j]], gone = g.round_of[vid[j]];
-                vdg[j] = gone >= 0 ? -1 : d;
-            }
+            for (int j = 0; j < kPeelItems; ++j) vdg[j] = vid[j] >= 0 ? g.deg[vid[j]] : INT_MAX;
 #pragma unroll
             for (int j = 0; j < kPeelItems; ++j) {
                 const int d = vdg[j];
                 if (vid[j] < 0) continue;
-                if (d < 0) ++cnt_gone;
-                else if (d <= k) ++cnt_le;
+                if (d <= k) ++cnt_le;
                 else if (d < mmin) { mmin = d; cnt_m = 1; }
                 else if (d == mmin) ++cnt_m;
             }
         }
-        // CTA report in one exchange: (#deg <= k, least degree above k, #at that degree, #gone)
+        // CTA report in one exchange: (#deg <= k, least degree above k, #at that degree)
+        __shared__ int s_rep[3][32];
+        __shared__ int s_dec[3];
         {
             const int wle = __reduce_add_sync(0xffffffffu, cnt_le);
             const int wmin = __reduce_min_sync(0xffffffffu, mmin);
             const int wcm = __reduce_add_sync(0xffffffffu, mmin == wmin ? cnt_m : 0);
-            const int wgo = __reduce_add_sync(0xffffffffu, cnt_gone);
-            if (lane == 0) {
-                s_rep[0][wib] = wle;
-                s_rep[1][wib] = wmin;
-                s_rep[2][wib] = wcm;
-                s_rep[3][wib] = wgo;
-            }
+            if (lane == 0) { s_rep[0][wib] = wle; s_rep[1][wib] = wmin; s_rep[2][wib] = wcm; }
             __syncthreads();
             if (wib == 0) {
                 const int a0 = lane < wpb ? s_rep[0][lane] : 0;
                 const int a1 = lane < wpb ? s_rep[1][lane] : INT_MAX;
                 const int a2 = lane < wpb ? s_rep[2][lane] : 0;
-                const int a3 = lane < wpb ? s_rep[3][lane] : 0;
                 const int bm = __reduce_min_sync(0xffffffffu, a1);
                 const int t_le = __reduce_add_sync(0xffffffffu, a0);
                 const int t_cm = __reduce_add_sync(0xffffffffu, a1 == bm ? a2 : 0);
-                const int t_go = __reduce_add_sync(0xffffffffu, a3);
-                if (lane == 0) { s_dec[0] = t_le; s_dec[1] = bm; s_dec[2] = t_cm; s_dec[3] = t_go; }
+                if (lane == 0) { s_dec[0] = t_le; s_dec[1] = bm; s_dec[2] = t_cm; }
             }
             __syncthreads();
         }
         cnt_le = s_dec[0];
         const int bmin = s_dec[1];
         cnt_m = s_dec[2];
-        cnt_gone = s_dec[3];
         PEEL_ADD(0, t_ph);
         // -- decide (identically in every CTA)
-        int total, prefix, newk, total_gone, prefix_gone;
+        int total, prefix, newk;
         if (solo) {
             if (cnt_le > 0) { newk = k; total = cnt_le; }
             else { newk = bmin; total = cnt_m; }
             prefix = 0;
-            total_gone = cnt_gone;
-            prefix_gone = 0;
         } else {
             if (tid == 0) {
                 g.blk_cnt[phase * nb + b] = cnt_le;
                 g.blk_min[phase * nb + b] = bmin;
                 g.blk_cm[phase * nb + b] = cnt_m;
-                g.blk_gone[phase * nb + b] = cnt_gone;
             }
-            if (!grid_barrier(c, limit_ns)) return;
+            if (!grid_barrier(g.ctrl, limit_ns)) return;
             PEEL_ADD(1, t_ph);
             // warp 0 reads every CTA's report
+            __shared__ int s_glob[3];
             if (wib == 0) {
-                int tle = 0, ple = 0, gm = INT_MAX, tgo = 0, pgo = 0;
+                int tle = 0, ple = 0, gm = INT_MAX;
                 for (int i = lane; i < nb; i += 32) {
-                    const int cl = g.blk_cnt[phase * nb + i];
-                    const int cg = g.blk_gone[phase * nb + i];
-                    tle += cl;
-                    tgo += cg;
-                    if (i < b) { ple += cl; pgo += cg; }
+                    const int c = g.blk_cnt[phase * nb + i];
+                    tle += c;
+                    if (i < b) ple += c;
                     gm = min(gm, g.blk_min[phase * nb + i]);
                 }
                 tle = __reduce_add_sync(0xffffffffu, tle);
                 ple = __reduce_add_sync(0xffffffffu, ple);
-                tgo = __reduce_add_sync(0xffffffffu, tgo);
-                pgo = __reduce_add_sync(0xffffffffu, pgo);
                 gm = __reduce_min_sync(0xffffffffu, gm);
                 if (tle == 0) {
                     int tm = 0, pm = 0;
                     for (int i = lane; i < nb; i += 32) {
-                        const int cm = g.blk_min[phase * nb + i] == gm ? g.blk_cm[phase * nb + i] : 0;
-                        tm += cm;
-                        if (i < b) pm += cm;
+                        const int c = g.blk_min[phase * nb + i] == gm ? g.blk_cm[phase * nb + i] : 0;
+                        tm += c;
+                        if (i < b) pm += c;
                     }
                     tle = __reduce_add_sync(0xffffffffu, tm);
                     ple = __reduce_add_sync(0xffffffffu, pm);
                 } else {
                     gm = k;
                 }
-                if (lane == 0) {
-                    s_glob[0] = tle; s_glob[1] = ple; s_glob[2] = gm; s_glob[3] = tgo;
-                    s_glob[4] = pgo;
-                }
+                if (lane == 0) { s_glob[0] = tle; s_glob[1] = ple; s_glob[2] = gm; }
             }
             __syncthreads();
             total = s_glob[0];
             prefix = s_glob[1];
             newk = s_glob[2];
-            total_gone = s_glob[3];
-            prefix_gone = s_glob[4];
             phase ^= 1;
         }
-        // every CTA has read the counter the round after this one appends to (it was last
-        // written by the scan round before this one): clear it for that round
-        if (b == 0 && tid == 0) c->front_cnt[(scans + 1) & 1] = 0;
         k = newk;
         dmax = k;
         // -- write: this round's removals in id order, and the stably compacted survivors
+        __shared__ int s_front[kPeelThreads * kPeelItems];   // this CTA's removed vertices
         const int my_first = pos + prefix;
-        int bf = my_first, bs = lo - prefix - prefix_gone;
-        for (int t0 = lo; t0 < hi; t0 += kPeelTile) {
+        int bf = my_first, bs = lo - prefix;
+        for (int t0 = lo; t0 < hi; t0 += tile) {
             if (!in_regs) {
 #pragma unroll
                 for (int j = 0; j < kPeelItems; ++j) {
                     const int i = t0 + tid * kPeelItems + j;
                     vid[j] = i < hi ? alive[i] : -1;
-                    vdg[j] = vid[j] < 0 ? INT_MAX : (g.round_of[vid[j]] >= 0 ? -1 : g.deg[vid[j]]);
+                    vdg[j] = vid[j] >= 0 ? g.deg[vid[j]] : INT_MAX;
                 }
             }
-            int nf = 0, ns = 0;
+            int nf = 0, nv = 0;
 #pragma unroll
             for (int j = 0; j < kPeelItems; ++j) {
-                nf += vid[j] >= 0 && vdg[j] >= 0 && vdg[j] <= k;
-                ns += vid[j] >= 0 && vdg[j] > k;
+                nv += vid[j] >= 0;
+                nf += vid[j] >= 0 && vdg[j] <= k;
             }
             int tot;
-            const int ex = block_excl_scan_int((ns << 16) | nf, &tot, sh);  // both < 2^16
-            const int rf = ex & 0xffff, rs = ex >> 16;
-            const int tf = tot & 0xffff, ts = tot >> 16;
-            int of = bf + rf, os = bs + rs;
+            const int ex = block_excl_scan_int((nv << 16) | nf, &tot, sh);  // both < 2^16
+            const int rf = ex & 0xffff, rv = ex >> 16;
+            const int tf = tot & 0xffff, tv = tot >> 16;
+            int of = bf + rf, os = bs + (rv - rf);
 #pragma unroll
             for (int j = 0; j < kPeelItems; ++j) {
                 const int v = vid[j];
-                if (v < 0 || vdg[j] < 0) continue;
+                if (v < 0) continue;
                 if (vdg[j] <= k) {
                     g.order[of] = v;
                     g.rank[v] = of;
@@ -441,15 +311,18 @@ __global__ void __launch_bounds__(kPeelThreads, 1) peel_kernel(DevGraph g, long 
                 }
             }
             bf += tf;
-            bs += ts;
+            bs += tv - tf;
         }
         // degrees re-read by the write step (slices longer than one tile) must not move before
         // every CTA has written
         if (in_regs || solo) __syncthreads();
-        else if (!grid_barrier(c, limit_ns)) return;
+        else if (!grid_barrier(g.ctrl, limit_ns)) return;
         PEEL_ADD(2, t_ph);
         // -- remove this CTA's vertices: one warp per vertex, lanes over its neighbours; a vertex
         // with kPeelBigDegree or more neighbours is queued and then handled by the whole CTA
+        __shared__ int s_big[kPeelBigQueue];
+        __shared__ int s_nbig;
+        __shared__ unsigned long long s_rd;       // adjacency entries this CTA removes
         if (tid == 0) {
             s_nbig = 0;
             s_rd = 0ULL;
@@ -457,8 +330,9 @@ __global__ void __launch_bounds__(kPeelThreads, 1) peel_kernel(DevGraph g, long 
         __syncthreads();
         for (int e = wib; e < bf - my_first; e += wpb) {
             const int v = in_regs ? s_front[e] : g.order[my_first + e];
-            const int deg_v = g.offs[v + 1] - g.offs[v];
-            if (deg_v >= kPeelBigDegree) {
+            const int elo = g.offs[v], ehi = g.offs[v + 1];
+            if (lane == 0) atomicAdd(&s_rd, (unsigned long long)(ehi - elo));
+            if (ehi - elo >= kPeelBigDegree) {
                 int slot = 0;
                 if (lane == 0) slot = atomicAdd(&s_nbig, 1);
                 slot = __shfl_sync(0xffffffffu, slot, 0);
@@ -467,194 +341,44 @@ __global__ void __launch_bounds__(kPeelThreads, 1) peel_kernel(DevGraph g, long 
                     continue;
                 }
             }
-            remove_edges(g, v, k, lane, 32, g.front, front_cnt);
-            if (lane == 0) atomicAdd(&s_rd, (unsigned long long)deg_v);
+            for (int j = elo + lane; j < ehi; j += 32) atomicSub(&g.deg[g.adj[j]], 1);
 #ifdef MCE_PROFILE
-            if (lane == 0 && blockIdx.x == 0) atomicMax(&c->peel_prof[6], (unsigned long long)deg_v);
+            if (lane == 0 && blockIdx.x == 0)
+                atomicMax(&g.ctrl->peel_prof[6], (unsigned long long)(ehi - elo));
 #endif
         }
         __syncthreads();
         const int nbig = min(s_nbig, kPeelBigQueue);
         for (int i = 0; i < nbig; ++i) {
-            const long long dv = remove_edges(g, s_big[i], k, tid, nthr, g.front, front_cnt);
-            if (tid == 0) atomicAdd(&s_rd, (unsigned long long)dv);
+            const int v = s_big[i];
+            const int elo = g.offs[v], ehi = g.offs[v + 1];
+            for (int j = elo + tid; j < ehi; j += nthr) atomicSub(&g.deg[g.adj[j]], 1);
 #ifdef MCE_PROFILE
-            if (tid == 0 && blockIdx.x == 0) atomicMax(&c->peel_prof[6], (unsigned long long)dv);
+            if (tid == 0 && blockIdx.x == 0)
+                atomicMax(&g.ctrl->peel_prof[6], (unsigned long long)(ehi - elo));
 #endif
         }
         if (!solo && tid == 0) g.blk_rd[b] = (long long)s_rd;
         __syncthreads();
         PEEL_ADD(3, t_ph);
         if (solo) __syncthreads();
-        else if (!grid_barrier(c, limit_ns)) return;
+        else if (!grid_barrier(g.ctrl, limit_ns)) return;
         PEEL_ADD(4, t_ph);
 #ifdef MCE_PROFILE
-        if (blockIdx.x == 0 && tid == 0) c->peel_prof[5 + (solo ? 8 : 0)]++;
+        if (blockIdx.x == 0 && tid == 0) g.ctrl->peel_prof[5 + (solo ? 8 : 0)]++;
 #endif
-        // every CTA learns how many adjacency entries the round removed
-        if (!solo) {
-            if (wib == 0) {
-                long long t = 0;
-                for (int i = lane; i < nb; i += 32) t += g.blk_rd[i];
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-                if (lane == 0) s_removed = t;
-            }
-            __syncthreads();
-            live_entries -= s_removed;
-        } else {
-            live_entries -= (long long)s_rd;
-        }
-        live_sum += n_live;
+        live_sum += n_alive;
         pos += total;
         n_alive -= total;
-        n_live -= total + total_gone;
         ++r;
-        ++scans;
-        {
-            int *t = alive;
-            alive = alive_next;
-            alive_next = t;
-        }
-        // ======================================================== frontier rounds (CTA 0)
-        const int fc = *(volatile int *)front_cnt;    // the same in every CTA
-        if (n_alive == 0 || fc == 0 || fc > kFrontCap) continue;
-        if (b == 0) {
-            int *cur = s_fa, *nxt = s_fb;
-            for (int i = tid; i < fc; i += nthr) cur[i] = __ldcg(g.front + i);
-            if (tid == 0) s_rd = 0ULL;
-            int cnt = fc;
-            __syncthreads();
-            // the frontier's adjacency entries, flattened: s_off[i] = entries of cur[0 .. i)
-            int *s_off = s_front, *s_base = s_front + kFrontCap + 8;
-            while (true) {
-#ifdef MCE_PROFILE
-                unsigned long long t_fr = globaltimer_ns();
-#endif
-                block_sort(cur, cnt);                       // ends with __syncthreads
-                {
-                    // 4 consecutive frontier entries per thread (cnt <= kFrontCap = 4 * threads)
-                    int d4[4], dsum = 0;
-#pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const int i = tid * 4 + t;
-                        d4[t] = 0;
-                        if (i < cnt) {
-                            const int v = cur[i];
-                            const int lo_v = g.offs[v];
-                            s_base[i] = lo_v;
-                            d4[t] = g.offs[v + 1] - lo_v;
-                        }
-                        dsum += d4[t];
-                    }
-                    int tot;
-                    int run = block_excl_scan_int(dsum, &tot, sh);
-#pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const int i = tid * 4 + t;
-                        if (i < cnt) s_off[i] = run;
-                        run += d4[t];
-                    }
-                    if (tid == 0) s_off[cnt] = tot;
-                }
-                __syncthreads();
-                const int edges = s_off[cnt];
-                // too many edges for one CTA: the grid takes this round (nothing written yet)
-                if (edges > kFrontEdges) break;
-                for (int i = tid; i < cnt; i += nthr) {
-                    const int v = cur[i];
-                    g.order[pos + i] = v;
-                    g.rank[v] = pos + i;
-                    g.round_of[v] = r;
-                    g.core[v] = k;
-                }
-                if (tid == 0) s_fcnt = 0;
-                __syncthreads();
-#ifdef MCE_PROFILE
-                if (tid == 0) {
-                    const unsigned long long now = globaltimer_ns();
-                    c->peel_prof[8 + 2] += now - t_fr;
-                    t_fr = now;
-                }
-#endif
-                // every thread takes a contiguous share of the entries, kPeelInFlight at a time
-                {
-                    const int f_begin = (int)((long long)edges * tid / nthr);
-                    const int f_end = (int)((long long)edges * (tid + 1) / nthr);
-                    int lo_i = 0, hi_i = cnt;                  // owner of f_begin: last i with
-                    while (hi_i - lo_i > 1) {                  // s_off[i] <= f_begin
-                        const int mid = (lo_i + hi_i) >> 1;
-                        if (s_off[mid] <= f_begin) lo_i = mid;
-                        else hi_i = mid;
-                    }
-                    int own = lo_i;
-                    for (int f0 = f_begin; f0 < f_end; f0 += kPeelInFlight) {
-                        int u[kPeelInFlight], old[kPeelInFlight];
-#pragma unroll
-                        for (int t = 0; t < kPeelInFlight; ++t) {
-                            const int f = f0 + t;
-                            u[t] = -1;
-                            if (f < f_end) {
-                                while (s_off[own + 1] <= f) ++own;
-                                u[t] = __ldg(g.adj + s_base[own] + (f - s_off[own]));
-                            }
-                        }
-#pragma unroll
-                        for (int t = 0; t < kPeelInFlight; ++t)
-                            old[t] = u[t] >= 0 ? atomicSub(&g.deg[u[t]], 1) : 0;
-#pragma unroll
-                        for (int t = 0; t < kPeelInFlight; ++t) {
-                            if (u[t] >= 0 && old[t] == k + 1) {
-                                const int at = atomicAdd(&s_fcnt, 1);
-                                if (at < kFrontCap) nxt[at] = u[t];
-                            }
-                        }
-                    }
-                }
-                if (tid == 0) s_rd += (unsigned long long)edges;
-                __syncthreads();
-                const int next = s_fcnt;
-                live_sum += cnt;
-                pos += cnt;
-                n_alive -= cnt;
-                ++r;
-#ifdef MCE_PROFILE
-                if (tid == 0) {
-                    c->peel_prof[8 + 3] += globaltimer_ns() - t_fr;
-                    c->peel_prof[8 + 5]++;
-                }
-#endif
-                // s_fcnt is cleared at the next round's write step, after this read
-                if (n_alive == 0 || next == 0 || next > kFrontCap) break;
-                int *t = cur;
-                cur = nxt;
-                nxt = t;
-                cnt = next;
-            }
-            if (!solo && tid == 0) {
-                c->fr_r = r;
-                c->fr_pos = pos;
-                c->fr_n_alive = n_alive;
-                c->fr_live_sum = live_sum;
-                c->fr_entries = (long long)s_rd;
-            }
-            if (solo) live_entries -= (long long)s_rd;
-        }
-        if (solo) {
-            __syncthreads();
-        } else {
-            if (!grid_barrier(c, limit_ns)) return;
-            r = *(volatile int *)&c->fr_r;
-            pos = *(volatile int *)&c->fr_pos;
-            n_alive = *(volatile int *)&c->fr_n_alive;
-            live_sum = *(volatile long long *)&c->fr_live_sum;
-            live_entries -= *(volatile long long *)&c->fr_entries;
-        }
+        int *t = alive;
+        alive = alive_next;
+        alive_next = t;
     }
     if (blockIdx.x == 0 && tid == 0) {
-        c->degeneracy = dmax;
-        c->rounds = r;
-        c->peel_live = live_sum;
+        g.ctrl->degeneracy = dmax;
+        g.ctrl->rounds = r;
+        g.ctrl->peel_live = live_sum;
     }
 }
 
@@ -880,32 +604,15 @@ cudaError_t launch_unit_offsets(const DevGraph &g, const int *roots, int n_roots
     return cudaGetLastError();
 }
 
-// The peel kernel's dynamic shared memory (the CTA's removed vertices, two frontiers) exceeds
-// the default 48 KiB: raise the limit once per device.
-cudaError_t peel_configure()
-{
-    constexpr int kMaxDev = 64;
-    static bool done[kMaxDev] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < kMaxDev && done[dev]) return cudaSuccess;
-    e = cudaFuncSetAttribute((const void *)peel_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kPeelSmemBytes);
-    if (e == cudaSuccess && dev >= 0 && dev < kMaxDev) done[dev] = true;
-    return e;
-}
-
+// The whole peel: one cooperative launch over peel_blocks CTAs.
 cudaError_t launch_peel(const DevGraph &g, int peel_blocks, long long spin_limit_ns,
                         cudaStream_t s)
 {
-    cudaError_t e = peel_configure();
-    if (e != cudaSuccess) return e;
     DevGraph gg = g;
     long long lim = spin_limit_ns;
     void *args[] = {&gg, &lim};
     return cudaLaunchCooperativeKernel((const void *)peel_kernel, dim3(peel_blocks),
-                                       dim3(kPeelThreads), args, kPeelSmemBytes, s);
+                                       dim3(kPeelThreads), args, 0, s);
 }
 
 cudaError_t launch_order(const DevGraph &g, int peel_blocks, long long spin_limit_ns,
@@ -945,9 +652,8 @@ cudaError_t launch_order(const DevGraph &g, int peel_blocks, long long spin_limi
 //
 // mce_order_noalloc: the degeneracy order of a small graph with no allocation at all, for
 // callers that may not call cudaMalloc (see include/mce.h).  The peel kernel above runs
-// unchanged; only its scratch (degrees, live lists, the removal order, the frontier, the
-// per-CTA reports and barrier counters) lives in one fixed array in device memory instead of a
-// handle's buffers.
+// unchanged; only its scratch (degrees, live lists, the removal order, the barrier counters)
+// lives in one fixed array in device memory instead of a handle's buffers.
 
 namespace mce {
 
@@ -956,8 +662,7 @@ namespace {
 constexpr int kNoAllocMaxN = 1 << 18;        // vertices
 constexpr int kNoAllocMaxBlocks = 1024;      // CTAs of the cooperative peel
 constexpr int kNoAllocCtrlWords = (int)((sizeof(DevCtrl) + 255) / 256 * 64);
-constexpr int kNoAllocWords = kNoAllocCtrlWords + 10 * kNoAllocMaxBlocks + kFrontCap +
-                              5 * kNoAllocMaxN;
+constexpr int kNoAllocWords = kNoAllocCtrlWords + 8 * kNoAllocMaxBlocks + 5 * kNoAllocMaxN;
 constexpr int kNoAllocMaxDevices = 64;
 
 // The whole scratch area: 5 MiB + a few KiB, held by every device that loads the library.
@@ -1022,9 +727,7 @@ extern "C" mce_status mce_order_noalloc(const int32_t *d_offsets, const int32_t 
     g.blk_min = g.blk_cnt + 2 * kNoAllocMaxBlocks;
     g.blk_cm = g.blk_min + 2 * kNoAllocMaxBlocks;
     g.blk_rd = reinterpret_cast<long long *>(g.blk_cm + 2 * kNoAllocMaxBlocks);
-    g.blk_gone = g.blk_cm + 4 * kNoAllocMaxBlocks;
-    g.front = g.blk_gone + 2 * kNoAllocMaxBlocks;
-    g.deg = g.front + kFrontCap;
+    g.deg = g.blk_cm + 4 * kNoAllocMaxBlocks;
     g.round_of = g.deg + kNoAllocMaxN;
     g.alive_a = g.round_of + kNoAllocMaxN;
     g.alive_b = g.alive_a + kNoAllocMaxN;

@@ -209,7 +209,7 @@ struct Acc {
     unsigned long long count, hash, nodes, donations;
     unsigned long long words;   // bitset words scored / intersected / tested (lane 0 counts)
 #ifdef MCE_PROFILE
-    unsigned long long prof[8];
+    unsigned long long prof[kProfSlots];
 #endif
 };
 
@@ -222,8 +222,7 @@ struct Acc {
 #define PROF_ADD(acc, slot, var) (void)0
 #endif
 enum { kProfBuild = 0, kProfPivot, kProfChild, kProfPartition, kProfDonate, kProfIdle,
-       kProfMaxRoot, kProfRoots };
-constexpr int kProfSmall = kProfPivot;   // small subtrees solved whole are part of the pivot work
+       kProfMaxRoot, kProfRoots, kProfSmall, kProfSplit, kProfHash, kProfWalk, kProfXList };
 
 struct RootCtx {
     unsigned *rowsP, *rowsX;
@@ -1111,6 +1110,7 @@ __device__ void build_and_search(const SearchArgs &a, RootCtx r, const WarpSmem 
         for (long long t = (long long)lane * CH; t < words; t += 32 * CH)
             ck_store<CH>(r.rowsP + t, ck_zero<CH>());
     }
+    PROF_START(t_hash);
     int slots = 32;
     while (slots < 2 * np) slots <<= 1;
     WarpSmem h = sm;
@@ -1127,6 +1127,7 @@ __device__ void build_and_search(const SearchArgs &a, RootCtx r, const WarpSmem 
         atomicOr(&h.filter[f >> 5], 1u << (f & 31));
     }
     __syncwarp();
+    PROF_ADD(acc, kProfHash, t_hash);
     int nxx = 0;
     bool covered = false;
     if constexpr (kIP) {
@@ -1135,7 +1136,10 @@ __device__ void build_and_search(const SearchArgs &a, RootCtx r, const WarpSmem 
         for (int i = lane; i < r.nx; i += 32) r.xx[i] = i;
         nxx = r.nx;
     } else if constexpr (!big) {
+        PROF_START(t_walk);
         build_flat<W>(a, r, h, deg, np, lane);
+        PROF_ADD(acc, kProfWalk, t_walk);
+        PROF_START(t_xl);
         // X_X and the coverage test: a vertex of X adjacent to all of P makes every clique of
         // this subtree extendable (it is the Tomita pivot of the root with P - N(pivot) empty),
         // so the subtree holds no maximal clique
@@ -1149,6 +1153,7 @@ __device__ void build_and_search(const SearchArgs &a, RootCtx r, const WarpSmem 
             if (cnt > 0) r.xx[nxx + __popc(m & lt)] = xi;
             nxx += __popc(m);
         }
+        PROF_ADD(acc, kProfXList, t_xl);
         if (covered) {
             acc.nodes++;
             PROF_ADD(acc, kProfBuild, t_build);
@@ -1252,8 +1257,10 @@ __device__ void build_and_search(const SearchArgs &a, RootCtx r, const WarpSmem 
         }
     }
     }
+    PROF_START(t_keys);
     for (int i = lane; i < np; i += 32) r.pkey[i] = vertex_key(r.pids[i]);
     __syncwarp();
+    PROF_ADD(acc, kProfXList, t_keys);
     PROF_ADD(acc, kProfBuild, t_build);
     const int q = lane % G;
     dfs<W>(a, r, bits_prefix<W>(np, q), ck_zero<CH>(), nxx, S, acc, s_hist, reinterpret_cast<unsigned *>(sm.cur_start), lane);
@@ -1302,6 +1309,7 @@ template <int W, bool big>
 __device__ void search_root(const SearchArgs &a, unsigned *ws, const WarpSmem &sm, int v, int deg,
                             int np, Acc &acc, unsigned long long *s_hist, int lane)
 {
+    PROF_START(t_split);
     RootCtx r = make_ctx<W>(ws, deg, np, np, deg - np);
     const int *Nv = a.g.adj + a.g.offs[v];
     const int rv = a.g.rank[v];
@@ -1326,6 +1334,7 @@ __device__ void search_root(const SearchArgs &a, unsigned *ws, const WarpSmem &s
         }
     }
     if (lane == 0) r.rids[0] = v;
+    PROF_ADD(acc, kProfSplit, t_split);
     build_and_search<W, big>(a, r, sm, vertex_key(v), acc, s_hist, lane);
 }
 
@@ -1595,9 +1604,9 @@ __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(Search
         atomicAdd(&a.g.ctrl->donations, acc.donations);
         atomicAdd(&a.g.ctrl->words[a.cls], acc.words);
 #ifdef MCE_PROFILE
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < kProfSlots; ++i) {
             if (i == kProfMaxRoot) atomicMax(&a.g.ctrl->prof[a.cls][i], acc.prof[i]);
-            else atomicAdd(&a.g.ctrl->prof[a.cls][i], acc.prof[i]);
+            else if (acc.prof[i]) atomicAdd(&a.g.ctrl->prof[a.cls][i], acc.prof[i]);
         }
         // this warp's load: its time in the kernel minus its time waiting in the worker list,
         // added to the slot of the SM it ran on (Section 4.3 compares per-block loads)
