@@ -130,7 +130,7 @@ mce_status mce_config_default(mce_config *cfg);
  *            if is_device_ptr == 0, else device pointers.  The graph must be simple and
  *            undirected: every edge listed in both directions, no self-loops, no repeats.
  *            The library copies both arrays; the caller may free them on return.
- *   n        number of vertices, 0 <= n.  offsets[n] must be < 2^31.
+ *   n        number of vertices, 0 <= n < 2^30.  offsets[n] must be < 2^31.
  *   cfg      NULL for defaults.
  *   stream   the copy, the input checks and the first degeneracy ordering run on it.
  *   out      receives the handle; *out is NULL on failure.
@@ -139,8 +139,9 @@ mce_status mce_config_default(mce_config *cfg);
  * `stream`); mce_destroy returns it to that pool, which keeps it for later handles until the
  * process ends or mce_trim_memory hands it back to the driver.
  * Errors: MCE_ERR_INVALID_ARG, MCE_ERR_ID_RANGE, MCE_ERR_NOT_SIMPLE, MCE_ERR_NOT_SYMMETRIC,
- * MCE_ERR_OUT_OF_MEMORY, MCE_ERR_LIMIT (a first-level P larger than 1024 vertices, a degree of
- * 2^21 or more, or with second-level subtrees n + m of 2^31 or more), MCE_ERR_CUDA.
+ * MCE_ERR_OUT_OF_MEMORY, MCE_ERR_LIMIT (n of 2^30 or more, a first-level P larger than 1024
+ * vertices, a degree of 2^21 or more, or with second-level subtrees n + m of 2^31 or more),
+ * MCE_ERR_CUDA.
  */
 mce_status mce_create(const int32_t *offsets, const int32_t *adj, int32_t n, int is_device_ptr,
                       const mce_config *cfg, void *stream, mce_graph **out);
@@ -227,7 +228,8 @@ mce_status mce_get_order(mce_graph *g, void *stream, int32_t *d_rank, int32_t *d
  * execution time down the same way from per-block SM clocks.  Then 16 values for the last
  * ordering, as seen by its first CTA, in nanoseconds: out[96 + p] for rounds run by all CTAs and
  * out[104 + p] for rounds run by one CTA, phase p = 0 scan, 1 report exchange, 2 decide and
- * write, 3 edge removal, 4 end-of-round barrier, 5 number of rounds; out[102] is the largest
+ * write, 3 edge removal, 4 end-of-round barrier, 5 number of rounds (rounds run from a frontier,
+ * without a scan, count as rounds run by one CTA); out[102] is the largest
  * degree of a vertex removed by the first CTA.  Then, per row-width class k, the load of every
  * SM in the last search (Section 4.3 judges the worker list by per-block loads): at
  * out[112 + k * 256 + s] the SM clock cycles that warps on SM s spent holding work (time in the
@@ -244,7 +246,7 @@ mce_status mce_get_profile(mce_graph *g, uint64_t *out);
  * allocator owns all of the GPU's memory, plug-ins that are only ever handed buffers, or
  * latency-critical paths that must not pay for cudaMalloc and the synchronisation it implies.
  * It neither creates a handle nor calls cudaMalloc, cudaFree or any allocating library routine;
- * its scratch space is one fixed array of about 5.3 MiB in device memory, which every GPU that
+ * its scratch space is one fixed array of about 6.2 MiB in device memory, which every GPU that
  * loads the library holds until the process exits.
  *   d_offsets, d_adj  device pointers to a simple undirected graph as a CSR (the same layout as
  *                     mce_create).  The input is NOT checked: validate it with mce_create first

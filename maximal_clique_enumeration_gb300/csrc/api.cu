@@ -374,6 +374,9 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
     MCE_ALLOC(h, g.blk_min, (size_t)2 * h->peel_blocks);
     MCE_ALLOC(h, g.blk_cm, (size_t)2 * h->peel_blocks);
     MCE_ALLOC(h, g.blk_rd, (size_t)h->peel_blocks);
+    MCE_ALLOC(h, g.blk_gone, (size_t)2 * h->peel_blocks);
+    MCE_ALLOC(h, g.front, (size_t)3 * kFrontCap);
+    MCE_ALLOC(h, g.rstart, (size_t)n + 1);
     if (h->cfg.profile) {
         for (int i = 0; i < 3; ++i) MCE_TRY(cudaEventCreate(&h->ev_order[i]));
         for (int k = 0; k < kNumGroups; ++k) {
@@ -480,6 +483,7 @@ mce_status mce_create(const int32_t *offsets, const int32_t *adj, int32_t n, int
     if (!out) return MCE_ERR_INVALID_ARG;
     *out = nullptr;
     if (n < 0 || !offsets) return MCE_ERR_INVALID_ARG;
+    if (n >= kRoundUnsorted) return MCE_ERR_LIMIT;      // the peel marks places below 2^30
     mce_graph *h = new (std::nothrow) mce_graph();
     if (!h) return MCE_ERR_OUT_OF_MEMORY;
     if (cfg) h->cfg = *cfg;

@@ -23,6 +23,8 @@ constexpr int kProfSms = 256;            // MCE_PROFILE builds: per-SM load slot
 constexpr int kProfSlots = 16;           // MCE_PROFILE builds: activity counters per class
 constexpr int kSmallP = 10;              // largest |P| of a search-tree node solved whole
 constexpr int kSmallPMax = 10;           // ... and the most its bit-sliced test allows
+constexpr int kFrontCap = 8192;          // largest round the peel runs from a frontier
+constexpr int kRoundUnsorted = 1 << 30;  // rstart flag: places are below 2^30 (n < 2^30)
 
 // Device-resident control block of a handle.
 struct DevCtrl {
@@ -30,6 +32,7 @@ struct DevCtrl {
     int degeneracy;              // peel output
     int rounds;                  // peel output
     long long peel_live;         // peel output: live vertices summed over rounds
+    int front_cnt[3];            // peel: frontier sizes, by round modulo 3
     int max_pcount;              // max |P| over first-level subtrees
     unsigned int bar_count;      // grid barrier arrivals (grows by the grid size per barrier)
     unsigned int bar_pad;
@@ -76,6 +79,10 @@ struct DevGraph {
     int *alive_a, *alive_b;
     int *blk_cnt, *blk_min, *blk_cm;   // peel per-CTA reports [2][grid]
     long long *blk_rd;                 // peel: adjacency entries removed per CTA [grid]
+    int *blk_gone;                     // peel per-CTA reports: live entries removed [2][grid]
+    int *front;                        // peel: frontiers of three consecutive rounds [3][kFrontCap]
+    int *rstart;                       // peel: first place of each round in the order [n + 1]
+                                       // (kRoundUnsorted set: a frontier round, sorted at the end)
     int ip;           // search over partial induced subgraphs (rows for P only), Section 3.4
     int l2;           // independent second-level subtrees, one per edge (Section 3.2)
     int *unit_cnt;    // l2: subtrees per root, in schedule order (scan input) [n]

@@ -8,11 +8,13 @@
 // its core number is the level at which it was removed.  Every vertex then has at most d
 // later neighbours, d being the degeneracy (largest level).
 //
-// One cooperative kernel runs all rounds: the remaining vertices stay in an id-ordered list
-// that is compacted stably every round, so each round's removals come out already in id
-// order and the order needs no sort.  Two grid-wide barriers separate the phases of a round;
-// once at most kPeelSoloVertices vertices remain, CTA 0 finishes alone with CTA barriers.
-// Every barrier wait is bounded by spin_limit_ns.
+// One cooperative kernel runs all rounds.  The remaining vertices stay in an id-ordered list
+// that is compacted stably in every round that scans it, so those rounds' removals come out in
+// id order.  Most rounds need no scan: at level k, a round that keeps the level removes exactly
+// the vertices whose degree fell to k in the round before, which that round's edge removal
+// collects; such a round takes one grid barrier instead of two and reads no live list.  Once at
+// most kPeelSoloVertices vertices remain, CTA 0 finishes alone with CTA barriers.  Every barrier
+// wait is bounded by spin_limit_ns.
 //
 // Then small kernels count every vertex's later neighbours |P| (Algorithm 3's P), count the
 // isolated vertices, bucket the first-level roots by |P|, heaviest first, and store the
@@ -97,8 +99,8 @@ __device__ __forceinline__ int block_excl_scan_int(int v, int *total, int *sh)
     return before + inc - v;
 }
 
-// Phase timers of the MCE_PROFILE build (CTA 0, thread 0; nanoseconds): slot = phase, +8 when
-// the round runs in a single CTA.  Phases: 0 scan, 1 report exchange (barrier), 2 decide and
+// Phase timers of the MCE_PROFILE build (CTA 0, thread 0; nanoseconds): slot = phase, +8 for
+// frontier rounds and rounds run in a single CTA (prof_off).  Phases: 0 scan, 1 report exchange (barrier), 2 decide and
 // write, 3 edge removal, 4 end-of-round barrier, 5 rounds, 6 max edges of one removed vertex.
 #ifdef MCE_PROFILE
 #define PEEL_MARK(var) unsigned long long var = globaltimer_ns()
@@ -106,7 +108,7 @@ __device__ __forceinline__ int block_excl_scan_int(int v, int *total, int *sh)
     do {                                                                               \
         if (blockIdx.x == 0 && threadIdx.x == 0) {                                     \
             const unsigned long long now_ = globaltimer_ns();                          \
-            g.ctrl->peel_prof[(slot) + (solo ? 8 : 0)] += now_ - (var);                \
+            g.ctrl->peel_prof[(slot) + prof_off] += now_ - (var);                      \
             var = now_;                                                                \
         }                                                                              \
     } while (0)
@@ -117,188 +119,399 @@ __device__ __forceinline__ int block_excl_scan_int(int v, int *total, int *sh)
 
 // Each thread holds up to kPeelItems consecutive entries of its CTA's part of the live list.
 constexpr int kPeelItems = 8;
+constexpr int kPeelTile = kPeelThreads * kPeelItems;
 constexpr int kPeelBigDegree = 1024;   // removed vertices this wide are handled by a whole CTA
 constexpr int kPeelBigQueue = 256;     // ... up to this many per round and CTA (then by warps)
 constexpr long long kPeelSoloEntries = 1 << 20;   // and the single-CTA finish needs few edges left
+constexpr int kPeelInFlight = 8;       // adjacency entries a thread has in flight in edge removal
+// Dynamic shared memory: the CTA's removed vertices of a scan round (kPeelTile), then in
+// frontier rounds the frontier's entry offsets (kFrontCap + 1) and adjacency bases (kFrontCap);
+// the sort of the rank pass reuses the first part.
+constexpr size_t kPeelSmemBytes = (size_t)(kPeelTile + 2 * kFrontCap + 8) * sizeof(int);
+static_assert(kFrontCap <= kPeelTile, "a frontier segment sorts in the first part");
 
-// One round of the peel, in a CTA that owns live[lo, hi):
-//   scan   -- load ids and current degrees once (kept in registers across the exchange) and
-//             report (#deg <= k, least degree above k, #vertices at that degree);
-//   decide -- from every CTA's report: if some vertex has deg <= k the round removes those,
-//             else the level rises to the least degree d' and the round removes deg == d';
-//   write  -- stable compaction: removed vertices get their rank (round, id order), round and
-//             core number; survivors go to the next live list;
-//   remove -- the CTA subtracts one degree from every neighbour of its own removed vertices
-//             (degrees of vertices already removed are never read again).
-// Grid barriers: after the scan (reports) and after the removal (degrees, next live list).
+// Appends u to the frontier of the next round (warp-aggregated; entries beyond kFrontCap are
+// counted, not stored).  All 32 lanes call it, `want` says whether this lane has a vertex.
+__device__ __forceinline__ void front_append(bool want, int u, int *front, int *front_cnt)
+{
+    const unsigned m = __ballot_sync(0xffffffffu, want);
+    if (!m) return;
+    const int lane = threadIdx.x & 31, leader = __ffs(m) - 1;
+    int base = 0;
+    if (lane == leader) base = atomicAdd(front_cnt, __popc(m));
+    base = __shfl_sync(0xffffffffu, base, leader);
+    const int at = base + __popc(m & ((1u << lane) - 1u));
+    if (want && at < kFrontCap) front[at] = u;
+}
+
+// Subtracts one from the degree of every adjacency entry in [f_begin, f_end) of the flattened
+// list of vertices s_vert / their offsets s_off, kPeelInFlight entries in flight, appending to the
+// next frontier every vertex whose degree falls from k + 1 to k (at level k those are exactly
+// the vertices the next round removes; a vertex removed earlier, or in this round, already has
+// degree <= k and is never appended).  Every lane of the warp calls it (appends are ballots).
+__device__ void remove_flat(const DevGraph &g, const int *s_off, const int *s_base, int n_vert,
+                            int f_begin, int f_end, int k, int *front, int *front_cnt)
+{
+    int lo = 0, hi = n_vert;                      // owner of f_begin: last i with s_off[i] <= f
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_off[mid] <= f_begin) lo = mid;
+        else hi = mid;
+    }
+    int own = lo;
+    // the warp runs until its longest thread is done (ballots need every lane)
+    int rounds = (f_end - f_begin + kPeelInFlight - 1) / kPeelInFlight;
+    rounds = __reduce_max_sync(0xffffffffu, rounds > 0 ? rounds : 0);
+    for (int it = 0; it < rounds; ++it) {
+        const int f0 = f_begin + it * kPeelInFlight;
+        int u[kPeelInFlight], old[kPeelInFlight];
+#pragma unroll
+        for (int t = 0; t < kPeelInFlight; ++t) {
+            const int f = f0 + t;
+            u[t] = -1;
+            if (f < f_end) {
+                while (s_off[own + 1] <= f) ++own;
+                u[t] = __ldg(g.adj + s_base[own] + (f - s_off[own]));
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < kPeelInFlight; ++t) old[t] = u[t] >= 0 ? atomicSub(&g.deg[u[t]], 1) : 0;
+#pragma unroll
+        for (int t = 0; t < kPeelInFlight; ++t)
+            front_append(u[t] >= 0 && old[t] == k + 1, u[t], front, front_cnt);
+    }
+}
+
+// Sorts s[0 .. cnt) ascending, cnt <= kFrontCap (room for the next power of two): bitonic, in
+// one warp's registers up to 32 entries, else by the whole CTA in shared memory.
+__device__ void block_sort(int *s, int cnt)
+{
+    const int lane = threadIdx.x & 31;
+    if (cnt <= 32) {
+        if (threadIdx.x < 32) {
+            int x = lane < cnt ? s[lane] : INT_MAX;
+#pragma unroll
+            for (int kk = 2; kk <= 32; kk <<= 1) {
+#pragma unroll
+                for (int j = kk >> 1; j > 0; j >>= 1) {
+                    const int y = __shfl_xor_sync(0xffffffffu, x, j);
+                    const bool take_min = ((lane & j) == 0) == ((lane & kk) == 0);
+                    x = take_min ? min(x, y) : max(x, y);
+                }
+            }
+            if (lane < cnt) s[lane] = x;
+        }
+        __syncthreads();
+        return;
+    }
+    int p2 = 64;
+    while (p2 < cnt) p2 <<= 1;
+    for (int i = cnt + (int)threadIdx.x; i < p2; i += blockDim.x) s[i] = INT_MAX;
+    __syncthreads();
+    for (int kk = 2; kk <= p2; kk <<= 1) {
+        for (int j = kk >> 1; j > 0; j >>= 1) {
+            for (int i = threadIdx.x; i < p2; i += blockDim.x) {
+                const int ixj = i ^ j;
+                if (ixj > i) {
+                    const int a = s[i], b = s[ixj];
+                    if ((a > b) == ((i & kk) == 0)) {
+                        s[i] = b;
+                        s[ixj] = a;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+// The canonical peel (see the top of this file) in one cooperative kernel, with two kinds of
+// round:
+//   scan round (the first round, every round that raises the level, and every round whose
+//   vertices did not fit a frontier) -- a CTA owns live[lo, hi):
+//     scan   -- load ids, current degrees and removal marks once (kept in registers across the
+//               exchange) and report (#deg <= k, least degree above k, #vertices at that degree,
+//               #entries removed by frontier rounds since the last compaction);
+//     decide -- from every CTA's report: if some vertex has deg <= k the round removes those,
+//               else the level rises to the least degree d' and the round removes deg == d';
+//     write  -- stable compaction: removed vertices get their rank (round, id order), round and
+//               core number; survivors go to the next live list;
+//     remove -- the CTA subtracts one degree from every neighbour of its own removed vertices;
+//   frontier round -- at level k a round that keeps the level removes exactly the vertices
+//   whose degree fell to k during the round before, which that round's edge removal collected
+//   (the frontier): no scan and no exchange, every CTA takes a share of the frontier's
+//   vertices (round, core number, unsorted place in the order) and of their adjacency entries.
+// Every round's edge removal collects the next frontier.  Grid barriers: two per scan round
+// (after the reports, and at the end), one per frontier round.  After the last round a pass
+// sorts each frontier round's vertices by id in place and writes their ranks.  Once few
+// vertices and few edges remain, CTA 0 goes on alone (CTA barriers only).
 __global__ void __launch_bounds__(kPeelThreads, 1) peel_kernel(DevGraph g, long long limit_ns)
 {
+    extern __shared__ int s_dyn[];
+    int *s_front = s_dyn;                       // scan round: this CTA's removed vertices
+    int *s_off = s_dyn + kPeelTile;             // frontier round: entry offsets [cnt + 1]
+    int *s_base = s_off + kFrontCap + 8;        // frontier round: adjacency bases [cnt]
     __shared__ int sh[32];
+    __shared__ int s_rep[4][32];
+    __shared__ int s_dec[4];
+    __shared__ int s_glob[5];
+    __shared__ int s_big[kPeelBigQueue];
+    __shared__ int s_nbig;
+    __shared__ unsigned long long s_rd;
+    __shared__ long long s_removed;
     const int tid = threadIdx.x, nthr = blockDim.x;
     const int lane = tid & 31, wib = tid >> 5, wpb = nthr >> 5;
     const int n = g.n;
+    DevCtrl *c = g.ctrl;
     for (int v = blockIdx.x * nthr + tid; v < n; v += gridDim.x * nthr) {
         g.deg[v] = g.offs[v + 1] - g.offs[v];
         g.round_of[v] = -1;
         g.alive_a[v] = v;
     }
-    if (!grid_barrier(g.ctrl, limit_ns)) return;
+    if (blockIdx.x == 0 && tid < 3) c->front_cnt[tid] = 0;
+    if (!grid_barrier(c, limit_ns)) return;
 
     int *alive = g.alive_a, *alive_next = g.alive_b;
-    int n_alive = n, k = 0, r = 0, pos = 0, phase = 0, dmax = 0;
+    int n_live = n;     // entries of the live list (frontier rounds remove without compacting)
+    int n_alive = n;    // vertices not removed yet
+    int k = 0, r = 0, pos = 0, phase = 0, dmax = 0;
     // adjacency entries of the remaining vertices, read from the offsets themselves (callers of
     // the allocation-free entry point pass no edge count)
     long long live_entries = n > 0 ? (long long)g.offs[n] - (long long)g.offs[0] : 0;
-    long long live_sum = 0;           // live vertices summed over rounds (CTA 0 keeps it)
+    long long live_sum = 0;   // live-list entries scanned plus frontier vertices, over rounds
     bool solo = false;
     int nb = gridDim.x, b = blockIdx.x;
-    const int tile = nthr * kPeelItems;
-    __shared__ long long s_removed;
     while (n_alive > 0) {
-        if (!solo && r > 0) {
-            // every CTA learns how many adjacency entries the last round removed
-            if (wib == 0) {
-                long long t = 0;
-                for (int i = lane; i < nb; i += 32) t += g.blk_rd[i];
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-                if (lane == 0) s_removed = t;
-            }
-            __syncthreads();
-            live_entries -= s_removed;
-        }
+        // round r reads the frontier round r - 1 collected, collects into the next buffer, and
+        // clears the one after (last read in round r - 1); three buffers, so no read races a write
+        const int fr_in = r % 3, fr_out = (r + 1) % 3, fr_clear = (r + 2) % 3;
+        int *front_in = g.front + (size_t)fr_in * kFrontCap;
+        int *front_out = g.front + (size_t)fr_out * kFrontCap;
+        const int fc = r > 0 ? *(volatile int *)&c->front_cnt[fr_in] : 0;   // same in every CTA
+        if (b == 0 && tid == 0) c->front_cnt[fr_clear] = 0;
         // one CTA finishes once few vertices and few edges remain (a dense core keeps the grid)
-        if (!solo && n_alive <= kPeelSoloVertices && live_entries <= kPeelSoloEntries) {
+        if (!solo && n_live <= kPeelSoloVertices && live_entries <= kPeelSoloEntries) {
             if (blockIdx.x != 0) return;
             solo = true;
             nb = 1;
             b = 0;
         }
         PEEL_MARK(t_ph);
-        const int chunk = (n_alive + nb - 1) / nb;
-        const int lo = min(b * chunk, n_alive), hi = min(lo + chunk, n_alive);
-        const bool in_regs = chunk <= tile;        // the same in every CTA
+        const bool frontier = fc > 0 && fc <= kFrontCap;
+        const int prof_off = solo || frontier ? 8 : 0;
+        (void)prof_off;
+        if (frontier) {
+            // ================================================ frontier round
+            // the frontier's adjacency entries, flattened (every CTA the whole prefix)
+            {
+                int dsum = 0;
+                const int per = (fc + nthr - 1) / nthr;       // <= kFrontCap / threads
+                const int i0 = min(tid * per, fc), i1 = min(i0 + per, fc);
+                for (int i = i0; i < i1; ++i) {
+                    const int v = __ldcg(front_in + i);
+                    const int lo_v = g.offs[v];
+                    s_base[i] = lo_v;
+                    s_off[i] = g.offs[v + 1] - lo_v;
+                    dsum += s_off[i];
+                }
+                int tot;
+                int run = block_excl_scan_int(dsum, &tot, sh);
+                for (int i = i0; i < i1; ++i) {
+                    const int d = s_off[i];
+                    s_off[i] = run;
+                    run += d;
+                }
+                if (tid == 0) s_off[fc] = tot;
+                __syncthreads();
+            }
+            const int edges = s_off[fc];
+            // this CTA's share of the frontier: round, core number, place in the order (the
+            // rank pass sorts the round's places by id at the end)
+            {
+                const int v0 = (int)((long long)fc * b / nb), v1 = (int)((long long)fc * (b + 1) / nb);
+                for (int i = v0 + tid; i < v1; i += nthr) {
+                    const int v = __ldcg(front_in + i);
+                    g.order[pos + i] = v;
+                    g.round_of[v] = r;
+                    g.core[v] = k;
+                }
+            }
+            if (b == 0 && tid == 0) g.rstart[r] = pos | kRoundUnsorted;
+            PEEL_ADD(2, t_ph);
+            // this CTA's share of the entries, a contiguous piece per thread
+            {
+                const long long e0 = (long long)edges * b / nb, e1 = (long long)edges * (b + 1) / nb;
+                const int f_begin = (int)(e0 + (e1 - e0) * tid / nthr);
+                const int f_end = (int)(e0 + (e1 - e0) * (tid + 1) / nthr);
+                remove_flat(g, s_off, s_base, fc, f_begin, f_end, k, front_out,
+                            &c->front_cnt[fr_out]);
+            }
+            __syncthreads();
+            PEEL_ADD(3, t_ph);
+            if (solo) __syncthreads();
+            else if (!grid_barrier(c, limit_ns)) return;
+            PEEL_ADD(4, t_ph);
+#ifdef MCE_PROFILE
+            if (blockIdx.x == 0 && tid == 0) c->peel_prof[5 + prof_off]++;
+#endif
+            live_entries -= edges;
+            live_sum += fc;
+            pos += fc;
+            n_alive -= fc;
+            ++r;
+            continue;
+        }
+        // ==================================================== scan round
+        const int chunk = (n_live + nb - 1) / nb;
+        const int lo = min(b * chunk, n_live), hi = min(lo + chunk, n_live);
+        const bool in_regs = chunk <= kPeelTile;   // the same in every CTA
         int vid[kPeelItems], vdg[kPeelItems];
-        // -- scan
-        int cnt_le = 0, mmin = INT_MAX, cnt_m = 0;
-        for (int t0 = lo; t0 < hi; t0 += tile) {
+        // -- scan (an entry removed by a frontier round gets vdg = -1)
+        int cnt_le = 0, mmin = INT_MAX, cnt_m = 0, cnt_gone = 0;
+        for (int t0 = lo; t0 < hi; t0 += kPeelTile) {
 #pragma unroll
             for (int j = 0; j < kPeelItems; ++j) {
                 const int i = t0 + tid * kPeelItems + j;
                 vid[j] = i < hi ? alive[i] : -1;
             }
 #pragma unroll
-            for (int j = 0; j < kPeelItems; ++j) vdg[j] = vid[j] >= 0 ? g.deg[vid[j]] : INT_MAX;
+            for (int j = 0; j < kPeelItems; ++j) {
+                if (vid[j] < 0) {
+                    vdg[j] = INT_MAX;
+                    continue;
+                }
+                const int d = g.deg[vid[j]], gone = g.round_of[vid[j]];
+                vdg[j] = gone >= 0 ? -1 : d;
+            }
 #pragma unroll
             for (int j = 0; j < kPeelItems; ++j) {
                 const int d = vdg[j];
                 if (vid[j] < 0) continue;
-                if (d <= k) ++cnt_le;
+                if (d < 0) ++cnt_gone;
+                else if (d <= k) ++cnt_le;
                 else if (d < mmin) { mmin = d; cnt_m = 1; }
                 else if (d == mmin) ++cnt_m;
             }
         }
-        // CTA report in one exchange: (#deg <= k, least degree above k, #at that degree)
-        __shared__ int s_rep[3][32];
-        __shared__ int s_dec[3];
+        // CTA report in one exchange: (#deg <= k, least degree above k, #at that degree, #gone)
         {
             const int wle = __reduce_add_sync(0xffffffffu, cnt_le);
             const int wmin = __reduce_min_sync(0xffffffffu, mmin);
             const int wcm = __reduce_add_sync(0xffffffffu, mmin == wmin ? cnt_m : 0);
-            if (lane == 0) { s_rep[0][wib] = wle; s_rep[1][wib] = wmin; s_rep[2][wib] = wcm; }
+            const int wgo = __reduce_add_sync(0xffffffffu, cnt_gone);
+            if (lane == 0) {
+                s_rep[0][wib] = wle;
+                s_rep[1][wib] = wmin;
+                s_rep[2][wib] = wcm;
+                s_rep[3][wib] = wgo;
+            }
             __syncthreads();
             if (wib == 0) {
                 const int a0 = lane < wpb ? s_rep[0][lane] : 0;
                 const int a1 = lane < wpb ? s_rep[1][lane] : INT_MAX;
                 const int a2 = lane < wpb ? s_rep[2][lane] : 0;
+                const int a3 = lane < wpb ? s_rep[3][lane] : 0;
                 const int bm = __reduce_min_sync(0xffffffffu, a1);
                 const int t_le = __reduce_add_sync(0xffffffffu, a0);
                 const int t_cm = __reduce_add_sync(0xffffffffu, a1 == bm ? a2 : 0);
-                if (lane == 0) { s_dec[0] = t_le; s_dec[1] = bm; s_dec[2] = t_cm; }
+                const int t_go = __reduce_add_sync(0xffffffffu, a3);
+                if (lane == 0) { s_dec[0] = t_le; s_dec[1] = bm; s_dec[2] = t_cm; s_dec[3] = t_go; }
             }
             __syncthreads();
         }
         cnt_le = s_dec[0];
         const int bmin = s_dec[1];
         cnt_m = s_dec[2];
+        cnt_gone = s_dec[3];
         PEEL_ADD(0, t_ph);
         // -- decide (identically in every CTA)
-        int total, prefix, newk;
+        int total, prefix, newk, total_gone, prefix_gone;
         if (solo) {
             if (cnt_le > 0) { newk = k; total = cnt_le; }
             else { newk = bmin; total = cnt_m; }
             prefix = 0;
+            total_gone = cnt_gone;
+            prefix_gone = 0;
         } else {
             if (tid == 0) {
                 g.blk_cnt[phase * nb + b] = cnt_le;
                 g.blk_min[phase * nb + b] = bmin;
                 g.blk_cm[phase * nb + b] = cnt_m;
+                g.blk_gone[phase * nb + b] = cnt_gone;
             }
-            if (!grid_barrier(g.ctrl, limit_ns)) return;
+            if (!grid_barrier(c, limit_ns)) return;
             PEEL_ADD(1, t_ph);
             // warp 0 reads every CTA's report
-            __shared__ int s_glob[3];
             if (wib == 0) {
-                int tle = 0, ple = 0, gm = INT_MAX;
+                int tle = 0, ple = 0, gm = INT_MAX, tgo = 0, pgo = 0;
                 for (int i = lane; i < nb; i += 32) {
-                    const int c = g.blk_cnt[phase * nb + i];
-                    tle += c;
-                    if (i < b) ple += c;
+                    const int cl = g.blk_cnt[phase * nb + i];
+                    const int cg = g.blk_gone[phase * nb + i];
+                    tle += cl;
+                    tgo += cg;
+                    if (i < b) { ple += cl; pgo += cg; }
                     gm = min(gm, g.blk_min[phase * nb + i]);
                 }
                 tle = __reduce_add_sync(0xffffffffu, tle);
                 ple = __reduce_add_sync(0xffffffffu, ple);
+                tgo = __reduce_add_sync(0xffffffffu, tgo);
+                pgo = __reduce_add_sync(0xffffffffu, pgo);
                 gm = __reduce_min_sync(0xffffffffu, gm);
                 if (tle == 0) {
                     int tm = 0, pm = 0;
                     for (int i = lane; i < nb; i += 32) {
-                        const int c = g.blk_min[phase * nb + i] == gm ? g.blk_cm[phase * nb + i] : 0;
-                        tm += c;
-                        if (i < b) pm += c;
+                        const int cm = g.blk_min[phase * nb + i] == gm ? g.blk_cm[phase * nb + i] : 0;
+                        tm += cm;
+                        if (i < b) pm += cm;
                     }
                     tle = __reduce_add_sync(0xffffffffu, tm);
                     ple = __reduce_add_sync(0xffffffffu, pm);
                 } else {
                     gm = k;
                 }
-                if (lane == 0) { s_glob[0] = tle; s_glob[1] = ple; s_glob[2] = gm; }
+                if (lane == 0) {
+                    s_glob[0] = tle; s_glob[1] = ple; s_glob[2] = gm; s_glob[3] = tgo;
+                    s_glob[4] = pgo;
+                }
             }
             __syncthreads();
             total = s_glob[0];
             prefix = s_glob[1];
             newk = s_glob[2];
+            total_gone = s_glob[3];
+            prefix_gone = s_glob[4];
             phase ^= 1;
         }
         k = newk;
         dmax = k;
+        if (b == 0 && tid == 0) g.rstart[r] = pos;
         // -- write: this round's removals in id order, and the stably compacted survivors
-        __shared__ int s_front[kPeelThreads * kPeelItems];   // this CTA's removed vertices
         const int my_first = pos + prefix;
-        int bf = my_first, bs = lo - prefix;
-        for (int t0 = lo; t0 < hi; t0 += tile) {
+        int bf = my_first, bs = lo - prefix - prefix_gone;
+        for (int t0 = lo; t0 < hi; t0 += kPeelTile) {
             if (!in_regs) {
 #pragma unroll
                 for (int j = 0; j < kPeelItems; ++j) {
                     const int i = t0 + tid * kPeelItems + j;
                     vid[j] = i < hi ? alive[i] : -1;
-                    vdg[j] = vid[j] >= 0 ? g.deg[vid[j]] : INT_MAX;
+                    vdg[j] = vid[j] < 0 ? INT_MAX : (g.round_of[vid[j]] >= 0 ? -1 : g.deg[vid[j]]);
                 }
             }
-            int nf = 0, nv = 0;
+            int nf = 0, ns = 0;
 #pragma unroll
             for (int j = 0; j < kPeelItems; ++j) {
-                nv += vid[j] >= 0;
-                nf += vid[j] >= 0 && vdg[j] <= k;
+                nf += vid[j] >= 0 && vdg[j] >= 0 && vdg[j] <= k;
+                ns += vid[j] >= 0 && vdg[j] > k;
             }
             int tot;
-            const int ex = block_excl_scan_int((nv << 16) | nf, &tot, sh);  // both < 2^16
-            const int rf = ex & 0xffff, rv = ex >> 16;
-            const int tf = tot & 0xffff, tv = tot >> 16;
-            int of = bf + rf, os = bs + (rv - rf);
+            const int ex = block_excl_scan_int((ns << 16) | nf, &tot, sh);  // both < 2^16
+            const int rf = ex & 0xffff, rs = ex >> 16;
+            const int tf = tot & 0xffff, ts = tot >> 16;
+            int of = bf + rf, os = bs + rs;
 #pragma unroll
             for (int j = 0; j < kPeelItems; ++j) {
                 const int v = vid[j];
-                if (v < 0) continue;
+                if (v < 0 || vdg[j] < 0) continue;
                 if (vdg[j] <= k) {
                     g.order[of] = v;
                     g.rank[v] = of;
@@ -311,27 +524,25 @@ __global__ void __launch_bounds__(kPeelThreads, 1) peel_kernel(DevGraph g, long 
                 }
             }
             bf += tf;
-            bs += tv - tf;
+            bs += ts;
         }
         // degrees re-read by the write step (slices longer than one tile) must not move before
         // every CTA has written
         if (in_regs || solo) __syncthreads();
-        else if (!grid_barrier(g.ctrl, limit_ns)) return;
+        else if (!grid_barrier(c, limit_ns)) return;
         PEEL_ADD(2, t_ph);
-        // -- remove this CTA's vertices: one warp per vertex, lanes over its neighbours; a vertex
-        // with kPeelBigDegree or more neighbours is queued and then handled by the whole CTA
-        __shared__ int s_big[kPeelBigQueue];
-        __shared__ int s_nbig;
-        __shared__ unsigned long long s_rd;       // adjacency entries this CTA removes
+        // -- remove this CTA's vertices: one warp per vertex, lanes over its neighbours
+        // (kPeelInFlight at a time); a vertex with kPeelBigDegree or more neighbours is queued
+        // and then handled by the whole CTA
         if (tid == 0) {
             s_nbig = 0;
             s_rd = 0ULL;
         }
         __syncthreads();
+        int *fcnt = &c->front_cnt[fr_out];
         for (int e = wib; e < bf - my_first; e += wpb) {
             const int v = in_regs ? s_front[e] : g.order[my_first + e];
             const int elo = g.offs[v], ehi = g.offs[v + 1];
-            if (lane == 0) atomicAdd(&s_rd, (unsigned long long)(ehi - elo));
             if (ehi - elo >= kPeelBigDegree) {
                 int slot = 0;
                 if (lane == 0) slot = atomicAdd(&s_nbig, 1);
@@ -341,10 +552,23 @@ __global__ void __launch_bounds__(kPeelThreads, 1) peel_kernel(DevGraph g, long 
                     continue;
                 }
             }
-            for (int j = elo + lane; j < ehi; j += 32) atomicSub(&g.deg[g.adj[j]], 1);
+            if (lane == 0) atomicAdd(&s_rd, (unsigned long long)(ehi - elo));
+            for (int j0 = elo; j0 < ehi; j0 += 32 * kPeelInFlight) {
+                int u[kPeelInFlight], old[kPeelInFlight];
+#pragma unroll
+                for (int t = 0; t < kPeelInFlight; ++t) {
+                    const int j = j0 + t * 32 + lane;
+                    u[t] = j < ehi ? __ldg(g.adj + j) : -1;
+                }
+#pragma unroll
+                for (int t = 0; t < kPeelInFlight; ++t)
+                    old[t] = u[t] >= 0 ? atomicSub(&g.deg[u[t]], 1) : 0;
+#pragma unroll
+                for (int t = 0; t < kPeelInFlight; ++t)
+                    front_append(u[t] >= 0 && old[t] == k + 1, u[t], front_out, fcnt);
+            }
 #ifdef MCE_PROFILE
-            if (lane == 0 && blockIdx.x == 0)
-                atomicMax(&g.ctrl->peel_prof[6], (unsigned long long)(ehi - elo));
+            if (lane == 0 && blockIdx.x == 0) atomicMax(&c->peel_prof[6], (unsigned long long)(ehi - elo));
 #endif
         }
         __syncthreads();
@@ -352,33 +576,81 @@ __global__ void __launch_bounds__(kPeelThreads, 1) peel_kernel(DevGraph g, long 
         for (int i = 0; i < nbig; ++i) {
             const int v = s_big[i];
             const int elo = g.offs[v], ehi = g.offs[v + 1];
-            for (int j = elo + tid; j < ehi; j += nthr) atomicSub(&g.deg[g.adj[j]], 1);
+            if (tid == 0) s_rd += (unsigned long long)(ehi - elo);
+            for (int j0 = elo + wib * 32 * kPeelInFlight; j0 < ehi; j0 += nthr * kPeelInFlight) {
+                int u[kPeelInFlight], old[kPeelInFlight];
+#pragma unroll
+                for (int t = 0; t < kPeelInFlight; ++t) {
+                    const int j = j0 + t * 32 + lane;
+                    u[t] = j < ehi ? __ldg(g.adj + j) : -1;
+                }
+#pragma unroll
+                for (int t = 0; t < kPeelInFlight; ++t)
+                    old[t] = u[t] >= 0 ? atomicSub(&g.deg[u[t]], 1) : 0;
+#pragma unroll
+                for (int t = 0; t < kPeelInFlight; ++t)
+                    front_append(u[t] >= 0 && old[t] == k + 1, u[t], front_out, fcnt);
+            }
 #ifdef MCE_PROFILE
-            if (tid == 0 && blockIdx.x == 0)
-                atomicMax(&g.ctrl->peel_prof[6], (unsigned long long)(ehi - elo));
+            if (tid == 0 && blockIdx.x == 0) atomicMax(&c->peel_prof[6], (unsigned long long)(ehi - elo));
 #endif
         }
         if (!solo && tid == 0) g.blk_rd[b] = (long long)s_rd;
         __syncthreads();
         PEEL_ADD(3, t_ph);
         if (solo) __syncthreads();
-        else if (!grid_barrier(g.ctrl, limit_ns)) return;
+        else if (!grid_barrier(c, limit_ns)) return;
         PEEL_ADD(4, t_ph);
 #ifdef MCE_PROFILE
-        if (blockIdx.x == 0 && tid == 0) g.ctrl->peel_prof[5 + (solo ? 8 : 0)]++;
+        if (blockIdx.x == 0 && tid == 0) c->peel_prof[5 + prof_off]++;
 #endif
-        live_sum += n_alive;
+        // every CTA learns how many adjacency entries the round removed
+        if (!solo) {
+            if (wib == 0) {
+                long long t = 0;
+                for (int i = lane; i < nb; i += 32) t += g.blk_rd[i];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+                if (lane == 0) s_removed = t;
+            }
+            __syncthreads();
+            live_entries -= s_removed;
+        } else {
+            live_entries -= (long long)s_rd;
+        }
+        live_sum += n_live;
         pos += total;
         n_alive -= total;
+        n_live -= total + total_gone;
         ++r;
         int *t = alive;
         alive = alive_next;
         alive_next = t;
     }
     if (blockIdx.x == 0 && tid == 0) {
-        g.ctrl->degeneracy = dmax;
-        g.ctrl->rounds = r;
-        g.ctrl->peel_live = live_sum;
+        c->degeneracy = dmax;
+        c->rounds = r;
+        c->peel_live = live_sum;
+        g.rstart[r] = pos;
+    }
+    // -- rank pass: each frontier round's places in the order sorted by id (rounds are (round,
+    // id) ranked), then every vertex of such a round gets its rank
+    if (solo) __syncthreads();
+    else if (!grid_barrier(c, limit_ns)) return;
+    for (int q = b; q < r; q += nb) {
+        const int s0 = g.rstart[q];
+        if (!(s0 & kRoundUnsorted)) continue;
+        const int start = s0 & ~kRoundUnsorted, end = g.rstart[q + 1] & ~kRoundUnsorted;
+        const int cnt = end - start;             // <= kFrontCap
+        for (int i = tid; i < cnt; i += nthr) s_front[i] = g.order[start + i];
+        __syncthreads();
+        block_sort(s_front, cnt);                // ends with __syncthreads
+        for (int i = tid; i < cnt; i += nthr) {
+            const int v = s_front[i];
+            g.order[start + i] = v;
+            g.rank[v] = start + i;
+        }
+        __syncthreads();
     }
 }
 
@@ -604,15 +876,27 @@ cudaError_t launch_unit_offsets(const DevGraph &g, const int *roots, int n_roots
     return cudaGetLastError();
 }
 
-// The whole peel: one cooperative launch over peel_blocks CTAs.
+// The whole peel: one cooperative launch over peel_blocks CTAs (its dynamic shared memory
+// exceeds the default 48 KiB: the limit is raised once per device).
 cudaError_t launch_peel(const DevGraph &g, int peel_blocks, long long spin_limit_ns,
                         cudaStream_t s)
 {
+    constexpr int kMaxDev = 64;
+    static bool configured[kMaxDev] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDev || !configured[dev]) {
+        e = cudaFuncSetAttribute((const void *)peel_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPeelSmemBytes);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < kMaxDev) configured[dev] = true;
+    }
     DevGraph gg = g;
     long long lim = spin_limit_ns;
     void *args[] = {&gg, &lim};
     return cudaLaunchCooperativeKernel((const void *)peel_kernel, dim3(peel_blocks),
-                                       dim3(kPeelThreads), args, 0, s);
+                                       dim3(kPeelThreads), args, kPeelSmemBytes, s);
 }
 
 cudaError_t launch_order(const DevGraph &g, int peel_blocks, long long spin_limit_ns,
@@ -662,7 +946,8 @@ namespace {
 constexpr int kNoAllocMaxN = 1 << 18;        // vertices
 constexpr int kNoAllocMaxBlocks = 1024;      // CTAs of the cooperative peel
 constexpr int kNoAllocCtrlWords = (int)((sizeof(DevCtrl) + 255) / 256 * 64);
-constexpr int kNoAllocWords = kNoAllocCtrlWords + 8 * kNoAllocMaxBlocks + 5 * kNoAllocMaxN;
+constexpr int kNoAllocWords = kNoAllocCtrlWords + 10 * kNoAllocMaxBlocks + 3 * kFrontCap +
+                              6 * kNoAllocMaxN + 64;
 constexpr int kNoAllocMaxDevices = 64;
 
 // The whole scratch area: 5 MiB + a few KiB, held by every device that loads the library.
@@ -727,11 +1012,14 @@ extern "C" mce_status mce_order_noalloc(const int32_t *d_offsets, const int32_t 
     g.blk_min = g.blk_cnt + 2 * kNoAllocMaxBlocks;
     g.blk_cm = g.blk_min + 2 * kNoAllocMaxBlocks;
     g.blk_rd = reinterpret_cast<long long *>(g.blk_cm + 2 * kNoAllocMaxBlocks);
-    g.deg = g.blk_cm + 4 * kNoAllocMaxBlocks;
+    g.blk_gone = g.blk_cm + 4 * kNoAllocMaxBlocks;
+    g.front = g.blk_gone + 2 * kNoAllocMaxBlocks;
+    g.deg = g.front + 3 * kFrontCap;
     g.round_of = g.deg + kNoAllocMaxN;
     g.alive_a = g.round_of + kNoAllocMaxN;
     g.alive_b = g.alive_a + kNoAllocMaxN;
     g.order = g.alive_b + kNoAllocMaxN;
+    g.rstart = g.order + kNoAllocMaxN;        // rounds <= n, plus one
     noalloc_prep_kernel<<<1, 1, 0, s>>>();
     if (cudaGetLastError() != cudaSuccess) return MCE_ERR_CUDA;
     if (n > 0 && launch_peel(g, blocks, 20LL * 1000 * 1000 * 1000, s) != cudaSuccess) {
