@@ -524,8 +524,9 @@ static mce_status order_impl(mce_graph *h, cudaStream_t s)
         MCE_TRY(cudaEventRecord(h->ev_order[1], s));
         h->order_timed = true;
     }
-    // peel, orient count (with the split) / scan / scatter (+ subtree count and its scan)
-    h->launches_order = h->n > 0 ? (h->g.l2 ? 8 : 4) : 0;
+    // peel, its rank pass, orient count (with the split) / scan / scatter (+ subtree count and
+    // its scan)
+    h->launches_order = h->n > 0 ? (h->g.l2 ? 9 : 5) : 0;
     return MCE_OK;
 }
 

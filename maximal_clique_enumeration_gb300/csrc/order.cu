@@ -242,9 +242,9 @@ __device__ void block_sort(int *s, int cnt)
 //   (the frontier): no scan and no exchange, every CTA takes a share of the frontier's
 //   vertices (round, core number, unsorted place in the order) and of their adjacency entries.
 // Every round's edge removal collects the next frontier.  Grid barriers: two per scan round
-// (after the reports, and at the end), one per frontier round.  After the last round a pass
-// sorts each frontier round's vertices by id in place and writes their ranks.  Once few
-// vertices and few edges remain, CTA 0 goes on alone (CTA barriers only).
+// (after the reports, and at the end), one per frontier round.  A second kernel then sorts
+// each frontier round's vertices by id in place and writes their ranks.  Once few vertices and
+// few edges remain, CTA 0 goes on alone (CTA barriers only).
 __global__ void __launch_bounds__(kPeelThreads, 1) peel_kernel(DevGraph g, long long limit_ns)
 {
     extern __shared__ int s_dyn[];
@@ -633,20 +633,26 @@ __global__ void __launch_bounds__(kPeelThreads, 1) peel_kernel(DevGraph g, long 
         c->peel_live = live_sum;
         g.rstart[r] = pos;
     }
-    // -- rank pass: each frontier round's places in the order sorted by id (rounds are (round,
-    // id) ranked), then every vertex of such a round gets its rank
-    if (solo) __syncthreads();
-    else if (!grid_barrier(c, limit_ns)) return;
-    for (int q = b; q < r; q += nb) {
+}
+
+// Rank pass after the peel: each frontier round's places in the order sorted by id (a vertex's
+// rank is its (round, id) position), then every vertex of such a round gets its rank.  One
+// round per CTA at a time.
+__global__ void __launch_bounds__(kPeelThreads) peel_rank_kernel(DevGraph g)
+{
+    __shared__ int s[kFrontCap];
+    if (load_status(g.ctrl) != 0) return;
+    const int rounds = g.ctrl->rounds;
+    for (int q = blockIdx.x; q < rounds; q += gridDim.x) {
         const int s0 = g.rstart[q];
         if (!(s0 & kRoundUnsorted)) continue;
         const int start = s0 & ~kRoundUnsorted, end = g.rstart[q + 1] & ~kRoundUnsorted;
         const int cnt = end - start;             // <= kFrontCap
-        for (int i = tid; i < cnt; i += nthr) s_front[i] = g.order[start + i];
+        for (int i = threadIdx.x; i < cnt; i += blockDim.x) s[i] = g.order[start + i];
         __syncthreads();
-        block_sort(s_front, cnt);                // ends with __syncthreads
-        for (int i = tid; i < cnt; i += nthr) {
-            const int v = s_front[i];
+        block_sort(s, cnt);                      // ends with __syncthreads
+        for (int i = threadIdx.x; i < cnt; i += blockDim.x) {
+            const int v = s[i];
             g.order[start + i] = v;
             g.rank[v] = start + i;
         }
@@ -895,8 +901,11 @@ cudaError_t launch_peel(const DevGraph &g, int peel_blocks, long long spin_limit
     DevGraph gg = g;
     long long lim = spin_limit_ns;
     void *args[] = {&gg, &lim};
-    return cudaLaunchCooperativeKernel((const void *)peel_kernel, dim3(peel_blocks),
-                                       dim3(kPeelThreads), args, kPeelSmemBytes, s);
+    e = cudaLaunchCooperativeKernel((const void *)peel_kernel, dim3(peel_blocks),
+                                    dim3(kPeelThreads), args, kPeelSmemBytes, s);
+    if (e != cudaSuccess) return e;
+    peel_rank_kernel<<<peel_blocks, kPeelThreads, 0, s>>>(g);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_order(const DevGraph &g, int peel_blocks, long long spin_limit_ns,
