@@ -49,8 +49,8 @@ WIDTHS = [1, 2, 4, 8, 16, 32]
 # workload (dram bytes read + written per counted bitset word).  It is scaled to a full launch
 # by the counted words, and only reported while the kernel sources hash to the version that
 # was captured.
-TRAFFIC_CAPTURE = {"sources": "b4a4ad260dfd7168", "width_class": 2,
-                   "bytes_per_word": 93.36e6 / 86953769.0}
+TRAFFIC_CAPTURE = {"sources": "b1a61f1bdc2488a9", "width_class": 2,
+                   "bytes_per_word": (86.808320e6 + 5.469184e6) / 90368612.0}
 KERNEL_SOURCES = ["maximal_clique_enumeration_gb300/csrc/search_impl.cuh",
                   "maximal_clique_enumeration_gb300/csrc/search_full.cu",
                   "maximal_clique_enumeration_gb300/csrc/mce_internal.cuh"]
