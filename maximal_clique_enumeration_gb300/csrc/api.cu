@@ -18,12 +18,20 @@ struct mce_graph {
     int sm_count = 0;
     int peel_blocks = 0;
     int search_threads = 0, n_workers = 0;
+    int build_blocks[3] = {};  // CTAs of the build launches of row width 1, 2, 4 words
     // per launch group g = 2k + b (row width 1 << k; b = 0 big-workspace roots, 1 the rest)
     int grp_blocks[kNumGroups] = {}, grp_workers[kNumGroups] = {}, grp_count[kNumGroups] = {};
     unsigned long long grp_ws[kNumGroups] = {};
     size_t cls_smem[kNumClasses] = {};
     long long uroots_cap = 0;
+    int n_uroots = 0;         // length of the caller's root list of the current call
     int small_lo = 1, small_hi = kSmallP;     // |P| range of the nodes solved whole
+    bool records = true;      // build the subtrees of narrow roots ahead of the search
+    int record_mask = 7;      // of the row widths 1, 2, 4 words (bits 0, 1, 2)
+    unsigned *bb = nullptr;   // their records (bb_quads quads) and offsets by schedule place
+    long long bb_quads = 0;
+    long long *rec_off = nullptr, *rec_scan = nullptr;
+    long long *urec_off = nullptr, *urec_scan = nullptr;   // the same for a caller's roots
     bool unit_own = false;    // unit_cnt / unit_scan were reallocated for a caller's root list
     int degeneracy = 0, max_degree = 0, hist_len = 2, rounds = 0;
     unsigned long long ws_words = 0;
@@ -222,6 +230,11 @@ mce_status run_search(mce_graph *h, cudaStream_t s, bool user_roots, const DevOu
     a.spin_limit_ns = h->cfg.spin_limit_ns;
     a.small_lo = h->small_lo;
     a.small_hi = h->small_hi;
+    if (h->bb) {
+        a.bb = h->bb;
+        a.bb_quads = h->bb_quads;
+        a.rec_off = user_roots ? h->urec_off : h->rec_off;
+    }
     for (int o = 0; o < kNumGroups; ++o) {
         const int gi = group_at(o), k = gi / 2;
         if (h->grp_workers[gi] == 0) continue;            // no vertex of the graph in this group
@@ -233,12 +246,25 @@ mce_status run_search(mce_graph *h, cudaStream_t s, bool user_roots, const DevOu
         MCE_TRY(cudaMemsetAsync(h->flag, 0, sizeof(int) * (size_t)a.n_workers, s));
         MCE_TRY(launch_search_prep(a, s));
         if (h->cfg.profile) MCE_TRY(cudaEventRecord(h->ev_grp[gi][0], s));
-        MCE_TRY(launch_search(a, h->grp_blocks[gi], h->search_threads, h->cls_smem[k], s));
+        // normal roots of row width <= 4 words: subtrees built ahead when the records fit (the
+        // schedule's always do; a caller's list is checked on the device, and the plain search
+        // launch after the record search does the work when they do not)
+        const bool rec = a.bb && (gi & 1) && k <= 2 && ((h->record_mask >> k) & 1);
+        a.rec_gate = rec ? a.rec_off + (user_roots ? h->n_uroots : h->n) : nullptr;
+        if (rec) {
+            MCE_TRY(launch_build(a, h->build_blocks[k], s));
+            MCE_TRY(launch_search(a, h->grp_blocks[gi], h->search_threads, h->cls_smem[k], true,
+                                  s));
+            h->launches_count += user_roots ? 2 : 1;   // build (+ the plain search launch)
+        }
+        if (!rec || user_roots)
+            MCE_TRY(launch_search(a, h->grp_blocks[gi], h->search_threads, h->cls_smem[k],
+                                  false, s));
         if (h->cfg.profile) {
             MCE_TRY(cudaEventRecord(h->ev_grp[gi][1], s));
             h->grp_timed[gi] = true;
         }
-        h->launches_count += 2;
+        h->launches_count += 2;                           // prep and search
     }
     return MCE_OK;
 }
@@ -438,6 +464,11 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
                 group_per_sm[gi] = h->cfg.blocks_per_sm;
         }
     }
+    for (int k = 0; k < 3; ++k) {
+        int per_sm = 0;
+        MCE_TRY(build_occupancy(k, &per_sm));
+        h->build_blocks[k] = (per_sm > 0 ? per_sm : 1) * h->sm_count;
+    }
     for (int gi = 0; gi < kNumGroups; ++gi) {
         const bool big = (gi & 1) == 0;
         h->grp_count[gi] = c.cls[2 * gi + 1] - c.cls[2 * gi];
@@ -460,6 +491,24 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
     }
     h->ws_words = ws_total;
     MCE_ALLOC(h, h->ws, ws_total);
+    // subtrees built ahead of the search (full induced subgraphs of first-level subtrees): one
+    // record per root of the schedule's normal launch groups of row width <= 4 words, when all
+    // of them fit in kRecCapQuads
+    if (h->records && !g.ip && !g.l2 && n > 0) {
+        MCE_ALLOC(h, h->rec_off, (size_t)n + 1);
+        MCE_ALLOC(h, h->rec_scan, (size_t)n / kScanBlock + 2);
+        MCE_TRY(launch_record_offsets(g, g.sched, g.ctrl->cls, n, h->rec_scan, h->rec_off, s));
+        long long total = 0;
+        MCE_TRY(cudaMemcpyAsync(&total, h->rec_off + n, sizeof(long long),
+                                cudaMemcpyDeviceToHost, s));
+        MCE_TRY(cudaStreamSynchronize(s));
+        // all or nothing: without room for every record the search builds every subtree
+        if (total > 0 && total <= kRecCapQuads &&
+            dev_alloc(h, &h->bb, (size_t)total * 4) == MCE_OK)
+            h->bb_quads = total;
+        else
+            h->bb = nullptr;
+    }
     MCE_ALLOC(h, h->ring, (size_t)h->n_workers);
     MCE_ALLOC(h, h->flag, (size_t)h->n_workers);
     MCE_ALLOC(h, h->ring_seq, (size_t)h->n_workers);
@@ -499,6 +548,8 @@ mce_status mce_create(const int32_t *offsets, const int32_t *adj, int32_t n, int
     // measurement builds only: the solver's |P| range from the environment
     if (const char *e = getenv("MCE_AB_SMALL_LO")) h->small_lo = atoi(e);
     if (const char *e = getenv("MCE_AB_SMALL_HI")) h->small_hi = atoi(e);
+    if (const char *e = getenv("MCE_AB_RECORDS")) h->records = atoi(e) != 0;
+    if (const char *e = getenv("MCE_AB_RECORD_MASK")) h->record_mask = atoi(e);
     if (h->small_hi > kSmallPMax) h->small_hi = kSmallPMax;
 #endif
     mce_status st = create_impl(h, offsets, adj, n, is_device_ptr, (cudaStream_t)stream);
@@ -520,13 +571,18 @@ static mce_status order_impl(mce_graph *h, cudaStream_t s)
     if (h->cfg.profile) MCE_TRY(cudaEventRecord(h->ev_order[0], s));
     MCE_TRY(launch_order(h->g, h->peel_blocks, h->cfg.spin_limit_ns, s,
                          h->cfg.profile && h->n > 0 ? h->ev_order[2] : nullptr));
+    // the schedule places the roots of a bucket in a different order at each call: the
+    // records' offsets follow it (their total does not change)
+    if (h->bb)
+        MCE_TRY(launch_record_offsets(h->g, h->g.sched, h->g.ctrl->cls, h->n, h->rec_scan,
+                                      h->rec_off, s));
     if (h->cfg.profile) {
         MCE_TRY(cudaEventRecord(h->ev_order[1], s));
         h->order_timed = true;
     }
     // peel, its rank pass, orient count (with the split) / scan / scatter (+ subtree count and
     // its scan)
-    h->launches_order = h->n > 0 ? (h->g.l2 ? 9 : 5) : 0;
+    h->launches_order = h->n > 0 ? (h->g.l2 ? 9 : 5) + (h->bb ? 3 : 0) : 0;
     return MCE_OK;
 }
 
@@ -573,9 +629,23 @@ static mce_status count_impl(mce_graph *h, cudaStream_t s, const int32_t *d_root
                 MCE_ALLOC(h, h->g.unit_scan, len / kScanBlock + 2);
                 h->unit_own = true;
             }
+            if (h->bb) {
+                // offsets of the records of the caller's roots, and their scan scratch
+                dev_free(h, h->urec_off, s);
+                dev_free(h, h->urec_scan, s);
+                h->urec_off = h->urec_scan = nullptr;
+                MCE_ALLOC(h, h->urec_off, (size_t)cap + 1);
+                MCE_ALLOC(h, h->urec_scan, (size_t)cap / kScanBlock + 2);
+            }
             h->uroots_cap = cap;
         }
+        h->n_uroots = (int)n_roots;
         MCE_TRY(launch_bin_roots(h->g, d_roots, (int)n_roots, s));
+        if (h->bb) {
+            MCE_TRY(launch_record_offsets(h->g, h->g.uroots, h->g.ctrl->ucls, (int)n_roots,
+                                          h->urec_scan, h->urec_off, s));
+            h->launches_count += 3;
+        }
         if (h->g.l2) {
             MCE_TRY(launch_unit_offsets(h->g, h->g.uroots, (int)n_roots, h->g.uroots_uoff, s));
             h->launches_count += 4;
@@ -731,7 +801,7 @@ mce_status mce_get_info(mce_graph *h, mce_info *info)
     info->hist_len = h->hist_len;
     info->peel_rounds = c.rounds;
     info->n_workers = h->n_workers;
-    info->workspace_bytes = (long long)(h->ws_words * 4ULL);
+    info->workspace_bytes = (long long)(h->ws_words * 4ULL) + h->bb_quads * 16;
     info->induced = h->g.ip ? 2 : 1;
     info->subtree_level = h->g.l2 ? 2 : 1;
     info->tree_nodes = c.tree_nodes;

@@ -117,6 +117,10 @@ struct SearchArgs {
     int cls;                 // row-width class of this launch (W = 1 << cls)
     int group;               // launch group (2 cls + 0 for big-workspace roots, + 1 otherwise)
     int small_lo, small_hi;  // nodes with small_lo <= |P| <= small_hi are solved whole
+    unsigned *bb;            // records of subtrees built ahead (null: none), bb_quads quads
+    long long bb_quads;
+    const long long *rec_off;  // quad offset of each root's record, by place in `roots` (+1)
+    const long long *rec_gate; // the records' total: they are in use iff it is <= bb_quads
     unsigned int *ws;        // per-warp workspace, ws_words each
     unsigned long long ws_words;
     int *ring;               // worker list: ring of idle warp ids [n_workers]
@@ -180,6 +184,43 @@ __host__ __device__ inline WsLayout ws_layout(int deg, int np, bool ip, bool l2)
     return l;
 }
 
+// Record of a first-level root built ahead of the search (full induced subgraph; 32-bit word
+// offsets from the record's start): header (np, nx, live X rows, covered), rows ((np + nx) * W),
+// P's ids (np), P's keys (2 np, 8-byte aligned), X's ids while building and then the indices
+// of the live X rows (nx).  Records start on 16-byte boundaries; sizes are kept in quads.
+struct RecLayout {
+    long long rows, pids, pkey, xx, total;
+};
+
+__host__ __device__ inline RecLayout rec_layout(int deg, int np, int W)
+{
+    RecLayout l;
+    long long o = 4;
+    l.rows = o; o += (long long)deg * W;
+    l.pids = o; o += np;
+    o = (o + 1) & ~1LL;
+    l.pkey = o; o += 2LL * np;
+    l.xx = o; o += deg - np;
+    l.total = (o + 3) & ~3LL;
+    return l;
+}
+
+__host__ __device__ inline long long rec_quads(int deg, int np, int W)
+{
+    return rec_layout(deg, np, W).total / 4;
+}
+
+constexpr long long kRecCapQuads = 1LL << 30;   // records of subtrees built ahead: 16 GiB at most
+#ifndef MCE_BUILD_MIN_BLOCKS
+#define MCE_BUILD_MIN_BLOCKS 4
+#endif
+#ifndef MCE_BUILD_BATCH
+#define MCE_BUILD_BATCH 16
+#endif
+constexpr int kBuildThreads = 256;
+constexpr int kBuildMinBlocks = MCE_BUILD_MIN_BLOCKS;
+constexpr int kBuildBatch = MCE_BUILD_BATCH;   // later-neighbour entries a lane has in flight
+
 // Schedule buckets: launch groups in launch order (widest rows first; per width the roots with
 // a big workspace, then the rest) and, inside a group, roots with a larger estimated cost
 // (|P| + 1)^2 * (core(v) + 1) first (log2 buckets).  Bucket 0 holds over-limit roots (group of
@@ -218,9 +259,22 @@ cudaError_t launch_order(const DevGraph &g, int peel_blocks, long long spin_limi
                          cudaStream_t s, cudaEvent_t ev_peel);
 cudaError_t launch_peel(const DevGraph &g, int peel_blocks, long long spin_limit_ns,
                         cudaStream_t s);
-cudaError_t launch_search(const SearchArgs &a, int blocks, int threads, size_t smem,
+// The search launch of launch group a.group; rec selects the variant that searches records.
+cudaError_t launch_search(const SearchArgs &a, int blocks, int threads, size_t smem, bool rec,
                           cudaStream_t s);
 cudaError_t launch_search_prep(const SearchArgs &a, cudaStream_t s);
+// Subtrees built ahead: rec_off[i] = quad offset of the record of the root at place i of
+// roots[0 .. n_slots) (the roots of the normal launch groups of row width <= 4 words have one;
+// range = the launch groups' places), rec_off[n_slots] = the total; scan_tmp holds
+// n_slots / kScanBlock + 2 partial sums.
+cudaError_t launch_record_offsets(const DevGraph &g, const int *roots, const int *range,
+                                  int n_slots, long long *scan_tmp, long long *rec_off,
+                                  cudaStream_t s);
+// The build launch of normal launch group a.group (row width 1 << a.cls <= 4 words).
+cudaError_t launch_build(const SearchArgs &a, int blocks, cudaStream_t s);
+// CTAs per SM of that build kernel.
+cudaError_t build_occupancy(int cls, int *blocks_per_sm);
+const void *build_kernel_full(int cls);
 // CTAs per SM of the kernel of launch group `group` (row-width class group / 2).
 cudaError_t search_occupancy(int group, int ip, int l2, int threads, size_t smem,
                              int *blocks_per_sm);
@@ -237,6 +291,10 @@ __host__ __device__ inline size_t warp_smem_bytes(int k)
 {
     return (size_t)hash_slots(k) * 8 + kFilterWords * 4 + 2 * 36 * 4 +
            (size_t)smem_row_words(k) * 4;
+}
+__host__ __device__ inline size_t build_smem_per_warp(int k)
+{
+    return (size_t)hash_slots(k) * 8 + kFilterWords * 4 + 2 * 36 * 4;
 }
 __host__ __device__ inline size_t search_smem_bytes(int k, int hist_len, int warps)
 {

@@ -18,4 +18,22 @@ const void *search_kernel_full(int cls, bool big)
     }
 }
 
+const void *search_kernel_full_rec(int cls)
+{
+    switch (cls) {
+    case 0: return (const void *)search_kernel<1, false, true>;
+    case 1: return (const void *)search_kernel<2, false, true>;
+    default: return (const void *)search_kernel<4, false, true>;
+    }
+}
+
+const void *build_kernel_full(int cls)
+{
+    switch (cls) {
+    case 0: return (const void *)build_kernel<1>;
+    case 1: return (const void *)build_kernel<2>;
+    default: return (const void *)build_kernel<4>;
+    }
+}
+
 }  // namespace mce

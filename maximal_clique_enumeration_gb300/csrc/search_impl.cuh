@@ -962,11 +962,10 @@ __device__ __forceinline__ int hash_find(const WarpSmem &sm, int id)
 // are taken 32 at a time; the warp walks the concatenation of their lists N+(u_t) with
 // consecutive lanes on consecutive entries (coalesced), WalkBatch entries per lane in flight.  A
 // hit on p_j sets bit j of row t, and, when u_t = p_t is in P, bit t of row j as well.
-template <int W>
+template <int W, int kB = WalkBatch<W>::value>
 __device__ void build_flat(const SearchArgs &a, const RootCtx &r, const WarpSmem &h, int deg,
                            int np, int lane)
 {
-    constexpr int kB = WalkBatch<W>::value;
     unsigned *rows = r.rowsP;   // rowsX follows rowsP directly
     for (int g0 = 0; g0 < deg; g0 += 32) {
         const int t = g0 + lane;
@@ -1338,6 +1337,167 @@ __device__ void search_root(const SearchArgs &a, unsigned *ws, const WarpSmem &s
     build_and_search<W, big>(a, r, sm, vertex_key(v), acc, s_hist, lane);
 }
 
+// ------------------------------------------------------------------ subtrees built ahead
+//
+// The default search (full induced subgraphs, first-level subtrees) of the normal roots of
+// row width W <= 4 runs in two launches per launch group: build_kernel builds every root's
+// induced subgraph into a record of its own (RecLayout), then the search kernel searches the
+// records.  The build is a walk of later-neighbour lists that waits on L2 gathers; in a kernel
+// of its own it runs with few registers at 32 warps per SM and kBuildBatch loads in flight per
+// lane, where the search kernel of 4-word rows holds 24 warps and 12 loads.  The search kernel
+// copies the P rows and only the X rows with a neighbour in P into shared memory when they fit
+// (more roots fit than when every X row is copied), and otherwise reads the rows in the
+// record.  Records are all or nothing: when they do not fit, every subtree is built by the
+// search kernel itself.
+
+// Are the records in use for this launch group?  (The build kernel and both search variants
+// read the same total, so exactly one search variant does the work.)
+__device__ __forceinline__ bool records_on(const SearchArgs &a)
+{
+    return a.rec_gate != nullptr && *a.rec_gate <= a.bb_quads;
+}
+
+// Does the root at place i of the list have a record?  (Both kernels decide by this alone.)
+__device__ __forceinline__ bool has_record(const SearchArgs &a, int i)
+{
+    return a.bb != nullptr && a.rec_off[i + 1] > a.rec_off[i] && a.rec_off[i + 1] <= a.bb_quads;
+}
+
+// Is the record at place i sized for a root of this degree and |P|?  (Always, unless the
+// offsets were computed for another arrangement of the list: then the kernels report
+// MCE_ERR_INTERNAL instead of writing past the record.)
+__device__ __forceinline__ bool record_matches(const SearchArgs &a, int i, int deg, int np, int W)
+{
+    return a.rec_off[i + 1] - a.rec_off[i] == rec_quads(deg, np, W);
+}
+
+// Builds the record of first-level root v (deg neighbours, np of them later) at rec.
+template <int W>
+__device__ void build_record(const SearchArgs &a, const WarpSmem &sm, int v, int deg, int np,
+                             unsigned *rec, int lane)
+{
+    constexpr int CH = Geo<W>::CH;
+    const RecLayout L = rec_layout(deg, np, W);
+    const unsigned lt = (1u << lane) - 1u;
+    RootCtx r{};
+    r.rowsP = rec + L.rows;
+    r.rowsX = r.rowsP + (long long)np * W;
+    r.pids = reinterpret_cast<int *>(rec + L.pids);
+    r.pkey = reinterpret_cast<unsigned long long *>(rec + L.pkey);
+    r.xids = reinterpret_cast<int *>(rec + L.xx);       // X's ids while building
+    r.xx = r.xids;                                      // then the live X rows, in place
+    r.np = np;
+    r.nx = deg - np;
+    r.deg = deg;
+    // split N(v) into P (later) and X (earlier), each in id order
+    const int *Nv = a.g.adj + a.g.offs[v];
+    const int rv = a.g.rank[v];
+    if (deg > 32 * kBatch) {
+        split_wide(a.g, Nv, deg, rv, r.pids, r.xids, lane);
+    } else {
+        int pi = 0, xi = 0;
+        for (int base = 0; base < deg; base += 32) {
+            const int j = base + lane;
+            const bool in = j < deg;
+            const int w = in ? __ldg(Nv + j) : 0;
+            const bool isP = in && __ldg(a.g.rank + w) > rv;
+            const unsigned mp = __ballot_sync(kFull, isP);
+            const unsigned mx = __ballot_sync(kFull, in && !isP);
+            if (isP) r.pids[pi + __popc(mp & lt)] = w;
+            else if (in) r.xids[xi + __popc(mx & lt)] = w;
+            pi += __popc(mp);
+            xi += __popc(mx);
+        }
+    }
+    for (long long t = (long long)lane * CH; t < (long long)deg * W; t += 32 * CH)
+        ck_store<CH>(r.rowsP + t, ck_zero<CH>());
+    int slots = 32;
+    while (slots < 2 * np) slots <<= 1;
+    WarpSmem h = sm;
+    h.slots = slots;
+    for (int i = lane; i < slots; i += 32) h.hkey[i] = -1;
+    for (int i = lane; i < kFilterWords; i += 32) h.filter[i] = 0u;
+    __syncwarp();
+    for (int i = lane; i < np; i += 32) {
+        const int id = r.pids[i];
+        unsigned sl = hash_slot(id, slots - 1);
+        while (atomicCAS(&h.hkey[sl], -1, id) != -1) sl = (sl + 1) & (unsigned)(slots - 1);
+        h.hval[sl] = i;
+        const unsigned f = filter_bit(id);
+        atomicOr(&h.filter[f >> 5], 1u << (f & 31));
+    }
+    __syncwarp();
+    build_flat<W, kBuildBatch>(a, r, h, deg, np, lane);
+    // the X rows with a neighbour in P, and whether one X vertex is adjacent to all of P (then
+    // the subtree holds no maximal clique: that vertex would be the root's Tomita pivot with
+    // nothing left to branch on)
+    int nxx = 0;
+    bool covered = false;
+    for (int base = 0; base < r.nx; base += 32) {
+        const int xi = base + lane;
+        int cnt = 0;
+        if (xi < r.nx)
+            for (int k = 0; k < W; ++k) cnt += __popc(r.rowsX[(long long)xi * W + k]);
+        covered = covered || __any_sync(kFull, cnt == np);
+        const unsigned m = __ballot_sync(kFull, cnt > 0);
+        if (cnt > 0) r.xx[nxx + __popc(m & lt)] = xi;
+        nxx += __popc(m);
+    }
+    for (int i = lane; i < np; i += 32) r.pkey[i] = vertex_key(r.pids[i]);
+    if (lane == 0) {
+        rec[0] = (unsigned)np;
+        rec[1] = (unsigned)r.nx;
+        rec[2] = (unsigned)nxx;
+        rec[3] = covered ? 1u : 0u;
+    }
+    __syncwarp();
+}
+
+// Searches the subtree of root v from its record (built by build_kernel).
+template <int W>
+__device__ void search_record(const SearchArgs &a, unsigned *ws, const WarpSmem &sm, int v,
+                              int deg, int np, const unsigned *rec, Acc &acc,
+                              unsigned long long *s_hist, int lane)
+{
+    constexpr int CH = Geo<W>::CH, G = Geo<W>::G;
+    PROF_START(t_build);
+    const RecLayout L = rec_layout(deg, np, W);
+    const int nxx = (int)rec[2];
+    if (rec[3]) {                                       // an X vertex covers P
+        acc.nodes++;
+        PROF_ADD(acc, kProfBuild, t_build);
+        return;
+    }
+    RootCtx r = make_ctx<W>(ws, deg, np, np, deg - np);
+    r.pids = reinterpret_cast<int *>(const_cast<unsigned *>(rec) + L.pids);
+    r.pkey = reinterpret_cast<unsigned long long *>(const_cast<unsigned *>(rec) + L.pkey);
+    const int *live = reinterpret_cast<const int *>(rec + L.xx);
+    const unsigned *rows = rec + L.rows;
+    if ((long long)(np + nxx) * W <= sm.rows_words) {
+        // P rows, then the live X rows packed, in shared memory
+        for (long long t = (long long)lane * CH; t < (long long)np * W; t += 32 * CH)
+            ck_store<CH>(sm.rows + t, ck_load<CH>(rows + t));
+        for (long long t = (long long)lane * CH; t < (long long)nxx * W; t += 32 * CH) {
+            const long long i = t / W;
+            ck_store<CH>(sm.rows + (long long)np * W + t,
+                         ck_load<CH>(rows + (long long)(np + live[i]) * W + (t - i * W)));
+        }
+        for (int i = lane; i < nxx; i += 32) r.xx[i] = i;
+        r.rowsP = sm.rows;
+        r.rowsX = sm.rows + (long long)np * W;
+    } else {
+        for (int i = lane; i < nxx; i += 32) r.xx[i] = live[i];
+        r.rowsP = const_cast<unsigned *>(rows);
+        r.rowsX = r.rowsP + (long long)np * W;
+    }
+    if (lane == 0) r.rids[0] = v;
+    __syncwarp();
+    PROF_ADD(acc, kProfBuild, t_build);
+    const int q = lane % G;
+    dfs<W>(a, r, bits_prefix<W>(np, q), ck_zero<CH>(), nxx, vertex_key(v), acc, s_hist,
+           reinterpret_cast<unsigned *>(sm.cur_start), lane);
+}
+
 // Second-level subtree of the edge {v, w}, v before w (Algorithm 4): R = {v, w},
 // P = N(v) n N(w) after w = N+(v) n N+(w), X = N(v) n N(w) before w.  The workspace keeps the
 // layout of root v, which holds any of its second-level subtrees.
@@ -1466,9 +1626,13 @@ __device__ __forceinline__ void search_unit(const SearchArgs &a, unsigned *ws, c
 // One persistent launch per row width W and launch group: the roots of that class, heaviest
 // first, then donated branches of those roots (Section 3.3).  Big: the group of roots whose
 // workspace exceeds kWsCapWords (their build code is compiled into these instances only).
-template <int W, bool Big>
+// Rec: the roots' subtrees were built ahead by build_kernel (normal groups, W <= 4).
+template <int W, bool Big, bool Rec = false>
 __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(SearchArgs a)
 {
+    if constexpr (!kIP && !kL2 && W <= 4) {
+        if (a.rec_gate != nullptr && records_on(a) != Rec) return;   // the other variant works
+    }
     extern __shared__ __align__(16) unsigned char s_raw[];
     unsigned long long *s_hist = reinterpret_cast<unsigned long long *>(s_raw);
     for (int i = threadIdx.x; i < a.out.hist_len; i += blockDim.x) s_hist[i] = 0ULL;
@@ -1537,7 +1701,15 @@ __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(Search
         } else if (np > kMaxP) {
             if (lane == 0) set_status(a.g.ctrl, MCE_ERR_LIMIT);
         } else {
-            search_unit<W, Big>(a, ws, sm, v, w, deg, np, acc, s_hist, lane);
+            if constexpr (Rec) {
+                if (has_record(a, pos) && record_matches(a, pos, deg, np, W))
+                    search_record<W>(a, ws, sm, v, deg, np, a.bb + a.rec_off[pos] * 4, acc,
+                                     s_hist, lane);
+                else if (lane == 0)
+                    set_status(a.g.ctrl, MCE_ERR_INTERNAL);   // every root has a record
+            } else {
+                search_unit<W, Big>(a, ws, sm, v, w, deg, np, acc, s_hist, lane);
+            }
         }
         __syncwarp();
         if (lane == 0) busy.fetch_sub(1, cuda::memory_order_acq_rel);
@@ -1619,6 +1791,44 @@ __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(Search
 #endif
     }
 }
+
+#if !MCE_SEARCH_IP && !MCE_SEARCH_L2
+// The subtree build ahead of the search (see "subtrees built ahead"): the warps take the roots
+// of one normal launch group of row width W <= 4 in turn and build each one's record.
+template <int W>
+__global__ void __launch_bounds__(kBuildThreads, kBuildMinBlocks) build_kernel(SearchArgs a)
+{
+    if (!records_on(a)) return;
+    extern __shared__ __align__(16) unsigned char s_raw[];
+    const int lane = threadIdx.x & 31, wpb = blockDim.x >> 5;
+    constexpr int k = W == 1 ? 0 : W == 2 ? 1 : 2;
+    WarpSmem sm;
+    {
+        unsigned char *mine = s_raw + (size_t)(threadIdx.x >> 5) * build_smem_per_warp(k);
+        sm.hkey = reinterpret_cast<int *>(mine);
+        sm.hval = sm.hkey + hash_slots(k);
+        sm.filter = reinterpret_cast<unsigned *>(sm.hval + hash_slots(k));
+        sm.slots = hash_slots(k);
+        sm.cur_start = reinterpret_cast<int *>(sm.filter + kFilterWords);
+        sm.cur_base = sm.cur_start + 36;
+        sm.rows = nullptr;
+        sm.rows_words = 0;
+    }
+    const int begin = a.range[2 * a.group], end = a.range[2 * a.group + 1];
+    for (int i = begin + blockIdx.x * wpb + (threadIdx.x >> 5); i < end; i += gridDim.x * wpb) {
+        if (load_status(a.g.ctrl) != 0) return;
+        if (!has_record(a, i)) continue;
+        const int v = a.roots[i];
+        const int deg = a.g.offs[v + 1] - a.g.offs[v];
+        const int np = a.g.pcount[v];
+        if (!record_matches(a, i, deg, np, W)) {
+            if (lane == 0) set_status(a.g.ctrl, MCE_ERR_INTERNAL);
+            continue;
+        }
+        build_record<W>(a, sm, v, deg, np, a.bb + a.rec_off[i] * 4, lane);
+    }
+}
+#endif
 
 }  // namespace
 

@@ -187,6 +187,24 @@ def test_repeat_is_deterministic():
     assert a == b
 
 
+@pytest.mark.parametrize("name,seed", [("rmat_s12", 1), ("sbm_c50", 2), ("planted50k", 3),
+                                       ("sbm1m", 1)])
+def test_count_after_each_reorder(name, seed):
+    # each order places the roots of a schedule bucket anew (atomic cursors), and roots of one
+    # bucket differ in degree: every count after a new order must still be the oracle's
+    g = G.config_graph(name, seed)
+    expect = O.count(g, threads=16).key()
+    with gpu_graph(g) as h:
+        for _ in range(4):
+            h.order()
+            assert h.count_result() == expect
+        if expect[0] > 2_000_000:
+            return
+        h.order()
+        ids, offs = h.enumerate()
+    assert len(_mce().cliques_from(ids, offs)) == expect[0]
+
+
 # ---------------------------------------------------------------- input handling and errors
 
 def _shuffled(g, seed):
