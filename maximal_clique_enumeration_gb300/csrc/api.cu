@@ -2,6 +2,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 #include <new>
 #include <vector>
@@ -32,6 +33,11 @@ struct mce_graph {
     long long bb_quads = 0;
     long long *rec_off = nullptr, *rec_scan = nullptr;
     long long *urec_off = nullptr, *urec_scan = nullptr;   // the same for a caller's roots
+    // the builds run on a stream of the handle's own, forked from the caller's stream, so that
+    // the build of a narrower group overlaps the search of the wider ones
+    bool use_side = true;
+    cudaStream_t side = nullptr;
+    cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_built[3] = {};
     bool unit_own = false;    // unit_cnt / unit_scan were reallocated for a caller's root list
     int degeneracy = 0, max_degree = 0, hist_len = 2, rounds = 0;
     unsigned long long ws_words = 0;
@@ -186,6 +192,10 @@ void free_all(mce_graph *h)
     for (int k = 0; k < kNumGroups; ++k)
         for (int i = 0; i < 2; ++i)
             if (h->ev_grp[k][i]) cudaEventDestroy(h->ev_grp[k][i]);
+    for (cudaEvent_t e : {h->ev_fork, h->ev_join, h->ev_built[0], h->ev_built[1], h->ev_built[2]})
+        if (e) cudaEventDestroy(e);
+    if (h->side) cudaStreamDestroy(h->side);
+    h->side = nullptr;
 }
 
 // Resets the per-search accumulators of the control block.
@@ -235,10 +245,41 @@ mce_status run_search(mce_graph *h, cudaStream_t s, bool user_roots, const DevOu
         a.bb_quads = h->bb_quads;
         a.rec_off = user_roots ? h->urec_off : h->rec_off;
     }
+    // normal roots of row width <= 4 words: subtrees built ahead when the records fit (the
+    // schedule's always do; a caller's list is checked on the device, and the plain search
+    // launch after the record search does the work when they do not)
+    auto launched = [&](int gi) {
+        return h->grp_workers[gi] != 0 && (user_roots || h->grp_count[gi] != 0);
+    };
+    auto with_records = [&](int gi) {
+        const int k = gi / 2;
+        return a.bb != nullptr && (gi & 1) && k <= 2 && ((h->record_mask >> k) & 1) &&
+               launched(gi);
+    };
+    const long long *gate = a.bb ? a.rec_off + (user_roots ? h->n_uroots : h->n) : nullptr;
+    bool forked = false;
+    if (h->side) {
+        // all builds on the side stream, widest first (the order of the searches)
+        for (int k = 2; k >= 0; --k) {
+            const int gi = 2 * k + 1;
+            if (!with_records(gi)) continue;
+            if (!forked) {
+                MCE_TRY(cudaEventRecord(h->ev_fork, s));
+                MCE_TRY(cudaStreamWaitEvent(h->side, h->ev_fork, 0));
+                forked = true;
+            }
+            SearchArgs b = a;
+            b.cls = k;
+            b.group = gi;
+            b.rec_gate = gate;
+            MCE_TRY(launch_build(b, h->build_blocks[k], h->side));
+            MCE_TRY(cudaEventRecord(h->ev_built[k], h->side));
+        }
+        if (forked) MCE_TRY(cudaEventRecord(h->ev_join, h->side));
+    }
     for (int o = 0; o < kNumGroups; ++o) {
         const int gi = group_at(o), k = gi / 2;
-        if (h->grp_workers[gi] == 0) continue;            // no vertex of the graph in this group
-        if (!user_roots && h->grp_count[gi] == 0) continue;
+        if (!launched(gi)) continue;                      // no root of the call in this group
         a.cls = k;
         a.group = gi;
         a.ws_words = h->grp_ws[gi];
@@ -246,13 +287,11 @@ mce_status run_search(mce_graph *h, cudaStream_t s, bool user_roots, const DevOu
         MCE_TRY(cudaMemsetAsync(h->flag, 0, sizeof(int) * (size_t)a.n_workers, s));
         MCE_TRY(launch_search_prep(a, s));
         if (h->cfg.profile) MCE_TRY(cudaEventRecord(h->ev_grp[gi][0], s));
-        // normal roots of row width <= 4 words: subtrees built ahead when the records fit (the
-        // schedule's always do; a caller's list is checked on the device, and the plain search
-        // launch after the record search does the work when they do not)
-        const bool rec = a.bb && (gi & 1) && k <= 2 && ((h->record_mask >> k) & 1);
-        a.rec_gate = rec ? a.rec_off + (user_roots ? h->n_uroots : h->n) : nullptr;
+        const bool rec = with_records(gi);
+        a.rec_gate = rec ? gate : nullptr;
         if (rec) {
-            MCE_TRY(launch_build(a, h->build_blocks[k], s));
+            if (forked) MCE_TRY(cudaStreamWaitEvent(s, h->ev_built[k], 0));
+            else MCE_TRY(launch_build(a, h->build_blocks[k], s));
             MCE_TRY(launch_search(a, h->grp_blocks[gi], h->search_threads, h->cls_smem[k], true,
                                   s));
             h->launches_count += user_roots ? 2 : 1;   // build (+ the plain search launch)
@@ -266,6 +305,7 @@ mce_status run_search(mce_graph *h, cudaStream_t s, bool user_roots, const DevOu
         }
         h->launches_count += 2;                           // prep and search
     }
+    if (forked) MCE_TRY(cudaStreamWaitEvent(s, h->ev_join, 0));
     return MCE_OK;
 }
 
@@ -508,6 +548,12 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
             h->bb_quads = total;
         else
             h->bb = nullptr;
+        if (h->bb && h->use_side) {
+            MCE_TRY(cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking));
+            for (cudaEvent_t *e : {&h->ev_fork, &h->ev_join, &h->ev_built[0], &h->ev_built[1],
+                                   &h->ev_built[2]})
+                MCE_TRY(cudaEventCreateWithFlags(e, cudaEventDisableTiming));
+        }
     }
     MCE_ALLOC(h, h->ring, (size_t)h->n_workers);
     MCE_ALLOC(h, h->flag, (size_t)h->n_workers);
@@ -550,6 +596,7 @@ mce_status mce_create(const int32_t *offsets, const int32_t *adj, int32_t n, int
     if (const char *e = getenv("MCE_AB_SMALL_HI")) h->small_hi = atoi(e);
     if (const char *e = getenv("MCE_AB_RECORDS")) h->records = atoi(e) != 0;
     if (const char *e = getenv("MCE_AB_RECORD_MASK")) h->record_mask = atoi(e);
+    if (const char *e = getenv("MCE_AB_SIDE")) h->use_side = atoi(e) != 0;
     if (h->small_hi > kSmallPMax) h->small_hi = kSmallPMax;
 #endif
     mce_status st = create_impl(h, offsets, adj, n, is_device_ptr, (cudaStream_t)stream);
