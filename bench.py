@@ -227,7 +227,8 @@ def stage_bytes(g, rank, roots, peel_live):
     build (a3):  per workload root v (|P| > 0), with W(v) words per row:
                  16 deg(v)  N(v) read, the rank of each neighbour, |N+(u)| and offset of each
                + 4 sum_{u in N(v)} |N+(u)|  the later-neighbour lists walked
-               + 4 deg(v) W(v)              the rows written
+               + 4 (deg(v) W(v) + deg(v) + 2 |P(v)| + 4)  the record written: rows, P's ids
+                                            and keys, the live X list, its header
     """
     n, m = g.n, g.m
     deg = g.degrees()
@@ -235,7 +236,7 @@ def stage_bytes(g, rank, roots, peel_live):
     src = np.repeat(np.arange(n), deg)
     walk = np.bincount(src, weights=pc[g.adj].astype(np.float64), minlength=n)
     w = np.select([pc <= 32, pc <= 64, pc <= 128, pc <= 256, pc <= 512], [1, 2, 4, 8, 16], 32)
-    per_root = 16.0 * deg + 4.0 * walk + 4.0 * deg * w
+    per_root = 16.0 * deg + 4.0 * walk + 4.0 * (deg * w + deg + 2.0 * pc + 4.0)
     sel = np.zeros(n, bool)
     sel[roots] = True
     sel &= pc > 0
@@ -563,6 +564,7 @@ def run_gb300(args, rank, world, local):
     ms_cls = np.zeros(mce.NUM_WIDTHS)
     words_cls = np.zeros(mce.NUM_WIDTHS)
     ms_order = ms_peel = 0.0
+    ms_bld = np.zeros(mce.NUM_WIDTHS)
     launches = 0
     barrier(world)
     torch.cuda.synchronize()
@@ -579,6 +581,7 @@ def run_gb300(args, rank, world, local):
         words_cls += np.asarray(info["words"], dtype=np.float64)
         ms_order += info["ms_order"]
         ms_peel += info["ms_peel"]
+        ms_bld += np.asarray(info["ms_build"])
         launches += info["launches"]
     wall = time.perf_counter() - wall0
     torch.cuda.synchronize()
@@ -624,37 +627,32 @@ def run_gb300(args, rank, world, local):
         "result": {"cliques": res[0], "hash": f"{res[1]:#018x}", "max_size": len(res[2]) - 1},
         "stage_ms": {"order": ms_order / args.steps, "peel": ms_peel / args.steps,
                      "search_by_width": {str(1 << i): float(ms_cls[i] / args.steps)
-                                         for i in range(mce.NUM_WIDTHS) if ms_cls[i] > 0}},
+                                         for i in range(mce.NUM_WIDTHS) if ms_cls[i] > 0},
+                     "build_by_width": {str(1 << i): float(ms_bld[i] / args.steps)
+                                        for i in range(mce.NUM_WIDTHS) if ms_bld[i] > 0}},
         "roofline": roofline, "clocks": clocks, "gpu_launches": launches,
         "wall_s_timed": wall,
     }
 
-    # graph stages against HBM: peel, orientation, and (from the activity profile) the build
+    # graph stages against HBM: peel, orientation, and the subtree build launches (rows of 1,
+    # 2 and 4 words; device time by CUDA events around each build launch)
     sb = stage_bytes(g, rank_arr, roots, info["peel_live"])
     peel_ms = ms_peel / args.steps
     stages = {"peel": _gbs(sb["peel"], peel_ms, hbm),
               "orient": _gbs(sb["orient"], ms_order / args.steps - peel_ms, hbm),
               "peel_live_vertices": info["peel_live"], "rounds": info["peel_rounds"],
               "bytes_formulas": "see stage_bytes() in bench.py"}
+    built = [c for c in range(mce.NUM_WIDTHS) if ms_bld[c] > 0]
+    if built:
+        stages["build"] = dict(_gbs(sum(sb["build_by_width"][c] for c in built),
+                                    float(sum(ms_bld[c] for c in built)) / args.steps, hbm),
+                               by_width={str(1 << c): _gbs(sb["build_by_width"][c],
+                                                           ms_bld[c] / args.steps, hbm)
+                                         for c in built},
+                               time_source="CUDA events around each build launch")
     if rank == 0 and world == 1 and not args.no_activity:
         progress("activity profile")
-        act = activity_profile(g, roots, args)
-        line["activity"] = act
-        # the build's device time: its SM cycles summed over warps, spread over the launch's
-        # warps, at the sampled clock
-        mhz = (clocks or {}).get("sm_mhz") or 2070.0
-        build_ms, build_bytes = 0.0, 0.0
-        for c in range(6):
-            a = act.get(str(1 << c)) if isinstance(act, dict) else None
-            if not a or not act["workers"][c]:
-                continue
-            build_ms += (a["cycles"]["build"] + a["cycles"]["split"]) / (mhz * 1e3) \
-                / act["workers"][c]
-            build_bytes += sb["build_by_width"][c]
-        if build_ms > 0:
-            stages["build"] = dict(_gbs(build_bytes, build_ms, hbm),
-                                   time_source="MCE_PROFILE activity cycles of the subtree "
-                                               "build, spread over each launch's warps")
+        line["activity"] = activity_profile(g, roots, args)
     line["graph_stages"] = stages
 
     if not args.no_heavy and args.scale == 20 and args.seed == 1:

@@ -118,6 +118,10 @@ typedef struct mce_info {
     float ms_peel;                     /* the peel's part of ms_order (profile = 1 only)     */
     int64_t peel_live;                 /* vertices still in the graph, summed over the peel's
                                           rounds (the live lists its rounds scan)            */
+    float ms_build[MCE_NUM_WIDTHS];    /* device time of the launch that builds the subtrees
+                                          of the class's roots ahead of its search (rows of
+                                          1, 2, 4 words; 0 where the search builds them
+                                          itself; profile = 1 only).  ms_search excludes it. */
 } mce_info;
 
 /* Writes the default configuration into *cfg.  Returns MCE_ERR_INVALID_ARG if cfg is NULL. */

@@ -62,7 +62,7 @@ class Info(ctypes.Structure):
                 ("ms_search", ctypes.c_float * NUM_WIDTHS), ("ms_order", ctypes.c_float),
                 ("launches", ctypes.c_int32), ("induced", ctypes.c_int32),
                 ("subtree_level", ctypes.c_int32), ("ms_peel", ctypes.c_float),
-                ("peel_live", ctypes.c_int64)]
+                ("peel_live", ctypes.c_int64), ("ms_build", ctypes.c_float * NUM_WIDTHS)]
 
     def as_dict(self):
         out = {}

@@ -57,6 +57,8 @@ struct mce_graph {
     cudaEvent_t ev_order[3] = {nullptr, nullptr, nullptr};   // start, end, after the peel
     cudaEvent_t ev_grp[kNumGroups][2] = {};
     bool grp_timed[kNumGroups] = {};
+    cudaEvent_t ev_bld[3][2] = {};               // around the build launches (rows 1, 2, 4 words)
+    bool bld_timed[3] = {};
     bool order_timed = false;
     int launches_order = 0, launches_count = 0;
 };
@@ -192,7 +194,9 @@ void free_all(mce_graph *h)
     for (int k = 0; k < kNumGroups; ++k)
         for (int i = 0; i < 2; ++i)
             if (h->ev_grp[k][i]) cudaEventDestroy(h->ev_grp[k][i]);
-    for (cudaEvent_t e : {h->ev_fork, h->ev_join, h->ev_built[0], h->ev_built[1], h->ev_built[2]})
+    for (cudaEvent_t e : {h->ev_fork, h->ev_join, h->ev_built[0], h->ev_built[1], h->ev_built[2],
+                          h->ev_bld[0][0], h->ev_bld[0][1], h->ev_bld[1][0], h->ev_bld[1][1],
+                          h->ev_bld[2][0], h->ev_bld[2][1]})
         if (e) cudaEventDestroy(e);
     if (h->side) cudaStreamDestroy(h->side);
     h->side = nullptr;
@@ -208,6 +212,7 @@ mce_status reset_search(mce_graph *h, cudaStream_t s)
     MCE_TRY(cudaMemsetAsync(h->g.prof_sm, 0, sizeof(unsigned long long) * kNumClasses * kProfSms,
                             s));
     for (int k = 0; k < kNumGroups; ++k) h->grp_timed[k] = false;
+    for (int k = 0; k < 3; ++k) h->bld_timed[k] = false;
     MCE_TRY(cudaMemsetAsync(h->hist_acc, 0, sizeof(unsigned long long) * h->hist_len, s));
     return MCE_OK;
 }
@@ -272,7 +277,12 @@ mce_status run_search(mce_graph *h, cudaStream_t s, bool user_roots, const DevOu
             b.cls = k;
             b.group = gi;
             b.rec_gate = gate;
+            if (h->cfg.profile) MCE_TRY(cudaEventRecord(h->ev_bld[k][0], h->side));
             MCE_TRY(launch_build(b, h->build_blocks[k], h->side));
+            if (h->cfg.profile) {
+                MCE_TRY(cudaEventRecord(h->ev_bld[k][1], h->side));
+                h->bld_timed[k] = true;
+            }
             MCE_TRY(cudaEventRecord(h->ev_built[k], h->side));
         }
         if (forked) MCE_TRY(cudaEventRecord(h->ev_join, h->side));
@@ -286,12 +296,22 @@ mce_status run_search(mce_graph *h, cudaStream_t s, bool user_roots, const DevOu
         a.n_workers = h->grp_workers[gi];
         MCE_TRY(cudaMemsetAsync(h->flag, 0, sizeof(int) * (size_t)a.n_workers, s));
         MCE_TRY(launch_search_prep(a, s));
-        if (h->cfg.profile) MCE_TRY(cudaEventRecord(h->ev_grp[gi][0], s));
         const bool rec = with_records(gi);
         a.rec_gate = rec ? gate : nullptr;
         if (rec) {
-            if (forked) MCE_TRY(cudaStreamWaitEvent(s, h->ev_built[k], 0));
-            else MCE_TRY(launch_build(a, h->build_blocks[k], s));
+            if (forked) {
+                MCE_TRY(cudaStreamWaitEvent(s, h->ev_built[k], 0));
+            } else {
+                if (h->cfg.profile) MCE_TRY(cudaEventRecord(h->ev_bld[k][0], s));
+                MCE_TRY(launch_build(a, h->build_blocks[k], s));
+                if (h->cfg.profile) {
+                    MCE_TRY(cudaEventRecord(h->ev_bld[k][1], s));
+                    h->bld_timed[k] = true;
+                }
+            }
+        }
+        if (h->cfg.profile) MCE_TRY(cudaEventRecord(h->ev_grp[gi][0], s));
+        if (rec) {
             MCE_TRY(launch_search(a, h->grp_blocks[gi], h->search_threads, h->cls_smem[k], true,
                                   s));
             h->launches_count += user_roots ? 2 : 1;   // build (+ the plain search launch)
@@ -448,6 +468,10 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
         for (int k = 0; k < kNumGroups; ++k) {
             MCE_TRY(cudaEventCreate(&h->ev_grp[k][0]));
             MCE_TRY(cudaEventCreate(&h->ev_grp[k][1]));
+        }
+        for (int k = 0; k < 3; ++k) {
+            MCE_TRY(cudaEventCreate(&h->ev_bld[k][0]));
+            MCE_TRY(cudaEventCreate(&h->ev_bld[k][1]));
         }
     }
     g.ip = h->cfg.induced == 2 ? 1 : 0;
@@ -866,6 +890,9 @@ mce_status mce_get_info(mce_graph *h, mce_info *info)
             MCE_TRY(cudaEventElapsedTime(&ms, h->ev_grp[gi][0], h->ev_grp[gi][1]));
             info->ms_search[k] += ms;
         }
+        info->ms_build[k] = 0.f;
+        if (k < 3 && h->bld_timed[k])
+            MCE_TRY(cudaEventElapsedTime(&info->ms_build[k], h->ev_bld[k][0], h->ev_bld[k][1]));
     }
     if (h->order_timed && h->n > 0) {
         MCE_TRY(cudaEventElapsedTime(&info->ms_order, h->ev_order[0], h->ev_order[1]));

@@ -748,12 +748,69 @@ __global__ void orient_scan_kernel(DevGraph g)
     buckets_to_cursors(g.bucket, g.ctrl->cls, &g.ctrl->n_sched);
 }
 
+// Warp-aggregated s[key] += 1 in shared memory for the active lanes; returns the old value
+// plus the lane's rank among the active lanes with the same key.  Every lane of the warp calls
+// it (the lanes with one key add once, so a popular bucket costs one atomic per warp).
+__device__ __forceinline__ int warp_agg_inc(int *s, int key, bool active)
+{
+    const unsigned act = __ballot_sync(0xffffffffu, active);
+    int r = 0;
+    if (active) {
+        const int lane = threadIdx.x & 31;
+        const unsigned peers = __match_any_sync(act, key);
+        const int leader = __ffs(peers) - 1;
+        int base = 0;
+        if (lane == leader) base = atomicAdd(s + key, __popc(peers));
+        base = __shfl_sync(peers, base, leader);
+        r = base + __popc(peers & ((1u << lane) - 1u));
+    }
+    return r;
+}
+
+// Places the items of [lo, hi) (one CTA's segment) into out[] at their buckets' cursors:
+// the CTA counts its items per bucket in shared memory, reserves each bucket's range with one
+// global atomic, then writes every item at its place in that range.  item(i, &b) returns the
+// value to place and sets its bucket b, or returns -1 for an item that is not placed.
+template <class Item>
+__device__ void segment_scatter(int lo, int hi, int *s_cur, int *cursor, int *out, Item item)
+{
+    for (int i = threadIdx.x; i < kNumBuckets; i += blockDim.x) s_cur[i] = 0;
+    __syncthreads();
+    for (int b0 = lo; b0 < hi; b0 += blockDim.x) {     // the same trip count for the whole CTA
+        const int i = b0 + threadIdx.x;
+        int b = 0;
+        const int v = i < hi ? item(i, &b) : -1;
+        warp_agg_inc(s_cur, b, v >= 0);
+    }
+    __syncthreads();
+    for (int k = threadIdx.x; k < kNumBuckets; k += blockDim.x) {
+        const int c = s_cur[k];
+        s_cur[k] = c ? atomicAdd(cursor + k, c) : 0;
+    }
+    __syncthreads();
+    for (int b0 = lo; b0 < hi; b0 += blockDim.x) {
+        const int i = b0 + threadIdx.x;
+        int b = 0;
+        const int v = i < hi ? item(i, &b) : -1;
+        const int at = warp_agg_inc(s_cur, b, v >= 0);
+        if (v >= 0) out[at] = v;
+    }
+}
+
+// Items per CTA of the segmented scatters.
+constexpr int kScatterSegment = 2048;
+
 __global__ void __launch_bounds__(kOrientThreads) orient_scatter_kernel(DevGraph g)
 {
-    for (int v = blockIdx.x * blockDim.x + threadIdx.x; v < g.n; v += gridDim.x * blockDim.x) {
+    __shared__ int s_cur[kNumBuckets];
+    const int lo = blockIdx.x * kScatterSegment;
+    const int hi = min(g.n, lo + kScatterSegment);
+    segment_scatter(lo, hi, s_cur, g.bucket, g.sched, [&](int v, int *b) {
         const int c = g.pcount[v];
-        if (c > 0) g.sched[atomicAdd(&g.bucket[sched_bucket(c, g.offs[v + 1] - g.offs[v], g.ip, g.l2, g.core[v])], 1)] = v;
-    }
+        if (c <= 0) return -1;
+        *b = sched_bucket(c, g.offs[v + 1] - g.offs[v], g.ip, g.l2, g.core[v]);
+        return v;
+    });
 }
 
 // ---- exclusive scan of an int array (three passes: CTA sums, scan of the sums, final)
@@ -808,14 +865,22 @@ __global__ void __launch_bounds__(kScanThreads) scan_final_kernel(const int *in,
 __global__ void __launch_bounds__(kOrientThreads) bin_count_kernel(DevGraph g, const int *roots,
                                                                    int n_roots)
 {
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_roots; i += gridDim.x * blockDim.x) {
-        const int v = roots[i];
-        if (v < 0 || v >= g.n) {
-            set_status(g.ctrl, MCE_ERR_ID_RANGE);
-            continue;
-        }
-        atomicAdd(&g.ubucket[sched_bucket(g.pcount[v], g.offs[v + 1] - g.offs[v], g.ip, g.l2, g.core[v])], 1);
+    __shared__ int s_cnt[kNumBuckets];
+    for (int i = threadIdx.x; i < kNumBuckets; i += blockDim.x) s_cnt[i] = 0;
+    __syncthreads();
+    for (int b0 = blockIdx.x * blockDim.x; b0 < n_roots; b0 += gridDim.x * blockDim.x) {
+        const int i = b0 + threadIdx.x;
+        const int v = i < n_roots ? roots[i] : 0;
+        const bool ok = i < n_roots && v >= 0 && v < g.n;
+        if (i < n_roots && !ok) set_status(g.ctrl, MCE_ERR_ID_RANGE);
+        const int b = ok ? sched_bucket(g.pcount[v], g.offs[v + 1] - g.offs[v], g.ip, g.l2,
+                                        g.core[v])
+                         : 0;
+        warp_agg_inc(s_cnt, b, ok);
     }
+    __syncthreads();
+    for (int k = threadIdx.x; k < kNumBuckets; k += blockDim.x)
+        if (s_cnt[k]) atomicAdd(&g.ubucket[k], s_cnt[k]);
 }
 
 __global__ void bin_scan_kernel(DevGraph g)
@@ -827,11 +892,15 @@ __global__ void bin_scan_kernel(DevGraph g)
 __global__ void __launch_bounds__(kOrientThreads) bin_scatter_kernel(DevGraph g, const int *roots,
                                                                      int n_roots)
 {
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_roots; i += gridDim.x * blockDim.x) {
+    __shared__ int s_cur[kNumBuckets];
+    const int lo = blockIdx.x * kScatterSegment;
+    const int hi = min(n_roots, lo + kScatterSegment);
+    segment_scatter(lo, hi, s_cur, g.ubucket, g.uroots, [&](int i, int *b) {
         const int v = roots[i];
-        if (v < 0 || v >= g.n) continue;
-        g.uroots[atomicAdd(&g.ubucket[sched_bucket(g.pcount[v], g.offs[v + 1] - g.offs[v], g.ip, g.l2, g.core[v])], 1)] = v;
-    }
+        if (v < 0 || v >= g.n) return -1;
+        *b = sched_bucket(g.pcount[v], g.offs[v + 1] - g.offs[v], g.ip, g.l2, g.core[v]);
+        return v;
+    });
 }
 
 }  // namespace
@@ -842,10 +911,11 @@ cudaError_t launch_bin_roots(const DevGraph &g, const int *roots, int n_roots, c
     if (e != cudaSuccess) return e;
     int b = (n_roots + kOrientThreads - 1) / kOrientThreads;
     if (b < 1) b = 1;
-    if (b > 4096) b = 4096;
+    if (b > 1024) b = 1024;
     bin_count_kernel<<<b, kOrientThreads, 0, s>>>(g, roots, n_roots);
     bin_scan_kernel<<<1, 32, 0, s>>>(g);
-    bin_scatter_kernel<<<b, kOrientThreads, 0, s>>>(g, roots, n_roots);
+    const int segs = (n_roots + kScatterSegment - 1) / kScatterSegment;
+    bin_scatter_kernel<<<segs > 0 ? segs : 1, kOrientThreads, 0, s>>>(g, roots, n_roots);
     return cudaGetLastError();
 }
 
@@ -928,9 +998,7 @@ cudaError_t launch_order(const DevGraph &g, int peel_blocks, long long spin_limi
     if (blocks > 8192) blocks = 8192;
     orient_count_kernel<<<blocks, kOrientThreads, 0, s>>>(g);
     orient_scan_kernel<<<1, 32, 0, s>>>(g);
-    int sb = (g.n + kOrientThreads - 1) / kOrientThreads;
-    if (sb > 8192) sb = 8192;
-    orient_scatter_kernel<<<sb, kOrientThreads, 0, s>>>(g);
+    orient_scatter_kernel<<<(g.n + kScatterSegment - 1) / kScatterSegment, kOrientThreads, 0, s>>>(g);
     if (g.l2) {
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;

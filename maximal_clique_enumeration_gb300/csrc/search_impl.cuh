@@ -648,6 +648,117 @@ __device__ void solve_small(const SearchArgs &a, const RootCtx &r, const Ck<W> &
     __syncwarp();
 }
 
+// The same for rows wider than 4 words, whose lanes hold 4-word chunks: lane l holds chunk
+// q = l % G of P, X_P and of every row it loads.  P's members are listed from the chunks (a
+// prefix of their counts over the G lanes of a row); N_i takes k single bits of p_i's row; an
+// X_P member extends C when the chunks of XP & AND of C's rows are nonzero in some lane; an X_X
+// row (one per lane) extends C when it holds C's at most kSmallPMax columns.
+template <int W>
+__device__ void solve_small_wide(const SearchArgs &a, const RootCtx &r, const Ck<Geo<W>::CH> &P,
+                                 const Ck<Geo<W>::CH> &XP, int lpX, unsigned long long S, int L,
+                                 int k, Acc &acc, unsigned long long *s_hist, unsigned *scratch,
+                                 int lane)
+{
+    constexpr int CH = Geo<W>::CH, G = Geo<W>::G;
+    const int q = lane % G;
+    int *mem = reinterpret_cast<int *>(scratch);                          // columns of P
+    unsigned long long *keys = reinterpret_cast<unsigned long long *>(scratch + 16);
+    {
+        const int cnt = ck_popc<CH>(P);
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < G; o <<= 1) {
+            const int y = __shfl_up_sync(kFull, incl, o, G);
+            if (q >= o) incl += y;
+        }
+        if (lane < G) {
+            int j = incl - cnt;
+#pragma unroll
+            for (int w = 0; w < CH; ++w) {
+                unsigned pm = P.w[w];
+                while (pm) {
+                    mem[j++] = (q * CH + w) * 32 + __ffs(pm) - 1;
+                    pm &= pm - 1u;
+                }
+            }
+        }
+    }
+    __syncwarp();
+    unsigned adj = 0;                                         // lane i < k: N(p_i) n P, packed
+    if (lane < k) {
+        const int my_p = mem[lane];
+        const unsigned *row = r.rowsP + (long long)my_p * W;
+        for (int j = 0; j < k; ++j) {
+            const int cj = mem[j];
+            adj |= ((row[cj >> 5] >> (cj & 31)) & 1u) << j;
+        }
+        keys[lane] = r.pkey[my_p];
+    }
+    unsigned V = subsets_of((1u << k) - 1u, lane);
+    for (int i = 0; i < k; ++i) {
+        const unsigned ni = __shfl_sync(kFull, adj, i) | (1u << i);
+        V &= ~(subsets_of(ni, lane) ^ subsets_with(i, lane));
+    }
+    __syncwarp();                                             // keys[] written
+    const int rsize = r.rsize + L;
+    unsigned long long words = (unsigned long long)k * k + (unsigned long long)k * ((1u << k) + 31u) / 32u;
+    unsigned cand = __ballot_sync(kFull, V != 0u);
+    while (cand) {
+        const int src = __ffs(cand) - 1;
+        const unsigned vs = __shfl_sync(kFull, V, src);
+        const unsigned C = (unsigned)src * 32u + (unsigned)(__ffs(vs) - 1);
+        if (lane == src) V &= V - 1u;
+        cand = __ballot_sync(kFull, V != 0u);
+        Ck<CH> common;
+#pragma unroll
+        for (int w = 0; w < CH; ++w) common.w[w] = 0xffffffffu;
+        unsigned long long sum = S;
+        for (unsigned cm = C; cm; cm &= cm - 1u) {
+            const int j = __ffs(cm) - 1;
+            common = ck_and<CH>(common, ck_load<CH>(r.rowsP + (long long)mem[j] * W + q * CH));
+            sum += keys[j];
+        }
+        const int c = __popc(C);
+        words += (unsigned long long)c * W;
+        bool dominated = __any_sync(kFull, ck_nonzero<CH>(ck_and<CH>(XP, common)));
+        for (int base = 0; base < lpX && !dominated; base += 32) {
+            const int t = base + lane;
+            bool hit = false;
+            if (t < lpX) {
+                const int x = r.xx[t];
+                hit = true;
+                if constexpr (kIP) {
+                    const int xid = r.xids[x];
+                    for (unsigned cm = C; cm && hit; cm &= cm - 1u)
+                        hit = x_adjacent(a.g, xid, r.pids[mem[__ffs(cm) - 1]]);
+                } else {
+                    const unsigned *row = r.rowsX + (long long)x * W;
+                    for (unsigned cm = C; cm && hit; cm &= cm - 1u) {
+                        const int col = mem[__ffs(cm) - 1];
+                        hit = (row[col >> 5] >> (col & 31)) & 1u;
+                    }
+                }
+            }
+            dominated = __any_sync(kFull, hit);
+            words += (unsigned long long)c * (unsigned)min(32, lpX - base);
+        }
+        if (dominated) continue;
+        const int size = rsize + c;
+        if (lane == 0) {
+            if (size >= a.out.hist_len) {                     // cannot happen: size <= d + 1
+                set_status(a.g.ctrl, MCE_ERR_INTERNAL);
+            } else {
+                acc.count++;
+                acc.hash += mix64(sum);
+                acc.nodes++;
+                atomicAdd(&s_hist[size], 1ULL);
+            }
+        }
+    }
+    if (lane == 0) acc.words += words;
+    __syncwarp();
+}
+
 // ------------------------------------------------------------------ worker list (Section 3.3)
 //
 // Idle warps put their id in a bounded multi-producer multi-consumer ring (one slot per warp,
@@ -787,6 +898,14 @@ __device__ void dfs(const SearchArgs &a, const RootCtx &r, Ck<Geo<W>::CH> P, Ck<
                 if (npop <= a.small_hi && npop >= a.small_lo && a.out.ids == nullptr) {
                     // the whole subtree at once; no stack entry, so the search backs up next
                     solve_small<W>(a, r, P, XP, lpX, S, L, npop, acc, s_hist, scratch, lane);
+                    PROF_ADD(acc, kProfSmall, t_piv);
+                    C = ck_zero<CH>();
+                    cursor = -1;
+                    goto next_candidate;
+                }
+            } else {
+                if (npop <= a.small_hi && npop >= a.small_lo && a.out.ids == nullptr) {
+                    solve_small_wide<W>(a, r, P, XP, lpX, S, L, npop, acc, s_hist, scratch, lane);
                     PROF_ADD(acc, kProfSmall, t_piv);
                     C = ck_zero<CH>();
                     cursor = -1;
@@ -1630,7 +1749,7 @@ __device__ __forceinline__ void search_unit(const SearchArgs &a, unsigned *ws, c
 template <int W, bool Big, bool Rec = false>
 __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(SearchArgs a)
 {
-    if constexpr (!kIP && !kL2 && W <= 4) {
+    if constexpr (!kIP && !kL2 && !Big && W <= 4) {
         if (a.rec_gate != nullptr && records_on(a) != Rec) return;   // the other variant works
     }
     extern __shared__ __align__(16) unsigned char s_raw[];
