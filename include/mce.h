@@ -78,6 +78,13 @@ typedef enum mce_status {
  *   subtree_level    1 (default): independent first-level subtrees, one per vertex
  *                    (Algorithm 3); 2: independent second-level subtrees, one per edge
  *                    (Algorithm 4, Section 3.2).  Other values: MCE_ERR_INVALID_ARG.
+ *   overlap_builds   1 (default): the subtrees of the roots with rows of 1, 2 and 4 words
+ *                    (full induced subgraphs, first-level subtrees) are built ahead of their
+ *                    search on a stream of the handle's own, forked from and joined back to
+ *                    the caller's stream, so a narrower class's build overlaps the wider
+ *                    classes' search; 0: each build runs on the caller's stream just before
+ *                    its search (mce_info.ms_build is then the build's own time).  Results
+ *                    are the same.  Other values: MCE_ERR_INVALID_ARG.
  */
 typedef struct mce_config {
     int32_t worker_list;
@@ -89,6 +96,7 @@ typedef struct mce_config {
     int64_t spin_limit_ns;
     int32_t induced;
     int32_t subtree_level;
+    int32_t overlap_builds;
 } mce_config;
 
 #define MCE_NUM_WIDTHS 6   /* search kernels, one per bitset row width 1, 2, 4, 8, 16, 32 words */

@@ -49,7 +49,7 @@ class Config(ctypes.Structure):
                 ("warps_per_block", ctypes.c_int32), ("blocks_per_sm", ctypes.c_int32),
                 ("profile", ctypes.c_int32), ("donate_rule", ctypes.c_int32),
                 ("spin_limit_ns", ctypes.c_int64), ("induced", ctypes.c_int32),
-                ("subtree_level", ctypes.c_int32)]
+                ("subtree_level", ctypes.c_int32), ("overlap_builds", ctypes.c_int32)]
 
 
 class Info(ctypes.Structure):

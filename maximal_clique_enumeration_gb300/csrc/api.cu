@@ -35,7 +35,6 @@ struct mce_graph {
     long long *urec_off = nullptr, *urec_scan = nullptr;   // the same for a caller's roots
     // the builds run on a stream of the handle's own, forked from the caller's stream, so that
     // the build of a narrower group overlaps the search of the wider ones
-    bool use_side = true;
     cudaStream_t side = nullptr;
     cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_built[3] = {};
     bool unit_own = false;    // unit_cnt / unit_scan were reallocated for a caller's root list
@@ -345,6 +344,7 @@ mce_status mce_config_default(mce_config *cfg)
     cfg->spin_limit_ns = 20LL * 1000 * 1000 * 1000;
     cfg->induced = 0;
     cfg->subtree_level = 1;
+    cfg->overlap_builds = 1;
     return MCE_OK;
 }
 
@@ -572,7 +572,7 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
             h->bb_quads = total;
         else
             h->bb = nullptr;
-        if (h->bb && h->use_side) {
+        if (h->bb && h->cfg.overlap_builds) {
             MCE_TRY(cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking));
             for (cudaEvent_t *e : {&h->ev_fork, &h->ev_join, &h->ev_built[0], &h->ev_built[1],
                                    &h->ev_built[2]})
@@ -609,7 +609,7 @@ mce_status mce_create(const int32_t *offsets, const int32_t *adj, int32_t n, int
     else mce_config_default(&h->cfg);
     if (h->cfg.donate_min_p < 1) h->cfg.donate_min_p = 1;
     if (h->cfg.induced < 0 || h->cfg.induced > 2 || h->cfg.subtree_level < 1 ||
-        h->cfg.subtree_level > 2) {
+        h->cfg.subtree_level > 2 || h->cfg.overlap_builds < 0 || h->cfg.overlap_builds > 1) {
         delete h;
         return MCE_ERR_INVALID_ARG;
     }
@@ -620,7 +620,6 @@ mce_status mce_create(const int32_t *offsets, const int32_t *adj, int32_t n, int
     if (const char *e = getenv("MCE_AB_SMALL_HI")) h->small_hi = atoi(e);
     if (const char *e = getenv("MCE_AB_RECORDS")) h->records = atoi(e) != 0;
     if (const char *e = getenv("MCE_AB_RECORD_MASK")) h->record_mask = atoi(e);
-    if (const char *e = getenv("MCE_AB_SIDE")) h->use_side = atoi(e) != 0;
     if (h->small_hi > kSmallPMax) h->small_hi = kSmallPMax;
 #endif
     mce_status st = create_impl(h, offsets, adj, n, is_device_ptr, (cudaStream_t)stream);

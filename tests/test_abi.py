@@ -48,10 +48,10 @@ def test_calls_that_need_no_gpu(lib):
     # argument errors are caught before any CUDA call
     assert lib.mce_create(None, None, 5, 0, None, None, ctypes.byref(out)) == 1
     assert lib.mce_create(None, None, 0, 0, None, None, None) == 1
-    assert (cfg.induced, cfg.subtree_level) == (0, 1)
+    assert (cfg.induced, cfg.subtree_level, cfg.overlap_builds) == (0, 1, 1)
     offs = (ctypes.c_int32 * 2)(0, 0)
     for field, value in [("induced", 3), ("induced", -1), ("subtree_level", 0),
-                         ("subtree_level", 3)]:
+                         ("subtree_level", 3), ("overlap_builds", 2), ("overlap_builds", -1)]:
         bad = mce.Config()
         lib.mce_config_default(ctypes.byref(bad))
         setattr(bad, field, value)

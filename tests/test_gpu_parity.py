@@ -187,6 +187,16 @@ def test_repeat_is_deterministic():
     assert a == b
 
 
+@pytest.mark.parametrize("overlap", [0, 1])
+def test_builds_on_either_stream(overlap):
+    # subtree builds on the handle's own stream or on the caller's: the same results
+    g = G.config_graph("rmat_s12", 2)
+    roots = np.arange(0, g.n, 3, dtype=np.int32)
+    with gpu_graph(g, overlap_builds=overlap) as h:
+        assert h.count_result() == O.count(g, threads=8).key()
+        assert h.count_roots_result(roots) == O.count(g, roots=roots, threads=8).key()
+
+
 @pytest.mark.parametrize("name,seed", [("rmat_s12", 1), ("sbm_c50", 2), ("planted50k", 3),
                                        ("sbm1m", 1)])
 def test_count_after_each_reorder(name, seed):
