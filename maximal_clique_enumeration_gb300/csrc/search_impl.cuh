@@ -1490,6 +1490,62 @@ __device__ __forceinline__ bool record_matches(const SearchArgs &a, int i, int d
     return a.rec_off[i + 1] - a.rec_off[i] == rec_quads(deg, np, W);
 }
 
+// A 1-word root builds its rows by binary search when its neighbours' later-neighbour lists
+// hold at least this many entries on average (measured: R-MAT s20's average 227 gains 36 %;
+// SBM's 34 loses to the walk, whose loads are independent where a search's are a chain).
+#ifndef MCE_SEARCH_MIN_AVG_LIST
+#define MCE_SEARCH_MIN_AVG_LIST 64
+#endif
+constexpr int kSearchMinAvgList = MCE_SEARCH_MIN_AVG_LIST;
+
+// Rows of a 1-word root (|P| <= 32) by binary search: instead of walking N+(u) for each
+// u in N(v) (about 225 entries per list on R-MAT), each member p_i of P is looked up in the
+// id-sorted N+(u) (about log2 |N+(u)| loads).  The warp takes 32 / S neighbours at a time,
+// S = |P| rounded up to a power of two lanes each, lane i of a group searching p_i; the
+// group's ballot is row t.  u = p_t in P holds only later vertices in N+(u), so a pair
+// (p_t, p_i) is searched only when p_i comes later than p_t, and the earlier one's hit also
+// sets bit t of row i (kept per lane, OR-ed into row i at the end).  No atomics.
+__device__ void build_rows_w1(const SearchArgs &a, const RootCtx &r, int deg, int np, int lane)
+{
+    int S = 1;
+    while (S < np) S <<= 1;
+    const int T = 32 / S;                       // neighbours per step
+    const int sub = lane / S, i = lane % S;
+    const int p = i < np ? r.pids[i] : -1;
+    const int rp = i < np ? __ldg(a.g.rank + p) : 0;
+    const unsigned gmask = S == 32 ? 0xffffffffu : ((1u << S) - 1u);
+    unsigned sym = 0;                           // bit t: p_t is an earlier P-neighbour of p_i
+    for (int t0 = 0; t0 < deg; t0 += T) {
+        const int t = t0 + sub;
+        bool found = false;
+        if (t < deg && i < np) {
+            const int u = t < np ? r.pids[t] : r.xids[t - np];
+            // p_i can be in N+(u) only if it comes after u (always, for u in X)
+            if (t >= np || rp > __ldg(a.g.rank + u)) {
+                const int *lst = a.g.padj + __ldg(a.g.offs + u);
+                int lo = 0, hi = __ldg(a.g.pcount + u);
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (__ldg(lst + mid) < p) lo = mid + 1;
+                    else hi = mid;
+                }
+                found = lo < __ldg(a.g.pcount + u) && __ldg(lst + lo) == p;
+            }
+        }
+        const unsigned m = __ballot_sync(kFull, found);
+        if (found && t < np) sym |= 1u << t;
+        if (i == 0 && t < deg) r.rowsP[t] = (m >> (sub * S)) & gmask;
+    }
+    // row i of P: its later P-neighbours (written above) and its earlier ones (sym, spread over
+    // the groups' lanes i)
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1)
+        if (o >= S) sym |= __shfl_xor_sync(kFull, sym, o);
+    __syncwarp();
+    if (lane < np) r.rowsP[lane] |= sym;
+    __syncwarp();
+}
+
 // Builds the record of first-level root v (deg neighbours, np of them later) at rec.
 template <int W>
 __device__ void build_record(const SearchArgs &a, const WarpSmem &sm, int v, int deg, int np,
@@ -1528,25 +1584,39 @@ __device__ void build_record(const SearchArgs &a, const WarpSmem &sm, int v, int
             xi += __popc(mx);
         }
     }
-    for (long long t = (long long)lane * CH; t < (long long)deg * W; t += 32 * CH)
-        ck_store<CH>(r.rowsP + t, ck_zero<CH>());
-    int slots = 32;
-    while (slots < 2 * np) slots <<= 1;
-    WarpSmem h = sm;
-    h.slots = slots;
-    for (int i = lane; i < slots; i += 32) h.hkey[i] = -1;
-    for (int i = lane; i < kFilterWords; i += 32) h.filter[i] = 0u;
-    __syncwarp();
-    for (int i = lane; i < np; i += 32) {
-        const int id = r.pids[i];
-        unsigned sl = hash_slot(id, slots - 1);
-        while (atomicCAS(&h.hkey[sl], -1, id) != -1) sl = (sl + 1) & (unsigned)(slots - 1);
-        h.hval[sl] = i;
-        const unsigned f = filter_bit(id);
-        atomicOr(&h.filter[f >> 5], 1u << (f & 31));
+    __syncwarp();                                       // P's and X's ids written
+    // 1-word roots whose later-neighbour lists are long on average: binary searches (the
+    // walk's cost grows with the lists, the searches' with their logarithm)
+    bool by_search = false;
+    if constexpr (W == 1) {
+        int walk = 0;
+        for (int t = lane; t < deg; t += 32)
+            walk += __ldg(a.g.pcount + (t < np ? r.pids[t] : r.xids[t - np]));
+        by_search = __reduce_add_sync(kFull, (unsigned)walk) >= (unsigned)(kSearchMinAvgList * deg);
     }
-    __syncwarp();
-    build_flat<W, kBuildBatch>(a, r, h, deg, np, lane);
+    if (by_search) {
+        build_rows_w1(a, r, deg, np, lane);
+    } else {
+        for (long long t = (long long)lane * CH; t < (long long)deg * W; t += 32 * CH)
+            ck_store<CH>(r.rowsP + t, ck_zero<CH>());
+        int slots = 32;
+        while (slots < 2 * np) slots <<= 1;
+        WarpSmem h = sm;
+        h.slots = slots;
+        for (int i = lane; i < slots; i += 32) h.hkey[i] = -1;
+        for (int i = lane; i < kFilterWords; i += 32) h.filter[i] = 0u;
+        __syncwarp();
+        for (int i = lane; i < np; i += 32) {
+            const int id = r.pids[i];
+            unsigned sl = hash_slot(id, slots - 1);
+            while (atomicCAS(&h.hkey[sl], -1, id) != -1) sl = (sl + 1) & (unsigned)(slots - 1);
+            h.hval[sl] = i;
+            const unsigned f = filter_bit(id);
+            atomicOr(&h.filter[f >> 5], 1u << (f & 31));
+        }
+        __syncwarp();
+        build_flat<W, kBuildBatch>(a, r, h, deg, np, lane);
+    }
     // the X rows with a neighbour in P, and whether one X vertex is adjacent to all of P (then
     // the subtree holds no maximal clique: that vertex would be the root's Tomita pivot with
     // nothing left to branch on)
