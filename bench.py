@@ -229,6 +229,9 @@ def stage_bytes(g, rank, roots, peel_live):
                + 4 sum_{u in N(v)} |N+(u)|  the later-neighbour lists walked
                + 4 (deg(v) W(v) + deg(v) + 2 |P(v)| + 4)  the record written: rows, P's ids
                                             and keys, the live X list, its header
+                 A 1-word root whose lists average >= 64 entries searches instead of walking:
+                 its walk term becomes 4 sum_u pairs(u) (ceil(log2(|N+(u)| + 1)) + 1), with
+                 pairs(u) = |P| for u in X and (|P| - 1) / 2 on average for u in P.
     """
     n, m = g.n, g.m
     deg = g.degrees()
@@ -236,7 +239,14 @@ def stage_bytes(g, rank, roots, peel_live):
     src = np.repeat(np.arange(n), deg)
     walk = np.bincount(src, weights=pc[g.adj].astype(np.float64), minlength=n)
     w = np.select([pc <= 32, pc <= 64, pc <= 128, pc <= 256, pc <= 512], [1, 2, 4, 8, 16], 32)
-    per_root = 16.0 * deg + 4.0 * walk + 4.0 * (deg * w + deg + 2.0 * pc + 4.0)
+    # 1-word roots on the binary-search path (the build kernel's rule)
+    steps = np.ceil(np.log2(pc[g.adj] + 1.0)) + 1.0
+    later = rank[g.adj] > rank[src]
+    pairs = np.where(later, (pc[src] - 1) / 2.0, pc[src].astype(np.float64))
+    probes = np.bincount(src, weights=pairs * steps, minlength=n)
+    search = (w == 1) & (walk >= 64.0 * deg)
+    read = np.where(search, probes, walk)
+    per_root = 16.0 * deg + 4.0 * read + 4.0 * (deg * w + deg + 2.0 * pc + 4.0)
     sel = np.zeros(n, bool)
     sel[roots] = True
     sel &= pc > 0
