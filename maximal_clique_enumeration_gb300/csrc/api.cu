@@ -36,7 +36,7 @@ struct mce_graph {
     // the builds run on a stream of the handle's own, forked from the caller's stream, so that
     // the build of a narrower group overlaps the search of the wider ones
     cudaStream_t side = nullptr;
-    cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_built[3] = {};
+    cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_built[6] = {};   // per launch group
     bool unit_own = false;    // unit_cnt / unit_scan were reallocated for a caller's root list
     int degeneracy = 0, max_degree = 0, hist_len = 2, rounds = 0;
     unsigned long long ws_words = 0;
@@ -56,8 +56,8 @@ struct mce_graph {
     cudaEvent_t ev_order[3] = {nullptr, nullptr, nullptr};   // start, end, after the peel
     cudaEvent_t ev_grp[kNumGroups][2] = {};
     bool grp_timed[kNumGroups] = {};
-    cudaEvent_t ev_bld[3][2] = {};               // around the build launches (rows 1, 2, 4 words)
-    bool bld_timed[3] = {};
+    cudaEvent_t ev_bld[6][2] = {};               // around the build launches (groups 0 .. 5)
+    bool bld_timed[6] = {};
     bool order_timed = false;
     int launches_order = 0, launches_count = 0;
 };
@@ -193,10 +193,11 @@ void free_all(mce_graph *h)
     for (int k = 0; k < kNumGroups; ++k)
         for (int i = 0; i < 2; ++i)
             if (h->ev_grp[k][i]) cudaEventDestroy(h->ev_grp[k][i]);
-    for (cudaEvent_t e : {h->ev_fork, h->ev_join, h->ev_built[0], h->ev_built[1], h->ev_built[2],
-                          h->ev_bld[0][0], h->ev_bld[0][1], h->ev_bld[1][0], h->ev_bld[1][1],
-                          h->ev_bld[2][0], h->ev_bld[2][1]})
+    for (cudaEvent_t e : {h->ev_fork, h->ev_join})
         if (e) cudaEventDestroy(e);
+    for (int gi = 0; gi < 6; ++gi)
+        for (cudaEvent_t e : {h->ev_built[gi], h->ev_bld[gi][0], h->ev_bld[gi][1]})
+            if (e) cudaEventDestroy(e);
     if (h->side) cudaStreamDestroy(h->side);
     h->side = nullptr;
 }
@@ -211,7 +212,7 @@ mce_status reset_search(mce_graph *h, cudaStream_t s)
     MCE_TRY(cudaMemsetAsync(h->g.prof_sm, 0, sizeof(unsigned long long) * kNumClasses * kProfSms,
                             s));
     for (int k = 0; k < kNumGroups; ++k) h->grp_timed[k] = false;
-    for (int k = 0; k < 3; ++k) h->bld_timed[k] = false;
+    for (int gi = 0; gi < 6; ++gi) h->bld_timed[gi] = false;
     MCE_TRY(cudaMemsetAsync(h->hist_acc, 0, sizeof(unsigned long long) * h->hist_len, s));
     return MCE_OK;
 }
@@ -249,7 +250,7 @@ mce_status run_search(mce_graph *h, cudaStream_t s, bool user_roots, const DevOu
         a.bb_quads = h->bb_quads;
         a.rec_off = user_roots ? h->urec_off : h->rec_off;
     }
-    // normal roots of row width <= 4 words: subtrees built ahead when the records fit (the
+    // roots of row width <= 4 words: subtrees built ahead when the records fit (the
     // schedule's always do; a caller's list is checked on the device, and the plain search
     // launch after the record search does the work when they do not)
     auto launched = [&](int gi) {
@@ -257,15 +258,26 @@ mce_status run_search(mce_graph *h, cudaStream_t s, bool user_roots, const DevOu
     };
     auto with_records = [&](int gi) {
         const int k = gi / 2;
-        return a.bb != nullptr && (gi & 1) && k <= 2 && ((h->record_mask >> k) & 1) &&
+        return a.bb != nullptr && k <= 2 && ((h->record_mask >> k) & 1) &&
                launched(gi);
     };
     const long long *gate = a.bb ? a.rec_off + (user_roots ? h->n_uroots : h->n) : nullptr;
+    // launch order: widest rows first, per width the big-workspace group first, except where
+    // both groups of a width search records: then the normal group goes first (its build is
+    // the long one; the big group's, the covering tests of a few hubs, overlaps its search)
+    int order[kNumGroups];
+    for (int o = 0; o < kNumGroups; ++o) order[o] = group_at(o);
+    for (int o = 0; o + 1 < kNumGroups; o += 2)
+        if (with_records(order[o]) && with_records(order[o + 1])) {
+            const int t = order[o];
+            order[o] = order[o + 1];
+            order[o + 1] = t;
+        }
     bool forked = false;
     if (h->side) {
-        // all builds on the side stream, widest first (the order of the searches)
-        for (int k = 2; k >= 0; --k) {
-            const int gi = 2 * k + 1;
+        // all builds on the side stream, in the order of the searches
+        for (int o = 0; o < kNumGroups; ++o) {
+            const int gi = order[o], k = gi / 2;
             if (!with_records(gi)) continue;
             if (!forked) {
                 MCE_TRY(cudaEventRecord(h->ev_fork, s));
@@ -276,18 +288,18 @@ mce_status run_search(mce_graph *h, cudaStream_t s, bool user_roots, const DevOu
             b.cls = k;
             b.group = gi;
             b.rec_gate = gate;
-            if (h->cfg.profile) MCE_TRY(cudaEventRecord(h->ev_bld[k][0], h->side));
+            if (h->cfg.profile) MCE_TRY(cudaEventRecord(h->ev_bld[gi][0], h->side));
             MCE_TRY(launch_build(b, h->build_blocks[k], h->side));
             if (h->cfg.profile) {
-                MCE_TRY(cudaEventRecord(h->ev_bld[k][1], h->side));
-                h->bld_timed[k] = true;
+                MCE_TRY(cudaEventRecord(h->ev_bld[gi][1], h->side));
+                h->bld_timed[gi] = true;
             }
-            MCE_TRY(cudaEventRecord(h->ev_built[k], h->side));
+            MCE_TRY(cudaEventRecord(h->ev_built[gi], h->side));
         }
         if (forked) MCE_TRY(cudaEventRecord(h->ev_join, h->side));
     }
     for (int o = 0; o < kNumGroups; ++o) {
-        const int gi = group_at(o), k = gi / 2;
+        const int gi = order[o], k = gi / 2;
         if (!launched(gi)) continue;                      // no root of the call in this group
         a.cls = k;
         a.group = gi;
@@ -299,13 +311,13 @@ mce_status run_search(mce_graph *h, cudaStream_t s, bool user_roots, const DevOu
         a.rec_gate = rec ? gate : nullptr;
         if (rec) {
             if (forked) {
-                MCE_TRY(cudaStreamWaitEvent(s, h->ev_built[k], 0));
+                MCE_TRY(cudaStreamWaitEvent(s, h->ev_built[gi], 0));
             } else {
-                if (h->cfg.profile) MCE_TRY(cudaEventRecord(h->ev_bld[k][0], s));
+                if (h->cfg.profile) MCE_TRY(cudaEventRecord(h->ev_bld[gi][0], s));
                 MCE_TRY(launch_build(a, h->build_blocks[k], s));
                 if (h->cfg.profile) {
-                    MCE_TRY(cudaEventRecord(h->ev_bld[k][1], s));
-                    h->bld_timed[k] = true;
+                    MCE_TRY(cudaEventRecord(h->ev_bld[gi][1], s));
+                    h->bld_timed[gi] = true;
                 }
             }
         }
@@ -469,9 +481,9 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
             MCE_TRY(cudaEventCreate(&h->ev_grp[k][0]));
             MCE_TRY(cudaEventCreate(&h->ev_grp[k][1]));
         }
-        for (int k = 0; k < 3; ++k) {
-            MCE_TRY(cudaEventCreate(&h->ev_bld[k][0]));
-            MCE_TRY(cudaEventCreate(&h->ev_bld[k][1]));
+        for (int gi = 0; gi < 6; ++gi) {
+            MCE_TRY(cudaEventCreate(&h->ev_bld[gi][0]));
+            MCE_TRY(cudaEventCreate(&h->ev_bld[gi][1]));
         }
     }
     g.ip = h->cfg.induced == 2 ? 1 : 0;
@@ -556,7 +568,7 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
     h->ws_words = ws_total;
     MCE_ALLOC(h, h->ws, ws_total);
     // subtrees built ahead of the search (full induced subgraphs of first-level subtrees): one
-    // record per root of the schedule's normal launch groups of row width <= 4 words, when all
+    // record per root of the schedule's launch groups of row width <= 4 words, when all
     // of them fit in kRecCapQuads
     if (h->records && !g.ip && !g.l2 && n > 0) {
         MCE_ALLOC(h, h->rec_off, (size_t)n + 1);
@@ -574,9 +586,10 @@ static mce_status create_impl(mce_graph *h, const int32_t *offsets, const int32_
             h->bb = nullptr;
         if (h->bb && h->cfg.overlap_builds) {
             MCE_TRY(cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking));
-            for (cudaEvent_t *e : {&h->ev_fork, &h->ev_join, &h->ev_built[0], &h->ev_built[1],
-                                   &h->ev_built[2]})
+            for (cudaEvent_t *e : {&h->ev_fork, &h->ev_join})
                 MCE_TRY(cudaEventCreateWithFlags(e, cudaEventDisableTiming));
+            for (int gi = 0; gi < 6; ++gi)
+                MCE_TRY(cudaEventCreateWithFlags(&h->ev_built[gi], cudaEventDisableTiming));
         }
     }
     MCE_ALLOC(h, h->ring, (size_t)h->n_workers);
@@ -890,8 +903,13 @@ mce_status mce_get_info(mce_graph *h, mce_info *info)
             info->ms_search[k] += ms;
         }
         info->ms_build[k] = 0.f;
-        if (k < 3 && h->bld_timed[k])
-            MCE_TRY(cudaEventElapsedTime(&info->ms_build[k], h->ev_bld[k][0], h->ev_bld[k][1]));
+        for (int b = 0; b < 2 && k < 3; ++b) {
+            const int gi = 2 * k + b;
+            if (!h->bld_timed[gi]) continue;
+            float ms = 0.f;
+            MCE_TRY(cudaEventElapsedTime(&ms, h->ev_bld[gi][0], h->ev_bld[gi][1]));
+            info->ms_build[k] += ms;
+        }
     }
     if (h->order_timed && h->n > 0) {
         MCE_TRY(cudaEventElapsedTime(&info->ms_order, h->ev_order[0], h->ev_order[1]));

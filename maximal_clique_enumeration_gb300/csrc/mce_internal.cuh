@@ -238,8 +238,11 @@ __device__ inline int sched_bucket(int np, int deg, bool ip, bool l2, int core)
     const int k = wclass_index(np);
     const int b = np > 0 && ws_layout(deg, np, ip, l2).total > kWsCapWords ? 0 : 1;
     // the subtree's cost grows with |P| and with how dense the region is (its core number)
-    const unsigned long long est = (unsigned long long)(np + 1) * (unsigned long long)(np + 1) *
-                                   (unsigned long long)(core + 1);
+    unsigned long long est = (unsigned long long)(np + 1) * (unsigned long long)(np + 1) *
+                             (unsigned long long)(core + 1);
+#ifdef MCE_EST_X_DIV
+    if (MCE_EST_X_DIV > 0) est *= 1ULL + (unsigned long long)(deg - np) / MCE_EST_X_DIV;
+#endif
     int lb = est ? 63 - __clzll((long long)est) : 0;
     lb = lb < kCostBuckets - 1 ? lb : kCostBuckets - 1;
     return 1 + position_of(2 * k + b) * kCostBuckets + (kCostBuckets - 1 - lb);
@@ -264,13 +267,13 @@ cudaError_t launch_search(const SearchArgs &a, int blocks, int threads, size_t s
                           cudaStream_t s);
 cudaError_t launch_search_prep(const SearchArgs &a, cudaStream_t s);
 // Subtrees built ahead: rec_off[i] = quad offset of the record of the root at place i of
-// roots[0 .. n_slots) (the roots of the normal launch groups of row width <= 4 words have one;
+// roots[0 .. n_slots) (the roots of the launch groups of row width <= 4 words have one;
 // range = the launch groups' places), rec_off[n_slots] = the total; scan_tmp holds
 // n_slots / kScanBlock + 2 partial sums.
 cudaError_t launch_record_offsets(const DevGraph &g, const int *roots, const int *range,
                                   int n_slots, long long *scan_tmp, long long *rec_off,
                                   cudaStream_t s);
-// The build launch of normal launch group a.group (row width 1 << a.cls <= 4 words).
+// The build launch of launch group a.group (row width 1 << a.cls <= 4 words).
 cudaError_t launch_build(const SearchArgs &a, int blocks, cudaStream_t s);
 // CTAs per SM of that build kernel.
 cudaError_t build_occupancy(int cls, int *blocks_per_sm);

@@ -81,13 +81,13 @@ __global__ void enum_close_kernel(DevOut o, const long long *totals)
 
 constexpr int kRecThreads = 256;   // 4 places per thread: kScanBlock places per CTA
 
-// Record size (quads) of the root at place i: roots of the normal launch groups of row width
-// 1, 2 and 4 words (groups 1, 3, 5) have one.
+// Record size (quads) of the root at place i: roots of the launch groups of row width 1, 2
+// and 4 words (groups 0 .. 5) have one.
 __device__ __forceinline__ long long record_quads(const DevGraph &g, const int *roots,
                                                   const int *range, int i)
 {
-    for (int k = 0; k < 3; ++k) {
-        const int gi = 2 * k + 1;
+    for (int gi = 0; gi < 6; ++gi) {
+        const int k = gi / 2;
         if (i >= range[2 * gi] && i < range[2 * gi + 1]) {
             const int v = roots[i];
             const int np = g.pcount[v];
@@ -179,7 +179,7 @@ const void *search_kernel_partial(int cls, bool big);
 const void *search_kernel_full_l2(int cls, bool big);
 const void *search_kernel_partial_l2(int cls, bool big);
 
-const void *search_kernel_full_rec(int cls);
+const void *search_kernel_full_rec(int cls, bool big);
 
 static const void *search_kernel_ptr(int cls, int ip, int l2, bool big)
 {
@@ -190,7 +190,7 @@ static const void *search_kernel_ptr(int cls, int ip, int l2, bool big)
 // Does launch group `group` have a variant that searches subtrees built ahead?
 static bool has_rec_variant(int group, int ip, int l2)
 {
-    return !ip && !l2 && (group & 1) && group / 2 <= 2;
+    return !ip && !l2 && group / 2 <= 2;
 }
 
 cudaError_t search_configure(int cls, int ip, int l2, size_t smem)
@@ -201,9 +201,12 @@ cudaError_t search_configure(int cls, int ip, int l2, size_t smem)
                                                    (int)smem);
         if (e != cudaSuccess) return e;
     }
-    if (has_rec_variant(2 * cls + 1, ip, l2))
-        return cudaFuncSetAttribute(search_kernel_full_rec(cls),
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    for (int big = 0; big < 2 && has_rec_variant(2 * cls + 1, ip, l2); ++big) {
+        const cudaError_t e = cudaFuncSetAttribute(search_kernel_full_rec(cls, big != 0),
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)smem);
+        if (e != cudaSuccess) return e;
+    }
     return cudaSuccess;
 }
 
@@ -215,8 +218,8 @@ cudaError_t search_occupancy(int group, int ip, int l2, int threads, size_t smem
     if (e != cudaSuccess || !has_rec_variant(group, ip, l2)) return e;
     // one geometry serves both variants
     int rec = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&rec, search_kernel_full_rec(group / 2),
-                                                      threads, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &rec, search_kernel_full_rec(group / 2, (group & 1) == 0), threads, smem);
     if (rec < *blocks_per_sm) *blocks_per_sm = rec;
     return e;
 }
@@ -227,7 +230,7 @@ cudaError_t launch_search(const SearchArgs &a, int blocks, int threads, size_t s
     SearchArgs aa = a;
     void *args[] = {&aa};
     const void *k = rec && has_rec_variant(a.group, a.g.ip, a.g.l2)
-                        ? search_kernel_full_rec(a.cls)
+                        ? search_kernel_full_rec(a.cls, (a.group & 1) == 0)
                         : search_kernel_ptr(a.cls, a.g.ip, a.g.l2, (a.group & 1) == 0);
     return cudaLaunchKernel(k, dim3(blocks), dim3(threads), args, smem, s);
 }

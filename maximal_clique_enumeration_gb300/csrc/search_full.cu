@@ -18,12 +18,12 @@ const void *search_kernel_full(int cls, bool big)
     }
 }
 
-const void *search_kernel_full_rec(int cls)
+const void *search_kernel_full_rec(int cls, bool big)
 {
     switch (cls) {
-    case 0: return (const void *)search_kernel<1, false, true>;
-    case 1: return (const void *)search_kernel<2, false, true>;
-    default: return (const void *)search_kernel<4, false, true>;
+    case 0: return big ? (const void *)search_kernel<1, true, true> : (const void *)search_kernel<1, false, true>;
+    case 1: return big ? (const void *)search_kernel<2, true, true> : (const void *)search_kernel<2, false, true>;
+    default: return big ? (const void *)search_kernel<4, true, true> : (const void *)search_kernel<4, false, true>;
     }
 }
 

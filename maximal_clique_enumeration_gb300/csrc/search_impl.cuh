@@ -1458,8 +1458,8 @@ __device__ void search_root(const SearchArgs &a, unsigned *ws, const WarpSmem &s
 
 // ------------------------------------------------------------------ subtrees built ahead
 //
-// The default search (full induced subgraphs, first-level subtrees) of the normal roots of
-// row width W <= 4 runs in two launches per launch group: build_kernel builds every root's
+// The default search (full induced subgraphs, first-level subtrees) of the roots of row width
+// W <= 4 runs in two launches per launch group: build_kernel builds every root's
 // induced subgraph into a record of its own (RecLayout), then the search kernel searches the
 // records.  The build is a walk of later-neighbour lists that waits on L2 gathers; in a kernel
 // of its own it runs with few registers at 32 warps per SM and kBuildBatch loads in flight per
@@ -1549,7 +1549,7 @@ __device__ void build_rows_w1(const SearchArgs &a, const RootCtx &r, int deg, in
 // Builds the record of first-level root v (deg neighbours, np of them later) at rec.
 template <int W>
 __device__ void build_record(const SearchArgs &a, const WarpSmem &sm, int v, int deg, int np,
-                             unsigned *rec, int lane)
+                             bool big, unsigned *rec, int lane)
 {
     constexpr int CH = Geo<W>::CH;
     const RecLayout L = rec_layout(deg, np, W);
@@ -1585,23 +1585,11 @@ __device__ void build_record(const SearchArgs &a, const WarpSmem &sm, int v, int
         }
     }
     __syncwarp();                                       // P's and X's ids written
-    // 1-word roots whose later-neighbour lists are long on average: binary searches (the
-    // walk's cost grows with the lists, the searches' with their logarithm)
-    bool by_search = false;
-    if constexpr (W == 1) {
-        int walk = 0;
-        for (int t = lane; t < deg; t += 32)
-            walk += __ldg(a.g.pcount + (t < np ? r.pids[t] : r.xids[t - np]));
-        by_search = __reduce_add_sync(kFull, (unsigned)walk) >= (unsigned)(kSearchMinAvgList * deg);
-    }
-    if (by_search) {
-        build_rows_w1(a, r, deg, np, lane);
-    } else {
-        for (long long t = (long long)lane * CH; t < (long long)deg * W; t += 32 * CH)
-            ck_store<CH>(r.rowsP + t, ck_zero<CH>());
+    // the hash of P and its filter, for the walk and the covering test
+    WarpSmem h = sm;
+    auto hash_p = [&]() {
         int slots = 32;
         while (slots < 2 * np) slots <<= 1;
-        WarpSmem h = sm;
         h.slots = slots;
         for (int i = lane; i < slots; i += 32) h.hkey[i] = -1;
         for (int i = lane; i < kFilterWords; i += 32) h.filter[i] = 0u;
@@ -1615,22 +1603,52 @@ __device__ void build_record(const SearchArgs &a, const WarpSmem &sm, int v, int
             atomicOr(&h.filter[f >> 5], 1u << (f & 31));
         }
         __syncwarp();
-        build_flat<W, kBuildBatch>(a, r, h, deg, np, lane);
+    };
+    // a root of the big-workspace group (a hub: X of thousands) is first tested for an X vertex
+    // adjacent to all of P, which is found early in X when there is one (then no rows are
+    // built: the subtree holds no maximal clique); the candidates' list goes in the rows' space
+    bool covered = false, hashed = false;
+    if (big) {
+        hash_p();
+        hashed = true;
+        RootCtx rc = r;
+        rc.spill = reinterpret_cast<int *>(r.rowsP);
+        covered = x_covers_p(a.g, rc, h, np, lane);
     }
-    // the X rows with a neighbour in P, and whether one X vertex is adjacent to all of P (then
-    // the subtree holds no maximal clique: that vertex would be the root's Tomita pivot with
-    // nothing left to branch on)
     int nxx = 0;
-    bool covered = false;
-    for (int base = 0; base < r.nx; base += 32) {
-        const int xi = base + lane;
-        int cnt = 0;
-        if (xi < r.nx)
-            for (int k = 0; k < W; ++k) cnt += __popc(r.rowsX[(long long)xi * W + k]);
-        covered = covered || __any_sync(kFull, cnt == np);
-        const unsigned m = __ballot_sync(kFull, cnt > 0);
-        if (cnt > 0) r.xx[nxx + __popc(m & lt)] = xi;
-        nxx += __popc(m);
+    if (!covered) {
+        // 1-word roots whose later-neighbour lists are long on average: binary searches (the
+        // walk's cost grows with the lists, the searches' with their logarithm)
+        bool by_search = false;
+        if constexpr (W == 1) {
+            int walk = 0;
+            for (int t = lane; t < deg; t += 32)
+                walk += __ldg(a.g.pcount + (t < np ? r.pids[t] : r.xids[t - np]));
+            by_search =
+                __reduce_add_sync(kFull, (unsigned)walk) >= (unsigned)(kSearchMinAvgList * deg);
+        }
+        if (by_search) {
+            build_rows_w1(a, r, deg, np, lane);
+        } else {
+            for (long long t = (long long)lane * CH; t < (long long)deg * W; t += 32 * CH)
+                ck_store<CH>(r.rowsP + t, ck_zero<CH>());
+            if (!hashed) hash_p();
+            __syncwarp();
+            build_flat<W, kBuildBatch>(a, r, h, deg, np, lane);
+        }
+        // the X rows with a neighbour in P, and whether one X vertex is adjacent to all of P
+        // (then the subtree holds no maximal clique: that vertex would be the root's Tomita
+        // pivot with nothing left to branch on)
+        for (int base = 0; base < r.nx; base += 32) {
+            const int xi = base + lane;
+            int cnt = 0;
+            if (xi < r.nx)
+                for (int k = 0; k < W; ++k) cnt += __popc(r.rowsX[(long long)xi * W + k]);
+            covered = covered || __any_sync(kFull, cnt == np);
+            const unsigned m = __ballot_sync(kFull, cnt > 0);
+            if (cnt > 0) r.xx[nxx + __popc(m & lt)] = xi;
+            nxx += __popc(m);
+        }
     }
     for (int i = lane; i < np; i += 32) r.pkey[i] = vertex_key(r.pids[i]);
     if (lane == 0) {
@@ -1815,11 +1833,11 @@ __device__ __forceinline__ void search_unit(const SearchArgs &a, unsigned *ws, c
 // One persistent launch per row width W and launch group: the roots of that class, heaviest
 // first, then donated branches of those roots (Section 3.3).  Big: the group of roots whose
 // workspace exceeds kWsCapWords (their build code is compiled into these instances only).
-// Rec: the roots' subtrees were built ahead by build_kernel (normal groups, W <= 4).
+// Rec: the roots' subtrees were built ahead by build_kernel (W <= 4).
 template <int W, bool Big, bool Rec = false>
 __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(SearchArgs a)
 {
-    if constexpr (!kIP && !kL2 && !Big && W <= 4) {
+    if constexpr (!kIP && !kL2 && W <= 4) {
         if (a.rec_gate != nullptr && records_on(a) != Rec) return;   // the other variant works
     }
     extern __shared__ __align__(16) unsigned char s_raw[];
@@ -1983,7 +2001,7 @@ __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(Search
 
 #if !MCE_SEARCH_IP && !MCE_SEARCH_L2
 // The subtree build ahead of the search (see "subtrees built ahead"): the warps take the roots
-// of one normal launch group of row width W <= 4 in turn and build each one's record.
+// of one launch group of row width W <= 4 in turn and build each one's record.
 template <int W>
 __global__ void __launch_bounds__(kBuildThreads, kBuildMinBlocks) build_kernel(SearchArgs a)
 {
@@ -2014,7 +2032,7 @@ __global__ void __launch_bounds__(kBuildThreads, kBuildMinBlocks) build_kernel(S
             if (lane == 0) set_status(a.g.ctrl, MCE_ERR_INTERNAL);
             continue;
         }
-        build_record<W>(a, sm, v, deg, np, a.bb + a.rec_off[i] * 4, lane);
+        build_record<W>(a, sm, v, deg, np, (a.group & 1) == 0, a.bb + a.rec_off[i] * 4, lane);
     }
 }
 #endif
