@@ -295,9 +295,11 @@ __host__ __device__ inline size_t warp_smem_bytes(int k)
     return (size_t)hash_slots(k) * 8 + kFilterWords * 4 + 2 * 36 * 4 +
            (size_t)smem_row_words(k) * 4;
 }
+// Per warp of the build kernel: the hash of P and its filter, the walk's cursors, and a queue
+// of 64 walked entries that passed the filter (ids and rows).
 __host__ __device__ inline size_t build_smem_per_warp(int k)
 {
-    return (size_t)hash_slots(k) * 8 + kFilterWords * 4 + 2 * 36 * 4;
+    return (size_t)hash_slots(k) * 8 + kFilterWords * 4 + 2 * 36 * 4 + 2 * 64 * 4;
 }
 __host__ __device__ inline size_t search_smem_bytes(int k, int hist_len, int warps)
 {

@@ -1490,6 +1490,125 @@ __device__ __forceinline__ bool record_matches(const SearchArgs &a, int i, int d
     return a.rec_off[i + 1] - a.rec_off[i] == rec_quads(deg, np, W);
 }
 
+// The build kernel's walk (rows of roots built ahead): the walk of build_flat, but an entry
+// that passes P's filter (about 6 % on R-MAT) is not looked up at once.  It goes into a queue
+// of the warp in shared memory (id, row), appended by ballot, and every 32 queued entries are
+// looked up in the hash and set in the rows by the whole warp.  Probing at once would run the
+// hash lookup and the row updates for the one or two positive lanes of most 32-entry steps.
+__device__ __forceinline__ bool filter_hit(const WarpSmem &h, int id)
+{
+    const unsigned f = filter_bit(id);
+    return (h.filter[f >> 5] >> (f & 31)) & 1u;
+}
+
+template <int W>
+__device__ __forceinline__ void drain_queue(const WarpSmem &h, unsigned *rows, int np,
+                                            const int *qw, const int *qt, int count, int lane)
+{
+    if (lane < count) {
+        const int id = qw[lane], tt = qt[lane];
+        const int mask = h.slots - 1;
+        unsigned s = hash_slot(id, mask);
+        int j = -1;
+        while (true) {
+            const int k = h.hkey[s];
+            if (k == id) { j = h.hval[s]; break; }
+            if (k < 0) break;
+            s = (s + 1) & (unsigned)mask;
+        }
+        if (j >= 0) {
+            atomicOr(rows + (long long)tt * W + (j >> 5), 1u << (j & 31));
+            if (tt < np) atomicOr(rows + (long long)j * W + (tt >> 5), 1u << (tt & 31));
+        }
+    }
+}
+
+template <int W, int kB>
+__device__ void build_flat_queued(const SearchArgs &a, const RootCtx &r, const WarpSmem &h,
+                                  int *qw, int *qt, int deg, int np, int lane)
+{
+    unsigned *rows = r.rowsP;
+    const unsigned lt = (1u << lane) - 1u;
+    int qn = 0;                                   // queued entries (the same in every lane)
+    for (int g0 = 0; g0 < deg; g0 += 32) {
+        const int t = g0 + lane;
+        int base = 0, len = 0;
+        if (t < deg) {
+            const int u = t < np ? r.pids[t] : r.xids[t - np];
+            base = __ldg(a.g.offs + u);
+            len = __ldg(a.g.pcount + u);
+        }
+        int incl = len;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const int total = __shfl_sync(kFull, incl, 31);
+        h.cur_start[lane] = incl - len;
+        h.cur_base[lane] = base;
+        if (lane == 0) h.cur_start[32] = total;
+        __syncwarp();
+        int own = 0, own_start = 0, own_next = h.cur_start[1], own_base = h.cur_base[0];
+        for (int f0 = 0; f0 < total; f0 += 32 * kB) {
+            int w[kB], ow[kB];
+#pragma unroll
+            for (int b = 0; b < kB; ++b) {
+                const int f = f0 + b * 32 + lane;
+                ow[b] = -1;
+                w[b] = -1;
+                if (f < total) {
+                    if (own_next <= f) {
+                        do {
+                            ++own;
+                            own_start = own_next;
+                            own_next = h.cur_start[own + 1];
+                        } while (own_next <= f);
+                        own_base = h.cur_base[own];
+                    }
+                    ow[b] = own;
+                    w[b] = __ldg(a.g.padj + own_base + (f - own_start));
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < kB; ++b) {
+                const bool pos = ow[b] >= 0 && filter_hit(h, w[b]);
+                const unsigned m = __ballot_sync(kFull, pos);
+                if (m == 0u) continue;
+                if (pos) {
+                    const int at = qn + __popc(m & lt);
+                    qw[at] = w[b];
+                    qt[at] = g0 + ow[b];
+                }
+                qn += __popc(m);
+                if (qn >= 32) {                   // a full warp's worth: look them up
+                    __syncwarp();
+                    drain_queue<W>(h, rows, np, qw, qt, 32, lane);
+                    const int rest = qn - 32;     // at most 31 left: move them to the front
+                    int kw = 0, kt = 0;
+                    if (lane < rest) {
+                        kw = qw[32 + lane];
+                        kt = qt[32 + lane];
+                    }
+                    __syncwarp();
+                    if (lane < rest) {
+                        qw[lane] = kw;
+                        qt[lane] = kt;
+                    }
+                    __syncwarp();
+                    qn = rest;
+                }
+            }
+        }
+        __syncwarp();
+    }
+    if (qn > 0) {
+        __syncwarp();
+        drain_queue<W>(h, rows, np, qw, qt, qn, lane);
+    }
+    __syncwarp();
+}
+
 // A 1-word root builds its rows by binary search when its neighbours' later-neighbour lists
 // hold at least this many entries on average (measured: R-MAT s20's average 227 gains 36 %;
 // SBM's 34 loses to the walk, whose loads are independent where a search's are a chain).
@@ -1634,7 +1753,14 @@ __device__ void build_record(const SearchArgs &a, const WarpSmem &sm, int v, int
                 ck_store<CH>(r.rowsP + t, ck_zero<CH>());
             if (!hashed) hash_p();
             __syncwarp();
-            build_flat<W, kBuildBatch>(a, r, h, deg, np, lane);
+#ifndef MCE_QUEUED_MIN_W
+#define MCE_QUEUED_MIN_W 4
+#endif
+            if constexpr (W >= MCE_QUEUED_MIN_W)
+                build_flat_queued<W, kBuildBatch>(a, r, h, sm.cur_base + 36,
+                                                  sm.cur_base + 36 + 64, deg, np, lane);
+            else
+                build_flat<W, kBuildBatch>(a, r, h, deg, np, lane);
         }
         // the X rows with a neighbour in P, and whether one X vertex is adjacent to all of P
         // (then the subtree holds no maximal clique: that vertex would be the root's Tomita
