@@ -301,10 +301,14 @@ __host__ __device__ inline size_t build_smem_per_warp(int k)
 {
     return (size_t)hash_slots(k) * 8 + kFilterWords * 4 + 2 * 36 * 4 + 2 * 64 * 4;
 }
+// The search kernel's size histogram, at the start of its shared memory.
+__host__ __device__ inline size_t smem_hist_bytes(int hist_len)
+{
+    return ((size_t)(hist_len + 1) * 8 + 15) & ~(size_t)15;
+}
 __host__ __device__ inline size_t search_smem_bytes(int k, int hist_len, int warps)
 {
-    const size_t hist = ((size_t)(hist_len + 1) * 8 + 15) & ~(size_t)15;
-    return hist + (size_t)warps * warp_smem_bytes(k);
+    return smem_hist_bytes(hist_len) + (size_t)warps * warp_smem_bytes(k);
 }
 cudaError_t search_configure(int cls, int ip, int l2, size_t smem);
 cudaError_t launch_bin_roots(const DevGraph &g, const int *roots, int n_roots, cudaStream_t s);
