@@ -283,8 +283,9 @@ constexpr bool kSmemStack = MCE_SMEM_STACK != 0;
 
 // Stack entry of level L.  The first StackLevels<W> levels live in the warp's shared memory,
 // in the space of the P hash and its filter, which no search uses (a subtree's build, when the
-// search kernel runs one, ends before its search starts); the others in the workspace.  A
-// warp's shared memory follows the size histogram, whose length is a kernel argument.
+// search kernel runs one, ends before its search starts); the others in the workspace.  The
+// search carries a pointer to the warp's scratch words (the build's cursor arrays), which
+// follow the hash and the filter: the stack starts a fixed distance before it.
 template <int W>
 struct StackLevels {
     static constexpr int k = W == 1 ? 0 : W == 2 ? 1 : W == 4 ? 2 : W == 8 ? 3 : W == 16 ? 4 : 5;
@@ -294,33 +295,28 @@ struct StackLevels {
 };
 
 template <int W>
-__device__ __forceinline__ unsigned *stack_at(const SearchArgs &a, const RootCtx &r, int L)
+__device__ __forceinline__ unsigned *stack_at(unsigned *scratch, const RootCtx &r, int L)
 {
-    if (L < StackLevels<W>::levels) {
-        extern __shared__ __align__(16) unsigned char s_raw[];
-        return reinterpret_cast<unsigned *>(
-                   s_raw + smem_hist_bytes(a.out.hist_len) +
-                   (size_t)(threadIdx.x >> 5) * warp_smem_bytes(StackLevels<W>::k)) +
-               L * StackLevels<W>::LV;
-    }
+    if (L < StackLevels<W>::levels) return scratch - StackLevels<W>::value + L * StackLevels<W>::LV;
     return r.stack + (long long)L * r.LV;
 }
 
 // Id of element e of the clique R u {c} at level L: R's level-0 part, then the vertex chosen
 // at each level below L, then c.
 template <int W>
-__device__ __forceinline__ int clique_elem(const SearchArgs &a, const RootCtx &r, int L, int c,
+__device__ __forceinline__ int clique_elem(unsigned *scratch, const RootCtx &r, int L, int c,
                                            int e)
 {
     if (e < r.rsize) return r.rids[e];
-    const int loc = e < r.rsize + L ? (int)stack_at<W>(a, r, e - r.rsize)[3] : c;
+    const int loc = e < r.rsize + L ? (int)stack_at<W>(scratch, r, e - r.rsize)[3] : c;
     return r.pids[loc];
 }
 
 // Reports the maximal clique R u {c}: `size` vertices, hash input `hsum` (sum of keys).
 template <int W>
 __device__ void report(const SearchArgs &a, const RootCtx &r, int L, int c, int size,
-                       unsigned long long hsum, Acc &acc, unsigned long long *s_hist, int lane)
+                       unsigned long long hsum, Acc &acc, unsigned long long *s_hist, int lane,
+                       unsigned *scratch)
 {
     if (size >= a.out.hist_len) {                   // cannot happen: size <= d + 1
         if (lane == 0) set_status(a.g.ctrl, MCE_ERR_INTERNAL);
@@ -346,9 +342,9 @@ __device__ void report(const SearchArgs &a, const RootCtx &r, int L, int c, int 
     const long long base = a.out.region_ids[size] + (long long)slot * size;
     if (lane == 0) a.out.offsets[cl] = base;
     for (int e = lane; e < size; e += 32) {
-        const int id = clique_elem<W>(a, r, L, c, e);
+        const int id = clique_elem<W>(scratch, r, L, c, e);
         int rk = 0;
-        for (int f = 0; f < size; ++f) rk += clique_elem<W>(a, r, L, c, f) < id;
+        for (int f = 0; f < size; ++f) rk += clique_elem<W>(scratch, r, L, c, f) < id;
         a.out.ids[base + rk] = id;
     }
 }
@@ -855,7 +851,7 @@ __device__ int ring_try_pop(const SearchArgs &a)
 // Copies the branch R u {c} with sets (Pc, XPc, xx[0..k)) into the workspace `dst` of another
 // warp: the P rows, the k live X rows (renumbered 0..k-1), the P ids and keys, R's ids.
 template <int W>
-__device__ void write_branch(const SearchArgs &a, const RootCtx &r, unsigned *dst, int L, int c,
+__device__ void write_branch(unsigned *scratch, const RootCtx &r, unsigned *dst, int L, int c,
                              const Ck<Geo<W>::CH> &Pc, const Ck<Geo<W>::CH> &XPc, int k,
                              unsigned long long Sc, int lane)
 {
@@ -904,7 +900,7 @@ __device__ void write_branch(const SearchArgs &a, const RootCtx &r, unsigned *ds
         dk[i] = r.pkey[i];
     }
     int *dr = reinterpret_cast<int *>(dst + lay.rids);
-    for (int e = lane; e < rsize; e += 32) dr[e] = clique_elem<W>(a, r, L, c, e);
+    for (int e = lane; e < rsize; e += 32) dr[e] = clique_elem<W>(scratch, r, L, c, e);
     __threadfence();          // every lane's part of the branch is visible GPU-wide ...
     __syncwarp();             // ... before lane 0 publishes it
 }
@@ -960,7 +956,7 @@ __device__ void dfs(const SearchArgs &a, const RootCtx &r, Ck<Geo<W>::CH> P, Ck<
             P0 = P;
             XP0 = XP;
             cursor = -1;
-            unsigned *lv = stack_at<W>(a, r, L);
+            unsigned *lv = stack_at<W>(scratch, r, L);
             if (lane < G) {
                 ck_store<CH>(lv + 8 + q * CH, P0);
                 ck_store<CH>(lv + 8 + W + q * CH, XP0);
@@ -979,7 +975,7 @@ __device__ void dfs(const SearchArgs &a, const RootCtx &r, Ck<Geo<W>::CH> P, Ck<
         if (c == INT_MAX) {                       // level exhausted: back up
             if (L == 0) return;
             --L;
-            const unsigned *lv = stack_at<W>(a, r, L);
+            const unsigned *lv = stack_at<W>(scratch, r, L);
             P0 = ck_load<CH>(lv + 8 + q * CH);
             XP0 = ck_load<CH>(lv + 8 + W + q * CH);
             C = ck_load<CH>(lv + 8 + 2 * W + q * CH);
@@ -1001,14 +997,14 @@ __device__ void dfs(const SearchArgs &a, const RootCtx &r, Ck<Geo<W>::CH> P, Ck<
         if (!__any_sync(kFull, ck_nonzero<CH>(Pc))) {
             // leaf: R u {c} is maximal iff X n N(c) is empty (Algorithm 2, lines 2-3)
             if (!__any_sync(kFull, ck_nonzero<CH>(XPc)) && !xx_hits<W>(a.g, r, lpX, c, acc, lane)) {
-                report<W>(a, r, L, c, r.rsize + L + 1, Sc, acc, s_hist, lane);
+                report<W>(a, r, L, c, r.rsize + L + 1, Sc, acc, s_hist, lane, scratch);
                 acc.nodes++;
             }
             PROF_ADD(acc, kProfChild, t_child);
             continue;
         }
         const bool more_same = lowest_above<W>(C, c, q) != INT_MAX;
-        if (lane == 0) stack_at<W>(a, r, L)[3] = (unsigned)c;
+        if (lane == 0) stack_at<W>(scratch, r, L)[3] = (unsigned)c;
         PROF_ADD(acc, kProfChild, t_child);
         PROF_START(t_part);
         const int lpXc = xx_partition<W>(a.g, r, lpX, c, lane);
@@ -1041,7 +1037,7 @@ __device__ void dfs(const SearchArgs &a, const RootCtx &r, Ck<Geo<W>::CH> P, Ck<
                 PROF_START(t_don);
                 if (recv >= 0) {
                     unsigned *dst = a.ws + (unsigned long long)recv * a.ws_words;
-                    write_branch<W>(a, r, dst, L, c, Pc, XPc, lpXc, Sc, lane);
+                    write_branch<W>(scratch, r, dst, L, c, Pc, XPc, lpXc, Sc, lane);
                     if (lane == 0) {
                         __threadfence();
                         dev_int(a.flag[recv]).store(kInboxFull, cuda::memory_order_release);
@@ -1916,7 +1912,7 @@ __device__ void search_edge(const SearchArgs &a, unsigned *ws, const WarpSmem &s
     const unsigned long long S = vertex_key(v) + vertex_key(w);
     if (np == 0) {
         // P empty: {v, w} is maximal iff X is empty too
-        if (nx == 0) report<W>(a, r, 0, 0, 2, S, acc, s_hist, lane);
+        if (nx == 0) report<W>(a, r, 0, 0, 2, S, acc, s_hist, lane, nullptr);   // level 0
         acc.nodes++;
         return;
     }
@@ -2065,7 +2061,7 @@ __global__ void __launch_bounds__(128, MinBlocks<W>::value) search_kernel(Search
                 single.rsize = 1;
                 if (lane == 0) single.rids[0] = v;
                 __syncwarp();
-                report<W>(a, single, 0, 0, 1, vertex_key(v), acc, s_hist, lane);
+                report<W>(a, single, 0, 0, 1, vertex_key(v), acc, s_hist, lane, nullptr);
             }
         } else if (np > kMaxP) {
             if (lane == 0) set_status(a.g.ctrl, MCE_ERR_LIMIT);
