@@ -54,8 +54,31 @@ static int check_unit(int deg, int np, bool ip, int np_u, int nx_u)
     return 0;
 }
 
+// Record of a root built ahead of its search (row width W = 1, 2 or 4 words): header, rows
+// (16-byte aligned), P's ids, P's keys (8-byte aligned), the X list, in order and inside a total
+// of whole 16-byte quads.  A root of the big-workspace group uses its rows' space as scratch for
+// the covering test's candidates, 256 words per chunk (32 lanes x 8 in flight), before the rows
+// are built: that space must hold them.
+static int check_record(int deg, int np, int W)
+{
+    const mce::RecLayout l = mce::rec_layout(deg, np, W);
+    if (l.rows != 4 || (l.rows & 3)) return fail("record rows after the header, aligned", deg, np, W, 0);
+    if (l.pids < l.rows + (long long)deg * W) return fail("record pids after rows", deg, np, W, 0);
+    if (l.pkey < l.pids + np || (l.pkey & 1)) return fail("record pkey placed, 8-byte aligned", deg, np, W, 0);
+    if (l.xx < l.pkey + 2LL * np) return fail("record X list after pkey", deg, np, W, 0);
+    if (l.total < l.xx + (deg - np) || (l.total & 3)) return fail("record total, whole quads", deg, np, W, 0);
+    if (mce::rec_quads(deg, np, W) * 4 != l.total) return fail("record quads", deg, np, W, 0);
+    const bool big = ws_layout(deg, np, false, false).total > mce::kWsCapWords;
+    if (big && (long long)deg * W < 256) return fail("hub's rows hold the covering scratch", deg, np, W, 0);
+    return 0;
+}
+
 int main()
 {
+    for (int W : {1, 2, 4})
+        for (int np = W == 1 ? 1 : 16 * W + 1; np <= 32 * W; ++np)
+            for (int e : {0, 1, 2, 3, 7, 100, 1000, 4095, 30000, 2000000})
+                if (check_record(np + e, np, W)) return 1;
     const int nps[] = {1, 2, 31, 32, 33, 63, 64, 65, 127, 128, 129, 255, 256, 257, 511, 512, 513,
                        1000, 1023, 1024};
     const int extra[] = {0, 1, 2, 7, 100, 1000, 30000, 2000000};

@@ -1,6 +1,7 @@
 """Host-side check of the per-warp workspace layout (`ws_layout` in the library's internal
 header): regions ordered, aligned and inside the total, and every second-level subtree of a
-root inside that root's regions.  Compiled with nvcc as host code and run on the CPU.
+root inside that root's regions; and of the records of subtrees built ahead (`rec_layout`).
+Compiled with nvcc as host code and run on the CPU.
 """
 import os
 import shutil
