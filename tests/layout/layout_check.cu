@@ -59,17 +59,23 @@ static int check_unit(int deg, int np, bool ip, int np_u, int nx_u)
 // of whole 16-byte quads.  A root of the big-workspace group uses its rows' space as scratch for
 // the covering test's candidates, 256 words per chunk (32 lanes x 8 in flight), before the rows
 // are built: that space must hold them.
+static int rfail(const char *what, int deg, int np, int W)
+{
+    std::printf("violation: %s (deg=%d np=%d W=%d)\n", what, deg, np, W);
+    return 1;
+}
+
 static int check_record(int deg, int np, int W)
 {
     const mce::RecLayout l = mce::rec_layout(deg, np, W);
-    if (l.rows != 4 || (l.rows & 3)) return fail("record rows after the header, aligned", deg, np, W, 0);
-    if (l.pids < l.rows + (long long)deg * W) return fail("record pids after rows", deg, np, W, 0);
-    if (l.pkey < l.pids + np || (l.pkey & 1)) return fail("record pkey placed, 8-byte aligned", deg, np, W, 0);
-    if (l.xx < l.pkey + 2LL * np) return fail("record X list after pkey", deg, np, W, 0);
-    if (l.total < l.xx + (deg - np) || (l.total & 3)) return fail("record total, whole quads", deg, np, W, 0);
-    if (mce::rec_quads(deg, np, W) * 4 != l.total) return fail("record quads", deg, np, W, 0);
+    if (l.rows != 4 || (l.rows & 3)) return rfail("record rows after the header, aligned", deg, np, W);
+    if (l.pids < l.rows + (long long)deg * W) return rfail("record pids after rows", deg, np, W);
+    if (l.pkey < l.pids + np || (l.pkey & 1)) return rfail("record pkey placed, 8-byte aligned", deg, np, W);
+    if (l.xx < l.pkey + 2LL * np) return rfail("record X list after pkey", deg, np, W);
+    if (l.total < l.xx + (deg - np) || (l.total & 3)) return rfail("record total, whole quads", deg, np, W);
+    if (mce::rec_quads(deg, np, W) * 4 != l.total) return rfail("record quads", deg, np, W);
     const bool big = ws_layout(deg, np, false, false).total > mce::kWsCapWords;
-    if (big && (long long)deg * W < 256) return fail("hub's rows hold the covering scratch", deg, np, W, 0);
+    if (big && (long long)deg * W < 256) return rfail("hub's rows hold the covering scratch", deg, np, W);
     return 0;
 }
 
