@@ -206,7 +206,9 @@ def workload_config(args, g, roots, pc, d):
         "roots_left_out": int((pc >= args.max_p).sum()),
         "root_fraction": args.root_fraction,
         "l2": "flushed between steps (256 MiB write, untimed)",
-        "induced": {0: "Delta/d rule", 1: "full", 2: "partial"}[getattr(args, "induced", 0)],
+        # the variant in use: the Delta / d > 200 rule resolved as the library resolves it
+        "induced": ({1: "full", 2: "partial"}[args.induced] if getattr(args, "induced", 0)
+                    else ("partial" if g.max_degree() > 200 * d else "full")),
         "subtree_level": getattr(args, "subtree_level", 1),
     }
 
