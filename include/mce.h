@@ -48,7 +48,7 @@ typedef enum mce_status {
     MCE_ERR_OUT_OF_MEMORY = 5,     /* a device or host allocation failed                       */
     MCE_ERR_BUFFER_TOO_SMALL = 6,  /* an output buffer cannot hold the result                  */
     MCE_ERR_DEVICE_TIMEOUT = 7,    /* a device-side wait exceeded mce_config.spin_limit_ns     */
-    MCE_ERR_LIMIT = 8,             /* the graph exceeds a documented size limit of this build  */
+    MCE_ERR_LIMIT = 8,             /* the graph exceeds a documented size limit of the library */
     MCE_ERR_CUDA = 9,              /* any other CUDA runtime error                             */
     MCE_ERR_INTERNAL = 10          /* a device-side consistency check failed (a library bug)   */
 } mce_status;

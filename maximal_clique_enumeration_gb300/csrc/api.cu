@@ -371,7 +371,7 @@ const char *mce_status_str(mce_status s)
     case MCE_ERR_OUT_OF_MEMORY: return "out of memory";
     case MCE_ERR_BUFFER_TOO_SMALL: return "output buffer too small";
     case MCE_ERR_DEVICE_TIMEOUT: return "device-side wait exceeded the spin limit";
-    case MCE_ERR_LIMIT: return "graph exceeds a size limit of this build";
+    case MCE_ERR_LIMIT: return "graph exceeds a size limit of the library";
     case MCE_ERR_CUDA: return "CUDA error";
     case MCE_ERR_INTERNAL: return "internal consistency check failed on the device";
     }
